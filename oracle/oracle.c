@@ -1,0 +1,479 @@
+/*
+ * oracle.c -- plain CPU oracle for the merge-path replacement merge.
+ *
+ * TEST INFRASTRUCTURE. This is the slow, sequential, obviously correct
+ * definition that the GPU library is checked against. Only the test suite,
+ * the smoke check and the benchmark's CPU-baseline leg load it; the product
+ * path never does. It shares no source, header, table or helper with the
+ * CUDA library, and it does not know how the GPU partitions work.
+ *
+ * Every function follows the definition it cites:
+ *   [MP]  "Day 36: CUDA merge path: merging sorted arrays in parallel"
+ *         (gpu-preview.ayushworks.com/days/36-merge-path)
+ *   [CH14] "Chapter 14: Merge Sort and Sample Sort", section 14.1
+ *         (maximumbeings.github.io/dsa_cuda_from_first_principles)
+ *   [CB]  "Everett: collision bitmap and rank experiment"
+ *         (ekmett.github.io/everett/collision-bitmap-and-rank-experiment.html)
+ *   [GC]  "Everett: GPU construction experiment"
+ *         (ekmett.github.io/everett/gpu-construction-experiment.html)
+ *
+ * Conventions (readings of the pages where they are silent):
+ *   - A is the older input, B the newer one. Equal keys put A first.
+ *   - A reference is src<<31 | index, src 0 = A, src 1 = B.
+ *   - Bitmaps (collision bits, tombstones) hold bit t in word t/32 at bit
+ *     position t%32 (least significant first).
+ *   - A dropped A record has ordinal 0xFFFFFFFF.
+ *   - FC payload bit t is bit (31 - t%32) of 32-bit word t/32.
+ *
+ * Parity of the exact Exp-Golomb bit pattern and of the payload word layout
+ * is pinned only by hand-derived fixtures (the pages give the lengths, not
+ * the bit strings); everything else is pinned by page examples, closed forms
+ * and brute force in the tests.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define REF_FROM_B 0x80000000u
+#define ORD_DROPPED 0xFFFFFFFFu
+
+/* ------------------------------------------------------------------------ */
+/* Stable merge. [CH14] "The Sequential (CPU) Baseline": walk two pointers,  */
+/* take A while A[i] <= B[j] so that ties go to A, then copy what is left.  */
+/* prov (optional) records which input each output came from: i for A[i],   */
+/* m + j for B[j] ([MP] "Exercise", the provenance check).                  */
+/* ------------------------------------------------------------------------ */
+#define ORACLE_DEFINE_MERGE(NAME, KEY)                                        \
+    void NAME(const KEY *A, const uint32_t *Apay, int64_t m, const KEY *B,    \
+              const uint32_t *Bpay, int64_t n, KEY *out, uint32_t *out_pay,   \
+              int64_t *prov) {                                                \
+        int64_t i = 0, j = 0, k = 0;                                          \
+        while (i < m && j < n) {                                              \
+            if (A[i] <= B[j]) {                                               \
+                out[k] = A[i];                                                \
+                if (out_pay) out_pay[k] = Apay[i];                            \
+                if (prov) prov[k] = i;                                        \
+                i++;                                                          \
+            } else {                                                          \
+                out[k] = B[j];                                                \
+                if (out_pay) out_pay[k] = Bpay[j];                            \
+                if (prov) prov[k] = m + j;                                    \
+                j++;                                                          \
+            }                                                                 \
+            k++;                                                              \
+        }                                                                     \
+        for (; i < m; i++, k++) {                                             \
+            out[k] = A[i];                                                    \
+            if (out_pay) out_pay[k] = Apay[i];                                \
+            if (prov) prov[k] = i;                                            \
+        }                                                                     \
+        for (; j < n; j++, k++) {                                             \
+            out[k] = B[j];                                                    \
+            if (out_pay) out_pay[k] = Bpay[j];                                \
+            if (prov) prov[k] = m + j;                                        \
+        }                                                                     \
+    }
+
+ORACLE_DEFINE_MERGE(oracle_merge_i32, int32_t)
+ORACLE_DEFINE_MERGE(oracle_merge_u64, uint64_t)
+
+/* ------------------------------------------------------------------------ */
+/* Co-rank by its definition. [MP] "The merge matrix, and the diagonal that  */
+/* cuts it" and [CH14] "The Concept, In Detail": the co-rank of k is the    */
+/* number of A elements among the first k outputs of the stable merge. The  */
+/* oracle walks the merge itself; it does no bisection.                     */
+/* Partition entries g = 0..G, G = ceil((m+n)/D), sit at k_g = min(gD, m+n) */
+/* and hold (i, j) with i + j = k_g: out_ij[2g] = i, out_ij[2g+1] = j.      */
+/* ------------------------------------------------------------------------ */
+#define ORACLE_DEFINE_PARTITION(NAME, KEY)                                    \
+    void NAME(const KEY *A, int64_t m, const KEY *B, int64_t n, int64_t D,    \
+              int64_t *out_ij) {                                              \
+        int64_t total = m + n;                                                \
+        int64_t G = (total + D - 1) / D;                                      \
+        int64_t i = 0, j = 0, g = 0;                                          \
+        for (g = 0; g <= G; g++) {                                            \
+            int64_t kg = g * D < total ? g * D : total;                       \
+            while (i + j < kg) {                                              \
+                if (j >= n || (i < m && A[i] <= B[j])) i++;                   \
+                else j++;                                                     \
+            }                                                                 \
+            out_ij[2 * g] = i;                                                \
+            out_ij[2 * g + 1] = j;                                            \
+        }                                                                     \
+    }
+
+ORACLE_DEFINE_PARTITION(oracle_partition_i32, int32_t)
+ORACLE_DEFINE_PARTITION(oracle_partition_u64, uint64_t)
+
+/* ------------------------------------------------------------------------ */
+/* Byte-string order: unsigned lexicographic bytes, a proper prefix sorts   */
+/* first ([GC], the prefix-cache paragraph: zero padding plus the length    */
+/* keeps proper-prefix order exact).                                        */
+/* ------------------------------------------------------------------------ */
+static int str_cmp(const uint8_t *a, uint64_t la, const uint8_t *b, uint64_t lb) {
+    uint64_t t, lmin = la < lb ? la : lb;
+    for (t = 0; t < lmin; t++) {
+        if (a[t] != b[t]) return a[t] < b[t] ? -1 : 1;
+    }
+    if (la == lb) return 0;
+    return la < lb ? -1 : 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Replacement merge by sequential dedup. [GC] third paragraph: the stable  */
+/* merge puts the older equal key first and only the newer record of each  */
+/* equal-key run is kept; a newer tombstone stays a record. [CB] "Corrected */
+/* record ordinals": C_i = 1 exactly when B holds A_i's key; lb_B[j] is the */
+/* lower bound of B_j in A. Outputs:                                        */
+/*   refs[0..count)       survivors in merged order                         */
+/*   C[ceil(m/32)]        collision bitmap (tail bits zero)                 */
+/*   lb_B[n]              lower bound of each B record in A                 */
+/*   ord_A[m], ord_B[n]   output position of each record (dropped: ~0)      */
+/* Any output pointer may be NULL. Returns count = m + n - popcount(C).     */
+/* ------------------------------------------------------------------------ */
+#define ORACLE_REPLACEMENT_BODY(A_LT_B, A_EQ_B, PREV_A_EQ_B)                  \
+    int64_t i = 0, j = 0, k = 0;                                              \
+    if (C) memset(C, 0, sizeof(uint32_t) * (size_t)((m + 31) / 32));          \
+    while (i < m || j < n) {                                                  \
+        int a_next = (j >= n) || (i < m && (A_LT_B || A_EQ_B));               \
+        if (a_next) {                                                         \
+            if (j < n && A_EQ_B) {                                            \
+                if (C) C[i / 32] |= 1u << (i % 32);                           \
+                if (ord_A) ord_A[i] = ORD_DROPPED;                            \
+                i++;                                                          \
+                continue;                                                     \
+            }                                                                 \
+            if (refs) refs[k] = (uint32_t)i;                                  \
+            if (ord_A) ord_A[i] = (uint32_t)k;                                \
+            i++;                                                              \
+        } else {                                                              \
+            int64_t hit = (i > 0 && PREV_A_EQ_B) ? 1 : 0;                     \
+            if (refs) refs[k] = REF_FROM_B | (uint32_t)j;                     \
+            if (lb_B) lb_B[j] = (uint32_t)(i - hit);                          \
+            if (ord_B) ord_B[j] = (uint32_t)k;                                \
+            j++;                                                              \
+        }                                                                     \
+        k++;                                                                  \
+    }                                                                         \
+    return k;
+
+int64_t oracle_replacement_u64(const uint64_t *A, int64_t m, const uint64_t *B,
+                               int64_t n, uint32_t *refs, uint32_t *C,
+                               uint32_t *lb_B, uint32_t *ord_A, uint32_t *ord_B) {
+    ORACLE_REPLACEMENT_BODY(A[i] < B[j], A[i] == B[j], A[i - 1] == B[j])
+}
+
+int64_t oracle_replacement_str(const uint8_t *Aar, const uint64_t *Aoff, int64_t m,
+                               const uint8_t *Bar, const uint64_t *Boff, int64_t n,
+                               uint32_t *refs, uint32_t *C, uint32_t *lb_B,
+                               uint32_t *ord_A, uint32_t *ord_B) {
+#define SA(x) (Aar + Aoff[(x)]), (Aoff[(x) + 1] - Aoff[(x)])
+#define SB(x) (Bar + Boff[(x)]), (Boff[(x) + 1] - Boff[(x)])
+    ORACLE_REPLACEMENT_BODY(str_cmp(SA(i), SB(j)) < 0, str_cmp(SA(i), SB(j)) == 0,
+                            str_cmp(SA(i - 1), SB(j)) == 0)
+#undef SA
+#undef SB
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exclusive collision rank. [CB] "Corrected record ordinals":              */
+/* R(i) = sum_{t<i} C_t for i = 0..m, endpoint included. Bit by bit.        */
+/* ------------------------------------------------------------------------ */
+void oracle_rank_prefix(const uint32_t *C, int64_t m, uint32_t *R) {
+    int64_t t;
+    R[0] = 0;
+    for (t = 0; t < m; t++) R[t + 1] = R[t] + ((C[t / 32] >> (t % 32)) & 1u);
+}
+
+/* ------------------------------------------------------------------------ */
+/* rank512 directory. [CB] "Temporary rank layouts": every 512-bit block    */
+/* has a 32-bit absolute prefix and seven 9-bit prefixes, one at each later */
+/* 64-bit word of the block. Layout (three u32 per block, floor(m/512)+1    */
+/* blocks so that R(m) is answerable at EOF):                               */
+/*   dir[3b]                 R(512 b)                                       */
+/*   dir[3b+1] | dir[3b+2]<<32   sum over s=1..7 of                         */
+/*                              (R(512b+64s) - R(512b)) << 9(s-1)           */
+/* Positions past m count as m (bits beyond A's length are zero).           */
+/* ------------------------------------------------------------------------ */
+void oracle_rank512_dir(const uint32_t *C, int64_t m, uint32_t *dir) {
+    uint32_t *R = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(m + 1));
+    int64_t b, nb = m / 512 + 1;
+    int s;
+    oracle_rank_prefix(C, m, R);
+    for (b = 0; b < nb; b++) {
+        int64_t base = 512 * b;
+        uint64_t packed = 0;
+        for (s = 1; s <= 7; s++) {
+            int64_t p = base + 64 * s;
+            if (p > m) p = m;
+            packed |= (uint64_t)(R[p] - R[base]) << (9 * (s - 1));
+        }
+        dir[3 * b] = R[base];
+        dir[3 * b + 1] = (uint32_t)(packed & 0xFFFFFFFFu);
+        dir[3 * b + 2] = (uint32_t)(packed >> 32);
+    }
+    free(R);
+}
+
+/* Rank queries R(pos[t]) for pos in [0, m], by the prefix definition. */
+void oracle_rank_query(const uint32_t *C, int64_t m, const uint32_t *pos, int64_t q,
+                       uint32_t *out) {
+    uint32_t *R = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(m + 1));
+    int64_t t;
+    oracle_rank_prefix(C, m, R);
+    for (t = 0; t < q; t++) out[t] = R[pos[t]];
+    free(R);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Corrected ordinals by the closed forms, [CB] "Corrected record ordinals" */
+/* and "The three experimental paths" (independent lower bounds, the        */
+/* simplest oracle for the formulas):                                       */
+/*   surviving A_i : i + lower_bound(B, A_i) - R(i)                         */
+/*   B_j, lb = lower_bound(A, B_j) : j + lb - R(lb)                         */
+/* C is recomputed here from the lower bounds, independently of the walk.  */
+/* ------------------------------------------------------------------------ */
+static int64_t lower_bound_u64(const uint64_t *X, int64_t len, uint64_t key) {
+    int64_t lo = 0, hi = len;
+    while (lo < hi) {
+        int64_t mid = lo + (hi - lo) / 2;
+        if (X[mid] < key) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+void oracle_ordinals_formula_u64(const uint64_t *A, int64_t m, const uint64_t *B,
+                                 int64_t n, uint32_t *C, uint32_t *lb_B,
+                                 uint32_t *ord_A, uint32_t *ord_B) {
+    uint32_t *R = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(m + 1));
+    int64_t i, j;
+    memset(C, 0, sizeof(uint32_t) * (size_t)((m + 31) / 32));
+    for (j = 0; j < n; j++) {
+        int64_t lb = lower_bound_u64(A, m, B[j]);
+        lb_B[j] = (uint32_t)lb;
+        if (lb < m && A[lb] == B[j]) C[lb / 32] |= 1u << (lb % 32);
+    }
+    oracle_rank_prefix(C, m, R);
+    for (i = 0; i < m; i++) {
+        if ((C[i / 32] >> (i % 32)) & 1u) ord_A[i] = ORD_DROPPED;
+        else ord_A[i] = (uint32_t)(i + lower_bound_u64(B, n, A[i]) - R[i]);
+    }
+    for (j = 0; j < n; j++) ord_B[j] = (uint32_t)(j + lb_B[j] - R[lb_B[j]]);
+    free(R);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Front-compressed record lengths and payload, [GC] the paragraphs on the  */
+/* control argument and the record length:                                  */
+/*   k_i  key length in bits, l_i exact bit LCP with the preceding surviving */
+/*        key (l_0 = 0, clamped to the shorter key)                         */
+/*   c_i  = 1 + l_i when i mod 15 = 0, else k_{i-1} - l_i                   */
+/*   record = EG0(c_i) EG0(k_i - l_i) key bits [l_i, k_i) value             */
+/*   value  = 0 for a tombstone, else 1 EG0(byte length) bytes              */
+/*   E(x)   = 2 floor(log2(x+1)) + 1                                        */
+/* EG0 is written as the textbook order-0 Exp-Golomb code: floor(log2(x+1)) */
+/* zero bits, then x+1 in binary. Bits are written MSB first with no        */
+/* padding between records; unused tail bits of the last word are zero.     */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const uint8_t *arena;
+    const uint64_t *off; /* count + 1 offsets */
+} oracle_bytes;
+
+static uint64_t key_len(const oracle_bytes *K, uint32_t idx) {
+    return K->off[idx + 1] - K->off[idx];
+}
+
+static int key_bit(const oracle_bytes *K, uint32_t idx, uint64_t p) {
+    uint8_t byte = K->arena[K->off[idx] + p / 8];
+    return (byte >> (7 - (p % 8))) & 1;
+}
+
+static int floor_log2_u64(uint64_t x) { /* x >= 1 */
+    int r = 0;
+    while (x > 1) {
+        x >>= 1;
+        r++;
+    }
+    return r;
+}
+
+static uint64_t eg0_len(uint64_t x) { return 2 * (uint64_t)floor_log2_u64(x + 1) + 1; }
+
+/* E(x), exported so that the tests can pin it to the textbook code length. */
+uint64_t oracle_eg0_len(uint64_t x) { return eg0_len(x); }
+
+
+static void put_bit(uint32_t *payload, uint64_t *pos, int bit) {
+    if (payload && bit) payload[*pos / 32] |= 1u << (31 - (*pos % 32));
+    (*pos)++;
+}
+
+static void put_eg0(uint32_t *payload, uint64_t *pos, uint64_t x) {
+    int z = floor_log2_u64(x + 1), b;
+    for (b = 0; b < z; b++) put_bit(payload, pos, 0);
+    for (b = z; b >= 0; b--) put_bit(payload, pos, (int)(((x + 1) >> b) & 1u));
+}
+
+/* Writes EG0(x) into a zeroed word buffer; returns the bits written. */
+uint64_t oracle_eg0_bits(uint64_t x, uint32_t *words) {
+    uint64_t pos = 0;
+    put_eg0(words, &pos, x);
+    return pos;
+}
+
+/* Returns the total number of payload bits, or -1 if a per-record field
+ * does not fit in 32 bits or the payload buffer is too small. payload may
+ * be NULL (lengths only); it is zeroed before writing when given. */
+int64_t oracle_fc_encode(const uint8_t *keyA_ar, const uint64_t *keyA_off,
+                         const uint8_t *valA_ar, const uint64_t *valA_off,
+                         const uint32_t *tombA, const uint8_t *keyB_ar,
+                         const uint64_t *keyB_off, const uint8_t *valB_ar,
+                         const uint64_t *valB_off, const uint32_t *tombB,
+                         const uint32_t *refs, int64_t N, uint32_t *lcp,
+                         uint32_t *ctrl, uint32_t *rec_bits, uint64_t *bit_off,
+                         uint32_t *payload, int64_t nwords) {
+    oracle_bytes KA = {keyA_ar, keyA_off}, KB = {keyB_ar, keyB_off};
+    oracle_bytes VA = {valA_ar, valA_off}, VB = {valB_ar, valB_off};
+    uint64_t pos = 0, k_prev = 0;
+    int64_t i;
+    if (payload) memset(payload, 0, sizeof(uint32_t) * (size_t)nwords);
+    for (i = 0; i < N; i++) {
+        uint32_t r = refs[i], idx = r & 0x7FFFFFFFu;
+        const oracle_bytes *K = (r & REF_FROM_B) ? &KB : &KA;
+        const oracle_bytes *V = (r & REF_FROM_B) ? &VB : &VA;
+        const uint32_t *T = (r & REF_FROM_B) ? tombB : tombA;
+        uint64_t k = 8 * key_len(K, idx), l = 0, c, v, L, p, start = pos;
+        int tomb = T ? (int)((T[idx / 32] >> (idx % 32)) & 1u) : 0;
+        if (i > 0) {
+            uint32_t pr = refs[i - 1], pidx = pr & 0x7FFFFFFFu;
+            const oracle_bytes *PK = (pr & REF_FROM_B) ? &KB : &KA;
+            uint64_t kmin = 8 * key_len(PK, pidx);
+            if (k < kmin) kmin = k;
+            while (l < kmin && key_bit(PK, pidx, l) == key_bit(K, idx, l)) l++;
+        }
+        c = (i % 15 == 0) ? 1 + l : k_prev - l;
+        if (tomb) v = 1;
+        else {
+            uint64_t vb = key_len(V, idx);
+            v = 1 + eg0_len(vb) + 8 * vb;
+        }
+        L = eg0_len(c) + eg0_len(k - l) + (k - l) + v;
+        if (l > 0xFFFFFFFFu || c > 0xFFFFFFFFu || L > 0xFFFFFFFFu) return -1;
+        if (lcp) lcp[i] = (uint32_t)l;
+        if (ctrl) ctrl[i] = (uint32_t)c;
+        if (rec_bits) rec_bits[i] = (uint32_t)L;
+        if (bit_off) bit_off[i] = start;
+        if (payload && (uint64_t)nwords * 32 < start + L) return -1;
+        put_eg0(payload, &pos, c);
+        put_eg0(payload, &pos, k - l);
+        for (p = l; p < k; p++) put_bit(payload, &pos, key_bit(K, idx, p));
+        if (tomb) put_bit(payload, &pos, 0);
+        else {
+            uint64_t vb = key_len(V, idx);
+            put_bit(payload, &pos, 1);
+            put_eg0(payload, &pos, vb);
+            for (p = 0; p < 8 * vb; p++) put_bit(payload, &pos, key_bit(V, idx, p));
+        }
+        if (pos != start + L) return -1; /* the length formula and the writer agree */
+        k_prev = k;
+    }
+    if (bit_off) bit_off[N] = pos;
+    return (int64_t)pos;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Independent FC decoder: parses a payload back into keys, values and      */
+/* tombstones, following the same record grammar in the reading direction. */
+/* Keys are rebuilt from the previous key's first l bits plus the literal   */
+/* suffix, where l = c - 1 at a 15-record restart and k_{i-1} - c elsewhere. */
+/* Outputs are caller-sized: key_ar/val_ar capacities in bytes, offsets     */
+/* N + 1 entries, tomb ceil(N/32) words. Returns bits consumed or a         */
+/* negative code on a malformed payload.                                    */
+/* ------------------------------------------------------------------------ */
+static int get_bit(const uint32_t *payload, uint64_t total, uint64_t *pos, int *bit) {
+    if (*pos >= total) return -1;
+    *bit = (int)((payload[*pos / 32] >> (31 - (*pos % 32))) & 1u);
+    (*pos)++;
+    return 0;
+}
+
+static int get_eg0(const uint32_t *payload, uint64_t total, uint64_t *pos, uint64_t *x) {
+    int z = 0, bit = 0, b;
+    uint64_t v = 1;
+    for (;;) {
+        if (get_bit(payload, total, pos, &bit)) return -1;
+        if (bit) break;
+        if (++z > 62) return -1;
+    }
+    for (b = 0; b < z; b++) {
+        if (get_bit(payload, total, pos, &bit)) return -1;
+        v = (v << 1) | (uint64_t)bit;
+    }
+    *x = v - 1;
+    return 0;
+}
+
+int64_t oracle_fc_decode(const uint32_t *payload, uint64_t total_bits, int64_t N,
+                         uint8_t *key_ar, uint64_t key_cap, uint64_t *key_off,
+                         uint8_t *val_ar, uint64_t val_cap, uint64_t *val_off,
+                         uint32_t *tomb) {
+    uint64_t pos = 0, kpos = 0, vpos = 0, prev_start = 0, k_prev = 0, t;
+    int64_t i;
+    int bit;
+    memset(tomb, 0, sizeof(uint32_t) * (size_t)((N + 31) / 32));
+    key_off[0] = 0;
+    val_off[0] = 0;
+    for (i = 0; i < N; i++) {
+        uint64_t c, d, l, k;
+        if (get_eg0(payload, total_bits, &pos, &c)) return -2;
+        if (get_eg0(payload, total_bits, &pos, &d)) return -2;
+        if (i % 15 == 0) {
+            if (c < 1) return -3;
+            l = c - 1;
+        } else {
+            if (c > k_prev) return -3;
+            l = k_prev - c;
+        }
+        if (l > k_prev) return -3;
+        k = l + d;
+        if (k % 8 != 0) return -4;
+        if (kpos + k / 8 > key_cap) return -5;
+        /* inherited prefix bits from the previous key, then the literal */
+        memset(key_ar + kpos, 0, (size_t)(k / 8));
+        for (t = 0; t < k; t++) {
+            int b;
+            if (t < l) {
+                b = (key_ar[prev_start + t / 8] >> (7 - t % 8)) & 1;
+            } else {
+                if (get_bit(payload, total_bits, &pos, &b)) return -2;
+            }
+            if (b) key_ar[kpos + t / 8] |= (uint8_t)(1u << (7 - t % 8));
+        }
+        prev_start = kpos;
+        kpos += k / 8;
+        key_off[i + 1] = kpos;
+        k_prev = k;
+        if (get_bit(payload, total_bits, &pos, &bit)) return -2;
+        if (!bit) {
+            tomb[i / 32] |= 1u << (i % 32);
+        } else {
+            uint64_t vb;
+            if (get_eg0(payload, total_bits, &pos, &vb)) return -2;
+            if (vpos + vb > val_cap) return -5;
+            for (t = 0; t < vb; t++) {
+                int b, q;
+                uint8_t byte = 0;
+                for (q = 0; q < 8; q++) {
+                    if (get_bit(payload, total_bits, &pos, &b)) return -2;
+                    byte = (uint8_t)((byte << 1) | b);
+                }
+                val_ar[vpos + t] = byte;
+            }
+            vpos += vb;
+        }
+        val_off[i + 1] = vpos;
+    }
+    return (int64_t)pos;
+}

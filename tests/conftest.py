@@ -1,0 +1,33 @@
+"""Shared pytest configuration: the `gpu` marker and golden-fixture reader."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def read_golden(name):
+    """Parse a `name: v0 v1 ...` fixture file into {name: [ints]}."""
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, vals = line.partition(":")
+            out[key.strip()] = [int(v, 0) for v in vals.split()]
+    return out
+
+
+@pytest.fixture(scope="session")
+def golden():
+    return read_golden

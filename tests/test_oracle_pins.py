@@ -1,0 +1,349 @@
+"""Pins for the CPU oracle: page examples, brute force, closed forms, invariants.
+
+Nothing here touches a GPU or the CUDA library. Each test ties the oracle to
+something other than itself: a value printed on a page (tests/golden), a
+textbook routine (a stable sort, a cumulative sum, a Python dict applied in
+chronological order, Python big-int arithmetic), or an invariant the pages
+state.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+# ---------------------------------------------------------------------------
+# Stable merge and co-rank
+# ---------------------------------------------------------------------------
+def test_worked_example_merge_and_crossings(golden):
+    g = golden("merge_path_worked_example.txt")
+    for dt in (np.int32, np.uint64):
+        a, b = np.array(g["a"], dt), np.array(g["b"], dt)
+        keys, _, prov = oracle.merge(a, b, provenance=True)
+        assert keys.tolist() == g["merged"]
+        assert [int(p < len(a)) for p in prov] == g["path_takes_a"]
+        assert oracle.corank(a, b, g["corank_k"][0]) == g["corank_i"][0]
+        for k, i in zip(g["crossing_k"], g["crossing_i"]):
+            assert oracle.corank(a, b, k) == i
+        part = oracle.partition(a, b, 2)
+        assert part[:, 0].tolist() == g["crossing_i"]
+        assert (part.sum(axis=1)).tolist() == g["crossing_k"]
+
+
+def test_chapter14_coranks(golden):
+    g = golden("corank_chapter14.txt")
+    A, B = np.array(g["A"], np.int32), np.array(g["B"], np.int32)
+    for k, i, j in zip(g["k"], g["i"], g["j"]):
+        assert (oracle.corank(A, B, k), k - oracle.corank(A, B, k)) == (i, j)
+    assert oracle.merge(A, B)[0].tolist() == g["merged"]
+
+
+def test_corank_trap(golden):
+    g = golden("corank_trap.txt")
+    assert oracle.corank(np.array(g["a"], np.int32), np.array(g["b"], np.int32),
+                         g["k"][0]) == g["i"][0]
+
+
+def test_tie_provenance(golden):
+    g = golden("tie_provenance.txt")
+    a, b = np.array(g["a"], np.int32), np.array(g["b"], np.int32)
+    keys, _, prov = oracle.merge(a, b, provenance=True)
+    assert keys.tolist() == g["values"]
+    assert prov.tolist() == g["provenance"]
+    assert oracle.corank(a, b, g["k"][0]) == g["i"][0]
+    # the page's point: the wrong split has the same values, other provenance
+    src = np.concatenate([a, b])
+    assert src[g["wrong_provenance"]].tolist() == g["values"]
+    assert g["wrong_provenance"] != prov.tolist()
+
+
+def _brute_coranks(A, B):
+    """Co-rank at every k from Python's stable sort of tagged elements."""
+    tagged = sorted([(int(x), 0) for x in A] + [(int(x), 1) for x in B],
+                    key=lambda t: (t[0], t[1]))
+    out = [0]
+    for _, src in tagged:
+        out.append(out[-1] + (src == 0))
+    return out
+
+
+def _sorted_sequences(alphabet, max_len):
+    for length in range(max_len + 1):
+        yield from itertools.combinations_with_replacement(alphabet, length)
+
+
+@pytest.mark.parametrize("dt", [np.int32, np.uint64])
+def test_corank_brute_force_all_small(dt):
+    seqs = list(_sorted_sequences(range(4), 4))
+    for sa in seqs:
+        A = np.array(sa, dt)
+        for sb in seqs:
+            B = np.array(sb, dt)
+            part = oracle.partition(A, B, 1)
+            assert part[:, 0].tolist() == _brute_coranks(A, B), (sa, sb)
+            assert (part.sum(axis=1) == np.arange(len(A) + len(B) + 1)).all()
+
+
+@pytest.mark.parametrize("m,n", [(0, 0), (0, 9), (9, 0), (1, 1), (7, 100), (5000, 3001),
+                                 (4096, 4096)])
+def test_merge_matches_stable_sort(m, n):
+    rng = np.random.default_rng(m * 7919 + n)
+    for dt, hi in ((np.int32, 64), (np.int32, 1 << 30), (np.uint64, 1 << 62)):
+        A = np.sort(rng.integers(-hi if dt == np.int32 else 0, hi, size=m).astype(dt))
+        B = np.sort(rng.integers(-hi if dt == np.int32 else 0, hi, size=n).astype(dt))
+        Apay = rng.integers(0, 2**32, size=m, dtype=np.uint32)
+        Bpay = rng.integers(0, 2**32, size=n, dtype=np.uint32)
+        keys, pay, prov = oracle.merge(A, B, Apay, Bpay, provenance=True)
+        cat = np.concatenate([A, B])
+        order = np.argsort(cat, kind="stable")
+        assert (keys == cat[order]).all()
+        assert (pay == np.concatenate([Apay, Bpay])[order]).all()
+        assert (prov == order).all()
+        # partition entries agree with the stable-sort order at every tile cut
+        D = 37
+        part = oracle.partition(A, B, D)
+        for g, (i, j) in enumerate(part):
+            k = min(g * D, m + n)
+            assert i + j == k and int((order[:k] < m).sum()) == i
+
+
+# ---------------------------------------------------------------------------
+# Replacement merge
+# ---------------------------------------------------------------------------
+def _chronological(A_keys, B_keys):
+    """Apply A then B to a dict: the newer record replaces the older one."""
+    d = {}
+    for i, k in enumerate(A_keys):
+        d[k] = (0, i)
+    for j, k in enumerate(B_keys):
+        d[k] = (1, j)
+    return [(src << 31) | idx for _, (src, idx) in sorted(d.items())]
+
+
+REPLACE_CASES = [  # (m, n, shared, universe)
+    (0, 0, 0, 16), (0, 5, 0, 16), (5, 0, 0, 16), (1, 1, 1, 4), (1, 1, 0, 4),
+    (64, 64, 64, 64 * 2), (64, 64, 0, 400), (33, 17, 9, 80), (1000, 300, 150, None),
+    (513, 2049, 513, 4000), (2048, 2048, 1024, 5000),
+]
+
+
+@pytest.mark.parametrize("m,n,shared,universe", REPLACE_CASES)
+def test_replacement_vs_chronological_map(m, n, shared, universe):
+    inp = synth.replace_random_small(seed=m * 31 + n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    A, B = inp.A, inp.B
+    r = oracle.replacement_u64(A, B)
+    assert r.refs.tolist() == _chronological(A.tolist(), B.tolist())
+    in_b = set(B.tolist())
+    C_expected = synth._bitmap(np.array([i for i, k in enumerate(A.tolist()) if k in in_b],
+                                        dtype=np.int64), m)
+    assert (r.C == C_expected).all()
+
+
+@pytest.mark.parametrize("m,n,shared,universe", REPLACE_CASES)
+def test_replacement_invariants_and_formula_ordinals(m, n, shared, universe):
+    inp = synth.replace_random_small(seed=m + 3 * n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    A, B = inp.A, inp.B
+    r = oracle.replacement_u64(A, B)
+    popc = int(sum(bin(int(w)).count("1") for w in r.C))
+    assert r.count == m + n - popc == m + n - shared
+    keys = np.array([B[x & 0x7FFFFFFF] if x >> 31 else A[x] for x in r.refs], np.uint64)
+    assert (keys[1:] > keys[:-1]).all()
+    assert sorted(int(x & 0x7FFFFFFF) for x in r.refs if x >> 31) == list(range(n))
+    # the walk's ordinals and the closed forms (independent lower bounds) agree
+    C2, lb2, ordA2, ordB2 = oracle.ordinals_formula_u64(A, B)
+    assert (C2 == r.C).all() and (lb2 == r.lb_B).all()
+    assert (ordA2 == r.ord_A).all() and (ordB2 == r.ord_B).all()
+    # unique and gap-free over count slots
+    live = np.concatenate([r.ord_A[r.ord_A != oracle.ORD_DROPPED], r.ord_B]).astype(np.int64)
+    assert sorted(live.tolist()) == list(range(r.count))
+    # lower bounds against numpy's searchsorted
+    assert (r.lb_B == np.searchsorted(A, B, side="left")).all()
+
+
+def test_replacement_skewed_generator_small():
+    inp = synth.replace_skewed(seed=4, m=40000, windows=4, window=256,
+                               per_window_shared=128, per_window_fresh=128)
+    r = oracle.replacement_u64(inp.A, inp.B)
+    assert r.count == len(inp.A) + len(inp.B) - inp.n_shared
+    assert r.refs.tolist() == _chronological(inp.A.tolist(), inp.B.tolist())
+
+
+def _str_cases():
+    yield [b"", b"a", b"ab", b"abc"], [b"ab", b"b"]
+    yield [b"\x00", b"\x00\x00", b"\xff"], [b"", b"\x00", b"\x00\x01", b"\xff\xff"]
+    yield [], [b"x"]
+    yield [b"x"], []
+    yield [], []
+    rng = np.random.default_rng(11)
+    pool = sorted({bytes(rng.integers(0, 3, size=rng.integers(0, 5)).astype(np.uint8))
+                   for _ in range(300)})
+    pick = rng.permutation(len(pool))
+    A = sorted(pool[t] for t in pick[: len(pool) // 2])
+    B = sorted(set(pool[t] for t in pick[len(pool) // 3:]))
+    yield A, B
+
+
+@pytest.mark.parametrize("case", list(_str_cases()))
+def test_replacement_str_vs_chronological_map(case):
+    ka, kb = case
+    s = synth.strings_from_lists(ka, kb)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    assert r.refs.tolist() == _chronological(ka, kb)
+    assert r.count == len(r.refs)
+
+
+# ---------------------------------------------------------------------------
+# Rank and the rank512 directory
+# ---------------------------------------------------------------------------
+def _maps():
+    rng = np.random.default_rng(5)
+    for m in (0, 1, 31, 32, 33, 63, 64, 65, 511, 512, 513, 2047, 2048, 2049, 5000):
+        for kind in ("zero", "one", "sparse", "random"):
+            if kind == "zero":
+                bits = np.zeros(m, bool)
+            elif kind == "one":
+                bits = np.ones(m, bool)
+            elif kind == "sparse":
+                bits = np.zeros(m, bool)
+                for p in (0, 31, 32, 33, 63, 64, 65, 511, 512, 513, 2047, 2048, m - 1):
+                    if 0 <= p < m:
+                        bits[p] = True
+            else:
+                bits = rng.random(m) < 0.3
+            yield m, kind, bits
+
+
+def _pack(bits):
+    return synth._bitmap(np.flatnonzero(bits).astype(np.int64), len(bits))
+
+
+@pytest.mark.parametrize("m,kind,bits", list(_maps()))
+def test_rank_prefix_and_directory(m, kind, bits):
+    C = _pack(bits)
+    R = oracle.rank_prefix(C, m)
+    expect = np.concatenate([[0], np.cumsum(bits)]).astype(np.uint32)
+    assert (R == expect).all()
+    # The directory answers R(p) at every p in [0, m] by the page's query:
+    # block prefix + packed 9-bit sub-prefix + at most one preceding 32-bit
+    # word + the masked current word.
+    d = oracle.rank512_dir(C, m)
+    assert len(d) == 3 * (m // 512 + 1)
+    for p in range(m + 1):
+        b, s = p // 512, (p % 512) // 64
+        r = int(d[3 * b])
+        if s:
+            packed = int(d[3 * b + 1]) | (int(d[3 * b + 2]) << 32)
+            r += (packed >> (9 * (s - 1))) & 0x1FF
+        w = p // 32
+        if p % 64 >= 32:
+            r += bin(int(C[w - 1])).count("1")
+        if p % 32:
+            r += bin(int(C[w]) & ((1 << (p % 32)) - 1)).count("1")
+        assert r == expect[p], (m, kind, p)
+    q = np.arange(m + 1, dtype=np.uint32)
+    assert (oracle.rank_query(C, m, q) == expect).all()
+
+
+# ---------------------------------------------------------------------------
+# Front compression
+# ---------------------------------------------------------------------------
+def test_eg0_closed_form_and_textbook_code():
+    xs = list(range(1 << 16)) + [(1 << s) + d for s in range(16, 21) for d in (-2, -1, 0, 1)]
+    xs += np.random.default_rng(3).integers(0, 1 << 20, size=2000).tolist()
+    for x in xs:
+        z = (x + 1).bit_length() - 1            # floor(log2(x+1))
+        textbook = "0" * z + bin(x + 1)[2:]     # order-0 Exp-Golomb code word
+        assert oracle.eg0_len(x) == 2 * z + 1 == len(textbook)
+    for x in xs[:4096:7] + xs[-50:]:
+        z = (x + 1).bit_length() - 1
+        assert oracle.eg0_bits(x) == "0" * z + bin(x + 1)[2:]
+
+
+def _encode_strings(s, refs):
+    return oracle.fc_encode((s.A.key_arena, s.A.key_off), (s.A.val_arena, s.A.val_off), s.A.tomb,
+                            (s.B.key_arena, s.B.key_off), (s.B.val_arena, s.B.val_off), s.B.tomb,
+                            refs)
+
+
+def test_fc_hand_derived(golden):
+    g = golden("fc_hand_derived.txt")
+    for name, val in (("one_tomb", None), ("one_empty", b"")):
+        s = synth.strings_from_lists([bytes(g[name + "_key"])], [], [val], [])
+        fc = _encode_strings(s, np.array([0], np.uint32))
+        assert fc.total_bits == g[name + "_bits"][0]
+        assert fc.payload.tolist() == g[name + "_words"]
+    s = synth.strings_from_lists([b"ab", b"ac"], [], [None, b"\xff"], [])
+    fc = _encode_strings(s, np.array([0, 1], np.uint32))
+    assert fc.total_bits == g["two_bits"][0]
+    assert fc.lcp.tolist() == g["two_lcp"]
+    assert fc.ctrl.tolist() == g["two_ctrl"]
+    assert fc.rec_bits.tolist() == g["two_rec_bits"]
+    assert fc.payload.tolist() == g["two_words"]
+
+
+def _bit_lcp(x: bytes, y: bytes) -> int:
+    """Leading equal bits of two byte strings, clamped to the shorter one."""
+    n = min(len(x), len(y))
+    if n == 0:
+        return 0
+    a = int.from_bytes(x[:n], "big")
+    b = int.from_bytes(y[:n], "big")
+    return 8 * n - (a ^ b).bit_length()
+
+
+def _check_fc_roundtrip(s):
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    fc = _encode_strings(s, r.refs)
+    N = r.count
+    keys = [s.B.key(x & 0x7FFFFFFF) if x >> 31 else s.A.key(x) for x in r.refs]
+    vals = [s.B.value(x & 0x7FFFFFFF) if x >> 31 else s.A.value(x) for x in r.refs]
+    assert int(fc.bit_off[N]) == fc.total_bits == int(fc.rec_bits.astype(np.int64).sum())
+    assert (np.diff(fc.bit_off.astype(np.int64)) == fc.rec_bits).all()
+    for i in range(N):
+        assert fc.lcp[i] == (0 if i == 0 else _bit_lcp(keys[i - 1], keys[i]))
+        if i > 0:
+            assert 8 * len(keys[i]) - fc.lcp[i] >= 1       # strictly increasing keys
+    if N:
+        assert fc.ctrl[0] == 1
+    key_cap = sum(len(k) for k in keys)
+    val_cap = sum(len(v) for v in vals if v is not None)
+    (ka, ko), (va, vo), tomb = oracle.fc_decode(fc.payload, fc.total_bits, N, key_cap, val_cap)
+    for i in range(N):
+        assert bytes(ka[int(ko[i]):int(ko[i + 1])]) == keys[i]
+        is_tomb = (int(tomb[i // 32]) >> (i % 32)) & 1
+        assert bool(is_tomb) == (vals[i] is None)
+        if vals[i] is not None:
+            assert bytes(va[int(vo[i]):int(vo[i + 1])]) == vals[i]
+    return fc
+
+
+def test_fc_roundtrip_edge_keys():
+    ka = [b"", b"\x00", b"\x00\x00", b"\x00\x01", b"\x7f", b"\x80", b"ab", b"abc", b"abd",
+          b"b" * 40, b"b" * 41, b"\xff" * 3]
+    kb = [b"\x00", b"\x00\x00\x00", b"abc", b"b" * 40 + b"\x01", b"\xff\xff"]
+    va = [None, b"", b"\x01", None, b"xyz", b"", b"\x00" * 16, None, b"q", b"", None, b"z"]
+    vb = [None, b"new", None, b"", b"\xff" * 16]
+    _check_fc_roundtrip(synth.strings_from_lists(ka, kb, va, vb))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_fc_roundtrip_prefix_tree(seed):
+    s = synth.strings(seed=seed, count=700, fanout=4, depth=2, max_suffix=12)
+    fc = _check_fc_roundtrip(s)
+    # restarts every 15 records: c_i = 1 + l_i there
+    assert fc.ctrl[15] == 1 + fc.lcp[15] and fc.ctrl[30] == 1 + fc.lcp[30]
+
+
+def test_synth_is_deterministic():
+    a = synth.replace_u64(seed=9, m=1000, n=300)
+    b = synth.replace_u64(seed=9, m=1000, n=300)
+    assert (a.A == b.A).all() and (a.B == b.B).all() and (a.tombB == b.tombB).all()
+    assert len(np.unique(a.A)) == 1000 and len(np.intersect1d(a.A, a.B)) == a.n_shared
+    s1 = synth.strings(seed=9, count=300, fanout=4, depth=2, max_suffix=6)
+    s2 = synth.strings(seed=9, count=300, fanout=4, depth=2, max_suffix=6)
+    assert (s1.A.key_arena == s2.A.key_arena).all() and (s1.B.key_off == s2.B.key_off).all()
