@@ -1,0 +1,259 @@
+/*
+ * lsmmerge.h -- C ABI of the GB300 merge-path replacement merge library.
+ *
+ * One shared library (liblsmmerge.so), hand-written CUDA kernels for sm_103a.
+ * The operations follow these pages:
+ *   [MP]   "Day 36: CUDA merge path: merging sorted arrays in parallel"
+ *   [CH14] "Chapter 14: Merge Sort and Sample Sort", section 14.1
+ *   [CB]   "Everett: collision bitmap and rank experiment"
+ *   [GC]   "Everett: GPU construction experiment"
+ *   [BP]   "Everett: byte-profile GPU merge"
+ *
+ * Conventions for every call
+ *   - A is the older sorted input, B the newer one. Equal keys put A first
+ *     ([GC], merge paragraph; [MP] "Exercise").
+ *   - Pointers named d_* or described as device memory are CUDA device
+ *     pointers owned by the caller; the library never allocates, frees or
+ *     keeps them. Scratch comes from a caller workspace sized by
+ *     lsm_workspace_size() ([CB] "Scratch space and likely costs": report the
+ *     actual temporary capacities).
+ *   - Sizes are int64_t element counts. Arrays of 8-byte keys, 4-byte
+ *     payloads and workspaces must start on a 16-byte boundary (the kernels
+ *     stage tiles with bulk asynchronous copies). Byte arenas must start on an
+ *     8-byte boundary and stay readable up to the next multiple of 8 bytes
+ *     past their last byte (keys are read in aligned 8-byte words; bytes past
+ *     a key's end are masked off).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call is asynchronous on that stream and returns after launching.
+ *   - Every call returns an lsm_status. Arguments are checked on the host
+ *     before any launch; a call that returns an error launched nothing,
+ *     except LSM_ERR_CUDA, which reports a failed launch.
+ *   - Inputs are trusted to be sorted (and unique where stated), as the
+ *     pages' parser trusts its accepted inputs ([BP] "Pipeline").
+ *   - Bounded device waits: a kernel that waits (for a bulk copy or for a
+ *     predecessor tile) gives up after about one second, records
+ *     LSM_ERR_TIMEOUT in a sticky device status word and returns;
+ *     lsm_get_device_status() reads it.
+ *   - Bitmaps hold bit t in 32-bit word t/32 at bit position t%32.
+ *   - A reference is src<<31 | index with src 0 = A and src 1 = B.
+ */
+#ifndef LSMMERGE_H
+#define LSMMERGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define LSM_API __attribute__((visibility("default")))
+#else
+#define LSM_API
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+enum {
+  LSM_OK = 0,
+  LSM_ERR_ARG = 1,       /* null pointer where data is needed, negative size */
+  LSM_ERR_DTYPE = 2,     /* key type not supported by this call */
+  LSM_ERR_OVERFLOW = 3,  /* sizes beyond the call's index range ([GC]: a 64-bit
+                            bound check precedes every 32-bit scan) */
+  LSM_ERR_CUDA = 4,      /* a CUDA launch or runtime call failed */
+  LSM_ERR_TIMEOUT = 5,   /* a bounded device wait ran out (device status) */
+  LSM_ERR_WORKSPACE = 6, /* workspace missing or smaller than required */
+  LSM_ERR_ALIGN = 7      /* a pointer misses its required alignment */
+};
+
+/* Key types. */
+enum { LSM_KEY_I32 = 1, LSM_KEY_U64 = 2 };
+
+/* Operations, for lsm_workspace_size(). */
+enum {
+  LSM_OP_MERGE_STABLE = 1,
+  LSM_OP_COLLISION_MARK = 2,
+  LSM_OP_COLLISION_MARK_STR = 3,
+  LSM_OP_RANK_BUILD = 4,
+  LSM_OP_REPLACEMENT_COMPACT = 5,
+  LSM_OP_FC_LENGTHS_SCAN = 6
+};
+
+#define LSM_REF_FROM_B 0x80000000u
+#define LSM_ORD_DROPPED 0xFFFFFFFFu
+
+/* A byte-string column in CSR form: record t occupies
+ * arena[off[t], off[t+1]). `off` holds count + 1 uint64 offsets. */
+typedef struct {
+  const uint8_t *arena;  /* device */
+  const uint64_t *off;   /* device, count + 1 entries */
+} lsm_bytes;
+
+/* Inputs of the front-compression passes. Keys and values of both sources;
+ * tombstone bitmaps may be NULL (no tombstones in that source). A value's
+ * bytes are ignored when its record is a tombstone. */
+typedef struct {
+  lsm_bytes keyA, valA;
+  const uint32_t *tombA; /* device bitmap, ceil(m/32) words, or NULL */
+  int64_t m;
+  lsm_bytes keyB, valB;
+  const uint32_t *tombB; /* device bitmap, ceil(n/32) words, or NULL */
+  int64_t n;
+} lsm_fc_input;
+
+/* ---- utilities ---------------------------------------------------------- */
+
+/* Human-readable name of a status code (static string). */
+LSM_API const char *lsm_status_string(int status);
+
+/* Version of this ABI (major * 100 + minor). */
+LSM_API int lsm_abi_version(void);
+
+/* Reads the sticky device status word of the current device into
+ * *host_status after synchronizing `stream`; resets it to LSM_OK when
+ * `reset` is nonzero. Blocks the calling host thread. */
+LSM_API int lsm_get_device_status(int32_t *host_status, int reset, void *stream);
+
+/* Bytes of workspace that `op` needs for the given sizes (and key type for
+ * LSM_OP_MERGE_STABLE). Host-only, never fails for valid sizes. The
+ * workspace is scratch: its contents on entry are ignored and on exit are
+ * unspecified. */
+LSM_API int lsm_workspace_size(int op, int key_type, int64_t m, int64_t n, size_t *bytes);
+
+/* ---- a1: merge path partition ------------------------------------------- */
+/* [MP] "The merge matrix, and the diagonal that cuts it"; [CH14] "The
+ * Concept, In Detail". For g = 0..G with G = ceil((m+n)/items_per_tile) and
+ * k_g = min(g * items_per_tile, m + n), writes the co-rank of k_g:
+ *   out_ij[2g]   = i, the number of A elements among the first k_g outputs
+ *                  of the stable merge with A first on ties;
+ *   out_ij[2g+1] = j = k_g - i.
+ * A, B: device, sorted ascending, key_type elements (int32 compares signed).
+ * out_ij: device, 2 * (G + 1) int64. items_per_tile >= 1. */
+LSM_API int lsm_merge_path_partition(int key_type, const void *A, int64_t m, const void *B,
+                                     int64_t n, int64_t items_per_tile, int64_t *out_ij,
+                                     void *stream);
+
+/* ---- a2: stable merge ---------------------------------------------------- */
+/* [CH14] "The Sequential (CPU) Baseline" defines the result; [MP] the
+ * partitioned form. Writes the m + n keys of A and B in ascending order,
+ * A's element first when keys are equal, and, when Apay/Bpay/out_pay are all
+ * non-NULL, each element's 32-bit payload beside it (payloads never take
+ * part in comparisons). Apay/Bpay/out_pay must be all NULL or all non-NULL.
+ * key_type: LSM_KEY_I32 or LSM_KEY_U64. out_keys must not alias the inputs.
+ * ws: at least lsm_workspace_size(LSM_OP_MERGE_STABLE, key_type, m, n). */
+LSM_API int lsm_merge_stable(int key_type, const void *A, const uint32_t *Apay, int64_t m,
+                             const void *B, const uint32_t *Bpay, int64_t n, void *out_keys,
+                             uint32_t *out_pay, void *ws, size_t ws_bytes, void *stream);
+
+/* ---- a3: collision bitmap ------------------------------------------------- */
+/* [CB] "Corrected record ordinals": for every B_j, lb_B[j] = lower_bound(A,
+ * B_j), the number of A keys strictly less than B_j, and bit C_i is set
+ * exactly when A_i == B_j for some j. The call clears C itself; bits at
+ * positions >= m stay zero. A and B strictly increasing (unique keys).
+ * A: device uint64[m]; B: device uint64[n]; C: device uint32[ceil(m/32)];
+ * lb_B: device uint32[n]. m, n < 2^31. */
+LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                               uint32_t *C, uint32_t *lb_B, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/* Same for byte-string keys in unsigned lexicographic order, a proper prefix
+ * first ([GC], prefix-cache paragraph). A and B are CSR columns of m and n
+ * strictly increasing keys. */
+LSM_API int lsm_collision_mark_str(const lsm_bytes *A, int64_t m, const lsm_bytes *B, int64_t n,
+                                   uint32_t *C, uint32_t *lb_B, void *ws, size_t ws_bytes,
+                                   void *stream);
+
+/* ---- a4: rank512 directory ------------------------------------------------ */
+/* [CB] "Temporary rank layouts" and "Corrected record ordinals". Over the
+ * bitmap C of m bits (tail bits zero) builds floor(m/512) + 1 entries of
+ * three uint32 each:
+ *   dir[3b]                       R(512 b), R(i) = sum_{t<i} C_t
+ *   dir[3b+1] | dir[3b+2] << 32   sub-prefix s = 1..7 in bits [9(s-1), 9s):
+ *                                 R(512 b + 64 s) - R(512 b)
+ * (positions past m count as m), and d_total[0] = R(m).
+ * C: device uint32[ceil(m/32)]; dir: device uint32[3 * (m/512 + 1)];
+ * d_total: device int64[1]. m < 2^31. At least one block is always built, so
+ * an empty A yields dir = {0,0,0} and R(0) = 0 ([CB] "Dispatch bindings"). */
+LSM_API int lsm_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* Rank queries: out[t] = R(pos[t]) for pos[t] in [0, m], using the directory,
+ * at most one preceding 32-bit word and the masked current word ([CB]
+ * "Temporary rank layouts"). A position above m yields 0xFFFFFFFF and
+ * records LSM_ERR_ARG in the device status. pos, out: device uint32[q]. */
+LSM_API int lsm_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
+                           const uint32_t *pos, int64_t q, uint32_t *out, void *stream);
+
+/* ---- a5: replacement merge by bitmap, rank and merge path ----------------- */
+/* [CB] "The three experimental paths" (bitmap, compact A, then Merge Path)
+ * and "Corrected record ordinals"; [GC] merge paragraph (keep the newer
+ * record; a newer tombstone remains a record). From the outputs of
+ * lsm_collision_mark (C, lb_B) and lsm_rank_build (dir) writes
+ *   out_refs[0..N)  the surviving records in merged order, N = m + n - R(m)
+ *   ord_A[i]        i + lower_bound(B, A_i) - R(i) for a surviving A_i,
+ *                   LSM_ORD_DROPPED when C_i = 1
+ *   ord_B[j]        j + lb_B[j] - R(lb_B[j])
+ *   d_count[0]      N
+ * The keys themselves are not read: B_j precedes A_i in the merge exactly
+ * when lb_B[j] <= i, so the merge path runs over positions.
+ * out_refs: device uint32[m + n] capacity; ord_A: uint32[m]; ord_B:
+ * uint32[n]; d_count: int64[1]. m, n < 2^31. */
+LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *C,
+                                          const uint32_t *dir, const uint32_t *lb_B,
+                                          uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
+                                          int64_t *d_count, void *ws, size_t ws_bytes,
+                                          void *stream);
+
+/* ---- a6: front-compression lengths and bit offsets ----------------------- */
+/* [GC], the control-argument equation and the record-length formula. For
+ * output record i (refs[i] names its key and value):
+ *   lcp[i]      l_i, exact bit LCP with record i-1's key, l_0 = 0, clamped
+ *               to the shorter key
+ *   ctrl[i]     c_i = 1 + l_i when i mod 15 = 0, else k_{i-1} - l_i
+ *   rec_bits[i] E(c_i) + E(k_i - l_i) + (k_i - l_i) + v_i, E(x) =
+ *               2 floor(log2(x+1)) + 1, v_i = 1 for a tombstone, else
+ *               1 + E(byte length) + 8 * byte length
+ *   bit_off[i]  sum_{t<i} rec_bits[t], for i = 0..N (bit_off[N] = total)
+ * Keys are byte strings; k_i = 8 * byte length. refs: device uint32[N];
+ * lcp, ctrl, rec_bits: device uint32[N]; bit_off: device uint64[N + 1].
+ * N < 2^31. A record whose fields exceed 32 bits records LSM_ERR_OVERFLOW in
+ * the device status. */
+LSM_API int lsm_fc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
+                                uint32_t *lcp, uint32_t *ctrl, uint32_t *rec_bits,
+                                uint64_t *bit_off, void *ws, size_t ws_bytes, void *stream);
+
+/* ---- a7: word-owned payload emit ------------------------------------------ */
+/* [GC], the paragraphs on exact lengths and on the record layout: one thread
+ * owns each 32-bit payload word, gathers its bits from the records that
+ * overlap it and writes it once. Record i occupies bits [bit_off[i],
+ * bit_off[i+1]) as EG0(c_i) EG0(k_i - l_i) key bits [l_i, k_i) value, value
+ * = 0 for a tombstone, else 1 EG0(byte length) bytes; EG0(x) is
+ * floor(log2(x+1)) zero bits followed by x+1 in binary. Stream bit t is bit
+ * 31 - t%32 of payload[t/32] (MSB first). All nwords words are written;
+ * bits past bit_off[N] are zero. nwords must be >= ceil(bit_off[N] / 32)
+ * (the host reads bit_off[N] once to size the payload). */
+LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
+                        const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
+                        uint32_t *payload, int64_t nwords, void *stream);
+
+/* ---- tuning ----------------------------------------------------------------- */
+/* Sets how many outputs each thread of lsm_merge_stable produces for the
+ * given key type (7, 11, 15 or 23; the tile is 256 times that). Process-wide
+ * setting, read at each call; the default is 15. This is the slice-size knob
+ * of [MP] "Measuring it against one thread" and "Results". */
+LSM_API int lsm_tune_merge_items(int key_type, int items_per_thread);
+
+/* ---- test hook ------------------------------------------------------------ */
+/* Launches one block that waits, with the same bounded wait the kernels
+ * use, on a device flag that nothing ever sets, and gives up after
+ * limit_ns nanoseconds (clamped to [1 us, 1 s]). The wait runs out by
+ * design: LSM_ERR_TIMEOUT is recorded in the device status word, the kernel
+ * returns and the CUDA context stays usable. Exists so that tests can check
+ * the timeout path without faulting or hanging a GPU. */
+LSM_API int lsm_debug_timeout_probe(int64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSMMERGE_H */

@@ -1,0 +1,348 @@
+"""Python binding of liblsmmerge.so, the GB300 merge-path replacement merge.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (PyTorch provides device memory and
+streams); each function passes their device pointers and the current CUDA
+stream to the C entry point of the same name (``lsm_<name>`` in
+``include/lsmmerge.h``) and raises ``LsmError`` on a non-zero status. Outputs
+the caller does not pass are allocated with torch.
+
+The library must be built first (``__graft_entry__.build()`` or
+``lsm_replacement_merge_gb300.build()``); importing this package never falls
+back to any other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblsmmerge.so")
+
+LSM_OK = 0
+LSM_ERR_TIMEOUT = 5
+LSM_KEY_I32 = 1
+LSM_KEY_U64 = 2
+LSM_OP_MERGE_STABLE = 1
+LSM_OP_COLLISION_MARK = 2
+LSM_OP_COLLISION_MARK_STR = 3
+LSM_OP_RANK_BUILD = 4
+LSM_OP_REPLACEMENT_COMPACT = 5
+LSM_OP_FC_LENGTHS_SCAN = 6
+REF_FROM_B = 0x80000000
+ORD_DROPPED = 0xFFFFFFFF
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LsmError(RuntimeError):
+    def __init__(self, name, status):
+        self.status = status
+        super().__init__("%s failed: %s" % (name, _status_string(status)))
+
+
+class _Bytes(ctypes.Structure):
+    _fields_ = [("arena", ctypes.c_void_p), ("off", ctypes.c_void_p)]
+
+
+class _FcInput(ctypes.Structure):
+    _fields_ = [("keyA", _Bytes), ("valA", _Bytes), ("tombA", ctypes.c_void_p), ("m", ctypes.c_int64),
+                ("keyB", _Bytes), ("valB", _Bytes), ("tombB", ctypes.c_void_p), ("n", ctypes.c_int64)]
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("liblsmmerge.so is not built (%s); run __graft_entry__.build()"
+                                   % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+            sig = {
+                "lsm_status_string": ([ctypes.c_int], ctypes.c_char_p),
+                "lsm_abi_version": ([], ctypes.c_int),
+                "lsm_get_device_status": ([P, ctypes.c_int, P], ctypes.c_int),
+                "lsm_workspace_size": ([ctypes.c_int, ctypes.c_int, I, I, P], ctypes.c_int),
+                "lsm_merge_path_partition": ([ctypes.c_int, P, I, P, I, I, P, P], ctypes.c_int),
+                "lsm_merge_stable": ([ctypes.c_int, P, P, I, P, P, I, P, P, P, S, P], ctypes.c_int),
+                "lsm_collision_mark": ([P, I, P, I, P, P, P, S, P], ctypes.c_int),
+                "lsm_collision_mark_str": ([P, I, P, I, P, P, P, S, P], ctypes.c_int),
+                "lsm_rank_build": ([P, I, P, P, P, S, P], ctypes.c_int),
+                "lsm_rank_query": ([P, P, I, P, I, P, P], ctypes.c_int),
+                "lsm_replacement_merge_compact": ([I, I, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+                "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
+                "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
+                "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
+                "lsm_tune_merge_items": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def _status_string(status):
+    try:
+        return lib().lsm_status_string(status).decode()
+    except Exception:  # pragma: no cover - only while reporting another error
+        return "status %d" % status
+
+
+def _check(name, rc):
+    if rc != LSM_OK:
+        raise LsmError(name, rc)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor, got one on %s" % t.device)
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _key_type(t):
+    if t.dtype == torch.int32:
+        return LSM_KEY_I32
+    if t.dtype in (torch.uint64, torch.int64):
+        return LSM_KEY_U64
+    raise TypeError("keys must be int32 or uint64 (int64 views are accepted), got %s" % t.dtype)
+
+
+def _empty(n, dtype, device):
+    return torch.empty(int(n), dtype=dtype, device=device)
+
+
+# ---------------------------------------------------------------------------
+# utilities
+# ---------------------------------------------------------------------------
+def abi_version() -> int:
+    return lib().lsm_abi_version()
+
+
+def workspace_size(op: int, m: int, n: int, key_type: int = LSM_KEY_U64) -> int:
+    out = ctypes.c_size_t(0)
+    _check("lsm_workspace_size", lib().lsm_workspace_size(op, key_type, m, n, ctypes.byref(out)))
+    return out.value
+
+
+def workspace(op: int, m: int, n: int, device, key_type: int = LSM_KEY_U64):
+    return torch.empty(workspace_size(op, m, n, key_type), dtype=torch.uint8, device=device)
+
+
+def get_device_status(reset: bool = False, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    _check("lsm_get_device_status",
+           lib().lsm_get_device_status(ctypes.byref(st), int(bool(reset)), _stream(stream)))
+    return st.value
+
+
+def tune_merge_items(key_type: int, items_per_thread: int) -> None:
+    _check("lsm_tune_merge_items", lib().lsm_tune_merge_items(key_type, items_per_thread))
+
+
+def debug_timeout_probe(limit_ns: int, stream=None) -> None:
+    _check("lsm_debug_timeout_probe", lib().lsm_debug_timeout_probe(int(limit_ns), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# a1, a2: partition and stable merge
+# ---------------------------------------------------------------------------
+def merge_path_partition(A, B, items_per_tile: int, out_ij=None, stream=None):
+    m, n = A.numel(), B.numel()
+    G = (m + n + items_per_tile - 1) // items_per_tile
+    if out_ij is None:
+        out_ij = _empty(2 * (G + 1), torch.int64, A.device)
+    _check("lsm_merge_path_partition",
+           lib().lsm_merge_path_partition(_key_type(A), _ptr(A), m, _ptr(B), n, items_per_tile,
+                                          _ptr(out_ij), _stream(stream)))
+    return out_ij.view(G + 1, 2)
+
+
+def merge_stable(A, B, Apay=None, Bpay=None, out_keys=None, out_pay=None, ws=None, stream=None):
+    kt = _key_type(A)
+    m, n = A.numel(), B.numel()
+    dev = A.device
+    if out_keys is None:
+        out_keys = _empty(m + n, A.dtype, dev)
+    if Apay is not None and out_pay is None:
+        out_pay = _empty(m + n, torch.uint32, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_MERGE_STABLE, m, n, dev, kt)
+    _check("lsm_merge_stable",
+           lib().lsm_merge_stable(kt, _ptr(A), _ptr(Apay), m, _ptr(B), _ptr(Bpay), n,
+                                  _ptr(out_keys), _ptr(out_pay), _ptr(ws), ws.numel(),
+                                  _stream(stream)))
+    return out_keys, out_pay
+
+
+# ---------------------------------------------------------------------------
+# a3 - a5: replacement merge
+# ---------------------------------------------------------------------------
+def collision_mark(A, B, C=None, lb_B=None, ws=None, stream=None):
+    m, n = A.numel(), B.numel()
+    dev = A.device
+    if C is None:
+        C = _empty((m + 31) // 32, torch.uint32, dev)
+    if lb_B is None:
+        lb_B = _empty(n, torch.uint32, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_COLLISION_MARK, m, n, dev)
+    _check("lsm_collision_mark",
+           lib().lsm_collision_mark(_ptr(A), m, _ptr(B), n, _ptr(C), _ptr(lb_B), _ptr(ws),
+                                    ws.numel(), _stream(stream)))
+    return C, lb_B
+
+
+class Bytes:
+    """A CSR byte column on the device: arena (uint8, padded so that it stays
+    readable to the next multiple of 8 bytes) and offsets (uint64[count+1])."""
+
+    def __init__(self, arena, off):
+        self.arena, self.off = arena, off
+
+    @property
+    def count(self):
+        return self.off.numel() - 1
+
+    @staticmethod
+    def from_numpy(arena: np.ndarray, off: np.ndarray, device):
+        size = int(len(arena))
+        padded = np.zeros((size + 7) // 8 * 8 + 8, dtype=np.uint8)
+        padded[:size] = arena
+        return Bytes(torch.from_numpy(padded).to(device),
+                     torch.from_numpy(np.ascontiguousarray(off, dtype=np.uint64)).to(device))
+
+    def _c(self):
+        return _Bytes(_ptr(self.arena), _ptr(self.off))
+
+
+def collision_mark_str(A: Bytes, B: Bytes, C=None, lb_B=None, ws=None, stream=None):
+    m, n = A.count, B.count
+    dev = A.off.device
+    if C is None:
+        C = _empty((m + 31) // 32, torch.uint32, dev)
+    if lb_B is None:
+        lb_B = _empty(n, torch.uint32, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_COLLISION_MARK_STR, m, n, dev)
+    a, b = A._c(), B._c()
+    _check("lsm_collision_mark_str",
+           lib().lsm_collision_mark_str(ctypes.byref(a), m, ctypes.byref(b), n, _ptr(C), _ptr(lb_B),
+                                        _ptr(ws), ws.numel(), _stream(stream)))
+    return C, lb_B
+
+
+def rank_build(C, m: int, dir_=None, d_total=None, ws=None, stream=None):
+    dev = C.device
+    if dir_ is None:
+        dir_ = _empty(3 * (m // 512 + 1), torch.uint32, dev)
+    if d_total is None:
+        d_total = _empty(1, torch.int64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_RANK_BUILD, m, 0, dev)
+    _check("lsm_rank_build",
+           lib().lsm_rank_build(_ptr(C) if m else None, m, _ptr(dir_), _ptr(d_total), _ptr(ws),
+                                ws.numel(), _stream(stream)))
+    return dir_, d_total
+
+
+def rank_query(C, dir_, m: int, pos, out=None, stream=None):
+    q = pos.numel()
+    if out is None:
+        out = _empty(q, torch.uint32, pos.device)
+    _check("lsm_rank_query",
+           lib().lsm_rank_query(_ptr(C) if m else None, _ptr(dir_), m, _ptr(pos), q, _ptr(out),
+                                _stream(stream)))
+    return out
+
+
+def replacement_merge_compact(m: int, n: int, C, dir_, lb_B, refs=None, ord_A=None, ord_B=None,
+                              d_count=None, ws=None, stream=None):
+    dev = dir_.device
+    if refs is None:
+        refs = _empty(max(m + n, 1), torch.uint32, dev)
+    if ord_A is None:
+        ord_A = _empty(m, torch.uint32, dev)
+    if ord_B is None:
+        ord_B = _empty(n, torch.uint32, dev)
+    if d_count is None:
+        d_count = _empty(1, torch.int64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
+    _check("lsm_replacement_merge_compact",
+           lib().lsm_replacement_merge_compact(m, n, _ptr(C) if m else None, _ptr(dir_),
+                                               _ptr(lb_B) if n else None, _ptr(refs),
+                                               _ptr(ord_A) if m else None, _ptr(ord_B) if n else None,
+                                               _ptr(d_count), _ptr(ws), ws.numel(), _stream(stream)))
+    return refs, ord_A, ord_B, d_count
+
+
+# ---------------------------------------------------------------------------
+# a6, a7: front compression
+# ---------------------------------------------------------------------------
+class FcInput:
+    """Keys, values and tombstone bitmaps of both sources, on the device."""
+
+    def __init__(self, keyA: Bytes, valA: Bytes, tombA, keyB: Bytes, valB: Bytes, tombB):
+        self.keyA, self.valA, self.tombA = keyA, valA, tombA
+        self.keyB, self.valB, self.tombB = keyB, valB, tombB
+
+    def _c(self):
+        return _FcInput(self.keyA._c(), self.valA._c(), _ptr(self.tombA), self.keyA.count,
+                        self.keyB._c(), self.valB._c(), _ptr(self.tombB), self.keyB.count)
+
+
+def fc_lengths_scan(fc: FcInput, refs, N: int, lcp=None, ctrl=None, rec_bits=None, bit_off=None,
+                    ws=None, stream=None):
+    dev = fc.keyA.off.device
+    if lcp is None:
+        lcp = _empty(N, torch.uint32, dev)
+    if ctrl is None:
+        ctrl = _empty(N, torch.uint32, dev)
+    if rec_bits is None:
+        rec_bits = _empty(N, torch.uint32, dev)
+    if bit_off is None:
+        bit_off = _empty(N + 1, torch.uint64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_FC_LENGTHS_SCAN, N, 0, dev)
+    c = fc._c()
+    _check("lsm_fc_lengths_scan",
+           lib().lsm_fc_lengths_scan(ctypes.byref(c), _ptr(refs) if N else None, N,
+                                     _ptr(lcp) if N else None, _ptr(ctrl) if N else None,
+                                     _ptr(rec_bits) if N else None, _ptr(bit_off), _ptr(ws),
+                                     ws.numel(), _stream(stream)))
+    return lcp, ctrl, rec_bits, bit_off
+
+
+def fc_emit(fc: FcInput, refs, N: int, lcp, ctrl, bit_off, nwords: int, payload=None, stream=None):
+    dev = fc.keyA.off.device
+    if payload is None:
+        payload = _empty(max(nwords, 1), torch.uint32, dev)
+    c = fc._c()
+    _check("lsm_fc_emit",
+           lib().lsm_fc_emit(ctypes.byref(c), _ptr(refs) if N else None, N,
+                             _ptr(lcp) if N else None, _ptr(ctrl) if N else None, _ptr(bit_off),
+                             _ptr(payload) if nwords else None, nwords, _stream(stream)))
+    return payload

@@ -1,0 +1,219 @@
+// common.cuh -- device helpers shared by the merge-path kernels (sm_103a).
+//
+// Bulk asynchronous copies (the TMA engine's 1-D form) stage each CTA's
+// merge-path tile into shared memory and write finished tiles back; an
+// mbarrier with a transaction count tracks the loads. Every wait is bounded
+// in time: past the limit the kernel records LSM_ERR_TIMEOUT in the status
+// word it was given and returns, so that a stuck wait cannot hang the GPU.
+#pragma once
+
+#include <cstdint>
+
+#include "lsmmerge.h"
+
+namespace lsm {
+
+constexpr int64_t kWaitLimitNs = 1000000000LL;  // one second
+
+__host__ __device__ constexpr int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// First error wins; later errors do not overwrite it.
+__device__ __forceinline__ void report(int32_t *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier --------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, for at most
+// limit_ns nanoseconds (and a bounded number of polls). Returns false when
+// the limit ran out.
+static __device__ __noinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 63 && globaltimer_ns() - t0 > static_cast<uint64_t>(limit_ns)) return false;
+  }
+  return false;
+}
+
+// ---- bulk copies -------------------------------------------------------------
+// global -> shared, completion counted on `bar` (bytes: multiple of 16,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// shared -> global in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (a following bulk store reads them).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- staging a 1-D span into shared memory ----------------------------------
+// Global elements [s, s + c) of size SZ (array base 16-byte aligned) land in
+// a 16-byte aligned shared buffer so that element s + x sits at buf[lead + x].
+// The 16-byte aligned interior [alo, ahi) moves with one bulk copy; the at
+// most 16/SZ - 1 elements after ahi move with plain loads (stage_tail), so
+// nothing past s + c is ever read.
+struct StagePlan {
+  int64_t first;      // global index of buf[0]
+  int64_t tail_from;  // first global index loaded with plain loads
+  int32_t lead;       // s - first
+  uint32_t bulk;      // bytes of the bulk copy (multiple of 16, may be 0)
+  int32_t span;       // lead + c: elements of buf in use
+};
+
+template <int SZ>
+__device__ __forceinline__ StagePlan stage_plan(int64_t s, int64_t c) {
+  const int64_t lo = s * SZ, hi = (s + c) * SZ;
+  const int64_t alo = lo & ~int64_t(15), ahi = hi & ~int64_t(15);
+  StagePlan p;
+  p.first = alo / SZ;
+  p.lead = static_cast<int32_t>(s - p.first);
+  p.bulk = static_cast<uint32_t>(ahi > alo ? ahi - alo : 0);
+  p.tail_from = ahi / SZ > s ? ahi / SZ : s;
+  p.span = static_cast<int32_t>(p.lead + c);
+  return p;
+}
+
+template <int SZ>
+__host__ __device__ constexpr int64_t stage_capacity_bytes(int64_t c) {
+  return align_up(c * SZ + 16, 16);
+}
+
+template <typename T>
+__device__ __forceinline__ void stage_issue(T *buf, const T *g, const StagePlan &p, uint64_t *bar) {
+  if (p.bulk) bulk_g2s(buf, g + p.first, p.bulk, bar);
+}
+
+template <typename T>
+__device__ __forceinline__ void stage_tail(T *buf, const T *g, const StagePlan &p, int64_t s,
+                                           int64_t c, int tid) {
+  const int64_t x = p.tail_from + tid;
+  if (x < s + c) buf[x - p.first] = g[x];
+}
+
+// ---- scans ------------------------------------------------------------------
+template <typename V>
+__device__ __forceinline__ V warp_inclusive_sum(V v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    V u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// Block-wide exclusive sum for a block of NT threads (NT multiple of 32).
+// `scratch` holds NT/32 + 1 values. Returns the exclusive prefix; *total
+// receives the block sum. Contains __syncthreads().
+template <int NT, typename V>
+__device__ __forceinline__ V block_exclusive_sum(V v, V *scratch, V *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  V inc = warp_inclusive_sum(v);
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    V w = lane < NT / 32 ? scratch[lane] : V(0);
+    V wi = warp_inclusive_sum(w);
+    if (lane < NT / 32) scratch[lane] = wi - w;
+    if (lane == NT / 32 - 1) scratch[NT / 32] = wi;
+  }
+  __syncthreads();
+  V out = scratch[warp] + inc - v;
+  *total = scratch[NT / 32];
+  __syncthreads();
+  return out;
+}
+
+template <int NT, typename V>
+__device__ __forceinline__ V block_sum(V v, V *scratch) {
+  V total;
+  block_exclusive_sum<NT>(v, scratch, &total);
+  return total;
+}
+
+// ---- warp-cooperative merge-path search ----------------------------------------
+// Finds, for one diagonal k, the co-rank i in [max(0, k-n), min(k, m)]: the
+// first i for which pred.too_small(i, k) is false, where too_small(i, k)
+// means "A_i precedes B_{k-i-1} in the merge" (so more A elements belong
+// before the diagonal). Each round the 32 lanes probe 32 evenly spaced
+// candidates and the ballot narrows the range about 33-fold, so a search
+// over 2^26 candidates takes six dependent rounds instead of 26.
+template <class Pred>
+__device__ __forceinline__ int64_t warp_corank(const Pred &pred, int64_t k, int64_t m, int64_t n) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = k > n ? k - n : 0;
+  int64_t hi = k < m ? k : m;
+  while (hi > lo) {
+    const int64_t span = hi - lo;
+    const bool last = span <= 32;
+    const int64_t p = last ? lo + lane : lo + ((int64_t)(lane + 1) * span) / 33;
+    const bool small = (p < hi) && pred.too_small(p, k);
+    const int t = __popc(__ballot_sync(0xffffffffu, small));
+    if (last) {
+      lo += t;
+      break;
+    }
+    const int64_t p_prev = t > 0 ? lo + ((int64_t)t * span) / 33 : lo - 1;
+    const int64_t p_next = t < 32 ? lo + ((int64_t)(t + 1) * span) / 33 : hi;
+    lo = p_prev + 1;
+    hi = p_next;
+  }
+  return lo;
+}
+
+}  // namespace lsm

@@ -1,0 +1,71 @@
+// internal.h -- launchers shared between the kernel files and the C ABI layer.
+// Host-side only; every launcher enqueues on `stream` and returns the CUDA
+// launch status. Argument checking happens in api.cu before these run.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "lsmmerge.h"
+
+namespace lsm {
+
+// Tile geometry. Items per thread are odd so that per-thread output runs in
+// shared memory fall on distinct banks.
+constexpr int kMergeThreads = 256;
+constexpr int kMarkThreads = 256;
+constexpr int kCompactThreads = 256;
+constexpr int kRankThreads = 256;
+
+int merge_items_per_thread(int key_type);  // current setting (tunable)
+int set_merge_items_per_thread(int key_type, int e);  // returns LSM_OK or LSM_ERR_ARG
+constexpr int kMarkItems = 15;
+constexpr int kCompactItems = 15;
+constexpr int64_t kMinMergeTile = kMergeThreads * 7;
+
+// --- merge.cu ---
+cudaError_t launch_partition_keys(int key_type, const void *A, int64_t m, const void *B, int64_t n,
+                                  int64_t D, int64_t *out_i, int64_t *out_ij, cudaStream_t s);
+cudaError_t launch_merge_stable(int key_type, const void *A, const uint32_t *Apay, int64_t m,
+                                const void *B, const uint32_t *Bpay, int64_t n, void *out,
+                                uint32_t *out_pay, int64_t *part_i, int32_t *status,
+                                cudaStream_t s);
+
+// --- replace.cu ---
+cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                  uint32_t *C, uint32_t *lb_B, int64_t *part_i, int32_t *status,
+                                  cudaStream_t s);
+cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
+                              uint32_t *cta_totals, cudaStream_t s);
+cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
+                              const uint32_t *pos, int64_t q, uint32_t *out, int32_t *status,
+                              cudaStream_t s);
+cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
+                           const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
+                           uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,
+                           cudaStream_t s);
+int64_t rank_build_ctas(int64_t m);
+
+// --- strings.cu ---
+cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,
+                                      uint32_t *C, uint32_t *lb_B, int64_t *part_i,
+                                      int32_t *status, cudaStream_t s);
+constexpr int kMarkStrThreads = 128;
+constexpr int kMarkStrItems = 7;
+
+// --- fc.cu ---
+int64_t fc_scan_tiles(int64_t N);
+size_t fc_scan_workspace_bytes(int64_t N);
+cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
+                                   uint32_t *lcp, uint32_t *ctrl, uint32_t *rec_bits,
+                                   uint64_t *bit_off, void *ws, int32_t *status, cudaStream_t s);
+cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
+                           const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
+                           uint32_t *payload, int64_t nwords, int32_t *status, cudaStream_t s);
+
+// --- api.cu ---
+cudaError_t launch_timeout_probe(int64_t limit_ns, int32_t *status, cudaStream_t s);
+
+}  // namespace lsm

@@ -1,0 +1,76 @@
+// strings.cuh -- byte-string keys on the device.
+//
+// Keys live in CSR arenas (bytes + uint64 offsets). They are read as
+// big-endian 8-byte windows built from aligned 8-byte loads, so that one
+// comparison step covers eight bytes; bytes past a key's end are masked to
+// zero. Order is unsigned lexicographic with a proper prefix first
+// ("Everett: GPU construction experiment", prefix-cache paragraph: zero
+// padding plus the original length keeps proper-prefix order exact; the
+// LCP clamps to the shorter key).
+//
+// Readability contract (checked on the host): each arena starts on an
+// 8-byte boundary and stays readable up to the next multiple of 8 bytes
+// past its last byte. A window load touches the aligned word holding `pos`
+// and, only when the key continues past it, the next aligned word.
+#pragma once
+
+#include <cstdint>
+
+#include "lsmmerge.h"
+
+namespace lsm {
+
+__device__ __forceinline__ uint64_t bswap64(uint64_t x) {
+  const uint32_t lo = static_cast<uint32_t>(x), hi = static_cast<uint32_t>(x >> 32);
+  return (static_cast<uint64_t>(__byte_perm(lo, 0, 0x0123)) << 32) | __byte_perm(hi, 0, 0x0123);
+}
+
+// Bytes [pos, min(pos + 8, end)) of `arena` as a big-endian word: byte pos
+// in bits 63..56. Requires pos < end.
+__device__ __forceinline__ uint64_t load_be64(const uint8_t *__restrict__ arena, uint64_t pos,
+                                              uint64_t end) {
+  const uint64_t *w = reinterpret_cast<const uint64_t *>(arena);
+  const uint64_t q = pos >> 3;
+  const unsigned r = static_cast<unsigned>(pos & 7);
+  uint64_t x = __ldg(w + q) >> (8 * r);
+  if (r && 8 * q + 8 < end) x |= __ldg(w + q + 1) << (64 - 8 * r);
+  uint64_t be = bswap64(x);
+  const uint64_t avail = end - pos;
+  if (avail < 8) be &= ~uint64_t(0) << (8 * (8 - avail));
+  return be;
+}
+
+struct KeyRef {
+  const uint8_t *arena;
+  uint64_t begin, end;
+};
+
+__device__ __forceinline__ KeyRef key_at(const lsm_bytes &col, int64_t idx) {
+  return KeyRef{col.arena, __ldg(col.off + idx), __ldg(col.off + idx + 1)};
+}
+
+// Three-way comparison: negative, zero or positive.
+__device__ __forceinline__ int key_cmp(const KeyRef &a, const KeyRef &b) {
+  const uint64_t la = a.end - a.begin, lb = b.end - b.begin;
+  const uint64_t l = la < lb ? la : lb;
+  for (uint64_t t = 0; t < l; t += 8) {
+    const uint64_t x = load_be64(a.arena, a.begin + t, a.begin + l);
+    const uint64_t y = load_be64(b.arena, b.begin + t, b.begin + l);
+    if (x != y) return x < y ? -1 : 1;
+  }
+  return la == lb ? 0 : (la < lb ? -1 : 1);
+}
+
+// Exact bit LCP, clamped to the shorter key.
+__device__ __forceinline__ uint64_t key_bit_lcp(const KeyRef &a, const KeyRef &b) {
+  const uint64_t la = a.end - a.begin, lb = b.end - b.begin;
+  const uint64_t l = la < lb ? la : lb;
+  for (uint64_t t = 0; t < l; t += 8) {
+    const uint64_t x = load_be64(a.arena, a.begin + t, a.begin + l);
+    const uint64_t y = load_be64(b.arena, b.begin + t, b.begin + l);
+    if (x != y) return 8 * t + static_cast<uint64_t>(__clzll(x ^ y));
+  }
+  return 8 * l;
+}
+
+}  // namespace lsm

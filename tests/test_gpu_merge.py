@@ -1,0 +1,124 @@
+"""GPU parity for the merge path partition and the stable merge (C ABI vs oracle).
+
+Bit-exact: keys, payloads and co-ranks must equal the oracle's element by
+element, with A first on ties."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from tests.gpu_util import down, up  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lsm():
+    import lsm_replacement_merge_gb300 as lsm
+    lsm.lib()
+    lsm.get_device_status(reset=True)
+    yield lsm
+    assert lsm.get_device_status() == lsm.LSM_OK
+    for kt in (lsm.LSM_KEY_I32, lsm.LSM_KEY_U64):
+        lsm.tune_merge_items(kt, 15)
+
+
+def test_worked_example_and_page_cases(lsm, golden):
+    g = golden("merge_path_worked_example.txt")
+    for dt in (np.int32, np.uint64):
+        a, b = np.array(g["a"], dt), np.array(g["b"], dt)
+        keys, _ = lsm.merge_stable(up(a), up(b))
+        assert down(keys).tolist() == g["merged"]
+        part = down(lsm.merge_path_partition(up(a), up(b), 2))
+        assert part[:, 0].tolist() == g["crossing_i"]
+        assert part.sum(axis=1).tolist() == g["crossing_k"]
+        assert down(lsm.merge_path_partition(up(a), up(b), 3))[1, 0] == g["corank_i"][0]
+    c = golden("corank_chapter14.txt")
+    part = down(lsm.merge_path_partition(up(np.array(c["A"], np.int32)),
+                                         up(np.array(c["B"], np.int32)), 1))
+    assert part[:8, 0].tolist() == c["i"] and part[:8, 1].tolist() == c["j"]
+    t = golden("corank_trap.txt")
+    part = down(lsm.merge_path_partition(up(np.array(t["a"], np.int32)),
+                                         up(np.array(t["b"], np.int32)), t["k"][0]))
+    assert part[1, 0] == t["i"][0]
+    p = golden("tie_provenance.txt")
+    a, b = np.array(p["a"], np.int32), np.array(p["b"], np.int32)
+    # payload = source index reproduces the provenance check of the exercise
+    keys, pay = lsm.merge_stable(up(a), up(b), up(np.arange(3, dtype=np.uint32)),
+                                 up(np.arange(3, 6, dtype=np.uint32)))
+    assert down(keys).tolist() == p["values"] and down(pay).tolist() == p["provenance"]
+    part = down(lsm.merge_path_partition(up(a), up(b), p["k"][0]))
+    assert part[1, 0] == p["i"][0]
+
+
+SIZES = [(0, 1), (1, 0), (1, 1), (7, 3), (3840 * 3 + 17, 1000), (4096, 4096), (50000, 70001),
+         (100000, 5), (5, 100000), (1 << 16, 1 << 16)]
+
+
+def _inputs(dt, m, n, seed, hi):
+    rng = np.random.default_rng(seed)
+    if dt == np.int32:
+        A = np.sort(rng.integers(-hi, hi, size=m).astype(np.int32))
+        B = np.sort(rng.integers(-hi, hi, size=n).astype(np.int32))
+    else:
+        A = np.sort(rng.integers(0, hi, size=m, dtype=np.uint64))
+        B = np.sort(rng.integers(0, hi, size=n, dtype=np.uint64))
+    return A, B, np.arange(m, dtype=np.uint32), (m + np.arange(n)).astype(np.uint32)
+
+
+@pytest.mark.parametrize("items", [7, 11, 15, 23])
+@pytest.mark.parametrize("dt,hi", [(np.int32, 3), (np.int32, 1 << 30), (np.uint64, 16),
+                                   (np.uint64, 1 << 63)])
+def test_merge_stable_parity(lsm, items, dt, hi):
+    kt = lsm.LSM_KEY_I32 if dt == np.int32 else lsm.LSM_KEY_U64
+    lsm.tune_merge_items(kt, items)
+    for s, (m, n) in enumerate(SIZES):
+        A, B, Ap, Bp = _inputs(dt, m, n, 1000 * items + s, hi)
+        ok, okp, _ = oracle.merge(A, B, Ap, Bp)
+        keys, pay = lsm.merge_stable(up(A), up(B), up(Ap), up(Bp))
+        assert np.array_equal(down(keys), ok), (m, n)
+        assert np.array_equal(down(pay), okp), (m, n)
+        keys2, none = lsm.merge_stable(up(A), up(B))
+        assert none is None and np.array_equal(down(keys2), ok)
+    lsm.tune_merge_items(kt, 15)
+
+
+@pytest.mark.parametrize("D", [1, 2, 7, 1000, 3840])
+def test_partition_parity(lsm, D):
+    for dt, hi in ((np.int32, 5), (np.uint64, 1 << 40)):
+        for m, n in ((0, 0), (0, 17), (17, 0), (300, 200), (20000, 3)):
+            A, B, _, _ = _inputs(dt, m, n, m + n + D, hi)
+            expect = oracle.partition(A, B, D)
+            got = down(lsm.merge_path_partition(up(A), up(B), D))
+            assert np.array_equal(got, expect), (dt, m, n, D)
+
+
+def test_all_equal_and_empty(lsm):
+    A = np.full(9000, 5, np.int32)
+    B = np.full(7000, 5, np.int32)
+    ok, okp, _ = oracle.merge(A, B, np.arange(9000, dtype=np.uint32),
+                              np.arange(9000, 16000, dtype=np.uint32))
+    keys, pay = lsm.merge_stable(up(A), up(B), up(np.arange(9000, dtype=np.uint32)),
+                                 up(np.arange(9000, 16000, dtype=np.uint32)))
+    assert np.array_equal(down(pay), okp)          # all of A, then all of B
+    keys, _ = lsm.merge_stable(up(np.zeros(0, np.uint64)), up(np.zeros(0, np.uint64)))
+    assert keys.numel() == 0
+
+
+def test_config_int32_4096(lsm):
+    mi = synth.merge_i32()
+    ok, okp, _ = oracle.merge(mi.A, mi.B, mi.Apay, mi.Bpay)
+    keys, pay = lsm.merge_stable(up(mi.A), up(mi.B), up(mi.Apay), up(mi.Bpay))
+    assert np.array_equal(down(keys), ok) and np.array_equal(down(pay), okp)
+
+
+def test_full_size_u64_2pow26(lsm):
+    """The 2^26 + 2^26 uint64 merge with payload, in the launch configuration
+    the benchmark times, compared whole against the oracle."""
+    mi = synth.merge_u64()
+    ok, okp, _ = oracle.merge(mi.A, mi.B, mi.Apay, mi.Bpay)
+    keys, pay = lsm.merge_stable(up(mi.A), up(mi.B), up(mi.Apay), up(mi.Bpay))
+    assert np.array_equal(down(keys), ok)
+    assert np.array_equal(down(pay), okp)

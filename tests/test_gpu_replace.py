@@ -1,0 +1,114 @@
+"""GPU parity for the replacement merge: collision bitmap and lower bounds,
+rank512 directory and queries, and the compaction into survivor refs and
+ordinals (C ABI vs oracle, bit-exact)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from tests.gpu_util import down, up  # noqa: E402
+from tests.test_oracle_pins import REPLACE_CASES, _maps, _pack  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lsm():
+    import lsm_replacement_merge_gb300 as lsm
+    lsm.lib()
+    lsm.get_device_status(reset=True)
+    yield lsm
+    assert lsm.get_device_status() == lsm.LSM_OK
+
+
+def run_pipeline(lsm, A, B):
+    m, n = len(A), len(B)
+    C, lb = lsm.collision_mark(up(A), up(B))
+    dir_, tot = lsm.rank_build(C, m)
+    refs, ordA, ordB, cnt = lsm.replacement_merge_compact(m, n, C, dir_, lb)
+    N = int(cnt.item())
+    return dict(C=down(C), lb=down(lb), dir=down(dir_), total=int(tot.item()), refs=down(refs)[:N],
+                ordA=down(ordA), ordB=down(ordB), count=N)
+
+
+def check_against_oracle(got, A, B):
+    r = oracle.replacement_u64(A, B)
+    m = len(A)
+    assert got["count"] == r.count
+    assert np.array_equal(got["C"], r.C)
+    assert np.array_equal(got["lb"], r.lb_B)
+    assert got["total"] == len(A) + len(B) - r.count
+    assert np.array_equal(got["dir"], oracle.rank512_dir(r.C, m))
+    assert np.array_equal(got["refs"], r.refs)
+    assert np.array_equal(got["ordA"], r.ord_A)
+    assert np.array_equal(got["ordB"], r.ord_B)
+
+
+@pytest.mark.parametrize("m,n,shared,universe", REPLACE_CASES + [
+    (20000, 7000, 7000, None), (7000, 20000, 7000, None), (100000, 100000, 50000, 250000),
+    (300000, 2000, 1000, None), (2000, 300000, 2000, None)])
+def test_replacement_pipeline_parity(lsm, m, n, shared, universe):
+    if m + n == 0:
+        C, lb = lsm.collision_mark(up(np.zeros(0, np.uint64)), up(np.zeros(0, np.uint64)))
+        dir_, tot = lsm.rank_build(C, 0)
+        refs, _, _, cnt = lsm.replacement_merge_compact(0, 0, C, dir_, lb)
+        assert int(cnt.item()) == 0 and int(tot.item()) == 0
+        assert down(dir_).tolist() == [0, 0, 0]
+        return
+    inp = synth.replace_random_small(seed=m * 7 + n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    check_against_oracle(run_pipeline(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_single_record_edges(lsm):
+    A = synth.replace_u64(seed=40, m=5000, n=10).A
+    for B in (A[2500:2501].copy(), np.array([A[2500] + np.uint64(1)], np.uint64),
+              A[:1].copy(), A[-1:].copy()):
+        check_against_oracle(run_pipeline(lsm, A, B), A, B)
+    # |A| = 0 against a clustered B
+    sk = synth.replace_skewed(seed=41, m=60000, windows=8, window=512, per_window_shared=200,
+                              per_window_fresh=100)
+    check_against_oracle(run_pipeline(lsm, np.zeros(0, np.uint64), sk.B), np.zeros(0, np.uint64), sk.B)
+    check_against_oracle(run_pipeline(lsm, sk.A, np.zeros(0, np.uint64)), sk.A, np.zeros(0, np.uint64))
+
+
+@pytest.mark.parametrize("m,kind,bits", list(_maps()))
+def test_rank_build_and_query_every_position(lsm, m, kind, bits):
+    C = _pack(bits)
+    Cd = up(C) if len(C) else up(np.zeros(4, np.uint32))
+    dir_, tot = lsm.rank_build(Cd, m)
+    R = oracle.rank_prefix(C, m)
+    assert np.array_equal(down(dir_), oracle.rank512_dir(C, m))
+    assert int(tot.item()) == int(R[m])
+    pos = np.arange(m + 1, dtype=np.uint32)
+    got = down(lsm.rank_query(Cd, dir_, m, up(pos)))
+    assert np.array_equal(got, R)
+
+
+def test_rank_query_out_of_range_sets_status(lsm):
+    C = _pack(np.ones(100, bool))
+    dir_, _ = lsm.rank_build(up(C), 100)
+    out = down(lsm.rank_query(up(C), dir_, 100, up(np.array([100, 101], np.uint32))))
+    assert out.tolist() == [100, 0xFFFFFFFF]
+    assert lsm.get_device_status(reset=True) == 1   # LSM_ERR_ARG, then cleared
+
+
+def test_config_replace_12M_4M(lsm):
+    inp = synth.replace_u64()
+    check_against_oracle(run_pipeline(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_config_skewed_2pow24(lsm):
+    inp = synth.replace_skewed()
+    check_against_oracle(run_pipeline(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_timeout_probe_reports_and_context_survives(lsm):
+    lsm.get_device_status(reset=True)
+    lsm.debug_timeout_probe(2_000_000)          # 2 ms wait on a flag nothing sets
+    assert lsm.get_device_status(reset=True) == lsm.LSM_ERR_TIMEOUT
+    A = np.arange(0, 100, 2, dtype=np.uint64)
+    B = np.arange(0, 100, 3, dtype=np.uint64)
+    check_against_oracle(run_pipeline(lsm, A, B), A, B)

@@ -1,0 +1,64 @@
+"""GPU parity for the string-key collision mark (and the key-free compaction
+that follows it) against the oracle's string replacement walk."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from tests.gpu_util import down, up  # noqa: E402
+from tests.test_oracle_pins import _str_cases  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lsm():
+    import lsm_replacement_merge_gb300 as lsm
+    lsm.lib()
+    lsm.get_device_status(reset=True)
+    yield lsm
+    assert lsm.get_device_status() == lsm.LSM_OK
+
+
+def run_str(lsm, s):
+    dev = torch.device("cuda:0")
+    A = lsm.Bytes.from_numpy(s.A.key_arena, s.A.key_off, dev)
+    B = lsm.Bytes.from_numpy(s.B.key_arena, s.B.key_off, dev)
+    m, n = A.count, B.count
+    if m + n == 0:
+        return None
+    C, lb = lsm.collision_mark_str(A, B)
+    if m == 0:
+        C = up(np.zeros(4, np.uint32))
+    dir_, _ = lsm.rank_build(C, m)
+    refs, ordA, ordB, cnt = lsm.replacement_merge_compact(m, n, C, dir_, lb)
+    N = int(cnt.item())
+    return down(C)[: (m + 31) // 32], down(lb), down(refs)[:N], down(ordA), down(ordB)
+
+
+def check(lsm, s):
+    got = run_str(lsm, s)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    if got is None:
+        assert r.count == 0
+        return
+    C, lb, refs, ordA, ordB = got
+    assert np.array_equal(C, r.C) and np.array_equal(lb, r.lb_B)
+    assert np.array_equal(refs, r.refs)
+    assert np.array_equal(ordA, r.ord_A) and np.array_equal(ordB, r.ord_B)
+
+
+@pytest.mark.parametrize("case", list(_str_cases()))
+def test_small_string_cases(lsm, case):
+    check(lsm, synth.strings_from_lists(*case))
+
+
+@pytest.mark.parametrize("seed,count", [(0, 500), (1, 3000), (2, 20000)])
+def test_prefix_tree_strings(lsm, seed, count):
+    check(lsm, synth.strings(seed=seed, count=count, fanout=8, depth=2, max_suffix=20))
+
+
+def test_config_strings_4M(lsm):
+    check(lsm, synth.strings())
