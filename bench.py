@@ -1,0 +1,570 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 merge-path replacement merge (one JSON line).
+
+Headline workload: the stable merge of two sorted uint64 key arrays of 2^26
+elements each, every key carrying a uint32 payload (its source index). One
+step is one lsm_merge_stable call (merge path partition + tile merge) over
+inputs already resident in HBM. The metric is merged elements per second
+(input elements / time); the line also reports the tile kernel's achieved HBM
+bandwidth against the measured copy peak.
+
+The same line carries, under "workloads", the other hot-path pipelines, each
+timed as a whole path:
+  int32 4096+4096 merge          (latency-bound)
+  replacement 12,000,000 + 4,000,000 uint64 keys: collision_mark, rank_build,
+                                 replacement_merge_compact
+  skewed replacement 2^24-1 + 65,536 keys (clustered)
+  string replacement + FC encode, 4,000,000 + 4,000,000 keys: collision_mark_str,
+                                 rank_build, replacement_merge_compact,
+                                 fc_lengths_scan, fc_emit
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank merges its own independent problem of the
+headline size (replicas; no data-path collective) and the value is the total
+over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "merged Gelem/s and achieved HBM GB/s (% of GB300 peak), 1 GPU, vs CPU oracle"
+UNIT = "Gelem/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-strings", action="store_true", help="skip the string/FC workload")
+    ap.add_argument("--items", type=int, default=0, help="merge items per thread (7/11/15/23)")
+    ap.add_argument("--sweep", action="store_true", help="also time every items-per-thread setting")
+    ap.add_argument("--log2", type=int, default=26,
+                    help="headline inputs hold 2^log2 keys each (26 = the full workload; smaller "
+                         "values serve profiler captures)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment: ranks, peaks, clocks
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def wait_first(self, timeout=3.0):
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t_begin, t_end):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if t_begin <= ts <= t_end] or \
+                 [p for ts, p in rows if t_begin - 0.3 <= ts <= t_end + 0.3]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"],
+                    "samples": 0}
+        sm = [float(p[1]) for p in inside if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for p in inside if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for p in inside for k in range(4) if p[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for name in ("merge.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "lsm_replacement_merge_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        ent = data[kernel_key]
+        if ent.get("source_digest") != kernel_source_digest():
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle as it stands, on bounded samples
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    mi = synth.merge_u64()
+    m, n = len(mi.A), len(mi.B)
+    # calibrate, then size each step so that warmup + steps stay near 90 s
+    x = 1 << 20
+    t0 = time.perf_counter()
+    oracle.merge(mi.A[:x], mi.B[:x], mi.Apay[:x], mi.Bpay[:x])
+    rate = 2 * x / max(time.perf_counter() - t0, 1e-6)
+    budget = 90.0 / max(args.steps + args.warmup, 1)
+    half = int(min(m, max(1 << 16, rate * budget / 2)))
+    times = []
+    for s in range(args.warmup + args.steps):
+        off = (s * 7919 * 64) % max(m - half + 1, 1)
+        a, b = mi.A[off:off + half], mi.B[off:off + half]
+        pa, pb = mi.Apay[off:off + half], mi.Bpay[off:off + half]
+        t0 = time.perf_counter()
+        oracle.merge(a, b, pa, pb)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    elems = 2 * half * len(times)
+    value = elems / total / 1e9
+    sample = ("two-pointer oracle merge of %d + %d contiguous elements per step (slices of the "
+              "2^26 + 2^26 uint64 + uint32-payload workload)" % (half, half))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u64+u32", "data": "synthetic",
+        "config": headline_config(m, n, 0),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def headline_config(m, n, items):
+    return {"workload": "stable merge, sorted uint64 keys with uint32 payload, m = n = 2^%d"
+                        % (m.bit_length() - 1),
+            "m": m, "n": n, "key": "u64", "payload": "u32", "items_per_thread": items,
+            "tile": 256 * items if items else None,
+            "l2": "inputs and outputs (3 GiB) exceed the 129 MB L2; no flush needed",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world, rank, local = dist_env()
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    import lsm_replacement_merge_gb300 as lsm
+    lsm.lib()
+    if args.items:
+        lsm.tune_merge_items(lsm.LSM_KEY_U64, args.items)
+    items = int(args.items or 15)
+    peak, peak_kind = hbm_peak()
+
+    # ---------------- headline: 2^26 + 2^26 uint64 merge with payload ----------------
+    mi = synth.merge_u64(seed=2 + rank, m=1 << args.log2, n=1 << args.log2)
+    m, n = len(mi.A), len(mi.B)
+    A = torch.from_numpy(mi.A).to(dev)
+    B = torch.from_numpy(mi.B).to(dev)
+    Ap = torch.from_numpy(mi.Apay).to(dev)
+    Bp = torch.from_numpy(mi.Bpay).to(dev)
+    out_k = torch.empty(m + n, dtype=torch.uint64, device=dev)
+    out_p = torch.empty(m + n, dtype=torch.uint32, device=dev)
+    ws = lsm.workspace(lsm.LSM_OP_MERGE_STABLE, m, n, dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lsm.merge_stable(A, B, Ap, Bp, out_keys=out_k, out_pay=out_p, ws=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local).start()
+    # keep the GPU busy until the sampler has produced its first sample
+    t_end_warm = time.time() + 3.0
+    while not sampler.lines and time.time() < t_end_warm:
+        step()
+        torch.cuda.synchronize()
+    K = args.steps
+    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for e in k_start + k_stop:
+        e.record(stream)  # create the CUDA events before the timed region
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    ev0.record(stream)
+    for s in range(K):
+        lsm.set_profile_events(k_start[s], k_stop[s])
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if pg:
+        pg.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_begin, t_end)
+    step_ms = ev0.elapsed_time(ev1) / K
+    kern_ms = statistics.mean(k_start[s].elapsed_time(k_stop[s]) for s in range(K))
+    if pg:
+        t = torch.tensor([step_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * (m + n) / (step_ms * 1e-3) / 1e9
+    alg_bytes = (m + n) * (8 + 4) * 2
+    achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("merge_tile_kernel<u64,payload,256,%d>" % items)
+
+    # sanity: the timed output is the merge (spot-check against a numpy merge of samples)
+    stride = max((m + n) // 4096, 1)
+    got = out_k.view(torch.int64)[::stride].cpu().numpy().view(np.uint64)
+    ref = np.sort(np.concatenate([mi.A, mi.B]))[::stride]
+    assert np.array_equal(got, ref), "timed merge output differs from the sorted inputs"
+
+    # ---------------- e2e: pinned host buffers through the public API -------------------
+    e2e = None
+    if rank == 0 or world > 1:
+        hA = torch.from_numpy(mi.A).pin_memory()
+        hB = torch.from_numpy(mi.B).pin_memory()
+        hAp = torch.from_numpy(mi.Apay).pin_memory()
+        hBp = torch.from_numpy(mi.Bpay).pin_memory()
+        hK = torch.empty(m + n, dtype=torch.uint64).pin_memory()
+        hP = torch.empty(m + n, dtype=torch.uint32).pin_memory()
+        dA, dB = torch.empty_like(A), torch.empty_like(B)
+        dAp, dBp = torch.empty_like(Ap), torch.empty_like(Bp)
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dAp.copy_(hAp, non_blocking=True)
+            dBp.copy_(hBp, non_blocking=True)
+            lsm.merge_stable(dA, dB, dAp, dBp, out_keys=out_k, out_pay=out_p, ws=ws)
+            hK.copy_(out_k, non_blocking=True)
+            hP.copy_(out_p, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        E = max(3, min(K, 10))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(E):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / E
+        assert np.array_equal(hK.view(torch.int64).numpy().view(np.uint64)[::stride], ref)
+        e2e = {"value": world * (m + n) / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": (m + n) * 12, "d2h_bytes_per_step": (m + n) * 12,
+               "ms_per_step": e2e_ms, "steps": E}
+        del hA, hB, hAp, hBp, hK, hP, dA, dB, dAp, dBp
+
+    # ---------------- CPU baseline: the oracle on the host cores (rank 0) ---------------
+    cpu = None
+    if rank == 0:
+        import oracle
+        reps, t_cpu = 0, 0.0
+        while reps < 1 or (t_cpu < 3.0 and reps < 10):
+            t0 = time.perf_counter()
+            oracle.merge(mi.A, mi.B, mi.Apay, mi.Bpay)
+            t_cpu += time.perf_counter() - t0
+            reps += 1
+        cpu = {"value": reps * (m + n) / t_cpu / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "the whole 2^26 + 2^26 merge with payload, %d run(s)" % reps}
+
+    sweep = None
+    if args.sweep and rank == 0:
+        sweep = {}
+        for e in (7, 11, 15, 23):
+            lsm.tune_merge_items(lsm.LSM_KEY_U64, e)
+            for _ in range(3):
+                step()
+            s0 = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
+            s1 = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
+            for e in s0 + s1:
+                e.record(stream)
+            for s in range(50):
+                lsm.set_profile_events(s0[s], s1[s])
+                step()
+            torch.cuda.synchronize()
+            kms = statistics.mean(s0[s].elapsed_time(s1[s]) for s in range(50))
+            sweep[str(e)] = {"kernel_ms": kms, "gbs": alg_bytes / (kms * 1e-3) / 1e9}
+        lsm.tune_merge_items(lsm.LSM_KEY_U64, items)
+
+    del A, B, Ap, Bp, out_k, out_p, ws
+    torch.cuda.empty_cache()
+
+    workloads = {}
+    if not args.no_extra and rank == 0:
+        workloads = extra_workloads(lsm, torch, dev, peak, args)
+
+    launches = 2 * K
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u64+u32", "data": "synthetic",
+        "config": headline_config(m, n, items),
+        "roofline": {"bound": "hbm", "kernel": "merge_tile_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kern_ms,
+                     "frac_of_8TBs_nominal": achieved / 8000.0},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "workloads": workloads,
+    }
+    if sweep:
+        line["items_sweep"] = sweep
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the other pipelines
+# ---------------------------------------------------------------------------
+class Flusher:
+    """Writes a buffer larger than L2 between timed iterations."""
+
+    def __init__(self, torch, dev):
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_pipeline(torch, stages, steps, flush, warmup=3):
+    """stages: list of (name, fn). Returns (mean ms per step, {name: mean kernel ms})."""
+    import lsm_replacement_merge_gb300 as lsm
+    for _ in range(warmup):
+        for _, fn in stages:
+            fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    tot, per = [], {name: [] for name, _ in stages}
+    for _ in range(steps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        ks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in stages]
+        for a, b in ks:
+            a.record(stream)
+            b.record(stream)
+        e0.record(stream)
+        for (name, fn), (a, b) in zip(stages, ks):
+            lsm.set_profile_events(a, b)
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tot.append(e0.elapsed_time(e1))
+        for (name, _), (a, b) in zip(stages, ks):
+            per[name].append(a.elapsed_time(b))
+    return statistics.mean(tot), {k: statistics.mean(v) for k, v in per.items()}
+
+
+def extra_workloads(lsm, torch, dev, peak, args):
+    out = {}
+    flush = Flusher(torch, dev)
+    steps = max(5, min(args.steps, 30))
+
+    # int32 4096 + 4096 with payload
+    mi = synth.merge_i32()
+    A, B = torch.from_numpy(mi.A).to(dev), torch.from_numpy(mi.B).to(dev)
+    Ap, Bp = torch.from_numpy(mi.Apay).to(dev), torch.from_numpy(mi.Bpay).to(dev)
+    ok = torch.empty(8192, dtype=torch.int32, device=dev)
+    op = torch.empty(8192, dtype=torch.uint32, device=dev)
+    ws = lsm.workspace(lsm.LSM_OP_MERGE_STABLE, 4096, 4096, dev, lsm.LSM_KEY_I32)
+    ms, per = time_pipeline(torch, [("merge_stable", lambda: lsm.merge_stable(
+        A, B, Ap, Bp, out_keys=ok, out_pay=op, ws=ws))], max(steps, 20), lambda: None)
+    out["merge_i32_4096"] = {"ms_per_step": ms, "gelem_s": 8192 / (ms * 1e-3) / 1e9,
+                             "kernel_ms": per, "note": "latency-bound (two launches)"}
+
+    # uint64 replacement pipelines
+    for name, gen in (("replace_u64_12M_4M", synth.replace_u64),
+                      ("replace_skewed_2pow24_65536", synth.replace_skewed)):
+        ri = gen()
+        m, n = len(ri.A), len(ri.B)
+        A, B = torch.from_numpy(ri.A).to(dev), torch.from_numpy(ri.B).to(dev)
+        C = torch.empty((m + 31) // 32, dtype=torch.uint32, device=dev)
+        lb = torch.empty(n, dtype=torch.uint32, device=dev)
+        dir_ = torch.empty(3 * (m // 512 + 1), dtype=torch.uint32, device=dev)
+        tot = torch.empty(1, dtype=torch.int64, device=dev)
+        refs = torch.empty(m + n, dtype=torch.uint32, device=dev)
+        oa = torch.empty(m, dtype=torch.uint32, device=dev)
+        ob = torch.empty(n, dtype=torch.uint32, device=dev)
+        cnt = torch.empty(1, dtype=torch.int64, device=dev)
+        w1 = lsm.workspace(lsm.LSM_OP_COLLISION_MARK, m, n, dev)
+        w2 = lsm.workspace(lsm.LSM_OP_RANK_BUILD, m, 0, dev)
+        w3 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
+        stages = [("collision_mark", lambda: lsm.collision_mark(A, B, C, lb, w1)),
+                  ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
+                  ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
+                      m, n, C, dir_, lb, refs, oa, ob, cnt, w3))]
+        ms, per = time_pipeline(torch, stages, steps, flush)
+        N = int(cnt.item())
+        alg = (8 * (m + n)                      # read keys
+               + 4 * ((m + 31) // 32)           # write C
+               + 12 * (m // 512 + 1)            # write dir
+               + 4 * N + 4 * (m + n))           # write refs, ord_A, ord_B
+        out[name] = {"m": m, "n": n, "survivors": N, "ms_per_step": ms,
+                     "gelem_s": (m + n) / (ms * 1e-3) / 1e9,
+                     "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
+                     "frac": alg / (ms * 1e-3) / 1e9 / peak,
+                     "frac_of_8TBs_nominal": alg / (ms * 1e-3) / 1e9 / 8000.0,
+                     "kernel_ms": per, "gpu_launches_per_step": 6,
+                     "l2": "flushed (256 MiB write) before every step"}
+        del A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w1, w2, w3
+        torch.cuda.empty_cache()
+
+    if args.no_strings:
+        return out
+    s = synth.strings()
+    Ak = lsm.Bytes.from_numpy(s.A.key_arena, s.A.key_off, dev)
+    Bk = lsm.Bytes.from_numpy(s.B.key_arena, s.B.key_off, dev)
+    fc = lsm.FcInput(Ak, lsm.Bytes.from_numpy(s.A.val_arena, s.A.val_off, dev),
+                     torch.from_numpy(s.A.tomb).to(dev), Bk,
+                     lsm.Bytes.from_numpy(s.B.val_arena, s.B.val_off, dev),
+                     torch.from_numpy(s.B.tomb).to(dev))
+    m, n = Ak.count, Bk.count
+    C = torch.empty((m + 31) // 32, dtype=torch.uint32, device=dev)
+    lb = torch.empty(n, dtype=torch.uint32, device=dev)
+    dir_ = torch.empty(3 * (m // 512 + 1), dtype=torch.uint32, device=dev)
+    tot = torch.empty(1, dtype=torch.int64, device=dev)
+    refs = torch.empty(m + n, dtype=torch.uint32, device=dev)
+    oa = torch.empty(m, dtype=torch.uint32, device=dev)
+    ob = torch.empty(n, dtype=torch.uint32, device=dev)
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    w1 = lsm.workspace(lsm.LSM_OP_COLLISION_MARK_STR, m, n, dev)
+    w2 = lsm.workspace(lsm.LSM_OP_RANK_BUILD, m, 0, dev)
+    w3 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
+    lsm.collision_mark_str(Ak, Bk, C, lb, w1)
+    lsm.rank_build(C, m, dir_, tot, w2)
+    lsm.replacement_merge_compact(m, n, C, dir_, lb, refs, oa, ob, cnt, w3)
+    N = int(cnt.item())
+    lcp = torch.empty(N, dtype=torch.uint32, device=dev)
+    ctrl = torch.empty(N, dtype=torch.uint32, device=dev)
+    rec = torch.empty(N, dtype=torch.uint32, device=dev)
+    off = torch.empty(N + 1, dtype=torch.uint64, device=dev)
+    w4 = lsm.workspace(lsm.LSM_OP_FC_LENGTHS_SCAN, N, 0, dev)
+    lsm.fc_lengths_scan(fc, refs, N, lcp, ctrl, rec, off, w4)
+    total_bits = int(off[N:].cpu().numpy()[0])
+    nwords = (total_bits + 31) // 32
+    payload = torch.empty(max(nwords, 4), dtype=torch.uint32, device=dev)
+    stages = [("collision_mark_str", lambda: lsm.collision_mark_str(Ak, Bk, C, lb, w1)),
+              ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
+              ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
+                  m, n, C, dir_, lb, refs, oa, ob, cnt, w3)),
+              ("fc_lengths_scan", lambda: lsm.fc_lengths_scan(fc, refs, N, lcp, ctrl, rec, off, w4)),
+              ("fc_emit", lambda: lsm.fc_emit(fc, refs, N, lcp, ctrl, off, nwords, payload))]
+    ms, per = time_pipeline(torch, stages, steps, flush)
+    key_bytes = len(s.A.key_arena) + len(s.B.key_arena) + 8 * (m + n + 2)
+    val_bytes = len(s.A.val_arena) + len(s.B.val_arena) + 8 * (m + n + 2) + 4 * (len(s.A.tomb) + len(s.B.tomb))
+    alg = (key_bytes + val_bytes                      # keys and values read once
+           + 4 * ((m + 31) // 32) + 12 * (m // 512 + 1) + 4 * N + 4 * (m + n)  # C, dir, refs, ords
+           + 12 * N + 8 * (N + 1) + 4 * nwords)      # lcp, ctrl, rec_bits, bit_off, payload
+    out["strings_fc_4M_4M"] = {"m": m, "n": n, "survivors": N, "payload_bits": total_bits,
+                               "ms_per_step": ms, "gelem_s": (m + n) / (ms * 1e-3) / 1e9,
+                               "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
+                               "frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": per,
+                               "gpu_launches_per_step": 9,
+                               "l2": "flushed (256 MiB write) before every step"}
+    return out
+
+
+if __name__ == "__main__":
+    main()

@@ -231,7 +231,8 @@ LSM_API int lsm_fc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs, in
  * floor(log2(x+1)) zero bits followed by x+1 in binary. Stream bit t is bit
  * 31 - t%32 of payload[t/32] (MSB first). All nwords words are written;
  * bits past bit_off[N] are zero. nwords must be >= ceil(bit_off[N] / 32)
- * (the host reads bit_off[N] once to size the payload). */
+ * (the host reads bit_off[N] once to size the payload); payload: device
+ * uint32[nwords], 16-byte aligned. */
 LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
                         const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                         uint32_t *payload, int64_t nwords, void *stream);
@@ -242,6 +243,15 @@ LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
  * setting, read at each call; the default is 15. This is the slice-size knob
  * of [MP] "Measuring it against one thread" and "Results". */
 LSM_API int lsm_tune_merge_items(int key_type, int items_per_thread);
+
+/* Profiling hook: the next call that launches a tile kernel (merge_stable,
+ * collision_mark, collision_mark_str, rank_build, replacement_merge_compact,
+ * fc_lengths_scan, fc_emit) records the CUDA event `start_event` on its
+ * stream just before its main kernel and `stop_event` just after it (for
+ * rank_build: around both of its kernels), then forgets both events.
+ * Process-wide, one-shot; pass NULL, NULL to cancel. The events are
+ * cudaEvent_t handles owned by the caller. */
+LSM_API int lsm_set_profile_events(void *start_event, void *stop_event);
 
 /* ---- test hook ------------------------------------------------------------ */
 /* Launches one block that waits, with the same bounded wait the kernels

@@ -86,6 +86,7 @@ def lib():
                 "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
                 "lsm_tune_merge_items": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
+                "lsm_set_profile_events": ([P, P], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -156,6 +157,17 @@ def get_device_status(reset: bool = False, stream=None) -> int:
     _check("lsm_get_device_status",
            lib().lsm_get_device_status(ctypes.byref(st), int(bool(reset)), _stream(stream)))
     return st.value
+
+
+def set_profile_events(start=None, stop=None) -> None:
+    """Time the next call's main kernel with two torch.cuda.Event objects
+    (created with enable_timing=True); see lsm_set_profile_events."""
+    for ev in (start, stop):
+        if ev is not None and not ev.cuda_event:
+            ev.record()  # torch creates the CUDA event lazily, at its first record
+    sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
+    ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+    _check("lsm_set_profile_events", lib().lsm_set_profile_events(sp, ep))
 
 
 def tune_merge_items(key_type: int, items_per_thread: int) -> None:

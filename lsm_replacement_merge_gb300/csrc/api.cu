@@ -57,6 +57,9 @@ __global__ void timeout_probe_kernel(const volatile int32_t *never_set, int64_t 
 
 __device__ int32_t g_never_set_flag;
 
+std::mutex g_prof_mu;
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
 // ---- workspace carving ----------------------------------------------------------
 struct Carver {
   uint8_t *p;
@@ -301,8 +304,17 @@ LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
   if (N < 0 || nwords < 0 || !bit_off || (N && (!refs || !lcp || !ctrl)) || (nwords && !payload))
     return LSM_ERR_ARG;
   if (N > kMax31 || N > in->m + in->n || nwords > (int64_t(1) << 40)) return LSM_ERR_OVERFLOW;
+  if (payload && !aligned16(payload)) return LSM_ERR_ALIGN;
   return cuda_status(launch_fc_emit(*in, refs, N, lcp, ctrl, bit_off, payload, nwords,
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_set_profile_events(void *start_event, void *stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return LSM_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return LSM_OK;
 }
 
 LSM_API int lsm_tune_merge_items(int key_type, int items_per_thread) {
@@ -318,6 +330,22 @@ LSM_API int lsm_debug_timeout_probe(int64_t limit_ns, void *stream) {
 }  // extern "C"
 
 namespace lsm {
+void profile_before(cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof_start) {
+    cudaEventRecord(g_prof_start, s);
+    g_prof_start = nullptr;
+  }
+}
+
+void profile_after(cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof_stop && !g_prof_start) {
+    cudaEventRecord(g_prof_stop, s);
+    g_prof_stop = nullptr;
+  }
+}
+
 cudaError_t launch_timeout_probe(int64_t limit_ns, int32_t *status, cudaStream_t s) {
   void *flag = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&flag, g_never_set_flag);

@@ -413,9 +413,11 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
   err = cudaFuncSetAttribute(fc_lengths_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(FcLayout::kBytes));
   if (err != cudaSuccess) return err;
+  profile_before(s);
   fc_lengths_kernel<<<static_cast<unsigned>(tiles > 0 ? tiles : 1), kFcThreads, FcLayout::kBytes, s>>>(
       make_source(in.keyA, in.valA, in.tombA), make_source(in.keyB, in.valB, in.tombB), refs, N, lcp,
       ctrl, rec_bits, bit_off, state, counter, status);
+  profile_after(s);
   return cudaGetLastError();
 }
 
@@ -424,9 +426,11 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
                            uint32_t *payload, int64_t nwords, int32_t * /*status*/, cudaStream_t s) {
   if (nwords == 0) return cudaSuccess;
   const int64_t runs = (nwords + kEmitRun - 1) / kEmitRun;
+  profile_before(s);
   fc_emit_kernel<<<static_cast<unsigned>(runs), kEmitThreads, 0, s>>>(
       make_source(in.keyA, in.valA, in.tombA), make_source(in.keyB, in.valB, in.tombB), refs, N, lcp,
       ctrl, bit_off, payload, nwords);
+  profile_after(s);
   return cudaGetLastError();
 }
 

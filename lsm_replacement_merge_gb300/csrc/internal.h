@@ -67,5 +67,9 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
 
 // --- api.cu ---
 cudaError_t launch_timeout_probe(int64_t limit_ns, int32_t *status, cudaStream_t s);
+// Profiling hook (lsm_set_profile_events): record the pending start/stop
+// events around a call's main kernel. No-ops when none are pending.
+void profile_before(cudaStream_t s);
+void profile_after(cudaStream_t s);
 
 }  // namespace lsm

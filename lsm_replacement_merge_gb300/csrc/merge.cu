@@ -193,8 +193,10 @@ cudaError_t launch_merge_tiles(const K *A, const uint32_t *Apay, int64_t m, cons
                                          static_cast<int>(L::kBytes));
   if (err != cudaSuccess) return err;
   const int64_t G = (m + n + L::D - 1) / L::D;
+  profile_before(s);
   kern<<<static_cast<unsigned>(G), kMergeThreads, L::kBytes, s>>>(A, Apay, m, B, Bpay, n, part_i,
                                                                   out, out_pay, status);
+  profile_after(s);
   return cudaGetLastError();
 }
 

@@ -449,7 +449,9 @@ cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *
   auto kern = collision_mark_kernel<kMarkThreads, kMarkItems>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::kBytes));
   if (err != cudaSuccess) return err;
+  profile_before(s);
   kern<<<static_cast<unsigned>(G), kMarkThreads, L::kBytes, s>>>(A, m, B, n, part_i, C, lb_B, status);
+  profile_after(s);
   return cudaGetLastError();
 }
 
@@ -458,10 +460,12 @@ int64_t rank_build_ctas(int64_t m) { return (m / 512 + 1 + kRankThreads - 1) / k
 cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
                               uint32_t *cta_totals, cudaStream_t s) {
   const int64_t ctas = rank_build_ctas(m);
+  profile_before(s);
   rank_count_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(C, m, cta_totals);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   rank_finish_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(C, m, cta_totals, dir, d_total);
+  profile_after(s);
   return cudaGetLastError();
 }
 
@@ -485,8 +489,10 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::kBytes));
   if (err != cudaSuccess) return err;
   // At least one CTA, so that d_count is written for two empty inputs.
+  profile_before(s);
   kern<<<static_cast<unsigned>(G > 0 ? G : 1), kCompactThreads, L::kBytes, s>>>(
       m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B, d_count, status);
+  profile_after(s);
   return cudaGetLastError();
 }
 

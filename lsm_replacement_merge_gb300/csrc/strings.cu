@@ -128,8 +128,10 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
       StrAFirst{A, B}, m, n, D, G, part_i, C, nwords);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || G == 0) return err;
+  profile_before(s);
   collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>
       <<<static_cast<unsigned>(G), kMarkStrThreads, 0, s>>>(A, m, B, n, part_i, C, lb_B);
+  profile_after(s);
   return cudaGetLastError();
 }
 
