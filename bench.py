@@ -169,6 +169,23 @@ def ncu_traffic(kernel_key):
         return None
 
 
+def slowest_rank_ms(step_ms, dist=None, device=None):
+    """Max of a per-rank step time over all ranks (the job is as fast as its
+    slowest rank). With no process group, the value itself."""
+    if dist is None:
+        return float(step_ms)
+    import torch
+    t = torch.tensor([float(step_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, elems_per_rank, step_ms):
+    """Whole-job Gelem/s: every rank merges its own problem of elems_per_rank
+    elements per step (replicas, weak scaling)."""
+    return world * elems_per_rank / (step_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------------------
 # the reference arm: the CPU oracle as it stands, on bounded samples
 # ---------------------------------------------------------------------------
@@ -295,11 +312,8 @@ def main():
     clocks = sampler.summary(t_begin, t_end)
     step_ms = ev0.elapsed_time(ev1) / K
     kern_ms = statistics.mean(k_start[s].elapsed_time(k_stop[s]) for s in range(K))
-    if pg:
-        t = torch.tensor([step_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * (m + n) / (step_ms * 1e-3) / 1e9
+    step_ms = slowest_rank_ms(step_ms, pg, dev)
+    value = job_throughput(world, m + n, step_ms)
     alg_bytes = (m + n) * (8 + 4) * 2
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
     traffic = ncu_traffic("merge_tile_kernel<u64,payload,256,%d>" % items)
