@@ -177,6 +177,27 @@ LSM_API int lsm_collision_mark_str(const lsm_bytes *A, int64_t m, const lsm_byte
 LSM_API int lsm_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
                            void *ws, size_t ws_bytes, void *stream);
 
+/* Allocation-free variant of lsm_rank_build, for callers that cannot call
+ * cudaMalloc or hand the library a workspace: code on a latency-critical path
+ * where a device allocation (which may block and synchronize the device) is
+ * not allowed after start-up, or a plug-in whose host program owns every
+ * device buffer through its own pool. The pages have no counterpart; this is
+ * a property of this library's interface, not of the method.
+ * Same arguments and results as lsm_rank_build without the workspace: the
+ * per-CTA totals live in a 16 KB static device array inside the library, so
+ * the call allocates nothing. Limits and rules:
+ *   - m <= 2^29 - 1 (536,870,911 bit positions); larger m returns
+ *     LSM_ERR_OVERFLOW before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array: calls that may overlap on
+ *     the GPU (different streams, or different host threads) race and must be
+ *     ordered by the caller. Each call rewrites every entry it reads, so the
+ *     contents left by an earlier call never matter. */
+LSM_API int lsm_rank_build_noalloc(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
+                                   void *stream);
+
 /* Rank queries: out[t] = R(pos[t]) for pos[t] in [0, m], using the directory,
  * at most one preceding 32-bit word and the masked current word ([CB]
  * "Temporary rank layouts"). A position above m yields 0xFFFFFFFF and

@@ -87,6 +87,7 @@ def lib():
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
                 "lsm_tune_merge_items": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
                 "lsm_set_profile_events": ([P, P], ctypes.c_int),
+                "lsm_rank_build_noalloc": ([P, I, P, P, P], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -277,6 +278,22 @@ def rank_build(C, m: int, dir_=None, d_total=None, ws=None, stream=None):
     _check("lsm_rank_build",
            lib().lsm_rank_build(_ptr(C) if m else None, m, _ptr(dir_), _ptr(d_total), _ptr(ws),
                                 ws.numel(), _stream(stream)))
+    return dir_, d_total
+
+
+def rank_build_noalloc(C, m: int, dir_=None, d_total=None, stream=None):
+    """lsm_rank_build_noalloc: rank_build whose scratch is a static device
+    array inside the library (m <= 2^29 - 1; calls on one device must not
+    overlap). Outputs not passed in are allocated here by torch; the C entry
+    point itself allocates nothing."""
+    dev = C.device
+    if dir_ is None:
+        dir_ = _empty(3 * (m // 512 + 1), torch.uint32, dev)
+    if d_total is None:
+        d_total = _empty(1, torch.int64, dev)
+    _check("lsm_rank_build_noalloc",
+           lib().lsm_rank_build_noalloc(_ptr(C) if m else None, m, _ptr(dir_), _ptr(d_total),
+                                        _stream(stream)))
     return dir_, d_total
 
 

@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -469,6 +470,39 @@ cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64
   return cudaGetLastError();
 }
 
+// ---- allocation-free rank_build --------------------------------------------------
+// Scratch for lsm_rank_build_noalloc: the per-CTA popcount totals live in this
+// file-scope device array instead of a caller workspace. 4096 CTAs of 256
+// 512-bit blocks cover m <= 2^29 - 1 bit positions; the array is 16 KB and every
+// device that loads the library keeps it until the process exits. The count
+// kernel overwrites every entry the finish kernel reads, so nothing in it has
+// to start at zero.
+constexpr int64_t kNoAllocRankCtas = 4096;
+constexpr int64_t kNoAllocRankMaxM = (int64_t(1) << 29) - 1;
+static __device__ __align__(256) uint32_t g_rank_noalloc_scratch[kNoAllocRankCtas];
+
+namespace {
+std::mutex g_noalloc_mu;
+uint32_t *g_noalloc_ptr[64];
+
+// Device address of the scratch array on the current device. In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+int noalloc_scratch(uint32_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LSM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    uint32_t *p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_rank_noalloc_scratch) != cudaSuccess)
+      return LSM_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return LSM_OK;
+}
+}  // namespace
+
 cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                               const uint32_t *pos, int64_t q, uint32_t *out, int32_t *status,
                               cudaStream_t s) {
@@ -497,3 +531,16 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
 }
 
 }  // namespace lsm
+
+// Allocation-free variant of lsm_rank_build (declared in include/lsmmerge.h).
+extern "C" LSM_API int lsm_rank_build_noalloc(const uint32_t *C, int64_t m, uint32_t *dir,
+                                              int64_t *d_total, void *stream) {
+  using namespace lsm;
+  if (m < 0 || !dir || !d_total || (m && !C)) return LSM_ERR_ARG;
+  if (m > kNoAllocRankMaxM) return LSM_ERR_OVERFLOW;
+  if (C && (reinterpret_cast<uintptr_t>(C) & 15u)) return LSM_ERR_ALIGN;
+  uint32_t *scratch = nullptr;
+  if (int r = noalloc_scratch(&scratch)) return r;
+  const cudaError_t e = launch_rank_build(C, m, dir, d_total, scratch, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LSM_OK : LSM_ERR_CUDA;
+}
