@@ -56,7 +56,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-strings", action="store_true", help="skip the string/FC workload")
-    ap.add_argument("--items", type=int, default=0, help="merge items per thread (7/11/15/23)")
+    ap.add_argument("--merge-config", default="11,2,1",
+                    help="merge tile configuration: items per thread, stages, output tiles")
     ap.add_argument("--sweep", action="store_true", help="also time every items-per-thread setting")
     ap.add_argument("--log2", type=int, default=26,
                     help="headline inputs hold 2^log2 keys each (26 = the full workload; smaller "
@@ -223,7 +224,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u64+u32", "data": "synthetic",
-        "config": headline_config(m, n, 0),
+        "config": headline_config(m, n, None),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -231,11 +232,13 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def headline_config(m, n, items):
+def headline_config(m, n, mcfg):
     return {"workload": "stable merge, sorted uint64 keys with uint32 payload, m = n = 2^%d"
                         % (m.bit_length() - 1),
-            "m": m, "n": n, "key": "u64", "payload": "u32", "items_per_thread": items,
-            "tile": 256 * items if items else None,
+            "m": m, "n": n, "key": "u64", "payload": "u32",
+            "merge_config": {"items_per_thread": mcfg[0], "stages": mcfg[1], "out_tiles": mcfg[2]}
+            if mcfg else None,
+            "tile": 256 * mcfg[0] if mcfg else None,
             "l2": "inputs and outputs (3 GiB) exceed the 129 MB L2; no flush needed",
             "parallelism": "replicas"}
 
@@ -259,9 +262,9 @@ def main():
         pg = dist
     import lsm_replacement_merge_gb300 as lsm
     lsm.lib()
-    if args.items:
-        lsm.tune_merge_items(lsm.LSM_KEY_U64, args.items)
-    items = int(args.items or 15)
+    mcfg = tuple(int(x) for x in args.merge_config.split(","))
+    lsm.tune_merge(lsm.LSM_KEY_U64, *mcfg)
+    items = mcfg[0]
     peak, peak_kind = hbm_peak()
 
     # ---------------- headline: 2^26 + 2^26 uint64 merge with payload ----------------
@@ -316,7 +319,20 @@ def main():
     value = job_throughput(world, m + n, step_ms)
     alg_bytes = (m + n) * (8 + 4) * 2
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("merge_tile_kernel<u64,payload,256,%d>" % items)
+    traffic = ncu_traffic("merge_tile_kernel<u64,payload,%d,%d,%d>" % mcfg)
+
+    # the partition step alone (the same co-ranks the merge computes first)
+    D = 256 * mcfg[0]
+    part_out = torch.empty(2 * ((m + n + D - 1) // D + 1), dtype=torch.int64, device=dev)
+    p0 = [torch.cuda.Event(enable_timing=True) for _ in range(20)]
+    p1 = [torch.cuda.Event(enable_timing=True) for _ in range(20)]
+    for q in range(20):
+        p0[q].record(stream)
+        lsm.merge_path_partition(A, B, D, out_ij=part_out)
+        p1[q].record(stream)
+    torch.cuda.synchronize()
+    partition_ms = statistics.mean(p0[q].elapsed_time(p1[q]) for q in range(5, 20))
+    del part_out
 
     # sanity: the timed output is the merge (spot-check against a numpy merge of samples)
     stride = max((m + n) // 4096, 1)
@@ -379,21 +395,21 @@ def main():
     sweep = None
     if args.sweep and rank == 0:
         sweep = {}
-        for e in (7, 11, 15, 23):
-            lsm.tune_merge_items(lsm.LSM_KEY_U64, e)
+        for cfg_e in lsm.MERGE_CONFIGS:
+            lsm.tune_merge(lsm.LSM_KEY_U64, *cfg_e)
             for _ in range(3):
                 step()
             s0 = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
             s1 = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
-            for e in s0 + s1:
-                e.record(stream)
-            for s in range(50):
-                lsm.set_profile_events(s0[s], s1[s])
+            for ev in s0 + s1:
+                ev.record(stream)
+            for q in range(50):
+                lsm.set_profile_events(s0[q], s1[q])
                 step()
             torch.cuda.synchronize()
-            kms = statistics.mean(s0[s].elapsed_time(s1[s]) for s in range(50))
-            sweep[str(e)] = {"kernel_ms": kms, "gbs": alg_bytes / (kms * 1e-3) / 1e9}
-        lsm.tune_merge_items(lsm.LSM_KEY_U64, items)
+            kms = statistics.mean(s0[q].elapsed_time(s1[q]) for q in range(50))
+            sweep["%d,%d,%d" % cfg_e] = {"kernel_ms": kms, "gbs": alg_bytes / (kms * 1e-3) / 1e9}
+        lsm.tune_merge(lsm.LSM_KEY_U64, *mcfg)
 
     del A, B, Ap, Bp, out_k, out_p, ws
     torch.cuda.empty_cache()
@@ -407,11 +423,12 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u64+u32", "data": "synthetic",
-        "config": headline_config(m, n, items),
+        "config": headline_config(m, n, mcfg),
         "roofline": {"bound": "hbm", "kernel": "merge_tile_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kern_ms,
+                     "partition_ms": partition_ms,
                      "frac_of_8TBs_nominal": achieved / 8000.0},
         "cpu_baseline": cpu,
         "e2e": e2e,

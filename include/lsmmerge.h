@@ -259,11 +259,14 @@ LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
                         uint32_t *payload, int64_t nwords, void *stream);
 
 /* ---- tuning ----------------------------------------------------------------- */
-/* Sets how many outputs each thread of lsm_merge_stable produces for the
- * given key type (7, 11, 15 or 23; the tile is 256 times that). Process-wide
- * setting, read at each call; the default is 15. This is the slice-size knob
- * of [MP] "Measuring it against one thread" and "Results". */
-LSM_API int lsm_tune_merge_items(int key_type, int items_per_thread);
+/* Selects the tile configuration of lsm_merge_stable for a key type:
+ * items_per_thread E (a tile is 256 E outputs), `stages` input tiles kept in
+ * flight per CTA, `out_tiles` output tiles (1 or 2). Compiled configurations
+ * (E, stages, out_tiles): (5,2,1) (7,2,1) (11,2,1) (15,2,1) (7,4,2) (11,3,2)
+ * (15,2,2) (7,3,1); any other returns LSM_ERR_ARG. Process-wide, read at each
+ * call; the default is (11,2,1). E is the slice-size knob of [MP] "Measuring
+ * it against one thread" and "Results". */
+LSM_API int lsm_tune_merge(int key_type, int items_per_thread, int stages, int out_tiles);
 
 /* Profiling hook: the next call that launches a tile kernel (merge_stable,
  * collision_mark, collision_mark_str, rank_build, replacement_merge_compact,

@@ -85,7 +85,7 @@ def lib():
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
-                "lsm_tune_merge_items": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
+                "lsm_tune_merge": ([ctypes.c_int] * 4, ctypes.c_int),
                 "lsm_set_profile_events": ([P, P], ctypes.c_int),
                 "lsm_rank_build_noalloc": ([P, I, P, P, P], ctypes.c_int),
             }
@@ -171,8 +171,13 @@ def set_profile_events(start=None, stop=None) -> None:
     _check("lsm_set_profile_events", lib().lsm_set_profile_events(sp, ep))
 
 
-def tune_merge_items(key_type: int, items_per_thread: int) -> None:
-    _check("lsm_tune_merge_items", lib().lsm_tune_merge_items(key_type, items_per_thread))
+MERGE_CONFIGS = ((5, 2, 1), (7, 2, 1), (11, 2, 1), (15, 2, 1), (7, 4, 2), (11, 3, 2), (15, 2, 2),
+                 (7, 3, 1))
+DEFAULT_MERGE_CONFIG = (11, 2, 1)
+
+
+def tune_merge(key_type: int, items_per_thread: int, stages: int, out_tiles: int) -> None:
+    _check("lsm_tune_merge", lib().lsm_tune_merge(key_type, items_per_thread, stages, out_tiles))
 
 
 def debug_timeout_probe(limit_ns: int, stream=None) -> None:

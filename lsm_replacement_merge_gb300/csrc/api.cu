@@ -317,8 +317,8 @@ LSM_API int lsm_set_profile_events(void *start_event, void *stop_event) {
   return LSM_OK;
 }
 
-LSM_API int lsm_tune_merge_items(int key_type, int items_per_thread) {
-  return set_merge_items_per_thread(key_type, items_per_thread);
+LSM_API int lsm_tune_merge(int key_type, int items_per_thread, int stages, int out_tiles) {
+  return set_merge_config(key_type, items_per_thread, stages, out_tiles);
 }
 
 LSM_API int lsm_debug_timeout_probe(int64_t limit_ns, void *stream) {

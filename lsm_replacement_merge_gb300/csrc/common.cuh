@@ -95,6 +95,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Waits until at most one committed bulk-store group still reads shared
+// memory (the most recent one may continue).
+__device__ __forceinline__ void bulk_wait_read_allow1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (a following bulk store reads them).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -126,6 +132,45 @@ __device__ __forceinline__ StagePlan stage_plan(int64_t s, int64_t c) {
   p.tail_from = ahi / SZ > s ? ahi / SZ : s;
   p.span = static_cast<int32_t>(p.lead + c);
   return p;
+}
+
+// Same, but the bulk copy runs up to the next 16-byte boundary past s + c
+// whenever that stays inside the array's first `limit` elements, so that a
+// span needs plain loads only at the very end of its array.
+template <int SZ>
+__device__ __forceinline__ StagePlan stage_plan_overfetch(int64_t s, int64_t c, int64_t limit) {
+  const int64_t lo = s * SZ, hi = (s + c) * SZ;
+  const int64_t alo = lo & ~int64_t(15);
+  const int64_t up = (hi + 15) & ~int64_t(15);
+  const int64_t ahi = up <= ((limit * SZ) & ~int64_t(15)) ? up : (hi & ~int64_t(15));
+  StagePlan p;
+  p.first = alo / SZ;
+  p.lead = static_cast<int32_t>(s - p.first);
+  p.bulk = static_cast<uint32_t>(ahi > alo ? ahi - alo : 0);
+  p.tail_from = ahi / SZ > s ? ahi / SZ : s;
+  p.span = static_cast<int32_t>(p.lead + c);
+  return p;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier over the first `nthreads` threads of the block (named barrier
+// `id`), returning whether any of them passed a true predicate.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <int SZ>
@@ -186,32 +231,19 @@ __device__ __forceinline__ V block_sum(V v, V *scratch) {
   return total;
 }
 
-// ---- warp-cooperative merge-path search ----------------------------------------
-// Finds, for one diagonal k, the co-rank i in [max(0, k-n), min(k, m)]: the
-// first i for which pred.too_small(i, k) is false, where too_small(i, k)
-// means "A_i precedes B_{k-i-1} in the merge" (so more A elements belong
-// before the diagonal). Each round the 32 lanes probe 32 evenly spaced
-// candidates and the ballot narrows the range about 33-fold, so a search
-// over 2^26 candidates takes six dependent rounds instead of 26.
+// ---- per-thread merge-path search -------------------------------------------------
+// The co-rank of diagonal k: the first i in [max(0, k-n), min(k, m)] for
+// which pred.too_small(i, k) is false, by plain bisection. One thread per
+// diagonal: every search touches two sectors per level, and tens of
+// thousands of searches in flight hide the dependent-load latency.
 template <class Pred>
-__device__ __forceinline__ int64_t warp_corank(const Pred &pred, int64_t k, int64_t m, int64_t n) {
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ int64_t thread_corank(const Pred &pred, int64_t k, int64_t m, int64_t n) {
   int64_t lo = k > n ? k - n : 0;
   int64_t hi = k < m ? k : m;
-  while (hi > lo) {
-    const int64_t span = hi - lo;
-    const bool last = span <= 32;
-    const int64_t p = last ? lo + lane : lo + ((int64_t)(lane + 1) * span) / 33;
-    const bool small = (p < hi) && pred.too_small(p, k);
-    const int t = __popc(__ballot_sync(0xffffffffu, small));
-    if (last) {
-      lo += t;
-      break;
-    }
-    const int64_t p_prev = t > 0 ? lo + ((int64_t)t * span) / 33 : lo - 1;
-    const int64_t p_next = t < 32 ? lo + ((int64_t)(t + 1) * span) / 33 : hi;
-    lo = p_prev + 1;
-    hi = p_next;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (pred.too_small(mid, k)) lo = mid + 1;
+    else hi = mid;
   }
   return lo;
 }

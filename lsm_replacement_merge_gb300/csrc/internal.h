@@ -20,10 +20,12 @@ constexpr int kCompactThreads = 256;
 constexpr int kRankThreads = 256;
 
 int merge_items_per_thread(int key_type);  // current setting (tunable)
-int set_merge_items_per_thread(int key_type, int e);  // returns LSM_OK or LSM_ERR_ARG
+// Selects the tile configuration (items per thread, input stages, output
+// tiles) of lsm_merge_stable; returns LSM_OK or LSM_ERR_ARG.
+int set_merge_config(int key_type, int items, int stages, int out_tiles);
 constexpr int kMarkItems = 15;
 constexpr int kCompactItems = 15;
-constexpr int64_t kMinMergeTile = kMergeThreads * 7;
+constexpr int64_t kMinMergeTile = kMergeThreads * 5;
 
 // --- merge.cu ---
 cudaError_t launch_partition_keys(int key_type, const void *A, int64_t m, const void *B, int64_t n,

@@ -7,18 +7,22 @@
 // listing, and "Go deeper") stages each block's spans in shared memory
 // before any thread searches; that is the design here:
 //
-//   1. partition_keys_kernel: one warp per tile boundary finds the co-rank
-//      of k_g = g * D with a 32-way probe per round (six rounds for 2^26).
-//   2. merge_tile_kernel: one CTA per tile of D = T * E outputs. Thread 0
-//      issues bulk copies of the tile's A and B spans (keys and payloads)
-//      into shared memory; each thread then bisects its own diagonal inside
-//      shared memory and walks E outputs into an output tile in shared
-//      memory; thread 0 writes the finished tile back with bulk stores.
-//      Global memory sees each input byte read once and each output byte
-//      written once, in 16-byte aligned bulk transfers.
+//   1. partition_keys_kernel: one thread per tile boundary bisects for the
+//      co-rank of k_g = g * D in global memory.
+//   2. merge_tile_kernel: a persistent, warp-specialized kernel that loops
+//      over tiles of D = 256 * E outputs. A producer warp keeps the bulk
+//      copies of the next tiles' A and B spans (keys and payloads) in flight
+//      through S shared-memory stages, each with a full and an empty
+//      mbarrier; eight merging warps take a stage, each thread bisects its
+//      own diagonal inside shared memory and walks E outputs into one of two
+//      output tiles, and thread 0 writes the tile back with a bulk store
+//      while the next tile merges. Global memory sees each input byte read
+//      once and each output byte written once, in 16-byte aligned bulk
+//      transfers.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -32,7 +36,9 @@ template <typename K>
 struct KeysAFirst {
   const K *A;
   const K *B;
-  __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const { return A[i] <= B[k - i - 1]; }
+  __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
+    return __ldg(A + i) <= __ldg(B + k - i - 1);
+  }
 };
 
 template <typename K>
@@ -41,189 +47,321 @@ __global__ void __launch_bounds__(256) partition_keys_kernel(const K *__restrict
                                                              int64_t D, int64_t G,
                                                              int64_t *__restrict__ out_i,
                                                              int64_t *__restrict__ out_ij) {
-  const int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (g > G) return;  // whole warps exit together: blockDim is a multiple of 32
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g > G) return;
   const int64_t total = m + n;
   const int64_t k = g * D < total ? g * D : total;
-  KeysAFirst<K> pred{A, B};
-  const int64_t i = warp_corank(pred, k, m, n);
-  if ((threadIdx.x & 31) == 0) {
-    if (out_i) out_i[g] = i;
-    if (out_ij) {
-      out_ij[2 * g] = i;
-      out_ij[2 * g + 1] = k - i;
-    }
+  const int64_t i = thread_corank(KeysAFirst<K>{A, B}, k, m, n);
+  if (out_i) out_i[g] = i;
+  if (out_ij) {
+    out_ij[2 * g] = i;
+    out_ij[2 * g + 1] = k - i;
   }
 }
 
-template <typename K, bool PAY, int T, int E>
+// Shared-memory layout of one CTA: S input stages (keys region then payload
+// region, each large enough for D elements plus the 16-byte alignment slack
+// of two spans), NOUT output tiles, and per stage a full barrier, an empty
+// barrier and a tile descriptor written by the producer.
+template <typename K, bool PAY, int E, int S, int NOUT>
 struct MergeLayout {
-  static constexpr int D = T * E;
+  static constexpr int D = kMergeThreads * E;
   static constexpr int SZ = sizeof(K);
-  static constexpr int64_t kBar = 0;
-  static constexpr int64_t kInKeys = 128;
-  static constexpr int64_t kInKeysBytes = align_up(int64_t(D) * SZ + 128, 16);
-  static constexpr int64_t kInPay = kInKeys + kInKeysBytes;
-  static constexpr int64_t kInPayBytes = PAY ? align_up(int64_t(D) * 4 + 128, 16) : 0;
-  static constexpr int64_t kOutKeys = kInPay + kInPayBytes;
-  static constexpr int64_t kOutPay = kOutKeys + align_up(int64_t(D) * SZ, 16);
-  static constexpr int64_t kBytes = kOutPay + (PAY ? align_up(int64_t(D) * 4, 16) : 0);
+  static constexpr int64_t kFull = 0;                                  // S x 8
+  static constexpr int64_t kEmpty = 8 * S;                             // S x 8
+  static constexpr int64_t kMeta = 16 * S;                             // S x 32
+  static constexpr int64_t kStage0 = align_up(48 * S, 128);
+  static constexpr int64_t kKeysBytes = align_up(int64_t(D) * SZ + 128, 16);
+  static constexpr int64_t kPayBytes = PAY ? align_up(int64_t(D) * 4 + 128, 16) : 0;
+  static constexpr int64_t kStageBytes = kKeysBytes + kPayBytes;
+  static constexpr int64_t kOut0 = kStage0 + S * kStageBytes;
+  static constexpr int64_t kOutKeysBytes = align_up(int64_t(D) * SZ, 16);
+  static constexpr int64_t kOutBytes = kOutKeysBytes + (PAY ? align_up(int64_t(D) * 4, 16) : 0);
+  static constexpr int64_t kBytes = kOut0 + NOUT * kOutBytes;
 };
 
-template <typename K, bool PAY, int T, int E>
-__global__ void __launch_bounds__(T) merge_tile_kernel(
+// A tile as the merging warps see it: counts and the element offsets of the
+// four spans inside the stage buffer (computed once, by the producer).
+struct TileDesc {
+  int32_t na, nb;
+  int32_t offA, offB;    // in keys, from the stage start
+  int32_t offPA, offPB;  // in uint32 words, from the payload region start
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(TileDesc) == 32, "descriptor slot");
+
+// Warp-specialized persistent kernel: warps 0..T/32-1 merge, the last warp
+// stages tiles. CTA c handles tiles c, c + P, c + 2P, ... (P = gridDim.x).
+// Stage s = r % S holds the r-th tile; full[s] completes when its bulk copies
+// land, empty[s] when every merging warp has finished reading it.
+template <typename K, bool PAY, int E, int S, int NOUT>
+__global__ void __launch_bounds__(kMergeThreads + 32) merge_tile_kernel(
     const K *__restrict__ A, const uint32_t *__restrict__ Apay, int64_t m, const K *__restrict__ B,
-    const uint32_t *__restrict__ Bpay, int64_t n, const int64_t *__restrict__ part_i,
+    const uint32_t *__restrict__ Bpay, int64_t n, const int64_t *__restrict__ part_i, int64_t G,
     K *__restrict__ out, uint32_t *__restrict__ out_pay, int32_t *status) {
-  using L = MergeLayout<K, PAY, T, E>;
+  using L = MergeLayout<K, PAY, E, S, NOUT>;
   constexpr int D = L::D;
   constexpr int SZ = L::SZ;
+  constexpr int T = kMergeThreads;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::kBar);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kFull);
+  uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L::kEmpty);
+  TileDesc *desc = reinterpret_cast<TileDesc *>(smem + L::kMeta);
   const int tid = threadIdx.x;
-
-  const int64_t g = blockIdx.x;
   const int64_t total = m + n;
-  const int64_t k0 = g * D;
-  const int64_t k1 = k0 + D < total ? k0 + D : total;
-  const int64_t i0 = part_i[g], i1 = part_i[g + 1];
-  const int64_t j0 = k0 - i0, j1 = k1 - i1;
-  const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
+  const int64_t P = gridDim.x;
 
-  // shared-memory placement of the four spans (A keys, B keys, payloads)
-  const StagePlan pa = stage_plan<SZ>(i0, na), pb = stage_plan<SZ>(j0, nb);
-  K *bufA = reinterpret_cast<K *>(smem + L::kInKeys);
-  K *bufB = reinterpret_cast<K *>(smem + L::kInKeys + stage_capacity_bytes<SZ>(pa.span));
-  StagePlan qa{}, qb{};
-  uint32_t *bufPA = nullptr, *bufPB = nullptr;
-  if (PAY) {
-    qa = stage_plan<4>(i0, na);
-    qb = stage_plan<4>(j0, nb);
-    bufPA = reinterpret_cast<uint32_t *>(smem + L::kInPay);
-    bufPB = reinterpret_cast<uint32_t *>(smem + L::kInPay + stage_capacity_bytes<4>(qa.span));
-  }
-
-  if (tid == 0) mbar_init(bar, 1);
-  __syncthreads();
   if (tid == 0) {
-    const uint32_t tx = pa.bulk + pb.bulk + (PAY ? qa.bulk + qb.bulk : 0u);
-    mbar_arrive_expect_tx(bar, tx);
-    stage_issue(bufA, A, pa, bar);
-    stage_issue(bufB, B, pb, bar);
-    if (PAY) {
-      stage_issue(bufPA, Apay, qa, bar);
-      stage_issue(bufPB, Bpay, qb, bar);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], T / 32);
     }
   }
-  stage_tail(bufA, A, pa, i0, na, tid);
-  stage_tail(bufB, B, pb, j0, nb, tid);
-  if (PAY) {
-    stage_tail(bufPA, Apay, qa, i0, na, tid);
-    stage_tail(bufPB, Bpay, qb, j0, nb, tid);
-  }
-  const bool ok = mbar_wait_bounded(bar, 0, kWaitLimitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(status, LSM_ERR_TIMEOUT);
+  __syncthreads();
+
+  if (tid >= T) {
+    // ---------------- producer warp ----------------
+    // The 32 lanes fetch the partition entries of 32 upcoming tiles at once;
+    // lane 0 then stages those tiles one after the other as stages free up.
+    const int lane = tid & 31;
+    for (int64_t r0 = 0; blockIdx.x + r0 * P < G; r0 += 32) {
+      const int64_t gl = blockIdx.x + (r0 + lane) * P;
+      int64_t pi0 = 0, pi1 = 0;
+      if (gl < G) {
+        pi0 = __ldg(part_i + gl);
+        pi1 = __ldg(part_i + gl + 1);
+      }
+      for (int q = 0; q < 32; ++q) {
+        const int64_t r = r0 + q;
+        const int64_t g = blockIdx.x + r * P;
+        if (g >= G) break;
+        const int64_t i0 = __shfl_sync(0xffffffffu, pi0, q);
+        const int64_t i1 = __shfl_sync(0xffffffffu, pi1, q);
+        int failed = 0;
+        if (lane == 0) {
+          const int s = static_cast<int>(r % S);
+          if (r >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((r / S) + 1) & 1),
+                                           kWaitLimitNs)) {
+            report(status, LSM_ERR_TIMEOUT);
+            failed = 1;
+          } else {
+            const int64_t k0 = g * D, k1 = k0 + D < total ? k0 + D : total;
+            const int64_t j0 = k0 - i0, j1 = k1 - i1;
+            const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
+            uint8_t *stage = smem + L::kStage0 + s * L::kStageBytes;
+            const StagePlan pa = stage_plan_overfetch<SZ>(i0, na, m);
+            const StagePlan pb = stage_plan_overfetch<SZ>(j0, nb, n);
+            K *bufA = reinterpret_cast<K *>(stage);
+            const int32_t offB = static_cast<int32_t>(stage_capacity_bytes<SZ>(pa.span) / SZ);
+            K *bufB = bufA + offB;
+            TileDesc td;
+            td.na = na;
+            td.nb = nb;
+            td.offA = pa.lead;
+            td.offB = offB + pb.lead;
+            td.offPA = td.offPB = 0;
+            // ragged ends (only where a span touches the end of its array) by
+            // plain loads, before the arrive so that the barrier covers them
+            for (int64_t x = pa.tail_from; x < i1; ++x) bufA[x - pa.first] = A[x];
+            for (int64_t x = pb.tail_from; x < j1; ++x) bufB[x - pb.first] = B[x];
+            uint32_t tx = pa.bulk + pb.bulk;
+            StagePlan qa{}, qb{};
+            uint32_t *bufPA = nullptr, *bufPB = nullptr;
+            if (PAY) {
+              qa = stage_plan_overfetch<4>(i0, na, m);
+              qb = stage_plan_overfetch<4>(j0, nb, n);
+              bufPA = reinterpret_cast<uint32_t *>(stage + L::kKeysBytes);
+              const int32_t offPB = static_cast<int32_t>(stage_capacity_bytes<4>(qa.span) / 4);
+              bufPB = bufPA + offPB;
+              td.offPA = qa.lead;
+              td.offPB = offPB + qb.lead;
+              for (int64_t x = qa.tail_from; x < i1; ++x) bufPA[x - qa.first] = Apay[x];
+              for (int64_t x = qb.tail_from; x < j1; ++x) bufPB[x - qb.first] = Bpay[x];
+              tx += qa.bulk + qb.bulk;
+            }
+            desc[s] = td;
+            mbar_arrive_expect_tx(&full[s], tx);
+            stage_issue(bufA, A, pa, &full[s]);
+            stage_issue(bufB, B, pb, &full[s]);
+            if (PAY) {
+              stage_issue(bufPA, Apay, qa, &full[s]);
+              stage_issue(bufPB, Bpay, qb, &full[s]);
+            }
+          }
+        }
+        if (__shfl_sync(0xffffffffu, failed, 0)) return;
+      }
+    }
     return;
   }
 
-  const K *sA = bufA + pa.lead;
-  const K *sB = bufB + pb.lead;
-  const uint32_t *sPA = PAY ? bufPA + qa.lead : nullptr;
-  const uint32_t *sPB = PAY ? bufPB + qb.lead : nullptr;
-  K *oK = reinterpret_cast<K *>(smem + L::kOutKeys);
-  uint32_t *oP = reinterpret_cast<uint32_t *>(smem + L::kOutPay);
+  // ---------------- merging warps ----------------
+  const int lane = tid & 31;
+  for (int64_t r = 0;; ++r) {
+    const int64_t g = blockIdx.x + r * P;
+    if (g >= G) break;
+    const int s = static_cast<int>(r % S);
+    // The output tile about to be written was last stored NOUT tiles ago;
+    // wait until at most NOUT - 1 stores still read shared memory.
+    if (tid == 0) {
+      if (NOUT == 1) bulk_wait_read_all();
+      else bulk_wait_read_allow1();
+    }
+    const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((r / S) & 1), kWaitLimitNs);
+    if (named_sync_or(1, T, !ok)) {
+      if (tid == 0) report(status, LSM_ERR_TIMEOUT);
+      break;
+    }
+    const TileDesc td = desc[s];
+    const int na = td.na, nb = td.nb;
+    const K *stageK = reinterpret_cast<const K *>(smem + L::kStage0 + s * L::kStageBytes);
+    const K *sA = stageK + td.offA;
+    const K *sB = stageK + td.offB;
+    const uint32_t *stageP =
+        reinterpret_cast<const uint32_t *>(smem + L::kStage0 + s * L::kStageBytes + L::kKeysBytes);
+    const uint32_t *sPA = stageP + td.offPA;
+    const uint32_t *sPB = stageP + td.offPB;
+    uint8_t *obuf = smem + L::kOut0 + (NOUT == 1 ? 0 : (r & 1)) * L::kOutBytes;
+    K *oK = reinterpret_cast<K *>(obuf);
+    uint32_t *oP = reinterpret_cast<uint32_t *>(obuf + L::kOutKeysBytes);
 
-  // This thread's diagonal inside the tile, bisected in shared memory with
-  // the same A-first test as the partition.
-  const int cnt = na + nb;
-  const int d = tid * E < cnt ? tid * E : cnt;
-  int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (sA[mid] <= sB[d - mid - 1]) lo = mid + 1;
-    else hi = mid;
-  }
-  int ai = lo, bi = d - lo;
-  K a = ai < na ? sA[ai] : K(0);
-  K b = bi < nb ? sB[bi] : K(0);
+    // This thread's diagonal inside the tile, bisected in shared memory with
+    // the same A-first test as the partition, then E merge steps.
+    const int cnt = na + nb;
+    const int d = tid * E < cnt ? tid * E : cnt;
+    int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sA[mid] <= sB[d - mid - 1]) lo = mid + 1;
+      else hi = mid;
+    }
+    int ai = lo, bi = d - lo;
+    K a = ai < na ? sA[ai] : K(0);
+    K b = bi < nb ? sB[bi] : K(0);
 #pragma unroll
-  for (int s = 0; s < E; ++s) {
-    const int pos = d + s;
-    if (pos < cnt) {
-      const bool takeA = (bi >= nb) || (ai < na && a <= b);
-      oK[pos] = takeA ? a : b;
-      if (PAY) oP[pos] = takeA ? sPA[ai] : sPB[bi];
-      if (takeA) {
-        ++ai;
-        if (ai < na) a = sA[ai];
-      } else {
-        ++bi;
-        if (bi < nb) b = sB[bi];
+    for (int q = 0; q < E; ++q) {
+      const int pos = d + q;
+      if (pos < cnt) {
+        const bool takeA = (bi >= nb) || (ai < na && a <= b);
+        oK[pos] = takeA ? a : b;
+        if (PAY) oP[pos] = takeA ? sPA[ai] : sPB[bi];
+        if (takeA) {
+          ++ai;
+          if (ai < na) a = sA[ai];
+        } else {
+          ++bi;
+          if (bi < nb) b = sB[bi];
+        }
       }
     }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
+    // this warp is done reading the stage: hand it back to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    fence_proxy_async_smem();
+    named_sync(1, T);
 
-  // Write the tile back: bulk stores for the 16-byte multiple prefix, plain
-  // stores for the ragged end of the last tile.
-  const int key_bulk = (cnt * SZ) & ~15;
-  const int pay_bulk = (cnt * 4) & ~15;
-  if (tid == 0) {
-    if (key_bulk) bulk_s2g(out + k0, oK, key_bulk);
-    if (PAY && pay_bulk) bulk_s2g(out_pay + k0, oP, pay_bulk);
-    bulk_commit();
+    const int64_t k0 = g * D;
+    const int key_bulk = (cnt * SZ) & ~15;
+    const int pay_bulk = (cnt * 4) & ~15;
+    if (tid == 0) {
+      if (key_bulk) bulk_s2g(out + k0, oK, key_bulk);
+      if (PAY && pay_bulk) bulk_s2g(out_pay + k0, oP, pay_bulk);
+      bulk_commit();
+    }
+    // ragged end of the last tile
+    for (int x = key_bulk / SZ + tid; x < cnt; x += T) out[k0 + x] = oK[x];
+    if (PAY)
+      for (int x = pay_bulk / 4 + tid; x < cnt; x += T) out_pay[k0 + x] = oP[x];
+    if (NOUT == 1) named_sync(1, T);  // the ragged-end reads precede the next tile's writes
   }
-  for (int x = key_bulk / SZ + tid; x < cnt; x += T) out[k0 + x] = oK[x];
-  if (PAY)
-    for (int x = pay_bulk / 4 + tid; x < cnt; x += T) out_pay[k0 + x] = oP[x];
   if (tid == 0) bulk_wait_read_all();
 }
 
-int g_items[3] = {0, 15, 15};  // indexed by key type
+// Tile configurations: items per thread E, input stages S, output tiles NOUT.
+struct MergeConfig {
+  int E, S, NOUT;
+};
+constexpr MergeConfig kMergeConfigs[] = {
+    {5, 2, 1}, {7, 2, 1}, {11, 2, 1}, {15, 2, 1}, {7, 4, 2}, {11, 3, 2}, {15, 2, 2}, {7, 3, 1},
+};
+constexpr int kNumMergeConfigs = sizeof(kMergeConfigs) / sizeof(kMergeConfigs[0]);
+int g_config[3] = {0, 2, 2};  // indexed by key type; (11, 2, 1)
 
-template <typename K, bool PAY, int E>
+int sm_count() {
+  static std::mutex mu;
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev];
+}
+
+template <typename K, bool PAY, int E, int S, int NOUT>
 cudaError_t launch_merge_tiles(const K *A, const uint32_t *Apay, int64_t m, const K *B,
                                const uint32_t *Bpay, int64_t n, K *out, uint32_t *out_pay,
                                const int64_t *part_i, int32_t *status, cudaStream_t s) {
-  using L = MergeLayout<K, PAY, kMergeThreads, E>;
-  auto kern = merge_tile_kernel<K, PAY, kMergeThreads, E>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(L::kBytes));
-  if (err != cudaSuccess) return err;
+  using L = MergeLayout<K, PAY, E, S, NOUT>;
+  static_assert(L::kBytes <= 225 * 1024, "tile configuration exceeds shared memory");
+  auto kern = merge_tile_kernel<K, PAY, E, S, NOUT>;
+  constexpr int threads = kMergeThreads + 32;
+  static int per_sm = 0;  // resident CTAs per SM for this instantiation
+  if (!per_sm) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(L::kBytes));
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, L::kBytes);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+  }
   const int64_t G = (m + n + L::D - 1) / L::D;
+  int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
+  if (grid < 1) grid = 1;
+  if (grid > G) grid = G;
   profile_before(s);
-  kern<<<static_cast<unsigned>(G), kMergeThreads, L::kBytes, s>>>(A, Apay, m, B, Bpay, n, part_i,
-                                                                  out, out_pay, status);
+  kern<<<static_cast<unsigned>(grid), threads, L::kBytes, s>>>(A, Apay, m, B, Bpay, n, part_i, G, out,
+                                                                out_pay, status);
   profile_after(s);
   return cudaGetLastError();
 }
 
+template <typename K, bool PAY, int C>
+cudaError_t launch_config(const K *A, const uint32_t *Apay, int64_t m, const K *B,
+                          const uint32_t *Bpay, int64_t n, K *out, uint32_t *out_pay,
+                          const int64_t *part_i, int32_t *status, cudaStream_t s) {
+  constexpr MergeConfig c = kMergeConfigs[C];
+  return launch_merge_tiles<K, PAY, c.E, c.S, c.NOUT>(A, Apay, m, B, Bpay, n, out, out_pay, part_i,
+                                                      status, s);
+}
+
 template <typename K, bool PAY>
-cudaError_t dispatch_merge(int E, const K *A, const uint32_t *Apay, int64_t m, const K *B,
+cudaError_t dispatch_merge(int cfg, const K *A, const uint32_t *Apay, int64_t m, const K *B,
                            const uint32_t *Bpay, int64_t n, K *out, uint32_t *out_pay,
                            const int64_t *part_i, int32_t *status, cudaStream_t s) {
-  switch (E) {
-    case 7:
-      return launch_merge_tiles<K, PAY, 7>(A, Apay, m, B, Bpay, n, out, out_pay, part_i, status, s);
-    case 11:
-      return launch_merge_tiles<K, PAY, 11>(A, Apay, m, B, Bpay, n, out, out_pay, part_i, status, s);
-    case 15:
-      return launch_merge_tiles<K, PAY, 15>(A, Apay, m, B, Bpay, n, out, out_pay, part_i, status, s);
-    case 23:
-      return launch_merge_tiles<K, PAY, 23>(A, Apay, m, B, Bpay, n, out, out_pay, part_i, status, s);
+#define LSM_MERGE_CASE(C) \
+  case C:                 \
+    return launch_config<K, PAY, C>(A, Apay, m, B, Bpay, n, out, out_pay, part_i, status, s);
+  switch (cfg) {
+    LSM_MERGE_CASE(0)
+    LSM_MERGE_CASE(1)
+    LSM_MERGE_CASE(2)
+    LSM_MERGE_CASE(3)
+    LSM_MERGE_CASE(4)
+    LSM_MERGE_CASE(5)
+    LSM_MERGE_CASE(6)
+    LSM_MERGE_CASE(7)
     default:
       return cudaErrorInvalidValue;
   }
+#undef LSM_MERGE_CASE
 }
+static_assert(kNumMergeConfigs == 8, "dispatch_merge lists every configuration");
 
 template <typename K>
 cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n, int64_t D,
                                    int64_t *out_i, int64_t *out_ij, cudaStream_t s) {
   const int64_t G = (m + n + D - 1) / D;
-  const int64_t threads = (G + 1) * 32;
-  const int64_t blocks = (threads + 255) / 256;
+  const int64_t blocks = (G + 1 + 255) / 256;
   partition_keys_kernel<K><<<static_cast<unsigned>(blocks), 256, 0, s>>>(A, m, B, n, D, G, out_i,
                                                                           out_ij);
   return cudaGetLastError();
@@ -232,14 +370,19 @@ cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n,
 }  // namespace
 
 int merge_items_per_thread(int key_type) {
-  return (key_type == LSM_KEY_I32 || key_type == LSM_KEY_U64) ? g_items[key_type] : 0;
+  return (key_type == LSM_KEY_I32 || key_type == LSM_KEY_U64) ? kMergeConfigs[g_config[key_type]].E : 0;
 }
 
-int set_merge_items_per_thread(int key_type, int e) {
+int set_merge_config(int key_type, int items, int stages, int out_tiles) {
   if (key_type != LSM_KEY_I32 && key_type != LSM_KEY_U64) return LSM_ERR_DTYPE;
-  if (e != 7 && e != 11 && e != 15 && e != 23) return LSM_ERR_ARG;
-  g_items[key_type] = e;
-  return LSM_OK;
+  for (int c = 0; c < kNumMergeConfigs; ++c) {
+    if (kMergeConfigs[c].E == items && kMergeConfigs[c].S == stages &&
+        kMergeConfigs[c].NOUT == out_tiles) {
+      g_config[key_type] = c;
+      return LSM_OK;
+    }
+  }
+  return LSM_ERR_ARG;
 }
 
 cudaError_t launch_partition_keys(int key_type, const void *A, int64_t m, const void *B, int64_t n,
@@ -255,8 +398,8 @@ cudaError_t launch_merge_stable(int key_type, const void *A, const uint32_t *Apa
                                 const void *B, const uint32_t *Bpay, int64_t n, void *out,
                                 uint32_t *out_pay, int64_t *part_i, int32_t *status,
                                 cudaStream_t s) {
-  const int E = merge_items_per_thread(key_type);
-  const int64_t D = int64_t(kMergeThreads) * E;
+  const int cfg = g_config[key_type];
+  const int64_t D = int64_t(kMergeThreads) * kMergeConfigs[cfg].E;
   cudaError_t err = launch_partition_keys(key_type, A, m, B, n, D, part_i, nullptr, s);
   if (err != cudaSuccess) return err;
   const bool pay = Apay != nullptr;
@@ -264,14 +407,14 @@ cudaError_t launch_merge_stable(int key_type, const void *A, const uint32_t *Apa
     auto a = static_cast<const int32_t *>(A);
     auto b = static_cast<const int32_t *>(B);
     auto o = static_cast<int32_t *>(out);
-    return pay ? dispatch_merge<int32_t, true>(E, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s)
-               : dispatch_merge<int32_t, false>(E, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s);
+    return pay ? dispatch_merge<int32_t, true>(cfg, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s)
+               : dispatch_merge<int32_t, false>(cfg, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s);
   }
   auto a = static_cast<const uint64_t *>(A);
   auto b = static_cast<const uint64_t *>(B);
   auto o = static_cast<uint64_t *>(out);
-  return pay ? dispatch_merge<uint64_t, true>(E, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s)
-             : dispatch_merge<uint64_t, false>(E, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s);
+  return pay ? dispatch_merge<uint64_t, true>(cfg, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s)
+             : dispatch_merge<uint64_t, false>(cfg, a, Apay, m, b, Bpay, n, o, out_pay, part_i, status, s);
 }
 
 }  // namespace lsm

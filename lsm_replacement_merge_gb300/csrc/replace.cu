@@ -53,14 +53,16 @@ namespace {
 struct U64AFirst {
   const uint64_t *A;
   const uint64_t *B;
-  __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const { return A[i] <= B[k - i - 1]; }
+  __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
+    return __ldg(A + i) <= __ldg(B + k - i - 1);
+  }
 };
 
 // B_j precedes A_i exactly when lb_B[j] <= i, so A_i precedes B_j when i < lb_B[j].
 struct PositionsBFirst {
   const uint32_t *lb_B;
   __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
-    return i < static_cast<int64_t>(lb_B[k - i - 1]);
+    return i < static_cast<int64_t>(__ldg(lb_B + k - i - 1));
   }
 };
 
@@ -74,19 +76,18 @@ __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, in
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
   }
-  const int64_t g = gtid >> 5;
+  const int64_t g = gtid;
   if (g > G) return;
   const int64_t total = m + n;
   const int64_t k = g * D < total ? g * D : total;
-  const int64_t i = warp_corank(pred, k, m, n);
-  if ((threadIdx.x & 31) == 0) out_i[g] = i;
+  out_i[g] = thread_corank(pred, k, m, n);
 }
 
 template <class Pred>
 cudaError_t launch_partition(const Pred &pred, int64_t m, int64_t n, int64_t D, int64_t *out_i,
                              uint32_t *clear_words, int64_t nclear, cudaStream_t s) {
   const int64_t G = (m + n + D - 1) / D;
-  int64_t threads = (G + 1) * 32;
+  int64_t threads = G + 1;
   if (clear_words && threads < nclear / 4) threads = nclear / 4;
   const int64_t blocks = (threads + 255) / 256;
   partition_kernel<Pred><<<static_cast<unsigned>(blocks), 256, 0, s>>>(pred, m, n, D, G, out_i,

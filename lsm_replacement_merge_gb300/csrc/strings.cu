@@ -38,12 +38,11 @@ __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int6
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
-  const int64_t g = gtid >> 5;
+  const int64_t g = gtid;
   if (g > G) return;
   const int64_t total = m + n;
   const int64_t k = g * D < total ? g * D : total;
-  const int64_t i = warp_corank(pred, k, m, n);
-  if ((threadIdx.x & 31) == 0) out_i[g] = i;
+  out_i[g] = thread_corank(pred, k, m, n);
 }
 
 template <int T, int E>
@@ -122,7 +121,7 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
   constexpr int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t nwords = (m + 31) / 32;
-  int64_t threads = (G + 1) * 32;
+  int64_t threads = G + 1;
   if (threads < nwords / 4) threads = nwords / 4;
   partition_str_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
       StrAFirst{A, B}, m, n, D, G, part_i, C, nwords);

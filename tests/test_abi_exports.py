@@ -52,5 +52,5 @@ def test_host_side_checks_without_gpu(lib):
                                   ctypes.c_size_t(0), None) == 3              # LSM_ERR_OVERFLOW
     assert lib.lsm_rank_build(ctypes.c_void_p(16), I(100), ctypes.c_void_p(16), ctypes.c_void_p(16),
                               ctypes.c_void_p(16), ctypes.c_size_t(0), None) == 6  # workspace
-    assert lib.lsm_tune_merge_items(2, 8) == 1
-    assert lib.lsm_tune_merge_items(2, 15) == 0
+    assert lib.lsm_tune_merge(2, 8, 2, 1) == 1
+    assert lib.lsm_tune_merge(2, 7, 2, 1) == 0

@@ -22,7 +22,7 @@ def lsm():
     yield lsm
     assert lsm.get_device_status() == lsm.LSM_OK
     for kt in (lsm.LSM_KEY_I32, lsm.LSM_KEY_U64):
-        lsm.tune_merge_items(kt, 15)
+        lsm.tune_merge(kt, *lsm.DEFAULT_MERGE_CONFIG)
 
 
 def test_worked_example_and_page_cases(lsm, golden):
@@ -68,21 +68,22 @@ def _inputs(dt, m, n, seed, hi):
     return A, B, np.arange(m, dtype=np.uint32), (m + np.arange(n)).astype(np.uint32)
 
 
-@pytest.mark.parametrize("items", [7, 11, 15, 23])
+@pytest.mark.parametrize("cfg", [(5, 2, 1), (7, 2, 1), (11, 2, 1), (15, 2, 1), (7, 4, 2),
+                                 (11, 3, 2), (15, 2, 2), (7, 3, 1)])
 @pytest.mark.parametrize("dt,hi", [(np.int32, 3), (np.int32, 1 << 30), (np.uint64, 16),
                                    (np.uint64, 1 << 63)])
-def test_merge_stable_parity(lsm, items, dt, hi):
+def test_merge_stable_parity(lsm, cfg, dt, hi):
     kt = lsm.LSM_KEY_I32 if dt == np.int32 else lsm.LSM_KEY_U64
-    lsm.tune_merge_items(kt, items)
+    lsm.tune_merge(kt, *cfg)
     for s, (m, n) in enumerate(SIZES):
-        A, B, Ap, Bp = _inputs(dt, m, n, 1000 * items + s, hi)
+        A, B, Ap, Bp = _inputs(dt, m, n, 1000 * cfg[0] + 10 * cfg[1] + s, hi)
         ok, okp, _ = oracle.merge(A, B, Ap, Bp)
         keys, pay = lsm.merge_stable(up(A), up(B), up(Ap), up(Bp))
         assert np.array_equal(down(keys), ok), (m, n)
         assert np.array_equal(down(pay), okp), (m, n)
         keys2, none = lsm.merge_stable(up(A), up(B))
         assert none is None and np.array_equal(down(keys2), ok)
-    lsm.tune_merge_items(kt, 15)
+    lsm.tune_merge(kt, *lsm.DEFAULT_MERGE_CONFIG)
 
 
 @pytest.mark.parametrize("D", [1, 2, 7, 1000, 3840])
