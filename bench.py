@@ -59,6 +59,10 @@ def parse_args():
     ap.add_argument("--merge-config", default="11,2,1",
                     help="merge tile configuration: items per thread, stages, output tiles")
     ap.add_argument("--sweep", action="store_true", help="also time every items-per-thread setting")
+    ap.add_argument("--only", default="",
+                    help="run only this extra workload (merge_i32_4096, replace_u64_12M_4M, "
+                         "replace_skewed_2pow24_65536, strings_fc_4M_4M) and print its result; "
+                         "for profiler captures")
     ap.add_argument("--log2", type=int, default=26,
                     help="headline inputs hold 2^log2 keys each (26 = the full workload; smaller "
                          "values serve profiler captures)")
@@ -262,6 +266,11 @@ def main():
         pg = dist
     import lsm_replacement_merge_gb300 as lsm
     lsm.lib()
+    if args.only:
+        peak, _ = hbm_peak()
+        print(json.dumps({"only": args.only,
+                          "workloads": extra_workloads(lsm, torch, dev, peak, args, only=args.only)}))
+        return
     mcfg = tuple(int(x) for x in args.merge_config.split(","))
     lsm.tune_merge(lsm.LSM_KEY_U64, *mcfg)
     items = mcfg[0]
@@ -488,12 +497,28 @@ def time_pipeline(torch, stages, steps, flush, warmup=3):
     return statistics.mean(tot), {k: statistics.mean(v) for k, v in per.items()}
 
 
-def extra_workloads(lsm, torch, dev, peak, args):
+def extra_workloads(lsm, torch, dev, peak, args, only=""):
     out = {}
     flush = Flusher(torch, dev)
     steps = max(5, min(args.steps, 30))
 
+    def wanted(name):
+        return not only or only == name
+
     # int32 4096 + 4096 with payload
+    if wanted("merge_i32_4096"):
+        extra_merge_i32(lsm, torch, dev, steps, out)
+    for name, gen in (("replace_u64_12M_4M", synth.replace_u64),
+                      ("replace_skewed_2pow24_65536", synth.replace_skewed)):
+        if wanted(name):
+            extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, args.sweep)
+    if args.no_strings or not wanted("strings_fc_4M_4M"):
+        return out
+    extra_strings(lsm, torch, dev, peak, steps, flush, out)
+    return out
+
+
+def extra_merge_i32(lsm, torch, dev, steps, out):
     mi = synth.merge_i32()
     A, B = torch.from_numpy(mi.A).to(dev), torch.from_numpy(mi.B).to(dev)
     Ap, Bp = torch.from_numpy(mi.Apay).to(dev), torch.from_numpy(mi.Bpay).to(dev)
@@ -505,45 +530,53 @@ def extra_workloads(lsm, torch, dev, peak, args):
     out["merge_i32_4096"] = {"ms_per_step": ms, "gelem_s": 8192 / (ms * 1e-3) / 1e9,
                              "kernel_ms": per, "note": "latency-bound (two launches)"}
 
-    # uint64 replacement pipelines
-    for name, gen in (("replace_u64_12M_4M", synth.replace_u64),
-                      ("replace_skewed_2pow24_65536", synth.replace_skewed)):
-        ri = gen()
-        m, n = len(ri.A), len(ri.B)
-        A, B = torch.from_numpy(ri.A).to(dev), torch.from_numpy(ri.B).to(dev)
-        C = torch.empty((m + 31) // 32, dtype=torch.uint32, device=dev)
-        lb = torch.empty(n, dtype=torch.uint32, device=dev)
-        dir_ = torch.empty(3 * (m // 512 + 1), dtype=torch.uint32, device=dev)
-        tot = torch.empty(1, dtype=torch.int64, device=dev)
-        refs = torch.empty(m + n, dtype=torch.uint32, device=dev)
-        oa = torch.empty(m, dtype=torch.uint32, device=dev)
-        ob = torch.empty(n, dtype=torch.uint32, device=dev)
-        cnt = torch.empty(1, dtype=torch.int64, device=dev)
-        w1 = lsm.workspace(lsm.LSM_OP_COLLISION_MARK, m, n, dev)
-        w2 = lsm.workspace(lsm.LSM_OP_RANK_BUILD, m, 0, dev)
-        w3 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
-        stages = [("collision_mark", lambda: lsm.collision_mark(A, B, C, lb, w1)),
-                  ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
-                  ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
-                      m, n, C, dir_, lb, refs, oa, ob, cnt, w3))]
-        ms, per = time_pipeline(torch, stages, steps, flush)
-        N = int(cnt.item())
-        alg = (8 * (m + n)                      # read keys
-               + 4 * ((m + 31) // 32)           # write C
-               + 12 * (m // 512 + 1)            # write dir
-               + 4 * N + 4 * (m + n))           # write refs, ord_A, ord_B
-        out[name] = {"m": m, "n": n, "survivors": N, "ms_per_step": ms,
-                     "gelem_s": (m + n) / (ms * 1e-3) / 1e9,
-                     "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
-                     "frac": alg / (ms * 1e-3) / 1e9 / peak,
-                     "frac_of_8TBs_nominal": alg / (ms * 1e-3) / 1e9 / 8000.0,
-                     "kernel_ms": per, "gpu_launches_per_step": 6,
-                     "l2": "flushed (256 MiB write) before every step"}
-        del A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w1, w2, w3
-        torch.cuda.empty_cache()
 
-    if args.no_strings:
-        return out
+def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=False):
+    ri = gen()
+    m, n = len(ri.A), len(ri.B)
+    A, B = torch.from_numpy(ri.A).to(dev), torch.from_numpy(ri.B).to(dev)
+    C = torch.empty((m + 31) // 32, dtype=torch.uint32, device=dev)
+    lb = torch.empty(n, dtype=torch.uint32, device=dev)
+    dir_ = torch.empty(3 * (m // 512 + 1), dtype=torch.uint32, device=dev)
+    tot = torch.empty(1, dtype=torch.int64, device=dev)
+    refs = torch.empty(m + n, dtype=torch.uint32, device=dev)
+    oa = torch.empty(m, dtype=torch.uint32, device=dev)
+    ob = torch.empty(n, dtype=torch.uint32, device=dev)
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    w1 = lsm.workspace(lsm.LSM_OP_COLLISION_MARK, m, n, dev)
+    w2 = lsm.workspace(lsm.LSM_OP_RANK_BUILD, m, 0, dev)
+    w3 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
+    stages = [("collision_mark", lambda: lsm.collision_mark(A, B, C, lb, w1)),
+              ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
+              ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
+                  m, n, C, dir_, lb, refs, oa, ob, cnt, w3))]
+    ms, per = time_pipeline(torch, stages, steps, flush)
+    N = int(cnt.item())
+    alg = (8 * (m + n)                      # read keys
+           + 4 * ((m + 31) // 32)           # write C
+           + 12 * (m // 512 + 1)            # write dir
+           + 4 * N + 4 * (m + n))           # write refs, ord_A, ord_B
+    out[name] = {"m": m, "n": n, "survivors": N, "ms_per_step": ms,
+                 "gelem_s": (m + n) / (ms * 1e-3) / 1e9,
+                 "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
+                 "frac": alg / (ms * 1e-3) / 1e9 / peak,
+                 "frac_of_8TBs_nominal": alg / (ms * 1e-3) / 1e9 / 8000.0,
+                 "kernel_ms": per, "gpu_launches_per_step": 6,
+                 "l2": "flushed (256 MiB write) before every step"}
+    if sweep:
+        res = {}
+        for kernel, label in ((0, "collision_mark"), (1, "replacement_merge_compact")):
+            for v in lsm.REPLACE_VARIANTS:
+                lsm.tune_replace(kernel, *v)
+                _, per_v = time_pipeline(torch, stages, steps, flush)
+                res["%s %d,%d" % (label, v[0], v[1])] = per_v[label]
+            lsm.tune_replace(kernel, *lsm.REPLACE_VARIANTS[0])
+        out[name]["variant_sweep_ms"] = res
+    del A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w1, w2, w3
+    torch.cuda.empty_cache()
+
+
+def extra_strings(lsm, torch, dev, peak, steps, flush, out):
     s = synth.strings()
     Ak = lsm.Bytes.from_numpy(s.A.key_arena, s.A.key_off, dev)
     Bk = lsm.Bytes.from_numpy(s.B.key_arena, s.B.key_off, dev)
@@ -594,7 +627,6 @@ def extra_workloads(lsm, torch, dev, peak, args):
                                "frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": per,
                                "gpu_launches_per_step": 9,
                                "l2": "flushed (256 MiB write) before every step"}
-    return out
 
 
 if __name__ == "__main__":

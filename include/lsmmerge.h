@@ -151,7 +151,7 @@ LSM_API int lsm_merge_stable(int key_type, const void *A, const uint32_t *Apay, 
  * exactly when A_i == B_j for some j. The call clears C itself; bits at
  * positions >= m stay zero. A and B strictly increasing (unique keys).
  * A: device uint64[m]; B: device uint64[n]; C: device uint32[ceil(m/32)];
- * lb_B: device uint32[n]. m, n < 2^31. */
+ * lb_B: device uint32[n]. A, B and lb_B 16-byte aligned. m, n < 2^31. */
 LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                uint32_t *C, uint32_t *lb_B, void *ws, size_t ws_bytes,
                                void *stream);
@@ -218,7 +218,8 @@ LSM_API int lsm_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
  * The keys themselves are not read: B_j precedes A_i in the merge exactly
  * when lb_B[j] <= i, so the merge path runs over positions.
  * out_refs: device uint32[m + n] capacity; ord_A: uint32[m]; ord_B:
- * uint32[n]; d_count: int64[1]. m, n < 2^31. */
+ * uint32[n]; d_count: int64[1]; C, lb_B, out_refs, ord_A and ord_B 16-byte
+ * aligned. m, n < 2^31. */
 LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *C,
                                           const uint32_t *dir, const uint32_t *lb_B,
                                           uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
@@ -276,6 +277,12 @@ LSM_API int lsm_tune_merge(int key_type, int items_per_thread, int stages, int o
  * Process-wide, one-shot; pass NULL, NULL to cancel. The events are
  * cudaEvent_t handles owned by the caller. */
 LSM_API int lsm_set_profile_events(void *start_event, void *stop_event);
+
+/* Selects the tile variant of lsm_collision_mark (kernel 0) or
+ * lsm_replacement_merge_compact (kernel 1): threads per CTA and items per
+ * thread, from the compiled set (256,11) (128,23) (256,23) (512,11).
+ * Process-wide; the default is (256,11). */
+LSM_API int lsm_tune_replace(int kernel, int threads, int items_per_thread);
 
 /* ---- test hook ------------------------------------------------------------ */
 /* Launches one block that waits, with the same bounded wait the kernels

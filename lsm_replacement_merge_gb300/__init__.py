@@ -86,6 +86,7 @@ def lib():
                 "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
                 "lsm_tune_merge": ([ctypes.c_int] * 4, ctypes.c_int),
+                "lsm_tune_replace": ([ctypes.c_int] * 3, ctypes.c_int),
                 "lsm_set_profile_events": ([P, P], ctypes.c_int),
                 "lsm_rank_build_noalloc": ([P, I, P, P, P], ctypes.c_int),
             }
@@ -174,6 +175,14 @@ def set_profile_events(start=None, stop=None) -> None:
 MERGE_CONFIGS = ((5, 2, 1), (7, 2, 1), (11, 2, 1), (15, 2, 1), (7, 4, 2), (11, 3, 2), (15, 2, 2),
                  (7, 3, 1))
 DEFAULT_MERGE_CONFIG = (11, 2, 1)
+
+
+REPLACE_VARIANTS = ((256, 11), (128, 23), (256, 23), (512, 11))
+
+
+def tune_replace(kernel: int, threads: int, items_per_thread: int) -> None:
+    """Tile variant of collision_mark (kernel 0) or replacement_merge_compact (1)."""
+    _check("lsm_tune_replace", lib().lsm_tune_replace(kernel, threads, items_per_thread))
 
 
 def tune_merge(key_type: int, items_per_thread: int, stages: int, out_tiles: int) -> None:

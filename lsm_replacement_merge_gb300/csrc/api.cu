@@ -87,7 +87,7 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n) {
       c.take<int64_t>(merge_tiles_max(m + n) + 1);
       break;
     case LSM_OP_COLLISION_MARK: {
-      const int64_t D = int64_t(kMarkThreads) * kMarkItems;
+      const int64_t D = replace_min_tile();
       c.take<int64_t>((m + n + D - 1) / D + 1);
       break;
     }
@@ -97,10 +97,10 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n) {
       break;
     }
     case LSM_OP_RANK_BUILD:
-      c.take<uint32_t>(rank_build_ctas(m));
+      c.take<uint64_t>(rank_build_ctas(m));
       break;
     case LSM_OP_REPLACEMENT_COMPACT: {
-      const int64_t D = int64_t(kCompactThreads) * kCompactItems;
+      const int64_t D = replace_min_tile();
       c.take<int64_t>((m + n + D - 1) / D + 1);
       break;
     }
@@ -211,10 +211,11 @@ LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, 
   if ((m && (!A || !C)) || (n && (!B || !lb_B))) return LSM_ERR_ARG;
   if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
   if (m + n == 0) return LSM_OK;
-  if ((A && !aligned16(A)) || (B && !aligned16(B))) return LSM_ERR_ALIGN;
+  if ((A && !aligned16(A)) || (B && !aligned16(B)) || (lb_B && !aligned16(lb_B)))
+    return LSM_ERR_ALIGN;
   if (int r = check_ws(LSM_OP_COLLISION_MARK, m, n, ws, ws_bytes)) return r;
   Carver c{static_cast<uint8_t *>(ws)};
-  const int64_t D = int64_t(kMarkThreads) * kMarkItems;
+  const int64_t D = replace_min_tile();
   int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
   return cuda_status(launch_collision_mark(A ? A : B, m, B ? B : A, n, C, lb_B, part, status_ptr(),
                                            static_cast<cudaStream_t>(stream)));
@@ -244,8 +245,9 @@ LSM_API int lsm_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t 
   if (C && !aligned16(C)) return LSM_ERR_ALIGN;
   if (int r = check_ws(LSM_OP_RANK_BUILD, m, 0, ws, ws_bytes)) return r;
   Carver c{static_cast<uint8_t *>(ws)};
-  uint32_t *totals = c.take<uint32_t>(rank_build_ctas(m));
-  return cuda_status(launch_rank_build(C, m, dir, d_total, totals, static_cast<cudaStream_t>(stream)));
+  uint64_t *state = c.take<uint64_t>(rank_build_ctas(m));
+  return cuda_status(launch_rank_build_ws(C, m, dir, d_total, state, status_ptr(),
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
@@ -264,10 +266,12 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
   if (m < 0 || n < 0 || !dir || !d_count) return LSM_ERR_ARG;
   if ((m && (!C || !ord_A)) || (n && (!lb_B || !ord_B)) || (m + n && !out_refs)) return LSM_ERR_ARG;
   if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
-  if (lb_B && !aligned16(lb_B)) return LSM_ERR_ALIGN;
+  if ((lb_B && !aligned16(lb_B)) || (C && !aligned16(C)) || !aligned16(out_refs) ||
+      (ord_A && !aligned16(ord_A)) || (ord_B && !aligned16(ord_B)))
+    return LSM_ERR_ALIGN;
   if (int r = check_ws(LSM_OP_REPLACEMENT_COMPACT, m, n, ws, ws_bytes)) return r;
   Carver c{static_cast<uint8_t *>(ws)};
-  const int64_t D = int64_t(kCompactThreads) * kCompactItems;
+  const int64_t D = replace_min_tile();
   int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
   return cuda_status(launch_compact(m, n, C, dir, lb_B, out_refs, ord_A, ord_B, d_count, part,
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
@@ -315,6 +319,10 @@ LSM_API int lsm_set_profile_events(void *start_event, void *stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);
   return LSM_OK;
+}
+
+LSM_API int lsm_tune_replace(int kernel, int threads, int items_per_thread) {
+  return set_replace_variant(kernel, threads, items_per_thread);
 }
 
 LSM_API int lsm_tune_merge(int key_type, int items_per_thread, int stages, int out_tiles) {

@@ -69,14 +69,6 @@ constexpr uint64_t kFlagAgg = uint64_t(1) << 62;
 constexpr uint64_t kFlagInc = uint64_t(2) << 62;
 constexpr uint64_t kValMask = (uint64_t(1) << 62) - 1;
 
-__device__ __forceinline__ void st_relaxed(uint64_t *p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
 
 template <typename V>
 __device__ __forceinline__ V warp_sum(V v) {
@@ -90,20 +82,20 @@ __device__ __forceinline__ V warp_sum(V v) {
 __device__ uint64_t lookback(uint64_t *state, uint32_t t, uint64_t agg, int32_t *status) {
   const int lane = threadIdx.x & 31;
   if (t == 0) {
-    if (lane == 0) st_relaxed(state, kFlagInc | agg);
+    if (lane == 0) st_relaxed_u64(state, kFlagInc | agg);
     return 0;
   }
-  if (lane == 0) st_relaxed(state + t, kFlagAgg | agg);
+  if (lane == 0) st_relaxed_u64(state + t, kFlagAgg | agg);
   uint64_t prefix = 0;
   int64_t base = static_cast<int64_t>(t) - 1;
   const uint64_t t0 = globaltimer_ns();
   bool timed_out = false;
   for (;;) {
     const int64_t idx = base - lane;
-    uint64_t v = idx >= 0 ? ld_relaxed(state + idx) : kFlagInc;
+    uint64_t v = idx >= 0 ? ld_relaxed_u64(state + idx) : kFlagInc;
     uint32_t polls = 0;
     while (!__all_sync(0xffffffffu, (v >> 62) != 0)) {
-      if ((v >> 62) == 0) v = ld_relaxed(state + idx);
+      if ((v >> 62) == 0) v = ld_relaxed_u64(state + idx);
       if ((++polls & 31) == 0) {
         const bool late = globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs);
         if (__any_sync(0xffffffffu, late)) {
@@ -123,7 +115,7 @@ __device__ uint64_t lookback(uint64_t *state, uint32_t t, uint64_t agg, int32_t 
   }
   if (lane == 0) {
     if (timed_out) report(status, LSM_ERR_TIMEOUT);
-    st_relaxed(state + t, kFlagInc | ((prefix + agg) & kValMask));
+    st_relaxed_u64(state + t, kFlagInc | ((prefix + agg) & kValMask));
   }
   return prefix;
 }

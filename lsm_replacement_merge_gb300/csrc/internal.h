@@ -15,16 +15,18 @@ namespace lsm {
 // Tile geometry. Items per thread are odd so that per-thread output runs in
 // shared memory fall on distinct banks.
 constexpr int kMergeThreads = 256;
-constexpr int kMarkThreads = 256;
-constexpr int kCompactThreads = 256;
 constexpr int kRankThreads = 256;
 
 int merge_items_per_thread(int key_type);  // current setting (tunable)
 // Selects the tile configuration (items per thread, input stages, output
 // tiles) of lsm_merge_stable; returns LSM_OK or LSM_ERR_ARG.
 int set_merge_config(int key_type, int items, int stages, int out_tiles);
-constexpr int kMarkItems = 15;
-constexpr int kCompactItems = 15;
+// Smallest tile (elements) over the replacement pipelines' variants: sizes
+// the partition arrays in their workspaces.
+int64_t replace_min_tile();
+// Selects the tile variant of collision_mark (kernel 0) or
+// replacement_merge_compact (kernel 1); LSM_OK or LSM_ERR_ARG.
+int set_replace_variant(int kernel, int threads, int items);
 constexpr int64_t kMinMergeTile = kMergeThreads * 5;
 
 // --- merge.cu ---
@@ -41,6 +43,10 @@ cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *
                                   cudaStream_t s);
 cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
                               uint32_t *cta_totals, cudaStream_t s);
+// Workspace version: one launch (epoch-tagged lookback) when the CTAs fit on
+// the device at once, else count + finish. ws: rank_build_ctas(m) uint64.
+cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
+                                 void *ws, int32_t *status, cudaStream_t s);
 cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                               const uint32_t *pos, int64_t q, uint32_t *out, int32_t *status,
                               cudaStream_t s);
@@ -66,6 +72,9 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
 cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                            uint32_t *payload, int64_t nwords, int32_t *status, cudaStream_t s);
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
 
 // --- api.cu ---
 cudaError_t launch_timeout_probe(int64_t limit_ns, int32_t *status, cudaStream_t s);

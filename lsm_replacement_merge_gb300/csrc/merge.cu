@@ -287,16 +287,6 @@ constexpr MergeConfig kMergeConfigs[] = {
 constexpr int kNumMergeConfigs = sizeof(kMergeConfigs) / sizeof(kMergeConfigs[0]);
 int g_config[3] = {0, 2, 2};  // indexed by key type; (11, 2, 1)
 
-int sm_count() {
-  static std::mutex mu;
-  static int cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
-  return cache[dev];
-}
-
 template <typename K, bool PAY, int E, int S, int NOUT>
 cudaError_t launch_merge_tiles(const K *A, const uint32_t *Apay, int64_t m, const K *B,
                                const uint32_t *Bpay, int64_t n, K *out, uint32_t *out_pay,
@@ -315,7 +305,7 @@ cudaError_t launch_merge_tiles(const K *A, const uint32_t *Apay, int64_t m, cons
     if (per_sm < 1) per_sm = 1;
   }
   const int64_t G = (m + n + L::D - 1) / L::D;
-  int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
+  int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
   if (grid < 1) grid = 1;
   if (grid > G) grid = G;
   profile_before(s);
@@ -368,6 +358,16 @@ cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n,
 }
 
 }  // namespace
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev];
+}
 
 int merge_items_per_thread(int key_type) {
   return (key_type == LSM_KEY_I32 || key_type == LSM_KEY_U64) ? kMergeConfigs[g_config[key_type]].E : 0;

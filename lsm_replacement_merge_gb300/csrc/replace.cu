@@ -12,60 +12,74 @@
 //   - "The three experimental paths", third path: survivors of A and all of
 //     B have disjoint keys and are merged by merge path.
 //
-// GPU design:
+// GPU design (both tile kernels run on the persistent, warp-specialized
+// pipeline of pipeline.cuh: a producer warp stages each merge-path tile with
+// bulk copies while the consumer warps work on the previous one):
 //   collision_mark   partition (co-rank per tile, A first on ties; the same
-//                    launch clears C) + one CTA per merge-path tile. The tile
-//                    stages A[i0-1, i1) and B[j0, j1] in shared memory with
-//                    bulk copies, walks its merge, and for each B element
-//                    records lb = (A elements before it) - (1 if the element
-//                    before it is an equal A). Each collision bit is set by
-//                    the tile that owns the A index (it peeks at the B
-//                    element after its span), so bitmap words that lie inside
-//                    one tile take plain stores and only boundary words need
-//                    atomicOr.
-//   rank_build       count -> prefix -> finish in two launches: per-CTA
-//                    popcount totals, then each CTA sums the totals before it
-//                    and writes its directory entries ([CB] "Dispatch
-//                    bindings": the constructor is count, global scan,
-//                    finish; the finish runs at least one block for empty A).
+//                    launch clears C), then per tile: the stage holds
+//                    A[i0-1, i1) and B[j0, j1]; every B key of the tile takes
+//                    its lower bound in the staged A span by a fixed-step
+//                    search ([CB]: "for each B record, find its lower bound
+//                    in A"); a match sets the collision bit. Each bit is set
+//                    by the tile that owns its A index (the tile's last A is
+//                    checked against the first B after the tile), so bitmap
+//                    words inside one tile take plain stores and only
+//                    boundary words need atomicOr.
+//   rank_build       one launch with a decoupled lookback over CTA totals
+//                    when all CTAs fit on the device at once; otherwise
+//                    count -> prefix -> finish in two launches ([CB]
+//                    "Dispatch bindings"); at least one block for empty A.
 //   compact          merge path over positions: B_j precedes A_i exactly when
 //                    lb_B[j] <= i (this is B_j <= A_i, since lb_B[j] counts the
 //                    A keys below B_j), so the merge of surviving A and B
-//                    needs lb_B and C only, never the keys. A tile starting at
-//                    diagonal k0 with co-rank i0 has R(i0) dropped records
-//                    before it (a rank query), so its first survivor lands at
-//                    k0 - R(i0); a block-wide exclusive scan of keep flags
-//                    places the rest. Refs and ordinals leave through shared
-//                    memory in coalesced runs.
+//                    needs lb_B and C only, never the keys. In a tile with
+//                    co-rank i0 at diagonal k0, B_j sits at slot
+//                    (j - j0) + (lb_B[j] - i0); a bitmap of those slots and
+//                    prefix popcounts over it and over C give every slot its
+//                    element and its output position, k0 - R(i0) + slot -
+//                    (dropped A records before the slot), where R(i0) is a
+//                    rank query. Refs and ordinals leave by bulk stores.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace lsm {
 
 namespace {
 
-// ---- partition: co-rank per tile on uint64 keys, A first; clears C ----------
+// ---- partition: co-rank per tile -----------------------------------------------
+// uint64 keys, A first on ties.
 struct U64AFirst {
   const uint64_t *A;
   const uint64_t *B;
+  __device__ __forceinline__ void first_thread_extra(int64_t) const {}
   __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
     return __ldg(A + i) <= __ldg(B + k - i - 1);
   }
 };
 
-// B_j precedes A_i exactly when lb_B[j] <= i, so A_i precedes B_j when i < lb_B[j].
+// Positions, B first: A_i precedes B_j exactly when i < lb_B[j]. The
+// compaction's partition also writes the survivor count N = m + n - R(m)
+// (first thread), so that the count exists even when there are no tiles.
 struct PositionsBFirst {
   const uint32_t *lb_B;
+  const uint32_t *C, *dir;
+  int64_t m, n;
+  int64_t *d_count;
+  __device__ __forceinline__ void first_thread_extra(int64_t gtid) const;
   __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
     return i < static_cast<int64_t>(__ldg(lb_B + k - i - 1));
   }
 };
 
+// One thread per tile boundary; the launch also clears `clear_words`.
 template <class Pred>
 __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, int64_t n, int64_t D,
                                                         int64_t G, int64_t *__restrict__ out_i,
@@ -76,6 +90,7 @@ __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, in
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
   }
+  pred.first_thread_extra(gtid);
   const int64_t g = gtid;
   if (g > G) return;
   const int64_t total = m + n;
@@ -93,110 +108,6 @@ cudaError_t launch_partition(const Pred &pred, int64_t m, int64_t n, int64_t D, 
   partition_kernel<Pred><<<static_cast<unsigned>(blocks), 256, 0, s>>>(pred, m, n, D, G, out_i,
                                                                        clear_words, nclear);
   return cudaGetLastError();
-}
-
-// ---- collision mark ------------------------------------------------------------
-template <int T, int E>
-struct MarkLayout {
-  static constexpr int D = T * E;
-  static constexpr int64_t kBar = 0;
-  static constexpr int64_t kKeys = 128;
-  static constexpr int64_t kKeysBytes = align_up(int64_t(D + 2) * 8 + 128, 16);
-  static constexpr int64_t kLB = kKeys + kKeysBytes;
-  static constexpr int64_t kLBBytes = align_up(int64_t(D) * 4, 16);
-  static constexpr int64_t kCw = kLB + kLBBytes;
-  static constexpr int64_t kCwBytes = align_up(int64_t(D / 32 + 4) * 4, 16);
-  static constexpr int64_t kBytes = kCw + kCwBytes;
-};
-
-template <int T, int E>
-__global__ void __launch_bounds__(T) collision_mark_kernel(const uint64_t *__restrict__ A, int64_t m,
-                                                           const uint64_t *__restrict__ B, int64_t n,
-                                                           const int64_t *__restrict__ part_i,
-                                                           uint32_t *__restrict__ C,
-                                                           uint32_t *__restrict__ lb_B,
-                                                           int32_t *status) {
-  using L = MarkLayout<T, E>;
-  constexpr int D = L::D;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::kBar);
-  uint32_t *sLB = reinterpret_cast<uint32_t *>(smem + L::kLB);
-  uint32_t *sCw = reinterpret_cast<uint32_t *>(smem + L::kCw);
-  const int tid = threadIdx.x;
-
-  const int64_t g = blockIdx.x;
-  const int64_t total = m + n;
-  const int64_t k0 = g * D;
-  const int64_t k1 = k0 + D < total ? k0 + D : total;
-  const int64_t i0 = part_i[g], i1 = part_i[g + 1];
-  const int64_t j0 = k0 - i0, j1 = k1 - i1;
-  const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
-  const int hp = i0 > 0 ? 1 : 0;   // A[i0-1] staged in front (for B's lower bounds)
-  const int hn = j1 < n ? 1 : 0;   // B[j1] staged behind (for A's collision bits)
-
-  const StagePlan pa = stage_plan<8>(i0 - hp, na + hp);
-  const StagePlan pb = stage_plan<8>(j0, nb + hn);
-  uint64_t *bufA = reinterpret_cast<uint64_t *>(smem + L::kKeys);
-  uint64_t *bufB = reinterpret_cast<uint64_t *>(smem + L::kKeys + stage_capacity_bytes<8>(pa.span));
-
-  const int64_t w0 = i0 >> 5;
-  const int nw = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
-  for (int x = tid; x < nw; x += T) sCw[x] = 0u;
-
-  if (tid == 0) mbar_init(bar, 1);
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, pa.bulk + pb.bulk);
-    stage_issue(bufA, A, pa, bar);
-    stage_issue(bufB, B, pb, bar);
-  }
-  stage_tail(bufA, A, pa, i0 - hp, na + hp, tid);
-  stage_tail(bufB, B, pb, j0, nb + hn, tid);
-  const bool ok = mbar_wait_bounded(bar, 0, kWaitLimitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(status, LSM_ERR_TIMEOUT);
-    return;
-  }
-
-  const uint64_t *sA = bufA + pa.lead + hp;  // sA[-1] = A[i0-1] when hp
-  const uint64_t *sB = bufB + pb.lead;       // sB[nb] = B[j1] when hn
-  const int cnt = na + nb;
-  const int d = tid * E < cnt ? tid * E : cnt;
-  int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (sA[mid] <= sB[d - mid - 1]) lo = mid + 1;
-    else hi = mid;
-  }
-  int ai = lo, bi = d - lo;
-#pragma unroll
-  for (int s = 0; s < E; ++s) {
-    if (d + s < cnt) {
-      const bool takeA = (bi >= nb) || (ai < na && sA[ai] <= sB[bi]);
-      if (takeA) {
-        // A_i collides exactly when the B element at the head equals it.
-        if ((bi < nb || hn) && sA[ai] == sB[bi]) {
-          const int64_t gi = i0 + ai;
-          atomicOr(&sCw[(gi >> 5) - w0], 1u << (gi & 31));
-        }
-        ++ai;
-      } else {
-        const uint64_t bk = sB[bi];
-        const int hit = ((ai > 0 || hp) && sA[ai - 1] == bk) ? 1 : 0;
-        sLB[bi] = static_cast<uint32_t>(i0 + ai - hit);
-        ++bi;
-      }
-    }
-  }
-  __syncthreads();
-  for (int x = tid; x < nb; x += T) lb_B[j0 + x] = sLB[x];
-  for (int x = tid; x < nw; x += T) {
-    const int64_t w = w0 + x;
-    const uint32_t bits = sCw[x];
-    const bool whole = (w * 32 >= i0) && (w * 32 + 32 <= i1);
-    if (whole) C[w] = bits;
-    else if (bits) atomicOr(&C[w], bits);
-  }
 }
 
 // ---- rank512 --------------------------------------------------------------------
@@ -293,6 +204,100 @@ __device__ __forceinline__ uint32_t rank512_at(const uint32_t *__restrict__ C,
   return r;
 }
 
+__device__ __forceinline__ void PositionsBFirst::first_thread_extra(int64_t gtid) const {
+  if (gtid == 0 && d_count) *d_count = m + n - static_cast<int64_t>(rank512_at(C, dir, m));
+}
+
+// Single-launch rank512 build: every CTA counts its 256 blocks, publishes
+// its total, looks back over its predecessors for the prefix (decoupled
+// lookback) and writes its entries. A state word is epoch << 32 | inclusive
+// flag << 31 | value; a word from another call carries another epoch and
+// reads as "not yet published", so the state needs no clearing pass. Used
+// only when all CTAs are resident at once, so every CTA a lookback waits for
+// is running; each wait is bounded in time.
+__global__ void __launch_bounds__(kRankThreads) rank_single_kernel(const uint32_t *__restrict__ C,
+                                                                   int64_t m,
+                                                                   uint32_t *__restrict__ dir,
+                                                                   int64_t *__restrict__ d_total,
+                                                                   uint64_t *state, uint32_t epoch,
+                                                                   int32_t *status) {
+  __shared__ uint32_t scratch[kRankThreads / 32 + 1];
+  __shared__ uint32_t s_prefix;
+  const int64_t nwords = (m + 31) / 32;
+  const int64_t nblk = m / 512 + 1;
+  const uint32_t t = blockIdx.x;
+  const int64_t b = static_cast<int64_t>(t) * kRankThreads + threadIdx.x;
+  uint32_t cum[8];
+  uint32_t tot = 0;
+  if (b < nblk) {
+    uint32_t w[16];
+    load_block_words(C, nwords, b, w);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      cum[s] = tot;
+      tot += __popc(w[2 * s]) + __popc(w[2 * s + 1]);
+    }
+  }
+  uint32_t agg;
+  const uint32_t excl = block_exclusive_sum<kRankThreads>(b < nblk ? tot : 0u, scratch, &agg);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const uint64_t tag = static_cast<uint64_t>(epoch) << 32;
+    uint32_t prefix = 0;
+    if (t == 0) {
+      if (lane == 0) st_relaxed_u64(state, tag | (1ull << 31) | agg);
+    } else {
+      if (lane == 0) st_relaxed_u64(state + t, tag | agg);
+      int64_t base = static_cast<int64_t>(t) - 1;
+      const uint64_t t0 = globaltimer_ns();
+      bool late = false;
+      for (;;) {
+        const int64_t idx = base - lane;
+        uint64_t v = idx >= 0 ? ld_relaxed_u64(state + idx) : (tag | (1ull << 31));
+        uint32_t polls = 0;
+        while (!__all_sync(0xffffffffu, (v >> 32) == epoch)) {
+          if ((v >> 32) != epoch) v = ld_relaxed_u64(state + idx);
+          if ((++polls & 31) == 0 &&
+              __any_sync(0xffffffffu, globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs))) {
+            late = true;
+            if ((v >> 32) != epoch) v = tag | (1ull << 31);  // give up: count it as zero
+          }
+        }
+        const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 31) & 1u);
+        if (inc) {
+          const int first = __ffs(inc) - 1;
+          uint32_t c = lane <= first ? static_cast<uint32_t>(v & 0x7FFFFFFFu) : 0u;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+          prefix += c;
+          break;
+        }
+        uint32_t c = static_cast<uint32_t>(v & 0x7FFFFFFFu);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        prefix += c;
+        base -= 32;
+      }
+      if (lane == 0) {
+        if (late) report(status, LSM_ERR_TIMEOUT);
+        st_relaxed_u64(state + t, tag | (1ull << 31) | ((prefix + agg) & 0x7FFFFFFFu));
+      }
+    }
+    if (lane == 0) s_prefix = prefix;
+  }
+  __syncthreads();
+  const uint32_t prefix = s_prefix;
+  if (b < nblk) {
+    uint64_t packed = 0;
+#pragma unroll
+    for (int s = 1; s < 8; ++s) packed |= static_cast<uint64_t>(cum[s]) << (9 * (s - 1));
+    dir[3 * b] = prefix + excl;
+    dir[3 * b + 1] = static_cast<uint32_t>(packed);
+    dir[3 * b + 2] = static_cast<uint32_t>(packed >> 32);
+  }
+  if (t == gridDim.x - 1 && threadIdx.x == 0) *d_total = static_cast<int64_t>(prefix) + agg;
+}
+
 __global__ void __launch_bounds__(256) rank_query_kernel(const uint32_t *__restrict__ C,
                                                          const uint32_t *__restrict__ dir, int64_t m,
                                                          const uint32_t *__restrict__ pos, int64_t q,
@@ -308,153 +313,341 @@ __global__ void __launch_bounds__(256) rank_query_kernel(const uint32_t *__restr
   out[t] = rank512_at(C, dir, p);
 }
 
-// ---- compact: merge path over positions ---------------------------------------------
-template <int T, int E>
-struct CompactLayout {
+// ---- collision mark ------------------------------------------------------------
+// One merge-path tile per pipeline step. The stage holds A[i0 - hp, i1) and
+// B[j0, j1 + hn): one A key before the span (for the lower bounds of B's
+// first keys) and one B key after it (for the collision bit of A's last key).
+template <int T_, int E_, int S_>
+struct MarkSpec {
+  static constexpr int T = T_;
+  static constexpr int E = E_;
+  static constexpr int S = S_;
   static constexpr int D = T * E;
-  static constexpr int64_t kBar = 0;
-  static constexpr int64_t kLB = 128;
-  static constexpr int64_t kLBBytes = align_up(int64_t(D) * 4 + 128, 16);
-  static constexpr int64_t kCw = kLB + kLBBytes;
-  static constexpr int64_t kCwBytes = align_up(int64_t(D / 32 + 4) * 4, 16);
-  static constexpr int64_t kRefs = kCw + kCwBytes;
-  static constexpr int64_t kOrdA = kRefs + align_up(int64_t(D) * 4, 16);
-  static constexpr int64_t kOrdB = kOrdA + align_up(int64_t(D) * 4, 16);
-  static constexpr int64_t kScan = kOrdB + align_up(int64_t(D) * 4, 16);
-  static constexpr int64_t kBytes = kScan + align_up(int64_t(T / 32 + 2) * 4, 16);
-};
-
-constexpr uint32_t kRecNone = 0u;
-constexpr uint32_t kRecA = 1u << 30;      // A element kept
-constexpr uint32_t kRecDrop = 2u << 30;   // A element dropped
-constexpr uint32_t kRecB = 3u << 30;      // B element
-constexpr uint32_t kRecIdx = (1u << 30) - 1u;
-
-template <int T, int E>
-__global__ void __launch_bounds__(T) compact_kernel(int64_t m, int64_t n, const uint32_t *__restrict__ C,
-                                                    const uint32_t *__restrict__ dir,
-                                                    const uint32_t *__restrict__ lb_B,
-                                                    const int64_t *__restrict__ part_i,
-                                                    uint32_t *__restrict__ refs,
-                                                    uint32_t *__restrict__ ord_A,
-                                                    uint32_t *__restrict__ ord_B,
-                                                    int64_t *__restrict__ d_count, int32_t *status) {
-  using L = CompactLayout<T, E>;
-  constexpr int D = L::D;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::kBar);
-  uint32_t *bufLB = reinterpret_cast<uint32_t *>(smem + L::kLB);
-  uint32_t *sCw = reinterpret_cast<uint32_t *>(smem + L::kCw);
-  uint32_t *sRefs = reinterpret_cast<uint32_t *>(smem + L::kRefs);
-  uint32_t *sOrdA = reinterpret_cast<uint32_t *>(smem + L::kOrdA);
-  uint32_t *sOrdB = reinterpret_cast<uint32_t *>(smem + L::kOrdB);
-  uint32_t *sScan = reinterpret_cast<uint32_t *>(smem + L::kScan);
-  __shared__ uint32_t sR0;
-  const int tid = threadIdx.x;
-
-  const int64_t g = blockIdx.x;
-  const int64_t total = m + n;
-  if (total == 0) {  // the single CTA launched for two empty inputs
-    if (tid == 0) *d_count = 0;
-    return;
+  static constexpr int64_t kStageBytes = align_up(int64_t(D + 4) * 8 + 160, 16);
+  static constexpr int64_t kLB = 0;
+  static constexpr int64_t kCw = align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kWorkBytes = kCw + align_up(int64_t(D / 32 + 4) * 4, 16);
+  struct Params {
+    const uint64_t *A, *B;
+    int64_t m, n;
+    const int64_t *part_i;
+    uint32_t *C, *lb_B;
+  };
+  struct Desc {
+    int64_t i0, j0;
+    int32_t na, nb, hp, hn, offA, offB;
+  };
+  __device__ static void init(uint8_t *work) {
+    uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
+    for (int x = threadIdx.x; x < D / 32 + 4; x += T) sCw[x] = 0u;
   }
-  const int64_t k0 = g * D;
-  const int64_t k1 = k0 + D < total ? k0 + D : total;
-  const int64_t i0 = part_i[g], i1 = part_i[g + 1];
-  const int64_t j0 = k0 - i0, j1 = k1 - i1;
-  const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
-
-  const StagePlan pl = stage_plan<4>(j0, nb);
-  if (tid == 0) mbar_init(bar, 1);
-  const int64_t w0 = i0 >> 5;
-  const int nw = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
-  for (int x = tid; x < nw; x += T) sCw[x] = C[w0 + x];
-  if (tid == 0) sR0 = rank512_at(C, dir, i0);
-  if (g == 0 && tid == 0) *d_count = total - static_cast<int64_t>(rank512_at(C, dir, m));
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, pl.bulk);
-    stage_issue(bufLB, lb_B, pl, bar);
+  __device__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
+    v[0] = __ldg(p.part_i + g);
+    v[1] = __ldg(p.part_i + g + 1);
   }
-  stage_tail(bufLB, lb_B, pl, j0, nb, tid);
-  const bool ok = mbar_wait_bounded(bar, 0, kWaitLimitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(status, LSM_ERR_TIMEOUT);
-    return;
+  __device__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
+                                 Desc &d, uint64_t *full) {
+    const int64_t total = p.m + p.n;
+    const int64_t i0 = v[0], i1 = v[1];
+    const int64_t k0 = g * D, k1 = k0 + D < total ? k0 + D : total;
+    const int64_t j0 = k0 - i0, j1 = k1 - i1;
+    const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
+    const int hp = i0 > 0 ? 1 : 0, hn = j1 < p.n ? 1 : 0;
+    const StagePlan pa = stage_plan_overfetch<8>(i0 - hp, na + hp, p.m);
+    const StagePlan pb = stage_plan_overfetch<8>(j0, nb + hn, p.n);
+    uint64_t *bufA = reinterpret_cast<uint64_t *>(stage);
+    const int32_t offB = static_cast<int32_t>(stage_capacity_bytes<8>(pa.span) / 8);
+    uint64_t *bufB = bufA + offB;
+    for (int64_t x = pa.tail_from; x < i1; ++x) bufA[x - pa.first] = p.A[x];
+    for (int64_t x = pb.tail_from; x < j1 + hn; ++x) bufB[x - pb.first] = p.B[x];
+    d.i0 = i0;
+    d.j0 = j0;
+    d.na = na;
+    d.nb = nb;
+    d.hp = hp;
+    d.hn = hn;
+    d.offA = pa.lead + hp;
+    d.offB = offB + pb.lead;
+    mbar_arrive_expect_tx(full, pa.bulk + pb.bulk);
+    stage_issue(bufA, p.A, pa, full);
+    stage_issue(bufB, p.B, pb, full);
   }
-  const uint32_t *sLB = bufLB + pl.lead;
-
-  const int cnt = na + nb;
-  const int d = tid * E < cnt ? tid * E : cnt;
-  int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (i0 + mid < static_cast<int64_t>(sLB[d - mid - 1])) lo = mid + 1;
-    else hi = mid;
-  }
-  int ai = lo, bi = d - lo;
-  uint32_t rec[E];
-  uint32_t kept = 0;
-#pragma unroll
-  for (int s = 0; s < E; ++s) {
-    rec[s] = kRecNone;
-    if (d + s < cnt) {
-      const bool takeA = (bi >= nb) || (ai < na && i0 + ai < static_cast<int64_t>(sLB[bi]));
-      if (takeA) {
-        const int64_t gi = i0 + ai;
-        const uint32_t drop = (sCw[(gi >> 5) - w0] >> (gi & 31)) & 1u;
-        rec[s] = (drop ? kRecDrop : kRecA) | static_cast<uint32_t>(ai);
-        kept += 1u - drop;
-        ++ai;
-      } else {
-        rec[s] = kRecB | static_cast<uint32_t>(bi);
-        ++kept;
-        ++bi;
+  __device__ static void consume(const Params &p, int64_t g, const Desc &dd, const uint8_t *stage,
+                                 uint8_t *work, uint64_t *empty) {
+    const int tid = threadIdx.x;
+    const uint64_t *sA = reinterpret_cast<const uint64_t *>(stage) + dd.offA;  // sA[-1] = A[i0-1]
+    const uint64_t *sB = reinterpret_cast<const uint64_t *>(stage) + dd.offB;  // sB[nb] = B[j1]
+    uint32_t *sLBbuf = reinterpret_cast<uint32_t *>(work + kLB);
+    uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
+    const int na = dd.na, nb = dd.nb, hp = dd.hp, hn = dd.hn;
+    const int64_t i0 = dd.i0, j0 = dd.j0, i1 = i0 + na;
+    uint32_t *sLB = sLBbuf + (j0 & 3);  // global alignment of lb_B[j0] mirrored
+    const int64_t w0 = i0 >> 5;
+    const int wbit0 = static_cast<int>(i0 - (w0 << 5));  // bit of A[i0] in word w0
+    // Every B key of the tile has its lower bound in A[i0 - hp, i1]: search
+    // the staged span (A[i0-1] included when it exists) with fixed steps.
+    const uint64_t *sAx = sA - hp;
+    const int lenx = na + hp;
+    const int top = lenx > 0 ? 1 << (31 - __clz(lenx)) : 0;  // largest power of two <= lenx
+    const uint32_t base = static_cast<uint32_t>(i0 - hp);
+    for (int bi = tid; bi < nb; bi += T) {
+      const uint64_t key = sB[bi];
+      int pos = -1;  // sAx[pos] < key, with sAx[-1] read as minus infinity
+      for (int step = top; step > 0; step >>= 1) {
+        const int probe = pos + step;
+        if (probe < lenx && sAx[probe] < key) pos = probe;
+      }
+      const int lbx = pos + 1;
+      sLB[bi] = base + static_cast<uint32_t>(lbx);
+      // A collision with A[i0-1] belongs to the previous tile, which finds it
+      // by peeking at this B key.
+      if (lbx < lenx && lbx >= hp && sAx[lbx] == key) {
+        const int x = wbit0 + (lbx - hp);
+        atomicOr(&sCw[x >> 5], 1u << (x & 31));
       }
     }
-  }
-  uint32_t kept_total;
-  uint32_t pos = block_exclusive_sum<T>(kept, sScan, &kept_total);
-  const int64_t out0 = k0 - static_cast<int64_t>(sR0);
-#pragma unroll
-  for (int s = 0; s < E; ++s) {
-    const uint32_t kind = rec[s] & ~kRecIdx, idx = rec[s] & kRecIdx;
-    if (kind == kRecA) {
-      sRefs[pos] = static_cast<uint32_t>(i0 + idx);
-      sOrdA[idx] = static_cast<uint32_t>(out0 + pos);
-      ++pos;
-    } else if (kind == kRecDrop) {
-      sOrdA[idx] = LSM_ORD_DROPPED;
-    } else if (kind == kRecB) {
-      sRefs[pos] = LSM_REF_FROM_B | static_cast<uint32_t>(j0 + idx);
-      sOrdB[idx] = static_cast<uint32_t>(out0 + pos);
-      ++pos;
+    // the tile's last A against the first B after the tile
+    if (tid == 0 && hn && na > 0 && sA[na - 1] == sB[nb]) {
+      const int x = wbit0 + na - 1;
+      atomicOr(&sCw[x >> 5], 1u << (x & 31));
     }
+    release_stage(empty);
+    fence_proxy_async_smem();
+    named_sync(1, T);
+    store_u32_run<T>(p.lb_B, j0, nb, sLBbuf);
+    if (tid == 0) bulk_commit();
+    const int nw = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
+    for (int x = tid; x < nw; x += T) {
+      const int64_t w = w0 + x;
+      const uint32_t bits = sCw[x];
+      sCw[x] = 0u;  // clean for the next tile
+      if (w * 32 >= i0 && w * 32 + 32 <= i1) p.C[w] = bits;
+      else if (bits) atomicOr(&p.C[w], bits);
+    }
+    if (tid == 0) bulk_wait_read_all();  // sLB is rewritten by the next tile
+    named_sync(1, T);
   }
-  __syncthreads();
-  for (uint32_t x = tid; x < kept_total; x += T) refs[out0 + x] = sRefs[x];
-  for (int x = tid; x < na; x += T) ord_A[i0 + x] = sOrdA[x];
-  for (int x = tid; x < nb; x += T) ord_B[j0 + x] = sOrdB[x];
-}
+};
+
+// ---- compact: merge path over positions ---------------------------------------------
+// One tile of the merge of (A positions, lb_B) per pipeline step. The stage
+// holds lb_B[j0, j1) and the collision words covering A[i0, i1); the
+// producer lanes also look up R(i0), so the tile's first survivor lands at
+// k0 - R(i0). In the tile's merged order (B first on ties) B_j sits at slot
+// (j - j0) + (lb_B[j] - i0); a bitmap of those slots and prefix popcounts
+// over it and over C give every slot its element and its output position
+// directly, without walking the merge.
+template <int T_, int E_, int S_>
+struct CompactSpec {
+  static constexpr int T = T_;
+  static constexpr int E = E_;
+  static constexpr int S = S_;
+  static constexpr int D = T * E;
+  static constexpr int NW = D / 32 + 2;  // slot-bitmap words
+  static constexpr int NC = D / 32 + 4;  // collision words of one tile, at most
+  static constexpr int64_t kLBBytes = align_up(int64_t(D) * 4 + 128, 16);
+  static constexpr int64_t kStageBytes = kLBBytes + align_up(int64_t(NC + 4) * 4 + 64, 16);
+  static constexpr int64_t kRefs = 0;
+  static constexpr int64_t kOrdA = align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kOrdB = kOrdA + align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kBpos = kOrdB + align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kPB = kBpos + align_up(int64_t(NW) * 4, 16);
+  static constexpr int64_t kPC = kPB + align_up(int64_t(NW + 1) * 4, 16);
+  static constexpr int64_t kScan = kPC + align_up(int64_t(NC + 1) * 4, 16);
+  static constexpr int64_t kWorkBytes = kScan + align_up(int64_t(T / 32 + 2) * 4, 16);
+  static_assert(NW <= T && NC <= T, "one thread per bitmap word");
+  struct Params {
+    int64_t m, n;
+    const uint32_t *C, *dir, *lb_B;
+    const int64_t *part_i;
+    uint32_t *refs, *ord_A, *ord_B;
+  };
+  struct Desc {
+    int64_t i0, j0, r0;
+    int32_t na, nb, offLB, offC;
+  };
+  __device__ static void init(uint8_t *work) {
+    uint32_t *sBpos = reinterpret_cast<uint32_t *>(work + kBpos);
+    for (int x = threadIdx.x; x < NW; x += T) sBpos[x] = 0u;
+  }
+  __device__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
+    v[0] = __ldg(p.part_i + g);
+    v[1] = __ldg(p.part_i + g + 1);
+    v[2] = rank512_at(p.C, p.dir, v[0]);
+  }
+  __device__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
+                                 Desc &d, uint64_t *full) {
+    const int64_t total = p.m + p.n;
+    const int64_t i0 = v[0], i1 = v[1];
+    const int64_t k0 = g * D, k1 = k0 + D < total ? k0 + D : total;
+    const int64_t j0 = k0 - i0, j1 = k1 - i1;
+    const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
+    const int64_t nwords = (p.m + 31) / 32;
+    const int64_t w0 = i0 >> 5;
+    const int nw = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
+    const StagePlan pl = stage_plan_overfetch<4>(j0, nb, p.n);
+    const StagePlan pc = stage_plan_overfetch<4>(w0, nw, nwords);
+    uint32_t *bufLB = reinterpret_cast<uint32_t *>(stage);
+    uint32_t *bufC = reinterpret_cast<uint32_t *>(stage + kLBBytes);
+    for (int64_t x = pl.tail_from; x < j1; ++x) bufLB[x - pl.first] = p.lb_B[x];
+    for (int64_t x = pc.tail_from; x < w0 + nw; ++x) bufC[x - pc.first] = p.C[x];
+    d.i0 = i0;
+    d.j0 = j0;
+    d.r0 = v[2];
+    d.na = na;
+    d.nb = nb;
+    d.offLB = pl.lead;
+    d.offC = pc.lead;
+    mbar_arrive_expect_tx(full, pl.bulk + pc.bulk);
+    stage_issue(bufLB, p.lb_B, pl, full);
+    stage_issue(bufC, p.C, pc, full);
+  }
+  __device__ static void consume(const Params &p, int64_t g, const Desc &dd, const uint8_t *stage,
+                                 uint8_t *work, uint64_t *empty) {
+    const int tid = threadIdx.x;
+    const uint32_t *sLB = reinterpret_cast<const uint32_t *>(stage) + dd.offLB;
+    const uint32_t *sCw = reinterpret_cast<const uint32_t *>(stage + kLBBytes) + dd.offC;
+    uint32_t *bufRefs = reinterpret_cast<uint32_t *>(work + kRefs);
+    uint32_t *bufOrdA = reinterpret_cast<uint32_t *>(work + kOrdA);
+    uint32_t *bufOrdB = reinterpret_cast<uint32_t *>(work + kOrdB);
+    uint32_t *sBpos = reinterpret_cast<uint32_t *>(work + kBpos);
+    uint32_t *sPB = reinterpret_cast<uint32_t *>(work + kPB);
+    uint32_t *sPC = reinterpret_cast<uint32_t *>(work + kPC);
+    uint32_t *sScan = reinterpret_cast<uint32_t *>(work + kScan);
+    const int na = dd.na, nb = dd.nb;
+    const int64_t i0 = dd.i0, j0 = dd.j0;
+    const int64_t out0 = g * D - dd.r0;
+    const int64_t w0 = i0 >> 5;
+    const int wbit0 = static_cast<int>(i0 - (w0 << 5));
+    const int nwc = na > 0 ? static_cast<int>((((i0 + na - 1) >> 5) - w0) + 1) : 0;
+    const uint32_t i0u = static_cast<uint32_t>(i0);
+    const int cnt = na + nb;
+    uint32_t *sRefs = bufRefs + (out0 & 3);
+    uint32_t *sOrdA = bufOrdA + (i0 & 3);
+    uint32_t *sOrdB = bufOrdB + (j0 & 3);
+
+    // 1. slots of the B records
+    for (int bi = tid; bi < nb; bi += T) {
+      const int slot = bi + static_cast<int>(sLB[bi] - i0u);
+      atomicOr(&sBpos[slot >> 5], 1u << (slot & 31));
+    }
+    const uint32_t cw_mine = tid < nwc ? sCw[tid] : 0u;
+    const uint32_t cmask0 = wbit0 ? (1u << wbit0) - 1u : 0u;  // bits before A[i0]
+    named_sync(1, T);
+    // 2. prefix popcounts: slot bitmap words and collision words. Only bits
+    //    of this tile's A records count: not those before A[i0] in the first
+    //    word, nor those of the next tile's records in the last word.
+    const uint32_t pb_mine = tid < NW ? static_cast<uint32_t>(__popc(sBpos[tid])) : 0u;
+    uint32_t cw_own = cw_mine;
+    if (tid == 0) cw_own &= ~cmask0;
+    const int xend = wbit0 + na;
+    if (tid == nwc - 1 && (xend & 31)) cw_own &= (1u << (xend & 31)) - 1u;
+    const uint32_t pc_mine = tid < nwc ? static_cast<uint32_t>(__popc(cw_own)) : 0u;
+    uint32_t totB, totC;
+    const uint32_t exB = consumer_exclusive_sum<T>(pb_mine, sScan, &totB);
+    if (tid < NW) sPB[tid] = exB;
+    const uint32_t exC = consumer_exclusive_sum<T>(pc_mine, sScan, &totC);
+    if (tid < nwc) sPC[tid] = exC;
+    named_sync(1, T);
+    // 3. every slot: its element, its output position (slot minus the A
+    //    records dropped before it) and its ordinal
+    for (int sl = tid; sl < cnt; sl += T) {
+      const int w = sl >> 5, bit = sl & 31;
+      const uint32_t bw = sBpos[w];
+      const int rb = static_cast<int>(sPB[w] + __popc(bw & ((1u << bit) - 1u)));
+      const int a = sl - rb;  // A records before this slot
+      // collision bits of tile A records [0, a): words before xa's word
+      // (prefix, first word masked) plus the bits below xa in its word
+      const int xa = wbit0 + a;
+      const int wa = xa >> 5;
+      const uint32_t cwa = a < na ? sCw[wa] : 0u;
+      int dropped_before = static_cast<int>(totC);
+      if (a < na)
+        dropped_before = static_cast<int>(sPC[wa]) + __popc(cwa & ((1u << (xa & 31)) - 1u)) -
+                         (wa == 0 ? __popc(cwa & cmask0) : 0);
+      const int outloc = sl - dropped_before;
+      if ((bw >> bit) & 1u) {
+        sRefs[outloc] = LSM_REF_FROM_B | static_cast<uint32_t>(j0 + rb);
+        sOrdB[rb] = static_cast<uint32_t>(out0 + outloc);
+      } else if ((cwa >> (xa & 31)) & 1u) {
+        sOrdA[a] = LSM_ORD_DROPPED;
+      } else {
+        sRefs[outloc] = i0u + static_cast<uint32_t>(a);
+        sOrdA[a] = static_cast<uint32_t>(out0 + outloc);
+      }
+    }
+    release_stage(empty);
+    const int kept_total = cnt - static_cast<int>(totC);
+    fence_proxy_async_smem();
+    named_sync(1, T);
+    store_u32_run<T>(p.refs, out0, kept_total, bufRefs);
+    store_u32_run<T>(p.ord_A, i0, na, bufOrdA);
+    store_u32_run<T>(p.ord_B, j0, nb, bufOrdB);
+    for (int x = tid; x < NW; x += T) sBpos[x] = 0u;  // clean for the next tile
+    if (tid == 0) {
+      bulk_commit();
+      bulk_wait_read_all();  // the buffers are rewritten by the next tile
+    }
+    named_sync(1, T);
+  }
+};
 
 }  // namespace
+
+// Tile variants of the two replacement pipelines: (consumer threads, items
+// per thread, stages). Selected process-wide by lsm_tune_replace.
+struct ReplaceVariant {
+  int T, E, S;
+};
+constexpr ReplaceVariant kReplaceVariants[] = {{256, 11, 2}, {128, 23, 2}, {256, 23, 2}, {512, 11, 2}};
+int g_mark_variant = 0, g_compact_variant = 0;
+
+template <int V>
+cudaError_t launch_mark_variant(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                uint32_t *C, uint32_t *lb_B, int64_t *part_i, int32_t *status,
+                                cudaStream_t s) {
+  constexpr ReplaceVariant v = kReplaceVariants[V];
+  using Spec = MarkSpec<v.T, v.E, v.S>;
+  constexpr int64_t D = Spec::D;
+  const int64_t nwords = (m + 31) / 32;
+  cudaError_t err = launch_partition(U64AFirst{A, B}, m, n, D, part_i, C, nwords, s);
+  if (err != cudaSuccess) return err;
+  const int64_t G = (m + n + D - 1) / D;
+  if (G == 0) return cudaSuccess;
+  typename Spec::Params p{A, B, m, n, part_i, C, lb_B};
+  profile_before(s);
+  err = launch_pipeline<Spec>(p, G, status, s, device_sm_count());
+  profile_after(s);
+  return err;
+}
 
 cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                   uint32_t *C, uint32_t *lb_B, int64_t *part_i, int32_t *status,
                                   cudaStream_t s) {
-  using L = MarkLayout<kMarkThreads, kMarkItems>;
-  const int64_t nwords = (m + 31) / 32;
-  cudaError_t err = launch_partition(U64AFirst{A, B}, m, n, L::D, part_i, C, nwords, s);
-  if (err != cudaSuccess) return err;
-  const int64_t G = (m + n + L::D - 1) / L::D;
-  if (G == 0) return cudaSuccess;
-  auto kern = collision_mark_kernel<kMarkThreads, kMarkItems>;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::kBytes));
-  if (err != cudaSuccess) return err;
-  profile_before(s);
-  kern<<<static_cast<unsigned>(G), kMarkThreads, L::kBytes, s>>>(A, m, B, n, part_i, C, lb_B, status);
-  profile_after(s);
-  return cudaGetLastError();
+  switch (g_mark_variant) {
+    case 1: return launch_mark_variant<1>(A, m, B, n, C, lb_B, part_i, status, s);
+    case 2: return launch_mark_variant<2>(A, m, B, n, C, lb_B, part_i, status, s);
+    case 3: return launch_mark_variant<3>(A, m, B, n, C, lb_B, part_i, status, s);
+    default: return launch_mark_variant<0>(A, m, B, n, C, lb_B, part_i, status, s);
+  }
+}
+
+int64_t replace_min_tile() {
+  int64_t d = INT64_MAX;
+  for (const ReplaceVariant &v : kReplaceVariants) d = d < int64_t(v.T) * v.E ? d : int64_t(v.T) * v.E;
+  return d;
+}
+
+int set_replace_variant(int kernel, int threads, int items) {
+  for (int i = 0; i < 4; ++i) {
+    if (kReplaceVariants[i].T == threads && kReplaceVariants[i].E == items) {
+      if (kernel == 0) g_mark_variant = i;
+      else if (kernel == 1) g_compact_variant = i;
+      else return LSM_ERR_ARG;
+      return LSM_OK;
+    }
+  }
+  return LSM_ERR_ARG;
 }
 
 int64_t rank_build_ctas(int64_t m) { return (m / 512 + 1 + kRankThreads - 1) / kRankThreads; }
@@ -469,6 +662,32 @@ cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64
   rank_finish_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(C, m, cta_totals, dir, d_total);
   profile_after(s);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
+                                 void *ws, int32_t *status, cudaStream_t s) {
+  static std::atomic<uint32_t> epoch_counter{0};
+  static int per_sm = -1;  // CTAs of rank_single_kernel resident per SM
+  if (per_sm < 0) {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, rank_single_kernel, kRankThreads, 0) !=
+        cudaSuccess)
+      v = 0;
+    per_sm = v;
+  }
+  const int64_t ctas = rank_build_ctas(m);
+  // one launch only while every CTA is resident at once, so each CTA a
+  // lookback waits for is already running
+  if (ctas <= static_cast<int64_t>(device_sm_count()) * per_sm) {
+    uint32_t epoch = ++epoch_counter;
+    if (epoch == 0) epoch = ++epoch_counter;
+    profile_before(s);
+    rank_single_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(
+        C, m, dir, d_total, static_cast<uint64_t *>(ws), epoch, status);
+    profile_after(s);
+    return cudaGetLastError();
+  }
+  return launch_rank_build(C, m, dir, d_total, static_cast<uint32_t *>(ws), s);
 }
 
 // ---- allocation-free rank_build --------------------------------------------------
@@ -512,23 +731,36 @@ cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
   return cudaGetLastError();
 }
 
+template <int V>
+cudaError_t launch_compact_variant(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
+                                   const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
+                                   uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
+                                   int32_t *status, cudaStream_t s) {
+  constexpr ReplaceVariant v = kReplaceVariants[V];
+  using Spec = CompactSpec<v.T, v.E, v.S>;
+  constexpr int64_t D = Spec::D;
+  cudaError_t err = launch_partition(PositionsBFirst{lb_B, C, dir, m, n, d_count}, m, n, D, part_i,
+                                     nullptr, 0, s);
+  if (err != cudaSuccess) return err;
+  const int64_t G = (m + n + D - 1) / D;
+  if (G == 0) return cudaSuccess;
+  typename Spec::Params p{m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B};
+  profile_before(s);
+  err = launch_pipeline<Spec>(p, G, status, s, device_sm_count());
+  profile_after(s);
+  return err;
+}
+
 cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
                            uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,
                            cudaStream_t s) {
-  using L = CompactLayout<kCompactThreads, kCompactItems>;
-  cudaError_t err = launch_partition(PositionsBFirst{lb_B}, m, n, L::D, part_i, nullptr, 0, s);
-  if (err != cudaSuccess) return err;
-  const int64_t G = (m + n + L::D - 1) / L::D;
-  auto kern = compact_kernel<kCompactThreads, kCompactItems>;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::kBytes));
-  if (err != cudaSuccess) return err;
-  // At least one CTA, so that d_count is written for two empty inputs.
-  profile_before(s);
-  kern<<<static_cast<unsigned>(G > 0 ? G : 1), kCompactThreads, L::kBytes, s>>>(
-      m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B, d_count, status);
-  profile_after(s);
-  return cudaGetLastError();
+  switch (g_compact_variant) {
+    case 1: return launch_compact_variant<1>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    case 2: return launch_compact_variant<2>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    case 3: return launch_compact_variant<3>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    default: return launch_compact_variant<0>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+  }
 }
 
 }  // namespace lsm
