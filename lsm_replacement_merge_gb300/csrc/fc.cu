@@ -22,12 +22,15 @@
 // bounded in time; a tile that gives up records LSM_ERR_TIMEOUT and still
 // publishes, so no other tile waits on it forever.
 //
-// fc_emit_kernel: one CTA per run of 256 x WPT payload words. One warp finds
-// the first and last record overlapping the run (32-way probes over
-// bit_off); each thread then owns WPT consecutive words, finds its first
-// record by bisection inside that range, and composes each word from the
-// fields of the records that overlap it. The run leaves through shared
-// memory with one bulk store.
+// fc_emit_kernel: one CTA owns a run of 4096 payload words (the word-owned
+// emit at CTA granularity: every global word is written once, by the CTA
+// that owns it). Two warps find the first and last record overlapping the
+// run (32-way probes over bit_off); the CTA gathers those records'
+// metadata into shared memory in one parallel pass; then one thread per
+// record writes the record's fields into the run's word buffer in shared
+// memory (words shared by two fields or records are ORed, words inside a
+// key or value field are stored whole), and the run leaves with one bulk
+// store.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -41,11 +44,12 @@ namespace lsm {
 namespace {
 
 constexpr int kFcThreads = 256;
-constexpr int kFcItems = 8;
+constexpr int kFcItems = 4;
 constexpr int kFcTile = kFcThreads * kFcItems;
 constexpr int kEmitThreads = 256;
-constexpr int kEmitWords = 8;  // words per thread
+constexpr int kEmitWords = 16;  // words per thread
 constexpr int kEmitRun = kEmitThreads * kEmitWords;
+constexpr int kEmitMaxRec = 512;  // records whose metadata one run stages at a time
 
 __device__ __forceinline__ uint64_t eg0_len(uint64_t x) {
   return 2 * static_cast<uint64_t>(63 - __clzll(static_cast<long long>(x + 1))) + 1;
@@ -122,7 +126,11 @@ __device__ uint64_t lookback(uint64_t *state, uint32_t t, uint64_t agg, int32_t 
 
 struct FcLayout {
   static constexpr int64_t kRefs = 0;                                   // u32[tile + 1]
-  static constexpr int64_t kLcp = align_up((kFcTile + 1) * 4, 16);      // u32[tile]
+  static constexpr int64_t kKb = align_up((kFcTile + 1) * 4, 16);       // u64[tile + 1]
+  static constexpr int64_t kKl = kKb + (kFcTile + 1) * 8;               // u32[tile + 1]
+  static constexpr int64_t kV = align_up(kKl + (kFcTile + 1) * 4, 16);  // u32[tile] value bits
+  static constexpr int64_t kSrc = kV + kFcTile * 4;                     // u8[tile + 1] from B
+  static constexpr int64_t kLcp = align_up(kSrc + kFcTile + 1, 16);     // u32[tile]
   static constexpr int64_t kCtrl = kLcp + kFcTile * 4;
   static constexpr int64_t kRec = kCtrl + kFcTile * 4;
   static constexpr int64_t kOff = kRec + kFcTile * 4;                   // u64[tile]
@@ -130,12 +138,52 @@ struct FcLayout {
   static constexpr int64_t kBytes = kScan + (kFcThreads / 32 + 2) * 8 + 16;
 };
 
+// 64 bits of an arena's bit stream (MSB first within bytes) starting at bit
+// sb, of which the first `need` (1..64) are used: aligned 8-byte loads,
+// byte-swapped; the second word is loaded only when the window crosses into
+// it, so nothing past the last needed byte's 8-byte word is read.
+__device__ __forceinline__ uint64_t bits64_at(const uint8_t *arena, uint64_t sb, int need) {
+  const uint64_t *w = reinterpret_cast<const uint64_t *>(arena);
+  const uint64_t t = sb >> 6;
+  const int sh = static_cast<int>(sb & 63);
+  uint64_t v = bswap64(__ldg(w + t)) << sh;
+  if (sh + need > 64) v |= bswap64(__ldg(w + t + 1)) >> (64 - sh);
+  return v;
+}
+
+// Exact bit LCP of two byte strings, clamped to the shorter one.
+__device__ __forceinline__ uint64_t bit_lcp(const uint8_t *aa, uint64_t ab, uint64_t alen,
+                                            const uint8_t *ba, uint64_t bb, uint64_t blen) {
+  const uint64_t L = 8 * (alen < blen ? alen : blen);
+  for (uint64_t t = 0; t < L; t += 64) {
+    const int need = L - t < 64 ? static_cast<int>(L - t) : 64;
+    uint64_t x = bits64_at(aa, 8 * ab + t, need);
+    uint64_t y = bits64_at(ba, 8 * bb + t, need);
+    if (need < 64) {
+      const uint64_t mask = ~uint64_t(0) << (64 - need);
+      x &= mask;
+      y &= mask;
+    }
+    if (x != y) return t + static_cast<uint64_t>(__clzll(static_cast<long long>(x ^ y)));
+  }
+  return L;
+}
+
+// One tile of 1024 records per CTA, in phases whose loads are independent
+// across records: (1) the refs, (2) every record's key offsets, value bits
+// and source, (3) each thread's four consecutive records: bit LCP with the
+// predecessor, control, record length; then a block scan and a decoupled
+// lookback over tiles turn lengths into bit offsets.
 __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N, uint32_t *__restrict__ lcp,
     uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec_bits, uint64_t *__restrict__ bit_off,
     uint64_t *state, uint32_t *tile_counter, int32_t *status) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t *sRefs = reinterpret_cast<uint32_t *>(smem + FcLayout::kRefs);
+  uint64_t *sKb = reinterpret_cast<uint64_t *>(smem + FcLayout::kKb);
+  uint32_t *sKl = reinterpret_cast<uint32_t *>(smem + FcLayout::kKl);
+  uint32_t *sV = reinterpret_cast<uint32_t *>(smem + FcLayout::kV);
+  uint8_t *sSrc = smem + FcLayout::kSrc;
   uint32_t *sLcp = reinterpret_cast<uint32_t *>(smem + FcLayout::kLcp);
   uint32_t *sCtrl = reinterpret_cast<uint32_t *>(smem + FcLayout::kCtrl);
   uint32_t *sRec = reinterpret_cast<uint32_t *>(smem + FcLayout::kRec);
@@ -153,48 +201,117 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   const uint32_t t = s_tile;
   const int64_t start = static_cast<int64_t>(t) * kFcTile;
   const int cnt = static_cast<int>(N - start < kFcTile ? N - start : kFcTile);
-  // sRefs[x] = refs[start - 1 + x]; sRefs[0] exists only after the first record
-  for (int x = tid; x <= cnt; x += kFcThreads)
-    if (start - 1 + x >= 0) sRefs[x] = refs[start - 1 + x];
+  // slot x holds record start - 1 + x (slot 0: the predecessor, if any)
+  const int first = start > 0 ? 0 : 1;
+  for (int x = first + tid; x <= cnt; x += kFcThreads) sRefs[x] = refs[start - 1 + x];
+  __syncthreads();
+  // (2) four records per thread per round: every load is issued before any
+  // result is stored
+  for (int x0 = first + tid; x0 <= cnt; x0 += 4 * kFcThreads) {
+    uint64_t kb[4], ke[4], vb[4], ve[4];
+    uint32_t tw[4], rr[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + u * kFcThreads;
+      const uint32_t r = sRefs[x <= cnt ? x : first];
+      rr[u] = r;
+      const uint32_t idx = r & ~LSM_REF_FROM_B;
+      const Source &src = pick(sa, sb, r);
+      kb[u] = __ldg(src.key.off + idx);
+      ke[u] = __ldg(src.key.off + idx + 1);
+      vb[u] = __ldg(src.val.off + idx);
+      ve[u] = __ldg(src.val.off + idx + 1);
+      tw[u] = src.tomb ? __ldg(src.tomb + (idx >> 5)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + u * kFcThreads;
+      if (x > cnt) continue;
+      const uint32_t idx = rr[u] & ~LSM_REF_FROM_B;
+      sKb[x] = kb[u];
+      sKl[x] = static_cast<uint32_t>(ke[u] - kb[u]);
+      sSrc[x] = (rr[u] & LSM_REF_FROM_B) ? 1 : 0;
+      if (x > 0) {
+        uint64_t v = 1;  // a tombstone is one bit
+        if (!((tw[u] >> (idx & 31)) & 1u)) {
+          const uint64_t vbytes = ve[u] - vb[u];
+          v = 1 + eg0_len(vbytes) + 8 * vbytes;
+        }
+        sV[x - 1] = v > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(v);
+      }
+    }
+  }
   __syncthreads();
 
+  // (3) this thread's records: the first two 64-bit windows of every key
+  // pair are loaded up front; longer common prefixes continue in a loop
   const int b0 = tid * kFcItems;
   uint64_t sum = 0;
   bool overflow = false;
-  if (b0 < cnt) {
-    KeyRef prev{nullptr, 0, 0};
-    uint64_t k_prev = 0;
-    if (start + b0 > 0) {
-      const uint32_t pr = sRefs[b0];
-      prev = key_at(pick(sa, sb, pr).key, pr & ~LSM_REF_FROM_B);
-      k_prev = 8 * (prev.end - prev.begin);
-    }
-    for (int s = 0; s < kFcItems && b0 + s < cnt; ++s) {
-      const int64_t i = start + b0 + s;
-      const uint32_t r = sRefs[b0 + s + 1];
-      const uint32_t idx = r & ~LSM_REF_FROM_B;
-      const Source &src = pick(sa, sb, r);
-      const KeyRef cur = key_at(src.key, idx);
-      const uint64_t k = 8 * (cur.end - cur.begin);
-      const uint64_t l = i == 0 ? 0 : key_bit_lcp(prev, cur);
-      const uint64_t c = (i % 15 == 0) ? 1 + l : k_prev - l;
-      uint64_t v;
-      if (is_tomb(src, idx)) {
-        v = 1;
-      } else {
-        const uint64_t vb = __ldg(src.val.off + idx + 1) - __ldg(src.val.off + idx);
-        v = 1 + eg0_len(vb) + 8 * vb;
+  uint64_t wx[kFcItems][2], wy[kFcItems][2];
+#pragma unroll
+  for (int q = 0; q < kFcItems; ++q) {
+    wx[q][0] = wy[q][0] = wx[q][1] = wy[q][1] = 0;
+    const int x = b0 + q + 1;
+    const int64_t i = start + b0 + q;
+    if (b0 + q < cnt && i > 0) {
+      const uint64_t L = 8 * static_cast<uint64_t>(sKl[x - 1] < sKl[x] ? sKl[x - 1] : sKl[x]);
+      const uint8_t *pa = sSrc[x - 1] ? sb.key.arena : sa.key.arena;
+      const uint8_t *ca = sSrc[x] ? sb.key.arena : sa.key.arena;
+      if (L > 0) {
+        const int n0 = L < 64 ? static_cast<int>(L) : 64;
+        wx[q][0] = bits64_at(pa, 8 * sKb[x - 1], n0);
+        wy[q][0] = bits64_at(ca, 8 * sKb[x], n0);
       }
-      const uint64_t L = eg0_len(c) + eg0_len(k - l) + (k - l) + v;
-      overflow |= (L > 0xFFFFFFFFull) || (c > 0xFFFFFFFFull);
-      sLcp[b0 + s] = static_cast<uint32_t>(l);
-      sCtrl[b0 + s] = static_cast<uint32_t>(c);
-      sRec[b0 + s] = static_cast<uint32_t>(L);
-      sOff[b0 + s] = L;  // length for now, offset after the scan
-      sum += L;
-      prev = cur;
-      k_prev = k;
+      if (L > 64) {
+        const int n1 = L - 64 < 64 ? static_cast<int>(L - 64) : 64;
+        wx[q][1] = bits64_at(pa, 8 * sKb[x - 1] + 64, n1);
+        wy[q][1] = bits64_at(ca, 8 * sKb[x] + 64, n1);
+      }
     }
+  }
+#pragma unroll
+  for (int q = 0; q < kFcItems; ++q) {
+    if (b0 + q >= cnt) break;
+    const int x = b0 + q + 1;  // this record's slot; x - 1 is its predecessor
+    const int64_t i = start + b0 + q;
+    const uint64_t k = 8 * static_cast<uint64_t>(sKl[x]);
+    uint64_t l = 0, k_prev = 0;
+    if (i > 0) {
+      k_prev = 8 * static_cast<uint64_t>(sKl[x - 1]);
+      const uint64_t L = k_prev < k ? k_prev : k;
+      l = L;
+      bool found = false;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t t0 = 64 * static_cast<uint64_t>(h);
+        if (!found && t0 < L) {
+          uint64_t xv = wx[q][h], yv = wy[q][h];
+          if (L - t0 < 64) {
+            const uint64_t mask = ~uint64_t(0) << (64 - (L - t0));
+            xv &= mask;
+            yv &= mask;
+          }
+          if (xv != yv) {
+            l = t0 + static_cast<uint64_t>(__clzll(static_cast<long long>(xv ^ yv)));
+            found = true;
+          }
+        }
+      }
+      if (!found && L > 128) {
+        const uint8_t *pa = sSrc[x - 1] ? sb.key.arena : sa.key.arena;
+        const uint8_t *ca = sSrc[x] ? sb.key.arena : sa.key.arena;
+        l = 128 + bit_lcp(pa, sKb[x - 1] + 16, sKl[x - 1] - 16, ca, sKb[x] + 16, sKl[x] - 16);
+      }
+    }
+    const uint64_t c = (i % 15 == 0) ? 1 + l : k_prev - l;
+    const uint64_t Lrec = eg0_len(c) + eg0_len(k - l) + (k - l) + sV[x - 1];
+    overflow |= (Lrec > 0xFFFFFFFFull) || (c > 0xFFFFFFFFull) || sV[x - 1] == 0xFFFFFFFFu;
+    sLcp[b0 + q] = static_cast<uint32_t>(l);
+    sCtrl[b0 + q] = static_cast<uint32_t>(c);
+    sRec[b0 + q] = static_cast<uint32_t>(Lrec);
+    sOff[b0 + q] = Lrec;  // length for now, offset after the scan
+    sum += Lrec;
   }
   if (overflow) report(status, LSM_ERR_OVERFLOW);
   uint64_t agg;
@@ -205,9 +322,9 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   }
   __syncthreads();
   uint64_t run = s_prefix + excl;
-  for (int s = 0; s < kFcItems && b0 + s < cnt; ++s) {
-    const uint64_t L = sOff[b0 + s];
-    sOff[b0 + s] = run;
+  for (int q = 0; q < kFcItems && b0 + q < cnt; ++q) {
+    const uint64_t L = sOff[b0 + q];
+    sOff[b0 + q] = run;
     run += L;
   }
   __syncthreads();
@@ -221,33 +338,6 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
 }
 
 // ---- emit ------------------------------------------------------------------------
-// Places bits [q0, q0 + len) of a W-bit numeric field (MSB first) that sits
-// at stream bits [fstart, fstart + W) into the word covering [wb, wb + 32).
-__device__ __forceinline__ void put_num(uint32_t &word, int64_t wb, int64_t fstart, int64_t W,
-                                        uint64_t V) {
-  const int64_t a = fstart > wb ? fstart : wb;
-  const int64_t e = fstart + W < wb + 32 ? fstart + W : wb + 32;
-  if (a >= e) return;
-  const int64_t q0 = a - fstart;
-  const int len = static_cast<int>(e - a);
-  const uint64_t chunk = (V >> (W - q0 - len)) & ((uint64_t(1) << len) - 1);
-  word |= static_cast<uint32_t>(chunk << (32 - (a - wb) - len));
-}
-
-// Same for a field whose bits come from an arena, starting at arena bit
-// src_bit; the field's bytes end at byte src_end.
-__device__ __forceinline__ void put_arena(uint32_t &word, int64_t wb, int64_t fstart, int64_t W,
-                                          const uint8_t *arena, uint64_t src_bit, uint64_t src_end) {
-  const int64_t a = fstart > wb ? fstart : wb;
-  const int64_t e = fstart + W < wb + 32 ? fstart + W : wb + 32;
-  if (a >= e) return;
-  const uint64_t sbit = src_bit + static_cast<uint64_t>(a - fstart);
-  const int len = static_cast<int>(e - a);
-  const uint64_t be = load_be64(arena, sbit >> 3, src_end);
-  const uint64_t chunk = (be << (sbit & 7)) >> (64 - len);
-  word |= static_cast<uint32_t>(chunk << (32 - (a - wb) - len));
-}
-
 struct RecordMeta {
   int64_t s, e;        // stream bits [s, e)
   uint64_t c, l, k;    // control, LCP bits, key bits
@@ -255,43 +345,6 @@ struct RecordMeta {
   bool tomb;
   KeyRef val;
 };
-
-__device__ __forceinline__ RecordMeta load_meta(const Source &sa, const Source &sb,
-                                                const uint32_t *refs, const uint32_t *lcp,
-                                                const uint32_t *ctrl, const uint64_t *bit_off,
-                                                int64_t r) {
-  RecordMeta M;
-  M.s = static_cast<int64_t>(__ldg(bit_off + r));
-  M.e = static_cast<int64_t>(__ldg(bit_off + r + 1));
-  M.c = __ldg(ctrl + r);
-  M.l = __ldg(lcp + r);
-  const uint32_t ref = __ldg(refs + r);
-  const uint32_t idx = ref & ~LSM_REF_FROM_B;
-  const Source &src = pick(sa, sb, ref);
-  M.key = key_at(src.key, idx);
-  M.k = 8 * (M.key.end - M.key.begin);
-  M.tomb = is_tomb(src, idx);
-  M.val = M.tomb ? KeyRef{nullptr, 0, 0} : key_at(src.val, idx);
-  return M;
-}
-
-__device__ __forceinline__ void compose(uint32_t &word, int64_t wb, const RecordMeta &M) {
-  const int64_t e1 = static_cast<int64_t>(eg0_len(M.c));
-  const uint64_t d = M.k - M.l;
-  const int64_t e2 = static_cast<int64_t>(eg0_len(d));
-  put_num(word, wb, M.s, e1, M.c + 1);
-  put_num(word, wb, M.s + e1, e2, d + 1);
-  const int64_t o3 = M.s + e1 + e2;
-  put_arena(word, wb, o3, static_cast<int64_t>(d), M.key.arena, 8 * M.key.begin + M.l, M.key.end);
-  const int64_t o4 = o3 + static_cast<int64_t>(d);
-  if (!M.tomb) {  // a tombstone is the single bit 0, already zero
-    const uint64_t vb = M.val.end - M.val.begin;
-    const int64_t ev = static_cast<int64_t>(eg0_len(vb));
-    put_num(word, wb, o4, 1 + ev, (uint64_t(1) << ev) | (vb + 1));
-    put_arena(word, wb, o4 + 1 + ev, static_cast<int64_t>(8 * vb), M.val.arena, 8 * M.val.begin,
-              M.val.end);
-  }
-}
 
 // Last index r in [lo, hi] with bit_off[r] <= bit (bit_off[lo] <= bit).
 __device__ __forceinline__ int64_t warp_record_at(const uint64_t *bit_off, int64_t lo, int64_t hi,
@@ -317,60 +370,174 @@ __device__ __forceinline__ int64_t warp_record_at(const uint64_t *bit_off, int64
   return lo;
 }
 
+// Shared-memory layout of one emit run: the output words and the metadata
+// of up to kEmitMaxRec records overlapping the run.
+struct EmitLayout {
+  static constexpr int64_t kOut = 0;                                   // u32[run]
+  static constexpr int64_t kS = kOut + int64_t(kEmitRun) * 4;          // u64[R + 1] start bits
+  static constexpr int64_t kKb = kS + int64_t(kEmitMaxRec + 1) * 8;    // u64 key byte begin
+  static constexpr int64_t kVb = kKb + int64_t(kEmitMaxRec) * 8;       // u64 value byte begin
+  static constexpr int64_t kC = kVb + int64_t(kEmitMaxRec) * 8;        // u32 control
+  static constexpr int64_t kL = kC + int64_t(kEmitMaxRec) * 4;         // u32 LCP bits
+  static constexpr int64_t kKl = kL + int64_t(kEmitMaxRec) * 4;        // u32 key bytes
+  static constexpr int64_t kVl = kKl + int64_t(kEmitMaxRec) * 4;       // u32 value bytes
+  static constexpr int64_t kF = kVl + int64_t(kEmitMaxRec) * 4;        // u32 flags
+  static constexpr int64_t kBytes = kF + int64_t(kEmitMaxRec) * 4 + 64;
+};
+constexpr uint32_t kFlagFromB = 1u, kFlagTomb = 2u;
+
+// ---- record-centric composition into a run's word buffer ------------------------
+// buf holds the run's words [w0, w0 + wn); only bits in the window [lo, hi)
+// are written. Numeric fields (W <= 64 bits, MSB first) OR their chunks in;
+// fields copied from an arena store whole words plainly (no other field or
+// record shares such a word) and OR the partial ones at their two ends.
+__device__ __forceinline__ void put_num_smem(uint32_t *buf, int64_t w0, int64_t lo, int64_t hi,
+                                             int64_t p, int W, uint64_t V) {
+  int64_t a = p > lo ? p : lo;
+  const int64_t e = p + W < hi ? p + W : hi;
+  while (a < e) {
+    const int64_t wb = a & ~int64_t(31);
+    const int64_t ce = e < wb + 32 ? e : wb + 32;
+    const int len = static_cast<int>(ce - a);
+    const int q0 = static_cast<int>(a - p);
+    const uint64_t chunk = (V >> (W - q0 - len)) & ((uint64_t(1) << len) - 1);
+    atomicOr(&buf[(wb >> 5) - w0], static_cast<uint32_t>(chunk << (32 - (a - wb) - len)));
+    a = ce;
+  }
+}
+
+// The arena's bit stream (MSB first within each byte) is the concatenation of
+// its aligned 32-bit words read big-endian, so the 32 source bits starting
+// at any bit are a funnel shift of two such words. A word past the field's
+// last byte is never loaded.
+__device__ __forceinline__ uint32_t be32_at(const uint8_t *arena, uint64_t t) {
+  return __byte_perm(__ldg(reinterpret_cast<const uint32_t *>(arena) + t), 0, 0x0123);
+}
+
+__device__ __forceinline__ void put_arena_smem(uint32_t *buf, int64_t w0, int64_t lo, int64_t hi,
+                                               int64_t p, int64_t W, const uint8_t *arena,
+                                               uint64_t src_bit, uint64_t /*src_end*/) {
+  int64_t x = p > lo ? p : lo;
+  const int64_t e = p + W < hi ? p + W : hi;
+  while (x < e) {
+    const int64_t wb = x & ~int64_t(31);
+    const int64_t ce = e < wb + 32 ? e : wb + 32;
+    const int len = static_cast<int>(ce - x);
+    const uint64_t sb = src_bit + static_cast<uint64_t>(x - p);
+    const uint64_t t = sb >> 5;
+    const int sh = static_cast<int>(sb & 31);
+    uint32_t v = be32_at(arena, t) << sh;
+    if (sh + len > 32) v |= be32_at(arena, t + 1) >> (32 - sh);
+    uint32_t *dst = &buf[(wb >> 5) - w0];
+    if (len == 32) {
+      *dst = v;
+    } else {
+      atomicOr(dst, (v >> (32 - len)) << (32 - static_cast<int>(x - wb) - len));
+    }
+    x = ce;
+  }
+}
+
+// Writes the bits of one record that fall in [lo, hi).
+__device__ __forceinline__ void emit_record(uint32_t *buf, int64_t w0, int64_t lo, int64_t hi,
+                                            const RecordMeta &M) {
+  if (M.e <= lo || M.s >= hi) return;
+  const int e1 = static_cast<int>(eg0_len(M.c));
+  const uint64_t d = M.k - M.l;
+  const int e2 = static_cast<int>(eg0_len(d));
+  put_num_smem(buf, w0, lo, hi, M.s, e1, M.c + 1);
+  put_num_smem(buf, w0, lo, hi, M.s + e1, e2, d + 1);
+  const int64_t o3 = M.s + e1 + e2;
+  put_arena_smem(buf, w0, lo, hi, o3, static_cast<int64_t>(d), M.key.arena, 8 * M.key.begin + M.l,
+                 M.key.end);
+  const int64_t o4 = o3 + static_cast<int64_t>(d);
+  if (!M.tomb) {  // a tombstone is the single bit 0, already zero
+    const uint64_t vb = M.val.end - M.val.begin;
+    const int ev = static_cast<int>(eg0_len(vb));
+    put_num_smem(buf, w0, lo, hi, o4, 1 + ev, (uint64_t(1) << ev) | (vb + 1));
+    put_arena_smem(buf, w0, lo, hi, o4 + 1 + ev, static_cast<int64_t>(8 * vb), M.val.arena,
+                   8 * M.val.begin, M.val.end);
+  }
+}
+
 __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N,
     const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
     const uint64_t *__restrict__ bit_off, uint32_t *__restrict__ payload, int64_t nwords) {
-  __shared__ __align__(16) uint32_t sOut[kEmitRun];
+  using L = EmitLayout;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint32_t *sOut = reinterpret_cast<uint32_t *>(smem + L::kOut);
+  uint64_t *sS = reinterpret_cast<uint64_t *>(smem + L::kS);
+  uint64_t *sKb = reinterpret_cast<uint64_t *>(smem + L::kKb);
+  uint64_t *sVb = reinterpret_cast<uint64_t *>(smem + L::kVb);
+  uint32_t *sC = reinterpret_cast<uint32_t *>(smem + L::kC);
+  uint32_t *sL = reinterpret_cast<uint32_t *>(smem + L::kL);
+  uint32_t *sKl = reinterpret_cast<uint32_t *>(smem + L::kKl);
+  uint32_t *sVl = reinterpret_cast<uint32_t *>(smem + L::kVl);
+  uint32_t *sF = reinterpret_cast<uint32_t *>(smem + L::kF);
   __shared__ int64_t sRange[2];
   const int tid = threadIdx.x;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEmitRun;
   const int64_t wn = nwords - w0 < kEmitRun ? nwords - w0 : kEmitRun;
   const uint64_t total = N > 0 ? __ldg(bit_off + N) : 0;
-  const uint64_t b0 = static_cast<uint64_t>(w0) * 32;
-  const bool any = b0 < total;
+  const int64_t lo = w0 * 32;
+  const int64_t hi = (w0 + wn) * 32 < static_cast<int64_t>(total) ? (w0 + wn) * 32
+                                                                  : static_cast<int64_t>(total);
+  const bool any = lo < hi;
+  for (int x = tid; x < kEmitRun; x += kEmitThreads) sOut[x] = 0u;
   if (any && tid < 64) {
     // warp 0: record holding the run's first bit; warp 1: its last bit
-    const uint64_t bend = b0 + static_cast<uint64_t>(wn) * 32;
-    const uint64_t bit = tid < 32 ? b0 : (bend < total ? bend : total) - 1;
+    const uint64_t bit = tid < 32 ? static_cast<uint64_t>(lo) : static_cast<uint64_t>(hi - 1);
     const int64_t r = warp_record_at(bit_off, 0, N - 1, bit);
     if ((tid & 31) == 0) sRange[tid >> 5] = r;
   }
   __syncthreads();
-  const int64_t wfirst = w0 + static_cast<int64_t>(tid) * kEmitWords;
-  uint32_t words[kEmitWords];
-#pragma unroll
-  for (int q = 0; q < kEmitWords; ++q) words[q] = 0u;
-  if (any && wfirst < w0 + wn && static_cast<uint64_t>(wfirst) * 32 < total) {
-    // this thread's first record, by bisection inside the run's record range
-    int64_t lo = sRange[0], hi = sRange[1];
-    const uint64_t bit = static_cast<uint64_t>(wfirst) * 32;
-    while (lo < hi) {
-      const int64_t mid = (lo + hi + 1) >> 1;
-      if (__ldg(bit_off + mid) <= bit) lo = mid;
-      else hi = mid - 1;
-    }
-    int64_t r = lo;
-    RecordMeta M = load_meta(sa, sb, refs, lcp, ctrl, bit_off, r);
-#pragma unroll 1
-    for (int q = 0; q < kEmitWords; ++q) {
-      const int64_t wb = (wfirst + q) * 32;
-      if (wfirst + q >= w0 + wn || static_cast<uint64_t>(wb) >= total) break;
-      uint32_t word = 0;
-      for (;;) {
-        compose(word, wb, M);
-        if (M.e < wb + 32 && r + 1 < N) {  // the next record starts inside this word
-          ++r;
-          M = load_meta(sa, sb, refs, lcp, ctrl, bit_off, r);
-          continue;
+  if (any) {
+    const int64_t r0 = sRange[0], r1 = sRange[1];
+    // records r0..r1, kEmitMaxRec at a time: gather their metadata in one
+    // parallel pass, then one thread per record writes its bits
+    for (int64_t c0 = r0; c0 <= r1; c0 += kEmitMaxRec) {
+      const int64_t R = r1 - c0 + 1 < kEmitMaxRec ? r1 - c0 + 1 : kEmitMaxRec;
+      for (int64_t x = tid; x < R; x += kEmitThreads) {
+        const int64_t r = c0 + x;
+        sS[x] = __ldg(bit_off + r);
+        if (x == R - 1) sS[R] = __ldg(bit_off + r + 1);
+        sC[x] = __ldg(ctrl + r);
+        sL[x] = __ldg(lcp + r);
+        const uint32_t ref = __ldg(refs + r);
+        const uint32_t idx = ref & ~LSM_REF_FROM_B;
+        const Source &src = pick(sa, sb, ref);
+        const uint64_t kb = __ldg(src.key.off + idx), ke = __ldg(src.key.off + idx + 1);
+        const bool tomb = is_tomb(src, idx);
+        uint64_t vb = 0, ve = 0;
+        if (!tomb) {
+          vb = __ldg(src.val.off + idx);
+          ve = __ldg(src.val.off + idx + 1);
         }
-        break;
+        sKb[x] = kb;
+        sKl[x] = static_cast<uint32_t>(ke - kb);
+        sVb[x] = vb;
+        sVl[x] = static_cast<uint32_t>(ve - vb);
+        sF[x] = ((ref & LSM_REF_FROM_B) ? kFlagFromB : 0u) | (tomb ? kFlagTomb : 0u);
       }
-      words[q] = word;
+      __syncthreads();
+      for (int64_t x = tid; x < R; x += kEmitThreads) {
+        RecordMeta M;
+        M.s = static_cast<int64_t>(sS[x]);
+        M.e = static_cast<int64_t>(sS[x + 1]);
+        M.c = sC[x];
+        M.l = sL[x];
+        const uint32_t f = sF[x];
+        const Source &src = (f & kFlagFromB) ? sb : sa;
+        M.key = KeyRef{src.key.arena, sKb[x], sKb[x] + sKl[x]};
+        M.k = 8 * static_cast<uint64_t>(sKl[x]);
+        M.tomb = (f & kFlagTomb) != 0;
+        M.val = KeyRef{src.val.arena, sVb[x], sVb[x] + sVl[x]};
+        emit_record(sOut, w0, lo, hi, M);
+      }
+      __syncthreads();
     }
   }
-#pragma unroll
-  for (int q = 0; q < kEmitWords; ++q) sOut[tid * kEmitWords + q] = words[q];
   fence_proxy_async_smem();
   __syncthreads();
   const int bulk_words = static_cast<int>(wn) & ~3;
@@ -418,8 +585,15 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
                            uint32_t *payload, int64_t nwords, int32_t * /*status*/, cudaStream_t s) {
   if (nwords == 0) return cudaSuccess;
   const int64_t runs = (nwords + kEmitRun - 1) / kEmitRun;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t err = cudaFuncSetAttribute(fc_emit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(EmitLayout::kBytes));
+    if (err != cudaSuccess) return err;
+    configured = true;
+  }
   profile_before(s);
-  fc_emit_kernel<<<static_cast<unsigned>(runs), kEmitThreads, 0, s>>>(
+  fc_emit_kernel<<<static_cast<unsigned>(runs), kEmitThreads, EmitLayout::kBytes, s>>>(
       make_source(in.keyA, in.valA, in.tombA), make_source(in.keyB, in.valB, in.tombB), refs, N, lcp,
       ctrl, bit_off, payload, nwords);
   profile_after(s);
