@@ -257,4 +257,38 @@ __device__ __forceinline__ int64_t thread_corank(const Pred &pred, int64_t k, in
   return lo;
 }
 
+// The same co-rank found by a group of L lanes (L a power of two <= 32,
+// groups aligned within the warp). Each round the group tests L pivots
+// spread evenly over the open range and keeps the interval between the last
+// pivot that is too small and the first that is not, so the range shrinks
+// (L + 1)-fold per round: fewer dependent rounds of loads than bisection,
+// for L times the loads per round. Every lane of the warp must call it (the
+// ballots span the warp); a lane with active = false joins with an empty
+// range and returns its lower end.
+template <int L, class Pred>
+__device__ __forceinline__ int64_t group_corank(const Pred &pred, int64_t k, int64_t m, int64_t n,
+                                                bool active) {
+  static_assert(L >= 1 && L <= 32 && (L & (L - 1)) == 0, "group size");
+  int64_t lo = k > n ? k - n : 0;
+  int64_t hi = k < m ? k : m;
+  if (!active) hi = lo;
+  const int lane = threadIdx.x & 31;
+  const int l = lane & (L - 1);
+  const int gbase = lane & ~(L - 1);
+  const uint32_t gmask = L == 32 ? 0xffffffffu : ((1u << L) - 1u);
+  while (__any_sync(0xffffffffu, lo < hi)) {
+    const int64_t span = hi - lo;
+    const bool open = span > 0;
+    const bool t = open && pred.too_small(lo + ((l + 1) * span) / (L + 1), k);
+    const int c = __popc((__ballot_sync(0xffffffffu, t) >> gbase) & gmask);
+    if (open) {
+      const int64_t nlo = c > 0 ? lo + (c * span) / (L + 1) + 1 : lo;
+      const int64_t nhi = c < L ? lo + ((c + 1) * span) / (L + 1) : hi;
+      lo = nlo;
+      hi = nhi;
+    }
+  }
+  return lo;
+}
+
 }  // namespace lsm

@@ -41,17 +41,34 @@ struct KeysAFirst {
   }
 };
 
+// Lanes per boundary search (group_corank); 1 is plain bisection, one
+// thread per boundary. With tens of thousands of boundaries the searches
+// are bound by random sector reads, not by their rounds, and more lanes per
+// search only add reads: bisection is fastest for this kernel.
+#ifndef LSM_MERGE_PARTITION_LANES
+#define LSM_MERGE_PARTITION_LANES 1
+#endif
+constexpr int kMergePartitionLanes = LSM_MERGE_PARTITION_LANES;
+
 template <typename K>
 __global__ void __launch_bounds__(256) partition_keys_kernel(const K *__restrict__ A, int64_t m,
                                                              const K *__restrict__ B, int64_t n,
                                                              int64_t D, int64_t G,
                                                              int64_t *__restrict__ out_i,
                                                              int64_t *__restrict__ out_ij) {
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (g > G) return;
+  const int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) /
+                    kMergePartitionLanes;
+  const bool active = g <= G;
   const int64_t total = m + n;
-  const int64_t k = g * D < total ? g * D : total;
-  const int64_t i = thread_corank(KeysAFirst<K>{A, B}, k, m, n);
+  const int64_t k = active ? (g * D < total ? g * D : total) : 0;
+  int64_t i;
+  if constexpr (kMergePartitionLanes == 1) {
+    if (!active) return;
+    i = thread_corank(KeysAFirst<K>{A, B}, k, m, n);
+  } else {
+    i = group_corank<kMergePartitionLanes>(KeysAFirst<K>{A, B}, k, m, n, active);
+    if (!active || (threadIdx.x & (kMergePartitionLanes - 1)) != 0) return;
+  }
   if (out_i) out_i[g] = i;
   if (out_ij) {
     out_ij[2 * g] = i;
@@ -351,7 +368,7 @@ template <typename K>
 cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n, int64_t D,
                                    int64_t *out_i, int64_t *out_ij, cudaStream_t s) {
   const int64_t G = (m + n + D - 1) / D;
-  const int64_t blocks = (G + 1 + 255) / 256;
+  const int64_t blocks = ((G + 1) * kMergePartitionLanes + 255) / 256;
   partition_keys_kernel<K><<<static_cast<unsigned>(blocks), 256, 0, s>>>(A, m, B, n, D, G, out_i,
                                                                           out_ij);
   return cudaGetLastError();

@@ -187,4 +187,61 @@ __device__ __forceinline__ V consumer_exclusive_sum(V v, V *scratch, V *total) {
   return out;
 }
 
+// Exclusive sum of `v` and exclusive maximum of `mx` over the T consumer
+// threads in one pass (named barrier 1). `scratch` holds 2 * (T/32 + 1)
+// values; *total is the sum over all threads and *mx_before the maximum of
+// `mx` over the threads before this one (0 for the first). The caller's
+// next barrier must come before scratch is written again.
+template <int NT>
+__device__ __forceinline__ uint32_t consumer_exclusive_sum_max(uint32_t v, uint32_t mx,
+                                                               uint32_t *scratch, uint32_t *total,
+                                                               uint32_t *mx_before) {
+  constexpr int NWARP = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = v, mi = mx;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, inc, off);
+    const uint32_t u = __shfl_up_sync(0xffffffffu, mi, off);
+    if (lane >= off) {
+      inc += t;
+      mi = u > mi ? u : mi;
+    }
+  }
+  // maximum over the lanes before this one
+  uint32_t mprev = __shfl_up_sync(0xffffffffu, mi, 1);
+  if (lane == 0) mprev = 0;
+  if (lane == 31) {
+    scratch[warp] = inc;
+    scratch[NWARP + 1 + warp] = mi;
+  }
+  named_sync(1, NT);
+  if (warp == 0) {
+    const uint32_t w = lane < NWARP ? scratch[lane] : 0u;
+    const uint32_t wm = lane < NWARP ? scratch[NWARP + 1 + lane] : 0u;
+    uint32_t wi = w, wmi = wm;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, wi, off);
+      const uint32_t u = __shfl_up_sync(0xffffffffu, wmi, off);
+      if (lane >= off) {
+        wi += t;
+        wmi = u > wmi ? u : wmi;
+      }
+    }
+    uint32_t wmprev = __shfl_up_sync(0xffffffffu, wmi, 1);
+    if (lane == 0) wmprev = 0;
+    if (lane < NWARP) {
+      scratch[lane] = wi - w;
+      scratch[NWARP + 1 + lane] = wmprev;
+    }
+    if (lane == NWARP - 1) scratch[NWARP] = wi;
+  }
+  named_sync(1, NT);
+  *total = scratch[NWARP];
+  const uint32_t wmb = scratch[NWARP + 1 + warp];
+  *mx_before = wmb > mprev ? wmb : mprev;
+  return scratch[warp] + inc - v;
+}
+
 }  // namespace lsm

@@ -17,11 +17,12 @@
 // bulk copies while the consumer warps work on the previous one):
 //   collision_mark   partition (co-rank per tile, A first on ties; the same
 //                    launch clears C), then per tile: the stage holds
-//                    A[i0-1, i1) and B[j0, j1]; every B key of the tile takes
-//                    its lower bound in the staged A span by a fixed-step
-//                    search ([CB]: "for each B record, find its lower bound
-//                    in A"); a match sets the collision bit. Each bit is set
-//                    by the tile that owns its A index (the tile's last A is
+//                    A[i0-1, i1) and B[j0, j1]; each thread bisects its own
+//                    diagonal of the tile and walks E merge steps, giving
+//                    every B key it passes its lower bound in A ([CB]: "for
+//                    each B record, find its lower bound in A") and every A
+//                    key that meets an equal B head its collision bit. Each
+//                    bit is set by the tile that owns its A index (the last A is
 //                    checked against the first B after the tile), so bitmap
 //                    words inside one tile take plain stores and only
 //                    boundary words need atomicOr.
@@ -59,27 +60,21 @@ namespace {
 struct U64AFirst {
   const uint64_t *A;
   const uint64_t *B;
-  __device__ __forceinline__ void first_thread_extra(int64_t) const {}
   __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
     return __ldg(A + i) <= __ldg(B + k - i - 1);
   }
 };
 
-// Positions, B first: A_i precedes B_j exactly when i < lb_B[j]. The
-// compaction's partition also writes the survivor count N = m + n - R(m)
-// (first thread), so that the count exists even when there are no tiles.
-struct PositionsBFirst {
-  const uint32_t *lb_B;
-  const uint32_t *C, *dir;
-  int64_t m, n;
-  int64_t *d_count;
-  __device__ __forceinline__ void first_thread_extra(int64_t gtid) const;
-  __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
-    return i < static_cast<int64_t>(__ldg(lb_B + k - i - 1));
-  }
-};
+// The co-rank of every tile boundary, each found by a group of
+// kPartitionLanes lanes (group_corank); the launch also clears
+// `clear_words`. With a few thousand boundaries the searches are bound by
+// their dependent rounds of loads, and four lanes (five-way splits) cut the
+// rounds from about 24 to 10 for fourfold the loads: the best measured.
+#ifndef LSM_MARK_PARTITION_LANES
+#define LSM_MARK_PARTITION_LANES 4
+#endif
+constexpr int kPartitionLanes = LSM_MARK_PARTITION_LANES;
 
-// One thread per tile boundary; the launch also clears `clear_words`.
 template <class Pred>
 __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, int64_t n, int64_t D,
                                                         int64_t G, int64_t *__restrict__ out_i,
@@ -90,19 +85,19 @@ __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, in
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
   }
-  pred.first_thread_extra(gtid);
-  const int64_t g = gtid;
-  if (g > G) return;
+  const int64_t g = gtid / kPartitionLanes;
+  const bool active = g <= G;
   const int64_t total = m + n;
-  const int64_t k = g * D < total ? g * D : total;
-  out_i[g] = thread_corank(pred, k, m, n);
+  const int64_t k = active ? (g * D < total ? g * D : total) : 0;
+  const int64_t i = group_corank<kPartitionLanes>(pred, k, m, n, active);
+  if (active && (threadIdx.x & (kPartitionLanes - 1)) == 0) out_i[g] = i;
 }
 
 template <class Pred>
 cudaError_t launch_partition(const Pred &pred, int64_t m, int64_t n, int64_t D, int64_t *out_i,
                              uint32_t *clear_words, int64_t nclear, cudaStream_t s) {
   const int64_t G = (m + n + D - 1) / D;
-  int64_t threads = G + 1;
+  int64_t threads = (G + 1) * kPartitionLanes;
   if (clear_words && threads < nclear / 4) threads = nclear / 4;
   const int64_t blocks = (threads + 255) / 256;
   partition_kernel<Pred><<<static_cast<unsigned>(blocks), 256, 0, s>>>(pred, m, n, D, G, out_i,
@@ -204,8 +199,76 @@ __device__ __forceinline__ uint32_t rank512_at(const uint32_t *__restrict__ C,
   return r;
 }
 
-__device__ __forceinline__ void PositionsBFirst::first_thread_extra(int64_t gtid) const {
-  if (gtid == 0 && d_count) *d_count = m + n - static_cast<int64_t>(rank512_at(C, dir, m));
+// The compaction's partition, by a scan over lb_B instead of one search per
+// boundary. With B first on ties, B_j sits at merged position
+// p_j = j + lb_B[j] (strictly increasing, below 2^32), so the co-rank of
+// diagonal k is i(k) = k - #{j : p_j < k}. A block takes the
+// kPosPerBlock records [jb, je) and owns the boundaries whose diagonal lies
+// in (p_{jb-1}, p_{je-1}] (the first block from k = 0, the last one up to
+// k = m + n); for each it counts the positions below k by a bisection over
+// the block's positions in shared memory. Results are clamped to the
+// diagonal's valid range, so an lb_B that is not a lower-bound array cannot
+// produce an out-of-range tile. Block 0 also writes the survivor count
+// N = m + n - R(m).
+constexpr int kPosThreads = 256;
+constexpr int kPosItems = 8;
+constexpr int kPosPerBlock = kPosThreads * kPosItems;
+
+__global__ void __launch_bounds__(kPosThreads) partition_positions_kernel(
+    const uint32_t *__restrict__ lb_B, int64_t m, int64_t n, int64_t D, int64_t G,
+    int64_t *__restrict__ out_i, const uint32_t *__restrict__ C, const uint32_t *__restrict__ dir,
+    int64_t *__restrict__ d_count) {
+  __shared__ uint32_t sp[kPosPerBlock];
+  __shared__ int64_t sRange[2];
+  const int t = threadIdx.x;
+  const int64_t jb = static_cast<int64_t>(blockIdx.x) * kPosPerBlock;
+  const int cnt = static_cast<int>(n - jb < kPosPerBlock ? n - jb : kPosPerBlock);
+  if (blockIdx.x == 0 && t == 0 && d_count)
+    *d_count = m + n - static_cast<int64_t>(rank512_at(C, dir, m));
+  // kPosItems consecutive records per thread: two 16-byte loads when the
+  // block is full (lb_B is 16-byte aligned and jb a multiple of 2048)
+  const int x0 = t * kPosItems;
+  if (cnt == kPosPerBlock) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(lb_B + jb + x0);
+    const uint4 u = __ldg(q), v = __ldg(q + 1);
+    const uint32_t lb[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < kPosItems; ++e) sp[x0 + e] = static_cast<uint32_t>(jb + x0 + e) + lb[e];
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPosItems; ++e)
+      if (x0 + e < cnt) sp[x0 + e] = static_cast<uint32_t>(jb + x0 + e) + __ldg(lb_B + jb + x0 + e);
+  }
+  __syncthreads();
+  if (t == 0) {
+    // boundaries g with p_{jb-1} < g D <= p_{je-1}
+    const bool last = jb + cnt >= n;
+    int64_t g_lo = 0;
+    if (jb > 0) g_lo = ((jb - 1) + static_cast<int64_t>(__ldg(lb_B + jb - 1))) / D + 1;
+    int64_t g_hi = G;
+    if (!last) {
+      const int64_t q = static_cast<int64_t>(sp[cnt - 1]) / D;
+      g_hi = q < G ? q : G;
+    }
+    sRange[0] = g_lo;
+    sRange[1] = g_hi;
+  }
+  __syncthreads();
+  const int64_t total = m + n;
+  const int64_t g_hi = sRange[1];
+  for (int64_t g = sRange[0] + t; g <= g_hi; g += kPosThreads) {
+    const int64_t k = g * D < total ? g * D : total;
+    int lo = 0, hi = cnt;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int64_t>(sp[mid]) < k) lo = mid + 1;
+      else hi = mid;
+    }
+    int64_t i = k - (jb + lo);
+    const int64_t ilo = k > n ? k - n : 0, ihi = k < m ? k : m;
+    i = i < ilo ? ilo : (i > ihi ? ihi : i);
+    out_i[g] = i;
+  }
 }
 
 // Single-launch rank512 build: every CTA counts its 256 blocks, publishes
@@ -337,15 +400,15 @@ struct MarkSpec {
     int64_t i0, j0;
     int32_t na, nb, hp, hn, offA, offB;
   };
-  __device__ static void init(uint8_t *work) {
+  __device__ __forceinline__ static void init(uint8_t *work) {
     uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
     for (int x = threadIdx.x; x < D / 32 + 4; x += T) sCw[x] = 0u;
   }
-  __device__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
+  __device__ __forceinline__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
     v[0] = __ldg(p.part_i + g);
     v[1] = __ldg(p.part_i + g + 1);
   }
-  __device__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
+  __device__ __forceinline__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
                                  Desc &d, uint64_t *full) {
     const int64_t total = p.m + p.n;
     const int64_t i0 = v[0], i1 = v[1];
@@ -372,7 +435,7 @@ struct MarkSpec {
     stage_issue(bufA, p.A, pa, full);
     stage_issue(bufB, p.B, pb, full);
   }
-  __device__ static void consume(const Params &p, int64_t g, const Desc &dd, const uint8_t *stage,
+  __device__ __forceinline__ static void consume(const Params &p, int64_t g, const Desc &dd, const uint8_t *stage,
                                  uint8_t *work, uint64_t *empty) {
     const int tid = threadIdx.x;
     const uint64_t *sA = reinterpret_cast<const uint64_t *>(stage) + dd.offA;  // sA[-1] = A[i0-1]
@@ -384,32 +447,50 @@ struct MarkSpec {
     uint32_t *sLB = sLBbuf + (j0 & 3);  // global alignment of lb_B[j0] mirrored
     const int64_t w0 = i0 >> 5;
     const int wbit0 = static_cast<int>(i0 - (w0 << 5));  // bit of A[i0] in word w0
-    // Every B key of the tile has its lower bound in A[i0 - hp, i1]: search
-    // the staged span (A[i0-1] included when it exists) with fixed steps.
-    const uint64_t *sAx = sA - hp;
-    const int lenx = na + hp;
-    const int top = lenx > 0 ? 1 << (31 - __clz(lenx)) : 0;  // largest power of two <= lenx
-    const uint32_t base = static_cast<uint32_t>(i0 - hp);
-    for (int bi = tid; bi < nb; bi += T) {
-      const uint64_t key = sB[bi];
-      int pos = -1;  // sAx[pos] < key, with sAx[-1] read as minus infinity
-      for (int step = top; step > 0; step >>= 1) {
-        const int probe = pos + step;
-        if (probe < lenx && sAx[probe] < key) pos = probe;
-      }
-      const int lbx = pos + 1;
-      sLB[bi] = base + static_cast<uint32_t>(lbx);
-      // A collision with A[i0-1] belongs to the previous tile, which finds it
-      // by peeking at this B key.
-      if (lbx < lenx && lbx >= hp && sAx[lbx] == key) {
-        const int x = wbit0 + (lbx - hp);
-        atomicOr(&sCw[x >> 5], 1u << (x & 31));
+    // Merge path inside the tile, A first on ties: this thread bisects its
+    // own diagonal, then walks E merge steps. A B key taken with i A keys
+    // before it has lower bound i0 + i, less one when the element just before
+    // it is an equal A key; an A key taken while the B head equals it has its
+    // collision bit set. The B head may be B[j1] (staged when it exists) only
+    // for the collision test of the tile's last A; a collision of A[i0-1]
+    // with B[j0] belongs to the previous tile.
+    const int cnt = na + nb;
+    const int nbx = nb + hn;  // readable B heads
+    const int d = tid * E < cnt ? tid * E : cnt;
+    int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sA[mid] <= sB[d - mid - 1]) lo = mid + 1;
+      else hi = mid;
+    }
+    int ai = lo, bi = d - lo;
+    const int ai0 = ai;
+    uint64_t a = ai < na ? sA[ai] : 0, b = bi < nbx ? sB[bi] : 0;
+    bool prev_eq = (ai > 0 || hp) && bi < nbx && sA[ai - 1] == b;
+    uint32_t cm = 0;  // collision bits of A[i0 + ai0 + t]
+    const uint32_t i0u = static_cast<uint32_t>(i0);
+#pragma unroll
+    for (int q = 0; q < E; ++q) {
+      if (d + q < cnt) {
+        const bool takeA = (bi >= nb) || (ai < na && a <= b);
+        const bool eq = bi < nbx && a == b;
+        if (takeA) {
+          cm |= (eq ? 1u : 0u) << (ai - ai0);
+          prev_eq = eq;
+          ++ai;
+          if (ai < na) a = sA[ai];
+        } else {
+          sLB[bi] = i0u + static_cast<uint32_t>(ai) - (prev_eq ? 1u : 0u);
+          prev_eq = false;
+          ++bi;
+          if (bi < nbx) b = sB[bi];
+        }
       }
     }
-    // the tile's last A against the first B after the tile
-    if (tid == 0 && hn && na > 0 && sA[na - 1] == sB[nb]) {
-      const int x = wbit0 + na - 1;
-      atomicOr(&sCw[x >> 5], 1u << (x & 31));
+    if (cm) {
+      const int x = wbit0 + ai0, sh = x & 31;
+      atomicOr(&sCw[x >> 5], cm << sh);
+      if (sh && (cm >> (32 - sh))) atomicOr(&sCw[(x >> 5) + 1], cm >> (32 - sh));
     }
     release_stage(empty);
     fence_proxy_async_smem();
@@ -443,39 +524,49 @@ struct CompactSpec {
   static constexpr int E = E_;
   static constexpr int S = S_;
   static constexpr int D = T * E;
-  static constexpr int NW = D / 32 + 2;  // slot-bitmap words
   static constexpr int NC = D / 32 + 4;  // collision words of one tile, at most
   static constexpr int64_t kLBBytes = align_up(int64_t(D) * 4 + 128, 16);
   static constexpr int64_t kStageBytes = kLBBytes + align_up(int64_t(NC + 4) * 4 + 64, 16);
   static constexpr int64_t kRefs = 0;
   static constexpr int64_t kOrdA = align_up(int64_t(D + 8) * 4, 16);
   static constexpr int64_t kOrdB = kOrdA + align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kBpos = kOrdB + align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kPB = kBpos + align_up(int64_t(NW) * 4, 16);
-  static constexpr int64_t kPC = kPB + align_up(int64_t(NW + 1) * 4, 16);
+  static constexpr int64_t kM = kOrdB + align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kPC = kM + align_up(int64_t(D + 1) * 4, 16);
   static constexpr int64_t kScan = kPC + align_up(int64_t(NC + 1) * 4, 16);
-  static constexpr int64_t kWorkBytes = kScan + align_up(int64_t(T / 32 + 2) * 4, 16);
-  static_assert(NW <= T && NC <= T, "one thread per bitmap word");
+  static constexpr int64_t kWorkBytes = kScan + align_up(int64_t(2 * (T / 32 + 1)) * 4, 16);
+  static_assert(NC <= T, "one thread per collision word");
   struct Params {
     int64_t m, n;
     const uint32_t *C, *dir, *lb_B;
     const int64_t *part_i;
     uint32_t *refs, *ord_A, *ord_B;
+    int32_t *status;
   };
   struct Desc {
     int64_t i0, j0, r0;
     int32_t na, nb, offLB, offC;
   };
-  __device__ static void init(uint8_t *work) {
-    uint32_t *sBpos = reinterpret_cast<uint32_t *>(work + kBpos);
-    for (int x = threadIdx.x; x < NW; x += T) sBpos[x] = 0u;
+  __device__ __forceinline__ static void init(uint8_t *work) {
+    uint32_t *sM = reinterpret_cast<uint32_t *>(work + kM);
+    for (int x = threadIdx.x; x < D + 1; x += T) sM[x] = 0u;
   }
-  __device__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
-    v[0] = __ldg(p.part_i + g);
-    v[1] = __ldg(p.part_i + g + 1);
-    v[2] = rank512_at(p.C, p.dir, v[0]);
+  // The co-ranks are clamped to their diagonals (and i1 - i0 to the tile's
+  // length), so the staged ranges stay inside the arrays whatever lb_B held.
+  __device__ __forceinline__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
+    const int64_t total = p.m + p.n;
+    const int64_t k0 = g * D, k1 = k0 + D < total ? k0 + D : total;
+    int64_t i0 = __ldg(p.part_i + g), i1 = __ldg(p.part_i + g + 1);
+    i0 = i0 < (k0 > p.n ? k0 - p.n : 0) ? (k0 > p.n ? k0 - p.n : 0) : i0;
+    i0 = i0 > (k0 < p.m ? k0 : p.m) ? (k0 < p.m ? k0 : p.m) : i0;
+    i1 = i1 < i0 ? i0 : i1;
+    i1 = i1 > i0 + (k1 - k0) ? i0 + (k1 - k0) : i1;
+    i1 = i1 > p.m ? p.m : i1;
+    i1 = i1 < k1 - p.n ? k1 - p.n : i1;
+    v[0] = i0;
+    v[1] = i1;
+    v[2] = rank512_at(p.C, p.dir, i0);
   }
-  __device__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
+  __device__ __forceinline__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
                                  Desc &d, uint64_t *full) {
     const int64_t total = p.m + p.n;
     const int64_t i0 = v[0], i1 = v[1];
@@ -502,7 +593,7 @@ struct CompactSpec {
     stage_issue(bufLB, p.lb_B, pl, full);
     stage_issue(bufC, p.C, pc, full);
   }
-  __device__ static void consume(const Params &p, int64_t g, const Desc &dd, const uint8_t *stage,
+  __device__ __forceinline__ static void consume(const Params &p, int64_t g, const Desc &dd, const uint8_t *stage,
                                  uint8_t *work, uint64_t *empty) {
     const int tid = threadIdx.x;
     const uint32_t *sLB = reinterpret_cast<const uint32_t *>(stage) + dd.offLB;
@@ -510,8 +601,7 @@ struct CompactSpec {
     uint32_t *bufRefs = reinterpret_cast<uint32_t *>(work + kRefs);
     uint32_t *bufOrdA = reinterpret_cast<uint32_t *>(work + kOrdA);
     uint32_t *bufOrdB = reinterpret_cast<uint32_t *>(work + kOrdB);
-    uint32_t *sBpos = reinterpret_cast<uint32_t *>(work + kBpos);
-    uint32_t *sPB = reinterpret_cast<uint32_t *>(work + kPB);
+    uint32_t *sM = reinterpret_cast<uint32_t *>(work + kM);
     uint32_t *sPC = reinterpret_cast<uint32_t *>(work + kPC);
     uint32_t *sScan = reinterpret_cast<uint32_t *>(work + kScan);
     const int na = dd.na, nb = dd.nb;
@@ -520,61 +610,96 @@ struct CompactSpec {
     const int64_t w0 = i0 >> 5;
     const int wbit0 = static_cast<int>(i0 - (w0 << 5));
     const int nwc = na > 0 ? static_cast<int>((((i0 + na - 1) >> 5) - w0) + 1) : 0;
-    const uint32_t i0u = static_cast<uint32_t>(i0);
+    const uint32_t i0u = static_cast<uint32_t>(i0), j0u = static_cast<uint32_t>(j0);
+    const uint32_t out0u = static_cast<uint32_t>(out0);
     const int cnt = na + nb;
     uint32_t *sRefs = bufRefs + (out0 & 3);
     uint32_t *sOrdA = bufOrdA + (i0 & 3);
     uint32_t *sOrdB = bufOrdB + (j0 & 3);
 
-    // 1. slots of the B records
+    // 1. With B first on ties, B record bi precedes tile A record a exactly
+    //    when L_bi = lb_B[j0 + bi] - i0 <= a, so the B records before A
+    //    record a number max{bi + 1 : L_bi <= a}. The last B record of each
+    //    run of equal L marks sM[L] = bi + 1; a prefix maximum over sM then
+    //    gives every A record its count. An L outside [0, na] or a falling L
+    //    means lb_B is not the lower-bound array of this merge: the tile is
+    //    skipped and the call reports LSM_ERR_ARG.
+    bool bad = false;
     for (int bi = tid; bi < nb; bi += T) {
-      const int slot = bi + static_cast<int>(sLB[bi] - i0u);
-      atomicOr(&sBpos[slot >> 5], 1u << (slot & 31));
+      const uint32_t L = sLB[bi] - i0u;
+      const uint32_t Ln = bi + 1 < nb ? sLB[bi + 1] - i0u : 0xFFFFFFFFu;
+      if (L > static_cast<uint32_t>(na) || Ln < L) bad = true;
+      else if (L < static_cast<uint32_t>(na) && Ln != L) sM[L] = static_cast<uint32_t>(bi + 1);
     }
-    const uint32_t cw_mine = tid < nwc ? sCw[tid] : 0u;
+    // collision words: bits of this tile's A records only (not those before
+    // A[i0] in the first word, nor the next tile's in the last word)
     const uint32_t cmask0 = wbit0 ? (1u << wbit0) - 1u : 0u;  // bits before A[i0]
-    named_sync(1, T);
-    // 2. prefix popcounts: slot bitmap words and collision words. Only bits
-    //    of this tile's A records count: not those before A[i0] in the first
-    //    word, nor those of the next tile's records in the last word.
-    const uint32_t pb_mine = tid < NW ? static_cast<uint32_t>(__popc(sBpos[tid])) : 0u;
-    uint32_t cw_own = cw_mine;
+    uint32_t cw_own = tid < nwc ? sCw[tid] : 0u;
     if (tid == 0) cw_own &= ~cmask0;
     const int xend = wbit0 + na;
     if (tid == nwc - 1 && (xend & 31)) cw_own &= (1u << (xend & 31)) - 1u;
-    const uint32_t pc_mine = tid < nwc ? static_cast<uint32_t>(__popc(cw_own)) : 0u;
-    uint32_t totB, totC;
-    const uint32_t exB = consumer_exclusive_sum<T>(pb_mine, sScan, &totB);
-    if (tid < NW) sPB[tid] = exB;
-    const uint32_t exC = consumer_exclusive_sum<T>(pc_mine, sScan, &totC);
+    if (named_sync_or(1, T, bad)) {
+      if (tid == 0) report(p.status, LSM_ERR_ARG);
+      release_stage(empty);
+      for (int x = tid; x < na; x += T) sM[x] = 0u;
+      named_sync(1, T);
+      return;
+    }
+    // 2. one scan: prefix popcounts of the collision words, and the prefix
+    //    maximum of sM over each thread's E consecutive A records
+    const int a0 = tid * E;
+    uint32_t mv[E];
+    uint32_t mloc = 0;
+#pragma unroll
+    for (int q = 0; q < E; ++q) {
+      mv[q] = a0 + q < na ? sM[a0 + q] : 0u;
+      mloc = mv[q] > mloc ? mv[q] : mloc;
+    }
+#pragma unroll
+    for (int q = 0; q < E; ++q)
+      if (a0 + q < na && mv[q]) sM[a0 + q] = 0u;  // clean for the next tile
+    uint32_t totC, mbefore;
+    const uint32_t exC = consumer_exclusive_sum_max<T>(
+        tid < nwc ? static_cast<uint32_t>(__popc(cw_own)) : 0u, mloc, sScan, &totC, &mbefore);
     if (tid < nwc) sPC[tid] = exC;
     named_sync(1, T);
-    // 3. every slot: its element, its output position (slot minus the A
-    //    records dropped before it) and its ordinal
-    for (int sl = tid; sl < cnt; sl += T) {
-      const int w = sl >> 5, bit = sl & 31;
-      const uint32_t bw = sBpos[w];
-      const int rb = static_cast<int>(sPB[w] + __popc(bw & ((1u << bit) - 1u)));
-      const int a = sl - rb;  // A records before this slot
-      // collision bits of tile A records [0, a): words before xa's word
-      // (prefix, first word masked) plus the bits below xa in its word
-      const int xa = wbit0 + a;
-      const int wa = xa >> 5;
-      const uint32_t cwa = a < na ? sCw[wa] : 0u;
-      int dropped_before = static_cast<int>(totC);
-      if (a < na)
-        dropped_before = static_cast<int>(sPC[wa]) + __popc(cwa & ((1u << (xa & 31)) - 1u)) -
-                         (wa == 0 ? __popc(cwa & cmask0) : 0);
-      const int outloc = sl - dropped_before;
-      if ((bw >> bit) & 1u) {
-        sRefs[outloc] = LSM_REF_FROM_B | static_cast<uint32_t>(j0 + rb);
-        sOrdB[rb] = static_cast<uint32_t>(out0 + outloc);
-      } else if ((cwa >> (xa & 31)) & 1u) {
-        sOrdA[a] = LSM_ORD_DROPPED;
-      } else {
-        sRefs[outloc] = i0u + static_cast<uint32_t>(a);
-        sOrdA[a] = static_cast<uint32_t>(out0 + outloc);
+    // collisions among tile A records [0, x), x in [0, na]
+    auto dropped_before = [&](int x) -> int {
+      if (x >= na) return static_cast<int>(totC);
+      const int xa = wbit0 + x, wa = xa >> 5;
+      const uint32_t cwa = sCw[wa];
+      return static_cast<int>(sPC[wa]) + __popc(cwa & ((1u << (xa & 31)) - 1u)) -
+             (wa == 0 ? __popc(cwa & cmask0) : 0);
+    };
+    // 3. A records: slot a + (B records before it), output slot minus the
+    //    dropped A records before it
+    if (a0 < na) {
+      int drops = dropped_before(a0);
+      uint32_t run = mbefore;
+#pragma unroll
+      for (int q = 0; q < E; ++q) {
+        const int a = a0 + q;
+        if (a < na) {
+          run = mv[q] > run ? mv[q] : run;
+          const int xa = wbit0 + a;
+          if ((sCw[xa >> 5] >> (xa & 31)) & 1u) {
+            sOrdA[a] = LSM_ORD_DROPPED;
+            ++drops;
+          } else {
+            const int ol = a + static_cast<int>(run) - drops;
+            sRefs[ol] = i0u + static_cast<uint32_t>(a);
+            sOrdA[a] = out0u + static_cast<uint32_t>(ol);
+          }
+        }
       }
+    }
+    // 4. B records: slot bi + L_bi, output slot minus the dropped A records
+    //    before it (those below L_bi)
+    for (int bi = tid; bi < nb; bi += T) {
+      const int L = static_cast<int>(sLB[bi] - i0u);
+      const int ol = bi + L - dropped_before(L);
+      sRefs[ol] = LSM_REF_FROM_B | (j0u + static_cast<uint32_t>(bi));
+      sOrdB[bi] = out0u + static_cast<uint32_t>(ol);
     }
     release_stage(empty);
     const int kept_total = cnt - static_cast<int>(totC);
@@ -583,7 +708,6 @@ struct CompactSpec {
     store_u32_run<T>(p.refs, out0, kept_total, bufRefs);
     store_u32_run<T>(p.ord_A, i0, na, bufOrdA);
     store_u32_run<T>(p.ord_B, j0, nb, bufOrdB);
-    for (int x = tid; x < NW; x += T) sBpos[x] = 0u;  // clean for the next tile
     if (tid == 0) {
       bulk_commit();
       bulk_wait_read_all();  // the buffers are rewritten by the next tile
@@ -739,12 +863,14 @@ cudaError_t launch_compact_variant(int64_t m, int64_t n, const uint32_t *C, cons
   constexpr ReplaceVariant v = kReplaceVariants[V];
   using Spec = CompactSpec<v.T, v.E, v.S>;
   constexpr int64_t D = Spec::D;
-  cudaError_t err = launch_partition(PositionsBFirst{lb_B, C, dir, m, n, d_count}, m, n, D, part_i,
-                                     nullptr, 0, s);
-  if (err != cudaSuccess) return err;
   const int64_t G = (m + n + D - 1) / D;
+  const int64_t blocks = n > 0 ? (n + kPosPerBlock - 1) / kPosPerBlock : 1;
+  partition_positions_kernel<<<static_cast<unsigned>(blocks), kPosThreads, 0, s>>>(
+      lb_B, m, n, D, G, part_i, C, dir, d_count);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
   if (G == 0) return cudaSuccess;
-  typename Spec::Params p{m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B};
+  typename Spec::Params p{m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B, status};
   profile_before(s);
   err = launch_pipeline<Spec>(p, G, status, s, device_sm_count());
   profile_after(s);

@@ -112,3 +112,19 @@ def test_timeout_probe_reports_and_context_survives(lsm):
     A = np.arange(0, 100, 2, dtype=np.uint64)
     B = np.arange(0, 100, 3, dtype=np.uint64)
     check_against_oracle(run_pipeline(lsm, A, B), A, B)
+
+
+def test_compact_rejects_lb_that_is_not_a_lower_bound_array(lsm):
+    # An lb_B that no collision mark could have produced (unsorted values)
+    # gives B records slots that collide or leave the tile: the kernel skips
+    # those tiles and records LSM_ERR_ARG; the context stays usable.
+    rng = np.random.default_rng(11)
+    m, n = 50000, 20000
+    A = np.arange(m, dtype=np.uint64) * 3
+    C = np.zeros((m + 31) // 32, np.uint32)
+    dir_, _ = lsm.rank_build(up(C), m)
+    lb = rng.integers(0, m + 1, n, dtype=np.uint64).astype(np.uint32)
+    lsm.replacement_merge_compact(m, n, up(C), dir_, up(lb))
+    assert lsm.get_device_status(reset=True) == 1   # LSM_ERR_ARG, then cleared
+    B = np.arange(n, dtype=np.uint64) * 5 + 1
+    check_against_oracle(run_pipeline(lsm, A, B), A, B)
