@@ -570,7 +570,7 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
                 lsm.tune_replace(kernel, *v)
                 _, per_v = time_pipeline(torch, stages, steps, flush)
                 res["%s %d,%d" % (label, v[0], v[1])] = per_v[label]
-            lsm.tune_replace(kernel, *lsm.REPLACE_VARIANTS[0])
+            lsm.tune_replace(kernel, *lsm.DEFAULT_REPLACE_VARIANT[kernel])
         out[name]["variant_sweep_ms"] = res
     del A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w1, w2, w3
     torch.cuda.empty_cache()

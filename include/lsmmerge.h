@@ -281,7 +281,8 @@ LSM_API int lsm_set_profile_events(void *start_event, void *stop_event);
 /* Selects the tile variant of lsm_collision_mark (kernel 0) or
  * lsm_replacement_merge_compact (kernel 1): threads per CTA and items per
  * thread, from the compiled set (256,11) (128,23) (256,23) (512,11).
- * Process-wide; the default is (256,11). */
+ * Process-wide; the defaults are (512,11) for kernel 0 and (256,11) for
+ * kernel 1. */
 LSM_API int lsm_tune_replace(int kernel, int threads, int items_per_thread);
 
 /* ---- test hook ------------------------------------------------------------ */

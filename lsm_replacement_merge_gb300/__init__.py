@@ -178,6 +178,7 @@ DEFAULT_MERGE_CONFIG = (11, 2, 1)
 
 
 REPLACE_VARIANTS = ((256, 11), (128, 23), (256, 23), (512, 11))
+DEFAULT_REPLACE_VARIANT = {0: (512, 11), 1: (256, 11)}  # kernel -> (threads, items)
 
 
 def tune_replace(kernel: int, threads: int, items_per_thread: int) -> None:

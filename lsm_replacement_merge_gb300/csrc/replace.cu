@@ -17,11 +17,12 @@
 // bulk copies while the consumer warps work on the previous one):
 //   collision_mark   partition (co-rank per tile, A first on ties; the same
 //                    launch clears C), then per tile: the stage holds
-//                    A[i0-1, i1) and B[j0, j1]; each thread bisects its own
-//                    diagonal of the tile and walks E merge steps, giving
-//                    every B key it passes its lower bound in A ([CB]: "for
-//                    each B record, find its lower bound in A") and every A
-//                    key that meets an equal B head its collision bit. Each
+//                    A[i0-1, i1) and B[j0, j1]; every B key of the tile takes
+//                    its lower bound in the staged A span ([CB]: "for each B
+//                    record, find its lower bound in A") by a two-level
+//                    search (group heads of 32 keys over the whole span, then
+//                    each key between its head's bound and the next); a
+//                    match sets the collision bit. Each
 //                    bit is set by the tile that owns its A index (the last A is
 //                    checked against the first B after the tile), so bitmap
 //                    words inside one tile take plain stores and only
@@ -389,7 +390,8 @@ struct MarkSpec {
   static constexpr int64_t kStageBytes = align_up(int64_t(D + 4) * 8 + 160, 16);
   static constexpr int64_t kLB = 0;
   static constexpr int64_t kCw = align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kWorkBytes = kCw + align_up(int64_t(D / 32 + 4) * 4, 16);
+  static constexpr int64_t kQ = kCw + align_up(int64_t(D / 32 + 4) * 4, 16);
+  static constexpr int64_t kWorkBytes = kQ + align_up(int64_t(D / 32 + 2) * 4, 16);
   struct Params {
     const uint64_t *A, *B;
     int64_t m, n;
@@ -442,55 +444,55 @@ struct MarkSpec {
     const uint64_t *sB = reinterpret_cast<const uint64_t *>(stage) + dd.offB;  // sB[nb] = B[j1]
     uint32_t *sLBbuf = reinterpret_cast<uint32_t *>(work + kLB);
     uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
+    int *sQ = reinterpret_cast<int *>(work + kQ);
     const int na = dd.na, nb = dd.nb, hp = dd.hp, hn = dd.hn;
     const int64_t i0 = dd.i0, j0 = dd.j0, i1 = i0 + na;
     uint32_t *sLB = sLBbuf + (j0 & 3);  // global alignment of lb_B[j0] mirrored
     const int64_t w0 = i0 >> 5;
     const int wbit0 = static_cast<int>(i0 - (w0 << 5));  // bit of A[i0] in word w0
-    // Merge path inside the tile, A first on ties: this thread bisects its
-    // own diagonal, then walks E merge steps. A B key taken with i A keys
-    // before it has lower bound i0 + i, less one when the element just before
-    // it is an equal A key; an A key taken while the B head equals it has its
-    // collision bit set. The B head may be B[j1] (staged when it exists) only
-    // for the collision test of the tile's last A; a collision of A[i0-1]
-    // with B[j0] belongs to the previous tile.
-    const int cnt = na + nb;
-    const int nbx = nb + hn;  // readable B heads
-    const int d = tid * E < cnt ? tid * E : cnt;
-    int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (sA[mid] <= sB[d - mid - 1]) lo = mid + 1;
-      else hi = mid;
+    // Every B key of the tile has its lower bound in the staged span
+    // A[i0 - hp, i1] (A[i0-1] included when it exists). Two levels: one
+    // thread per group of 32 consecutive B keys finds the group head's bound
+    // over the whole span; then each B key searches only between its group
+    // head's bound and the next head's. A warp's 32 lanes hold one group, so
+    // they share the range and the number of steps.
+    const uint64_t *sAx = sA - hp;
+    const int lenx = na + hp;
+    const uint32_t base = static_cast<uint32_t>(i0 - hp);
+    const int ngroups = (nb + 31) >> 5;
+    for (int q = tid; q < ngroups; q += T) {
+      const uint64_t key = sB[q << 5];
+      int lo = 0, hi = lenx;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sAx[mid] < key) lo = mid + 1;
+        else hi = mid;
+      }
+      sQ[q] = lo;
     }
-    int ai = lo, bi = d - lo;
-    const int ai0 = ai;
-    uint64_t a = ai < na ? sA[ai] : 0, b = bi < nbx ? sB[bi] : 0;
-    bool prev_eq = (ai > 0 || hp) && bi < nbx && sA[ai - 1] == b;
-    uint32_t cm = 0;  // collision bits of A[i0 + ai0 + t]
-    const uint32_t i0u = static_cast<uint32_t>(i0);
-#pragma unroll
-    for (int q = 0; q < E; ++q) {
-      if (d + q < cnt) {
-        const bool takeA = (bi >= nb) || (ai < na && a <= b);
-        const bool eq = bi < nbx && a == b;
-        if (takeA) {
-          cm |= (eq ? 1u : 0u) << (ai - ai0);
-          prev_eq = eq;
-          ++ai;
-          if (ai < na) a = sA[ai];
-        } else {
-          sLB[bi] = i0u + static_cast<uint32_t>(ai) - (prev_eq ? 1u : 0u);
-          prev_eq = false;
-          ++bi;
-          if (bi < nbx) b = sB[bi];
-        }
+    if (tid == 0) sQ[ngroups] = lenx;
+    named_sync(1, T);
+    for (int bi = tid; bi < nb; bi += T) {
+      const uint64_t key = sB[bi];
+      const int q = bi >> 5;
+      int lo = sQ[q], hi = (bi & 31) ? sQ[q + 1] : lo;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sAx[mid] < key) lo = mid + 1;
+        else hi = mid;
+      }
+      sLB[bi] = base + static_cast<uint32_t>(lo);
+      // A collision with A[i0-1] belongs to the previous tile, which finds it
+      // by peeking at this B key.
+      if (lo < lenx && lo >= hp && sAx[lo] == key) {
+        const int x = wbit0 + (lo - hp);
+        atomicOr(&sCw[x >> 5], 1u << (x & 31));
       }
     }
-    if (cm) {
-      const int x = wbit0 + ai0, sh = x & 31;
-      atomicOr(&sCw[x >> 5], cm << sh);
-      if (sh && (cm >> (32 - sh))) atomicOr(&sCw[(x >> 5) + 1], cm >> (32 - sh));
+    // the tile's last A against the first B after the tile
+    if (tid == 0 && hn && na > 0 && sA[na - 1] == sB[nb]) {
+      const int x = wbit0 + na - 1;
+      atomicOr(&sCw[x >> 5], 1u << (x & 31));
     }
     release_stage(empty);
     fence_proxy_async_smem();
@@ -724,7 +726,9 @@ struct ReplaceVariant {
   int T, E, S;
 };
 constexpr ReplaceVariant kReplaceVariants[] = {{256, 11, 2}, {128, 23, 2}, {256, 23, 2}, {512, 11, 2}};
-int g_mark_variant = 0, g_compact_variant = 0;
+// Defaults, measured on the 12M + 4M uint64 workload: (512,11) for the
+// collision mark, (256,11) for the compaction.
+int g_mark_variant = 3, g_compact_variant = 0;
 
 template <int V>
 cudaError_t launch_mark_variant(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,

@@ -128,3 +128,15 @@ def test_compact_rejects_lb_that_is_not_a_lower_bound_array(lsm):
     assert lsm.get_device_status(reset=True) == 1   # LSM_ERR_ARG, then cleared
     B = np.arange(n, dtype=np.uint64) * 5 + 1
     check_against_oracle(run_pipeline(lsm, A, B), A, B)
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("variant", [(256, 11), (128, 23), (256, 23), (512, 11)])
+def test_every_tile_variant_matches_oracle(lsm, kernel, variant):
+    inp = synth.replace_random_small(seed=41 + kernel, m=300000, n=100000, shared=25000,
+                                     universe=None)
+    lsm.tune_replace(kernel, *variant)
+    try:
+        check_against_oracle(run_pipeline(lsm, inp.A, inp.B), inp.A, inp.B)
+    finally:
+        lsm.tune_replace(kernel, *lsm.DEFAULT_REPLACE_VARIANT[kernel])
