@@ -262,16 +262,15 @@ __device__ __forceinline__ int64_t thread_corank(const Pred &pred, int64_t k, in
 // spread evenly over the open range and keeps the interval between the last
 // pivot that is too small and the first that is not, so the range shrinks
 // (L + 1)-fold per round: fewer dependent rounds of loads than bisection,
-// for L times the loads per round. Every lane of the warp must call it (the
-// ballots span the warp); a lane with active = false joins with an empty
-// range and returns its lower end.
+// for L times the loads per round. [lo, hi] is a bracket known to hold the
+// co-rank, inside [max(0, k - n), min(k, m)]. Every lane of the warp must
+// call it (the ballots span the warp); a lane with active = false joins with
+// an empty range and returns its lower end.
 template <int L, class Pred>
-__device__ __forceinline__ int64_t group_corank(const Pred &pred, int64_t k, int64_t m, int64_t n,
-                                                bool active) {
+__device__ __forceinline__ int64_t group_corank_in(const Pred &pred, int64_t k, int64_t lo,
+                                                   int64_t hi, bool active) {
   static_assert(L >= 1 && L <= 32 && (L & (L - 1)) == 0, "group size");
-  int64_t lo = k > n ? k - n : 0;
-  int64_t hi = k < m ? k : m;
-  if (!active) hi = lo;
+  if (!active || hi < lo) hi = lo;
   const int lane = threadIdx.x & 31;
   const int l = lane & (L - 1);
   const int gbase = lane & ~(L - 1);
@@ -289,6 +288,13 @@ __device__ __forceinline__ int64_t group_corank(const Pred &pred, int64_t k, int
     }
   }
   return lo;
+}
+
+// group_corank_in over the diagonal's whole range [max(0, k - n), min(k, m)].
+template <int L, class Pred>
+__device__ __forceinline__ int64_t group_corank(const Pred &pred, int64_t k, int64_t m, int64_t n,
+                                                bool active) {
+  return group_corank_in<L>(pred, k, k > n ? k - n : 0, k < m ? k : m, active);
 }
 
 }  // namespace lsm

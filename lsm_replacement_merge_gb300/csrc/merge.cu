@@ -7,8 +7,9 @@
 // listing, and "Go deeper") stages each block's spans in shared memory
 // before any thread searches; that is the design here:
 //
-//   1. partition_keys_kernel: one thread per tile boundary bisects for the
-//      co-rank of k_g = g * D in global memory.
+//   1. partition_keys_kernel: one thread per tile boundary finds the co-rank
+//      of k_g = g * D in global memory, first on a sample grid shared by all
+//      boundaries (L2-resident), then by bisection inside the bracket.
 //   2. merge_tile_kernel: a persistent, warp-specialized kernel that loops
 //      over tiles of D = 256 * E outputs. A producer warp keeps the bulk
 //      copies of the next tiles' A and B spans (keys and payloads) in flight
@@ -31,24 +32,71 @@ namespace lsm {
 
 namespace {
 
-// A_i precedes B_j in the stable merge exactly when A_i <= B_j (ties to A).
-template <typename K>
-struct KeysAFirst {
-  const K *A;
-  const K *B;
-  __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
-    return __ldg(A + i) <= __ldg(B + k - i - 1);
-  }
-};
+// Sampled co-rank (A_i precedes B_j in the stable merge exactly when
+// A_i <= B_j: ties go to A). With tens of thousands of boundaries a plain bisection
+// is bound by its scattered reads (two 32-byte sectors per level, ~27 levels
+// for 2^27 elements), not by its rounds. Here the search first runs on the
+// grid i = t s of A: at a grid point, B[k - i - 1] lies between the B grid
+// elements B[u s] and B[(u + 1) s] (u = floor((k - i - 1) / s)), so
+// A[i] <= B[u s] proves i too small and A[i] > B[(u + 1) s] proves it is
+// not. The proven-too-small grid points form a prefix (found by bisection
+// over t), and at most two grid points after it are undecided, so the
+// co-rank lies in a bracket of at most 2 s positions; a plain bisection
+// finishes inside it. Every search reads the same grid elements, which stay
+// in L2, so only the last ~log2(2 s) levels read scattered sectors. Measured
+// on 2^26 + 2^26 uint64 keys (47,663 boundaries): plain bisection 44 us;
+// with L2 flushed first (as after the previous merge) 37.5 us at s = 512
+// and 33.4 us from s = 2048 up.
+constexpr int64_t kPartitionSample = 4096;
 
-// Lanes per boundary search (group_corank); 1 is plain bisection, one
-// thread per boundary. With tens of thousands of boundaries the searches
-// are bound by random sector reads, not by their rounds, and more lanes per
-// search only add reads: bisection is fastest for this kernel.
-#ifndef LSM_MERGE_PARTITION_LANES
-#define LSM_MERGE_PARTITION_LANES 1
-#endif
-constexpr int kMergePartitionLanes = LSM_MERGE_PARTITION_LANES;
+template <typename K>
+__device__ __forceinline__ int64_t sampled_corank(const K *__restrict__ A, const K *__restrict__ B,
+                                                  int64_t k, int64_t m, int64_t n) {
+  constexpr int64_t s = kPartitionSample;
+  const int64_t lo_k = k > n ? k - n : 0, hi_k = k < m ? k : m;
+  int64_t lo = lo_k, hi = hi_k;
+  const int64_t tmin = (lo_k + s - 1) / s, tmax = hi_k / s;
+  if (hi_k > lo_k && tmin <= tmax) {
+    int64_t a = tmin, b = tmax + 1;  // proven too small on [tmin, a)
+    while (a < b) {
+      const int64_t t = (a + b) >> 1;
+      const int64_t i = t * s;
+      bool small = false;
+      if (i < hi_k) small = __ldg(A + i) <= __ldg(B + ((k - i - 1) / s) * s);
+      if (small) a = t + 1;
+      else b = t;
+    }
+    const int64_t t1 = a - 1;
+    if (t1 >= tmin) lo = t1 * s + 1;
+    // the first of the next three grid points proven not too small
+    bool big[3];
+    int64_t at[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int64_t i = (t1 + 1 + q) * s;
+      at[q] = i;
+      big[q] = false;
+      if (t1 + 1 + q <= tmax) {
+        if (i >= hi_k) {
+          big[q] = true;
+        } else {
+          int64_t ub = ((k - i - 1) / s + 1) * s;
+          if (ub > n - 1) ub = n - 1;
+          big[q] = __ldg(A + i) > __ldg(B + ub);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 2; q >= 0; --q)
+      if (big[q] && at[q] < hi) hi = at[q];
+  }
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (__ldg(A + mid) <= __ldg(B + k - mid - 1)) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
 
 template <typename K>
 __global__ void __launch_bounds__(256) partition_keys_kernel(const K *__restrict__ A, int64_t m,
@@ -56,19 +104,11 @@ __global__ void __launch_bounds__(256) partition_keys_kernel(const K *__restrict
                                                              int64_t D, int64_t G,
                                                              int64_t *__restrict__ out_i,
                                                              int64_t *__restrict__ out_ij) {
-  const int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) /
-                    kMergePartitionLanes;
-  const bool active = g <= G;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g > G) return;
   const int64_t total = m + n;
-  const int64_t k = active ? (g * D < total ? g * D : total) : 0;
-  int64_t i;
-  if constexpr (kMergePartitionLanes == 1) {
-    if (!active) return;
-    i = thread_corank(KeysAFirst<K>{A, B}, k, m, n);
-  } else {
-    i = group_corank<kMergePartitionLanes>(KeysAFirst<K>{A, B}, k, m, n, active);
-    if (!active || (threadIdx.x & (kMergePartitionLanes - 1)) != 0) return;
-  }
+  const int64_t k = g * D < total ? g * D : total;
+  const int64_t i = sampled_corank(A, B, k, m, n);
   if (out_i) out_i[g] = i;
   if (out_ij) {
     out_ij[2 * g] = i;
@@ -368,7 +408,7 @@ template <typename K>
 cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n, int64_t D,
                                    int64_t *out_i, int64_t *out_ij, cudaStream_t s) {
   const int64_t G = (m + n + D - 1) / D;
-  const int64_t blocks = ((G + 1) * kMergePartitionLanes + 255) / 256;
+  const int64_t blocks = (G + 1 + 255) / 256;
   partition_keys_kernel<K><<<static_cast<unsigned>(blocks), 256, 0, s>>>(A, m, B, n, D, G, out_i,
                                                                           out_ij);
   return cudaGetLastError();
