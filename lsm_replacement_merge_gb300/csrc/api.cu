@@ -42,6 +42,7 @@ int32_t *status_ptr() {
 
 __global__ void timeout_probe_kernel(const volatile int32_t *never_set, int64_t limit_ns,
                                      int32_t *status) {
+  pdl_begin();
   // Waits for a flag that no one writes, with the same bounded-time rule as
   // every other wait in this library.
   const uint64_t t0 = globaltimer_ns();
@@ -358,7 +359,7 @@ cudaError_t launch_timeout_probe(int64_t limit_ns, int32_t *status, cudaStream_t
   void *flag = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&flag, g_never_set_flag);
   if (e != cudaSuccess) return e;
-  timeout_probe_kernel<<<1, 32, 0, s>>>(static_cast<const volatile int32_t *>(flag), limit_ns, status);
-  return cudaGetLastError();
+  return launch_kernel(true, timeout_probe_kernel, 1, 32, 0, s,
+                       static_cast<const volatile int32_t *>(flag), limit_ns, status);
 }
 }  // namespace lsm

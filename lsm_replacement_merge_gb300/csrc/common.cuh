@@ -7,7 +7,10 @@
 // word it was given and returns, so that a stuck wait cannot hang the GPU.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
+#include <utility>
 
 #include "lsmmerge.h"
 
@@ -15,7 +18,39 @@ namespace lsm {
 
 constexpr int64_t kWaitLimitNs = 1000000000LL;  // one second
 
+// Programmatic dependent launch. Every kernel of this library starts with
+// pdl_begin(): it waits until the kernel before it on the stream has
+// finished and its writes are visible, then lets the kernel after it launch.
+// Launched with programmatic stream serialization (launch_kernel below), the
+// next kernel's launch and prologue so overlap this one's run, while every
+// kernel still sees all earlier work complete before it touches memory;
+// launched without it, the wait returns at once.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __host__ __device__ constexpr int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Launches `kern` on stream s, with programmatic stream serialization when
+// `pdl` is set (see pdl_begin). Measured on GB300: it shortens the five-launch
+// replacement step by about 5 us, and lengthens the two-launch merge step by
+// about 25 us (the merge's launches go without it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), unsigned grid, unsigned block,
+                          size_t smem, cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

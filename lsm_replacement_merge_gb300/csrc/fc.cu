@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N, uint32_t *__restrict__ lcp,
     uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec_bits, uint64_t *__restrict__ bit_off,
     uint64_t *state, uint32_t *tile_counter, int32_t *status) {
+  pdl_begin();
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t *sRefs = reinterpret_cast<uint32_t *>(smem + FcLayout::kRefs);
   uint64_t *sKb = reinterpret_cast<uint64_t *>(smem + FcLayout::kKb);
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N,
     const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
     const uint64_t *__restrict__ bit_off, uint32_t *__restrict__ payload, int64_t nwords) {
+  pdl_begin();
   using L = EmitLayout;
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t *sOut = reinterpret_cast<uint32_t *>(smem + L::kOut);
@@ -573,11 +575,12 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
                              static_cast<int>(FcLayout::kBytes));
   if (err != cudaSuccess) return err;
   profile_before(s);
-  fc_lengths_kernel<<<static_cast<unsigned>(tiles > 0 ? tiles : 1), kFcThreads, FcLayout::kBytes, s>>>(
-      make_source(in.keyA, in.valA, in.tombA), make_source(in.keyB, in.valB, in.tombB), refs, N, lcp,
-      ctrl, rec_bits, bit_off, state, counter, status);
+  err = launch_kernel(true, fc_lengths_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
+                      kFcThreads, FcLayout::kBytes, s, make_source(in.keyA, in.valA, in.tombA),
+                      make_source(in.keyB, in.valB, in.tombB), refs, N, lcp, ctrl, rec_bits,
+                      bit_off, state, counter, status);
   profile_after(s);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
@@ -593,11 +596,13 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
     configured = true;
   }
   profile_before(s);
-  fc_emit_kernel<<<static_cast<unsigned>(runs), kEmitThreads, EmitLayout::kBytes, s>>>(
-      make_source(in.keyA, in.valA, in.tombA), make_source(in.keyB, in.valB, in.tombB), refs, N, lcp,
-      ctrl, bit_off, payload, nwords);
+  const cudaError_t err = launch_kernel(true, fc_emit_kernel, static_cast<unsigned>(runs),
+                                        kEmitThreads, EmitLayout::kBytes, s,
+                                        make_source(in.keyA, in.valA, in.tombA),
+                                        make_source(in.keyB, in.valB, in.tombB), refs, N, lcp, ctrl,
+                                        bit_off, payload, nwords);
   profile_after(s);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace lsm

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(256) partition_keys_kernel(const K *__restrict
                                                              int64_t D, int64_t G,
                                                              int64_t *__restrict__ out_i,
                                                              int64_t *__restrict__ out_ij) {
+  pdl_begin();
   const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (g > G) return;
   const int64_t total = m + n;
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(kMergeThreads + 32) merge_tile_kernel(
     const K *__restrict__ A, const uint32_t *__restrict__ Apay, int64_t m, const K *__restrict__ B,
     const uint32_t *__restrict__ Bpay, int64_t n, const int64_t *__restrict__ part_i, int64_t G,
     K *__restrict__ out, uint32_t *__restrict__ out_pay, int32_t *status) {
+  pdl_begin();
   using L = MergeLayout<K, PAY, E, S, NOUT>;
   constexpr int D = L::D;
   constexpr int SZ = L::SZ;
@@ -366,10 +368,11 @@ cudaError_t launch_merge_tiles(const K *A, const uint32_t *Apay, int64_t m, cons
   if (grid < 1) grid = 1;
   if (grid > G) grid = G;
   profile_before(s);
-  kern<<<static_cast<unsigned>(grid), threads, L::kBytes, s>>>(A, Apay, m, B, Bpay, n, part_i, G, out,
-                                                                out_pay, status);
+  const cudaError_t err = launch_kernel(false, kern, static_cast<unsigned>(grid), threads,
+                                        L::kBytes, s, A, Apay, m, B, Bpay, n, part_i, G, out,
+                                        out_pay, status);
   profile_after(s);
-  return cudaGetLastError();
+  return err;
 }
 
 template <typename K, bool PAY, int C>
@@ -409,9 +412,8 @@ cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n,
                                    int64_t *out_i, int64_t *out_ij, cudaStream_t s) {
   const int64_t G = (m + n + D - 1) / D;
   const int64_t blocks = (G + 1 + 255) / 256;
-  partition_keys_kernel<K><<<static_cast<unsigned>(blocks), 256, 0, s>>>(A, m, B, n, D, G, out_i,
-                                                                          out_ij);
-  return cudaGetLastError();
+  return launch_kernel(false, partition_keys_kernel<K>, static_cast<unsigned>(blocks), 256, 0, s, A,
+                       m, B, n, D, G, out_i, out_ij);
 }
 
 }  // namespace

@@ -52,6 +52,7 @@ __device__ __forceinline__ void release_stage(uint64_t *empty) {
 template <class Spec>
 __global__ void __launch_bounds__(Spec::T + 32) tile_pipeline_kernel(typename Spec::Params p,
                                                                      int64_t G, int32_t *status) {
+  pdl_begin();
   using L = PipelineLayout<Spec>;
   constexpr int S = Spec::S;
   constexpr int T = Spec::T;
@@ -139,8 +140,8 @@ cudaError_t launch_pipeline(const typename Spec::Params &p, int64_t G, int32_t *
   int64_t grid = static_cast<int64_t>(sms) * per_sm;
   if (grid < 1) grid = 1;
   if (grid > G) grid = G;
-  kern<<<static_cast<unsigned>(grid), Spec::T + 32, L::kBytes, s>>>(p, G, status);
-  return cudaGetLastError();
+  return launch_kernel(true, kern, static_cast<unsigned>(grid), Spec::T + 32, L::kBytes, s, p, G,
+                       status);
 }
 
 // Writes global uint32 elements [g0, g0 + count) from a shared buffer that

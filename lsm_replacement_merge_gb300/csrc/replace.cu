@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, in
                                                         int64_t G, int64_t *__restrict__ out_i,
                                                         uint32_t *__restrict__ clear_words,
                                                         int64_t nclear) {
+  pdl_begin();
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (clear_words) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -101,9 +102,8 @@ cudaError_t launch_partition(const Pred &pred, int64_t m, int64_t n, int64_t D, 
   int64_t threads = (G + 1) * kPartitionLanes;
   if (clear_words && threads < nclear / 4) threads = nclear / 4;
   const int64_t blocks = (threads + 255) / 256;
-  partition_kernel<Pred><<<static_cast<unsigned>(blocks), 256, 0, s>>>(pred, m, n, D, G, out_i,
-                                                                       clear_words, nclear);
-  return cudaGetLastError();
+  return launch_kernel(true, partition_kernel<Pred>, static_cast<unsigned>(blocks), 256, 0, s, pred,
+                       m, n, D, G, out_i, clear_words, nclear);
 }
 
 // ---- rank512 --------------------------------------------------------------------
@@ -129,6 +129,7 @@ __device__ __forceinline__ void load_block_words(const uint32_t *__restrict__ C,
 __global__ void __launch_bounds__(kRankThreads) rank_count_kernel(const uint32_t *__restrict__ C,
                                                                   int64_t m,
                                                                   uint32_t *__restrict__ cta_totals) {
+  pdl_begin();
   __shared__ uint32_t scratch[kRankThreads / 32 + 1];
   const int64_t nwords = (m + 31) / 32;
   const int64_t nblk = m / 512 + 1;
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kRankThreads) rank_finish_kernel(const uint32_
                                                                    const uint32_t *__restrict__ cta_totals,
                                                                    uint32_t *__restrict__ dir,
                                                                    int64_t *__restrict__ d_total) {
+  pdl_begin();
   __shared__ uint32_t scratch[kRankThreads / 32 + 1];
   const int64_t nwords = (m + 31) / 32;
   const int64_t nblk = m / 512 + 1;
@@ -219,6 +221,7 @@ __global__ void __launch_bounds__(kPosThreads) partition_positions_kernel(
     const uint32_t *__restrict__ lb_B, int64_t m, int64_t n, int64_t D, int64_t G,
     int64_t *__restrict__ out_i, const uint32_t *__restrict__ C, const uint32_t *__restrict__ dir,
     int64_t *__restrict__ d_count) {
+  pdl_begin();
   __shared__ uint32_t sp[kPosPerBlock];
   __shared__ int64_t sRange[2];
   const int t = threadIdx.x;
@@ -285,6 +288,7 @@ __global__ void __launch_bounds__(kRankThreads) rank_single_kernel(const uint32_
                                                                    int64_t *__restrict__ d_total,
                                                                    uint64_t *state, uint32_t epoch,
                                                                    int32_t *status) {
+  pdl_begin();
   __shared__ uint32_t scratch[kRankThreads / 32 + 1];
   __shared__ uint32_t s_prefix;
   const int64_t nwords = (m + 31) / 32;
@@ -366,6 +370,7 @@ __global__ void __launch_bounds__(256) rank_query_kernel(const uint32_t *__restr
                                                          const uint32_t *__restrict__ dir, int64_t m,
                                                          const uint32_t *__restrict__ pos, int64_t q,
                                                          uint32_t *__restrict__ out, int32_t *status) {
+  pdl_begin();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= q) return;
   const int64_t p = pos[t];
@@ -784,12 +789,13 @@ cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64
                               uint32_t *cta_totals, cudaStream_t s) {
   const int64_t ctas = rank_build_ctas(m);
   profile_before(s);
-  rank_count_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(C, m, cta_totals);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_kernel(true, rank_count_kernel, static_cast<unsigned>(ctas),
+                                  kRankThreads, 0, s, C, m, cta_totals);
   if (err != cudaSuccess) return err;
-  rank_finish_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(C, m, cta_totals, dir, d_total);
+  err = launch_kernel(true, rank_finish_kernel, static_cast<unsigned>(ctas), kRankThreads, 0, s, C,
+                      m, cta_totals, dir, d_total);
   profile_after(s);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
@@ -810,10 +816,11 @@ cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, in
     uint32_t epoch = ++epoch_counter;
     if (epoch == 0) epoch = ++epoch_counter;
     profile_before(s);
-    rank_single_kernel<<<static_cast<unsigned>(ctas), kRankThreads, 0, s>>>(
-        C, m, dir, d_total, static_cast<uint64_t *>(ws), epoch, status);
+    const cudaError_t err = launch_kernel(true, rank_single_kernel, static_cast<unsigned>(ctas),
+                                          kRankThreads, 0, s, C, m, dir, d_total,
+                                          static_cast<uint64_t *>(ws), epoch, status);
     profile_after(s);
-    return cudaGetLastError();
+    return err;
   }
   return launch_rank_build(C, m, dir, d_total, static_cast<uint32_t *>(ws), s);
 }
@@ -855,8 +862,8 @@ cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                               const uint32_t *pos, int64_t q, uint32_t *out, int32_t *status,
                               cudaStream_t s) {
   if (q == 0) return cudaSuccess;
-  rank_query_kernel<<<static_cast<unsigned>((q + 255) / 256), 256, 0, s>>>(C, dir, m, pos, q, out, status);
-  return cudaGetLastError();
+  return launch_kernel(true, rank_query_kernel, static_cast<unsigned>((q + 255) / 256), 256, 0, s,
+                       C, dir, m, pos, q, out, status);
 }
 
 template <int V>
@@ -869,9 +876,8 @@ cudaError_t launch_compact_variant(int64_t m, int64_t n, const uint32_t *C, cons
   constexpr int64_t D = Spec::D;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t blocks = n > 0 ? (n + kPosPerBlock - 1) / kPosPerBlock : 1;
-  partition_positions_kernel<<<static_cast<unsigned>(blocks), kPosThreads, 0, s>>>(
-      lb_B, m, n, D, G, part_i, C, dir, d_count);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_kernel(true, partition_positions_kernel, static_cast<unsigned>(blocks),
+                                  kPosThreads, 0, s, lb_B, m, n, D, G, part_i, C, dir, d_count);
   if (err != cudaSuccess) return err;
   if (G == 0) return cudaSuccess;
   typename Spec::Params p{m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B, status};

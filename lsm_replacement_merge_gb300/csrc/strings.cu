@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int6
                                                             int64_t *__restrict__ out_i,
                                                             uint32_t *__restrict__ clear_words,
                                                             int64_t nclear) {
+  pdl_begin();
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
@@ -51,6 +52,7 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
                                                                const int64_t *__restrict__ part_i,
                                                                uint32_t *__restrict__ C,
                                                                uint32_t *__restrict__ lb_B) {
+  pdl_begin();
   constexpr int D = T * E;
   __shared__ uint32_t sLB[D];
   __shared__ uint32_t sCw[D / 32 + 4];
@@ -123,15 +125,15 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
   const int64_t nwords = (m + 31) / 32;
   int64_t threads = G + 1;
   if (threads < nwords / 4) threads = nwords / 4;
-  partition_str_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
-      StrAFirst{A, B}, m, n, D, G, part_i, C, nwords);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_kernel(true, partition_str_kernel,
+                                  static_cast<unsigned>((threads + 255) / 256), 256, 0, s,
+                                  StrAFirst{A, B}, m, n, D, G, part_i, C, nwords);
   if (err != cudaSuccess || G == 0) return err;
   profile_before(s);
-  collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>
-      <<<static_cast<unsigned>(G), kMarkStrThreads, 0, s>>>(A, m, B, n, part_i, C, lb_B);
+  err = launch_kernel(true, collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>,
+                      static_cast<unsigned>(G), kMarkStrThreads, 0, s, A, m, B, n, part_i, C, lb_B);
   profile_after(s);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace lsm

@@ -110,3 +110,27 @@ def test_prefix_tree(lsm, seed, count):
 def test_config_strings_4M(lsm):
     """The full string workload: 4,000,000 + 4,000,000 keys."""
     check_fc(lsm, synth.strings())
+
+
+def test_many_tiny_records_per_run(lsm):
+    # 3-byte keys sharing long prefixes, mostly tombstones: a dozen bits per
+    # record, so one run of 4096 payload words holds ~10,000 records and its
+    # metadata is staged in many chunks; words straddle chunk boundaries.
+    ka = [int(x).to_bytes(3, "big") for x in range(0, 120000, 2)]
+    kb = [int(x).to_bytes(3, "big") for x in range(1, 120000, 6)]
+    va = [None if x % 7 else b"" for x in range(len(ka))]
+    vb = [None if x % 5 else b"\x01" for x in range(len(kb))]
+    check_fc(lsm, synth.strings_from_lists(ka, kb, va, vb))
+
+
+def test_records_spanning_many_runs(lsm):
+    # values of 40-100 KB: a record covers several runs of 4096 words, so
+    # whole runs are composed from one record's value bytes
+    rng = np.random.default_rng(21)
+    ka = [b"k%04d" % t for t in range(0, 40, 2)]
+    kb = [b"k%04d" % t for t in range(1, 40, 4)]
+    va = [bytes(rng.integers(0, 256, int(rng.integers(40000, 100000))).astype(np.uint8)) if t % 3 == 0
+          else b"x" for t in range(len(ka))]
+    vb = [bytes(rng.integers(0, 256, 70001).astype(np.uint8)) if t % 2 else None
+          for t in range(len(kb))]
+    check_fc(lsm, synth.strings_from_lists(ka, kb, va, vb))
