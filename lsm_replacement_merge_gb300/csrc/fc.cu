@@ -415,27 +415,58 @@ __device__ __forceinline__ uint32_t be32_at(const uint8_t *arena, uint64_t t) {
   return __byte_perm(__ldg(reinterpret_cast<const uint32_t *>(arena) + t), 0, 0x0123);
 }
 
+// `len` (1..32) bits of the arena's stream starting at bit sb, right-aligned.
+__device__ __forceinline__ uint32_t arena_bits(const uint8_t *arena, uint64_t sb, int len) {
+  const uint64_t t = sb >> 5;
+  const int sh = static_cast<int>(sb & 31);
+  uint32_t v = be32_at(arena, t) << sh;
+  if (sh + len > 32) v |= be32_at(arena, t + 1) >> (32 - sh);
+  return v >> (32 - len);
+}
+
+// Copies the bits [p, p + W) of a field read from `arena` at src_bit into the
+// run's words, only where they fall in [lo, hi): a partial first word and a
+// partial last word are ORed (other fields share them); the full words in
+// between, which no other field touches, are stored. Source and destination
+// advance together, so every full word is one funnel shift of two
+// consecutive source words at a fixed offset.
 __device__ __forceinline__ void put_arena_smem(uint32_t *buf, int64_t w0, int64_t lo, int64_t hi,
                                                int64_t p, int64_t W, const uint8_t *arena,
                                                uint64_t src_bit, uint64_t /*src_end*/) {
   int64_t x = p > lo ? p : lo;
   const int64_t e = p + W < hi ? p + W : hi;
-  while (x < e) {
+  if (x >= e) return;
+  uint64_t sb = src_bit + static_cast<uint64_t>(x - p);
+  if (x & 31) {  // partial first word
     const int64_t wb = x & ~int64_t(31);
     const int64_t ce = e < wb + 32 ? e : wb + 32;
     const int len = static_cast<int>(ce - x);
-    const uint64_t sb = src_bit + static_cast<uint64_t>(x - p);
-    const uint64_t t = sb >> 5;
-    const int sh = static_cast<int>(sb & 31);
-    uint32_t v = be32_at(arena, t) << sh;
-    if (sh + len > 32) v |= be32_at(arena, t + 1) >> (32 - sh);
-    uint32_t *dst = &buf[(wb >> 5) - w0];
-    if (len == 32) {
-      *dst = v;
-    } else {
-      atomicOr(dst, (v >> (32 - len)) << (32 - static_cast<int>(x - wb) - len));
-    }
+    atomicOr(&buf[(wb >> 5) - w0], arena_bits(arena, sb, len) << (wb + 32 - ce));
+    sb += static_cast<uint64_t>(len);
     x = ce;
+  }
+  const int nfull = static_cast<int>((e - x) >> 5);
+  if (nfull > 0) {
+    uint32_t *dst = &buf[(x >> 5) - w0];
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(arena) + (sb >> 5);
+    const int sh = static_cast<int>(sb & 31);
+    uint32_t cur = __byte_perm(__ldg(src), 0, 0x0123);
+    if (sh) {
+      for (int q = 0; q < nfull; ++q) {
+        const uint32_t nxt = __byte_perm(__ldg(src + q + 1), 0, 0x0123);
+        dst[q] = __funnelshift_l(nxt, cur, sh);
+        cur = nxt;
+      }
+    } else {
+      dst[0] = cur;
+      for (int q = 1; q < nfull; ++q) dst[q] = __byte_perm(__ldg(src + q), 0, 0x0123);
+    }
+    x += int64_t(32) * nfull;
+    sb += uint64_t(32) * nfull;
+  }
+  if (x < e) {  // partial last word
+    const int len = static_cast<int>(e - x);
+    atomicOr(&buf[(x >> 5) - w0], arena_bits(arena, sb, len) << (32 - len));
   }
 }
 
