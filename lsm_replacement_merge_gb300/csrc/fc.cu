@@ -447,19 +447,21 @@ __device__ __forceinline__ void put_arena_smem(uint32_t *buf, int64_t w0, int64_
   }
   const int nfull = static_cast<int>((e - x) >> 5);
   if (nfull > 0) {
+    // batches of up to 8 words: all source loads of a batch are issued
+    // before any is used, so a field costs one load latency per batch
     uint32_t *dst = &buf[(x >> 5) - w0];
     const uint32_t *src = reinterpret_cast<const uint32_t *>(arena) + (sb >> 5);
     const int sh = static_cast<int>(sb & 31);
-    uint32_t cur = __byte_perm(__ldg(src), 0, 0x0123);
-    if (sh) {
-      for (int q = 0; q < nfull; ++q) {
-        const uint32_t nxt = __byte_perm(__ldg(src + q + 1), 0, 0x0123);
-        dst[q] = __funnelshift_l(nxt, cur, sh);
-        cur = nxt;
-      }
-    } else {
-      dst[0] = cur;
-      for (int q = 1; q < nfull; ++q) dst[q] = __byte_perm(__ldg(src + q), 0, 0x0123);
+    const int extra = sh ? 1 : 0;  // a shifted word also takes bits of the next
+    for (int q0 = 0; q0 < nfull; q0 += 8) {
+      const int cnt = nfull - q0 < 8 ? nfull - q0 : 8;
+      uint32_t w[9];
+#pragma unroll
+      for (int u = 0; u < 9; ++u)
+        w[u] = u < cnt + extra ? __byte_perm(__ldg(src + q0 + u), 0, 0x0123) : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (u < cnt) dst[q0 + u] = sh ? __funnelshift_l(w[u + 1], w[u], sh) : w[u];
     }
     x += int64_t(32) * nfull;
     sb += uint64_t(32) * nfull;
@@ -492,6 +494,14 @@ __device__ __forceinline__ void emit_record(uint32_t *buf, int64_t w0, int64_t l
   }
 }
 
+// Persistent: CTA c writes the contiguous runs [c R / P, (c + 1) R / P) of
+// kEmitRun payload words each (R runs, P CTAs). Only its first run searches
+// bit_off for the record holding the run's first bit; every run then stages
+// the metadata of kEmitMaxRec records from that record on (more chunks when
+// the run needs more), composes the records that meet the run into a shared
+// word buffer (one thread per record), and takes the record holding the
+// next run's first bit from the staged offsets. Each run leaves by one bulk
+// store.
 __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N,
     const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
@@ -508,30 +518,30 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
   uint32_t *sKl = reinterpret_cast<uint32_t *>(smem + L::kKl);
   uint32_t *sVl = reinterpret_cast<uint32_t *>(smem + L::kVl);
   uint32_t *sF = reinterpret_cast<uint32_t *>(smem + L::kF);
-  __shared__ int64_t sRange[2];
+  __shared__ int64_t sNext;  // record holding the next run's first bit
   const int tid = threadIdx.x;
-  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEmitRun;
-  const int64_t wn = nwords - w0 < kEmitRun ? nwords - w0 : kEmitRun;
-  const uint64_t total = N > 0 ? __ldg(bit_off + N) : 0;
-  const int64_t lo = w0 * 32;
-  const int64_t hi = (w0 + wn) * 32 < static_cast<int64_t>(total) ? (w0 + wn) * 32
-                                                                  : static_cast<int64_t>(total);
-  const bool any = lo < hi;
-  for (int x = tid; x < kEmitRun; x += kEmitThreads) sOut[x] = 0u;
-  if (any && tid < 64) {
-    // warp 0: record holding the run's first bit; warp 1: its last bit
-    const uint64_t bit = tid < 32 ? static_cast<uint64_t>(lo) : static_cast<uint64_t>(hi - 1);
-    const int64_t r = warp_record_at(bit_off, 0, N - 1, bit);
-    if ((tid & 31) == 0) sRange[tid >> 5] = r;
+  const int64_t runs = (nwords + kEmitRun - 1) / kEmitRun;
+  const int64_t P = gridDim.x;
+  const int64_t ra = blockIdx.x * runs / P, rb = (blockIdx.x + 1) * runs / P;
+  const int64_t total = N > 0 ? static_cast<int64_t>(__ldg(bit_off + N)) : 0;
+  if (ra < rb && tid < 32) {
+    const int64_t lo0 = ra * kEmitRun * 32;
+    int64_t r = 0;
+    if (lo0 < total) r = warp_record_at(bit_off, 0, N - 1, static_cast<uint64_t>(lo0));
+    if (tid == 0) sNext = r;
   }
-  __syncthreads();
-  if (any) {
-    const int64_t r0 = sRange[0], r1 = sRange[1];
-    // records r0..r1, kEmitMaxRec at a time: gather their metadata in one
-    // parallel pass, then one thread per record writes its bits
-    for (int64_t c0 = r0; c0 <= r1; c0 += kEmitMaxRec) {
-      const int64_t R = r1 - c0 + 1 < kEmitMaxRec ? r1 - c0 + 1 : kEmitMaxRec;
-      for (int64_t x = tid; x < R; x += kEmitThreads) {
+  for (int64_t run = ra; run < rb; ++run) {
+    const int64_t w0 = run * kEmitRun;
+    const int64_t wn = nwords - w0 < kEmitRun ? nwords - w0 : kEmitRun;
+    const int64_t lo = w0 * 32;
+    const int64_t hi = (w0 + wn) * 32 < total ? (w0 + wn) * 32 : total;
+    for (int x = tid; x < kEmitRun; x += kEmitThreads) sOut[x] = 0u;
+    __syncthreads();  // sNext is set and sOut is clear
+    int64_t c0 = sNext;
+    while (lo < hi) {
+      // records c0 .. c0 + R - 1, the first holding bit max(lo, ...) of this run
+      const int R = static_cast<int>(N - c0 < kEmitMaxRec ? N - c0 : kEmitMaxRec);
+      for (int x = tid; x < R; x += kEmitThreads) {
         const int64_t r = c0 + x;
         sS[x] = __ldg(bit_off + r);
         if (x == R - 1) sS[R] = __ldg(bit_off + r + 1);
@@ -554,7 +564,7 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
         sF[x] = ((ref & LSM_REF_FROM_B) ? kFlagFromB : 0u) | (tomb ? kFlagTomb : 0u);
       }
       __syncthreads();
-      for (int64_t x = tid; x < R; x += kEmitThreads) {
+      for (int x = tid; x < R && static_cast<int64_t>(sS[x]) < hi; x += kEmitThreads) {
         RecordMeta M;
         M.s = static_cast<int64_t>(sS[x]);
         M.e = static_cast<int64_t>(sS[x + 1]);
@@ -568,18 +578,32 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
         M.val = KeyRef{src.val.arena, sVb[x], sVb[x] + sVl[x]};
         emit_record(sOut, w0, lo, hi, M);
       }
-      __syncthreads();
+      const bool more = static_cast<int64_t>(sS[R]) < hi && c0 + R < N;
+      if (!more && tid == 0) {
+        // the record holding bit hi: the first staged record ending past it
+        int a = 0, b = R;
+        while (a < b) {
+          const int mid = (a + b) >> 1;
+          if (static_cast<int64_t>(sS[mid + 1]) <= hi) a = mid + 1;
+          else b = mid;
+        }
+        sNext = c0 + (a < R ? a : R - 1);
+      }
+      __syncthreads();  // the chunk's metadata is free for the next chunk
+      if (!more) break;
+      c0 += R;
     }
+    fence_proxy_async_smem();
+    __syncthreads();
+    const int bulk_words = static_cast<int>(wn) & ~3;
+    if (tid == 0) {
+      if (bulk_words) bulk_s2g(payload + w0, sOut, static_cast<uint32_t>(bulk_words) * 4);
+      bulk_commit();
+    }
+    for (int x = bulk_words + tid; x < wn; x += kEmitThreads) payload[w0 + x] = sOut[x];
+    if (tid == 0) bulk_wait_read_all();
+    __syncthreads();  // the store has read sOut before the next run clears it
   }
-  fence_proxy_async_smem();
-  __syncthreads();
-  const int bulk_words = static_cast<int>(wn) & ~3;
-  if (tid == 0) {
-    if (bulk_words) bulk_s2g(payload + w0, sOut, static_cast<uint32_t>(bulk_words) * 4);
-    bulk_commit();
-  }
-  for (int x = bulk_words + tid; x < wn; x += kEmitThreads) payload[w0 + x] = sOut[x];
-  if (tid == 0) bulk_wait_read_all();
 }
 
 Source make_source(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb) {
@@ -626,8 +650,19 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
     if (err != cudaSuccess) return err;
     configured = true;
   }
+  static int per_sm = 0;
+  if (!per_sm) {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fc_emit_kernel, kEmitThreads,
+                                                      EmitLayout::kBytes) != cudaSuccess)
+      v = 1;
+    per_sm = v > 0 ? v : 1;
+  }
+  int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
+  if (grid < 1) grid = 1;
+  if (grid > runs) grid = runs;
   profile_before(s);
-  const cudaError_t err = launch_kernel(true, fc_emit_kernel, static_cast<unsigned>(runs),
+  const cudaError_t err = launch_kernel(true, fc_emit_kernel, static_cast<unsigned>(grid),
                                         kEmitThreads, EmitLayout::kBytes, s,
                                         make_source(in.keyA, in.valA, in.tombA),
                                         make_source(in.keyB, in.valB, in.tombB), refs, N, lcp, ctrl,
