@@ -542,6 +542,7 @@ struct CompactSpec {
   static constexpr int64_t kScan = kPC + align_up(int64_t(NC + 1) * 4, 16);
   static constexpr int64_t kWorkBytes = kScan + align_up(int64_t(2 * (T / 32 + 1)) * 4, 16);
   static_assert(NC <= T, "one thread per collision word");
+  static_assert(E <= 32, "a thread's collision bits fit one 64-bit window");
   struct Params {
     int64_t m, n;
     const uint32_t *C, *dir, *lb_B;
@@ -683,20 +684,21 @@ struct CompactSpec {
     if (a0 < na) {
       int drops = dropped_before(a0);
       uint32_t run = mbefore;
+      // the collision bits of this thread's E records (E <= 32): one 64-bit
+      // window over the two words they span; bit q belongs to record a0 + q
+      const int xa0 = wbit0 + a0;
+      const uint64_t win =
+          ((static_cast<uint64_t>(sCw[(xa0 >> 5) + 1]) << 32) | sCw[xa0 >> 5]) >> (xa0 & 31);
+      const int lim = na - a0 < E ? na - a0 : E;
 #pragma unroll
       for (int q = 0; q < E; ++q) {
-        const int a = a0 + q;
-        if (a < na) {
+        if (q < lim) {
           run = mv[q] > run ? mv[q] : run;
-          const int xa = wbit0 + a;
-          if ((sCw[xa >> 5] >> (xa & 31)) & 1u) {
-            sOrdA[a] = LSM_ORD_DROPPED;
-            ++drops;
-          } else {
-            const int ol = a + static_cast<int>(run) - drops;
-            sRefs[ol] = i0u + static_cast<uint32_t>(a);
-            sOrdA[a] = out0u + static_cast<uint32_t>(ol);
-          }
+          const bool dropped = (win >> q) & 1u;
+          const int ol = a0 + q + static_cast<int>(run) - drops;
+          if (!dropped) sRefs[ol] = i0u + static_cast<uint32_t>(a0 + q);
+          sOrdA[a0 + q] = dropped ? LSM_ORD_DROPPED : out0u + static_cast<uint32_t>(ol);
+          drops += dropped ? 1 : 0;
         }
       }
     }
