@@ -34,8 +34,9 @@ __host__ __device__ constexpr int64_t align_up(int64_t x, int64_t a) { return (x
 
 // Launches `kern` on stream s, with programmatic stream serialization when
 // `pdl` is set (see pdl_begin). Measured on GB300: it shortens the five-launch
-// replacement step by about 5 us, and lengthens the two-launch merge step by
-// about 25 us (the merge's launches go without it).
+// replacement step by about 6 us, and lengthens the merge step by about 25 us
+// and the string + FC step by about 90 us, where a kernel launched early holds
+// SM room that the waves of the one before it need (those launch without it).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), unsigned grid, unsigned block,
                           size_t smem, cudaStream_t s, Args &&...args) {

@@ -15,18 +15,19 @@
 // EG0(x) is the order-0 Exp-Golomb code word: floor(log2(x+1)) zero bits,
 // then x+1 in binary; as a number of E(x) bits it is simply x + 1.
 //
-// fc_lengths_kernel: one CTA per tile of 2048 records (tile ids taken in
-// launch order from a counter). Each thread computes eight consecutive
-// records; a block scan and a decoupled lookback over the tiles turn the
-// lengths into 64-bit offsets in a single pass. Each lookback wait is
-// bounded in time; a tile that gives up records LSM_ERR_TIMEOUT and still
-// publishes, so no other tile waits on it forever.
+// fc_lengths_kernel: one CTA per tile of 1024 records; four consecutive
+// records per thread: LCP, control, record length; the tile's total goes to
+// the workspace. fc_tile_scan_kernel (one CTA) turns the tile totals into
+// exclusive prefixes, and fc_offsets_kernel adds each tile's prefix to a
+// block scan of its record lengths to write the 64-bit bit offsets. (A
+// single pass with a decoupled lookback was measured slower: tiles finish
+// out of order and a finished tile waits for its predecessors' totals.)
 //
-// fc_emit_kernel: one CTA owns a run of 4096 payload words (the word-owned
-// emit at CTA granularity: every global word is written once, by the CTA
-// that owns it). Two warps find the first and last record overlapping the
-// run (32-way probes over bit_off); the CTA gathers those records'
-// metadata into shared memory in one parallel pass; then one thread per
+// fc_emit_kernel: persistent; each CTA writes a contiguous range of runs of
+// 4096 payload words (the word-owned emit at CTA granularity: every global
+// word is written once, by the CTA that owns it). The CTA's first run finds
+// its first record by 32-way probes over bit_off; every run stages the
+// metadata of the records from there in shared memory, one thread per
 // record writes the record's fields into the run's word buffer in shared
 // memory (words shared by two fields or records are ORed, words inside a
 // key or value field are stored whole), and the run leaves with one bulk
@@ -68,61 +69,6 @@ __device__ __forceinline__ bool is_tomb(const Source &s, uint32_t idx) {
   return s.tomb && ((__ldg(s.tomb + (idx >> 5)) >> (idx & 31)) & 1u);
 }
 
-// ---- lookback state ------------------------------------------------------------
-constexpr uint64_t kFlagAgg = uint64_t(1) << 62;
-constexpr uint64_t kFlagInc = uint64_t(2) << 62;
-constexpr uint64_t kValMask = (uint64_t(1) << 62) - 1;
-
-
-template <typename V>
-__device__ __forceinline__ V warp_sum(V v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Called by warp 0 of tile t with the tile's aggregate; returns the sum of
-// all earlier tiles (to every lane).
-__device__ uint64_t lookback(uint64_t *state, uint32_t t, uint64_t agg, int32_t *status) {
-  const int lane = threadIdx.x & 31;
-  if (t == 0) {
-    if (lane == 0) st_relaxed_u64(state, kFlagInc | agg);
-    return 0;
-  }
-  if (lane == 0) st_relaxed_u64(state + t, kFlagAgg | agg);
-  uint64_t prefix = 0;
-  int64_t base = static_cast<int64_t>(t) - 1;
-  const uint64_t t0 = globaltimer_ns();
-  bool timed_out = false;
-  for (;;) {
-    const int64_t idx = base - lane;
-    uint64_t v = idx >= 0 ? ld_relaxed_u64(state + idx) : kFlagInc;
-    uint32_t polls = 0;
-    while (!__all_sync(0xffffffffu, (v >> 62) != 0)) {
-      if ((v >> 62) == 0) v = ld_relaxed_u64(state + idx);
-      if ((++polls & 31) == 0) {
-        const bool late = globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs);
-        if (__any_sync(0xffffffffu, late)) {
-          timed_out = true;
-          if ((v >> 62) == 0) v = kFlagInc;  // give up: count the missing tile as zero
-        }
-      }
-    }
-    const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 62) == 2);
-    if (inc) {
-      const int first = __ffs(inc) - 1;  // nearest tile that has its inclusive prefix
-      prefix += warp_sum<uint64_t>(lane <= first ? (v & kValMask) : 0);
-      break;
-    }
-    prefix += warp_sum<uint64_t>(v & kValMask);
-    base -= 32;
-  }
-  if (lane == 0) {
-    if (timed_out) report(status, LSM_ERR_TIMEOUT);
-    st_relaxed_u64(state + t, kFlagInc | ((prefix + agg) & kValMask));
-  }
-  return prefix;
-}
 
 struct FcLayout {
   static constexpr int64_t kRefs = 0;                                   // u32[tile + 1]
@@ -133,8 +79,7 @@ struct FcLayout {
   static constexpr int64_t kLcp = align_up(kSrc + kFcTile + 1, 16);     // u32[tile]
   static constexpr int64_t kCtrl = kLcp + kFcTile * 4;
   static constexpr int64_t kRec = kCtrl + kFcTile * 4;
-  static constexpr int64_t kOff = kRec + kFcTile * 4;                   // u64[tile]
-  static constexpr int64_t kScan = kOff + kFcTile * 8;                  // u64[T/32 + 1]
+  static constexpr int64_t kScan = align_up(kRec + kFcTile * 4, 16);   // u64[T/32 + 1]
   static constexpr int64_t kBytes = kScan + (kFcThreads / 32 + 2) * 8 + 16;
 };
 
@@ -172,12 +117,12 @@ __device__ __forceinline__ uint64_t bit_lcp(const uint8_t *aa, uint64_t ab, uint
 // One tile of 1024 records per CTA, in phases whose loads are independent
 // across records: (1) the refs, (2) every record's key offsets, value bits
 // and source, (3) each thread's four consecutive records: bit LCP with the
-// predecessor, control, record length; then a block scan and a decoupled
-// lookback over tiles turn lengths into bit offsets.
+// predecessor, control, record length; the tile's total is written for the
+// offset scan.
 __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N, uint32_t *__restrict__ lcp,
     uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec_bits, uint64_t *__restrict__ bit_off,
-    uint64_t *state, uint32_t *tile_counter, int32_t *status) {
+    uint64_t *tile_sum, int32_t *status) {
   pdl_begin();
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t *sRefs = reinterpret_cast<uint32_t *>(smem + FcLayout::kRefs);
@@ -188,18 +133,13 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   uint32_t *sLcp = reinterpret_cast<uint32_t *>(smem + FcLayout::kLcp);
   uint32_t *sCtrl = reinterpret_cast<uint32_t *>(smem + FcLayout::kCtrl);
   uint32_t *sRec = reinterpret_cast<uint32_t *>(smem + FcLayout::kRec);
-  uint64_t *sOff = reinterpret_cast<uint64_t *>(smem + FcLayout::kOff);
   uint64_t *sScan = reinterpret_cast<uint64_t *>(smem + FcLayout::kScan);
-  __shared__ uint32_t s_tile;
-  __shared__ uint64_t s_prefix;
   const int tid = threadIdx.x;
   if (N == 0) {
     if (tid == 0) bit_off[0] = 0;
     return;
   }
-  if (tid == 0) s_tile = atomicAdd(tile_counter, 1u);
-  __syncthreads();
-  const uint32_t t = s_tile;
+  const uint32_t t = blockIdx.x;
   const int64_t start = static_cast<int64_t>(t) * kFcTile;
   const int cnt = static_cast<int>(N - start < kFcTile ? N - start : kFcTile);
   // slot x holds record start - 1 + x (slot 0: the predecessor, if any)
@@ -311,31 +251,76 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
     sLcp[b0 + q] = static_cast<uint32_t>(l);
     sCtrl[b0 + q] = static_cast<uint32_t>(c);
     sRec[b0 + q] = static_cast<uint32_t>(Lrec);
-    sOff[b0 + q] = Lrec;  // length for now, offset after the scan
     sum += Lrec;
   }
   if (overflow) report(status, LSM_ERR_OVERFLOW);
-  uint64_t agg;
-  const uint64_t excl = block_exclusive_sum<kFcThreads, uint64_t>(sum, sScan, &agg);
-  if (tid < 32) {
-    const uint64_t p = lookback(state, t, agg, status);
-    if (tid == 0) s_prefix = p;
-  }
-  __syncthreads();
-  uint64_t run = s_prefix + excl;
-  for (int q = 0; q < kFcItems && b0 + q < cnt; ++q) {
-    const uint64_t L = sOff[b0 + q];
-    sOff[b0 + q] = run;
-    run += L;
-  }
-  __syncthreads();
+  const uint64_t agg = block_sum<kFcThreads, uint64_t>(sum, sScan);
+  if (tid == 0) tile_sum[t] = agg;
   for (int x = tid; x < cnt; x += kFcThreads) {
     lcp[start + x] = sLcp[x];
     ctrl[start + x] = sCtrl[x];
     rec_bits[start + x] = sRec[x];
-    bit_off[start + x] = sOff[x];
   }
-  if (start + cnt == N && tid == 0) bit_off[N] = s_prefix + agg;
+}
+
+// The exclusive prefix sums of the tile totals, in place, by one CTA in
+// chunks of kScanThreads * 8; tile_sum[tiles] receives the grand total.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) fc_tile_scan_kernel(uint64_t *tile_sum,
+                                                                    int64_t tiles) {
+  pdl_begin();
+  __shared__ uint64_t scratch[kScanThreads / 32 + 1];
+  const int tid = threadIdx.x;
+  uint64_t carry = 0;
+  for (int64_t base = 0; base < tiles; base += kScanThreads * 8) {
+    uint64_t v[8];
+    uint64_t local = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t idx = base + int64_t(tid) * 8 + u;
+      v[u] = idx < tiles ? tile_sum[idx] : 0;
+      local += v[u];
+    }
+    uint64_t total;
+    uint64_t run = carry + block_exclusive_sum<kScanThreads, uint64_t>(local, scratch, &total);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t idx = base + int64_t(tid) * 8 + u;
+      if (idx < tiles) tile_sum[idx] = run;
+      run += v[u];
+    }
+    carry += total;
+  }
+  if (tid == 0) tile_sum[tiles] = carry;
+}
+
+// bit_off for tile t: its exclusive tile prefix plus a block scan of its
+// records' lengths; the last tile also writes bit_off[N], the total.
+__global__ void __launch_bounds__(kFcThreads) fc_offsets_kernel(const uint32_t *__restrict__ rec_bits,
+                                                                int64_t N, const uint64_t *tile_sum,
+                                                                int64_t tiles,
+                                                                uint64_t *__restrict__ bit_off) {
+  pdl_begin();
+  __shared__ uint64_t scratch[kFcThreads / 32 + 1];
+  const int tid = threadIdx.x;
+  const int64_t t = blockIdx.x;
+  const int64_t start = t * kFcTile;
+  const int64_t b0 = start + int64_t(tid) * kFcItems;
+  uint32_t r[kFcItems];
+  uint64_t local = 0;
+#pragma unroll
+  for (int q = 0; q < kFcItems; ++q) {
+    r[q] = b0 + q < N ? __ldg(rec_bits + b0 + q) : 0u;
+    local += r[q];
+  }
+  uint64_t total;
+  uint64_t run = tile_sum[t] + block_exclusive_sum<kFcThreads, uint64_t>(local, scratch, &total);
+#pragma unroll
+  for (int q = 0; q < kFcItems; ++q) {
+    if (b0 + q < N) bit_off[b0 + q] = run;
+    run += r[q];
+  }
+  if (t == tiles - 1 && tid == 0) bit_off[N] = tile_sum[tiles];
 }
 
 // ---- emit ------------------------------------------------------------------------
@@ -622,19 +607,22 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
                                    uint32_t *lcp, uint32_t *ctrl, uint32_t *rec_bits,
                                    uint64_t *bit_off, void *ws, int32_t *status, cudaStream_t s) {
   const int64_t tiles = fc_scan_tiles(N);
-  uint32_t *counter = static_cast<uint32_t *>(ws);
-  uint64_t *state = reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(ws) + 256);
-  cudaError_t err = cudaMemsetAsync(ws, 0, fc_scan_workspace_bytes(N), s);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(fc_lengths_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(FcLayout::kBytes));
+  uint64_t *tile_sum = static_cast<uint64_t *>(ws);  // tiles + 1 entries
+  cudaError_t err = cudaFuncSetAttribute(fc_lengths_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(FcLayout::kBytes));
   if (err != cudaSuccess) return err;
   profile_before(s);
-  err = launch_kernel(true, fc_lengths_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
+  err = launch_kernel(false, fc_lengths_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
                       kFcThreads, FcLayout::kBytes, s, make_source(in.keyA, in.valA, in.tombA),
                       make_source(in.keyB, in.valB, in.tombB), refs, N, lcp, ctrl, rec_bits,
-                      bit_off, state, counter, status);
-  profile_after(s);
+                      bit_off, tile_sum, status);
+  if (err == cudaSuccess && N > 0)
+    err = launch_kernel(false, fc_tile_scan_kernel, 1u, kScanThreads, 0, s, tile_sum, tiles);
+  if (err == cudaSuccess && N > 0)
+    err = launch_kernel(false, fc_offsets_kernel, static_cast<unsigned>(tiles), kFcThreads, 0, s,
+                        rec_bits, N, tile_sum, tiles, bit_off);
+  profile_after(s);  // the profiled span covers all three launches
   return err;
 }
 
@@ -662,7 +650,7 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
   if (grid < 1) grid = 1;
   if (grid > runs) grid = runs;
   profile_before(s);
-  const cudaError_t err = launch_kernel(true, fc_emit_kernel, static_cast<unsigned>(grid),
+  const cudaError_t err = launch_kernel(false, fc_emit_kernel, static_cast<unsigned>(grid),
                                         kEmitThreads, EmitLayout::kBytes, s,
                                         make_source(in.keyA, in.valA, in.tombA),
                                         make_source(in.keyB, in.valB, in.tombB), refs, N, lcp, ctrl,

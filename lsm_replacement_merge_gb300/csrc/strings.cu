@@ -125,12 +125,12 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
   const int64_t nwords = (m + 31) / 32;
   int64_t threads = G + 1;
   if (threads < nwords / 4) threads = nwords / 4;
-  cudaError_t err = launch_kernel(true, partition_str_kernel,
+  cudaError_t err = launch_kernel(false, partition_str_kernel,
                                   static_cast<unsigned>((threads + 255) / 256), 256, 0, s,
                                   StrAFirst{A, B}, m, n, D, G, part_i, C, nwords);
   if (err != cudaSuccess || G == 0) return err;
   profile_before(s);
-  err = launch_kernel(true, collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>,
+  err = launch_kernel(false, collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>,
                       static_cast<unsigned>(G), kMarkStrThreads, 0, s, A, m, B, n, part_i, C, lb_B);
   profile_after(s);
   return err;
