@@ -296,29 +296,48 @@ __global__ void __launch_bounds__(kScanThreads) fc_tile_scan_kernel(uint64_t *ti
 
 // bit_off for tile t: its exclusive tile prefix plus a block scan of its
 // records' lengths; the last tile also writes bit_off[N], the total.
-__global__ void __launch_bounds__(kFcThreads) fc_offsets_kernel(const uint32_t *__restrict__ rec_bits,
-                                                                int64_t N, const uint64_t *tile_sum,
-                                                                int64_t tiles,
-                                                                uint64_t *__restrict__ bit_off) {
+__global__ void __launch_bounds__(kFcThreads) fc_offsets_kernel(
+    const uint32_t *__restrict__ rec_bits, int64_t N, const uint64_t *tile_sum, int64_t tiles,
+    uint64_t *__restrict__ bit_off) {
   pdl_begin();
   __shared__ uint64_t scratch[kFcThreads / 32 + 1];
   const int tid = threadIdx.x;
   const int64_t t = blockIdx.x;
   const int64_t start = t * kFcTile;
   const int64_t b0 = start + int64_t(tid) * kFcItems;
-  uint32_t r[kFcItems];
-  uint64_t local = 0;
+  static_assert(kFcItems == 4, "one 16-byte load of lengths per thread");
+  // 16-byte accesses when both arrays allow them (a full group of four)
+  const uintptr_t addr_bits =
+      reinterpret_cast<uintptr_t>(rec_bits) | reinterpret_cast<uintptr_t>(bit_off);
+  const bool vec = b0 + 4 <= N && (addr_bits & 15) == 0;
+  uint32_t r[4];
+  if (vec) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(rec_bits + b0));
+    r[0] = v.x;
+    r[1] = v.y;
+    r[2] = v.z;
+    r[3] = v.w;
+  } else {
 #pragma unroll
-  for (int q = 0; q < kFcItems; ++q) {
-    r[q] = b0 + q < N ? __ldg(rec_bits + b0 + q) : 0u;
-    local += r[q];
+    for (int q = 0; q < 4; ++q) r[q] = b0 + q < N ? __ldg(rec_bits + b0 + q) : 0u;
   }
+  const uint64_t local = uint64_t(r[0]) + r[1] + r[2] + r[3];
   uint64_t total;
   uint64_t run = tile_sum[t] + block_exclusive_sum<kFcThreads, uint64_t>(local, scratch, &total);
+  uint64_t o[4];
 #pragma unroll
-  for (int q = 0; q < kFcItems; ++q) {
-    if (b0 + q < N) bit_off[b0 + q] = run;
+  for (int q = 0; q < 4; ++q) {
+    o[q] = run;
     run += r[q];
+  }
+  if (vec) {
+    ulonglong2 *dst = reinterpret_cast<ulonglong2 *>(bit_off + b0);
+    dst[0] = make_ulonglong2(o[0], o[1]);
+    dst[1] = make_ulonglong2(o[2], o[3]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (b0 + q < N) bit_off[b0 + q] = o[q];
   }
   if (t == tiles - 1 && tid == 0) bit_off[N] = tile_sum[tiles];
 }
