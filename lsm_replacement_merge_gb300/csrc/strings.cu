@@ -30,6 +30,13 @@ struct StrAFirst {
   }
 };
 
+// Lanes per boundary search (group_corank): each round of a string search
+// is two dependent loads (offsets, then key bytes), so the rounds dominate.
+#ifndef LSM_STR_PARTITION_LANES
+#define LSM_STR_PARTITION_LANES 4
+#endif
+constexpr int kStrPartitionLanes = LSM_STR_PARTITION_LANES;
+
 __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int64_t m, int64_t n,
                                                             int64_t D, int64_t G,
                                                             int64_t *__restrict__ out_i,
@@ -39,11 +46,12 @@ __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int6
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
-  const int64_t g = gtid;
-  if (g > G) return;
+  const int64_t g = gtid / kStrPartitionLanes;
+  const bool active = g <= G;
   const int64_t total = m + n;
-  const int64_t k = g * D < total ? g * D : total;
-  out_i[g] = thread_corank(pred, k, m, n);
+  const int64_t k = active ? (g * D < total ? g * D : total) : 0;
+  const int64_t i = group_corank<kStrPartitionLanes>(pred, k, m, n, active);
+  if (active && (threadIdx.x & (kStrPartitionLanes - 1)) == 0) out_i[g] = i;
 }
 
 template <int T, int E>
@@ -123,7 +131,7 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
   constexpr int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t nwords = (m + 31) / 32;
-  int64_t threads = G + 1;
+  int64_t threads = (G + 1) * kStrPartitionLanes;
   if (threads < nwords / 4) threads = nwords / 4;
   cudaError_t err = launch_kernel(false, partition_str_kernel,
                                   static_cast<unsigned>((threads + 255) / 256), 256, 0, s,
