@@ -545,27 +545,50 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     while (lo < hi) {
       // records c0 .. c0 + R - 1, the first holding bit max(lo, ...) of this run
       const int R = static_cast<int>(N - c0 < kEmitMaxRec ? N - c0 : kEmitMaxRec);
-      for (int x = tid; x < R; x += kEmitThreads) {
-        const int64_t r = c0 + x;
-        sS[x] = __ldg(bit_off + r);
-        if (x == R - 1) sS[R] = __ldg(bit_off + r + 1);
-        sC[x] = __ldg(ctrl + r);
-        sL[x] = __ldg(lcp + r);
-        const uint32_t ref = __ldg(refs + r);
-        const uint32_t idx = ref & ~LSM_REF_FROM_B;
-        const Source &src = pick(sa, sb, ref);
-        const uint64_t kb = __ldg(src.key.off + idx), ke = __ldg(src.key.off + idx + 1);
-        const bool tomb = is_tomb(src, idx);
-        uint64_t vb = 0, ve = 0;
-        if (!tomb) {
-          vb = __ldg(src.val.off + idx);
-          ve = __ldg(src.val.off + idx + 1);
+      // two records per thread per round; every load of a round is issued
+      // before any is used (the value offsets are read for tombstones too,
+      // which keeps them off the tombstone bit's dependency chain)
+      for (int x0 = tid; x0 < R; x0 += 2 * kEmitThreads) {
+        uint32_t ref[2];
+        uint64_t bo[2];
+        uint32_t cc[2], ll[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int x = x0 + u * kEmitThreads;
+          const int64_t r = c0 + (x < R ? x : x0);
+          ref[u] = __ldg(refs + r);
+          bo[u] = __ldg(bit_off + r);
+          cc[u] = __ldg(ctrl + r);
+          ll[u] = __ldg(lcp + r);
         }
-        sKb[x] = kb;
-        sKl[x] = static_cast<uint32_t>(ke - kb);
-        sVb[x] = vb;
-        sVl[x] = static_cast<uint32_t>(ve - vb);
-        sF[x] = ((ref & LSM_REF_FROM_B) ? kFlagFromB : 0u) | (tomb ? kFlagTomb : 0u);
+        uint64_t kb[2], ke[2], vb[2], ve[2];
+        uint32_t tw[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t idx = ref[u] & ~LSM_REF_FROM_B;
+          const Source &src = pick(sa, sb, ref[u]);
+          kb[u] = __ldg(src.key.off + idx);
+          ke[u] = __ldg(src.key.off + idx + 1);
+          vb[u] = __ldg(src.val.off + idx);
+          ve[u] = __ldg(src.val.off + idx + 1);
+          tw[u] = src.tomb ? __ldg(src.tomb + (idx >> 5)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int x = x0 + u * kEmitThreads;
+          if (x >= R) continue;
+          const uint32_t idx = ref[u] & ~LSM_REF_FROM_B;
+          const bool tomb = (tw[u] >> (idx & 31)) & 1u;
+          sS[x] = bo[u];
+          if (x == R - 1) sS[R] = __ldg(bit_off + c0 + x + 1);
+          sC[x] = cc[u];
+          sL[x] = ll[u];
+          sKb[x] = kb[u];
+          sKl[x] = static_cast<uint32_t>(ke[u] - kb[u]);
+          sVb[x] = tomb ? 0 : vb[u];
+          sVl[x] = tomb ? 0u : static_cast<uint32_t>(ve[u] - vb[u]);
+          sF[x] = ((ref[u] & LSM_REF_FROM_B) ? kFlagFromB : 0u) | (tomb ? kFlagTomb : 0u);
+        }
       }
       __syncthreads();
       for (int x = tid; x < R && static_cast<int64_t>(sS[x]) < hi; x += kEmitThreads) {
