@@ -155,9 +155,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ---- staging a 1-D span into shared memory ----------------------------------
 // Global elements [s, s + c) of size SZ (array base 16-byte aligned) land in
 // a 16-byte aligned shared buffer so that element s + x sits at buf[lead + x].
-// The 16-byte aligned interior [alo, ahi) moves with one bulk copy; the at
-// most 16/SZ - 1 elements after ahi move with plain loads (stage_tail), so
-// nothing past s + c is ever read.
+// A 16-byte aligned range [alo, ahi) moves with one bulk copy; elements of
+// the span past ahi (at most 16/SZ - 1, and only at the end of the array)
+// move with plain loads, so nothing past the array's end is ever read.
 struct StagePlan {
   int64_t first;      // global index of buf[0]
   int64_t tail_from;  // first global index loaded with plain loads
@@ -166,22 +166,10 @@ struct StagePlan {
   int32_t span;       // lead + c: elements of buf in use
 };
 
-template <int SZ>
-__device__ __forceinline__ StagePlan stage_plan(int64_t s, int64_t c) {
-  const int64_t lo = s * SZ, hi = (s + c) * SZ;
-  const int64_t alo = lo & ~int64_t(15), ahi = hi & ~int64_t(15);
-  StagePlan p;
-  p.first = alo / SZ;
-  p.lead = static_cast<int32_t>(s - p.first);
-  p.bulk = static_cast<uint32_t>(ahi > alo ? ahi - alo : 0);
-  p.tail_from = ahi / SZ > s ? ahi / SZ : s;
-  p.span = static_cast<int32_t>(p.lead + c);
-  return p;
-}
-
-// Same, but the bulk copy runs up to the next 16-byte boundary past s + c
-// whenever that stays inside the array's first `limit` elements, so that a
-// span needs plain loads only at the very end of its array.
+// The plan for [s, s + c) of an array of `limit` elements: the bulk copy
+// runs from the 16-byte boundary at or below s up to the next 16-byte
+// boundary past s + c whenever that stays inside the array, so that a span
+// needs plain loads only at the very end of its array.
 template <int SZ>
 __device__ __forceinline__ StagePlan stage_plan_overfetch(int64_t s, int64_t c, int64_t limit) {
   const int64_t lo = s * SZ, hi = (s + c) * SZ;
@@ -223,16 +211,11 @@ __host__ __device__ constexpr int64_t stage_capacity_bytes(int64_t c) {
   return align_up(c * SZ + 16, 16);
 }
 
+// Issues a plan's bulk copy (if any) against mbarrier `bar`; the caller
+// loads the elements from p.tail_from on with plain loads.
 template <typename T>
 __device__ __forceinline__ void stage_issue(T *buf, const T *g, const StagePlan &p, uint64_t *bar) {
   if (p.bulk) bulk_g2s(buf, g + p.first, p.bulk, bar);
-}
-
-template <typename T>
-__device__ __forceinline__ void stage_tail(T *buf, const T *g, const StagePlan &p, int64_t s,
-                                           int64_t c, int tid) {
-  const int64_t x = p.tail_from + tid;
-  if (x < s + c) buf[x - p.first] = g[x];
 }
 
 // ---- scans ------------------------------------------------------------------
@@ -276,24 +259,10 @@ __device__ __forceinline__ V block_sum(V v, V *scratch) {
   return total;
 }
 
-// ---- per-thread merge-path search -------------------------------------------------
-// The co-rank of diagonal k: the first i in [max(0, k-n), min(k, m)] for
-// which pred.too_small(i, k) is false, by plain bisection. One thread per
-// diagonal: every search touches two sectors per level, and tens of
-// thousands of searches in flight hide the dependent-load latency.
-template <class Pred>
-__device__ __forceinline__ int64_t thread_corank(const Pred &pred, int64_t k, int64_t m, int64_t n) {
-  int64_t lo = k > n ? k - n : 0;
-  int64_t hi = k < m ? k : m;
-  while (lo < hi) {
-    const int64_t mid = (lo + hi) >> 1;
-    if (pred.too_small(mid, k)) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// The same co-rank found by a group of L lanes (L a power of two <= 32,
+// ---- merge-path co-rank searches ---------------------------------------------------
+// The co-rank of diagonal k is the first i in [max(0, k-n), min(k, m)] for
+// which pred.too_small(i, k) is false.
+// That co-rank found by a group of L lanes (L a power of two <= 32,
 // groups aligned within the warp). Each round the group tests L pivots
 // spread evenly over the open range and keeps the interval between the last
 // pivot that is too small and the first that is not, so the range shrinks

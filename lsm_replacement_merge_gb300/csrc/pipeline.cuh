@@ -167,27 +167,6 @@ __device__ __forceinline__ void store_u32_run(uint32_t *gbase, int64_t g0, int c
   if (t >= 8 && t < 8 + tail) gbase[g0 + head + body + (t - 8)] = sbuf[shift + head + body + (t - 8)];
 }
 
-// Block-wide exclusive sum over the T consumer threads (named barrier 1).
-// `scratch` holds T/32 + 1 values.
-template <int NT, typename V>
-__device__ __forceinline__ V consumer_exclusive_sum(V v, V *scratch, V *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  V inc = warp_inclusive_sum(v);
-  if (lane == 31) scratch[warp] = inc;
-  named_sync(1, NT);
-  if (warp == 0) {
-    V w = lane < NT / 32 ? scratch[lane] : V(0);
-    V wi = warp_inclusive_sum(w);
-    if (lane < NT / 32) scratch[lane] = wi - w;
-    if (lane == NT / 32 - 1) scratch[NT / 32] = wi;
-  }
-  named_sync(1, NT);
-  V out = scratch[warp] + inc - v;
-  *total = scratch[NT / 32];
-  named_sync(1, NT);
-  return out;
-}
-
 // Exclusive sum of `v` and exclusive maximum of `mx` over the T consumer
 // threads in one pass (named barrier 1). `scratch` holds 2 * (T/32 + 1)
 // values; *total is the sum over all threads and *mx_before the maximum of

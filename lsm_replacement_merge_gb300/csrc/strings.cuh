@@ -61,16 +61,4 @@ __device__ __forceinline__ int key_cmp(const KeyRef &a, const KeyRef &b) {
   return la == lb ? 0 : (la < lb ? -1 : 1);
 }
 
-// Exact bit LCP, clamped to the shorter key.
-__device__ __forceinline__ uint64_t key_bit_lcp(const KeyRef &a, const KeyRef &b) {
-  const uint64_t la = a.end - a.begin, lb = b.end - b.begin;
-  const uint64_t l = la < lb ? la : lb;
-  for (uint64_t t = 0; t < l; t += 8) {
-    const uint64_t x = load_be64(a.arena, a.begin + t, a.begin + l);
-    const uint64_t y = load_be64(b.arena, b.begin + t, b.begin + l);
-    if (x != y) return 8 * t + static_cast<uint64_t>(__clzll(x ^ y));
-  }
-  return 8 * l;
-}
-
 }  // namespace lsm
