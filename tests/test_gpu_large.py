@@ -121,3 +121,111 @@ def test_replacement_beyond_2pow31_elements(lsm):
     refs_exp[ordA_exp[keep]] = iA[keep]
     refs_exp[ordB_exp] = jB + LSM_REF_FROM_B
     assert bool((_u32(refs[:N]) == refs_exp).all())
+
+
+def _eg0_len(x):
+    import numpy as np
+    return 2 * (np.floor(np.log2(x.astype(np.float64) + 1)).astype(np.int64)) + 1
+
+
+def test_fc_payload_beyond_2pow32_bits(lsm):
+    # 532,480 records with 8-byte keys 0, 1, 2, ... (A the even ones, B the
+    # odd ones) and 1 KB values: a 4.36 Gbit payload. With consecutive integer
+    # keys every length is a closed form (the LCP of r-1 and r is 63 minus the
+    # trailing zeros of r); the payload is checked by decoding records at the
+    # start, across bit 2^32 and at the end with a plain bit reader.
+    import numpy as np
+    _need(8)
+    h = (1 << 18) + 4096
+    N = 2 * h
+    d = dev()
+
+    def side(par, mul, add):
+        keys = (np.arange(h, dtype=np.uint64) * 2 + par).astype(">u8").view(np.uint8)
+        kb = lsm.Bytes.from_numpy(keys, np.arange(h + 1, dtype=np.uint64) * 8, d)
+        t = torch.arange(h, device=d, dtype=torch.int64)[:, None]
+        b = torch.arange(1024, device=d, dtype=torch.int64)[None, :]
+        arena = torch.zeros(h * 1024 + 8, dtype=torch.uint8, device=d)
+        arena[:h * 1024] = ((t * mul + b * 7 + add) & 255).to(torch.uint8).reshape(-1)
+        voff = (torch.arange(h + 1, device=d, dtype=torch.int64) * 1024).view(torch.uint64)
+        return kb, lsm.Bytes(arena, voff)
+
+    kA, vA = side(0, 131, 0)
+    kB, vB = side(1, 29, 5)
+    tomb_rec = (np.arange(h) % 97) == 3  # A records t with t % 97 == 3
+    tw = np.zeros((h + 31) // 32, dtype=np.uint32)
+    for t in np.nonzero(tomb_rec)[0]:
+        tw[t // 32] |= np.uint32(1 << (t % 32))
+    fc = lsm.FcInput(kA, vA, torch.from_numpy(tw).to(d), kB, vB, None)
+    C, lb = lsm.collision_mark_str(kA, kB)
+    dir_, _ = lsm.rank_build(C, h)
+    refs, _, _, cnt = lsm.replacement_merge_compact(h, h, C, dir_, lb)
+    assert int(cnt.item()) == N
+    r = np.arange(N, dtype=np.int64)
+    refs_exp = np.where(r % 2 == 1, LSM_REF_FROM_B, 0) | (r >> 1)
+    assert np.array_equal(_u32(refs[:N]).cpu().numpy(), refs_exp)
+    lcp, ctrl, rec, off = lsm.fc_lengths_scan(fc, refs, N)
+    # closed forms
+    x = np.maximum((r - 1) ^ r, 1)
+    l_exp = np.where(r == 0, 0, 64 - (np.floor(np.log2(x.astype(np.float64))).astype(np.int64) + 1))
+    c_exp = np.where(r % 15 == 0, 1 + l_exp, 64 - l_exp)
+    dd = 64 - l_exp
+    tomb = (r % 2 == 0) & tomb_rec[r >> 1]
+    v = np.where(tomb, 1, 1 + _eg0_len(np.array([1024]))[0] + 8 * 1024)
+    rec_exp = _eg0_len(c_exp) + _eg0_len(dd) + dd + v
+    off_exp = np.zeros(N + 1, dtype=np.int64)
+    off_exp[1:] = np.cumsum(rec_exp)
+    total = int(off_exp[N])
+    assert total > (1 << 32)
+    assert np.array_equal(_u32(lcp).cpu().numpy(), l_exp)
+    assert np.array_equal(_u32(ctrl).cpu().numpy(), c_exp)
+    assert np.array_equal(_u32(rec).cpu().numpy(), rec_exp)
+    assert np.array_equal(off.view(torch.int64).cpu().numpy(), off_exp)
+    nwords = (total + 31) // 32 + 3
+    words = _u32(lsm.fc_emit(fc, refs, N, lcp, ctrl, off, nwords)).cpu().numpy().astype(np.uint64)
+    assert not words[(total + 31) // 32:].any()
+    if total % 32:
+        assert int(words[total // 32]) & ((1 << (32 - total % 32)) - 1) == 0
+
+    def bits(p, k):  # k <= 32 stream bits from p, as an integer
+        q, s = p >> 5, p & 31
+        w = (int(words[q]) << 32) | (int(words[q + 1]) if q + 1 < len(words) else 0)
+        return (w >> (64 - s - k)) & ((1 << k) - 1)
+
+    def eg0(p):
+        z = 0
+        while bits(p + z, 1) == 0:
+            z += 1
+        return bits(p + z, z + 1) - 1, p + 2 * z + 1
+
+    cross = int(np.searchsorted(off_exp, 1 << 32, side="right")) - 1
+    sample = sorted(set([0, 1, 2, 14, 15, 16, 1000] + list(range(cross - 2, cross + 4))
+                        + [N - 2, N - 1]))
+    for i in sample:
+        p = int(off_exp[i])
+        c, p = eg0(p)
+        assert c == c_exp[i]
+        dlen, p = eg0(p)
+        assert dlen == dd[i]
+        key = 0
+        for q in range(0, dlen, 32):
+            k = min(32, dlen - q)
+            key = (key << k) | bits(p + q, k)
+        assert key == i & ((1 << dlen) - 1)
+        p += dlen
+        if tomb[i]:
+            assert bits(p, 1) == 0
+            p += 1
+        else:
+            assert bits(p, 1) == 1
+            vlen, p = eg0(p + 1)
+            assert vlen == 1024
+            t = i >> 1
+            mul, add = (131, 0) if i % 2 == 0 else (29, 5)
+            for b in range(0, 1024, 4):
+                exp = 0
+                for u in range(4):
+                    exp = (exp << 8) | ((t * mul + (b + u) * 7 + add) & 255)
+                assert bits(p + 8 * b, 32) == exp
+            p += 8 * 1024
+        assert p == off_exp[i + 1]
