@@ -61,6 +61,8 @@ def _load():
             _lib.oracle_replacement_u64.restype = I
             _lib.oracle_replacement_str.argtypes = [P, P, I, P, P, I, P, P, P, P, P]
             _lib.oracle_replacement_str.restype = I
+            _lib.oracle_materialize_u64.argtypes = [P, P, P, I, P, P, P, I, P, I, P, P, P]
+            _lib.oracle_materialize_u64.restype = None
             _lib.oracle_rank_prefix.argtypes = [P, I, P]
             _lib.oracle_rank_prefix.restype = None
             _lib.oracle_rank512_dir.argtypes = [P, I, P]
@@ -169,6 +171,22 @@ def replacement_u64(A, B):
     cnt = _load().oracle_replacement_u64(_p(A), m, _p(B), n, _p(refs), _p(C),
                                          _p(lb_B), _p(ord_A), _p(ord_B))
     return Replacement(refs[:cnt].copy(), C, lb_B, ord_A, ord_B, int(cnt))
+
+
+def materialize_u64(A, valA, tombA, B, valB, tombB, refs):
+    """Keys, values and tombstone bits of the survivors refs names, in order
+    (oracle_materialize_u64). A tombstone bitmap may be None."""
+    A, B = _c(A, np.uint64), _c(B, np.uint64)
+    valA, valB = _c(valA, np.uint32), _c(valB, np.uint32)
+    tA, tB = _c(tombA, np.uint32), _c(tombB, np.uint32)
+    refs = _c(refs, np.uint32)
+    N = len(refs)
+    keys = np.empty(N, dtype=np.uint64)
+    vals = np.empty(N, dtype=np.uint32)
+    tomb = np.zeros((N + 31) // 32, dtype=np.uint32)
+    _load().oracle_materialize_u64(_p(A), _p(valA), _p(tA), len(A), _p(B), _p(valB), _p(tB),
+                                   len(B), _p(refs), N, _p(keys), _p(vals), _p(tomb))
+    return keys, vals, tomb
 
 
 def replacement_str(Aarena, Aoff, Barena, Boff):

@@ -176,6 +176,36 @@ int64_t oracle_replacement_str(const uint8_t *Aar, const uint64_t *Aoff, int64_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* Materialized survivors. [GC] merge paragraph: of each equal-key run the  */
+/* newer record is kept, and a newer tombstone stays a record. Output       */
+/* record t is the source record refs[t] names: its key, its 32-bit value   */
+/* (when value arrays are given) and its tombstone flag, bit t of out_tomb  */
+/* (bit t%32 of word t/32; bits past N zero). A tombstone bitmap may be     */
+/* NULL (no tombstones in that input).                                      */
+/* ------------------------------------------------------------------------ */
+static int bit_at(const uint32_t *bits, int64_t i) {
+    return bits ? (int)((bits[i / 32] >> (i % 32)) & 1u) : 0;
+}
+
+void oracle_materialize_u64(const uint64_t *A, const uint32_t *Aval, const uint32_t *tombA,
+                            int64_t m, const uint64_t *B, const uint32_t *Bval,
+                            const uint32_t *tombB, int64_t n, const uint32_t *refs, int64_t N,
+                            uint64_t *out_keys, uint32_t *out_vals, uint32_t *out_tomb) {
+    int64_t t;
+    (void)m;
+    (void)n;
+    if (out_tomb) memset(out_tomb, 0, sizeof(uint32_t) * (size_t)((N + 31) / 32));
+    for (t = 0; t < N; t++) {
+        const int from_b = (refs[t] & REF_FROM_B) != 0;
+        const int64_t idx = (int64_t)(refs[t] & ~REF_FROM_B);
+        if (out_keys) out_keys[t] = from_b ? B[idx] : A[idx];
+        if (out_vals) out_vals[t] = from_b ? Bval[idx] : Aval[idx];
+        if (out_tomb && (from_b ? bit_at(tombB, idx) : bit_at(tombA, idx)))
+            out_tomb[t / 32] |= 1u << (t % 32);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Exclusive collision rank. [CB] "Corrected record ordinals":              */
 /* R(i) = sum_{t<i} C_t for i = 0..m, endpoint included. Bit by bit.        */
 /* ------------------------------------------------------------------------ */

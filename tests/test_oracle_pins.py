@@ -165,6 +165,35 @@ def test_replacement_invariants_and_formula_ordinals(m, n, shared, universe):
     assert (r.lb_B == np.searchsorted(A, B, side="left")).all()
 
 
+@pytest.mark.parametrize("m,n,shared,universe", REPLACE_CASES)
+def test_materialized_survivors_vs_chronological_map(m, n, shared, universe):
+    # Apply A then B, each record (key, value, tombstone), to a dict: the
+    # surviving records in key order are the materialized output.
+    inp = synth.replace_random_small(seed=m * 5 + n + 7 * shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    rng = np.random.default_rng(m + n + shared)
+    valA = rng.integers(0, 2**32, m, dtype=np.uint32)
+    valB = rng.integers(0, 2**32, n, dtype=np.uint32)
+    tA = rng.random(m) < 0.2
+    tB = rng.random(n) < 0.2
+    tombA = synth._bitmap(np.nonzero(tA)[0].astype(np.int64), m)
+    tombB = synth._bitmap(np.nonzero(tB)[0].astype(np.int64), n)
+    d = {}
+    for i, k in enumerate(inp.A.tolist()):
+        d[k] = (int(valA[i]), bool(tA[i]))
+    for j, k in enumerate(inp.B.tolist()):
+        d[k] = (int(valB[j]), bool(tB[j]))
+    items = sorted(d.items())
+    r = oracle.replacement_u64(inp.A, inp.B)
+    keys, vals, tomb = oracle.materialize_u64(inp.A, valA, tombA, inp.B, valB, tombB, r.refs)
+    assert keys.tolist() == [k for k, _ in items]
+    assert vals.tolist() == [v for _, (v, _) in items]
+    flags = [bool((int(tomb[t // 32]) >> (t % 32)) & 1) for t in range(len(items))]
+    assert flags == [f for _, (_, f) in items]
+    if len(items) % 32:  # bits past the last record are zero
+        assert int(tomb[-1]) >> (len(items) % 32) == 0
+
+
 def test_replacement_skewed_generator_small():
     inp = synth.replace_skewed(seed=4, m=40000, windows=4, window=256,
                                per_window_shared=128, per_window_fresh=128)
