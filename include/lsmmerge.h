@@ -226,6 +226,26 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                           int64_t *d_count, void *ws, size_t ws_bytes,
                                           void *stream);
 
+/* Materialized survivors of the replacement merge ([GC] merge paragraph: of
+ * each equal-key run the newer record is kept, and a newer tombstone stays a
+ * record). For t < N = d_count[0] (the count lsm_replacement_merge_compact
+ * wrote), record t is the source record out_refs[t] names:
+ *   out_keys[t]   its key
+ *   out_vals[t]   its 32-bit value (when Aval, Bval and out_vals are given)
+ *   out_tomb      bit t (bit t%32 of word t/32) = its tombstone flag; the
+ *                 words covering [0, N) are written, bits past N zero.
+ * tombA / tombB: tombstone bitmaps of the inputs (bit i of word i/32), each
+ * may be NULL (no tombstones in that input); out_tomb may be NULL. Records
+ * t >= N are not touched. All pointers are device pointers; A, B, out_keys:
+ * uint64, 16-byte aligned; out_keys and out_vals hold m + n entries,
+ * out_tomb ceil((m + n) / 32) words. m, n < 2^31. No workspace. */
+LSM_API int lsm_replacement_materialize(const uint64_t *A, const uint32_t *Aval,
+                                        const uint32_t *tombA, int64_t m, const uint64_t *B,
+                                        const uint32_t *Bval, const uint32_t *tombB, int64_t n,
+                                        const uint32_t *refs, const int64_t *d_count,
+                                        uint64_t *out_keys, uint32_t *out_vals,
+                                        uint32_t *out_tomb, void *stream);
+
 /* ---- a6: front-compression lengths and bit offsets ----------------------- */
 /* [GC], the control-argument equation and the record-length formula. For
  * output record i (refs[i] names its key and value):

@@ -82,6 +82,8 @@ def lib():
                 "lsm_rank_build": ([P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_rank_query": ([P, P, I, P, I, P, P], ctypes.c_int),
                 "lsm_replacement_merge_compact": ([I, I, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
+                "lsm_replacement_materialize": ([P, P, P, I, P, P, P, I, P, P, P, P, P, P],
+                                                ctypes.c_int),
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
@@ -341,6 +343,28 @@ def replacement_merge_compact(m: int, n: int, C, dir_, lb_B, refs=None, ord_A=No
                                                _ptr(ord_A) if m else None, _ptr(ord_B) if n else None,
                                                _ptr(d_count), _ptr(ws), ws.numel(), _stream(stream)))
     return refs, ord_A, ord_B, d_count
+
+
+def replacement_materialize(A, B, refs, d_count, valA=None, valB=None, tombA=None, tombB=None,
+                            out_keys=None, out_vals=None, out_tomb=None, stream=None):
+    """lsm_replacement_materialize: the survivors' keys, values (when valA and
+    valB are given) and tombstone bits, in merged order, for the first
+    d_count[0] refs. Returns (out_keys, out_vals, out_tomb)."""
+    m, n = A.numel(), B.numel()
+    dev = refs.device
+    if out_keys is None:
+        out_keys = _empty(max(m + n, 1), A.dtype, dev)
+    if out_vals is None and valA is not None:
+        out_vals = _empty(max(m + n, 1), torch.uint32, dev)
+    if out_tomb is None:
+        out_tomb = torch.zeros(max((m + n + 31) // 32, 1), dtype=torch.uint32, device=dev)
+    _check("lsm_replacement_materialize",
+           lib().lsm_replacement_materialize(_ptr(A) if m else None, _ptr(valA) if m else None,
+                                             _ptr(tombA), m, _ptr(B) if n else None,
+                                             _ptr(valB) if n else None, _ptr(tombB), n,
+                                             _ptr(refs), _ptr(d_count), _ptr(out_keys),
+                                             _ptr(out_vals), _ptr(out_tomb), _stream(stream)))
+    return out_keys, out_vals, out_tomb
 
 
 # ---------------------------------------------------------------------------

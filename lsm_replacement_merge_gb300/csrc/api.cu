@@ -278,6 +278,25 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
+LSM_API int lsm_replacement_materialize(const uint64_t *A, const uint32_t *Aval,
+                                        const uint32_t *tombA, int64_t m, const uint64_t *B,
+                                        const uint32_t *Bval, const uint32_t *tombB, int64_t n,
+                                        const uint32_t *refs, const int64_t *d_count,
+                                        uint64_t *out_keys, uint32_t *out_vals,
+                                        uint32_t *out_tomb, void *stream) {
+  if (m < 0 || n < 0 || !d_count) return LSM_ERR_ARG;
+  if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
+  if (m + n == 0) return LSM_OK;
+  if ((m && !A) || (n && !B) || !refs || !out_keys) return LSM_ERR_ARG;
+  if (out_vals && ((m && !Aval) || (n && !Bval))) return LSM_ERR_ARG;
+  for (const void *p : {static_cast<const void *>(A), static_cast<const void *>(B),
+                        static_cast<const void *>(out_keys)})
+    if (p && !aligned16(p)) return LSM_ERR_ALIGN;
+  return cuda_status(launch_materialize(A, Aval, tombA, m, B, Bval, tombB, n, refs, d_count,
+                                        out_keys, out_vals, out_tomb, status_ptr(),
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 static int check_fc_input(const lsm_fc_input *in) {
   if (!in || in->m < 0 || in->n < 0) return LSM_ERR_ARG;
   if (in->m > kMax31 || in->n > kMax31) return LSM_ERR_OVERFLOW;

@@ -50,6 +50,11 @@ cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, in
 cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                               const uint32_t *pos, int64_t q, uint32_t *out, int32_t *status,
                               cudaStream_t s);
+cudaError_t launch_materialize(const uint64_t *A, const uint32_t *Aval, const uint32_t *tombA,
+                               int64_t m, const uint64_t *B, const uint32_t *Bval,
+                               const uint32_t *tombB, int64_t n, const uint32_t *refs,
+                               const int64_t *d_count, uint64_t *out_keys, uint32_t *out_vals,
+                               uint32_t *out_tomb, int32_t *status, cudaStream_t s);
 cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
                            uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,

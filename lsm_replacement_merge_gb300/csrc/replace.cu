@@ -382,6 +382,49 @@ __global__ void __launch_bounds__(256) rank_query_kernel(const uint32_t *__restr
   out[t] = rank512_at(C, dir, p);
 }
 
+// ---- materialized survivors -------------------------------------------------------
+// One warp per 32 consecutive output records, grid-stride over [0, N) with
+// N = d_count[0] read on the device. Each lane copies its record's key (and
+// value) from the input its ref names; a ballot of the warp's tombstone
+// flags is one word of the output bitmap. A count past m + n or a ref past
+// its input records LSM_ERR_ARG and writes nothing for it.
+__global__ void __launch_bounds__(256) materialize_kernel(
+    const uint64_t *__restrict__ A, const uint32_t *__restrict__ Aval,
+    const uint32_t *__restrict__ tombA, int64_t m, const uint64_t *__restrict__ B,
+    const uint32_t *__restrict__ Bval, const uint32_t *__restrict__ tombB, int64_t n,
+    const uint32_t *__restrict__ refs, const int64_t *__restrict__ d_count,
+    uint64_t *__restrict__ out_keys, uint32_t *__restrict__ out_vals,
+    uint32_t *__restrict__ out_tomb, int32_t *status) {
+  pdl_begin();
+  const int64_t N = *d_count;
+  if (N < 0 || N > m + n) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(status, LSM_ERR_ARG);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; w * 32 < N;
+       w += warps) {
+    const int64_t t = w * 32 + lane;
+    bool tomb = false;
+    if (t < N) {
+      const uint32_t ref = __ldg(refs + t);
+      const bool from_b = (ref & LSM_REF_FROM_B) != 0;
+      const int64_t idx = ref & ~LSM_REF_FROM_B;
+      if (idx < (from_b ? n : m)) {
+        out_keys[t] = __ldg((from_b ? B : A) + idx);
+        if (out_vals) out_vals[t] = __ldg((from_b ? Bval : Aval) + idx);
+        const uint32_t *tb = from_b ? tombB : tombA;
+        tomb = tb && ((__ldg(tb + (idx >> 5)) >> (idx & 31)) & 1u);
+      } else {
+        report(status, LSM_ERR_ARG);
+      }
+    }
+    const uint32_t word = __ballot_sync(0xffffffffu, tomb);
+    if (out_tomb && lane == 0) out_tomb[w] = word;
+  }
+}
+
 // ---- collision mark ------------------------------------------------------------
 // One merge-path tile per pipeline step. The stage holds A[i0 - hp, i1) and
 // B[j0, j1 + hn): one A key before the span (for the lower bounds of B's
@@ -885,6 +928,23 @@ cudaError_t launch_compact_variant(int64_t m, int64_t n, const uint32_t *C, cons
   typename Spec::Params p{m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B, status};
   profile_before(s);
   err = launch_pipeline<Spec>(p, G, status, s, device_sm_count());
+  profile_after(s);
+  return err;
+}
+
+cudaError_t launch_materialize(const uint64_t *A, const uint32_t *Aval, const uint32_t *tombA,
+                               int64_t m, const uint64_t *B, const uint32_t *Bval,
+                               const uint32_t *tombB, int64_t n, const uint32_t *refs,
+                               const int64_t *d_count, uint64_t *out_keys, uint32_t *out_vals,
+                               uint32_t *out_tomb, int32_t *status, cudaStream_t s) {
+  const int64_t need = (m + n + 255) / 256;  // one thread per record at most
+  int64_t blocks = static_cast<int64_t>(device_sm_count()) * 8;
+  if (blocks > need) blocks = need;
+  if (blocks < 1) blocks = 1;
+  profile_before(s);
+  const cudaError_t err = launch_kernel(true, materialize_kernel, static_cast<unsigned>(blocks), 256,
+                                        0, s, A, Aval, tombA, m, B, Bval, tombB, n, refs, d_count,
+                                        out_keys, out_vals, out_tomb, status);
   profile_after(s);
   return err;
 }

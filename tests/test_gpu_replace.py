@@ -140,3 +140,66 @@ def test_every_tile_variant_matches_oracle(lsm, kernel, variant):
         check_against_oracle(run_pipeline(lsm, inp.A, inp.B), inp.A, inp.B)
     finally:
         lsm.tune_replace(kernel, *lsm.DEFAULT_REPLACE_VARIANT[kernel])
+
+
+def _materialize_check(lsm, A, B, valA, valB, tombA, tombB):
+    m, n = len(A), len(B)
+    Cd, lb = lsm.collision_mark(up(A), up(B))
+    dir_, _ = lsm.rank_build(Cd, m)
+    refs, _, _, cnt = lsm.replacement_merge_compact(m, n, Cd, dir_, lb)
+    N = int(cnt.item())
+    keys, vals, tomb = lsm.replacement_materialize(
+        up(A), up(B), refs, cnt, valA=up(valA), valB=up(valB),
+        tombA=None if tombA is None else up(tombA), tombB=None if tombB is None else up(tombB))
+    r = oracle.replacement_u64(A, B)
+    ek, ev, et = oracle.materialize_u64(A, valA, tombA, B, valB, tombB, r.refs)
+    assert N == r.count
+    assert np.array_equal(down(keys)[:N], ek)
+    assert np.array_equal(down(vals)[:N], ev)
+    assert np.array_equal(down(tomb)[:(N + 31) // 32], et)
+
+
+@pytest.mark.parametrize("m,n,shared,universe", REPLACE_CASES + [(300000, 100000, 25000, None)])
+def test_materialize_parity(lsm, m, n, shared, universe):
+    if m + n == 0:
+        return
+    inp = synth.replace_random_small(seed=m * 3 + n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    rng = np.random.default_rng(m + 7 * n)
+    tA = synth._bitmap(np.nonzero(rng.random(m) < 0.1)[0].astype(np.int64), m)
+    tB = synth._bitmap(np.nonzero(rng.random(n) < 0.1)[0].astype(np.int64), n)
+    _materialize_check(lsm, inp.A, inp.B, inp.valA, inp.valB, tA if m else None,
+                       tB if n else None)
+
+
+def test_materialize_without_values_or_tombstones(lsm):
+    inp = synth.replace_random_small(seed=5, m=5000, n=3000, shared=1000)
+    m, n = len(inp.A), len(inp.B)
+    Cd, lb = lsm.collision_mark(up(inp.A), up(inp.B))
+    dir_, _ = lsm.rank_build(Cd, m)
+    refs, _, _, cnt = lsm.replacement_merge_compact(m, n, Cd, dir_, lb)
+    keys, vals, tomb = lsm.replacement_materialize(up(inp.A), up(inp.B), refs, cnt)
+    r = oracle.replacement_u64(inp.A, inp.B)
+    ek, _, _ = oracle.materialize_u64(inp.A, inp.valA, None, inp.B, inp.valB, None, r.refs)
+    assert vals is None
+    assert np.array_equal(down(keys)[:r.count], ek)
+    assert not down(tomb)[:(r.count + 31) // 32].any()
+
+
+def test_config_replace_12M_4M_materialized(lsm):
+    inp = synth.replace_u64()
+    _materialize_check(lsm, inp.A, inp.B, inp.valA, inp.valB, None, inp.tombB)
+
+
+def test_materialize_rejects_a_ref_past_its_input(lsm):
+    A = np.arange(100, dtype=np.uint64)
+    B = np.arange(100, 150, dtype=np.uint64)
+    refs = np.array([0, 1, 99, 100, LSM_REF_FROM_B_PY | 49, LSM_REF_FROM_B_PY | 50], np.uint32)
+    cnt = torch.tensor([len(refs)], dtype=torch.int64, device="cuda")
+    keys, _, _ = lsm.replacement_materialize(up(A), up(B), up(refs), cnt)
+    assert lsm.get_device_status(reset=True) == 1   # LSM_ERR_ARG, then cleared
+    got = down(keys)
+    assert got[0] == 0 and got[1] == 1 and got[2] == 99 and got[4] == 149
+
+
+LSM_REF_FROM_B_PY = 0x80000000
