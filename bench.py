@@ -610,6 +610,25 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
                  "frac_of_8TBs_nominal": alg / (ms * 1e-3) / 1e9 / 8000.0,
                  "kernel_ms": per, "gpu_launches_per_step": 5,
                  "l2": "flushed (256 MiB write) before every step"}
+    # The materialized row: the same step plus the survivors' keys, values
+    # and tombstone bits gathered in merged order.
+    vA, vB = torch.from_numpy(ri.valA).to(dev), torch.from_numpy(ri.valB).to(dev)
+    tB = torch.from_numpy(ri.tombB).to(dev)
+    ok = torch.empty(m + n, dtype=A.dtype, device=dev)
+    ov = torch.empty(m + n, dtype=torch.uint32, device=dev)
+    otb = torch.empty((m + n + 31) // 32, dtype=torch.uint32, device=dev)
+    stages_mat = stages + [("replacement_materialize", lambda: lsm.replacement_materialize(
+        A, B, refs, cnt, valA=vA, valB=vB, tombB=tB, out_keys=ok, out_vals=ov, out_tomb=otb))]
+    ms_mat, per_mat = time_pipeline(torch, stages_mat, steps, flush)
+    alg_mat = (alg + 4 * (m + n) + 4 * len(ri.tombB)   # read values and B's tombstone bits
+               + 8 * N + 4 * N + 4 * ((N + 31) // 32))  # write keys, values, tombstone bits
+    out[name]["materialized"] = {
+        "ms_per_step": ms_mat, "gelem_s": (m + n) / (ms_mat * 1e-3) / 1e9,
+        "algorithmic_bytes": alg_mat, "gbs": alg_mat / (ms_mat * 1e-3) / 1e9,
+        "frac": alg_mat / (ms_mat * 1e-3) / 1e9 / peak,
+        "kernel_ms": {"replacement_materialize": per_mat["replacement_materialize"]},
+        "gpu_launches_per_step": 6}
+    del vA, vB, tB, ok, ov, otb
     if sweep:
         res = {}
         for kernel, label in ((0, "collision_mark"), (1, "replacement_merge_compact")):
