@@ -236,9 +236,9 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
  *                 words covering [0, N) are written, bits past N zero.
  * tombA / tombB: tombstone bitmaps of the inputs (bit i of word i/32), each
  * may be NULL (no tombstones in that input); out_tomb may be NULL. Records
- * t >= N are not touched. All pointers are device pointers; A, B, out_keys:
- * uint64, 16-byte aligned; out_keys and out_vals hold m + n entries,
- * out_tomb ceil((m + n) / 32) words. m, n < 2^31. No workspace. */
+ * t >= N are not touched. All pointers are device pointers; A, B, refs,
+ * out_keys and out_vals 16-byte aligned; out_keys and out_vals hold m + n
+ * entries, out_tomb ceil((m + n) / 32) words. m, n < 2^31. No workspace. */
 LSM_API int lsm_replacement_materialize(const uint64_t *A, const uint32_t *Aval,
                                         const uint32_t *tombA, int64_t m, const uint64_t *B,
                                         const uint32_t *Bval, const uint32_t *tombB, int64_t n,

@@ -290,7 +290,8 @@ LSM_API int lsm_replacement_materialize(const uint64_t *A, const uint32_t *Aval,
   if ((m && !A) || (n && !B) || !refs || !out_keys) return LSM_ERR_ARG;
   if (out_vals && ((m && !Aval) || (n && !Bval))) return LSM_ERR_ARG;
   for (const void *p : {static_cast<const void *>(A), static_cast<const void *>(B),
-                        static_cast<const void *>(out_keys)})
+                        static_cast<const void *>(out_keys), static_cast<const void *>(refs),
+                        static_cast<const void *>(out_vals)})
     if (p && !aligned16(p)) return LSM_ERR_ALIGN;
   return cuda_status(launch_materialize(A, Aval, tombA, m, B, Bval, tombB, n, refs, d_count,
                                         out_keys, out_vals, out_tomb, status_ptr(),
