@@ -54,14 +54,119 @@ __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int6
   if (active && (threadIdx.x & (kStrPartitionLanes - 1)) == 0) out_i[g] = i;
 }
 
+// Settles the order of two keys that agree on their first 16 bytes and are
+// both longer than 16, for every lane of the warp with `tail` set; `c` is
+// returned unchanged on the other lanes. All 32 lanes call it together. The
+// warp takes up to four such pairs a round, eight lanes a pair and one
+// 8-byte window a lane, so a pair whose shorter key ends within 80 bytes
+// costs one round of loads, and no lane compares alone.
+__device__ __forceinline__ int warp_tail_cmp(bool tail, int c, const uint8_t *arenaA, uint64_t ba,
+                                             uint64_t la, const uint8_t *arenaB, uint64_t bb,
+                                             uint64_t lb) {
+  constexpr unsigned kAll = 0xffffffffu;
+  unsigned pend = __ballot_sync(kAll, tail);
+  const int lane = threadIdx.x & 31, grp = lane >> 3, sub = lane & 7;
+  while (pend) {
+    int src = -1;  // the lane whose pair this lane's group settles
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (pend) {
+        if (q == grp) src = __ffs(pend) - 1;
+        pend &= pend - 1;
+      }
+    }
+    const int from = src < 0 ? lane : src;
+    const uint64_t gba = __shfl_sync(kAll, ba, from), gla = __shfl_sync(kAll, la, from);
+    const uint64_t gbb = __shfl_sync(kAll, bb, from), glb = __shfl_sync(kAll, lb, from);
+    const uint64_t l = gla < glb ? gla : glb;
+    bool done = src < 0;
+    int res = 0;
+    for (uint64_t t = 16; !__all_sync(kAll, done); t += 64) {
+      const uint64_t p = t + 8 * sub;
+      const bool in = !done && p < l;
+      uint64_t x = 0, y = 0;
+      if (in) {
+        x = load_be64(arenaA, gba + p, gba + l);
+        y = load_be64(arenaB, gbb + p, gbb + l);
+      }
+      const unsigned gdiff = (__ballot_sync(kAll, in && x != y) >> (8 * grp)) & 0xFFu;
+      const int first = 8 * grp + (gdiff ? __ffs(gdiff) - 1 : 0);
+      const uint64_t xs = __shfl_sync(kAll, x, first), ys = __shfl_sync(kAll, y, first);
+      if (!done) {
+        if (gdiff) {
+          res = xs < ys ? -1 : 1;
+          done = true;
+        } else if (t + 64 >= l) {
+          res = gla == glb ? 0 : (gla < glb ? -1 : 1);
+          done = true;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = __shfl_sync(kAll, res, 8 * q), s = __shfl_sync(kAll, src, 8 * q);
+      if (lane == s) c = r;
+    }
+  }
+  return c;
+}
+
+// A tile's staged keys. Each key keeps a prefix cache: the big-endian words
+// of bytes 0..7 and 8..15 (zero past its end) in k0/k1; A slot x starts at
+// begA[x] and ends at begA[x + 1], B slot y likewise in begB. Differing
+// words order two keys. With equal words and one length at most 16, the
+// shorter key is a proper prefix of the other (its missing bytes are the
+// other's zero bytes), or the keys are equal. Only keys longer than 16
+// bytes with equal first 16 bytes read further bytes, in warp_tail_cmp.
+struct TileKeys {
+  const uint64_t *k0A, *k1A, *k0B, *k1B, *begA, *begB;
+  const uint8_t *arenaA, *arenaB;
+  // Order of A slot sa against B slot y; all 32 lanes call it, `open` says
+  // whether this lane has a pair (the result is 0 when it has none).
+  __device__ __forceinline__ int cmp(bool open, int sa, int y) const {
+    int c = 0;
+    bool tail = false;
+    uint64_t ba = 0, la = 0, bb = 0, lb = 0;
+    if (open) {
+      const uint64_t a0 = k0A[sa], b0 = k0B[y];
+      const uint64_t a1 = k1A[sa], b1 = k1B[y];
+      if (a0 != b0) {
+        c = a0 < b0 ? -1 : 1;
+      } else if (a1 != b1) {
+        c = a1 < b1 ? -1 : 1;
+      } else {
+        ba = begA[sa];
+        la = begA[sa + 1] - ba;
+        bb = begB[y];
+        lb = begB[y + 1] - bb;
+        if (la <= 16 || lb <= 16) c = la == lb ? 0 : (la < lb ? -1 : 1);
+        else tail = true;
+      }
+    }
+    return warp_tail_cmp(tail, c, arenaA, ba, la, arenaB, bb, lb);
+  }
+};
+
+// One tile of T * E merged keys per CTA (T a multiple of 32). The tile's
+// keys (and A[i0 - 1], B[j1] where they exist) are staged once in shared
+// memory; each thread then finds its diagonal's co-rank by bisection and
+// walks E merge steps, every comparison on the staged prefixes, the warp's
+// lanes in step so that equal-prefix pairs are settled together. A B key's
+// lower bound is the A count before it in the A-first merge, one less when
+// the A key just before it is equal; an A key equal to the B head it is
+// taken before sets its collision bit.
 template <int T, int E>
 __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int64_t m, lsm_bytes B,
                                                                int64_t n,
                                                                const int64_t *__restrict__ part_i,
                                                                uint32_t *__restrict__ C,
                                                                uint32_t *__restrict__ lb_B) {
+  static_assert(T % 32 == 0, "whole warps");
   pdl_begin();
   constexpr int D = T * E;
+  constexpr int NK = D + 2;             // staged keys at most
+  constexpr int NQ = (NK + T - 1) / T;  // staged keys per thread at most
+  __shared__ uint64_t sK0[NK], sK1[NK], sBeg[NK + 2];
   __shared__ uint32_t sLB[D];
   __shared__ uint32_t sCw[D / 32 + 4];
   const int tid = threadIdx.x;
@@ -75,29 +180,66 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
   const int64_t w0 = i0 >> 5;
   const int nw = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
   for (int x = tid; x < nw; x += T) sCw[x] = 0u;
+
+  // A slots [A[i0-1]] A[i0..i1), then B slots B[j0..j1) [B[j1]]; start
+  // offsets in sBeg with one end offset after each side's run
+  const int hp = i0 > 0 ? 1 : 0, hn = j1 < n ? 1 : 0;
+  const int nA = hp + na, nB = nb + hn, nst = nA + nB;
+  {
+    uint64_t kb[NQ], ke[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int x = tid + q * T;
+      kb[q] = ke[q] = 0;
+      if (x < nst) {
+        const uint64_t *off = x < nA ? A.off + (i0 - hp + x) : B.off + (j0 + (x - nA));
+        kb[q] = __ldg(off);
+        ke[q] = __ldg(off + 1);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int x = tid + q * T;
+      if (x < nst) {
+        const uint8_t *arena = x < nA ? A.arena : B.arena;
+        const uint64_t len = ke[q] - kb[q];
+        sK0[x] = len > 0 ? load_be64(arena, kb[q], ke[q]) : 0;
+        sK1[x] = len > 8 ? load_be64(arena, kb[q] + 8, ke[q]) : 0;
+        const int xb = x < nA ? x : x + 1;  // B's starts follow A's end offset
+        sBeg[xb] = kb[q];
+        if (x == nA - 1 || x == nst - 1) sBeg[xb + 1] = ke[q];
+      }
+    }
+  }
   __syncthreads();
+  const TileKeys keys{sK0, sK1, sK0 + nA, sK1 + nA, sBeg, sBeg + nA + 1, A.arena, B.arena};
+  // A[i0 + a] is A slot hp + a; B[j0 + b] is B slot b
 
   const int cnt = na + nb;
   const int d = tid * E < cnt ? tid * E : cnt;
   int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-  while (lo < hi) {
+  while (__any_sync(0xffffffffu, lo < hi)) {
+    const bool open = lo < hi;
     const int mid = (lo + hi) >> 1;
-    if (key_cmp(key_at(A, i0 + mid), key_at(B, j0 + d - mid - 1)) <= 0) lo = mid + 1;
-    else hi = mid;
+    const int c = keys.cmp(open, hp + mid, d - mid - 1);
+    if (open) {
+      if (c <= 0) lo = mid + 1;
+      else hi = mid;
+    }
   }
   int ai = lo, bi = d - lo;
   // prev_eq: the element just before B's head in the merge is an A key equal
   // to it (then that B's lower bound is one less than the A count).
-  bool prev_eq = false;
-  if (d < cnt && i0 + ai > 0 && j0 + bi < n)
-    prev_eq = key_cmp(key_at(A, i0 + ai - 1), key_at(B, j0 + bi)) == 0;
-  for (int s = 0; s < E && d + s < cnt; ++s) {
+  const bool pq = d < cnt && i0 + ai > 0 && j0 + bi < n;
+  bool prev_eq = keys.cmp(pq, hp + ai - 1, bi) == 0 && pq;
+  for (int s = 0; s < E; ++s) {
     // c = cmp(A head, B head); B head may be B[j1] (one past the tile) only
     // for the collision test of A's last element.
-    int c = 0;
+    const bool live = d + s < cnt;
     const bool has_a = ai < na;
     const bool has_b = j0 + bi < n;
-    if (has_a && has_b) c = key_cmp(key_at(A, i0 + ai), key_at(B, j0 + bi));
+    const int c = keys.cmp(live && has_a && has_b, hp + ai, bi);
+    if (!live) continue;
     const bool takeA = (bi >= nb) || (has_a && c <= 0);
     if (takeA) {
       if (has_b && c == 0) {

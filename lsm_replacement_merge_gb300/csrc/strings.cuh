@@ -49,16 +49,23 @@ __device__ __forceinline__ KeyRef key_at(const lsm_bytes &col, int64_t idx) {
   return KeyRef{col.arena, __ldg(col.off + idx), __ldg(col.off + idx + 1)};
 }
 
-// Three-way comparison: negative, zero or positive.
-__device__ __forceinline__ int key_cmp(const KeyRef &a, const KeyRef &b) {
+// Three-way comparison of two keys whose first `from` bytes are known to be
+// equal (from a multiple of 8, at most the shorter length): negative, zero
+// or positive.
+__device__ __forceinline__ int key_cmp_from(const KeyRef &a, const KeyRef &b, uint64_t from) {
   const uint64_t la = a.end - a.begin, lb = b.end - b.begin;
   const uint64_t l = la < lb ? la : lb;
-  for (uint64_t t = 0; t < l; t += 8) {
+  for (uint64_t t = from; t < l; t += 8) {
     const uint64_t x = load_be64(a.arena, a.begin + t, a.begin + l);
     const uint64_t y = load_be64(b.arena, b.begin + t, b.begin + l);
     if (x != y) return x < y ? -1 : 1;
   }
   return la == lb ? 0 : (la < lb ? -1 : 1);
+}
+
+// Three-way comparison: negative, zero or positive.
+__device__ __forceinline__ int key_cmp(const KeyRef &a, const KeyRef &b) {
+  return key_cmp_from(a, b, 0);
 }
 
 }  // namespace lsm

@@ -60,5 +60,30 @@ def test_prefix_tree_strings(lsm, seed, count):
     check(lsm, synth.strings(seed=seed, count=count, fanout=8, depth=2, max_suffix=20))
 
 
+def _stem_lists(seed, count):
+    """Keys cut from one random 24-byte stem at every length 0..24, then
+    tails of up to 12 bytes over {0, 1, 255}: many pairs agree on their first
+    8 or 16 bytes, or differ only by trailing zero bytes, and lengths fall on
+    both sides of the 8- and 16-byte word edges."""
+    rng = np.random.default_rng(seed)
+    stem = bytes(rng.integers(0, 256, size=24).astype(np.uint8))
+    alphabet = np.array([0, 1, 255], dtype=np.uint8)
+    pool = set()
+    while len(pool) < count:
+        cut = int(rng.integers(0, 25))
+        tail = alphabet[rng.integers(0, 3, size=int(rng.integers(0, 13)))].tobytes()
+        pool.add(stem[:cut] + tail)
+    keys = sorted(pool)
+    pick = rng.permutation(len(keys))
+    A = sorted(keys[t] for t in pick[: len(keys) // 2])
+    B = sorted(keys[t] for t in pick[len(keys) // 3:])
+    return A, B
+
+
+@pytest.mark.parametrize("seed,count", [(3, 700), (4, 6000)])
+def test_keys_sharing_long_prefixes(lsm, seed, count):
+    check(lsm, synth.strings_from_lists(*_stem_lists(seed, count)))
+
+
 def test_config_strings_4M(lsm):
     check(lsm, synth.strings())
