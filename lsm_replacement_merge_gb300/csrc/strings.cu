@@ -54,6 +54,27 @@ __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int6
   if (active && (threadIdx.x & (kStrPartitionLanes - 1)) == 0) out_i[g] = i;
 }
 
+// Bytes [16, len) of two keys that agree on their first 16 bytes and are
+// both longer than 16, by one lane: 32 bytes a round with the eight
+// windows' loads issued together, so keys up to 48 bytes take one round.
+__device__ __forceinline__ int key_cmp_tail16(const uint8_t *pa, uint64_t ba, uint64_t la,
+                                              const uint8_t *pb, uint64_t bb, uint64_t lb) {
+  const uint64_t l = la < lb ? la : lb;
+  for (uint64_t t = 16; t < l; t += 32) {
+    uint64_t x[4], y[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t p = t + 8 * q;
+      x[q] = p < l ? load_be64(pa, ba + p, ba + l) : 0;
+      y[q] = p < l ? load_be64(pb, bb + p, bb + l) : 0;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (x[q] != y[q]) return x[q] < y[q] ? -1 : 1;
+  }
+  return la == lb ? 0 : (la < lb ? -1 : 1);
+}
+
 // Settles the order of two keys that agree on their first 16 bytes and are
 // both longer than 16, for every lane of the warp with `tail` set; `c` is
 // returned unchanged on the other lanes. All 32 lanes call it together. The
@@ -116,14 +137,20 @@ __device__ __forceinline__ int warp_tail_cmp(bool tail, int c, const uint8_t *ar
 // begA[x] and ends at begA[x + 1], B slot y likewise in begB. Differing
 // words order two keys. With equal words and one length at most 16, the
 // shorter key is a proper prefix of the other (its missing bytes are the
-// other's zero bytes), or the keys are equal. Only keys longer than 16
-// bytes with equal first 16 bytes read further bytes, in warp_tail_cmp.
+// other's zero bytes), or the keys are equal. Two keys longer than 16 bytes
+// with equal first 16 bytes need their further bytes: in exact mode from
+// warp_tail_cmp; otherwise, when their lengths agree too, they are taken as
+// equal and the pair is listed in `vlist` (`vn` counts the entries, also
+// past `vcap`) for the caller to check.
 struct TileKeys {
   const uint64_t *k0A, *k1A, *k0B, *k1B, *begA, *begB;
   const uint8_t *arenaA, *arenaB;
+  uint32_t *vlist;
+  int *vn;
+  int vcap;
   // Order of A slot sa against B slot y; all 32 lanes call it, `open` says
   // whether this lane has a pair (the result is 0 when it has none).
-  __device__ __forceinline__ int cmp(bool open, int sa, int y) const {
+  __device__ __forceinline__ int cmp(bool open, int sa, int y, bool exact) const {
     int c = 0;
     bool tail = false;
     uint64_t ba = 0, la = 0, bb = 0, lb = 0;
@@ -139,8 +166,14 @@ struct TileKeys {
         la = begA[sa + 1] - ba;
         bb = begB[y];
         lb = begB[y + 1] - bb;
-        if (la <= 16 || lb <= 16) c = la == lb ? 0 : (la < lb ? -1 : 1);
-        else tail = true;
+        if (la <= 16 || lb <= 16) {
+          c = la == lb ? 0 : (la < lb ? -1 : 1);
+        } else if (!exact && la == lb) {
+          const int v = atomicAdd(vn, 1);
+          if (v < vcap) vlist[v] = (static_cast<uint32_t>(sa) << 16) | static_cast<uint32_t>(y);
+        } else {
+          tail = true;
+        }
       }
     }
     return warp_tail_cmp(tail, c, arenaA, ba, la, arenaB, bb, lb);
@@ -151,10 +184,13 @@ struct TileKeys {
 // keys (and A[i0 - 1], B[j1] where they exist) are staged once in shared
 // memory; each thread then finds its diagonal's co-rank by bisection and
 // walks E merge steps, every comparison on the staged prefixes, the warp's
-// lanes in step so that equal-prefix pairs are settled together. A B key's
-// lower bound is the A count before it in the A-first merge, one less when
-// the A key just before it is equal; an A key equal to the B head it is
-// taken before sets its collision bit.
+// lanes in step. A B key's lower bound is the A count before it in the
+// A-first merge, one less when the A key just before it is equal; an A key
+// equal to the B head it is taken before sets its collision bit. The first
+// pass takes long keys with equal 16-byte prefixes and equal lengths as
+// equal (in the common case these are the colliding keys) and the CTA then
+// checks every such pair at once; if one differs, or the list overflowed,
+// the tile runs again with exact comparisons.
 template <int T, int E>
 __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int64_t m, lsm_bytes B,
                                                                int64_t n,
@@ -167,9 +203,13 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
   constexpr int NK = D + 2;             // staged keys at most
   constexpr int NQ = (NK + T - 1) / T;  // staged keys per thread at most
   __shared__ uint64_t sK0[NK], sK1[NK], sBeg[NK + 2];
+  constexpr int kVCap = D / 2;           // pairs taken as equal, checked after
   __shared__ uint32_t sLB[D];
   __shared__ uint32_t sCw[D / 32 + 4];
+  __shared__ uint32_t sV[kVCap];
+  __shared__ int sVn;
   const int tid = threadIdx.x;
+  if (tid == 0) sVn = 0;
   const int64_t g = blockIdx.x;
   const int64_t total = m + n;
   const int64_t k0 = g * D;
@@ -212,49 +252,64 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
     }
   }
   __syncthreads();
-  const TileKeys keys{sK0, sK1, sK0 + nA, sK1 + nA, sBeg, sBeg + nA + 1, A.arena, B.arena};
+  const TileKeys keys{sK0, sK1, sK0 + nA, sK1 + nA, sBeg, sBeg + nA + 1,
+                      A.arena, B.arena, sV, &sVn, kVCap};
   // A[i0 + a] is A slot hp + a; B[j0 + b] is B slot b
 
   const int cnt = na + nb;
   const int d = tid * E < cnt ? tid * E : cnt;
-  int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-  while (__any_sync(0xffffffffu, lo < hi)) {
-    const bool open = lo < hi;
-    const int mid = (lo + hi) >> 1;
-    const int c = keys.cmp(open, hp + mid, d - mid - 1);
-    if (open) {
-      if (c <= 0) lo = mid + 1;
-      else hi = mid;
-    }
-  }
-  int ai = lo, bi = d - lo;
-  // prev_eq: the element just before B's head in the merge is an A key equal
-  // to it (then that B's lower bound is one less than the A count).
-  const bool pq = d < cnt && i0 + ai > 0 && j0 + bi < n;
-  bool prev_eq = keys.cmp(pq, hp + ai - 1, bi) == 0 && pq;
-  for (int s = 0; s < E; ++s) {
-    // c = cmp(A head, B head); B head may be B[j1] (one past the tile) only
-    // for the collision test of A's last element.
-    const bool live = d + s < cnt;
-    const bool has_a = ai < na;
-    const bool has_b = j0 + bi < n;
-    const int c = keys.cmp(live && has_a && has_b, hp + ai, bi);
-    if (!live) continue;
-    const bool takeA = (bi >= nb) || (has_a && c <= 0);
-    if (takeA) {
-      if (has_b && c == 0) {
-        const int64_t gi = i0 + ai;
-        atomicOr(&sCw[(gi >> 5) - w0], 1u << (gi & 31));
+  for (int pass = 0;; ++pass) {
+    const bool exact = pass > 0;
+    int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
+    while (__any_sync(0xffffffffu, lo < hi)) {
+      const bool open = lo < hi;
+      const int mid = (lo + hi) >> 1;
+      const int c = keys.cmp(open, hp + mid, d - mid - 1, exact);
+      if (open) {
+        if (c <= 0) lo = mid + 1;
+        else hi = mid;
       }
-      prev_eq = has_b && c == 0;
-      ++ai;
-    } else {
-      sLB[bi] = static_cast<uint32_t>(i0 + ai - (prev_eq ? 1 : 0));
-      prev_eq = false;
-      ++bi;
     }
+    int ai = lo, bi = d - lo;
+    // prev_eq: the element just before B's head in the merge is an A key
+    // equal to it (then that B's lower bound is one less than the A count).
+    const bool pq = d < cnt && i0 + ai > 0 && j0 + bi < n;
+    bool prev_eq = keys.cmp(pq, hp + ai - 1, bi, exact) == 0 && pq;
+    for (int s = 0; s < E; ++s) {
+      // c = cmp(A head, B head); B head may be B[j1] (one past the tile)
+      // only for the collision test of A's last element.
+      const bool live = d + s < cnt;
+      const bool has_a = ai < na;
+      const bool has_b = j0 + bi < n;
+      const int c = keys.cmp(live && has_a && has_b, hp + ai, bi, exact);
+      if (!live) continue;
+      const bool takeA = (bi >= nb) || (has_a && c <= 0);
+      if (takeA) {
+        if (has_b && c == 0) {
+          const int64_t gi = i0 + ai;
+          atomicOr(&sCw[(gi >> 5) - w0], 1u << (gi & 31));
+        }
+        prev_eq = has_b && c == 0;
+        ++ai;
+      } else {
+        sLB[bi] = static_cast<uint32_t>(i0 + ai - (prev_eq ? 1 : 0));
+        prev_eq = false;
+        ++bi;
+      }
+    }
+    __syncthreads();
+    if (exact) break;
+    const int nv = sVn;
+    bool wrong = nv > kVCap;
+    for (int x = tid; x < nv && x < kVCap; x += T) {
+      const int sa = static_cast<int>(sV[x] >> 16), y = static_cast<int>(sV[x] & 0xFFFFu);
+      const uint64_t ba = keys.begA[sa], bb = keys.begB[y], l = keys.begA[sa + 1] - ba;
+      if (key_cmp_tail16(A.arena, ba, l, B.arena, bb, l) != 0) wrong = true;
+    }
+    if (!__syncthreads_or(wrong)) break;
+    for (int x = tid; x < nw; x += T) sCw[x] = 0u;
+    __syncthreads();
   }
-  __syncthreads();
   for (int x = tid; x < nb; x += T) lb_B[j0 + x] = sLB[x];
   for (int x = tid; x < nw; x += T) {
     const int64_t w = w0 + x;

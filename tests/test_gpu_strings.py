@@ -85,5 +85,15 @@ def test_keys_sharing_long_prefixes(lsm, seed, count):
     check(lsm, synth.strings_from_lists(*_stem_lists(seed, count)))
 
 
+def test_keys_with_one_16_byte_prefix(lsm):
+    # Every key is one 16-byte stem and an 8-byte big-endian counter: all
+    # pairs agree on their first 16 bytes and on their length, so the order
+    # comes from bytes 16..23 alone (A holds multiples of 2, B of 3).
+    stem = bytes(range(40, 56))
+    A = [stem + (2 * i).to_bytes(8, "big") for i in range(3000)]
+    B = [stem + (3 * j).to_bytes(8, "big") for j in range(2000)]
+    check(lsm, synth.strings_from_lists(A, B))
+
+
 def test_config_strings_4M(lsm):
     check(lsm, synth.strings())
