@@ -613,15 +613,17 @@ struct CompactSpec {
   static constexpr int NC = D / 32 + 4;  // collision words of one tile, at most
   static constexpr int64_t kLBBytes = align_up(int64_t(D) * 4 + 128, 16);
   static constexpr int64_t kStageBytes = kLBBytes + align_up(int64_t(NC + 4) * 4 + 64, 16);
+  // ord_A and ord_B of a tile share one buffer (na + nb <= D), and the marks
+  // (values <= D) are 16-bit: with 256 x 11 tiles four CTAs fit on an SM
   static constexpr int64_t kRefs = 0;
-  static constexpr int64_t kOrdA = align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kOrdB = kOrdA + align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kM = kOrdB + align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kPC = kM + align_up(int64_t(D + 1) * 4, 16);
+  static constexpr int64_t kOrd = align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kM = kOrd + align_up(int64_t(D + 16) * 4, 16);
+  static constexpr int64_t kPC = kM + align_up(int64_t(D + 1) * 2, 16);
   static constexpr int64_t kScan = kPC + align_up(int64_t(NC + 1) * 4, 16);
   static constexpr int64_t kWorkBytes = kScan + align_up(int64_t(2 * (T / 32 + 1)) * 4, 16);
   static_assert(NC <= T, "one thread per collision word");
   static_assert(E <= 32, "a thread's collision bits fit one 64-bit window");
+  static_assert(D < 65536, "16-bit marks");
   struct Params {
     int64_t m, n;
     const uint32_t *C, *dir, *lb_B;
@@ -634,8 +636,8 @@ struct CompactSpec {
     int32_t na, nb, offLB, offC;
   };
   __device__ __forceinline__ static void init(uint8_t *work) {
-    uint32_t *sM = reinterpret_cast<uint32_t *>(work + kM);
-    for (int x = threadIdx.x; x < D + 1; x += T) sM[x] = 0u;
+    uint16_t *sM = reinterpret_cast<uint16_t *>(work + kM);
+    for (int x = threadIdx.x; x < D + 1; x += T) sM[x] = 0;
   }
   // The co-ranks are clamped to their diagonals (and i1 - i0 to the tile's
   // length), so the staged ranges stay inside the arrays whatever lb_B held.
@@ -686,9 +688,8 @@ struct CompactSpec {
     const uint32_t *sLB = reinterpret_cast<const uint32_t *>(stage) + dd.offLB;
     const uint32_t *sCw = reinterpret_cast<const uint32_t *>(stage + kLBBytes) + dd.offC;
     uint32_t *bufRefs = reinterpret_cast<uint32_t *>(work + kRefs);
-    uint32_t *bufOrdA = reinterpret_cast<uint32_t *>(work + kOrdA);
-    uint32_t *bufOrdB = reinterpret_cast<uint32_t *>(work + kOrdB);
-    uint32_t *sM = reinterpret_cast<uint32_t *>(work + kM);
+    uint32_t *bufOrd = reinterpret_cast<uint32_t *>(work + kOrd);
+    uint16_t *sM = reinterpret_cast<uint16_t *>(work + kM);
     uint32_t *sPC = reinterpret_cast<uint32_t *>(work + kPC);
     uint32_t *sScan = reinterpret_cast<uint32_t *>(work + kScan);
     const int na = dd.na, nb = dd.nb;
@@ -700,9 +701,11 @@ struct CompactSpec {
     const uint32_t i0u = static_cast<uint32_t>(i0), j0u = static_cast<uint32_t>(j0);
     const uint32_t out0u = static_cast<uint32_t>(out0);
     const int cnt = na + nb;
+    // ord_B's part of the shared buffer starts on a 16-byte boundary past ord_A's
+    const int offB = (na + 3 + 4) & ~3;
     uint32_t *sRefs = bufRefs + (out0 & 3);
-    uint32_t *sOrdA = bufOrdA + (i0 & 3);
-    uint32_t *sOrdB = bufOrdB + (j0 & 3);
+    uint32_t *sOrdA = bufOrd + (i0 & 3);
+    uint32_t *sOrdB = bufOrd + offB + (j0 & 3);
 
     // 1. With B first on ties, B record bi precedes tile A record a exactly
     //    when L_bi = lb_B[j0 + bi] - i0 <= a, so the B records before A
@@ -716,7 +719,7 @@ struct CompactSpec {
       const uint32_t L = sLB[bi] - i0u;
       const uint32_t Ln = bi + 1 < nb ? sLB[bi + 1] - i0u : 0xFFFFFFFFu;
       if (L > static_cast<uint32_t>(na) || Ln < L) bad = true;
-      else if (L < static_cast<uint32_t>(na) && Ln != L) sM[L] = static_cast<uint32_t>(bi + 1);
+      else if (L < static_cast<uint32_t>(na) && Ln != L) sM[L] = static_cast<uint16_t>(bi + 1);
     }
     // collision words: bits of this tile's A records only (not those before
     // A[i0] in the first word, nor the next tile's in the last word)
@@ -728,7 +731,7 @@ struct CompactSpec {
     if (named_sync_or(1, T, bad)) {
       if (tid == 0) report(p.status, LSM_ERR_ARG);
       release_stage(empty);
-      for (int x = tid; x < na; x += T) sM[x] = 0u;
+      for (int x = tid; x < na; x += T) sM[x] = 0;
       named_sync(1, T);
       return;
     }
@@ -744,7 +747,7 @@ struct CompactSpec {
     }
 #pragma unroll
     for (int q = 0; q < E; ++q)
-      if (a0 + q < na && mv[q]) sM[a0 + q] = 0u;  // clean for the next tile
+      if (a0 + q < na && mv[q]) sM[a0 + q] = 0;  // clean for the next tile
     uint32_t totC, mbefore;
     const uint32_t exC = consumer_exclusive_sum_max<T>(
         tid < nwc ? static_cast<uint32_t>(__popc(cw_own)) : 0u, mloc, sScan, &totC, &mbefore);
@@ -794,8 +797,8 @@ struct CompactSpec {
     fence_proxy_async_smem();
     named_sync(1, T);
     store_u32_run<T>(p.refs, out0, kept_total, bufRefs);
-    store_u32_run<T>(p.ord_A, i0, na, bufOrdA);
-    store_u32_run<T>(p.ord_B, j0, nb, bufOrdB);
+    store_u32_run<T>(p.ord_A, i0, na, bufOrd);
+    store_u32_run<T>(p.ord_B, j0, nb, bufOrd + offB);
     if (tid == 0) {
       bulk_commit();
       bulk_wait_read_all();  // the buffers are rewritten by the next tile
