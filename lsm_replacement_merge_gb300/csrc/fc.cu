@@ -79,7 +79,9 @@ struct FcLayout {
   static constexpr int64_t kLcp = align_up(kSrc + kFcTile + 1, 16);     // u32[tile]
   static constexpr int64_t kCtrl = kLcp + kFcTile * 4;
   static constexpr int64_t kRec = kCtrl + kFcTile * 4;
-  static constexpr int64_t kScan = align_up(kRec + kFcTile * 4, 16);   // u64[T/32 + 1]
+  static constexpr int64_t kP0 = align_up(kRec + kFcTile * 4, 16);    // u64[tile + 1] bytes 0..7
+  static constexpr int64_t kP1 = kP0 + (kFcTile + 1) * 8;               // u64[tile + 1] bytes 8..15
+  static constexpr int64_t kScan = align_up(kP1 + (kFcTile + 1) * 8, 16);  // u64[T/32 + 1]
   static constexpr int64_t kBytes = kScan + (kFcThreads / 32 + 2) * 8 + 16;
 };
 
@@ -133,6 +135,8 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   uint32_t *sLcp = reinterpret_cast<uint32_t *>(smem + FcLayout::kLcp);
   uint32_t *sCtrl = reinterpret_cast<uint32_t *>(smem + FcLayout::kCtrl);
   uint32_t *sRec = reinterpret_cast<uint32_t *>(smem + FcLayout::kRec);
+  uint64_t *sP0 = reinterpret_cast<uint64_t *>(smem + FcLayout::kP0);
+  uint64_t *sP1 = reinterpret_cast<uint64_t *>(smem + FcLayout::kP1);
   uint64_t *sScan = reinterpret_cast<uint64_t *>(smem + FcLayout::kScan);
   const int tid = threadIdx.x;
   if (N == 0) {
@@ -184,33 +188,41 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   }
   __syncthreads();
 
-  // (3) this thread's records: the first two 64-bit windows of every key
-  // pair are loaded up front; longer common prefixes continue in a loop
-  const int b0 = tid * kFcItems;
-  uint64_t sum = 0;
-  bool overflow = false;
-  uint64_t wx[kFcItems][2], wy[kFcItems][2];
+  // (3) every slot's key: its first 16 bytes as two big-endian words (zero
+  // past the key's end), each key loaded once although two records
+  // compare it; every load is issued before any result is stored
+  {
+    constexpr int kSlotsPerThread = (kFcTile + 1 + kFcThreads - 1) / kFcThreads;
+    uint64_t w0[kSlotsPerThread], w1[kSlotsPerThread];
 #pragma unroll
-  for (int q = 0; q < kFcItems; ++q) {
-    wx[q][0] = wy[q][0] = wx[q][1] = wy[q][1] = 0;
-    const int x = b0 + q + 1;
-    const int64_t i = start + b0 + q;
-    if (b0 + q < cnt && i > 0) {
-      const uint64_t L = 8 * static_cast<uint64_t>(sKl[x - 1] < sKl[x] ? sKl[x - 1] : sKl[x]);
-      const uint8_t *pa = sSrc[x - 1] ? sb.key.arena : sa.key.arena;
-      const uint8_t *ca = sSrc[x] ? sb.key.arena : sa.key.arena;
-      if (L > 0) {
-        const int n0 = L < 64 ? static_cast<int>(L) : 64;
-        wx[q][0] = bits64_at(pa, 8 * sKb[x - 1], n0);
-        wy[q][0] = bits64_at(ca, 8 * sKb[x], n0);
+    for (int q = 0; q < kSlotsPerThread; ++q) {
+      const int x = first + tid + q * kFcThreads;
+      w0[q] = w1[q] = 0;
+      if (x <= cnt) {
+        const uint8_t *ar = sSrc[x] ? sb.key.arena : sa.key.arena;
+        const uint64_t kb = sKb[x], ke = kb + sKl[x];
+        if (ke > kb) w0[q] = load_be64(ar, kb, ke);
+        if (ke > kb + 8) w1[q] = load_be64(ar, kb + 8, ke);
       }
-      if (L > 64) {
-        const int n1 = L - 64 < 64 ? static_cast<int>(L - 64) : 64;
-        wx[q][1] = bits64_at(pa, 8 * sKb[x - 1] + 64, n1);
-        wy[q][1] = bits64_at(ca, 8 * sKb[x] + 64, n1);
+    }
+#pragma unroll
+    for (int q = 0; q < kSlotsPerThread; ++q) {
+      const int x = first + tid + q * kFcThreads;
+      if (x <= cnt) {
+        sP0[x] = w0[q];
+        sP1[x] = w1[q];
       }
     }
   }
+  __syncthreads();
+
+  // (4) this thread's four consecutive records: the bit LCP with the
+  // predecessor from the cached words (the first differing bit, clamped to
+  // the shorter key; past 128 equal bits the keys' further bytes decide),
+  // control and record length
+  const int b0 = tid * kFcItems;
+  uint64_t sum = 0;
+  bool overflow = false;
 #pragma unroll
   for (int q = 0; q < kFcItems; ++q) {
     if (b0 + q >= cnt) break;
@@ -221,25 +233,11 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
     if (i > 0) {
       k_prev = 8 * static_cast<uint64_t>(sKl[x - 1]);
       const uint64_t L = k_prev < k ? k_prev : k;
-      l = L;
-      bool found = false;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint64_t t0 = 64 * static_cast<uint64_t>(h);
-        if (!found && t0 < L) {
-          uint64_t xv = wx[q][h], yv = wy[q][h];
-          if (L - t0 < 64) {
-            const uint64_t mask = ~uint64_t(0) << (64 - (L - t0));
-            xv &= mask;
-            yv &= mask;
-          }
-          if (xv != yv) {
-            l = t0 + static_cast<uint64_t>(__clzll(static_cast<long long>(xv ^ yv)));
-            found = true;
-          }
-        }
-      }
-      if (!found && L > 128) {
+      const uint64_t d0 = sP0[x - 1] ^ sP0[x], d1 = sP1[x - 1] ^ sP1[x];
+      l = d0 ? static_cast<uint64_t>(__clzll(static_cast<long long>(d0)))
+             : (d1 ? 64 + static_cast<uint64_t>(__clzll(static_cast<long long>(d1))) : 128);
+      if (l > L) l = L;
+      if (l == 128 && L > 128) {
         const uint8_t *pa = sSrc[x - 1] ? sb.key.arena : sa.key.arena;
         const uint8_t *ca = sSrc[x] ? sb.key.arena : sa.key.arena;
         l = 128 + bit_lcp(pa, sKb[x - 1] + 16, sKl[x - 1] - 16, ca, sKb[x] + 16, sKl[x] - 16);
