@@ -662,7 +662,11 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
     w1 = lsm.workspace(lsm.LSM_OP_COLLISION_MARK_STR, m, n, dev)
     w2 = lsm.workspace(lsm.LSM_OP_RANK_BUILD, m, 0, dev)
     w3 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
-    lsm.collision_mark_str(Ak, Bk, C, lb, w1)
+    # the mark also writes the key prefix tables the lengths pass reads
+    pA = torch.empty(2 * m, dtype=torch.uint64, device=dev)
+    pB = torch.empty(2 * n, dtype=torch.uint64, device=dev)
+    fc.prefixA, fc.prefixB = pA, pB
+    lsm.collision_mark_str_prefix(Ak, Bk, C, lb, pA, pB, w1)
     lsm.rank_build(C, m, dir_, tot, w2)
     lsm.replacement_merge_compact(m, n, C, dir_, lb, refs, oa, ob, cnt, w3)
     N = int(cnt.item())
@@ -675,7 +679,8 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
     total_bits = int(off[N:].cpu().numpy()[0])
     nwords = (total_bits + 31) // 32
     payload = torch.empty(max(nwords, 4), dtype=torch.uint32, device=dev)
-    stages = [("collision_mark_str", lambda: lsm.collision_mark_str(Ak, Bk, C, lb, w1)),
+    stages = [("collision_mark_str", lambda: lsm.collision_mark_str_prefix(Ak, Bk, C, lb, pA, pB,
+                                                                            w1)),
               ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
               ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
                   m, n, C, dir_, lb, refs, oa, ob, cnt, w3)),

@@ -91,7 +91,10 @@ typedef struct {
 
 /* Inputs of the front-compression passes. Keys and values of both sources;
  * tombstone bitmaps may be NULL (no tombstones in that source). A value's
- * bytes are ignored when its record is a tombstone. */
+ * bytes are ignored when its record is a tombstone. prefixA and prefixB
+ * are optional (both or neither): the key prefix tables that
+ * lsm_collision_mark_str_prefix writes; with them lsm_fc_lengths_scan takes
+ * each key's first 16 bytes from the table instead of the arena. */
 typedef struct {
   lsm_bytes keyA, valA;
   const uint32_t *tombA; /* device bitmap, ceil(m/32) words, or NULL */
@@ -99,6 +102,8 @@ typedef struct {
   lsm_bytes keyB, valB;
   const uint32_t *tombB; /* device bitmap, ceil(n/32) words, or NULL */
   int64_t n;
+  const uint64_t *prefixA; /* device, 2 * m words, 16-byte aligned, or NULL */
+  const uint64_t *prefixB; /* device, 2 * n words, 16-byte aligned, or NULL */
 } lsm_fc_input;
 
 /* ---- utilities ---------------------------------------------------------- */
@@ -162,6 +167,18 @@ LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, 
 LSM_API int lsm_collision_mark_str(const lsm_bytes *A, int64_t m, const lsm_bytes *B, int64_t n,
                                    uint32_t *C, uint32_t *lb_B, void *ws, size_t ws_bytes,
                                    void *stream);
+
+/* lsm_collision_mark_str, and also the key prefix tables the call holds
+ * anyway: for key t of A, prefixA[2t] and prefixA[2t+1] are its bytes 0..7
+ * and 8..15 read as big-endian words, zero past the key's end (likewise
+ * prefixB for B). They serve lsm_fc_lengths_scan through lsm_fc_input
+ * (the LCP of two keys then needs no key bytes unless their first 16 bytes
+ * agree). prefixA: device uint64[2m], prefixB: device uint64[2n], both
+ * 16-byte aligned; either may be NULL (that table is not written). */
+LSM_API int lsm_collision_mark_str_prefix(const lsm_bytes *A, int64_t m, const lsm_bytes *B,
+                                          int64_t n, uint32_t *C, uint32_t *lb_B,
+                                          uint64_t *prefixA, uint64_t *prefixB, void *ws,
+                                          size_t ws_bytes, void *stream);
 
 /* ---- a4: rank512 directory ------------------------------------------------ */
 /* [CB] "Temporary rank layouts" and "Corrected record ordinals". Over the

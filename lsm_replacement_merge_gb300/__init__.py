@@ -52,7 +52,8 @@ class _Bytes(ctypes.Structure):
 
 class _FcInput(ctypes.Structure):
     _fields_ = [("keyA", _Bytes), ("valA", _Bytes), ("tombA", ctypes.c_void_p), ("m", ctypes.c_int64),
-                ("keyB", _Bytes), ("valB", _Bytes), ("tombB", ctypes.c_void_p), ("n", ctypes.c_int64)]
+                ("keyB", _Bytes), ("valB", _Bytes), ("tombB", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("prefixA", ctypes.c_void_p), ("prefixB", ctypes.c_void_p)]
 
 
 def build(force: bool = False) -> str:
@@ -79,6 +80,7 @@ def lib():
                 "lsm_merge_stable": ([ctypes.c_int, P, P, I, P, P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_collision_mark": ([P, I, P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_collision_mark_str": ([P, I, P, I, P, P, P, S, P], ctypes.c_int),
+                "lsm_collision_mark_str_prefix": ([P, I, P, I, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_rank_build": ([P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_rank_query": ([P, P, I, P, I, P, P], ctypes.c_int),
                 "lsm_replacement_merge_compact": ([I, I, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
@@ -284,6 +286,31 @@ def collision_mark_str(A: Bytes, B: Bytes, C=None, lb_B=None, ws=None, stream=No
     return C, lb_B
 
 
+def collision_mark_str_prefix(A: Bytes, B: Bytes, C=None, lb_B=None, prefixA=None, prefixB=None,
+                              ws=None, stream=None):
+    """lsm_collision_mark_str_prefix: the string collision mark, and the key
+    prefix tables (uint64[2 count] per source) that FcInput can carry.
+    Returns (C, lb_B, prefixA, prefixB)."""
+    m, n = A.count, B.count
+    dev = A.off.device
+    if C is None:
+        C = _empty((m + 31) // 32, torch.uint32, dev)
+    if lb_B is None:
+        lb_B = _empty(n, torch.uint32, dev)
+    if prefixA is None:
+        prefixA = _empty(max(2 * m, 2), torch.uint64, dev)
+    if prefixB is None:
+        prefixB = _empty(max(2 * n, 2), torch.uint64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_COLLISION_MARK_STR, m, n, dev)
+    a, b = A._c(), B._c()
+    _check("lsm_collision_mark_str_prefix",
+           lib().lsm_collision_mark_str_prefix(ctypes.byref(a), m, ctypes.byref(b), n, _ptr(C),
+                                               _ptr(lb_B), _ptr(prefixA), _ptr(prefixB), _ptr(ws),
+                                               ws.numel(), _stream(stream)))
+    return C, lb_B, prefixA, prefixB
+
+
 def rank_build(C, m: int, dir_=None, d_total=None, ws=None, stream=None):
     dev = C.device
     if dir_ is None:
@@ -371,15 +398,19 @@ def replacement_materialize(A, B, refs, d_count, valA=None, valB=None, tombA=Non
 # a6, a7: front compression
 # ---------------------------------------------------------------------------
 class FcInput:
-    """Keys, values and tombstone bitmaps of both sources, on the device."""
+    """Keys, values and tombstone bitmaps of both sources, on the device, and
+    optionally the key prefix tables from collision_mark_str_prefix."""
 
-    def __init__(self, keyA: Bytes, valA: Bytes, tombA, keyB: Bytes, valB: Bytes, tombB):
+    def __init__(self, keyA: Bytes, valA: Bytes, tombA, keyB: Bytes, valB: Bytes, tombB,
+                 prefixA=None, prefixB=None):
         self.keyA, self.valA, self.tombA = keyA, valA, tombA
         self.keyB, self.valB, self.tombB = keyB, valB, tombB
+        self.prefixA, self.prefixB = prefixA, prefixB
 
     def _c(self):
         return _FcInput(self.keyA._c(), self.valA._c(), _ptr(self.tombA), self.keyA.count,
-                        self.keyB._c(), self.valB._c(), _ptr(self.tombB), self.keyB.count)
+                        self.keyB._c(), self.valB._c(), _ptr(self.tombB), self.keyB.count,
+                        _ptr(self.prefixA), _ptr(self.prefixB))
 
 
 def fc_lengths_scan(fc: FcInput, refs, N: int, lcp=None, ctrl=None, rec_bits=None, bit_off=None,

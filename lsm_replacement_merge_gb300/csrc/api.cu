@@ -144,7 +144,7 @@ LSM_API const char *lsm_status_string(int status) {
   }
 }
 
-LSM_API int lsm_abi_version(void) { return 100; }
+LSM_API int lsm_abi_version(void) { return 101; }
 
 LSM_API int lsm_get_device_status(int32_t *host_status, int reset, void *stream) {
   if (!host_status) return LSM_ERR_ARG;
@@ -225,17 +225,27 @@ LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, 
 LSM_API int lsm_collision_mark_str(const lsm_bytes *A, int64_t m, const lsm_bytes *B, int64_t n,
                                    uint32_t *C, uint32_t *lb_B, void *ws, size_t ws_bytes,
                                    void *stream) {
+  return lsm_collision_mark_str_prefix(A, m, B, n, C, lb_B, nullptr, nullptr, ws, ws_bytes,
+                                       stream);
+}
+
+LSM_API int lsm_collision_mark_str_prefix(const lsm_bytes *A, int64_t m, const lsm_bytes *B,
+                                          int64_t n, uint32_t *C, uint32_t *lb_B,
+                                          uint64_t *prefixA, uint64_t *prefixB, void *ws,
+                                          size_t ws_bytes, void *stream) {
   if (m < 0 || n < 0 || !A || !B) return LSM_ERR_ARG;
   if ((m && (!A->arena || !A->off || !C)) || (n && (!B->arena || !B->off || !lb_B)))
     return LSM_ERR_ARG;
   if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
   if (m + n == 0) return LSM_OK;
   if ((m && !aligned8(A->arena)) || (n && !aligned8(B->arena))) return LSM_ERR_ALIGN;
+  if ((prefixA && !aligned16(prefixA)) || (prefixB && !aligned16(prefixB))) return LSM_ERR_ALIGN;
   if (int r = check_ws(LSM_OP_COLLISION_MARK_STR, m, n, ws, ws_bytes)) return r;
   Carver c{static_cast<uint8_t *>(ws)};
   const int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
   int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
-  return cuda_status(launch_collision_mark_str(*A, m, *B, n, C, lb_B, part, status_ptr(),
+  return cuda_status(launch_collision_mark_str(*A, m, *B, n, C, lb_B, m ? prefixA : nullptr,
+                                               n ? prefixB : nullptr, part, status_ptr(),
                                                static_cast<cudaStream_t>(stream)));
 }
 
@@ -308,6 +318,12 @@ static int check_fc_input(const lsm_fc_input *in) {
   for (const void *p : {static_cast<const void *>(in->keyA.arena), static_cast<const void *>(in->valA.arena),
                         static_cast<const void *>(in->keyB.arena), static_cast<const void *>(in->valB.arena)})
     if (p && !aligned8(p)) return LSM_ERR_ALIGN;
+  // prefix tables: both or neither (an empty side needs none)
+  if ((in->prefixA || in->prefixB) &&
+      ((in->m && !in->prefixA) || (in->n && !in->prefixB)))
+    return LSM_ERR_ARG;
+  if ((in->prefixA && !aligned16(in->prefixA)) || (in->prefixB && !aligned16(in->prefixB)))
+    return LSM_ERR_ALIGN;
   return LSM_OK;
 }
 

@@ -59,6 +59,7 @@ __device__ __forceinline__ uint64_t eg0_len(uint64_t x) {
 struct Source {
   lsm_bytes key, val;
   const uint32_t *tomb;
+  const uint64_t *prefix;  // the key prefix table (2 words per key), or NULL
 };
 
 __device__ __forceinline__ const Source &pick(const Source &a, const Source &b, uint32_t ref) {
@@ -150,10 +151,14 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   const int first = start > 0 ? 0 : 1;
   for (int x = first + tid; x <= cnt; x += kFcThreads) sRefs[x] = refs[start - 1 + x];
   __syncthreads();
+  // with prefix tables (the call checks that every non-empty source has
+  // one; records name non-empty sources only) the keys' first 16 bytes come
+  // with the offsets; otherwise from the arenas, in phase (3)
+  const bool tables = sa.prefix != nullptr || sb.prefix != nullptr;
   // (2) four records per thread per round: every load is issued before any
   // result is stored
   for (int x0 = first + tid; x0 <= cnt; x0 += 4 * kFcThreads) {
-    uint64_t kb[4], ke[4], vb[4], ve[4];
+    uint64_t kb[4], ke[4], vb[4], ve[4], p0[4], p1[4];
     uint32_t tw[4], rr[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -167,6 +172,12 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
       vb[u] = __ldg(src.val.off + idx);
       ve[u] = __ldg(src.val.off + idx + 1);
       tw[u] = src.tomb ? __ldg(src.tomb + (idx >> 5)) : 0u;
+      p0[u] = p1[u] = 0;
+      if (tables) {
+        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2 *>(src.prefix) + idx);
+        p0[u] = v.x;
+        p1[u] = v.y;
+      }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -176,6 +187,8 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
       sKb[x] = kb[u];
       sKl[x] = static_cast<uint32_t>(ke[u] - kb[u]);
       sSrc[x] = (rr[u] & LSM_REF_FROM_B) ? 1 : 0;
+      sP0[x] = p0[u];
+      sP1[x] = p1[u];
       if (x > 0) {
         uint64_t v = 1;  // a tombstone is one bit
         if (!((tw[u] >> (idx & 31)) & 1u)) {
@@ -188,10 +201,11 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   }
   __syncthreads();
 
-  // (3) every slot's key: its first 16 bytes as two big-endian words (zero
-  // past the key's end), each key loaded once although two records
-  // compare it; every load is issued before any result is stored
-  {
+  // (3) without prefix tables, every slot's key: its first 16 bytes as two
+  // big-endian words (zero past the key's end), each key loaded once
+  // although two records compare it; every load is issued before any
+  // result is stored
+  if (!tables) {
     constexpr int kSlotsPerThread = (kFcTile + 1 + kFcThreads - 1) / kFcThreads;
     uint64_t w0[kSlotsPerThread], w1[kSlotsPerThread];
 #pragma unroll
@@ -631,8 +645,9 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
   }
 }
 
-Source make_source(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb) {
-  return Source{key, val, tomb};
+Source make_source(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb,
+                   const uint64_t *prefix = nullptr) {
+  return Source{key, val, tomb, prefix};
 }
 
 }  // namespace
@@ -654,9 +669,10 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
   if (err != cudaSuccess) return err;
   profile_before(s);
   err = launch_kernel(false, fc_lengths_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
-                      kFcThreads, FcLayout::kBytes, s, make_source(in.keyA, in.valA, in.tombA),
-                      make_source(in.keyB, in.valB, in.tombB), refs, N, lcp, ctrl, rec_bits,
-                      bit_off, tile_sum, status);
+                      kFcThreads, FcLayout::kBytes, s,
+                      make_source(in.keyA, in.valA, in.tombA, in.prefixA),
+                      make_source(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, lcp, ctrl,
+                      rec_bits, bit_off, tile_sum, status);
   if (err == cudaSuccess && N > 0)
     err = launch_kernel(false, fc_tile_scan_kernel, 1u, kScanThreads, 0, s, tile_sum, tiles);
   if (err == cudaSuccess && N > 0)

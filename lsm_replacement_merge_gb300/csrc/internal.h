@@ -62,9 +62,11 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
 int64_t rank_build_ctas(int64_t m);
 
 // --- strings.cu ---
+// prefixA / prefixB: optional key prefix tables (2 words per key), or NULL.
 cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,
-                                      uint32_t *C, uint32_t *lb_B, int64_t *part_i,
-                                      int32_t *status, cudaStream_t s);
+                                      uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
+                                      uint64_t *prefixB, int64_t *part_i, int32_t *status,
+                                      cudaStream_t s);
 constexpr int kMarkStrThreads = 128;
 constexpr int kMarkStrItems = 7;
 

@@ -196,7 +196,9 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
                                                                int64_t n,
                                                                const int64_t *__restrict__ part_i,
                                                                uint32_t *__restrict__ C,
-                                                               uint32_t *__restrict__ lb_B) {
+                                                               uint32_t *__restrict__ lb_B,
+                                                               uint64_t *__restrict__ prefixA,
+                                                               uint64_t *__restrict__ prefixB) {
   static_assert(T % 32 == 0, "whole warps");
   pdl_begin();
   constexpr int D = T * E;
@@ -243,11 +245,20 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
       if (x < nst) {
         const uint8_t *arena = x < nA ? A.arena : B.arena;
         const uint64_t len = ke[q] - kb[q];
-        sK0[x] = len > 0 ? load_be64(arena, kb[q], ke[q]) : 0;
-        sK1[x] = len > 8 ? load_be64(arena, kb[q] + 8, ke[q]) : 0;
+        const uint64_t w0 = len > 0 ? load_be64(arena, kb[q], ke[q]) : 0;
+        const uint64_t w1 = len > 8 ? load_be64(arena, kb[q] + 8, ke[q]) : 0;
+        sK0[x] = w0;
+        sK1[x] = w1;
         const int xb = x < nA ? x : x + 1;  // B's starts follow A's end offset
         sBeg[xb] = kb[q];
         if (x == nA - 1 || x == nst - 1) sBeg[xb + 1] = ke[q];
+        // the prefix tables: every key of the tile once (not A[i0-1], B[j1])
+        if (x < nA) {
+          if (prefixA && x >= hp)
+            reinterpret_cast<ulonglong2 *>(prefixA)[i0 - hp + x] = make_ulonglong2(w0, w1);
+        } else if (prefixB && x - nA < nb) {
+          reinterpret_cast<ulonglong2 *>(prefixB)[j0 + (x - nA)] = make_ulonglong2(w0, w1);
+        }
       }
     }
   }
@@ -323,8 +334,9 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
 }  // namespace
 
 cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,
-                                      uint32_t *C, uint32_t *lb_B, int64_t *part_i,
-                                      int32_t * /*status*/, cudaStream_t s) {
+                                      uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
+                                      uint64_t *prefixB, int64_t *part_i, int32_t * /*status*/,
+                                      cudaStream_t s) {
   constexpr int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t nwords = (m + 31) / 32;
@@ -336,7 +348,8 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
   if (err != cudaSuccess || G == 0) return err;
   profile_before(s);
   err = launch_kernel(false, collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>,
-                      static_cast<unsigned>(G), kMarkStrThreads, 0, s, A, m, B, n, part_i, C, lb_B);
+                      static_cast<unsigned>(G), kMarkStrThreads, 0, s, A, m, B, n, part_i, C, lb_B,
+                      prefixA, prefixB);
   profile_after(s);
   return err;
 }

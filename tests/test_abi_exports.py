@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_side_checks_without_gpu(lib):
     lib.lsm_status_string.restype = ctypes.c_char_p
     assert lib.lsm_status_string(0) == b"LSM_OK"
-    assert lib.lsm_abi_version() == 100
+    assert lib.lsm_abi_version() == 101
     size = ctypes.c_size_t(0)
     assert lib.lsm_workspace_size(1, 2, 1 << 26, 1 << 26, ctypes.byref(size)) == 0
     assert size.value > 0

@@ -44,6 +44,22 @@ def gpu_refs(lsm, fc):
     return refs, int(cnt.item())
 
 
+def _prefix_table(arena, off):
+    """Each key's bytes 0..7 and 8..15 as big-endian words, zero past its end
+    (the definition the prefix tables follow), as uint64[2 count]."""
+    off = np.asarray(off, dtype=np.int64)
+    count = len(off) - 1
+    if count <= 0:
+        return np.zeros(0, np.uint64)
+    lens = off[1:] - off[:-1]
+    idx = off[:-1, None] + np.arange(16)[None, :]
+    src = np.asarray(arena, dtype=np.uint8)
+    safe = np.minimum(idx, max(len(src) - 1, 0))
+    rows = np.where(np.arange(16)[None, :] < lens[:, None], src[safe] if len(src) else 0, 0)
+    rows = np.ascontiguousarray(rows.astype(np.uint8))
+    return rows.view(">u8").astype(np.uint64).reshape(-1)
+
+
 def check_fc(lsm, s, extra_words=3):
     fc = device_input(lsm, s)
     if fc.keyA.count + fc.keyB.count == 0:
@@ -67,6 +83,23 @@ def check_fc(lsm, s, extra_words=3):
     got = down(payload)[:nwords]
     assert np.array_equal(got[:len(exp.payload)], exp.payload)
     assert not got[len(exp.payload):].any()        # words past the payload are zero
+    # the same through the key prefix tables that the string mark writes
+    m, n = fc.keyA.count, fc.keyB.count
+    C2, lb2, pA, pB = lsm.collision_mark_str_prefix(fc.keyA, fc.keyB)
+    if m:
+        assert np.array_equal(down(C2)[: (m + 31) // 32], r.C)
+        assert np.array_equal(down(pA)[: 2 * m], _prefix_table(s.A.key_arena, s.A.key_off))
+    if n:
+        assert np.array_equal(down(lb2), r.lb_B)
+        assert np.array_equal(down(pB)[: 2 * n], _prefix_table(s.B.key_arena, s.B.key_off))
+    fcp = lsm.FcInput(fc.keyA, fc.valA, fc.tombA, fc.keyB, fc.valB, fc.tombB, pA, pB)
+    lcp2, ctrl2, rec2, off2 = lsm.fc_lengths_scan(fcp, refs, N)
+    assert np.array_equal(down(lcp2), exp.lcp)
+    assert np.array_equal(down(ctrl2), exp.ctrl)
+    assert np.array_equal(down(rec2), exp.rec_bits)
+    assert np.array_equal(down(off2), exp.bit_off)
+    payload2 = lsm.fc_emit(fcp, refs, N, lcp2, ctrl2, off2, nwords)
+    assert np.array_equal(down(payload2)[:nwords], got)
     return exp
 
 
