@@ -1,16 +1,20 @@
 // strings.cu -- collision bitmap and lower bounds for byte-string keys.
 //
 // The same merge-path tiling as the uint64 collision mark ("Everett:
-// collision bitmap and rank experiment", "Corrected record ordinals"),
-// with keys compared in place in their arenas (strings.cuh). A partition
-// warp finds the co-rank of each tile boundary (A first on ties); each
-// thread bisects its own diagonal inside the tile and walks E merge steps,
-// keeping one comparison per step. For each B element it records the lower
-// bound (A elements before it, minus one when the element just before it
-// is an equal A key); for each A element it sets C_i when the B key at the
-// head equals it. Bits are gathered per tile in shared memory; words inside
-// the tile's A range take plain stores, boundary words atomicOr into the
-// bitmap the partition launch cleared.
+// collision bitmap and rank experiment", "Corrected record ordinals"). A
+// partition launch finds the co-rank of each tile boundary (A first on
+// ties), comparing keys in place in their arenas (strings.cuh). Each tile
+// then stages its keys' prefix caches ("Everett: GPU construction
+// experiment", prefix-cache paragraph: the first 16 bytes, zero-padded, and
+// the length) in shared memory; each thread bisects its own diagonal and
+// walks E merge steps, one comparison per step, on the cached prefixes. For
+// each B element it records the lower bound (A elements before it, minus
+// one when the element just before it is an equal A key); for each A
+// element it sets C_i when the B key at the head equals it. Bits are
+// gathered per tile in shared memory; words inside the tile's A range take
+// plain stores, boundary words atomicOr into the bitmap the partition
+// launch cleared. The tile can also write its keys' cached prefixes out (the
+// key prefix tables of the front-compression lengths pass).
 #include <cuda_runtime.h>
 
 #include <cstdint>
