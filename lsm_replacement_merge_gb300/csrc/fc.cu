@@ -17,7 +17,9 @@
 //
 // fc_lengths_kernel: one CTA per tile of 1024 records; four consecutive
 // records per thread: LCP, control, record length; the tile's total goes to
-// the workspace. fc_tile_scan_kernel (one CTA) turns the tile totals into
+// the workspace. The LCP comes from each key's first 16 bytes, cached once
+// per tile (from the key prefix tables when the input carries them, else
+// from the arenas); only keys agreeing on all 128 bits read further. fc_tile_scan_kernel (one CTA) turns the tile totals into
 // exclusive prefixes, and fc_offsets_kernel adds each tile's prefix to a
 // block scan of its record lengths to write the 64-bit bit offsets. (A
 // single pass with a decoupled lookback was measured slower: tiles finish
