@@ -54,3 +54,39 @@ def test_host_side_checks_without_gpu(lib):
                               ctypes.c_void_p(16), ctypes.c_size_t(0), None) == 6  # workspace
     assert lib.lsm_tune_merge(2, 8, 2, 1) == 1
     assert lib.lsm_tune_merge(2, 7, 2, 1) == 0
+
+
+class _Bytes(ctypes.Structure):
+    _fields_ = [("arena", ctypes.c_void_p), ("off", ctypes.c_void_p)]
+
+
+class _FcInput(ctypes.Structure):
+    _fields_ = [("keyA", _Bytes), ("valA", _Bytes), ("tombA", ctypes.c_void_p), ("m", ctypes.c_int64),
+                ("keyB", _Bytes), ("valB", _Bytes), ("tombB", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("prefixA", ctypes.c_void_p), ("prefixB", ctypes.c_void_p)]
+
+
+def test_prefix_table_checks_without_gpu(lib):
+    # the key prefix tables: 16-byte aligned, and both or neither for the
+    # lengths pass (an empty source needs none); caught on the host
+    I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    a = _Bytes(P(64), P(128))
+    b = _Bytes(P(64), P(128))
+    assert lib.lsm_collision_mark_str_prefix(ctypes.byref(a), I(10), ctypes.byref(b), I(10), P(16),
+                                             P(16), P(24), P(32), P(16), S(1 << 20), None) == 7
+    assert lib.lsm_collision_mark_str_prefix(ctypes.byref(a), I(-1), ctypes.byref(b), I(10), P(16),
+                                             P(16), None, None, P(16), S(1 << 20), None) == 1
+
+    def lengths(prefixA, prefixB, m=10, n=10):
+        fc = _FcInput(_Bytes(P(64), P(128)), _Bytes(P(64), P(128)), None, I(m),
+                      _Bytes(P(64), P(128)), _Bytes(P(64), P(128)), None, I(n),
+                      P(prefixA) if prefixA else None, P(prefixB) if prefixB else None)
+        return lib.lsm_fc_lengths_scan(ctypes.byref(fc), P(16), I(5), P(16), P(16), P(16), P(16),
+                                       None, S(0), None)
+
+    assert lengths(256, None) == 1          # one table for two non-empty sources
+    assert lengths(None, 256) == 1
+    assert lengths(264, 256) == 7           # not 16-byte aligned
+    assert lengths(256, 264) == 7
+    assert lengths(256, None, n=0) == 6     # an empty B needs no table: on to the workspace check
+    assert lengths(None, None) == 6
