@@ -471,6 +471,15 @@ __device__ __forceinline__ void put_arena_smem(uint32_t *buf, int64_t w0, int64_
     const uint32_t *src = reinterpret_cast<const uint32_t *>(arena) + (sb >> 5);
     const int sh = static_cast<int>(sb & 31);
     const int extra = sh ? 1 : 0;  // a shifted word also takes bits of the next
+    if (nfull <= 4) {  // short fields (most values): one batch of at most five loads
+      uint32_t w[5];
+#pragma unroll
+      for (int u = 0; u < 5; ++u)
+        w[u] = u < nfull + extra ? __byte_perm(__ldg(src + u), 0, 0x0123) : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (u < nfull) dst[u] = sh ? __funnelshift_l(w[u + 1], w[u], sh) : w[u];
+    } else
     for (int q0 = 0; q0 < nfull; q0 += 8) {
       const int cnt = nfull - q0 < 8 ? nfull - q0 : 8;
       uint32_t w[9];
@@ -497,8 +506,12 @@ __device__ __forceinline__ void emit_record(uint32_t *buf, int64_t w0, int64_t l
   const int e1 = static_cast<int>(eg0_len(M.c));
   const uint64_t d = M.k - M.l;
   const int e2 = static_cast<int>(eg0_len(d));
-  put_num_smem(buf, w0, lo, hi, M.s, e1, M.c + 1);
-  put_num_smem(buf, w0, lo, hi, M.s + e1, e2, d + 1);
+  if (e1 + e2 <= 64) {  // both codes as one field: EG0(c) EG0(d) = (c+1, d+1) in e1 + e2 bits
+    put_num_smem(buf, w0, lo, hi, M.s, e1 + e2, ((M.c + 1) << e2) | (d + 1));
+  } else {
+    put_num_smem(buf, w0, lo, hi, M.s, e1, M.c + 1);
+    put_num_smem(buf, w0, lo, hi, M.s + e1, e2, d + 1);
+  }
   const int64_t o3 = M.s + e1 + e2;
   put_arena_smem(buf, w0, lo, hi, o3, static_cast<int64_t>(d), M.key.arena, 8 * M.key.begin + M.l,
                  M.key.end);
