@@ -525,6 +525,96 @@ __device__ __forceinline__ void emit_record(uint32_t *buf, int64_t w0, int64_t l
   }
 }
 
+// ---- the same composition in run-relative 32-bit positions ----------------------
+// For every record shorter than 2^30 bits (then all its positions fit in 32
+// bits): p is a field's first bit relative to the run's first bit (it may
+// be negative), the window is [0, H), and buf word j holds run bits
+// [32 j, 32 j + 32). The steps are those of put_num_smem, put_arena_smem
+// and emit_record, on 32-bit positions.
+__device__ __forceinline__ void put_num32(uint32_t *buf, int H, int p, int W, uint64_t V) {
+  int a = p > 0 ? p : 0;
+  const int e = p + W < H ? p + W : H;
+  while (a < e) {
+    const int wb = a & ~31;
+    const int ce = e < wb + 32 ? e : wb + 32;
+    const int len = ce - a;
+    const int q0 = a - p;
+    const uint32_t chunk = static_cast<uint32_t>((V >> (W - q0 - len)) & ((uint64_t(1) << len) - 1));
+    atomicOr(&buf[wb >> 5], chunk << (32 - (a - wb) - len));
+    a = ce;
+  }
+}
+
+__device__ __forceinline__ void put_arena32(uint32_t *buf, int H, int p, int W,
+                                            const uint8_t *arena, uint64_t src_bit) {
+  int x = p > 0 ? p : 0;
+  const int e = p + W < H ? p + W : H;
+  if (x >= e) return;
+  uint64_t sb = src_bit + static_cast<uint64_t>(x - p);
+  if (x & 31) {  // partial first word
+    const int wb = x & ~31;
+    const int ce = e < wb + 32 ? e : wb + 32;
+    const int len = ce - x;
+    atomicOr(&buf[wb >> 5], arena_bits(arena, sb, len) << (wb + 32 - ce));
+    sb += static_cast<uint64_t>(len);
+    x = ce;
+  }
+  const int nfull = (e - x) >> 5;
+  if (nfull > 0) {
+    uint32_t *dst = &buf[x >> 5];
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(arena) + (sb >> 5);
+    const int sh = static_cast<int>(sb & 31);
+    const int extra = sh ? 1 : 0;  // a shifted word also takes bits of the next
+    if (nfull <= 4) {
+      uint32_t w[5];
+#pragma unroll
+      for (int u = 0; u < 5; ++u)
+        w[u] = u < nfull + extra ? __byte_perm(__ldg(src + u), 0, 0x0123) : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (u < nfull) dst[u] = sh ? __funnelshift_l(w[u + 1], w[u], sh) : w[u];
+    } else {
+      for (int q0 = 0; q0 < nfull; q0 += 8) {
+        const int cnt = nfull - q0 < 8 ? nfull - q0 : 8;
+        uint32_t w[9];
+#pragma unroll
+        for (int u = 0; u < 9; ++u)
+          w[u] = u < cnt + extra ? __byte_perm(__ldg(src + q0 + u), 0, 0x0123) : 0u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (u < cnt) dst[q0 + u] = sh ? __funnelshift_l(w[u + 1], w[u], sh) : w[u];
+      }
+    }
+    x += 32 * nfull;
+    sb += uint64_t(32) * static_cast<uint64_t>(nfull);
+  }
+  if (x < e) {  // partial last word
+    const int len = e - x;
+    atomicOr(&buf[x >> 5], arena_bits(arena, sb, len) << (32 - len));
+  }
+}
+
+__device__ __forceinline__ void emit_record32(uint32_t *buf, int H, int P, const RecordMeta &M) {
+  const int e1 = static_cast<int>(eg0_len(M.c));
+  const uint64_t d = M.k - M.l;
+  const int e2 = static_cast<int>(eg0_len(d));
+  if (e1 + e2 <= 64) {
+    put_num32(buf, H, P, e1 + e2, ((M.c + 1) << e2) | (d + 1));
+  } else {
+    put_num32(buf, H, P, e1, M.c + 1);
+    put_num32(buf, H, P + e1, e2, d + 1);
+  }
+  const int o3 = P + e1 + e2;
+  put_arena32(buf, H, o3, static_cast<int>(d), M.key.arena, 8 * M.key.begin + M.l);
+  if (!M.tomb) {  // a tombstone is the single bit 0, already zero
+    const int o4 = o3 + static_cast<int>(d);
+    const uint64_t vb = M.val.end - M.val.begin;
+    const int ev = static_cast<int>(eg0_len(vb));
+    put_num32(buf, H, o4, 1 + ev, (uint64_t(1) << ev) | (vb + 1));
+    put_arena32(buf, H, o4 + 1 + ev, static_cast<int>(8 * vb), M.val.arena, 8 * M.val.begin);
+  }
+}
+
 // Persistent: CTA c writes the contiguous runs [c R / P, (c + 1) R / P) of
 // kEmitRun payload words each (R runs, P CTAs). Only its first run searches
 // bit_off for the record holding the run's first bit; every run then stages
@@ -630,7 +720,10 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
         M.k = 8 * static_cast<uint64_t>(sKl[x]);
         M.tomb = (f & kFlagTomb) != 0;
         M.val = KeyRef{src.val.arena, sVb[x], sVb[x] + sVl[x]};
-        emit_record(sOut, w0, lo, hi, M);
+        if (M.e - M.s < (int64_t(1) << 30))
+          emit_record32(sOut, static_cast<int>(hi - lo), static_cast<int>(M.s - lo), M);
+        else
+          emit_record(sOut, w0, lo, hi, M);
       }
       const bool more = static_cast<int64_t>(sS[R]) < hi && c0 + R < N;
       if (!more && tid == 0) {
