@@ -68,9 +68,6 @@ __device__ __forceinline__ const Source &pick(const Source &a, const Source &b, 
   return (ref & LSM_REF_FROM_B) ? b : a;
 }
 
-__device__ __forceinline__ bool is_tomb(const Source &s, uint32_t idx) {
-  return s.tomb && ((__ldg(s.tomb + (idx >> 5)) >> (idx & 31)) & 1u);
-}
 
 
 struct FcLayout {
