@@ -528,18 +528,20 @@ __device__ __forceinline__ void emit_record(uint32_t *buf, int64_t w0, int64_t l
 // be negative), the window is [0, H), and buf word j holds run bits
 // [32 j, 32 j + 32). The steps are those of put_num_smem, put_arena_smem
 // and emit_record, on 32-bit positions.
+// A numeric field of 1 <= W <= 64 bits (MSB first) at p, ORed in: the
+// value MSB-aligned in 64 bits, shifted into the (at most three) words it
+// meets. The run's window starts on a word boundary and no field reaches
+// past the stream's end, so keeping the words inside [0, (H + 31) / 32) is
+// the whole clip.
 __device__ __forceinline__ void put_num32(uint32_t *buf, int H, int p, int W, uint64_t V) {
-  int a = p > 0 ? p : 0;
-  const int e = p + W < H ? p + W : H;
-  while (a < e) {
-    const int wb = a & ~31;
-    const int ce = e < wb + 32 ? e : wb + 32;
-    const int len = ce - a;
-    const int q0 = a - p;
-    const uint32_t chunk = static_cast<uint32_t>((V >> (W - q0 - len)) & ((uint64_t(1) << len) - 1));
-    atomicOr(&buf[wb >> 5], chunk << (32 - (a - wb) - len));
-    a = ce;
-  }
+  const int WN = (H + 31) >> 5;
+  const uint64_t a = V << (64 - W);
+  const int j = p >> 5;  // floor, p may be negative
+  const int r = p & 31;
+  if (j >= 0 && j < WN) atomicOr(&buf[j], static_cast<uint32_t>(a >> (32 + r)));
+  if (W + r > 32 && j + 1 >= 0 && j + 1 < WN) atomicOr(&buf[j + 1], static_cast<uint32_t>(a >> r));
+  if (W + r > 64 && j + 2 >= 0 && j + 2 < WN)
+    atomicOr(&buf[j + 2], static_cast<uint32_t>(a << (32 - r)));
 }
 
 __device__ __forceinline__ void put_arena32(uint32_t *buf, int H, int p, int W,
