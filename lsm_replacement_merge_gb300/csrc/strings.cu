@@ -248,9 +248,8 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
       const int x = tid + q * T;
       if (x < nst) {
         const uint8_t *arena = x < nA ? A.arena : B.arena;
-        const uint64_t len = ke[q] - kb[q];
-        const uint64_t w0 = len > 0 ? load_be64(arena, kb[q], ke[q]) : 0;
-        const uint64_t w1 = len > 8 ? load_be64(arena, kb[q] + 8, ke[q]) : 0;
+        uint64_t w0, w1;
+        load_prefix16(arena, kb[q], ke[q], w0, w1);
         sK0[x] = w0;
         sK1[x] = w1;
         const int xb = x < nA ? x : x + 1;  // B's starts follow A's end offset

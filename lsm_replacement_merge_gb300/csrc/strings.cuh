@@ -40,6 +40,51 @@ __device__ __forceinline__ uint64_t load_be64(const uint8_t *__restrict__ arena,
   return be;
 }
 
+// Bytes [kb, min(kb + 16, ke)) as two big-endian words (bytes kb..kb+7 in
+// w0, kb+8..kb+15 in w1, zero past ke). Only the aligned 8-byte words that
+// hold key bytes are loaded (at most three); each output 32-bit word is one
+// byte permute of two consecutive 32-bit source words, which does the
+// byte shift and the byte swap at once.
+__device__ __forceinline__ void load_prefix16(const uint8_t *__restrict__ arena, uint64_t kb,
+                                              uint64_t ke, uint64_t &w0, uint64_t &w1) {
+  if (ke <= kb) {
+    w0 = w1 = 0;
+    return;
+  }
+  const uint64_t *w = reinterpret_cast<const uint64_t *>(arena);
+  const uint64_t q = kb >> 3;
+  const uint64_t lastb = kb + 15 < ke - 1 ? kb + 15 : ke - 1;  // last byte needed
+  const uint64_t lim = lastb >> 3;
+  const uint64_t a = __ldg(w + q);
+  const uint64_t b = q + 1 <= lim ? __ldg(w + q + 1) : 0;
+  const uint64_t c = q + 2 <= lim ? __ldg(w + q + 2) : 0;
+  const uint32_t t[6] = {static_cast<uint32_t>(a), static_cast<uint32_t>(a >> 32),
+                         static_cast<uint32_t>(b), static_cast<uint32_t>(b >> 32),
+                         static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32)};
+  const unsigned r = static_cast<unsigned>(kb & 7);
+  const unsigned s = r & 3;
+  const unsigned sel = (s << 12) | ((s + 1) << 8) | ((s + 2) << 4) | (s + 3);
+  const bool hi4 = r >= 4;  // the window starts in the second 32-bit word
+  const uint32_t u0 = hi4 ? t[1] : t[0], u1 = hi4 ? t[2] : t[1], u2 = hi4 ? t[3] : t[2];
+  const uint32_t u3 = hi4 ? t[4] : t[3], u4 = hi4 ? t[5] : t[4];
+  uint32_t o0 = __byte_perm(u0, u1, sel), o1 = __byte_perm(u1, u2, sel);
+  uint32_t o2 = __byte_perm(u2, u3, sel), o3 = __byte_perm(u3, u4, sel);
+  const uint64_t len = ke - kb;
+  if (len < 16) {  // zero the bytes past the key's end
+    const int n = static_cast<int>(len);
+    auto keep = [n](int k) -> uint32_t {  // bytes 4k..4k+3 of the window
+      const int have = n - 4 * k;
+      return have >= 4 ? ~0u : (have <= 0 ? 0u : ~0u << (8 * (4 - have)));
+    };
+    o0 &= keep(0);
+    o1 &= keep(1);
+    o2 &= keep(2);
+    o3 &= keep(3);
+  }
+  w0 = (static_cast<uint64_t>(o0) << 32) | o1;
+  w1 = (static_cast<uint64_t>(o2) << 32) | o3;
+}
+
 struct KeyRef {
   const uint8_t *arena;
   uint64_t begin, end;
