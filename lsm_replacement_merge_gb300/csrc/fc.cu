@@ -214,8 +214,7 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
       if (x <= cnt) {
         const uint8_t *ar = sSrc[x] ? sb.key.arena : sa.key.arena;
         const uint64_t kb = sKb[x], ke = kb + sKl[x];
-        if (ke > kb) w0[q] = load_be64(ar, kb, ke);
-        if (ke > kb + 8) w1[q] = load_be64(ar, kb + 8, ke);
+        load_prefix16(ar, kb, ke, w0[q], w1[q]);
       }
     }
 #pragma unroll
