@@ -272,6 +272,12 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
 
   const int cnt = na + nb;
   const int d = tid * E < cnt ? tid * E : cnt;
+  // 32-bit forms of the walk's index tests: B[j0 + b] exists for b < nbh;
+  // A[i0 + a] for a >= 1 - hp; A index i0 + a is bit wb0 + a of the tile's
+  // first collision word; lower bounds are below 2^31 (checked on the host)
+  const int nbh = static_cast<int>(n - j0 < D + 1 ? n - j0 : D + 1);
+  const int wb0 = static_cast<int>(i0 - (w0 << 5));
+  const uint32_t i0u = static_cast<uint32_t>(i0);
   for (int pass = 0;; ++pass) {
     const bool exact = pass > 0;
     int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
@@ -287,26 +293,26 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
     int ai = lo, bi = d - lo;
     // prev_eq: the element just before B's head in the merge is an A key
     // equal to it (then that B's lower bound is one less than the A count).
-    const bool pq = d < cnt && i0 + ai > 0 && j0 + bi < n;
+    const bool pq = d < cnt && ai + hp > 0 && bi < nbh;
     bool prev_eq = keys.cmp(pq, hp + ai - 1, bi, exact) == 0 && pq;
     for (int s = 0; s < E; ++s) {
       // c = cmp(A head, B head); B head may be B[j1] (one past the tile)
       // only for the collision test of A's last element.
       const bool live = d + s < cnt;
       const bool has_a = ai < na;
-      const bool has_b = j0 + bi < n;
+      const bool has_b = bi < nbh;
       const int c = keys.cmp(live && has_a && has_b, hp + ai, bi, exact);
       if (!live) continue;
       const bool takeA = (bi >= nb) || (has_a && c <= 0);
       if (takeA) {
         if (has_b && c == 0) {
-          const int64_t gi = i0 + ai;
-          atomicOr(&sCw[(gi >> 5) - w0], 1u << (gi & 31));
+          const int x = wb0 + ai;
+          atomicOr(&sCw[x >> 5], 1u << (x & 31));
         }
         prev_eq = has_b && c == 0;
         ++ai;
       } else {
-        sLB[bi] = static_cast<uint32_t>(i0 + ai - (prev_eq ? 1 : 0));
+        sLB[bi] = i0u + static_cast<uint32_t>(ai) - (prev_eq ? 1u : 0u);
         prev_eq = false;
         ++bi;
       }
