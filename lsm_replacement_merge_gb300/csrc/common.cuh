@@ -33,10 +33,12 @@ __device__ __forceinline__ void pdl_begin() {
 __host__ __device__ constexpr int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 // Launches `kern` on stream s, with programmatic stream serialization when
-// `pdl` is set (see pdl_begin). Measured on GB300: it shortens the five-launch
-// replacement step by about 6 us, and lengthens the merge step by about 25 us
-// and the string + FC step by about 90 us, where a kernel launched early holds
-// SM room that the waves of the one before it need (those launch without it).
+// `pdl` is set (see pdl_begin). It pays where the kernel before leaves SM
+// room free (a partition of a few blocks per SM, a one-CTA scan): measured on
+// GB300, the replacement chain gains ~6 us and the merge's tile launch ~1 us.
+// Where the kernel before runs in waves, an early-launched kernel holds room
+// those waves need: the string + FC chain lost ~90 us with every launch
+// early, so its wave-filling launches go without it.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), unsigned grid, unsigned block,
                           size_t smem, cudaStream_t s, Args &&...args) {
