@@ -53,6 +53,14 @@ def _load():
                 fn = getattr(_lib, name)
                 fn.argtypes = [P, P, I, P, P, I, P, P, P]
                 fn.restype = None
+            for name in ("oracle_mergesort_pass_i32", "oracle_mergesort_pass_u64"):
+                fn = getattr(_lib, name)
+                fn.argtypes = [P, P, I, I, P, P]
+                fn.restype = None
+            for name in ("oracle_merge_sort_i32", "oracle_merge_sort_u64"):
+                fn = getattr(_lib, name)
+                fn.argtypes = [P, P, I, P, P]
+                fn.restype = I
             for name in ("oracle_partition_i32", "oracle_partition_u64"):
                 fn = getattr(_lib, name)
                 fn.argtypes = [P, I, P, I, I, P]
@@ -137,6 +145,38 @@ def corank(A, B, k):
     if k == 0:
         return 0
     return int(partition(A, B, k)[1, 0])
+
+
+def merge_sort_pass(keys, width, pay=None):
+    """One bottom-up merge sort pass ([CH14] 14.2): adjacent runs of `width`
+    merged pairwise, the left run first on ties. Returns (keys, payload|None)."""
+    kind = _kind(keys)
+    keys = _c(keys, kind)
+    n = len(keys)
+    pay = _c(pay, np.uint32)
+    out = np.empty(n, dtype=kind)
+    out_pay = np.empty(n, dtype=np.uint32) if pay is not None else None
+    fn = (_load().oracle_mergesort_pass_i32 if kind == np.int32
+          else _load().oracle_mergesort_pass_u64)
+    fn(_p(keys), _p(pay), n, int(width), _p(out), _p(out_pay))
+    return out, out_pay
+
+
+def merge_sort(keys, pay=None):
+    """Bottom-up merge sort ([CH14] 14.2), widths 1, 2, 4, ... Returns
+    (keys, payload|None, passes)."""
+    kind = _kind(keys)
+    keys = _c(keys, kind)
+    n = len(keys)
+    pay = _c(pay, np.uint32)
+    out = np.empty(n, dtype=kind)
+    out_pay = np.empty(n, dtype=np.uint32) if pay is not None else None
+    fn = (_load().oracle_merge_sort_i32 if kind == np.int32
+          else _load().oracle_merge_sort_u64)
+    passes = fn(_p(keys), _p(pay), n, _p(out), _p(out_pay))
+    if passes < 0:
+        raise MemoryError("oracle merge sort: scratch allocation failed")
+    return out, out_pay, int(passes)
 
 
 def _kind(A):

@@ -10,7 +10,7 @@
  * Every function follows the definition it cites:
  *   [MP]  "Day 36: CUDA merge path: merging sorted arrays in parallel"
  *         (gpu-preview.ayushworks.com/days/36-merge-path)
- *   [CH14] "Chapter 14: Merge Sort and Sample Sort", section 14.1
+ *   [CH14] "Chapter 14: Merge Sort and Sample Sort", sections 14.1 and 14.2
  *         (maximumbeings.github.io/dsa_cuda_from_first_principles)
  *   [CB]  "Everett: collision bitmap and rank experiment"
  *         (ekmett.github.io/everett/collision-bitmap-and-rank-experiment.html)
@@ -104,6 +104,56 @@ ORACLE_DEFINE_MERGE(oracle_merge_u64, uint64_t)
 
 ORACLE_DEFINE_PARTITION(oracle_partition_i32, int32_t)
 ORACLE_DEFINE_PARTITION(oracle_partition_u64, uint64_t)
+
+/* ------------------------------------------------------------------------ */
+/* Bottom-up merge sort. [CH14] section 14.2 "From Merge to Merge Sort":    */
+/* every element starts as a sorted run of length 1; one pass merges each   */
+/* pair of adjacent runs of the current width with the stable merge above   */
+/* (the left run plays A, so equal keys keep their input order), and the    */
+/* width doubles until a single run covers the array. A run with no right   */
+/* partner at the end of a pass is copied through unchanged (the stable     */
+/* merge with an empty B). The pair offset is added back before the merge   */
+/* ("COMMON TRAP" of that section): pair p covers [2pw, min(2pw+2w, n)).     */
+/* ------------------------------------------------------------------------ */
+#define ORACLE_DEFINE_SORT(PASS, SORT, MERGE, KEY)                            \
+    void PASS(const KEY *in, const uint32_t *pay, int64_t n, int64_t width,   \
+              KEY *out, uint32_t *out_pay) {                                  \
+        int64_t start;                                                        \
+        for (start = 0; start < n; start += 2 * width) {                      \
+            int64_t mid = start + width < n ? start + width : n;              \
+            int64_t end = start + 2 * width < n ? start + 2 * width : n;      \
+            MERGE(in + start, pay ? pay + start : NULL, mid - start,          \
+                  in + mid, pay ? pay + mid : NULL, end - mid, out + start,   \
+                  out_pay ? out_pay + start : NULL, NULL);                    \
+        }                                                                     \
+    }                                                                         \
+    /* Returns the number of passes, or -1 if scratch could not be had. */    \
+    int64_t SORT(const KEY *in, const uint32_t *pay, int64_t n, KEY *out,     \
+                 uint32_t *out_pay) {                                         \
+        KEY *tk = (KEY *)malloc((size_t)(n > 0 ? n : 1) * sizeof(KEY));       \
+        uint32_t *tp = pay ? (uint32_t *)malloc((size_t)(n > 0 ? n : 1) * 4)  \
+                           : NULL;                                            \
+        int64_t width, passes = 0;                                            \
+        if (!tk || (pay && !tp)) {                                            \
+            free(tk);                                                         \
+            free(tp);                                                         \
+            return -1;                                                        \
+        }                                                                     \
+        memcpy(out, in, (size_t)n * sizeof(KEY));                             \
+        if (pay) memcpy(out_pay, pay, (size_t)n * 4);                         \
+        for (width = 1; width < n; width *= 2) {                              \
+            PASS(out, pay ? out_pay : NULL, n, width, tk, tp);                \
+            memcpy(out, tk, (size_t)n * sizeof(KEY));                         \
+            if (pay) memcpy(out_pay, tp, (size_t)n * 4);                      \
+            passes++;                                                         \
+        }                                                                     \
+        free(tk);                                                             \
+        free(tp);                                                             \
+        return passes;                                                        \
+    }
+
+ORACLE_DEFINE_SORT(oracle_mergesort_pass_i32, oracle_merge_sort_i32, oracle_merge_i32, int32_t)
+ORACLE_DEFINE_SORT(oracle_mergesort_pass_u64, oracle_merge_sort_u64, oracle_merge_u64, uint64_t)
 
 /* ------------------------------------------------------------------------ */
 /* Byte-string order: unsigned lexicographic bytes, a proper prefix sorts   */

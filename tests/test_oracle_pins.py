@@ -111,6 +111,54 @@ def test_merge_matches_stable_sort(m, n):
 
 
 # ---------------------------------------------------------------------------
+# Bottom-up merge sort ([CH14] 14.2)
+# ---------------------------------------------------------------------------
+def test_mergesort_worked_example(golden):
+    g = golden("mergesort_chapter14.txt")
+    for dt in (np.int32, np.uint64):
+        x = np.array(g["input"], dt)
+        for w in (1, 2, 4):
+            x, _ = oracle.merge_sort_pass(x, w)
+            assert x.tolist() == g["after_width_%d" % w]
+        keys, _, passes = oracle.merge_sort(np.array(g["input"], dt))
+        assert keys.tolist() == g["after_width_4"] and passes == g["passes"][0]
+    # the section's pair view: position 5 of the width-2 pass belongs to the
+    # pair starting at 4, whose output is the merge of its two runs alone
+    x1 = np.array(g["after_width_1"], np.int32)
+    x2, _ = oracle.merge_sort_pass(x1, 2)
+    p0, loc = g["pair_view_pair_start"][0], g["pair_view_local"][0]
+    assert p0 + loc == g["pair_view_position"][0]
+    pair = oracle.merge(x1[p0:p0 + 2], x1[p0 + 2:p0 + 4])[0]
+    assert x2[p0:p0 + 4].tolist() == pair.tolist()
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 7, 8, 9, 1000, 4096, 4097, 30011])
+def test_mergesort_matches_stable_sort(n):
+    rng = np.random.default_rng(n + 17)
+    for dt, lo, hi in ((np.int32, -8, 8), (np.int32, -2**31, 2**31 - 1),
+                       (np.uint64, 0, 2**64 - 1), (np.uint64, 0, 5)):
+        keys = rng.integers(lo, hi, size=n, dtype=np.int64 if dt == np.int32 else np.uint64,
+                            endpoint=True).astype(dt)
+        pay = np.arange(n, dtype=np.uint32)
+        out, out_pay, passes = oracle.merge_sort(keys, pay)
+        order = np.argsort(keys, kind="stable")
+        assert (out == keys[order]).all()
+        assert (out_pay == order).all()
+        assert passes == (0 if n <= 1 else int(np.ceil(np.log2(n))))
+
+
+def test_mergesort_pass_keeps_a_lone_tail_run():
+    # n = 7 at width 4: one pair [0, 8) clipped to 7 merges runs [0,4) and
+    # [4,7); at width 8 the whole array is a lone run and is copied
+    x = np.array([0, 1, 7, 9, 1, 2, 7], np.int32)
+    y, p = oracle.merge_sort_pass(x, 8, np.arange(7, dtype=np.uint32))
+    assert y.tolist() == x.tolist() and p.tolist() == list(range(7))
+    y, p = oracle.merge_sort_pass(x, 4, np.arange(7, dtype=np.uint32))
+    assert y.tolist() == [0, 1, 1, 2, 7, 7, 9]
+    assert p.tolist() == [0, 1, 4, 5, 2, 6, 3]  # equal keys: left run first
+
+
+# ---------------------------------------------------------------------------
 # Replacement merge
 # ---------------------------------------------------------------------------
 def _chronological(A_keys, B_keys):
