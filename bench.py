@@ -62,7 +62,8 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true", help="also time every items-per-thread setting")
     ap.add_argument("--only", default="",
                     help="run only this extra workload (merge_i32_4096, replace_u64_12M_4M, "
-                         "replace_skewed_2pow24_65536, strings_fc_4M_4M) and print its result; "
+                         "replace_skewed_2pow24_65536, merge_sort_u64_2pow27, strings_fc_4M_4M) "
+                         "and print its result; "
                          "for profiler captures")
     ap.add_argument("--log2", type=int, default=26,
                     help="headline inputs hold 2^log2 keys each (26 = the full workload; smaller "
@@ -559,10 +560,46 @@ def extra_workloads(lsm, torch, dev, peak, args, only=""):
                       ("replace_skewed_2pow24_65536", synth.replace_skewed)):
         if wanted(name):
             extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, args.sweep)
+    if wanted("merge_sort_u64_2pow27"):
+        extra_merge_sort(lsm, torch, dev, peak, steps, flush, out)
     if args.no_strings or not wanted("strings_fc_4M_4M"):
         return out
     extra_strings(lsm, torch, dev, peak, steps, flush, out)
     return out
+
+
+def extra_merge_sort(lsm, torch, dev, peak, steps, flush, out):
+    """Bottom-up merge sort of 2^27 uniform uint64 keys with uint32 payloads:
+    the block sort to runs of 2816, then one partition + tile launch per pass."""
+    si = synth.sort_u64()
+    N = len(si.keys)
+    keys, pay = torch.from_numpy(si.keys).to(dev), torch.from_numpy(si.pay).to(dev)
+    ok = torch.empty_like(keys)
+    op = torch.empty_like(pay)
+    ws = lsm.workspace(lsm.LSM_OP_MERGE_SORT, N, 0, dev, lsm.LSM_KEY_U64)
+    ms, per = time_pipeline(torch, [("merge_sort", lambda: lsm.merge_sort(
+        keys, pay, out_keys=ok, out_pay=op, ws=ws))], steps, flush)
+    tile = 256 * 11
+    passes = 0
+    w = tile
+    while w < N:
+        passes += 1
+        w *= 2
+    pass_bytes = 2 * 12 * N  # one pass reads and writes every key and payload
+    last = per["merge_sort"]
+    out["merge_sort_u64_2pow27"] = {
+        "N": N, "ms_per_step": ms, "gelem_s": N / (ms * 1e-3) / 1e9,
+        "passes": {"block_sort": 1, "global": passes},
+        "algorithmic_bytes": (1 + passes) * pass_bytes,
+        "gbs": (1 + passes) * pass_bytes / (ms * 1e-3) / 1e9,
+        "frac": (1 + passes) * pass_bytes / (ms * 1e-3) / 1e9 / peak,
+        "last_pass_tile_kernel_ms": last,
+        "last_pass_tile_kernel_gbs": pass_bytes / (last * 1e-3) / 1e9,
+        "last_pass_tile_kernel_frac": pass_bytes / (last * 1e-3) / 1e9 / peak,
+        "gpu_launches_per_step": 1 + 2 * passes,
+        "l2": "flushed (256 MiB write) before every step; inputs 1.5 GiB"}
+    del keys, pay, ok, op, ws
+    torch.cuda.empty_cache()
 
 
 def extra_merge_i32(lsm, torch, dev, steps, out):

@@ -4,7 +4,7 @@
  * One shared library (liblsmmerge.so), hand-written CUDA kernels for sm_103a.
  * The operations follow these pages:
  *   [MP]   "Day 36: CUDA merge path: merging sorted arrays in parallel"
- *   [CH14] "Chapter 14: Merge Sort and Sample Sort", section 14.1
+ *   [CH14] "Chapter 14: Merge Sort and Sample Sort", sections 14.1, 14.2
  *   [CB]   "Everett: collision bitmap and rank experiment"
  *   [GC]   "Everett: GPU construction experiment"
  *   [BP]   "Everett: byte-profile GPU merge"
@@ -76,7 +76,8 @@ enum {
   LSM_OP_COLLISION_MARK_STR = 3,
   LSM_OP_RANK_BUILD = 4,
   LSM_OP_REPLACEMENT_COMPACT = 5,
-  LSM_OP_FC_LENGTHS_SCAN = 6
+  LSM_OP_FC_LENGTHS_SCAN = 6,
+  LSM_OP_MERGE_SORT = 7
 };
 
 #define LSM_REF_FROM_B 0x80000000u
@@ -149,6 +150,24 @@ LSM_API int lsm_merge_path_partition(int key_type, const void *A, int64_t m, con
 LSM_API int lsm_merge_stable(int key_type, const void *A, const uint32_t *Apay, int64_t m,
                              const void *B, const uint32_t *Bpay, int64_t n, void *out_keys,
                              uint32_t *out_pay, void *ws, size_t ws_bytes, void *stream);
+
+/* ---- f1: bottom-up merge sort -------------------------------------------- */
+/* [CH14] section 14.2 "From Merge to Merge Sort: Repeated Pairwise Merging":
+ * sorts N keys by passes of the stable merge above over adjacent runs whose
+ * width doubles each pass (1, 2, 4, ...), the left run first on ties, so the
+ * result is the stable sort: out_keys ascending, equal keys in input order,
+ * and, when pay and out_pay are both non-NULL, each key's 32-bit payload
+ * beside it (payloads never take part in comparisons; both NULL or both
+ * non-NULL).
+ * keys: device, N elements of key_type (LSM_KEY_I32 compares signed); pay:
+ * device uint32[N] or NULL; out_keys / out_pay: device, N elements, must not
+ * alias the inputs. All 16-byte aligned. N < 2^40. The input is not
+ * modified. ws: at least lsm_workspace_size(LSM_OP_MERGE_SORT, key_type, N,
+ * 0) bytes (one N-element copy of keys and payloads for the passes to
+ * alternate with, plus the partition array). N = 0 returns LSM_OK. */
+LSM_API int lsm_merge_sort(int key_type, const void *keys, const uint32_t *pay, int64_t N,
+                           void *out_keys, uint32_t *out_pay, void *ws, size_t ws_bytes,
+                           void *stream);
 
 /* ---- a3: collision bitmap ------------------------------------------------- */
 /* [CB] "Corrected record ordinals": for every B_j, lb_B[j] = lower_bound(A,

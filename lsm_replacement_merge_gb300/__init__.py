@@ -33,6 +33,7 @@ LSM_OP_COLLISION_MARK_STR = 3
 LSM_OP_RANK_BUILD = 4
 LSM_OP_REPLACEMENT_COMPACT = 5
 LSM_OP_FC_LENGTHS_SCAN = 6
+LSM_OP_MERGE_SORT = 7
 REF_FROM_B = 0x80000000
 ORD_DROPPED = 0xFFFFFFFF
 
@@ -78,6 +79,7 @@ def lib():
                 "lsm_workspace_size": ([ctypes.c_int, ctypes.c_int, I, I, P], ctypes.c_int),
                 "lsm_merge_path_partition": ([ctypes.c_int, P, I, P, I, I, P, P], ctypes.c_int),
                 "lsm_merge_stable": ([ctypes.c_int, P, P, I, P, P, I, P, P, P, S, P], ctypes.c_int),
+                "lsm_merge_sort": ([ctypes.c_int, P, P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_collision_mark": ([P, I, P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_collision_mark_str": ([P, I, P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_collision_mark_str_prefix": ([P, I, P, I, P, P, P, P, P, S, P], ctypes.c_int),
@@ -226,6 +228,22 @@ def merge_stable(A, B, Apay=None, Bpay=None, out_keys=None, out_pay=None, ws=Non
            lib().lsm_merge_stable(kt, _ptr(A), _ptr(Apay), m, _ptr(B), _ptr(Bpay), n,
                                   _ptr(out_keys), _ptr(out_pay), _ptr(ws), ws.numel(),
                                   _stream(stream)))
+    return out_keys, out_pay
+
+
+def merge_sort(keys, pay=None, out_keys=None, out_pay=None, ws=None, stream=None):
+    kt = _key_type(keys)
+    N = keys.numel()
+    dev = keys.device
+    if out_keys is None:
+        out_keys = _empty(N, keys.dtype, dev)
+    if pay is not None and out_pay is None:
+        out_pay = _empty(N, torch.uint32, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_MERGE_SORT, N, 0, dev, kt)
+    _check("lsm_merge_sort",
+           lib().lsm_merge_sort(kt, _ptr(keys), _ptr(pay), N, _ptr(out_keys), _ptr(out_pay),
+                                _ptr(ws), ws.numel(), _stream(stream)))
     return out_keys, out_pay
 
 

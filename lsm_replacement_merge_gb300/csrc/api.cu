@@ -81,9 +81,25 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? LSM_OK : LSM_ERR_CUDA
 
 int64_t merge_tiles_max(int64_t total) { return (total + kMinMergeTile - 1) / kMinMergeTile; }
 
-size_t ws_bytes_for(int op, int64_t m, int64_t n) {
+// Scratch of lsm_merge_sort: the alternate key and payload buffers of its
+// passes, then the partition array.
+template <typename KP, typename PP, typename IP>
+void carve_merge_sort(Carver &c, int key_type, int64_t N, KP *keys, PP *pay, IP *part) {
+  const int64_t D = merge_sort_tile();
+  void *k = c.take<uint8_t>(N * (key_type == LSM_KEY_I32 ? 4 : 8));
+  uint32_t *p = c.take<uint32_t>(N);
+  int64_t *q = c.take<int64_t>((N + D - 1) / D + 1);
+  if (keys) *keys = k;
+  if (pay) *pay = p;
+  if (part) *part = q;
+}
+
+size_t ws_bytes_for(int op, int64_t m, int64_t n, int key_type = LSM_KEY_U64) {
   Carver c{nullptr};
   switch (op) {
+    case LSM_OP_MERGE_SORT:
+      carve_merge_sort<void *, uint32_t *, int64_t *>(c, key_type, m, nullptr, nullptr, nullptr);
+      break;
     case LSM_OP_MERGE_STABLE:
       c.take<int64_t>(merge_tiles_max(m + n) + 1);
       break;
@@ -114,10 +130,11 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n) {
   return static_cast<size_t>(align_up(static_cast<int64_t>(c.used), 256)) + 256;
 }
 
-int check_ws(int op, int64_t m, int64_t n, const void *ws, size_t ws_bytes) {
+int check_ws(int op, int64_t m, int64_t n, const void *ws, size_t ws_bytes,
+             int key_type = LSM_KEY_U64) {
   if (!ws) return LSM_ERR_WORKSPACE;
   if (!aligned16(ws)) return LSM_ERR_ALIGN;
-  if (ws_bytes < ws_bytes_for(op, m, n)) return LSM_ERR_WORKSPACE;
+  if (ws_bytes < ws_bytes_for(op, m, n, key_type)) return LSM_ERR_WORKSPACE;
   return LSM_OK;
 }
 
@@ -160,10 +177,11 @@ LSM_API int lsm_get_device_status(int32_t *host_status, int reset, void *stream)
 
 LSM_API int lsm_workspace_size(int op, int key_type, int64_t m, int64_t n, size_t *bytes) {
   if (!bytes || m < 0 || n < 0) return LSM_ERR_ARG;
-  if (op == LSM_OP_MERGE_STABLE && key_type != LSM_KEY_I32 && key_type != LSM_KEY_U64)
+  if ((op == LSM_OP_MERGE_STABLE || op == LSM_OP_MERGE_SORT) && key_type != LSM_KEY_I32 &&
+      key_type != LSM_KEY_U64)
     return LSM_ERR_DTYPE;
-  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_FC_LENGTHS_SCAN) return LSM_ERR_ARG;
-  *bytes = ws_bytes_for(op, m, n);
+  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_MERGE_SORT) return LSM_ERR_ARG;
+  *bytes = ws_bytes_for(op, m, n, key_type);
   return LSM_OK;
 }
 
@@ -203,6 +221,29 @@ LSM_API int lsm_merge_stable(int key_type, const void *A, const uint32_t *Apay, 
   const void *a = A ? A : B, *b = B ? B : A;
   return cuda_status(launch_merge_stable(key_type, a, ap, m, b, bp, n, out_keys, pay ? out_pay : nullptr,
                                          part, status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_merge_sort(int key_type, const void *keys, const uint32_t *pay, int64_t N,
+                           void *out_keys, uint32_t *out_pay, void *ws, size_t ws_bytes,
+                           void *stream) {
+  if (key_type != LSM_KEY_I32 && key_type != LSM_KEY_U64) return LSM_ERR_DTYPE;
+  if (N < 0) return LSM_ERR_ARG;
+  if (!pay != !out_pay) return LSM_ERR_ARG;
+  if (N && (!keys || !out_keys)) return LSM_ERR_ARG;
+  if (N > (int64_t(1) << 40)) return LSM_ERR_OVERFLOW;
+  if (N == 0) return LSM_OK;
+  for (const void *p : {keys, static_cast<const void *>(out_keys), static_cast<const void *>(pay),
+                        static_cast<const void *>(out_pay)})
+    if (p && !aligned16(p)) return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_MERGE_SORT, N, 0, ws, ws_bytes, key_type)) return r;
+  Carver c{static_cast<uint8_t *>(ws)};
+  void *tmp = nullptr;
+  uint32_t *tmp_pay = nullptr;
+  int64_t *part = nullptr;
+  carve_merge_sort(c, key_type, N, &tmp, &tmp_pay, &part);
+  return cuda_status(launch_merge_sort(key_type, keys, pay, N, out_keys, out_pay, tmp,
+                                       pay ? tmp_pay : nullptr, part, status_ptr(),
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,

@@ -36,6 +36,13 @@ cudaError_t launch_merge_stable(int key_type, const void *A, const uint32_t *Apa
                                 const void *B, const uint32_t *Bpay, int64_t n, void *out,
                                 uint32_t *out_pay, int64_t *part_i, int32_t *status,
                                 cudaStream_t s);
+// Bottom-up merge sort: block sort to runs of merge_sort_tile() elements,
+// then one partition + tile-kernel launch per pass. tmp / tmp_pay: N
+// elements each (tmp_pay only with a payload); part: ceil(N / tile) + 1.
+int64_t merge_sort_tile();
+cudaError_t launch_merge_sort(int key_type, const void *in, const uint32_t *in_pay, int64_t N,
+                              void *out, uint32_t *out_pay, void *tmp, uint32_t *tmp_pay,
+                              int64_t *part, int32_t *status, cudaStream_t s);
 
 // --- replace.cu ---
 cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,

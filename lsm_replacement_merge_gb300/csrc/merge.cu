@@ -1,4 +1,5 @@
-// merge.cu -- merge path partition and the stable merge of two sorted arrays.
+// merge.cu -- merge path partition, the stable merge of two sorted arrays,
+// and the bottom-up merge sort built from that merge.
 //
 // "Day 36: CUDA merge path", section "The merge matrix, and the diagonal
 // that cuts it": the first k merge outputs are A[0, i) and B[0, k - i) for
@@ -152,11 +153,17 @@ static_assert(sizeof(TileDesc) == 32, "descriptor slot");
 // stages tiles. CTA c handles tiles c, c + P, c + 2P, ... (P = gridDim.x).
 // Stage s = r % S holds the r-th tile; full[s] completes when its bulk copies
 // land, empty[s] when every merging warp has finished reading it.
-template <typename K, bool PAY, int E, int S, int NOUT>
+//
+// SEG selects one pass of the bottom-up merge sort instead of one merge: A
+// and B are then the same array of m = n = N elements, made of sorted runs
+// of w elements, and tile g (whose D outputs lie inside one pair of runs,
+// since D divides 2w) merges its pair's left run (as A) with its right run
+// (as B). part_i then holds co-ranks local to each boundary's pair.
+template <typename K, bool PAY, int E, int S, int NOUT, bool SEG = false>
 __global__ void __launch_bounds__(kMergeThreads + 32) merge_tile_kernel(
     const K *__restrict__ A, const uint32_t *__restrict__ Apay, int64_t m, const K *__restrict__ B,
     const uint32_t *__restrict__ Bpay, int64_t n, const int64_t *__restrict__ part_i, int64_t G,
-    K *__restrict__ out, uint32_t *__restrict__ out_pay, int32_t *status) {
+    K *__restrict__ out, uint32_t *__restrict__ out_pay, int32_t *status, int64_t w) {
   pdl_begin();
   using L = MergeLayout<K, PAY, E, S, NOUT>;
   constexpr int D = L::D;
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(kMergeThreads + 32) merge_tile_kernel(
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L::kEmpty);
   TileDesc *desc = reinterpret_cast<TileDesc *>(smem + L::kMeta);
   const int tid = threadIdx.x;
-  const int64_t total = m + n;
+  const int64_t total = SEG ? m : m + n;
   const int64_t P = gridDim.x;
 
   if (tid == 0) {
@@ -205,10 +212,22 @@ __global__ void __launch_bounds__(kMergeThreads + 32) merge_tile_kernel(
             failed = 1;
           } else {
             const int64_t k0 = g * D, k1 = k0 + D < total ? k0 + D : total;
-            const int64_t j0 = k0 - i0, j1 = k1 - i1;
-            const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
+            // the tile's spans [a0, a1) of A and [j0, j1) of B
+            int64_t a0 = i0, a1 = i1, j0 = k0 - i0, j1 = k1 - i1;
+            if (SEG) {
+              const int64_t ps = (k0 / (2 * w)) * (2 * w);  // the pair's first element
+              const int64_t la = w < total - ps ? w : total - ps;
+              const int64_t lab = 2 * w < total - ps ? 2 * w : total - ps;
+              // the pair's last tile ends where the pair ends: all of its left run
+              const int64_t e1 = k1 - ps == lab ? la : i1;
+              a0 = ps + i0;
+              a1 = ps + e1;
+              j0 = ps + la + (k0 - ps - i0);
+              j1 = ps + la + (k1 - ps - e1);
+            }
+            const int na = static_cast<int>(a1 - a0), nb = static_cast<int>(j1 - j0);
             uint8_t *stage = smem + L::kStage0 + s * L::kStageBytes;
-            const StagePlan pa = stage_plan_overfetch<SZ>(i0, na, m);
+            const StagePlan pa = stage_plan_overfetch<SZ>(a0, na, m);
             const StagePlan pb = stage_plan_overfetch<SZ>(j0, nb, n);
             K *bufA = reinterpret_cast<K *>(stage);
             const int32_t offB = static_cast<int32_t>(stage_capacity_bytes<SZ>(pa.span) / SZ);
@@ -221,20 +240,20 @@ __global__ void __launch_bounds__(kMergeThreads + 32) merge_tile_kernel(
             td.offPA = td.offPB = 0;
             // ragged ends (only where a span touches the end of its array) by
             // plain loads, before the arrive so that the barrier covers them
-            for (int64_t x = pa.tail_from; x < i1; ++x) bufA[x - pa.first] = A[x];
+            for (int64_t x = pa.tail_from; x < a1; ++x) bufA[x - pa.first] = A[x];
             for (int64_t x = pb.tail_from; x < j1; ++x) bufB[x - pb.first] = B[x];
             uint32_t tx = pa.bulk + pb.bulk;
             StagePlan qa{}, qb{};
             uint32_t *bufPA = nullptr, *bufPB = nullptr;
             if (PAY) {
-              qa = stage_plan_overfetch<4>(i0, na, m);
+              qa = stage_plan_overfetch<4>(a0, na, m);
               qb = stage_plan_overfetch<4>(j0, nb, n);
               bufPA = reinterpret_cast<uint32_t *>(stage + L::kKeysBytes);
               const int32_t offPB = static_cast<int32_t>(stage_capacity_bytes<4>(qa.span) / 4);
               bufPB = bufPA + offPB;
               td.offPA = qa.lead;
               td.offPB = offPB + qb.lead;
-              for (int64_t x = qa.tail_from; x < i1; ++x) bufPA[x - qa.first] = Apay[x];
+              for (int64_t x = qa.tail_from; x < a1; ++x) bufPA[x - qa.first] = Apay[x];
               for (int64_t x = qb.tail_from; x < j1; ++x) bufPB[x - qb.first] = Bpay[x];
               tx += qa.bulk + qb.bulk;
             }
@@ -372,7 +391,7 @@ cudaError_t launch_merge_tiles(const K *A, const uint32_t *Apay, int64_t m, cons
   // the tile CTAs' room free (measured: step 0.5102 ms against 0.5114 ms)
   const cudaError_t err = launch_kernel(true, kern, static_cast<unsigned>(grid), threads,
                                         L::kBytes, s, A, Apay, m, B, Bpay, n, part_i, G, out,
-                                        out_pay, status);
+                                        out_pay, status, int64_t(0));
   profile_after(s);
   return err;
 }
@@ -418,7 +437,229 @@ cudaError_t launch_partition_typed(const K *A, int64_t m, const K *B, int64_t n,
                        m, B, n, D, G, out_i, out_ij);
 }
 
+// ---- bottom-up merge sort ([CH14] section 14.2) ------------------------------------
+// The sort runs the chapter's passes (runs of width w merged in pairs, w
+// doubling) with two changes of where the passes run, not of what they
+// compute: the passes of widths 1 .. D/2 happen inside one CTA's shared
+// memory (block_sort_kernel leaves sorted runs of D elements), and each
+// pass from w = D on is one segmented partition plus one launch of the
+// persistent tile kernel, whose tiles never straddle a pair because D
+// divides 2w.
+constexpr int kSortE = 11;  // items per thread of the sort's tiles
+constexpr int kSortS = 2;   // input stages of its tile kernel
+constexpr int kSortD = kMergeThreads * kSortE;
+
+template <typename K>
+__device__ __forceinline__ K sort_key_max();
+template <>
+__device__ __forceinline__ int32_t sort_key_max<int32_t>() { return 0x7fffffff; }
+template <>
+__device__ __forceinline__ uint64_t sort_key_max<uint64_t>() { return ~0ull; }
+
+// Sorts each tile of D = 256 E elements stably. Every thread sorts its E
+// consecutive elements in registers (odd-even transposition: E rounds of
+// compare-exchange that swaps only strictly greater pairs, so it is stable;
+// positions past the tile's end hold the largest key and stay behind the
+// real elements, equal or not), then the CTA runs the chapter's passes over
+// shared memory with widths E, 2E, ..., each thread finding the pair of
+// its E outputs from its output position, its co-rank inside that pair by
+// bisection (ties to the left run), and merging E outputs.
+template <typename K, bool PAY, int E>
+__global__ void __launch_bounds__(kMergeThreads) block_sort_kernel(
+    const K *__restrict__ in, const uint32_t *__restrict__ in_pay, int64_t N, K *__restrict__ out,
+    uint32_t *__restrict__ out_pay) {
+  pdl_begin();
+  constexpr int T = kMergeThreads, D = T * E;
+  extern __shared__ __align__(16) uint8_t smem[];
+  // two buffers of D keys, then two of D payloads; buffer b starts at b * D
+  K *const sk = reinterpret_cast<K *>(smem);
+  uint32_t *const sp = reinterpret_cast<uint32_t *>(smem + 2 * D * sizeof(K));
+  const int tid = threadIdx.x;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * D;
+  const int cnt = static_cast<int>(N - base < D ? N - base : D);
+  for (int x = tid; x < cnt; x += T) {
+    sk[x] = in[base + x];
+    if (PAY) sp[x] = in_pay[base + x];
+  }
+  __syncthreads();
+
+  const int d = tid * E;
+  K k[E];
+  uint32_t p[E];
+#pragma unroll
+  for (int q = 0; q < E; ++q) {
+    const bool v = d + q < cnt;
+    k[q] = v ? sk[d + q] : sort_key_max<K>();
+    p[q] = (PAY && v) ? sp[d + q] : 0u;
+  }
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+#pragma unroll
+    for (int i = r & 1; i + 1 < E; i += 2) {
+      if (k[i + 1] < k[i]) {
+        const K tk = k[i];
+        k[i] = k[i + 1];
+        k[i + 1] = tk;
+        if (PAY) {
+          const uint32_t tp = p[i];
+          p[i] = p[i + 1];
+          p[i + 1] = tp;
+        }
+      }
+    }
+  }
+  __syncthreads();  // every thread has read its elements before they are overwritten
+#pragma unroll
+  for (int q = 0; q < E; ++q) {
+    if (d + q < cnt) {
+      sk[d + q] = k[q];
+      if (PAY) sp[d + q] = p[q];
+    }
+  }
+  __syncthreads();
+
+  int src = 0;
+  for (int w = E; w < cnt; w *= 2) {
+    if (d < cnt) {
+      const int ps = (d / (2 * w)) * (2 * w);
+      const int la = w < cnt - ps ? w : cnt - ps;
+      const int lb = w < cnt - ps - la ? w : cnt - ps - la;
+      const K *a = sk + src * D + ps;
+      const K *b = a + la;
+      const int kd = d - ps;
+      int lo = kd > lb ? kd - lb : 0, hi = kd < la ? kd : la;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= b[kd - mid - 1]) lo = mid + 1;
+        else hi = mid;
+      }
+      int ai = lo, bi = kd - lo;
+      const uint32_t *pa = sp + src * D + ps;
+      const uint32_t *pb = pa + la;
+      K *ok = sk + (src ^ 1) * D + ps;
+      uint32_t *op = sp + (src ^ 1) * D + ps;
+      const int end = la + lb;
+#pragma unroll
+      for (int q = 0; q < E; ++q) {
+        const int pos = kd + q;
+        if (pos < end) {
+          const bool takeA = bi >= lb || (ai < la && a[ai] <= b[bi]);
+          if (takeA) {
+            ok[pos] = a[ai];
+            if (PAY) op[pos] = pa[ai];
+            ++ai;
+          } else {
+            ok[pos] = b[bi];
+            if (PAY) op[pos] = pb[bi];
+            ++bi;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    src ^= 1;
+  }
+  for (int x = tid; x < cnt; x += T) {
+    out[base + x] = sk[src * D + x];
+    if (PAY) out_pay[base + x] = sp[src * D + x];
+  }
+}
+
+// Co-ranks of one sort pass: boundary g sits at k = min(gD, N) inside the
+// pair that starts at ps = floor(k / 2w) 2w; its entry is the co-rank of
+// k - ps in the merge of the pair's runs [ps, ps + la) and [ps + la, ps + la + lb).
+template <typename K>
+__global__ void __launch_bounds__(256) partition_sort_kernel(const K *__restrict__ src, int64_t N,
+                                                             int64_t w, int64_t D, int64_t G,
+                                                             int64_t *__restrict__ out_i) {
+  pdl_begin();
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g > G) return;
+  const int64_t k = g * D < N ? g * D : N;
+  const int64_t ps = (k / (2 * w)) * (2 * w);
+  const int64_t la = w < N - ps ? w : N - ps;
+  const int64_t lb = w < N - ps - la ? w : N - ps - la;
+  out_i[g] = sampled_corank(src + ps, src + ps + la, k - ps, la, lb);
+}
+
+template <typename K, bool PAY>
+cudaError_t launch_merge_sort_typed(const K *in, const uint32_t *in_pay, int64_t N, K *out,
+                                    uint32_t *out_pay, K *tmp, uint32_t *tmp_pay, int64_t *part,
+                                    int32_t *status, cudaStream_t s) {
+  constexpr int D = kSortD;
+  using L = MergeLayout<K, PAY, kSortE, kSortS, 1>;
+  static_assert(L::D == D, "the pass tiles and the sorted runs have the same size");
+  constexpr size_t kBlockSmem = 2 * size_t(D) * (sizeof(K) + (PAY ? 4 : 0));
+  auto bkern = block_sort_kernel<K, PAY, kSortE>;
+  auto mkern = merge_tile_kernel<K, PAY, kSortE, kSortS, 1, true>;
+  constexpr int mthreads = kMergeThreads + 32;
+  static int per_sm = 0;  // resident tile CTAs per SM
+  if (!per_sm) {
+    cudaError_t err = cudaFuncSetAttribute(bkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kBlockSmem));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(mkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(L::kBytes));
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mkern, mthreads, L::kBytes);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+  }
+  const int64_t G = (N + D - 1) / D;
+  int passes = 0;
+  for (int64_t w = D; w < N; w *= 2) ++passes;
+  // ping-pong so that the last pass lands in `out`
+  K *kb[2] = {out, tmp};
+  uint32_t *pb[2] = {out_pay, tmp_pay};
+  int cur = passes & 1;
+  // the profiling hook brackets the last launch that moves every element:
+  // the last pass's tile kernel, or the block sort when it is the only one
+  if (passes == 0) profile_before(s);
+  cudaError_t err = launch_kernel(false, bkern, static_cast<unsigned>(G), kMergeThreads,
+                                  kBlockSmem, s, in, in_pay, N, kb[cur], pb[cur]);
+  if (passes == 0) profile_after(s);
+  if (err != cudaSuccess) return err;
+  int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
+  if (grid < 1) grid = 1;
+  if (grid > G) grid = G;
+  for (int64_t w = D; w < N; w *= 2) {
+    err = launch_kernel(false, partition_sort_kernel<K>, static_cast<unsigned>((G + 1 + 255) / 256),
+                        256, 0, s, static_cast<const K *>(kb[cur]), N, w, int64_t(D), G, part);
+    if (err != cudaSuccess) return err;
+    const bool last = 2 * w >= N;
+    if (last) profile_before(s);
+    err = launch_kernel(true, mkern, static_cast<unsigned>(grid), mthreads, L::kBytes, s,
+                        static_cast<const K *>(kb[cur]), static_cast<const uint32_t *>(pb[cur]), N,
+                        static_cast<const K *>(kb[cur]), static_cast<const uint32_t *>(pb[cur]), N,
+                        static_cast<const int64_t *>(part), G, kb[cur ^ 1], pb[cur ^ 1], status, w);
+    if (last) profile_after(s);
+    if (err != cudaSuccess) return err;
+    cur ^= 1;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
+
+int64_t merge_sort_tile() { return kSortD; }
+
+cudaError_t launch_merge_sort(int key_type, const void *in, const uint32_t *in_pay, int64_t N,
+                              void *out, uint32_t *out_pay, void *tmp, uint32_t *tmp_pay,
+                              int64_t *part, int32_t *status, cudaStream_t s) {
+  const bool pay = in_pay != nullptr;
+  if (key_type == LSM_KEY_I32) {
+    auto i = static_cast<const int32_t *>(in);
+    auto o = static_cast<int32_t *>(out);
+    auto t = static_cast<int32_t *>(tmp);
+    return pay ? launch_merge_sort_typed<int32_t, true>(i, in_pay, N, o, out_pay, t, tmp_pay, part, status, s)
+               : launch_merge_sort_typed<int32_t, false>(i, in_pay, N, o, out_pay, t, tmp_pay, part, status, s);
+  }
+  auto i = static_cast<const uint64_t *>(in);
+  auto o = static_cast<uint64_t *>(out);
+  auto t = static_cast<uint64_t *>(tmp);
+  return pay ? launch_merge_sort_typed<uint64_t, true>(i, in_pay, N, o, out_pay, t, tmp_pay, part, status, s)
+             : launch_merge_sort_typed<uint64_t, false>(i, in_pay, N, o, out_pay, t, tmp_pay, part, status, s);
+}
 
 int device_sm_count() {
   static std::mutex mu;

@@ -18,6 +18,11 @@ sizes for the parity tests):
   replace_skewed A = 2^24 - 1 unique keys; B = 65,536 keys clustered in 64
                  windows of 1024 consecutive A positions, half of each
                  window's B keys drawn from A and half fresh keys inside it
+  sort_u64       2^27 uniform 64-bit keys in input order, each with a uint32
+                 payload holding its input position (the element count and
+                 layout of the 2^26 + 2^26 merge's output)
+  sort_i32       int32 keys uniform in a range (heavy ties when narrow), same
+                 payload
   strings        4,000,000 unique byte-string keys per input built from a
                  prefix tree (fanout 16, depth 4, 2-byte edge labels) plus a
                  random 0-56 byte suffix; 20% of B's keys are A keys; values
@@ -69,6 +74,28 @@ def merge_u64(seed: int = 2, m: int = 1 << 26, n: int = 1 << 26) -> MergeInput:
     B = np.sort(_raw_u64(rng, n))
     Apay, Bpay = _source_index_payload(m, n)
     return MergeInput(A, B, Apay, Bpay)
+
+
+# ---------------------------------------------------------------------------
+# Merge-sort inputs (unsorted)
+# ---------------------------------------------------------------------------
+@dataclass
+class SortInput:
+    keys: np.ndarray   # unsorted keys
+    pay: np.ndarray    # uint32 payload = input position
+
+
+def sort_u64(seed: int = 6, N: int = 1 << 27) -> SortInput:
+    """Uniform 64-bit keys in input order; payload = input position."""
+    rng = _rng(seed)
+    return SortInput(_raw_u64(rng, N), np.arange(N, dtype=np.uint32))
+
+
+def sort_i32(seed: int = 7, N: int = 4096, lo: int = 0, hi: int = 4096) -> SortInput:
+    """int32 keys uniform in [lo, hi) in input order (ties when the range is
+    narrow); payload = input position."""
+    rng = _rng(seed)
+    return SortInput(rng.integers(lo, hi, size=N, dtype=np.int32), np.arange(N, dtype=np.uint32))
 
 
 # ---------------------------------------------------------------------------

@@ -56,6 +56,31 @@ def test_host_side_checks_without_gpu(lib):
     assert lib.lsm_tune_merge(2, 7, 2, 1) == 0
 
 
+def test_merge_sort_host_checks_without_gpu(lib):
+    I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    sizes = {}
+    for kt in (1, 2):
+        for N in (1, 2816, 1 << 27):
+            size = ctypes.c_size_t(0)
+            assert lib.lsm_workspace_size(7, kt, N, 0, ctypes.byref(size)) == 0
+            sizes[kt, N] = size.value
+        # the alternate buffers: one key and one payload per element, at least
+        assert sizes[kt, 1 << 27] >= (1 << 27) * (4 if kt == 1 else 8) + (1 << 27) * 4
+    assert sizes[2, 1 << 27] > sizes[1, 1 << 27]
+    size = ctypes.c_size_t(0)
+    assert lib.lsm_workspace_size(7, 9, 10, 0, ctypes.byref(size)) == 2   # LSM_ERR_DTYPE
+    assert lib.lsm_merge_sort(3, P(16), None, I(4), P(16), None, P(16), S(1 << 20), None) == 2
+    assert lib.lsm_merge_sort(2, P(16), None, I(-1), P(16), None, P(16), S(1 << 20), None) == 1
+    # payload in without payload out, and the reverse
+    assert lib.lsm_merge_sort(2, P(16), P(16), I(4), P(16), None, P(16), S(1 << 20), None) == 1
+    assert lib.lsm_merge_sort(2, P(16), None, I(4), P(16), P(16), P(16), S(1 << 20), None) == 1
+    assert lib.lsm_merge_sort(2, P(16), None, I(1 << 41), P(16), None, P(16), S(1 << 20),
+                              None) == 3                                   # LSM_ERR_OVERFLOW
+    assert lib.lsm_merge_sort(2, P(24), None, I(4), P(16), None, P(16), S(1 << 20), None) == 7
+    assert lib.lsm_merge_sort(2, P(16), None, I(4), P(16), None, P(16), S(8), None) == 6
+    assert lib.lsm_merge_sort(2, None, None, I(0), None, None, None, S(0), None) == 0
+
+
 class _Bytes(ctypes.Structure):
     _fields_ = [("arena", ctypes.c_void_p), ("off", ctypes.c_void_p)]
 
