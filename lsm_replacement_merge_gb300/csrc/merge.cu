@@ -477,9 +477,14 @@ __global__ void __launch_bounds__(kMergeThreads) block_sort_kernel(
   const int tid = threadIdx.x;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * D;
   const int cnt = static_cast<int>(N - base < D ? N - base : D);
-  for (int x = tid; x < cnt; x += T) {
-    sk[x] = in[base + x];
-    if (PAY) sp[x] = in_pay[base + x];
+  // coalesced loads, all E (and E payload) loads of a thread in flight at once
+#pragma unroll
+  for (int q = 0; q < E; ++q) {
+    const int x = tid + q * T;
+    if (x < cnt) {
+      sk[x] = in[base + x];
+      if (PAY) sp[x] = in_pay[base + x];
+    }
   }
   __syncthreads();
 
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(kMergeThreads) block_sort_kernel(
       }
     }
   }
-  __syncthreads();  // every thread has read its elements before they are overwritten
+  // each thread writes back exactly the positions it read
 #pragma unroll
   for (int q = 0; q < E; ++q) {
     if (d + q < cnt) {
@@ -516,10 +521,14 @@ __global__ void __launch_bounds__(kMergeThreads) block_sort_kernel(
       if (PAY) sp[d + q] = p[q];
     }
   }
-  __syncthreads();
+  // A pass whose pairs (2w elements) fit in one warp's 32 E elements reads
+  // and writes only that warp's span, so the barrier before it can be the
+  // warp's own: warps run the first passes (w = E .. 16 E) independently.
+  __syncwarp();
 
   int src = 0;
   for (int w = E; w < cnt; w *= 2) {
+    if (2 * w > 32 * E) __syncthreads();
     if (d < cnt) {
       const int ps = (d / (2 * w)) * (2 * w);
       const int la = w < cnt - ps ? w : cnt - ps;
@@ -533,35 +542,46 @@ __global__ void __launch_bounds__(kMergeThreads) block_sort_kernel(
         if (a[mid] <= b[kd - mid - 1]) lo = mid + 1;
         else hi = mid;
       }
+      // The pair's runs are adjacent: B's element bi sits at a[la + bi]. Each
+      // step is branch-free (lanes of a warp take A or B independently): one
+      // payload load and one head reload at a computed index, clamped into
+      // the pair so that an exhausted run's reload stays in bounds (its value
+      // is then never compared).
       int ai = lo, bi = kd - lo;
-      const uint32_t *pa = sp + src * D + ps;
-      const uint32_t *pb = pa + la;
+      const uint32_t *pp = sp + src * D + ps;
       K *ok = sk + (src ^ 1) * D + ps;
       uint32_t *op = sp + (src ^ 1) * D + ps;
       const int end = la + lb;
+      K ha = a[ai < end ? ai : end - 1];
+      K hb = a[la + bi < end ? la + bi : end - 1];
 #pragma unroll
       for (int q = 0; q < E; ++q) {
         const int pos = kd + q;
         if (pos < end) {
-          const bool takeA = bi >= lb || (ai < la && a[ai] <= b[bi]);
-          if (takeA) {
-            ok[pos] = a[ai];
-            if (PAY) op[pos] = pa[ai];
-            ++ai;
-          } else {
-            ok[pos] = b[bi];
-            if (PAY) op[pos] = pb[bi];
-            ++bi;
-          }
+          const bool takeA = bi >= lb || (ai < la && ha <= hb);
+          const int from = takeA ? ai : la + bi;
+          ok[pos] = takeA ? ha : hb;
+          if (PAY) op[pos] = pp[from];
+          ai += takeA ? 1 : 0;
+          bi += takeA ? 0 : 1;
+          const int nx = from + 1 < end ? from + 1 : end - 1;
+          const K nv = a[nx];
+          ha = takeA ? nv : ha;
+          hb = takeA ? hb : nv;
         }
       }
     }
-    __syncthreads();
+    __syncwarp();
     src ^= 1;
   }
-  for (int x = tid; x < cnt; x += T) {
-    out[base + x] = sk[src * D + x];
-    if (PAY) out_pay[base + x] = sp[src * D + x];
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < E; ++q) {
+    const int x = tid + q * T;
+    if (x < cnt) {
+      out[base + x] = sk[src * D + x];
+      if (PAY) out_pay[base + x] = sp[src * D + x];
+    }
   }
 }
 
