@@ -75,6 +75,10 @@ def _load():
             _lib.oracle_rank_prefix.restype = None
             _lib.oracle_rank512_dir.argtypes = [P, I, P]
             _lib.oracle_rank512_dir.restype = None
+            _lib.oracle_rank2048_dir.argtypes = [P, I, P, P]
+            _lib.oracle_rank2048_dir.restype = None
+            _lib.oracle_rank2048_query.argtypes = [P, P, P, P, I, P]
+            _lib.oracle_rank2048_query.restype = None
             _lib.oracle_rank_query.argtypes = [P, I, P, I, P]
             _lib.oracle_rank_query.restype = None
             _lib.oracle_ordinals_formula_u64.argtypes = [P, I, P, I, P, P, P, P]
@@ -257,6 +261,26 @@ def rank512_dir(C, m):
     dir_ = np.empty(3 * (m // 512 + 1), dtype=np.uint32)
     _load().oracle_rank512_dir(_p(C), m, _p(dir_))
     return dir_
+
+
+def rank2048_dir(C, m):
+    """The rank2048 layout: (dir uint64[floor(m/2048)+1], epochs uint64[floor(m/2^32)+1])."""
+    C = _c(C, np.uint32)
+    dir_ = np.empty(m // 2048 + 1, dtype=np.uint64)
+    epochs = np.empty(m // (1 << 32) + 1, dtype=np.uint64)
+    _load().oracle_rank2048_dir(_p(C), m, _p(dir_), _p(epochs))
+    return dir_, epochs
+
+
+def rank2048_query(C, dir_, epochs, pos):
+    """R(p) for each p by the rank2048 query procedure (uint64)."""
+    C = _c(C, np.uint32)
+    dir_ = _c(dir_, np.uint64)
+    epochs = _c(epochs, np.uint64)
+    pos = _c(pos, np.uint64)
+    out = np.empty(len(pos), dtype=np.uint64)
+    _load().oracle_rank2048_query(_p(C), _p(dir_), _p(epochs), _p(pos), len(pos), _p(out))
+    return out
 
 
 def rank_query(C, m, pos):

@@ -306,6 +306,69 @@ void oracle_rank_query(const uint32_t *C, int64_t m, const uint32_t *pos, int64_
 }
 
 /* ------------------------------------------------------------------------ */
+/* rank2048 directory. [CB] "Temporary rank layouts": Everett's other layout */
+/* keeps one 8-byte entry per 2048 bits holding three packed populations of */
+/* its 512-bit runs, with absolute counts at epochs of 2^32 bits; its       */
+/* storage is (1/8 + 8/2048)|A| bytes with the bitmap ("Scratch space and  */
+/* likely costs"). The page fixes the contents, not the bit packing; the    */
+/* reading taken here:                                                      */
+/*   epochs[e], e = 0..floor(m/2^32):  R(2^32 e), a full 64-bit count       */
+/*   dir[b],    b = 0..floor(m/2048):                                       */
+/*     bits  0..31  R(2048 b) - epochs[floor(2048 b / 2^32)]                */
+/*     bits 32..41  population of bits [2048b, 2048b+512)                   */
+/*     bits 42..51  population of bits [2048b+512, 2048b+1024)              */
+/*     bits 52..61  population of bits [2048b+1024, 2048b+1536)             */
+/* (a population is at most 512, ten bits). Built by one sequential walk    */
+/* over the bits with a running count; positions past m count as zero.      */
+/* ------------------------------------------------------------------------ */
+void oracle_rank2048_dir(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs) {
+    int64_t nb = m / 2048 + 1, b, t;
+    uint64_t R = 0;
+    for (b = 0; b < nb; b++) {
+        int64_t base = 2048 * b;
+        int r;
+        uint64_t entry;
+        if ((base & ((INT64_C(1) << 32) - 1)) == 0) epochs[base >> 32] = R;
+        entry = R - epochs[base >> 32];
+        for (r = 0; r < 4; r++) {
+            uint64_t pop = 0;
+            for (t = base + 512 * r; t < base + 512 * (r + 1) && t < m; t++)
+                pop += (C[t / 32] >> (t % 32)) & 1u;
+            if (r < 3) entry |= pop << (32 + 10 * r);
+            R += pop;
+        }
+        dir[b] = entry;
+    }
+    /* an epoch that starts inside the last block's span past m (m >= 2^32 e
+       > 2048 floor(m/2048)) cannot exist: 2^32 is a multiple of 2048 */
+}
+
+/* R(pos[t]) by the rank2048 layout's query procedure: the epoch, the       */
+/* entry's relative count, the populations of the earlier 512-bit runs of   */
+/* its 2048-bit block, then the whole 32-bit words of the current run      */
+/* before pos and the masked word holding pos. pos in [0, m].              */
+void oracle_rank2048_query(const uint32_t *C, const uint64_t *dir, const uint64_t *epochs,
+                           const uint64_t *pos, int64_t q, uint64_t *out) {
+    int64_t t;
+    for (t = 0; t < q; t++) {
+        uint64_t p = pos[t], w;
+        uint64_t e = dir[p >> 11];
+        uint64_t R = epochs[p >> 32] + (e & 0xFFFFFFFFu);
+        int r, runs = (int)((p >> 9) & 3);
+        for (r = 0; r < runs; r++) R += (e >> (32 + 10 * r)) & 0x3FFu;
+        for (w = (p >> 9) * 16; w < (p >> 5); w++) {
+            uint32_t x = C[w];
+            while (x) { R += x & 1u; x >>= 1; }
+        }
+        if (p & 31) {
+            uint32_t x = C[p >> 5] & ((1u << (p & 31)) - 1u);
+            while (x) { R += x & 1u; x >>= 1; }
+        }
+        out[t] = R;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Corrected ordinals by the closed forms, [CB] "Corrected record ordinals" */
 /* and "The three experimental paths" (independent lower bounds, the        */
 /* simplest oracle for the formulas):                                       */

@@ -326,6 +326,49 @@ def test_rank_prefix_and_directory(m, kind, bits):
     assert (oracle.rank_query(C, m, q) == expect).all()
 
 
+def _maps2048():
+    yield from _maps()
+    rng = np.random.default_rng(6)
+    for m in (4095, 4096, 4097, 6143, 6144, 6145, 10000):
+        yield m, "one", np.ones(m, bool)
+        yield m, "random", rng.random(m) < 0.5
+
+
+@pytest.mark.parametrize("m,kind,bits", list(_maps2048()))
+def test_rank2048_directory(m, kind, bits):
+    C = _pack(bits)
+    expect = np.concatenate([[0], np.cumsum(bits)]).astype(np.uint64)
+    d, ep = oracle.rank2048_dir(C, m)
+    assert len(d) == m // 2048 + 1 and len(ep) == 1 and ep[0] == 0
+    # the fields: relative count at the block start, then the populations of
+    # the block's first three 512-bit runs, ten bits each
+    for b in range(len(d)):
+        e = int(d[b])
+        assert e & 0xFFFFFFFF == expect[2048 * b]
+        for r in range(3):
+            lo, hi = min(2048 * b + 512 * r, m), min(2048 * b + 512 * (r + 1), m)
+            assert (e >> (32 + 10 * r)) & 0x3FF == int(bits[lo:hi].sum())
+        assert e >> 62 == 0
+    # the query procedure answers R(p) at every position, EOF included
+    q = np.arange(m + 1, dtype=np.uint64)
+    assert (oracle.rank2048_query(C, d, ep, q) == expect).all()
+
+
+def test_rank2048_epochs_past_2pow32():
+    # all ones past one epoch: R(p) = p, the second epoch holds 2^32 and its
+    # first entry counts from zero again
+    m = (1 << 32) + 5000
+    C = np.full((m + 31) // 32, 0xFFFFFFFF, dtype=np.uint32)
+    C[-1] = (1 << (m % 32)) - 1
+    d, ep = oracle.rank2048_dir(C, m)
+    assert ep.tolist() == [0, 1 << 32]
+    b = (1 << 32) // 2048
+    assert int(d[b]) & 0xFFFFFFFF == 0 and int(d[b - 1]) & 0xFFFFFFFF == (1 << 32) - 2048
+    pos = np.array([0, 1, (1 << 32) - 1, 1 << 32, (1 << 32) + 1, (1 << 32) + 2047,
+                    (1 << 32) + 2048, (1 << 32) + 4999, m], dtype=np.uint64)
+    assert (oracle.rank2048_query(C, d, ep, pos) == pos).all()
+
+
 # ---------------------------------------------------------------------------
 # Front compression
 # ---------------------------------------------------------------------------
