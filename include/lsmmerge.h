@@ -77,7 +77,8 @@ enum {
   LSM_OP_RANK_BUILD = 4,
   LSM_OP_REPLACEMENT_COMPACT = 5,
   LSM_OP_FC_LENGTHS_SCAN = 6,
-  LSM_OP_MERGE_SORT = 7
+  LSM_OP_MERGE_SORT = 7,
+  LSM_OP_RANK2048_BUILD = 8
 };
 
 #define LSM_REF_FROM_B 0x80000000u
@@ -240,6 +241,33 @@ LSM_API int lsm_rank_build_noalloc(const uint32_t *C, int64_t m, uint32_t *dir, 
  * records LSM_ERR_ARG in the device status. pos, out: device uint32[q]. */
 LSM_API int lsm_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                            const uint32_t *pos, int64_t q, uint32_t *out, void *stream);
+
+/* ---- f3: rank2048 directory ---------------------------------------------- */
+/* [CB] "Temporary rank layouts": the other temporary layout, one 8-byte
+ * entry per 2048 bits with three packed populations of its 512-bit runs and
+ * absolute counts at epochs of 2^32 bits; [CB] "Scratch space and likely
+ * costs": (1/8 + 8/2048)|A| bytes with the bitmap. Layout (the pages give the
+ * contents, this packing is a reading):
+ *   epochs[e], e = 0..floor(m/2^32):  R(2^32 e)
+ *   dir[b],    b = 0..floor(m/2048):  bits 0..31 = R(2048 b) - epochs[2048 b
+ *     >> 32]; bits 32+10r..41+10r = population of bits [2048b + 512r,
+ *     2048b + 512(r+1)) for r = 0, 1, 2; bits 62..63 zero.
+ * R(i) = number of set bits of C below i. *d_total = R(m).
+ * C: device uint32[ceil(m/32)], 16-byte aligned, bits at positions >= m zero.
+ * dir: device uint64[floor(m/2048)+1]; epochs: device uint64[floor(m/2^32)+1];
+ * d_total: device int64. m < 2^36. ws: at least
+ * lsm_workspace_size(LSM_OP_RANK2048_BUILD, 0, m, 0) bytes. */
+LSM_API int lsm_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs,
+                               int64_t *d_total, void *ws, size_t ws_bytes, void *stream);
+
+/* out[t] = R(pos[t]) from the rank2048 directory: the epoch, the entry's
+ * count, the earlier runs' populations, then popcounts of the current run's
+ * words before pos[t] and of the masked word holding it. pos[t] in [0, m]
+ * (EOF allowed); a position past m yields UINT64_MAX and records LSM_ERR_ARG
+ * in the device status word. pos, out: device uint64[q]. */
+LSM_API int lsm_rank2048_query(const uint32_t *C, const uint64_t *dir, const uint64_t *epochs,
+                               int64_t m, const uint64_t *pos, int64_t q, uint64_t *out,
+                               void *stream);
 
 /* ---- a5: replacement merge by bitmap, rank and merge path ----------------- */
 /* [CB] "The three experimental paths" (bitmap, compact A, then Merge Path)

@@ -34,6 +34,7 @@ LSM_OP_RANK_BUILD = 4
 LSM_OP_REPLACEMENT_COMPACT = 5
 LSM_OP_FC_LENGTHS_SCAN = 6
 LSM_OP_MERGE_SORT = 7
+LSM_OP_RANK2048_BUILD = 8
 REF_FROM_B = 0x80000000
 ORD_DROPPED = 0xFFFFFFFF
 
@@ -85,6 +86,8 @@ def lib():
                 "lsm_collision_mark_str_prefix": ([P, I, P, I, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_rank_build": ([P, I, P, P, P, S, P], ctypes.c_int),
                 "lsm_rank_query": ([P, P, I, P, I, P, P], ctypes.c_int),
+                "lsm_rank2048_build": ([P, I, P, P, P, P, S, P], ctypes.c_int),
+                "lsm_rank2048_query": ([P, P, P, I, P, I, P, P], ctypes.c_int),
                 "lsm_replacement_merge_compact": ([I, I, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_replacement_materialize": ([P, P, P, I, P, P, P, I, P, P, P, P, P, P],
                                                 ctypes.c_int),
@@ -357,6 +360,31 @@ def rank_build_noalloc(C, m: int, dir_=None, d_total=None, stream=None):
            lib().lsm_rank_build_noalloc(_ptr(C) if m else None, m, _ptr(dir_), _ptr(d_total),
                                         _stream(stream)))
     return dir_, d_total
+
+
+def rank2048_build(C, m: int, dir_=None, epochs=None, d_total=None, ws=None, stream=None):
+    dev = C.device
+    if dir_ is None:
+        dir_ = _empty(m // 2048 + 1, torch.uint64, dev)
+    if epochs is None:
+        epochs = _empty(m // (1 << 32) + 1, torch.uint64, dev)
+    if d_total is None:
+        d_total = _empty(1, torch.int64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_RANK2048_BUILD, m, 0, dev)
+    _check("lsm_rank2048_build",
+           lib().lsm_rank2048_build(_ptr(C), m, _ptr(dir_), _ptr(epochs), _ptr(d_total), _ptr(ws),
+                                    ws.numel(), _stream(stream)))
+    return dir_, epochs, d_total
+
+
+def rank2048_query(C, dir_, epochs, m: int, pos, out=None, stream=None):
+    if out is None:
+        out = _empty(pos.numel(), torch.uint64, pos.device)
+    _check("lsm_rank2048_query",
+           lib().lsm_rank2048_query(_ptr(C), _ptr(dir_), _ptr(epochs), m, _ptr(pos), pos.numel(),
+                                    _ptr(out), _stream(stream)))
+    return out
 
 
 def rank_query(C, dir_, m: int, pos, out=None, stream=None):

@@ -116,6 +116,9 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n, int key_type = LSM_KEY_U64) {
     case LSM_OP_RANK_BUILD:
       c.take<uint64_t>(rank_build_ctas(m));
       break;
+    case LSM_OP_RANK2048_BUILD:
+      c.take<uint32_t>(rank2048_build_ctas(m));
+      break;
     case LSM_OP_REPLACEMENT_COMPACT: {
       const int64_t D = replace_min_tile();
       c.take<int64_t>((m + n + D - 1) / D + 1);
@@ -180,7 +183,7 @@ LSM_API int lsm_workspace_size(int op, int key_type, int64_t m, int64_t n, size_
   if ((op == LSM_OP_MERGE_STABLE || op == LSM_OP_MERGE_SORT) && key_type != LSM_KEY_I32 &&
       key_type != LSM_KEY_U64)
     return LSM_ERR_DTYPE;
-  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_MERGE_SORT) return LSM_ERR_ARG;
+  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_RANK2048_BUILD) return LSM_ERR_ARG;
   *bytes = ws_bytes_for(op, m, n, key_type);
   return LSM_OK;
 }
@@ -308,6 +311,29 @@ LSM_API int lsm_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
   if (m > kMax31 || q > kMax31) return LSM_ERR_OVERFLOW;
   return cuda_status(launch_rank_query(C, dir, m, pos, q, out, status_ptr(),
                                        static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs,
+                               int64_t *d_total, void *ws, size_t ws_bytes, void *stream) {
+  if (m < 0 || !dir || !epochs || !d_total || (m && !C)) return LSM_ERR_ARG;
+  if (m >= (int64_t(1) << 36)) return LSM_ERR_OVERFLOW;
+  if ((C && !aligned16(C)) || !aligned8(dir) || !aligned8(epochs)) return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_RANK2048_BUILD, m, 0, ws, ws_bytes)) return r;
+  Carver c{static_cast<uint8_t *>(ws)};
+  uint32_t *totals = c.take<uint32_t>(rank2048_build_ctas(m));
+  return cuda_status(launch_rank2048_build(C, m, dir, epochs, d_total, totals,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_rank2048_query(const uint32_t *C, const uint64_t *dir, const uint64_t *epochs,
+                               int64_t m, const uint64_t *pos, int64_t q, uint64_t *out,
+                               void *stream) {
+  if (m < 0 || q < 0 || !dir || !epochs || (m && !C) || (q && (!pos || !out))) return LSM_ERR_ARG;
+  if (m >= (int64_t(1) << 36) || q > kMax31) return LSM_ERR_OVERFLOW;
+  if (C && !aligned16(C)) return LSM_ERR_ALIGN;
+  if (q == 0) return LSM_OK;
+  return cuda_status(launch_rank2048_query(C, dir, epochs, m, pos, q, out, status_ptr(),
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *C,

@@ -68,6 +68,15 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
                            cudaStream_t s);
 int64_t rank_build_ctas(int64_t m);
 
+// --- rank2048.cu ---
+int64_t rank2048_build_ctas(int64_t m);
+// cta_totals: rank2048_build_ctas(m) uint32 of scratch.
+cudaError_t launch_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs,
+                                  int64_t *d_total, uint32_t *cta_totals, cudaStream_t s);
+cudaError_t launch_rank2048_query(const uint32_t *C, const uint64_t *dir, const uint64_t *epochs,
+                                  int64_t m, const uint64_t *pos, int64_t q, uint64_t *out,
+                                  int32_t *status, cudaStream_t s);
+
 // --- strings.cu ---
 // prefixA / prefixB: optional key prefix tables (2 words per key), or NULL.
 cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,

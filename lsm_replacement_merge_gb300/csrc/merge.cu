@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kMergeThreads) block_sort_kernel(
     uint32_t *__restrict__ out_pay) {
   pdl_begin();
   constexpr int T = kMergeThreads, D = T * E;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   // two buffers of D keys, then two of D payloads; buffer b starts at b * D
   K *const sk = reinterpret_cast<K *>(smem);
   uint32_t *const sp = reinterpret_cast<uint32_t *>(smem + 2 * D * sizeof(K));

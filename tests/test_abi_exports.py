@@ -56,6 +56,21 @@ def test_host_side_checks_without_gpu(lib):
     assert lib.lsm_tune_merge(2, 7, 2, 1) == 0
 
 
+def test_rank2048_host_checks_without_gpu(lib):
+    I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    size = ctypes.c_size_t(0)
+    assert lib.lsm_workspace_size(8, 0, 12_000_000, 0, ctypes.byref(size)) == 0
+    # one uint32 total per CTA of 256 blocks of 2048 bits, plus slack
+    assert 4 * 23 <= size.value <= 4096
+    assert lib.lsm_rank2048_build(P(16), I(-1), P(16), P(16), P(16), P(16), S(4096), None) == 1
+    assert lib.lsm_rank2048_build(P(16), I(1 << 36), P(16), P(16), P(16), P(16), S(1 << 30),
+                                  None) == 3
+    assert lib.lsm_rank2048_build(P(20), I(100), P(16), P(16), P(16), P(16), S(4096), None) == 7
+    assert lib.lsm_rank2048_build(P(16), I(100), P(16), P(16), P(16), P(16), S(1), None) == 6
+    assert lib.lsm_rank2048_query(P(16), None, P(16), I(10), P(16), I(1), P(16), None) == 1
+    assert lib.lsm_rank2048_query(P(16), P(16), P(16), I(10), P(16), I(0), P(16), None) == 0
+
+
 def test_merge_sort_host_checks_without_gpu(lib):
     I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
     sizes = {}
