@@ -666,6 +666,25 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
         "kernel_ms": {"replacement_materialize": per_mat["replacement_materialize"]},
         "gpu_launches_per_step": 6}
     del vA, vB, tB, ok, ov, otb
+    # The same step with the rank2048 directory in place of rank512 ("Suggested
+    # separate modes": collision512 against collision2048 in the whole pipeline).
+    d2 = torch.empty(m // 2048 + 1, dtype=torch.uint64, device=dev)
+    e2 = torch.empty(m // (1 << 32) + 1, dtype=torch.uint64, device=dev)
+    w4 = lsm.workspace(lsm.LSM_OP_RANK2048_BUILD, m, 0, dev)
+    stages_2048 = [stages[0],
+                   ("rank2048_build", lambda: lsm.rank2048_build(C, m, d2, e2, tot, w4)),
+                   ("replacement_merge_compact", lambda: lsm.replacement_merge_compact_rank2048(
+                       m, n, C, d2, e2, lb, refs, oa, ob, cnt, w3))]
+    ms_2048, per_2048 = time_pipeline(torch, stages_2048, steps, flush)
+    alg_2048 = alg - 12 * (m // 512 + 1) + 8 * (m // 2048 + 1) + 8 * len(e2)
+    out[name]["rank2048"] = {
+        "ms_per_step": ms_2048, "gelem_s": (m + n) / (ms_2048 * 1e-3) / 1e9,
+        "algorithmic_bytes": alg_2048, "gbs": alg_2048 / (ms_2048 * 1e-3) / 1e9,
+        "frac": alg_2048 / (ms_2048 * 1e-3) / 1e9 / peak,
+        "kernel_ms": per_2048, "gpu_launches_per_step": 5,
+        "directory_bytes": {"rank512": 12 * (m // 512 + 1) + w2.numel(),
+                            "rank2048": 8 * (m // 2048 + 1) + 8 * len(e2) + w4.numel()}}
+    del d2, e2, w4
     if sweep:
         res = {}
         for kernel, label in ((0, "collision_mark"), (1, "replacement_merge_compact")):

@@ -290,6 +290,20 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                           int64_t *d_count, void *ws, size_t ws_bytes,
                                           void *stream);
 
+/* The same compaction, reading R(i) from the rank2048 directory
+ * (lsm_rank2048_build) instead of the rank512 one: [CB] "Suggested separate
+ * modes" (collision512 against collision2048) compares the two layouts
+ * inside the whole pipeline. Every output equals lsm_replacement_merge_compact's.
+ * dir, epochs: device, as lsm_rank2048_build wrote them for this C and m.
+ * Other arguments, limits and the workspace as lsm_replacement_merge_compact
+ * (ws sized by LSM_OP_REPLACEMENT_COMPACT). */
+LSM_API int lsm_replacement_merge_compact_rank2048(int64_t m, int64_t n, const uint32_t *C,
+                                                   const uint64_t *dir, const uint64_t *epochs,
+                                                   const uint32_t *lb_B, uint32_t *out_refs,
+                                                   uint32_t *ord_A, uint32_t *ord_B,
+                                                   int64_t *d_count, void *ws, size_t ws_bytes,
+                                                   void *stream);
+
 /* Materialized survivors of the replacement merge ([GC] merge paragraph: of
  * each equal-key run the newer record is kept, and a newer tombstone stays a
  * record). For t < N = d_count[0] (the count lsm_replacement_merge_compact

@@ -355,6 +355,27 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
+LSM_API int lsm_replacement_merge_compact_rank2048(int64_t m, int64_t n, const uint32_t *C,
+                                                   const uint64_t *dir, const uint64_t *epochs,
+                                                   const uint32_t *lb_B, uint32_t *out_refs,
+                                                   uint32_t *ord_A, uint32_t *ord_B,
+                                                   int64_t *d_count, void *ws, size_t ws_bytes,
+                                                   void *stream) {
+  if (m < 0 || n < 0 || !dir || !epochs || !d_count) return LSM_ERR_ARG;
+  if ((m && (!C || !ord_A)) || (n && (!lb_B || !ord_B)) || (m + n && !out_refs)) return LSM_ERR_ARG;
+  if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
+  if ((lb_B && !aligned16(lb_B)) || (C && !aligned16(C)) || !aligned16(out_refs) ||
+      (ord_A && !aligned16(ord_A)) || (ord_B && !aligned16(ord_B)))
+    return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_REPLACEMENT_COMPACT, m, n, ws, ws_bytes)) return r;
+  Carver c{static_cast<uint8_t *>(ws)};
+  const int64_t D = replace_min_tile();
+  int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
+  return cuda_status(launch_compact_rank2048(m, n, C, dir, epochs, lb_B, out_refs, ord_A, ord_B,
+                                             d_count, part, status_ptr(),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 LSM_API int lsm_replacement_materialize(const uint64_t *A, const uint32_t *Aval,
                                         const uint32_t *tombA, int64_t m, const uint64_t *B,
                                         const uint32_t *Bval, const uint32_t *tombB, int64_t n,

@@ -66,6 +66,11 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
                            uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,
                            cudaStream_t s);
+// The compaction reading R(i) from the rank2048 directory (default tile shape).
+cudaError_t launch_compact_rank2048(int64_t m, int64_t n, const uint32_t *C, const uint64_t *dir,
+                                    const uint64_t *epochs, const uint32_t *lb_B, uint32_t *refs,
+                                    uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
+                                    int64_t *part_i, int32_t *status, cudaStream_t s);
 int64_t rank_build_ctas(int64_t m);
 
 // --- rank2048.cu ---

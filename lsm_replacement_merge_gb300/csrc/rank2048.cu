@@ -129,11 +129,15 @@ int64_t rank2048_build_ctas(int64_t m) {
 cudaError_t launch_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs,
                                   int64_t *d_total, uint32_t *cta_totals, cudaStream_t s) {
   const int64_t ctas = rank2048_build_ctas(m);
+  profile_before(s);  // the profiling hook brackets both launches
   cudaError_t err = launch_kernel(true, rank2048_count_kernel, static_cast<unsigned>(ctas),
                                   kRank2048Threads, 0, s, C, m, cta_totals);
-  if (err != cudaSuccess) return err;
-  return launch_kernel(true, rank2048_finish_kernel, static_cast<unsigned>(ctas), kRank2048Threads,
-                       0, s, C, m, static_cast<const uint32_t *>(cta_totals), dir, epochs, d_total);
+  if (err == cudaSuccess)
+    err = launch_kernel(true, rank2048_finish_kernel, static_cast<unsigned>(ctas),
+                        kRank2048Threads, 0, s, C, m, static_cast<const uint32_t *>(cta_totals),
+                        dir, epochs, d_total);
+  profile_after(s);
+  return err;
 }
 
 cudaError_t launch_rank2048_query(const uint32_t *C, const uint64_t *dir, const uint64_t *epochs,

@@ -49,6 +49,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "rank2048.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
 
@@ -202,6 +203,22 @@ __device__ __forceinline__ uint32_t rank512_at(const uint32_t *__restrict__ C,
   return r;
 }
 
+// The rank layouts the compaction reads R(i) from: the 512-bit directory
+// above, or the 2048-bit one ("Temporary rank layouts" names both; "Suggested
+// separate modes" compares them inside the whole pipeline).
+struct Rank512Dir {
+  const uint32_t *dir;
+  __device__ __forceinline__ uint64_t at(const uint32_t *__restrict__ C, int64_t p) const {
+    return rank512_at(C, dir, p);
+  }
+};
+struct Rank2048Dir {
+  const uint64_t *dir, *epochs;
+  __device__ __forceinline__ uint64_t at(const uint32_t *__restrict__ C, int64_t p) const {
+    return rank2048_at(C, dir, epochs, p);
+  }
+};
+
 // The compaction's partition, by a scan over lb_B instead of one search per
 // boundary. With B first on ties, B_j sits at merged position
 // p_j = j + lb_B[j] (strictly increasing, below 2^32), so the co-rank of
@@ -217,9 +234,10 @@ constexpr int kPosThreads = 256;
 constexpr int kPosItems = 8;
 constexpr int kPosPerBlock = kPosThreads * kPosItems;
 
+template <class RD>
 __global__ void __launch_bounds__(kPosThreads) partition_positions_kernel(
     const uint32_t *__restrict__ lb_B, int64_t m, int64_t n, int64_t D, int64_t G,
-    int64_t *__restrict__ out_i, const uint32_t *__restrict__ C, const uint32_t *__restrict__ dir,
+    int64_t *__restrict__ out_i, const uint32_t *__restrict__ C, RD rank,
     int64_t *__restrict__ d_count) {
   pdl_begin();
   __shared__ uint32_t sp[kPosPerBlock];
@@ -228,7 +246,7 @@ __global__ void __launch_bounds__(kPosThreads) partition_positions_kernel(
   const int64_t jb = static_cast<int64_t>(blockIdx.x) * kPosPerBlock;
   const int cnt = static_cast<int>(n - jb < kPosPerBlock ? n - jb : kPosPerBlock);
   if (blockIdx.x == 0 && t == 0 && d_count)
-    *d_count = m + n - static_cast<int64_t>(rank512_at(C, dir, m));
+    *d_count = m + n - static_cast<int64_t>(rank.at(C, m));
   // kPosItems consecutive records per thread: two 16-byte loads when the
   // block is full (lb_B is 16-byte aligned and jb a multiple of 2048)
   const int x0 = t * kPosItems;
@@ -604,7 +622,7 @@ struct MarkSpec {
 // (j - j0) + (lb_B[j] - i0); a bitmap of those slots and prefix popcounts
 // over it and over C give every slot its element and its output position
 // directly, without walking the merge.
-template <int T_, int E_, int S_>
+template <int T_, int E_, int S_, class RD = Rank512Dir>
 struct CompactSpec {
   static constexpr int T = T_;
   static constexpr int E = E_;
@@ -626,7 +644,9 @@ struct CompactSpec {
   static_assert(D < 65536, "16-bit marks");
   struct Params {
     int64_t m, n;
-    const uint32_t *C, *dir, *lb_B;
+    const uint32_t *C;
+    RD rank;
+    const uint32_t *lb_B;
     const int64_t *part_i;
     uint32_t *refs, *ord_A, *ord_B;
     int32_t *status;
@@ -653,7 +673,7 @@ struct CompactSpec {
     i1 = i1 < k1 - p.n ? k1 - p.n : i1;
     v[0] = i0;
     v[1] = i1;
-    v[2] = rank512_at(p.C, p.dir, i0);
+    v[2] = static_cast<int64_t>(p.rank.at(p.C, i0));
   }
   __device__ __forceinline__ static void produce(const Params &p, int64_t g, const int64_t v[4], uint8_t *stage,
                                  Desc &d, uint64_t *full) {
@@ -950,21 +970,21 @@ cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                        C, dir, m, pos, q, out, status);
 }
 
-template <int V>
-cudaError_t launch_compact_variant(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
+template <int V, class RD>
+cudaError_t launch_compact_variant(int64_t m, int64_t n, const uint32_t *C, RD rank,
                                    const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
                                    uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
                                    int32_t *status, cudaStream_t s) {
   constexpr ReplaceVariant v = kReplaceVariants[V];
-  using Spec = CompactSpec<v.T, v.E, v.S>;
+  using Spec = CompactSpec<v.T, v.E, v.S, RD>;
   constexpr int64_t D = Spec::D;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t blocks = n > 0 ? (n + kPosPerBlock - 1) / kPosPerBlock : 1;
-  cudaError_t err = launch_kernel(true, partition_positions_kernel, static_cast<unsigned>(blocks),
-                                  kPosThreads, 0, s, lb_B, m, n, D, G, part_i, C, dir, d_count);
+  cudaError_t err = launch_kernel(true, partition_positions_kernel<RD>, static_cast<unsigned>(blocks),
+                                  kPosThreads, 0, s, lb_B, m, n, D, G, part_i, C, rank, d_count);
   if (err != cudaSuccess) return err;
   if (G == 0) return cudaSuccess;
-  typename Spec::Params p{m, n, C, dir, lb_B, part_i, refs, ord_A, ord_B, status};
+  typename Spec::Params p{m, n, C, rank, lb_B, part_i, refs, ord_A, ord_B, status};
   profile_before(s);
   err = launch_pipeline<Spec>(p, G, status, s, device_sm_count());
   profile_after(s);
@@ -995,12 +1015,24 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
                            uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,
                            cudaStream_t s) {
+  const Rank512Dir rank{dir};
   switch (g_compact_variant) {
-    case 1: return launch_compact_variant<1>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
-    case 2: return launch_compact_variant<2>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
-    case 3: return launch_compact_variant<3>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
-    default: return launch_compact_variant<0>(m, n, C, dir, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    case 1: return launch_compact_variant<1>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    case 2: return launch_compact_variant<2>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    case 3: return launch_compact_variant<3>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
+    default: return launch_compact_variant<0>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);
   }
+}
+
+// The same compaction reading R(i) from the rank2048 directory; the tile
+// shape is the default compaction variant's.
+cudaError_t launch_compact_rank2048(int64_t m, int64_t n, const uint32_t *C, const uint64_t *dir,
+                                    const uint64_t *epochs, const uint32_t *lb_B, uint32_t *refs,
+                                    uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
+                                    int64_t *part_i, int32_t *status, cudaStream_t s) {
+  const Rank2048Dir rank{dir, epochs};
+  return launch_compact_variant<0>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i,
+                                   status, s);
 }
 
 }  // namespace lsm

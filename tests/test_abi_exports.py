@@ -69,6 +69,13 @@ def test_rank2048_host_checks_without_gpu(lib):
     assert lib.lsm_rank2048_build(P(16), I(100), P(16), P(16), P(16), P(16), S(1), None) == 6
     assert lib.lsm_rank2048_query(P(16), None, P(16), I(10), P(16), I(1), P(16), None) == 1
     assert lib.lsm_rank2048_query(P(16), P(16), P(16), I(10), P(16), I(0), P(16), None) == 0
+    # the rank2048 compaction checks its arguments like the rank512 one
+    assert lib.lsm_replacement_merge_compact_rank2048(I(10), I(10), P(16), P(16), None, P(16),
+                                                      P(16), P(16), P(16), P(16), P(16), S(1 << 20),
+                                                      None) == 1
+    assert lib.lsm_replacement_merge_compact_rank2048(I(1 << 31), I(10), P(16), P(16), P(16),
+                                                      P(16), P(16), P(16), P(16), P(16), P(16),
+                                                      S(1 << 20), None) == 3
 
 
 def test_merge_sort_host_checks_without_gpu(lib):

@@ -94,3 +94,50 @@ def test_rank2048_epochs_past_2pow32(lsm):
     pos = np.array([0, 1, 511, 512, 2047, 2048, (1 << 32) - 1, 1 << 32, (1 << 32) + 1,
                     (1 << 32) + 1535, (1 << 32) + 2048, (1 << 32) + 4999, m], dtype=np.uint64)
     assert np.array_equal(down(lsm.rank2048_query(C, d, e, m, up(pos))), pos)
+
+
+# ---- the replacement pipeline reading R(i) from the rank2048 directory ------
+from tests.test_oracle_pins import REPLACE_CASES  # noqa: E402
+
+
+def _pipeline_2048(lsm, A, B):
+    m, n = len(A), len(B)
+    C, lb = lsm.collision_mark(up(A), up(B))
+    if m == 0:
+        C = torch.zeros(4, dtype=torch.uint32, device="cuda")
+    d, e, tot = lsm.rank2048_build(C, m)
+    refs, ordA, ordB, cnt = lsm.replacement_merge_compact_rank2048(m, n, C, d, e, lb)
+    N = int(cnt.item())
+    return dict(C=down(C)[:(m + 31) // 32], dir=down(d), epochs=down(e), total=int(tot.item()),
+                refs=down(refs)[:N], ordA=down(ordA), ordB=down(ordB), count=N)
+
+
+def _check_pipeline(got, A, B):
+    r = oracle.replacement_u64(A, B)
+    d, e = oracle.rank2048_dir(r.C, len(A))
+    assert got["count"] == r.count
+    assert np.array_equal(got["C"], r.C)
+    assert got["total"] == len(A) + len(B) - r.count
+    assert np.array_equal(got["dir"], d) and np.array_equal(got["epochs"], e)
+    assert np.array_equal(got["refs"], r.refs)
+    assert np.array_equal(got["ordA"], r.ord_A)
+    assert np.array_equal(got["ordB"], r.ord_B)
+
+
+@pytest.mark.parametrize("m,n,shared,universe", [c for c in REPLACE_CASES if c[0] + c[1] > 0] + [
+    (20000, 7000, 7000, None), (100000, 100000, 50000, 250000), (300000, 2000, 1000, None),
+    (2000, 300000, 2000, None)])
+def test_rank2048_pipeline_parity(lsm, m, n, shared, universe):
+    inp = synth.replace_random_small(seed=m * 7 + n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    _check_pipeline(_pipeline_2048(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_rank2048_pipeline_replace_12M_4M(lsm):
+    inp = synth.replace_u64()
+    _check_pipeline(_pipeline_2048(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_rank2048_pipeline_skewed_2pow24(lsm):
+    inp = synth.replace_skewed()
+    _check_pipeline(_pipeline_2048(lsm, inp.A, inp.B), inp.A, inp.B)
