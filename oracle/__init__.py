@@ -87,6 +87,10 @@ def _load():
             _lib.oracle_fc_encode.restype = I
             _lib.oracle_fc_decode.argtypes = [P, U, I, P, U, P, P, U, P, P]
             _lib.oracle_fc_decode.restype = I
+            _lib.oracle_ef_sizes.argtypes = [I, U, P]
+            _lib.oracle_ef_sizes.restype = None
+            _lib.oracle_ef_build.argtypes = [P, I, U, P, P, P, P]
+            _lib.oracle_ef_build.restype = I
             _lib.oracle_eg0_len.argtypes = [U]
             _lib.oracle_eg0_len.restype = U
             _lib.oracle_eg0_bits.argtypes = [U, P]
@@ -355,6 +359,35 @@ def fc_encode(keysA, valsA, tombA, keysB, valsB, tombB, refs, with_payload=True)
                                   nwords)
         assert t2 == total
     return FC(lcp, ctrl, rec, off, payload, int(total))
+
+
+class EF:
+    """Elias-Fano navigation sections over sampled record offsets."""
+
+    def __init__(self, n, L, lows, highs, samples, sparse):
+        self.n, self.L = n, L
+        self.lows, self.highs, self.samples, self.sparse = lows, highs, samples, sparse
+
+
+def ef_sizes(N, U):
+    """(n, L, lows words, highs words, groups) for N records and last entry U."""
+    out = np.empty(5, dtype=np.int64)
+    _load().oracle_ef_sizes(int(N), int(U), _p(out))
+    return tuple(int(v) for v in out)
+
+
+def ef_build(bit_off, N, w=0):
+    """EF sections over bit_off[0, 15, 30, ...] and bit_off[N], minus w per ordinal."""
+    bit_off = _c(bit_off, np.uint64)
+    U = int(bit_off[N]) - int(N) * int(w)
+    n, L, nl, nh, G = ef_sizes(N, U)
+    lows = np.zeros(max(nl, 1), dtype=np.uint64)
+    highs = np.zeros(max(nh, 1), dtype=np.uint64)
+    samples = np.zeros(2 * G, dtype=np.uint64)
+    sparse = np.zeros(max(n, 1), dtype=np.uint64)
+    ns = _load().oracle_ef_build(_p(bit_off), int(N), int(w), _p(lows), _p(highs), _p(samples),
+                                 _p(sparse))
+    return EF(n, L, lows[:nl], highs[:nh], samples, sparse[:ns])
 
 
 def fc_decode(payload, total_bits, N, key_cap, val_cap):

@@ -459,6 +459,81 @@ static void put_eg0(uint32_t *payload, uint64_t *pos, uint64_t x) {
     for (b = z; b >= 0; b--) put_bit(payload, pos, (int)(((x + 1) >> b) & 1u));
 }
 
+
+/* ------------------------------------------------------------------------ */
+/* Elias-Fano navigation over the record offsets. [GC] "GPU construction    */
+/* experiment": physical offsets are sampled at ordinals 0, 15, 30, ... and */
+/* at EOF (the payload extent); when every encoded value has the same width */
+/* w, the sequence subtracts w times the sample's ordinal; the EF sections   */
+/* are lows, highs, select samples and sparse exceptions, a 256-entry group */
+/* being sparse when its high-position span is at least 4096 bits. The rest */
+/* is textbook Elias-Fano; the layout is this library's reading:           */
+/*   entries  x_s = bit_off[15 s] - 15 s w for s = 0..ceil(N/15)-1, then     */
+/*            x_{n-1} = bit_off[N] - N w; n = ceil(N/15) + 1, U = x_{n-1}    */
+/*   L        the largest L with n 2^L <= U (0 when U < n)                  */
+/*   lows     x_s mod 2^L at bit positions [sL, sL + L) of a uint64 array    */
+/*            (bit t in word t/64 at position t%64), ceil(nL/64) words      */
+/*   highs    bit (x_s >> L) + s set for every s; (U >> L) + n bits, in      */
+/*            ceil(((U >> L) + n)/64) uint64 words, same bit order          */
+/*   samples  group g = entries [256 g, min(256 g + 256, n)):               */
+/*            samples[2g] = the high position of entry 256 g;              */
+/*            samples[2g+1] = e_g << 1 | sparse_g, where sparse_g = (high   */
+/*            position of the group's last entry - that of its first >= 4096) */
+/*            and e_g = the number of entries in sparse groups before g     */
+/*   sparse   the high position of every entry of every sparse group, in   */
+/*            entry order (group g's at [e_g, e_g + its entry count))       */
+/* Unused bits of every word are zero. Returns the number of sparse entries. */
+/* ------------------------------------------------------------------------ */
+static uint64_t ef_entry(const uint64_t *bit_off, int64_t N, uint64_t w, int64_t n, int64_t s) {
+    int64_t ord = s == n - 1 ? N : 15 * s;
+    return bit_off[ord] - (uint64_t)ord * w;
+}
+
+/* sizes[0] = n, [1] = L, [2] = lows words, [3] = highs words, [4] = groups */
+void oracle_ef_sizes(int64_t N, uint64_t U, int64_t *sizes) {
+    int64_t n = (N + 14) / 15 + 1;
+    int L = 0;
+    while (L < 63 && ((unsigned __int128)n << (L + 1)) <= U) L++;
+    sizes[0] = n;
+    sizes[1] = L;
+    sizes[2] = (n * L + 63) / 64;
+    sizes[3] = (int64_t)(((U >> L) + (uint64_t)n + 63) / 64);
+    sizes[4] = (n + 255) / 256;
+}
+
+int64_t oracle_ef_build(const uint64_t *bit_off, int64_t N, uint64_t w, uint64_t *lows,
+                        uint64_t *highs, uint64_t *samples, uint64_t *sparse) {
+    int64_t sz[5], n, L, s, g, e = 0;
+    uint64_t U;
+    n = (N + 14) / 15 + 1;
+    U = ef_entry(bit_off, N, w, n, n - 1);
+    oracle_ef_sizes(N, U, sz);
+    L = sz[1];
+    memset(lows, 0, (size_t)sz[2] * 8);
+    memset(highs, 0, (size_t)sz[3] * 8);
+    for (s = 0; s < n; s++) {
+        uint64_t x = ef_entry(bit_off, N, w, n, s);
+        uint64_t h = (x >> L) + (uint64_t)s;
+        int64_t b;
+        for (b = 0; b < L; b++)
+            if ((x >> b) & 1u) lows[(s * L + b) / 64] |= (uint64_t)1 << ((s * L + b) % 64);
+        highs[h / 64] |= (uint64_t)1 << (h % 64);
+    }
+    for (g = 0; g < sz[4]; g++) {
+        int64_t first = 256 * g, last = 256 * g + 255 < n - 1 ? 256 * g + 255 : n - 1;
+        uint64_t h0 = (ef_entry(bit_off, N, w, n, first) >> L) + (uint64_t)first;
+        uint64_t h1 = (ef_entry(bit_off, N, w, n, last) >> L) + (uint64_t)last;
+        int sp = h1 - h0 >= 4096;
+        samples[2 * g] = h0;
+        samples[2 * g + 1] = ((uint64_t)e << 1) | (uint64_t)sp;
+        if (sp) {
+            for (s = first; s <= last; s++)
+                sparse[e++] = (ef_entry(bit_off, N, w, n, s) >> L) + (uint64_t)s;
+        }
+    }
+    return e;
+}
+
 /* Writes EG0(x) into a zeroed word buffer; returns the bits written. */
 uint64_t oracle_eg0_bits(uint64_t x, uint32_t *words) {
     uint64_t pos = 0;

@@ -467,3 +467,90 @@ def test_synth_is_deterministic():
     s1 = synth.strings(seed=9, count=300, fanout=4, depth=2, max_suffix=6)
     s2 = synth.strings(seed=9, count=300, fanout=4, depth=2, max_suffix=6)
     assert (s1.A.key_arena == s2.A.key_arena).all() and (s1.B.key_off == s2.B.key_off).all()
+
+
+# ---------------------------------------------------------------------------
+# Elias-Fano navigation over record offsets ([GC])
+# ---------------------------------------------------------------------------
+def _bits_le(words, nbits):
+    """Bits 0..nbits-1 of a uint64 array, bit t in word t/64 at position t%64."""
+    b = np.unpackbits(np.asarray(words, dtype="<u8").view(np.uint8), bitorder="little")
+    return b[:nbits], b[nbits:]
+
+
+def _ef_expect(bit_off, N, w):
+    ords = list(range(0, N, 15)) + [N]
+    return [int(bit_off[o]) - o * w for o in ords]
+
+
+def _check_ef(bit_off, N, w=0):
+    x = _ef_expect(bit_off, N, w)
+    ef = oracle.ef_build(bit_off, N, w)
+    n, L, U = len(x), ef.L, x[-1]
+    assert ef.n == n
+    # L: the largest L with n 2^L <= U, or 0
+    assert (n << L) <= U < (n << (L + 1)) if L else U < 2 * n
+    # lows: x mod 2^L at [sL, sL + L), nothing past nL
+    lo, pad = _bits_le(ef.lows, n * L)
+    assert not pad.any() and len(ef.lows) == (n * L + 63) // 64
+    for s_ in range(n):
+        v = sum(int(lo[s_ * L + b]) << b for b in range(L))
+        assert v == x[s_] & ((1 << L) - 1)
+    # highs: one set bit per entry, x recovered from its position
+    nh = (U >> L) + n
+    hi, pad = _bits_le(ef.highs, nh)
+    assert not pad.any() and len(ef.highs) == (nh + 63) // 64
+    h = np.flatnonzero(hi)
+    assert len(h) == n
+    for s_ in range(n):
+        assert ((int(h[s_]) - s_) << L) | (x[s_] & ((1 << L) - 1)) == x[s_]
+    # samples and sparse exceptions, group by group
+    e = 0
+    exc = []
+    for g in range((n + 255) // 256):
+        first, last = 256 * g, min(256 * g + 255, n - 1)
+        sp = int(h[last] - h[first]) >= 4096
+        assert int(ef.samples[2 * g]) == h[first]
+        assert int(ef.samples[2 * g + 1]) == (e << 1) | int(sp)
+        if sp:
+            exc += [int(v) for v in h[first:last + 1]]
+            e += last - first + 1
+    assert [int(v) for v in ef.sparse] == exc
+    return ef
+
+
+def _offsets(rng, N, lo, hi):
+    return np.concatenate([[0], np.cumsum(rng.integers(lo, hi, size=N))]).astype(np.uint64)
+
+
+@pytest.mark.parametrize("N", [0, 1, 14, 15, 16, 29, 30, 31, 3839, 3840, 3841, 100_000])
+def test_ef_sections_decode(N):
+    rng = np.random.default_rng(N + 5)
+    _check_ef(_offsets(rng, N, 3, 400), N)
+    # a common value width w: every record at least w bits long
+    _check_ef(_offsets(rng, N, 40, 60), N, w=40)
+    _check_ef(_offsets(rng, N, 1, 2), N, w=1)  # every x equal: repeated entries
+
+
+def test_ef_sparse_threshold_exact():
+    # 4001 entries; group 0 climbs to x_255 and everything after repeats it,
+    # so L = 0 and group 0 spans x_255 + 255 high positions
+    for top, sparse in ((3840, False), (3841, True)):
+        n = 4001
+        x = np.zeros(n, dtype=np.uint64)
+        x[1:255] = np.arange(1, 255)
+        x[255:] = top
+        N = 15 * (n - 1)
+        bit_off = np.repeat(x[:-1], 15)
+        bit_off = np.concatenate([bit_off, [x[-1]]]).astype(np.uint64)
+        ef = _check_ef(bit_off, N)
+        assert ef.L == 0 and (int(ef.samples[1]) & 1) == int(sparse)
+        assert len(ef.sparse) == (256 if sparse else 0)
+
+
+def test_ef_over_an_fc_scan():
+    # the sequence the FC length scan produces for the prefix-tree keys
+    s = synth.strings(seed=9, count=3000)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    fc = _encode_strings(s, r.refs)
+    _check_ef(fc.bit_off, r.count)
