@@ -754,6 +754,22 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
                                "frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": per,
                                "gpu_launches_per_step": 7,
                                "l2": "flushed (256 MiB write) before every step"}
+    # The same step followed by the Elias-Fano navigation over bit_off.
+    n_ef, L, nl, nh, G = lsm.ef_sizes(N, total_bits)
+    lows = torch.empty(max(nl, 1), dtype=torch.uint64, device=dev)
+    highs = torch.empty(nh, dtype=torch.uint64, device=dev)
+    samples = torch.empty(2 * G, dtype=torch.uint64, device=dev)
+    sparse = torch.empty(n_ef, dtype=torch.uint64, device=dev)
+    nsp = torch.empty(1, dtype=torch.int64, device=dev)
+    stages_ef = stages + [("fc_ef_build", lambda: lsm.fc_ef_build(
+        off, N, total_bits, 0, lows, highs, samples, sparse, nsp))]
+    ms_ef, per_ef = time_pipeline(torch, stages_ef, steps, flush)
+    ef_bytes = 8 * n_ef + 8 * (nl + nh + 2 * G) + 8 * int(nsp.item())
+    out["strings_fc_4M_4M"]["with_ef"] = {
+        "ms_per_step": ms_ef, "ef_entries": n_ef, "ef_L": L,
+        "ef_sparse_entries": int(nsp.item()), "ef_algorithmic_bytes": ef_bytes,
+        "kernel_ms": {"fc_ef_build": per_ef["fc_ef_build"]},
+        "gpu_launches_per_step": 9}
 
 
 if __name__ == "__main__":

@@ -357,6 +357,42 @@ LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
                         const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                         uint32_t *payload, int64_t nwords, void *stream);
 
+/* ---- f2: Elias-Fano navigation over the record offsets ------------------- */
+/* [GC] "GPU construction experiment": physical offsets sampled at ordinals
+ * 0, 15, 30, ... plus EOF; with a common encoded value width w every entry
+ * subtracts w times its ordinal; the sections are EF lows, highs, select
+ * samples and sparse exceptions, a 256-entry group being sparse when its
+ * high-position span is at least 4096 bits. The pages fix these contents;
+ * the bit layout is this library's reading (textbook Elias-Fano):
+ *   entries  x_s = bit_off[15 s] - 15 s w for s < n - 1, and
+ *            x_{n-1} = bit_off[N] - N w;  n = ceil(N/15) + 1;  U = x_{n-1}
+ *   L        the largest L with n 2^L <= U (0 when U < n)
+ *   lows     x_s mod 2^L at bits [sL, sL+L) (bit t = bit t%64 of word t/64)
+ *   highs    bit (x_s >> L) + s set for every s, (U >> L) + n bits
+ *   samples  per group g of entries [256g, min(256g+256, n)):
+ *            samples[2g] = high position of entry 256g; samples[2g+1] =
+ *            e_g << 1 | sparse_g, e_g = entries of sparse groups before g
+ *   sparse   the high position of every entry of each sparse group, in order
+ * Every unused bit of every word is zero. */
+
+/* Host-only sizes for N records and U = bit_off[N] - N w: sizes[0] = n,
+ * [1] = L, [2] = lows uint64 words, [3] = highs uint64 words, [4] = groups
+ * (samples take 2 * groups uint64; sparse at most n uint64). */
+LSM_API int lsm_ef_sizes(int64_t N, uint64_t U, int64_t *sizes);
+
+/* Builds the four sections from bit_off (device uint64[N+1], nondecreasing,
+ * as lsm_fc_lengths_scan wrote it) and writes the number of sparse entries
+ * to *d_nsparse (device int64). w: the common value width in bits (0 when
+ * widths differ); every record must be at least w bits long. U must equal
+ * bit_off[N] - N w (the host reads bit_off[N] to size the sections); when
+ * it does not, LSM_ERR_ARG is recorded in the device status word and no
+ * write leaves the sections. lows, highs, samples: device, sized by
+ * lsm_ef_sizes (lows may be NULL when it has no words); sparse: device,
+ * n uint64. All 8-byte aligned. N < 2^31. Two launches. */
+LSM_API int lsm_fc_ef_build(const uint64_t *bit_off, int64_t N, uint64_t w, uint64_t U,
+                            uint64_t *lows, uint64_t *highs, uint64_t *samples, uint64_t *sparse,
+                            int64_t *d_nsparse, void *stream);
+
 /* ---- tuning ----------------------------------------------------------------- */
 /* Selects the tile configuration of lsm_merge_stable for a key type:
  * items_per_thread E (a tile is 256 E outputs), `stages` input tiles kept in

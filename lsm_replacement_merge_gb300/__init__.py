@@ -95,6 +95,9 @@ def lib():
                                                 ctypes.c_int),
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
+                "lsm_ef_sizes": ([I, ctypes.c_uint64, P], ctypes.c_int),
+                "lsm_fc_ef_build": ([P, I, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, P, P],
+                                    ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
                 "lsm_tune_merge": ([ctypes.c_int] * 4, ctypes.c_int),
                 "lsm_tune_replace": ([ctypes.c_int] * 3, ctypes.c_int),
@@ -514,3 +517,35 @@ def fc_emit(fc: FcInput, refs, N: int, lcp, ctrl, bit_off, nwords: int, payload=
                              _ptr(lcp) if N else None, _ptr(ctrl) if N else None, _ptr(bit_off),
                              _ptr(payload) if nwords else None, nwords, _stream(stream)))
     return payload
+
+
+# ---------------------------------------------------------------------------
+# f2: Elias-Fano navigation over the record offsets
+# ---------------------------------------------------------------------------
+def ef_sizes(N: int, U: int):
+    """(n, L, lows words, highs words, groups) for N records, last entry U."""
+    out = (ctypes.c_int64 * 5)()
+    _check("lsm_ef_sizes", lib().lsm_ef_sizes(N, U, out))
+    return tuple(int(v) for v in out)
+
+
+def fc_ef_build(bit_off, N: int, U: int, w: int = 0, lows=None, highs=None, samples=None,
+                sparse=None, d_nsparse=None, stream=None):
+    """U = bit_off[N] - N w, read by the caller. Returns (lows, highs, samples,
+    sparse, d_nsparse); sparse holds n slots, the first d_nsparse of them used."""
+    dev = bit_off.device
+    n, L, nl, nh, G = ef_sizes(N, U)
+    if lows is None:
+        lows = _empty(max(nl, 1), torch.uint64, dev)
+    if highs is None:
+        highs = _empty(nh, torch.uint64, dev)
+    if samples is None:
+        samples = _empty(2 * G, torch.uint64, dev)
+    if sparse is None:
+        sparse = _empty(n, torch.uint64, dev)
+    if d_nsparse is None:
+        d_nsparse = _empty(1, torch.int64, dev)
+    _check("lsm_fc_ef_build",
+           lib().lsm_fc_ef_build(_ptr(bit_off), N, w, U, _ptr(lows), _ptr(highs), _ptr(samples),
+                                 _ptr(sparse), _ptr(d_nsparse), _stream(stream)))
+    return lows, highs, samples, sparse, d_nsparse

@@ -226,6 +226,29 @@ LSM_API int lsm_merge_stable(int key_type, const void *A, const uint32_t *Apay, 
                                          part, status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
+LSM_API int lsm_ef_sizes(int64_t N, uint64_t U, int64_t *sizes) {
+  if (N < 0 || !sizes) return LSM_ERR_ARG;
+  if (N > kMax31) return LSM_ERR_OVERFLOW;
+  ef_layout(N, U, sizes);
+  return LSM_OK;
+}
+
+LSM_API int lsm_fc_ef_build(const uint64_t *bit_off, int64_t N, uint64_t w, uint64_t U,
+                            uint64_t *lows, uint64_t *highs, uint64_t *samples, uint64_t *sparse,
+                            int64_t *d_nsparse, void *stream) {
+  if (N < 0 || !bit_off || !highs || !samples || !sparse || !d_nsparse) return LSM_ERR_ARG;
+  if (N > kMax31) return LSM_ERR_OVERFLOW;
+  int64_t sz[5];
+  ef_layout(N, U, sz);
+  if (sz[2] > 0 && !lows) return LSM_ERR_ARG;
+  for (const void *p : {static_cast<const void *>(bit_off), static_cast<const void *>(lows),
+                        static_cast<const void *>(highs), static_cast<const void *>(samples),
+                        static_cast<const void *>(sparse)})
+    if (p && !aligned8(p)) return LSM_ERR_ALIGN;
+  return cuda_status(launch_ef_build(bit_off, N, w, U, lows, highs, samples, sparse, d_nsparse,
+                                     status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
 LSM_API int lsm_merge_sort(int key_type, const void *keys, const uint32_t *pay, int64_t N,
                            void *out_keys, uint32_t *out_pay, void *ws, size_t ws_bytes,
                            void *stream) {

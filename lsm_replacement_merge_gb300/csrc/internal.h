@@ -101,6 +101,13 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                            uint32_t *payload, int64_t nwords, int32_t *status, cudaStream_t s);
 
+// --- ef.cu ---
+// sizes: n entries, L, lows words, highs words, groups (host-only).
+void ef_layout(int64_t N, uint64_t U, int64_t sizes[5]);
+cudaError_t launch_ef_build(const uint64_t *bit_off, int64_t N, uint64_t w, uint64_t U,
+                            uint64_t *lows, uint64_t *highs, uint64_t *samples, uint64_t *sparse,
+                            int64_t *d_nsparse, int32_t *status, cudaStream_t s);
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 

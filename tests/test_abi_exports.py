@@ -78,6 +78,22 @@ def test_rank2048_host_checks_without_gpu(lib):
                                                       S(1 << 20), None) == 3
 
 
+def test_ef_sizes_without_gpu(lib):
+    import numpy as np
+    import oracle
+    out = (ctypes.c_int64 * 5)()
+    for N, U in ((0, 0), (1, 5), (14, 1000), (15, 1000), (7_200_000, 2_500_000_000),
+                 (100, (1 << 64) - 1)):
+        assert lib.lsm_ef_sizes(ctypes.c_int64(N), ctypes.c_uint64(U), out) == 0
+        assert tuple(out) == oracle.ef_sizes(N, U)
+    assert lib.lsm_ef_sizes(ctypes.c_int64(-1), ctypes.c_uint64(0), out) == 1
+    I, P = ctypes.c_int64, ctypes.c_void_p
+    assert lib.lsm_fc_ef_build(None, I(10), ctypes.c_uint64(0), ctypes.c_uint64(0), P(8), P(8),
+                               P(8), P(8), P(8), None) == 1
+    assert lib.lsm_fc_ef_build(P(12), I(10), ctypes.c_uint64(0), ctypes.c_uint64(100), P(8),
+                               P(8), P(8), P(8), P(8), None) == 7
+
+
 def test_merge_sort_host_checks_without_gpu(lib):
     I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
     sizes = {}

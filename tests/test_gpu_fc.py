@@ -100,7 +100,24 @@ def check_fc(lsm, s, extra_words=3):
     assert np.array_equal(down(off2), exp.bit_off)
     payload2 = lsm.fc_emit(fcp, refs, N, lcp2, ctrl2, off2, nwords)
     assert np.array_equal(down(payload2)[:nwords], got)
+    # the Elias-Fano navigation over the scanned offsets
+    check_ef(lsm, off, N, exp.bit_off)
     return exp
+
+
+def check_ef(lsm, d_off, N, want_off, w=0):
+    """EF sections built on the GPU from d_off (device) against the oracle's
+    built from want_off (the oracle's own offsets, equal to d_off)."""
+    want = oracle.ef_build(want_off, N, w)
+    U = int(want_off[N]) - N * w
+    lows, highs, samples, sparse, ns = lsm.fc_ef_build(d_off, N, U, w)
+    n, L, nl, nh, G = lsm.ef_sizes(N, U)
+    assert (n, L) == (want.n, want.L)
+    assert np.array_equal(down(lows)[:nl], want.lows)
+    assert np.array_equal(down(highs)[:nh], want.highs)
+    assert np.array_equal(down(samples), want.samples)
+    k = int(ns.item())
+    assert k == len(want.sparse) and np.array_equal(down(sparse)[:k], want.sparse)
 
 
 def test_hand_derived_words(lsm, golden):
