@@ -685,6 +685,17 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
         "directory_bytes": {"rank512": 12 * (m // 512 + 1) + w2.numel(),
                             "rank2048": 8 * (m // 2048 + 1) + 8 * len(e2) + w4.numel()}}
     del d2, e2, w4
+    # The tiled direct scatter in place of the compaction ("The three
+    # experimental paths", second path): the same outputs, the keys read again.
+    stages_sc = stages[:2] + [("replacement_direct_scatter", lambda: lsm.replacement_direct_scatter(
+        A, B, C, dir_, lb, refs, oa, ob, cnt))]
+    ms_sc, per_sc = time_pipeline(torch, stages_sc, steps, flush)
+    alg_sc = alg + 8 * (m + n) + 4 * n  # keys read again, lb_B read
+    out[name]["direct_scatter"] = {
+        "ms_per_step": ms_sc, "gelem_s": (m + n) / (ms_sc * 1e-3) / 1e9,
+        "algorithmic_bytes": alg_sc, "gbs": alg_sc / (ms_sc * 1e-3) / 1e9,
+        "frac": alg_sc / (ms_sc * 1e-3) / 1e9 / peak,
+        "kernel_ms": per_sc, "gpu_launches_per_step": 4}
     if sweep:
         res = {}
         for kernel, label in ((0, "collision_mark"), (1, "replacement_merge_compact")):

@@ -304,6 +304,25 @@ LSM_API int lsm_replacement_merge_compact_rank2048(int64_t m, int64_t n, const u
                                                    int64_t *d_count, void *ws, size_t ws_bytes,
                                                    void *stream);
 
+/* [CB] "The three experimental paths", the tiled direct scatter: each thread
+ * takes 32 consecutive A records, finds lower_bound(B, A_i) for the first by
+ * one binary search and for the rest by advancing a cursor through B, and
+ * every record scatters to its corrected ordinal ([CB] "Corrected record
+ * ordinals": i + lower_bound(B, A_i) - R(i) for a surviving A_i, j + lb_B[j]
+ * - R(lb_B[j]) for B_j): ord_A[i] (0xFFFFFFFF when dropped), ord_B[j] and
+ * out_refs[ordinal] = the record's reference. *d_count = m + n - R(m). Every
+ * output equals lsm_replacement_merge_compact's; this path reads the keys
+ * again where the compaction reads only lb_B and C. A, B: the keys given to
+ * lsm_collision_mark; C, lb_B: its outputs; dir: lsm_rank_build's. A record
+ * whose ordinal would fall outside [0, N) (inputs that break the contract)
+ * records LSM_ERR_ARG in the device status word and writes no ref. All
+ * arrays 16-byte aligned; m, n < 2^31. One launch; no workspace. */
+LSM_API int lsm_replacement_direct_scatter(const uint64_t *A, int64_t m, const uint64_t *B,
+                                           int64_t n, const uint32_t *C, const uint32_t *dir,
+                                           const uint32_t *lb_B, uint32_t *out_refs,
+                                           uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
+                                           void *stream);
+
 /* Materialized survivors of the replacement merge ([GC] merge paragraph: of
  * each equal-key run the newer record is kept, and a newer tombstone stays a
  * record). For t < N = d_count[0] (the count lsm_replacement_merge_compact

@@ -91,6 +91,8 @@ def lib():
                 "lsm_replacement_merge_compact": ([I, I, P, P, P, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_replacement_merge_compact_rank2048": ([I, I, P, P, P, P, P, P, P, P, P, S, P],
                                                            ctypes.c_int),
+                "lsm_replacement_direct_scatter": ([P, I, P, I, P, P, P, P, P, P, P, P],
+                                                   ctypes.c_int),
                 "lsm_replacement_materialize": ([P, P, P, I, P, P, P, I, P, P, P, P, P, P],
                                                 ctypes.c_int),
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
@@ -420,6 +422,26 @@ def replacement_merge_compact(m: int, n: int, C, dir_, lb_B, refs=None, ord_A=No
                                                _ptr(lb_B) if n else None, _ptr(refs),
                                                _ptr(ord_A) if m else None, _ptr(ord_B) if n else None,
                                                _ptr(d_count), _ptr(ws), ws.numel(), _stream(stream)))
+    return refs, ord_A, ord_B, d_count
+
+
+def replacement_direct_scatter(A, B, C, dir_, lb_B, refs=None, ord_A=None, ord_B=None,
+                               d_count=None, stream=None):
+    m, n = A.numel(), B.numel()
+    dev = dir_.device
+    if refs is None:
+        refs = _empty(max(m + n, 1), torch.uint32, dev)
+    if ord_A is None:
+        ord_A = _empty(m, torch.uint32, dev)
+    if ord_B is None:
+        ord_B = _empty(n, torch.uint32, dev)
+    if d_count is None:
+        d_count = _empty(1, torch.int64, dev)
+    _check("lsm_replacement_direct_scatter",
+           lib().lsm_replacement_direct_scatter(
+               _ptr(A) if m else None, m, _ptr(B) if n else None, n, _ptr(C) if m else None,
+               _ptr(dir_), _ptr(lb_B) if n else None, _ptr(refs), _ptr(ord_A) if m else None,
+               _ptr(ord_B) if n else None, _ptr(d_count), _stream(stream)))
     return refs, ord_A, ord_B, d_count
 
 

@@ -378,6 +378,25 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
+LSM_API int lsm_replacement_direct_scatter(const uint64_t *A, int64_t m, const uint64_t *B,
+                                           int64_t n, const uint32_t *C, const uint32_t *dir,
+                                           const uint32_t *lb_B, uint32_t *out_refs,
+                                           uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
+                                           void *stream) {
+  if (m < 0 || n < 0 || !dir || !d_count) return LSM_ERR_ARG;
+  if ((m && (!A || !C || !ord_A)) || (n && (!B || !lb_B || !ord_B)) || (m + n && !out_refs))
+    return LSM_ERR_ARG;
+  if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
+  for (const void *p : {static_cast<const void *>(A), static_cast<const void *>(B),
+                        static_cast<const void *>(C), static_cast<const void *>(lb_B),
+                        static_cast<const void *>(out_refs), static_cast<const void *>(ord_A),
+                        static_cast<const void *>(ord_B)})
+    if (p && !aligned16(p)) return LSM_ERR_ALIGN;
+  return cuda_status(launch_direct_scatter(A, m, B, n, C, dir, lb_B, out_refs, ord_A, ord_B,
+                                           d_count, status_ptr(),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 LSM_API int lsm_replacement_merge_compact_rank2048(int64_t m, int64_t n, const uint32_t *C,
                                                    const uint64_t *dir, const uint64_t *epochs,
                                                    const uint32_t *lb_B, uint32_t *out_refs,

@@ -101,6 +101,12 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                            uint32_t *payload, int64_t nwords, int32_t *status, cudaStream_t s);
 
+// --- scatter.cu ---
+cudaError_t launch_direct_scatter(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                  const uint32_t *C, const uint32_t *dir, const uint32_t *lb_B,
+                                  uint32_t *refs, uint32_t *ord_A, uint32_t *ord_B,
+                                  int64_t *d_count, int32_t *status, cudaStream_t s);
+
 // --- ef.cu ---
 // sizes: n entries, L, lows words, highs words, groups (host-only).
 void ef_layout(int64_t N, uint64_t U, int64_t sizes[5]);

@@ -50,6 +50,7 @@
 
 #include "common.cuh"
 #include "rank2048.cuh"
+#include "rank512.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
 
@@ -183,24 +184,6 @@ __global__ void __launch_bounds__(kRankThreads) rank_finish_kernel(const uint32_
     dir[3 * b + 2] = static_cast<uint32_t>(packed >> 32);
   }
   if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) *d_total = static_cast<int64_t>(prefix) + cta_sum;
-}
-
-// R(p) for p in [0, m]: directory entry, packed sub-prefix, at most one
-// preceding 32-bit word and the masked current word.
-__device__ __forceinline__ uint32_t rank512_at(const uint32_t *__restrict__ C,
-                                               const uint32_t *__restrict__ dir, int64_t p) {
-  const int64_t b = p >> 9;
-  uint32_t r = dir[3 * b];
-  const int s = static_cast<int>((p >> 6) & 7);
-  if (s) {
-    const uint64_t packed = static_cast<uint64_t>(dir[3 * b + 1]) |
-                            (static_cast<uint64_t>(dir[3 * b + 2]) << 32);
-    r += static_cast<uint32_t>((packed >> (9 * (s - 1))) & 0x1FFu);
-  }
-  const int64_t w = p >> 5;
-  if (p & 32) r += __popc(C[w - 1]);
-  if (p & 31) r += __popc(C[w] & ((1u << (p & 31)) - 1u));
-  return r;
 }
 
 // The rank layouts the compaction reads R(i) from: the 512-bit directory

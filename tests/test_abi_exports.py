@@ -94,6 +94,20 @@ def test_ef_sizes_without_gpu(lib):
                                P(8), P(8), P(8), P(8), None) == 7
 
 
+def test_direct_scatter_host_checks_without_gpu(lib):
+    I, P = ctypes.c_int64, ctypes.c_void_p
+    args = [P(16), I(10), P(16), I(10), P(16), P(16), P(16), P(16), P(16), P(16), P(16), None]
+    bad = list(args)
+    bad[5] = None                                              # dir
+    assert lib.lsm_replacement_direct_scatter(*bad) == 1
+    bad = list(args)
+    bad[1] = I(1 << 31)
+    assert lib.lsm_replacement_direct_scatter(*bad) == 3
+    bad = list(args)
+    bad[2] = P(24)                                             # B misaligned
+    assert lib.lsm_replacement_direct_scatter(*bad) == 7
+
+
 def test_merge_sort_host_checks_without_gpu(lib):
     I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
     sizes = {}

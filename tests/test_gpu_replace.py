@@ -203,3 +203,43 @@ def test_materialize_rejects_a_ref_past_its_input(lsm):
 
 
 LSM_REF_FROM_B_PY = 0x80000000
+
+
+# ---- the tiled direct scatter path ([CB] "The three experimental paths") ----
+def run_direct_scatter(lsm, A, B):
+    m, n = len(A), len(B)
+    dA, dB = up(A), up(B)
+    C, lb = lsm.collision_mark(dA, dB)
+    if m == 0:
+        C = up(np.zeros(4, np.uint32))
+    dir_, _ = lsm.rank_build(C, m)
+    refs, ordA, ordB, cnt = lsm.replacement_direct_scatter(dA, dB, C, dir_, lb)
+    N = int(cnt.item())
+    return dict(refs=down(refs)[:N], ordA=down(ordA), ordB=down(ordB), count=N)
+
+
+def check_scatter(got, A, B):
+    r = oracle.replacement_u64(A, B)
+    assert got["count"] == r.count
+    assert np.array_equal(got["refs"], r.refs)
+    assert np.array_equal(got["ordA"], r.ord_A)
+    assert np.array_equal(got["ordB"], r.ord_B)
+
+
+@pytest.mark.parametrize("m,n,shared,universe", [c for c in REPLACE_CASES if c[0] + c[1] > 0] + [
+    (20000, 7000, 7000, None), (7000, 20000, 7000, None), (100000, 100000, 50000, 250000),
+    (300000, 2000, 1000, None), (2000, 300000, 2000, None)])
+def test_direct_scatter_parity(lsm, m, n, shared, universe):
+    inp = synth.replace_random_small(seed=m * 7 + n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    check_scatter(run_direct_scatter(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_direct_scatter_replace_12M_4M(lsm):
+    inp = synth.replace_u64()
+    check_scatter(run_direct_scatter(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_direct_scatter_skewed_2pow24(lsm):
+    inp = synth.replace_skewed()
+    check_scatter(run_direct_scatter(lsm, inp.A, inp.B), inp.A, inp.B)
