@@ -685,6 +685,20 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
         "directory_bytes": {"rank512": 12 * (m // 512 + 1) + w2.numel(),
                             "rank2048": 8 * (m // 2048 + 1) + 8 * len(e2) + w4.numel()}}
     del d2, e2, w4
+    # The fused pass: mark, ordinals and refs in one tile pipeline, then the
+    # rank512 build over C (the same outputs as the three calls above).
+    w5 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_FUSED, m, n, dev)
+    stages_fu = [("replacement_merge_fused", lambda: lsm.replacement_merge_fused(
+        A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w5))]
+    ms_fu, per_fu = time_pipeline(torch, stages_fu, steps, flush)
+    out[name]["fused"] = {
+        "ms_per_step": ms_fu, "gelem_s": (m + n) / (ms_fu * 1e-3) / 1e9,
+        "algorithmic_bytes": alg, "gbs": alg / (ms_fu * 1e-3) / 1e9,
+        "frac": alg / (ms_fu * 1e-3) / 1e9 / peak,
+        "frac_of_8TBs_nominal": alg / (ms_fu * 1e-3) / 1e9 / 8000.0,
+        "kernel_ms": {"fused_tile_kernel": per_fu["replacement_merge_fused"]},
+        "gpu_launches_per_step": 3}
+    del w5
     # The tiled direct scatter in place of the compaction ("The three
     # experimental paths", second path): the same outputs, the keys read again.
     stages_sc = stages[:2] + [("replacement_direct_scatter", lambda: lsm.replacement_direct_scatter(

@@ -78,7 +78,8 @@ enum {
   LSM_OP_REPLACEMENT_COMPACT = 5,
   LSM_OP_FC_LENGTHS_SCAN = 6,
   LSM_OP_MERGE_SORT = 7,
-  LSM_OP_RANK2048_BUILD = 8
+  LSM_OP_RANK2048_BUILD = 8,
+  LSM_OP_REPLACEMENT_FUSED = 9
 };
 
 #define LSM_REF_FROM_B 0x80000000u
@@ -289,6 +290,24 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                           uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
                                           int64_t *d_count, void *ws, size_t ws_bytes,
                                           void *stream);
+
+/* a3 + a4 + a5 in one call: the same outputs as lsm_collision_mark,
+ * lsm_rank_build and lsm_replacement_merge_compact in turn (C, lb_B, dir,
+ * *d_total = R(m), out_refs, ord_A, ord_B, *d_count = m + n - R(m)), from
+ * one pass over merge-path tiles of the keys ([GC] merge paragraph: a
+ * partitioned merge whose neighbouring-key comparison and scan keep the
+ * newer record of each equal-key run) plus the rank512 build over C. Each
+ * tile finds its lower bounds and collision bits on staged keys and places
+ * its records at the ordinals of [CB] "Corrected record ordinals", taking
+ * R of its first A record from a decoupled lookback over the tiles'
+ * collision counts. Arguments, alignment and limits as those three calls;
+ * C needs no clearing. ws: at least
+ * lsm_workspace_size(LSM_OP_REPLACEMENT_FUSED, 0, m, n) bytes. */
+LSM_API int lsm_replacement_merge_fused(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                        uint32_t *C, uint32_t *lb_B, uint32_t *dir,
+                                        int64_t *d_total, uint32_t *out_refs, uint32_t *ord_A,
+                                        uint32_t *ord_B, int64_t *d_count, void *ws,
+                                        size_t ws_bytes, void *stream);
 
 /* The same compaction, reading R(i) from the rank2048 directory
  * (lsm_rank2048_build) instead of the rank512 one: [CB] "Suggested separate

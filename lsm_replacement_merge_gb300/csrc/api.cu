@@ -119,6 +119,13 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n, int key_type = LSM_KEY_U64) {
     case LSM_OP_RANK2048_BUILD:
       c.take<uint32_t>(rank2048_build_ctas(m));
       break;
+    case LSM_OP_REPLACEMENT_FUSED: {
+      const int64_t G = (m + n + fused_tile() - 1) / fused_tile();
+      c.take<int64_t>(G + 1);
+      c.take<uint64_t>(G > 0 ? G : 1);
+      c.take<uint64_t>(rank_build_ctas(m));
+      break;
+    }
     case LSM_OP_REPLACEMENT_COMPACT: {
       const int64_t D = replace_min_tile();
       c.take<int64_t>((m + n + D - 1) / D + 1);
@@ -183,7 +190,7 @@ LSM_API int lsm_workspace_size(int op, int key_type, int64_t m, int64_t n, size_
   if ((op == LSM_OP_MERGE_STABLE || op == LSM_OP_MERGE_SORT) && key_type != LSM_KEY_I32 &&
       key_type != LSM_KEY_U64)
     return LSM_ERR_DTYPE;
-  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_RANK2048_BUILD) return LSM_ERR_ARG;
+  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_REPLACEMENT_FUSED) return LSM_ERR_ARG;
   *bytes = ws_bytes_for(op, m, n, key_type);
   return LSM_OK;
 }
@@ -376,6 +383,33 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
   int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
   return cuda_status(launch_compact(m, n, C, dir, lb_B, out_refs, ord_A, ord_B, d_count, part,
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_replacement_merge_fused(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                        uint32_t *C, uint32_t *lb_B, uint32_t *dir,
+                                        int64_t *d_total, uint32_t *out_refs, uint32_t *ord_A,
+                                        uint32_t *ord_B, int64_t *d_count, void *ws,
+                                        size_t ws_bytes, void *stream) {
+  if (m < 0 || n < 0 || !dir || !d_total || !d_count) return LSM_ERR_ARG;
+  if ((m && (!A || !C || !ord_A)) || (n && (!B || !lb_B || !ord_B)) || (m + n && !out_refs))
+    return LSM_ERR_ARG;
+  if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
+  for (const void *p : {static_cast<const void *>(A), static_cast<const void *>(B),
+                        static_cast<const void *>(C), static_cast<const void *>(lb_B),
+                        static_cast<const void *>(out_refs), static_cast<const void *>(ord_A),
+                        static_cast<const void *>(ord_B)})
+    if (p && !aligned16(p)) return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_REPLACEMENT_FUSED, m, n, ws, ws_bytes)) return r;
+  Carver c{static_cast<uint8_t *>(ws)};
+  const int64_t G = (m + n + fused_tile() - 1) / fused_tile();
+  int64_t *part = c.take<int64_t>(G + 1);
+  uint64_t *state = c.take<uint64_t>(G > 0 ? G : 1);
+  uint64_t *rank_ws = c.take<uint64_t>(rank_build_ctas(m));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_replacement_fused(A ? A : B, m, B ? B : A, n, C, lb_B, out_refs, ord_A,
+                                           ord_B, d_count, part, state, status_ptr(), s);
+  if (e == cudaSuccess) e = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status_ptr(), s);
+  return cuda_status(e);
 }
 
 LSM_API int lsm_replacement_direct_scatter(const uint64_t *A, int64_t m, const uint64_t *B,

@@ -72,6 +72,14 @@ cudaError_t launch_compact_rank2048(int64_t m, int64_t n, const uint32_t *C, con
                                     uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
                                     int64_t *part_i, int32_t *status, cudaStream_t s);
 int64_t rank_build_ctas(int64_t m);
+// The fused pass: collision bits, lb_B, ordinals, refs and the count in one
+// tile pipeline. part_i: ceil((m+n)/fused_tile()) + 1 int64; state: as many
+// uint64 tile states as tiles.
+int64_t fused_tile();
+cudaError_t launch_replacement_fused(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                     uint32_t *C, uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
+                                     uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
+                                     uint64_t *state, int32_t *status, cudaStream_t s);
 
 // --- rank2048.cu ---
 int64_t rank2048_build_ctas(int64_t m);

@@ -82,12 +82,18 @@ template <class Pred>
 __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, int64_t n, int64_t D,
                                                         int64_t G, int64_t *__restrict__ out_i,
                                                         uint32_t *__restrict__ clear_words,
-                                                        int64_t nclear) {
+                                                        int64_t nclear,
+                                                        uint64_t *__restrict__ clear_states,
+                                                        int64_t nstates) {
   pdl_begin();
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (clear_words) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
+  }
+  if (clear_states) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t w = gtid; w < nstates; w += stride) clear_states[w] = 0u;
   }
   const int64_t g = gtid / kPartitionLanes;
   const bool active = g <= G;
@@ -99,13 +105,14 @@ __global__ void __launch_bounds__(256) partition_kernel(Pred pred, int64_t m, in
 
 template <class Pred>
 cudaError_t launch_partition(const Pred &pred, int64_t m, int64_t n, int64_t D, int64_t *out_i,
-                             uint32_t *clear_words, int64_t nclear, cudaStream_t s) {
+                             uint32_t *clear_words, int64_t nclear, cudaStream_t s,
+                             uint64_t *clear_states = nullptr, int64_t nstates = 0) {
   const int64_t G = (m + n + D - 1) / D;
   int64_t threads = (G + 1) * kPartitionLanes;
   if (clear_words && threads < nclear / 4) threads = nclear / 4;
   const int64_t blocks = (threads + 255) / 256;
   return launch_kernel(true, partition_kernel<Pred>, static_cast<unsigned>(blocks), 256, 0, s, pred,
-                       m, n, D, G, out_i, clear_words, nclear);
+                       m, n, D, G, out_i, clear_words, nclear, clear_states, nstates);
 }
 
 // ---- rank512 --------------------------------------------------------------------
@@ -810,6 +817,314 @@ struct CompactSpec {
   }
 };
 
+// ---- fused: collision bits, lower bounds, ordinals and refs in one pass -------------
+// The three steps above in one pass over merge-path tiles of the keys (A
+// first on ties): each tile stages A[i0-1, i1) and B[j0, j1] as the mark
+// does and finds lb_B and its own collision bits, then places its records as
+// the compaction does. R(i0), the collisions of all earlier tiles, comes from
+// a decoupled lookback over the tiles' collision counts instead of the rank
+// directory (every A record before i0 lies in an earlier tile). In this
+// A-first order a colliding B_j follows its equal A_i, so B record bi sits at
+// tile slot bi + L'_bi with L'_bi = lb_B[j] + c_j - i0 (c_j = 1 when B_j
+// matched), and precedes tile A record a exactly when L'_bi <= a. Every
+// output position is k0 + slot - (R(i0) + dropped tile A records before the
+// slot): the ordinals of [CB] "Corrected record ordinals". Tile states are
+// flag << 62 | value words (1 = aggregate, 2 = inclusive prefix), cleared by
+// the partition launch; each lookback wait is bounded in time. All CTAs of
+// the persistent grid are resident, and a tile waits only on earlier tiles,
+// each of which its CTA reaches without waiting on a later one.
+constexpr uint64_t kStateAgg = 1ull << 62, kStateInc = 2ull << 62;
+constexpr uint64_t kStateVal = (1ull << 62) - 1;
+
+template <int T_, int E_, int S_>
+struct FusedSpec {
+  static constexpr int T = T_;
+  static constexpr int E = E_;
+  static constexpr int S = S_;
+  static constexpr int D = T * E;
+  static constexpr int NC = D / 32 + 4;  // collision words of one tile, at most
+  static constexpr int64_t kStageBytes = align_up(int64_t(D + 4) * 8 + 160, 16);
+  static constexpr int64_t kLB = 0;
+  static constexpr int64_t kRefs = kLB + align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kOrd = kRefs + align_up(int64_t(D + 8) * 4, 16);
+  static constexpr int64_t kLp = kOrd + align_up(int64_t(D + 16) * 4, 16);
+  static constexpr int64_t kM = kLp + align_up(int64_t(D) * 2, 16);
+  static constexpr int64_t kCw = kM + align_up(int64_t(D + 1) * 2, 16);
+  static constexpr int64_t kPC = kCw + align_up(int64_t(NC) * 4, 16);
+  static constexpr int64_t kQ = kPC + align_up(int64_t(NC + 1) * 4, 16);
+  static constexpr int64_t kScan = kQ + align_up(int64_t(D / 32 + 2) * 4, 16);
+  static constexpr int64_t kBcast = kScan + align_up(int64_t(2 * (T / 32 + 1)) * 4, 16);
+  static constexpr int64_t kWorkBytes = kBcast + 16;
+  static_assert(NC <= T, "one thread per collision word");
+  static_assert(E <= 32, "a thread's collision bits fit one 64-bit window");
+  static_assert(D < 65536, "16-bit slots");
+  struct Params {
+    const uint64_t *A, *B;
+    int64_t m, n, G;
+    const int64_t *part_i;
+    uint32_t *C, *lb_B, *refs, *ord_A, *ord_B;
+    int64_t *d_count;
+    uint64_t *state;
+    int32_t *status;
+  };
+  struct Desc {
+    int64_t i0, j0;
+    int32_t na, nb, hp, hn, offA, offB;
+  };
+  __device__ __forceinline__ static void init(uint8_t *work) {
+    uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
+    uint16_t *sM = reinterpret_cast<uint16_t *>(work + kM);
+    for (int x = threadIdx.x; x < NC; x += T) sCw[x] = 0u;
+    for (int x = threadIdx.x; x < D + 1; x += T) sM[x] = 0;
+  }
+  __device__ __forceinline__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
+    v[0] = __ldg(p.part_i + g);
+    v[1] = __ldg(p.part_i + g + 1);
+  }
+  __device__ __forceinline__ static void produce(const Params &p, int64_t g, const int64_t v[4],
+                                                 uint8_t *stage, Desc &d, uint64_t *full) {
+    const int64_t total = p.m + p.n;
+    const int64_t i0 = v[0], i1 = v[1];
+    const int64_t k0 = g * D, k1 = k0 + D < total ? k0 + D : total;
+    const int64_t j0 = k0 - i0, j1 = k1 - i1;
+    const int na = static_cast<int>(i1 - i0), nb = static_cast<int>(j1 - j0);
+    const int hp = i0 > 0 ? 1 : 0, hn = j1 < p.n ? 1 : 0;
+    const StagePlan pa = stage_plan_overfetch<8>(i0 - hp, na + hp, p.m);
+    const StagePlan pb = stage_plan_overfetch<8>(j0, nb + hn, p.n);
+    uint64_t *bufA = reinterpret_cast<uint64_t *>(stage);
+    const int32_t offB = static_cast<int32_t>(stage_capacity_bytes<8>(pa.span) / 8);
+    uint64_t *bufB = bufA + offB;
+    for (int64_t x = pa.tail_from; x < i1; ++x) bufA[x - pa.first] = p.A[x];
+    for (int64_t x = pb.tail_from; x < j1 + hn; ++x) bufB[x - pb.first] = p.B[x];
+    d.i0 = i0;
+    d.j0 = j0;
+    d.na = na;
+    d.nb = nb;
+    d.hp = hp;
+    d.hn = hn;
+    d.offA = pa.lead + hp;
+    d.offB = offB + pb.lead;
+    mbar_arrive_expect_tx(full, pa.bulk + pb.bulk);
+    stage_issue(bufA, p.A, pa, full);
+    stage_issue(bufB, p.B, pb, full);
+  }
+
+  // R(i0) for tile g: publish the tile's collision count, sum the earlier
+  // tiles' published counts back to the first inclusive prefix (warp 0).
+  __device__ __forceinline__ static uint32_t lookback(const Params &p, int64_t g, uint32_t totC,
+                                                      uint32_t *bcast) {
+    const int tid = threadIdx.x;
+    if (tid < 32) {
+      const int lane = tid;
+      uint64_t prefix = 0;
+      if (g == 0) {
+        if (lane == 0) st_relaxed_u64(p.state, kStateInc | totC);
+      } else {
+        if (lane == 0) st_relaxed_u64(p.state + g, kStateAgg | totC);
+        int64_t base = g - 1;
+        const uint64_t t0 = globaltimer_ns();
+        bool late = false;
+        for (;;) {
+          const int64_t idx = base - lane;
+          uint64_t v = idx >= 0 ? ld_relaxed_u64(p.state + idx) : kStateInc;
+          uint32_t polls = 0;
+          while (!__all_sync(0xffffffffu, (v >> 62) != 0)) {
+            if ((v >> 62) == 0) v = ld_relaxed_u64(p.state + idx);
+            if ((++polls & 31) == 0 &&
+                __any_sync(0xffffffffu, globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs))) {
+              late = true;
+              if ((v >> 62) == 0) v = kStateInc;  // give up: counted as zero
+            }
+          }
+          const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 62) == 2);
+          uint64_t c = v & kStateVal;
+          if (inc) {
+            const int first = __ffs(inc) - 1;
+            c = lane <= first ? c : 0;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+          prefix += c;
+          if (inc) break;
+          base -= 32;
+        }
+        if (lane == 0) {
+          if (late) report(p.status, LSM_ERR_TIMEOUT);
+          st_relaxed_u64(p.state + g, kStateInc | ((prefix + totC) & kStateVal));
+        }
+      }
+      if (lane == 0) *bcast = static_cast<uint32_t>(prefix);
+    }
+    named_sync(1, T);
+    return *bcast;
+  }
+
+  __device__ __forceinline__ static void consume(const Params &p, int64_t g, const Desc &dd,
+                                                 const uint8_t *stage, uint8_t *work,
+                                                 uint64_t *empty) {
+    const int tid = threadIdx.x;
+    const uint64_t *sA = reinterpret_cast<const uint64_t *>(stage) + dd.offA;  // sA[-1] = A[i0-1]
+    const uint64_t *sB = reinterpret_cast<const uint64_t *>(stage) + dd.offB;  // sB[nb] = B[j1]
+    uint32_t *sLBbuf = reinterpret_cast<uint32_t *>(work + kLB);
+    uint32_t *bufRefs = reinterpret_cast<uint32_t *>(work + kRefs);
+    uint32_t *bufOrd = reinterpret_cast<uint32_t *>(work + kOrd);
+    uint16_t *sLp = reinterpret_cast<uint16_t *>(work + kLp);
+    uint16_t *sM = reinterpret_cast<uint16_t *>(work + kM);
+    uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
+    uint32_t *sPC = reinterpret_cast<uint32_t *>(work + kPC);
+    int *sQ = reinterpret_cast<int *>(work + kQ);
+    uint32_t *sScan = reinterpret_cast<uint32_t *>(work + kScan);
+    uint32_t *sBcast = reinterpret_cast<uint32_t *>(work + kBcast);
+    const int na = dd.na, nb = dd.nb, hp = dd.hp, hn = dd.hn;
+    const int64_t i0 = dd.i0, j0 = dd.j0, i1 = i0 + na;
+    const int64_t k0 = g * D;
+    uint32_t *sLB = sLBbuf + (j0 & 3);  // global alignment of lb_B[j0] mirrored
+    const int64_t w0 = i0 >> 5;
+    const int wbit0 = static_cast<int>(i0 - (w0 << 5));  // bit of A[i0] in word w0
+    const int nwc = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
+
+    // 1. lower bounds over the staged A span (with A[i0-1] when it exists):
+    //    group heads first, then each B key between its head's bound and the
+    //    next head's; the match bit of each B, its slot offset L', and the
+    //    collision bits of this tile's own A records
+    const uint64_t *sAx = sA - hp;
+    const int lenx = na + hp;
+    const uint32_t base = static_cast<uint32_t>(i0 - hp);
+    const int ngroups = (nb + 31) >> 5;
+    for (int q = tid; q < ngroups; q += T) {
+      const uint64_t key = sB[q << 5];
+      int lo = 0, hi = lenx;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sAx[mid] < key) lo = mid + 1;
+        else hi = mid;
+      }
+      sQ[q] = lo;
+    }
+    if (tid == 0) sQ[ngroups] = lenx;
+    named_sync(1, T);
+    for (int bi = tid; bi < nb; bi += T) {
+      const uint64_t key = sB[bi];
+      const int q = bi >> 5;
+      int lo = sQ[q], hi = (bi & 31) ? sQ[q + 1] : lo;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sAx[mid] < key) lo = mid + 1;
+        else hi = mid;
+      }
+      sLB[bi] = base + static_cast<uint32_t>(lo);
+      const bool match = lo < lenx && sAx[lo] == key;
+      // a match with A[i0-1] is the previous tile's collision bit
+      if (match && lo >= hp) {
+        const int x = wbit0 + (lo - hp);
+        atomicOr(&sCw[x >> 5], 1u << (x & 31));
+      }
+      int Lp = lo - hp + (match ? 1 : 0);  // in [0, na] for a valid partition
+      Lp = Lp < 0 ? 0 : (Lp > na ? na : Lp);
+      sLp[bi] = static_cast<uint16_t>(Lp);
+    }
+    // the tile's last A against the first B after the tile
+    if (tid == 0 && hn && na > 0 && sA[na - 1] == sB[nb]) {
+      const int x = wbit0 + na - 1;
+      atomicOr(&sCw[x >> 5], 1u << (x & 31));
+    }
+    release_stage(empty);  // the keys are not read again
+    named_sync(1, T);
+
+    // 2. the last B of each run of equal L' marks sM[L'] = bi + 1: B records
+    //    before tile A record a = the prefix maximum of sM up to a
+    for (int bi = tid; bi < nb; bi += T) {
+      const int L = sLp[bi];
+      const int Ln = bi + 1 < nb ? sLp[bi + 1] : -1;
+      if (L < na && Ln != L) sM[L] = static_cast<uint16_t>(bi + 1);
+    }
+    named_sync(1, T);
+    // 3. one scan: prefix popcounts of the tile's collision words and the
+    //    prefix maximum of sM over each thread's E consecutive A records
+    const int a0 = tid * E;
+    uint32_t mv[E];
+    uint32_t mloc = 0;
+#pragma unroll
+    for (int q = 0; q < E; ++q) {
+      mv[q] = a0 + q < na ? sM[a0 + q] : 0u;
+      mloc = mv[q] > mloc ? mv[q] : mloc;
+    }
+#pragma unroll
+    for (int q = 0; q < E; ++q)
+      if (a0 + q < na && mv[q]) sM[a0 + q] = 0;  // clean for the next tile
+    const uint32_t cw_own = tid < nwc ? sCw[tid] : 0u;
+    uint32_t totC, mbefore;
+    const uint32_t exC = consumer_exclusive_sum_max<T>(static_cast<uint32_t>(__popc(cw_own)), mloc,
+                                                       sScan, &totC, &mbefore);
+    if (tid < nwc) sPC[tid] = exC;
+    // 4. R(i0) from the earlier tiles (contains a barrier over the consumers)
+    const uint32_t r0 = lookback(p, g, totC, sBcast);
+    const int64_t out0 = k0 - r0;
+    const uint32_t i0u = static_cast<uint32_t>(i0), j0u = static_cast<uint32_t>(j0);
+    const uint32_t out0u = static_cast<uint32_t>(out0);
+    const int cnt = na + nb;
+    const int offB = (na + 3 + 4) & ~3;  // ord_B's part starts past ord_A's, 16-byte aligned
+    uint32_t *sRefs = bufRefs + (out0 & 3);
+    uint32_t *sOrdA = bufOrd + (i0 & 3);
+    uint32_t *sOrdB = bufOrd + offB + (j0 & 3);
+    // dropped tile A records among [0, x), x in [0, na]
+    auto dropped_before = [&](int x) -> int {
+      if (x >= na) return static_cast<int>(totC);
+      const int xa = wbit0 + x, wa = xa >> 5;
+      return static_cast<int>(sPC[wa]) + __popc(sCw[wa] & ((1u << (xa & 31)) - 1u));
+    };
+    // 5. A records: slot a + (B records before it) minus the dropped before it
+    if (a0 < na) {
+      int drops = dropped_before(a0);
+      uint32_t run = mbefore;
+      const int xa0 = wbit0 + a0;
+      const uint64_t win =
+          ((static_cast<uint64_t>(sCw[(xa0 >> 5) + 1]) << 32) | sCw[xa0 >> 5]) >> (xa0 & 31);
+      const int lim = na - a0 < E ? na - a0 : E;
+#pragma unroll
+      for (int q = 0; q < E; ++q) {
+        if (q < lim) {
+          run = mv[q] > run ? mv[q] : run;
+          const bool dropped = (win >> q) & 1u;
+          const int ol = a0 + q + static_cast<int>(run) - drops;
+          if (!dropped) sRefs[ol] = i0u + static_cast<uint32_t>(a0 + q);
+          sOrdA[a0 + q] = dropped ? LSM_ORD_DROPPED : out0u + static_cast<uint32_t>(ol);
+          drops += dropped ? 1 : 0;
+        }
+      }
+    }
+    // 6. B records: slot bi + L' minus the dropped A records before it
+    for (int bi = tid; bi < nb; bi += T) {
+      const int L = sLp[bi];
+      const int ol = bi + L - dropped_before(L);
+      sRefs[ol] = LSM_REF_FROM_B | (j0u + static_cast<uint32_t>(bi));
+      sOrdB[bi] = out0u + static_cast<uint32_t>(ol);
+    }
+    fence_proxy_async_smem();
+    named_sync(1, T);
+    store_u32_run<T>(p.lb_B, j0, nb, sLBbuf);
+    store_u32_run<T>(p.refs, out0, cnt - static_cast<int>(totC), bufRefs);
+    store_u32_run<T>(p.ord_A, i0, na, bufOrd);
+    store_u32_run<T>(p.ord_B, j0, nb, bufOrd + offB);
+    if (tid == 0) {
+      bulk_commit();
+      if (g == p.G - 1) *p.d_count = p.m + p.n - (static_cast<int64_t>(r0) + totC);
+    }
+    // collision words: whole words inside the tile's A range by plain
+    // stores, the shared boundary words by atomicOr (C was cleared)
+    for (int x = tid; x < nwc; x += T) {
+      const int64_t w = w0 + x;
+      const uint32_t bits = sCw[x];
+      if (w * 32 >= i0 && w * 32 + 32 <= i1) p.C[w] = bits;
+      else if (bits) atomicOr(&p.C[w], bits);
+    }
+    named_sync(1, T);  // every read of sCw is done before it is cleared
+    for (int x = tid; x < nwc + 1 && x < NC; x += T) sCw[x] = 0u;
+    if (tid == 0) bulk_wait_read_all();  // the staging buffers are rewritten by the next tile
+    named_sync(1, T);
+  }
+};
+
 }  // namespace
 
 // Tile variants of the two replacement pipelines: (consumer threads, items
@@ -850,6 +1165,35 @@ cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *
     case 3: return launch_mark_variant<3>(A, m, B, n, C, lb_B, part_i, status, s);
     default: return launch_mark_variant<0>(A, m, B, n, C, lb_B, part_i, status, s);
   }
+}
+
+// ---- fused replacement ---------------------------------------------------------------
+constexpr int kFusedT = 256, kFusedE = 11, kFusedS = 2;
+using FusedDefault = FusedSpec<kFusedT, kFusedE, kFusedS>;
+
+__global__ void set_count_kernel(int64_t *d_count, int64_t v) {
+  pdl_begin();
+  *d_count = v;
+}
+
+int64_t fused_tile() { return FusedDefault::D; }
+
+cudaError_t launch_replacement_fused(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                     uint32_t *C, uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
+                                     uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
+                                     uint64_t *state, int32_t *status, cudaStream_t s) {
+  using Spec = FusedDefault;
+  constexpr int64_t D = Spec::D;
+  const int64_t G = (m + n + D - 1) / D;
+  if (G == 0) return launch_kernel(false, set_count_kernel, 1, 1, 0, s, d_count, int64_t(0));
+  const int64_t nwords = (m + 31) / 32;
+  cudaError_t err = launch_partition(U64AFirst{A, B}, m, n, D, part_i, C, nwords, s, state, G);
+  if (err != cudaSuccess) return err;
+  typename Spec::Params p{A, B, m, n, G, part_i, C, lb_B, refs, ord_A, ord_B, d_count, state, status};
+  profile_before(s);
+  err = launch_pipeline<Spec>(p, G, status, s, device_sm_count());
+  profile_after(s);
+  return err;
 }
 
 int64_t replace_min_tile() {

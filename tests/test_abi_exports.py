@@ -108,6 +108,28 @@ def test_direct_scatter_host_checks_without_gpu(lib):
     assert lib.lsm_replacement_direct_scatter(*bad) == 7
 
 
+def test_fused_host_checks_without_gpu(lib):
+    I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    size = ctypes.c_size_t(0)
+    assert lib.lsm_workspace_size(9, 0, 12_000_000, 4_000_000, ctypes.byref(size)) == 0
+    tiles = (16_000_000 + 2815) // 2816
+    assert size.value >= 16 * tiles  # a co-rank and a state per tile
+    args = [P(16), I(10), P(16), I(10), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16),
+            P(16), S(1 << 20), None]
+    bad = list(args)
+    bad[6] = None                                              # dir
+    assert lib.lsm_replacement_merge_fused(*bad) == 1
+    bad = list(args)
+    bad[3] = I(1 << 31)
+    assert lib.lsm_replacement_merge_fused(*bad) == 3
+    bad = list(args)
+    bad[8] = P(20)                                             # refs misaligned
+    assert lib.lsm_replacement_merge_fused(*bad) == 7
+    bad = list(args)
+    bad[13] = S(8)
+    assert lib.lsm_replacement_merge_fused(*bad) == 6
+
+
 def test_merge_sort_host_checks_without_gpu(lib):
     I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
     sizes = {}

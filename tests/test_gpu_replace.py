@@ -243,3 +243,58 @@ def test_direct_scatter_replace_12M_4M(lsm):
 def test_direct_scatter_skewed_2pow24(lsm):
     inp = synth.replace_skewed()
     check_scatter(run_direct_scatter(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+# ---- the fused pass: mark, rank, ordinals and refs in one call ----------------
+def run_fused(lsm, A, B):
+    m, n = len(A), len(B)
+    C, lb, dir_, tot, refs, ordA, ordB, cnt = lsm.replacement_merge_fused(up(A), up(B))
+    N = int(cnt.item())
+    return dict(C=down(C)[:(m + 31) // 32], lb=down(lb), dir=down(dir_), total=int(tot.item()),
+                refs=down(refs)[:N], ordA=down(ordA), ordB=down(ordB), count=N)
+
+
+@pytest.mark.parametrize("m,n,shared,universe", REPLACE_CASES + [
+    (20000, 7000, 7000, None), (7000, 20000, 7000, None), (100000, 100000, 50000, 250000),
+    (300000, 2000, 1000, None), (2000, 300000, 2000, None), (1000000, 1000000, 1000000, None)])
+def test_fused_parity(lsm, m, n, shared, universe):
+    inp = synth.replace_random_small(seed=m * 7 + n + shared, m=m, n=n, shared=shared,
+                                     universe=universe)
+    check_against_oracle(run_fused(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_fused_single_record_edges(lsm):
+    for A, B in (([5], [5]), ([5], [6]), ([6], [5]), ([], [1]), ([1], []), ([1, 2, 3], [0, 2, 4])):
+        A = np.array(A, np.uint64)
+        B = np.array(B, np.uint64)
+        check_against_oracle(run_fused(lsm, A, B), A, B)
+
+
+def test_fused_empty(lsm):
+    e = up(np.zeros(0, np.uint64))
+    *_, refs, _, _, cnt = lsm.replacement_merge_fused(e, e)
+    assert int(cnt.item()) == 0
+
+
+def test_fused_replace_12M_4M(lsm):
+    inp = synth.replace_u64()
+    check_against_oracle(run_fused(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_fused_skewed_2pow24(lsm):
+    inp = synth.replace_skewed()
+    check_against_oracle(run_fused(lsm, inp.A, inp.B), inp.A, inp.B)
+
+
+def test_fused_twice_reuses_workspace(lsm):
+    # the tile states are cleared by each call's partition: a workspace left
+    # by an earlier call (other sizes) must not leak into the next one
+    ws = lsm.workspace(lsm.LSM_OP_REPLACEMENT_FUSED, 300000, 300000, torch.device("cuda"))
+    for seed, (m, n, shared) in enumerate(((300000, 300000, 100000), (200000, 50000, 40000))):
+        inp = synth.replace_random_small(seed=seed + 99, m=m, n=n, shared=shared)
+        C, lb, dir_, tot, refs, ordA, ordB, cnt = lsm.replacement_merge_fused(up(inp.A), up(inp.B),
+                                                                            ws=ws)
+        N = int(cnt.item())
+        got = dict(C=down(C)[:(m + 31) // 32], lb=down(lb), dir=down(dir_), total=int(tot.item()),
+                   refs=down(refs)[:N], ordA=down(ordA), ordB=down(ordB), count=N)
+        check_against_oracle(got, inp.A, inp.B)
