@@ -819,20 +819,25 @@ struct CompactSpec {
 
 // ---- fused: collision bits, lower bounds, ordinals and refs in one pass -------------
 // The three steps above in one pass over merge-path tiles of the keys (A
-// first on ties): each tile stages A[i0-1, i1) and B[j0, j1] as the mark
-// does and finds lb_B and its own collision bits, then places its records as
-// the compaction does. R(i0), the collisions of all earlier tiles, comes from
-// a decoupled lookback over the tiles' collision counts instead of the rank
-// directory (every A record before i0 lies in an earlier tile). In this
-// A-first order a colliding B_j follows its equal A_i, so B record bi sits at
-// tile slot bi + L'_bi with L'_bi = lb_B[j] + c_j - i0 (c_j = 1 when B_j
-// matched), and precedes tile A record a exactly when L'_bi <= a. Every
-// output position is k0 + slot - (R(i0) + dropped tile A records before the
-// slot): the ordinals of [CB] "Corrected record ordinals". Tile states are
-// flag << 62 | value words (1 = aggregate, 2 = inclusive prefix), cleared by
-// the partition launch; each lookback wait is bounded in time. All CTAs of
-// the persistent grid are resident, and a tile waits only on earlier tiles,
-// each of which its CTA reaches without waiting on a later one.
+// first on ties), by the stable merge's own walk: each tile stages A[i0-1,
+// i1) and B[j0, j1] (the keys on either side included where they exist);
+// each of T threads bisects its diagonal d = tid E inside the staged spans
+// and walks E merge steps, which give every record directly:
+//   an A record is dropped exactly when the B head it is compared with (the
+//     next B in merged order, B[j1] past the tile's end) has its key;
+//   a B record's lb_B is i0 plus the tile A records taken before it, minus
+//     one when the A record just before it has its key;
+//   every record's merged slot is d + step.
+// One scan of the threads' drop counts gives each slot its dropped A records
+// before it, and R(i0), the collisions of all earlier tiles, comes from a
+// decoupled lookback over the tiles' collision counts (every A record
+// before i0 lies in an earlier tile), so a record lands at k0 + slot -
+// (R(i0) + dropped before it in the tile): the ordinals of [CB] "Corrected
+// record ordinals". Tile states are flag << 62 | value words (1 = aggregate,
+// 2 = inclusive prefix), cleared by the partition launch; each lookback wait
+// is bounded in time. All CTAs of the persistent grid are resident, and a
+// tile waits only on earlier tiles, each of which its CTA reaches without
+// waiting on a later one.
 constexpr uint64_t kStateAgg = 1ull << 62, kStateInc = 2ull << 62;
 constexpr uint64_t kStateVal = (1ull << 62) - 1;
 
@@ -847,17 +852,11 @@ struct FusedSpec {
   static constexpr int64_t kLB = 0;
   static constexpr int64_t kRefs = kLB + align_up(int64_t(D + 8) * 4, 16);
   static constexpr int64_t kOrd = kRefs + align_up(int64_t(D + 8) * 4, 16);
-  static constexpr int64_t kLp = kOrd + align_up(int64_t(D + 16) * 4, 16);
-  static constexpr int64_t kM = kLp + align_up(int64_t(D) * 2, 16);
-  static constexpr int64_t kCw = kM + align_up(int64_t(D + 1) * 2, 16);
-  static constexpr int64_t kPC = kCw + align_up(int64_t(NC) * 4, 16);
-  static constexpr int64_t kQ = kPC + align_up(int64_t(NC + 1) * 4, 16);
-  static constexpr int64_t kScan = kQ + align_up(int64_t(D / 32 + 2) * 4, 16);
-  static constexpr int64_t kBcast = kScan + align_up(int64_t(2 * (T / 32 + 1)) * 4, 16);
+  static constexpr int64_t kCw = kOrd + align_up(int64_t(D + 16) * 4, 16);
+  static constexpr int64_t kScan = kCw + align_up(int64_t(NC) * 4, 16);
+  static constexpr int64_t kBcast = kScan + align_up(int64_t(T / 32 + 1) * 4, 16);
   static constexpr int64_t kWorkBytes = kBcast + 16;
-  static_assert(NC <= T, "one thread per collision word");
-  static_assert(E <= 32, "a thread's collision bits fit one 64-bit window");
-  static_assert(D < 65536, "16-bit slots");
+  static_assert(D < 32768, "15-bit tile indices");
   struct Params {
     const uint64_t *A, *B;
     int64_t m, n, G;
@@ -873,9 +872,7 @@ struct FusedSpec {
   };
   __device__ __forceinline__ static void init(uint8_t *work) {
     uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
-    uint16_t *sM = reinterpret_cast<uint16_t *>(work + kM);
     for (int x = threadIdx.x; x < NC; x += T) sCw[x] = 0u;
-    for (int x = threadIdx.x; x < D + 1; x += T) sM[x] = 0;
   }
   __device__ __forceinline__ static void fetch(const Params &p, int64_t g, int64_t v[4]) {
     v[0] = __ldg(p.part_i + g);
@@ -962,143 +959,124 @@ struct FusedSpec {
   __device__ __forceinline__ static void consume(const Params &p, int64_t g, const Desc &dd,
                                                  const uint8_t *stage, uint8_t *work,
                                                  uint64_t *empty) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint64_t *sA = reinterpret_cast<const uint64_t *>(stage) + dd.offA;  // sA[-1] = A[i0-1]
     const uint64_t *sB = reinterpret_cast<const uint64_t *>(stage) + dd.offB;  // sB[nb] = B[j1]
     uint32_t *sLBbuf = reinterpret_cast<uint32_t *>(work + kLB);
     uint32_t *bufRefs = reinterpret_cast<uint32_t *>(work + kRefs);
     uint32_t *bufOrd = reinterpret_cast<uint32_t *>(work + kOrd);
-    uint16_t *sLp = reinterpret_cast<uint16_t *>(work + kLp);
-    uint16_t *sM = reinterpret_cast<uint16_t *>(work + kM);
     uint32_t *sCw = reinterpret_cast<uint32_t *>(work + kCw);
-    uint32_t *sPC = reinterpret_cast<uint32_t *>(work + kPC);
-    int *sQ = reinterpret_cast<int *>(work + kQ);
     uint32_t *sScan = reinterpret_cast<uint32_t *>(work + kScan);
     uint32_t *sBcast = reinterpret_cast<uint32_t *>(work + kBcast);
     const int na = dd.na, nb = dd.nb, hp = dd.hp, hn = dd.hn;
     const int64_t i0 = dd.i0, j0 = dd.j0, i1 = i0 + na;
     const int64_t k0 = g * D;
-    uint32_t *sLB = sLBbuf + (j0 & 3);  // global alignment of lb_B[j0] mirrored
+    const int cnt = na + nb;
     const int64_t w0 = i0 >> 5;
     const int wbit0 = static_cast<int>(i0 - (w0 << 5));  // bit of A[i0] in word w0
     const int nwc = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
 
-    // 1. lower bounds over the staged A span (with A[i0-1] when it exists):
-    //    group heads first, then each B key between its head's bound and the
-    //    next head's; the match bit of each B, its slot offset L', and the
-    //    collision bits of this tile's own A records
-    const uint64_t *sAx = sA - hp;
-    const int lenx = na + hp;
-    const uint32_t base = static_cast<uint32_t>(i0 - hp);
-    const int ngroups = (nb + 31) >> 5;
-    for (int q = tid; q < ngroups; q += T) {
-      const uint64_t key = sB[q << 5];
-      int lo = 0, hi = lenx;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (sAx[mid] < key) lo = mid + 1;
-        else hi = mid;
-      }
-      sQ[q] = lo;
+    // 1. this thread's diagonal, bisected in the staged spans (A first on
+    //    ties), then E merge steps. Each record is kept as one word:
+    //    bit 31 = from B, bit 30 = dropped A / B matching the A before it,
+    //    bits 0..14 = its index in its tile span.
+    const int d = tid * E < cnt ? tid * E : cnt;
+    int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sA[mid] <= sB[d - mid - 1]) lo = mid + 1;
+      else hi = mid;
     }
-    if (tid == 0) sQ[ngroups] = lenx;
-    named_sync(1, T);
-    for (int bi = tid; bi < nb; bi += T) {
-      const uint64_t key = sB[bi];
-      const int q = bi >> 5;
-      int lo = sQ[q], hi = (bi & 31) ? sQ[q + 1] : lo;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (sAx[mid] < key) lo = mid + 1;
-        else hi = mid;
-      }
-      sLB[bi] = base + static_cast<uint32_t>(lo);
-      const bool match = lo < lenx && sAx[lo] == key;
-      // a match with A[i0-1] is the previous tile's collision bit
-      if (match && lo >= hp) {
-        const int x = wbit0 + (lo - hp);
-        atomicOr(&sCw[x >> 5], 1u << (x & 31));
-      }
-      int Lp = lo - hp + (match ? 1 : 0);  // in [0, na] for a valid partition
-      Lp = Lp < 0 ? 0 : (Lp > na ? na : Lp);
-      sLp[bi] = static_cast<uint16_t>(Lp);
-    }
-    // the tile's last A against the first B after the tile
-    if (tid == 0 && hn && na > 0 && sA[na - 1] == sB[nb]) {
-      const int x = wbit0 + na - 1;
-      atomicOr(&sCw[x >> 5], 1u << (x & 31));
-    }
-    release_stage(empty);  // the keys are not read again
-    named_sync(1, T);
-
-    // 2. the last B of each run of equal L' marks sM[L'] = bi + 1: B records
-    //    before tile A record a = the prefix maximum of sM up to a
-    for (int bi = tid; bi < nb; bi += T) {
-      const int L = sLp[bi];
-      const int Ln = bi + 1 < nb ? sLp[bi + 1] : -1;
-      if (L < na && Ln != L) sM[L] = static_cast<uint16_t>(bi + 1);
-    }
-    named_sync(1, T);
-    // 3. one scan: prefix popcounts of the tile's collision words and the
-    //    prefix maximum of sM over each thread's E consecutive A records
-    const int a0 = tid * E;
-    uint32_t mv[E];
-    uint32_t mloc = 0;
+    int ai = lo, bi = d - lo;
+    const int nbx = nb + hn;  // B keys staged, the one after the tile included
+    uint64_t a = ai < na ? sA[ai] : 0, b = bi < nbx ? sB[bi] : 0;
+    // A B record matches an A record exactly when the last A record taken
+    // before it has its key (with A first on ties the equal A comes right
+    // before it: no other B fits between equal keys). The last A before the
+    // thread's first record is A[i0 + ai - 1], or A[i0 - 1] when ai = 0.
+    bool prevA = ai > 0 || hp;
+    uint64_t prevkey = prevA ? sA[ai - 1] : 0;
+    uint32_t rec[E];
+    uint32_t drops = 0;
 #pragma unroll
     for (int q = 0; q < E; ++q) {
-      mv[q] = a0 + q < na ? sM[a0 + q] : 0u;
-      mloc = mv[q] > mloc ? mv[q] : mloc;
+      rec[q] = 0xFFFFFFFFu;
+      if (d + q < cnt) {
+        const bool takeA = bi >= nb || (ai < na && a <= b);
+        if (takeA) {
+          const bool dropped = bi < nbx && b == a;  // the next B has this key
+          rec[q] = (dropped ? 0x40000000u : 0u) | static_cast<uint32_t>(ai);
+          drops += dropped ? 1u : 0u;
+          prevA = true;
+          prevkey = a;
+          ++ai;
+          a = ai < na ? sA[ai] : 0;
+        } else {
+          const bool match = prevA && prevkey == b;
+          rec[q] = 0x80000000u | (match ? 0x40000000u : 0u) | static_cast<uint32_t>(bi) |
+                   (static_cast<uint32_t>(ai) << 15);
+          ++bi;
+          b = bi < nbx ? sB[bi] : 0;
+        }
+      }
     }
+    release_stage(empty);  // the keys are not read again
+    // 2. exclusive scan of the drop counts in merged order (thread order)
+    uint32_t inc = drops;
 #pragma unroll
-    for (int q = 0; q < E; ++q)
-      if (a0 + q < na && mv[q]) sM[a0 + q] = 0;  // clean for the next tile
-    const uint32_t cw_own = tid < nwc ? sCw[tid] : 0u;
-    uint32_t totC, mbefore;
-    const uint32_t exC = consumer_exclusive_sum_max<T>(static_cast<uint32_t>(__popc(cw_own)), mloc,
-                                                       sScan, &totC, &mbefore);
-    if (tid < nwc) sPC[tid] = exC;
-    // 4. R(i0) from the earlier tiles (contains a barrier over the consumers)
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) sScan[warp] = inc;
+    named_sync(1, T);
+    if (warp == 0) {
+      const uint32_t w = lane < T / 32 ? sScan[lane] : 0u;
+      uint32_t wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += t;
+      }
+      if (lane < T / 32) sScan[lane] = wi - w;
+      if (lane == T / 32 - 1) sScan[T / 32] = wi;
+    }
+    named_sync(1, T);
+    uint32_t before = sScan[warp] + inc - drops;  // dropped A records before slot d
+    const uint32_t totC = sScan[T / 32];
+    // 3. R(i0) from the earlier tiles (contains a barrier over the consumers)
     const uint32_t r0 = lookback(p, g, totC, sBcast);
     const int64_t out0 = k0 - r0;
-    const uint32_t i0u = static_cast<uint32_t>(i0), j0u = static_cast<uint32_t>(j0);
     const uint32_t out0u = static_cast<uint32_t>(out0);
-    const int cnt = na + nb;
+    const uint32_t i0u = static_cast<uint32_t>(i0), j0u = static_cast<uint32_t>(j0);
     const int offB = (na + 3 + 4) & ~3;  // ord_B's part starts past ord_A's, 16-byte aligned
     uint32_t *sRefs = bufRefs + (out0 & 3);
     uint32_t *sOrdA = bufOrd + (i0 & 3);
     uint32_t *sOrdB = bufOrd + offB + (j0 & 3);
-    // dropped tile A records among [0, x), x in [0, na]
-    auto dropped_before = [&](int x) -> int {
-      if (x >= na) return static_cast<int>(totC);
-      const int xa = wbit0 + x, wa = xa >> 5;
-      return static_cast<int>(sPC[wa]) + __popc(sCw[wa] & ((1u << (xa & 31)) - 1u));
-    };
-    // 5. A records: slot a + (B records before it) minus the dropped before it
-    if (a0 < na) {
-      int drops = dropped_before(a0);
-      uint32_t run = mbefore;
-      const int xa0 = wbit0 + a0;
-      const uint64_t win =
-          ((static_cast<uint64_t>(sCw[(xa0 >> 5) + 1]) << 32) | sCw[xa0 >> 5]) >> (xa0 & 31);
-      const int lim = na - a0 < E ? na - a0 : E;
+    uint32_t *sLB = sLBbuf + (j0 & 3);
+    // 4. every record to its output slot
 #pragma unroll
-      for (int q = 0; q < E; ++q) {
-        if (q < lim) {
-          run = mv[q] > run ? mv[q] : run;
-          const bool dropped = (win >> q) & 1u;
-          const int ol = a0 + q + static_cast<int>(run) - drops;
-          if (!dropped) sRefs[ol] = i0u + static_cast<uint32_t>(a0 + q);
-          sOrdA[a0 + q] = dropped ? LSM_ORD_DROPPED : out0u + static_cast<uint32_t>(ol);
-          drops += dropped ? 1 : 0;
+    for (int q = 0; q < E; ++q) {
+      const uint32_t r = rec[q];
+      if (r != 0xFFFFFFFFu) {
+        const int slot = d + q;
+        const int ol = slot - static_cast<int>(before);
+        const uint32_t idx = r & 0x7FFFu;
+        if (r & 0x80000000u) {
+          const uint32_t ai_at = (r >> 15) & 0x7FFFu;
+          sLB[idx] = i0u + ai_at - ((r & 0x40000000u) ? 1u : 0u);
+          sRefs[ol] = LSM_REF_FROM_B | (j0u + idx);
+          sOrdB[idx] = out0u + static_cast<uint32_t>(ol);
+        } else if (r & 0x40000000u) {
+          sOrdA[idx] = LSM_ORD_DROPPED;
+          const int x = wbit0 + static_cast<int>(idx);
+          atomicOr(&sCw[x >> 5], 1u << (x & 31));
+          ++before;
+        } else {
+          sRefs[ol] = i0u + idx;
+          sOrdA[idx] = out0u + static_cast<uint32_t>(ol);
         }
       }
-    }
-    // 6. B records: slot bi + L' minus the dropped A records before it
-    for (int bi = tid; bi < nb; bi += T) {
-      const int L = sLp[bi];
-      const int ol = bi + L - dropped_before(L);
-      sRefs[ol] = LSM_REF_FROM_B | (j0u + static_cast<uint32_t>(bi));
-      sOrdB[bi] = out0u + static_cast<uint32_t>(ol);
     }
     fence_proxy_async_smem();
     named_sync(1, T);
@@ -1115,11 +1093,10 @@ struct FusedSpec {
     for (int x = tid; x < nwc; x += T) {
       const int64_t w = w0 + x;
       const uint32_t bits = sCw[x];
+      sCw[x] = 0u;  // clean for the next tile
       if (w * 32 >= i0 && w * 32 + 32 <= i1) p.C[w] = bits;
       else if (bits) atomicOr(&p.C[w], bits);
     }
-    named_sync(1, T);  // every read of sCw is done before it is cleared
-    for (int x = tid; x < nwc + 1 && x < NC; x += T) sCw[x] = 0u;
     if (tid == 0) bulk_wait_read_all();  // the staging buffers are rewritten by the next tile
     named_sync(1, T);
   }
