@@ -27,8 +27,11 @@
  *
  * Parity of the exact Exp-Golomb bit pattern and of the payload word layout
  * is pinned only by hand-derived fixtures (the pages give the lengths, not
- * the bit strings); everything else is pinned by page examples, closed forms
- * and brute force in the tests.
+ * the bit strings); the bit packing of the rank2048 entries and the layout
+ * of the Elias-Fano sections are readings too (their contents, every R(p)
+ * and every sampled offset, are pinned, their bit positions are not);
+ * everything else is pinned by page examples, closed forms and brute force
+ * in the tests.
  */
 #include <stdint.h>
 #include <stdlib.h>
