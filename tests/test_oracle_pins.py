@@ -147,6 +147,17 @@ def test_mergesort_matches_stable_sort(n):
         assert passes == (0 if n <= 1 else int(np.ceil(np.log2(n))))
 
 
+def test_mergesort_brute_force_small():
+    # every sequence of length <= 6 over {0, 1, 2}: the oracle's keys and
+    # input positions against Python's stable sort of (key, position)
+    for n in range(7):
+        for seq in itertools.product(range(3), repeat=n):
+            keys = np.array(seq, dtype=np.int32)
+            out, pay, _ = oracle.merge_sort(keys, np.arange(n, dtype=np.uint32))
+            want = sorted(range(n), key=lambda t: seq[t])
+            assert pay.tolist() == want and out.tolist() == [seq[t] for t in want]
+
+
 def test_mergesort_pass_keeps_a_lone_tail_run():
     # n = 7 at width 4: one pair [0, 8) clipped to 7 merges runs [0,4) and
     # [4,7); at width 8 the whole array is a lone run and is copied
