@@ -91,6 +91,12 @@ def _load():
             _lib.oracle_ef_sizes.restype = None
             _lib.oracle_ef_build.argtypes = [P, I, U, P, P, P, P]
             _lib.oracle_ef_build.restype = I
+            _lib.oracle_leb128.argtypes = [U, P]
+            _lib.oracle_leb128.restype = U
+            _lib.oracle_bytefc_encode.argtypes = [P] * 10 + [P, I, U, P, P, P, P, P, I]
+            _lib.oracle_bytefc_encode.restype = I
+            _lib.oracle_bytefc_decode.argtypes = [P, U, I, U, P, U, P, P, U, P, P]
+            _lib.oracle_bytefc_decode.restype = I
             _lib.oracle_eg0_len.argtypes = [U]
             _lib.oracle_eg0_len.restype = U
             _lib.oracle_eg0_bits.argtypes = [U, P]
@@ -359,6 +365,59 @@ def fc_encode(keysA, valsA, tombA, keysB, valsB, tombB, refs, with_payload=True)
                                   nwords)
         assert t2 == total
     return FC(lcp, ctrl, rec, off, payload, int(total))
+
+
+def leb128(x):
+    """Textbook unsigned LEB128 bytes of x."""
+    out = np.zeros(10, dtype=np.uint8)
+    n = _load().oracle_leb128(int(x), _p(out))
+    return out[:n].tolist()
+
+
+def bytefc_encode(keysA, valsA, tombA, keysB, valsB, tombB, refs, W=0, with_payload=True):
+    """Sequential byte-profile FC encoder ([BP]). Returns an FC record whose
+    rec_bits / bit_off / payload / total_bits hold record bytes, byte offsets,
+    payload bytes (uint8) and the payload length in bytes."""
+    refs = _c(refs, np.uint32)
+    N = len(refs)
+    ka, koa = _c(keysA[0], np.uint8), _c(keysA[1], np.uint64)
+    kb, kob = _c(keysB[0], np.uint8), _c(keysB[1], np.uint64)
+    va, voa = _c(valsA[0], np.uint8), _c(valsA[1], np.uint64)
+    vb, vob = _c(valsB[0], np.uint8), _c(valsB[1], np.uint64)
+    ta, tb = _c(tombA, np.uint32), _c(tombB, np.uint32)
+    lcp = np.empty(N, dtype=np.uint32)
+    ctrl = np.empty(N, dtype=np.uint32)
+    rec = np.empty(N, dtype=np.uint32)
+    off = np.empty(N + 1, dtype=np.uint64)
+    lib = _load()
+    args = [_p(ka), _p(koa), _p(va), _p(voa), _p(ta), _p(kb), _p(kob), _p(vb), _p(vob), _p(tb),
+            _p(refs), N, int(W)]
+    total = lib.oracle_bytefc_encode(*args, _p(lcp), _p(ctrl), _p(rec), _p(off), None, 0)
+    if total < 0:
+        raise ValueError("byte FC: a field exceeds 32 bits or a record breaks the common width")
+    payload = None
+    if with_payload:
+        payload = np.zeros(max(int(total), 1), dtype=np.uint8)[:int(total)]
+        t2 = lib.oracle_bytefc_encode(*args, None, None, None, None,
+                                      _p(payload) if total else None, int(total))
+        assert t2 == total
+    return FC(lcp, ctrl, rec, off, payload, int(total))
+
+
+def bytefc_decode(payload, N, W, key_cap, val_cap):
+    """Independent byte-profile decoder. Returns (keys (arena, off), vals (arena, off), tombs)."""
+    payload = _c(payload, np.uint8)
+    key_ar = np.zeros(max(key_cap, 1), dtype=np.uint8)
+    val_ar = np.zeros(max(val_cap, 1), dtype=np.uint8)
+    key_off = np.empty(N + 1, dtype=np.uint64)
+    val_off = np.empty(N + 1, dtype=np.uint64)
+    tomb = np.zeros(max((N + 31) // 32, 1), dtype=np.uint32)
+    rc = _load().oracle_bytefc_decode(_p(payload) if len(payload) else None, len(payload), N,
+                                      int(W), _p(key_ar), key_cap, _p(key_off), _p(val_ar),
+                                      val_cap, _p(val_off), _p(tomb))
+    if rc != len(payload):
+        raise ValueError("byte FC decode failed (%d)" % rc)
+    return (key_ar, key_off), (val_ar, val_off), tomb
 
 
 class EF:

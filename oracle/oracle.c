@@ -16,6 +16,8 @@
  *         (ekmett.github.io/everett/collision-bitmap-and-rank-experiment.html)
  *   [GC]  "Everett: GPU construction experiment"
  *         (ekmett.github.io/everett/gpu-construction-experiment.html)
+ *   [BP]  "Everett: byte-profile GPU merge"
+ *         (ekmett.github.io/everett/byte-profile-gpu-merge.html)
  *
  * Conventions (readings of the pages where they are silent):
  *   - A is the older input, B the newer one. Equal keys put A first.
@@ -601,6 +603,171 @@ int64_t oracle_fc_encode(const uint8_t *keyA_ar, const uint64_t *keyA_off,
         k_prev = k;
     }
     if (bit_off) bit_off[N] = pos;
+    return (int64_t)pos;
+}
+
+
+/* ------------------------------------------------------------------------ */
+/* Byte-profile front compression. [BP] "Pipeline": the byte profile's      */
+/* records carry byte LEB128 counts, FC literals and optional-value tags;   */
+/* a common encoded value width is detected ("width seventeen means a      */
+/* one-byte presence tag and sixteen payload bytes"); blocks and sampling   */
+/* stay at 15 records; records are sized, scanned and emitted in order.     */
+/* The pages do not print the record grammar. Reading: the bit profile's    */
+/* record ([GC] control-argument equation and record-length formula) with   */
+/* bytes for bits and LEB128 for Exp-Golomb:                                */
+/*   p_i = byte LCP with the previous record's key (p_0 = 0), K_i = key    */
+/*   length in bytes; control b_i = 1 + p_i when i mod 15 = 0, else         */
+/*   K_{i-1} - p_i; record = LEB128(b_i) LEB128(K_i - p_i) key bytes        */
+/*   [p_i, K_i) then the value: tag byte 0 for a tombstone, else tag 1,     */
+/*   LEB128(value length) and the value bytes; with a common width W > 0    */
+/*   (every record present, every value W - 1 bytes) the length is left     */
+/*   out. LEB128 is the textbook unsigned form: seven bits per byte, low    */
+/*   group first, the top bit set on every byte but the last.               */
+/* Returns the payload bytes, or -1 (a field past 32 bits, a record that    */
+/* breaks the common width, or a payload buffer too small).                 */
+/* ------------------------------------------------------------------------ */
+static uint64_t leb_len(uint64_t x) {
+    uint64_t n = 1;
+    while (x >= 128) { x >>= 7; n++; }
+    return n;
+}
+
+uint64_t oracle_leb128(uint64_t x, uint8_t *out) {
+    uint64_t n = 0;
+    do {
+        uint8_t b = (uint8_t)(x & 0x7F);
+        x >>= 7;
+        if (x) b |= 0x80;
+        out[n++] = b;
+    } while (x);
+    return n;
+}
+
+int64_t oracle_bytefc_encode(const uint8_t *keyA_ar, const uint64_t *keyA_off,
+                             const uint8_t *valA_ar, const uint64_t *valA_off,
+                             const uint32_t *tombA, const uint8_t *keyB_ar,
+                             const uint64_t *keyB_off, const uint8_t *valB_ar,
+                             const uint64_t *valB_off, const uint32_t *tombB,
+                             const uint32_t *refs, int64_t N, uint64_t W, uint32_t *lcp,
+                             uint32_t *ctrl, uint32_t *rec_bytes, uint64_t *byte_off,
+                             uint8_t *payload, int64_t cap) {
+    oracle_bytes KA = {keyA_ar, keyA_off}, KB = {keyB_ar, keyB_off};
+    oracle_bytes VA = {valA_ar, valA_off}, VB = {valB_ar, valB_off};
+    uint64_t pos = 0, k_prev = 0;
+    int64_t i;
+    for (i = 0; i < N; i++) {
+        uint32_t r = refs[i], idx = r & 0x7FFFFFFFu;
+        const oracle_bytes *K = (r & REF_FROM_B) ? &KB : &KA;
+        const oracle_bytes *V = (r & REF_FROM_B) ? &VB : &VA;
+        const uint32_t *T = (r & REF_FROM_B) ? tombB : tombA;
+        uint64_t k = key_len(K, idx), l = 0, c, v, L, q, start = pos;
+        int tomb = T ? (int)((T[idx / 32] >> (idx % 32)) & 1u) : 0;
+        if (i > 0) {
+            uint32_t pr = refs[i - 1], pidx = pr & 0x7FFFFFFFu;
+            const oracle_bytes *PK = (pr & REF_FROM_B) ? &KB : &KA;
+            uint64_t kmin = key_len(PK, pidx);
+            if (k < kmin) kmin = k;
+            while (l < kmin && PK->arena[PK->off[pidx] + l] == K->arena[K->off[idx] + l]) l++;
+        }
+        c = (i % 15 == 0) ? 1 + l : k_prev - l;
+        if (tomb) {
+            if (W) return -1;
+            v = 1;
+        } else {
+            uint64_t vb = key_len(V, idx);
+            if (W && vb + 1 != W) return -1;
+            v = W ? W : 1 + leb_len(vb) + vb;
+        }
+        L = leb_len(c) + leb_len(k - l) + (k - l) + v;
+        if (l > 0xFFFFFFFFu || c > 0xFFFFFFFFu || L > 0xFFFFFFFFu) return -1;
+        if (lcp) lcp[i] = (uint32_t)l;
+        if (ctrl) ctrl[i] = (uint32_t)c;
+        if (rec_bytes) rec_bytes[i] = (uint32_t)L;
+        if (byte_off) byte_off[i] = start;
+        if (payload) {
+            if ((uint64_t)cap < start + L) return -1;
+            pos += oracle_leb128(c, payload + pos);
+            pos += oracle_leb128(k - l, payload + pos);
+            for (q = l; q < k; q++) payload[pos++] = K->arena[K->off[idx] + q];
+            if (tomb) payload[pos++] = 0;
+            else {
+                uint64_t vb = key_len(V, idx);
+                payload[pos++] = 1;
+                if (!W) pos += oracle_leb128(vb, payload + pos);
+                for (q = 0; q < vb; q++) payload[pos++] = V->arena[V->off[idx] + q];
+            }
+            if (pos != start + L) return -1; /* the length formula and the writer agree */
+        } else {
+            pos += L;
+        }
+        k_prev = k;
+    }
+    if (byte_off) byte_off[N] = pos;
+    return (int64_t)pos;
+}
+
+/* Independent byte-profile decoder: reads the records back in the same     */
+/* grammar. Returns the bytes consumed or a negative code on a malformed    */
+/* payload. Output capacities as oracle_fc_decode's.                        */
+static int get_leb(const uint8_t *payload, uint64_t total, uint64_t *pos, uint64_t *x) {
+    uint64_t v = 0;
+    int shift = 0;
+    for (;;) {
+        uint8_t b;
+        if (*pos >= total || shift > 63) return -1;
+        b = payload[(*pos)++];
+        v |= (uint64_t)(b & 0x7F) << shift;
+        shift += 7;
+        if (!(b & 0x80)) break;
+    }
+    *x = v;
+    return 0;
+}
+
+int64_t oracle_bytefc_decode(const uint8_t *payload, uint64_t total, int64_t N, uint64_t W,
+                             uint8_t *key_ar, uint64_t key_cap, uint64_t *key_off,
+                             uint8_t *val_ar, uint64_t val_cap, uint64_t *val_off,
+                             uint32_t *tomb) {
+    uint64_t pos = 0, kpos = 0, vpos = 0, prev_len = 0;
+    int64_t i;
+    key_off[0] = 0;
+    val_off[0] = 0;
+    for (i = 0; i < N; i++) {
+        uint64_t c, s, l, t, vb;
+        uint8_t tag;
+        if (get_leb(payload, total, &pos, &c) || get_leb(payload, total, &pos, &s)) return -1;
+        if (i % 15 == 0) {
+            if (c < 1) return -2;
+            l = c - 1;
+        } else {
+            if (c > prev_len) return -2;
+            l = prev_len - c;
+        }
+        if (i == 0 && l) return -2;
+        if (l > prev_len || kpos + l + s > key_cap || pos + s > total) return -3;
+        for (t = 0; t < l; t++) key_ar[kpos + t] = key_ar[key_off[i - (i > 0)] + t];
+        for (t = 0; t < s; t++) key_ar[kpos + l + t] = payload[pos + t];
+        pos += s;
+        kpos += l + s;
+        key_off[i + 1] = kpos;
+        prev_len = l + s;
+        if (pos >= total) return -4;
+        tag = payload[pos++];
+        if (tag == 0) {
+            tomb[i / 32] |= 1u << (i % 32);
+        } else if (tag == 1) {
+            if (W) vb = W - 1;
+            else if (get_leb(payload, total, &pos, &vb)) return -4;
+            if (vpos + vb > val_cap || pos + vb > total) return -4;
+            for (t = 0; t < vb; t++) val_ar[vpos + t] = payload[pos + t];
+            pos += vb;
+            vpos += vb;
+        } else {
+            return -5;
+        }
+        val_off[i + 1] = vpos;
+    }
     return (int64_t)pos;
 }
 

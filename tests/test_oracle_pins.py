@@ -565,3 +565,94 @@ def test_ef_over_an_fc_scan():
     r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
     fc = _encode_strings(s, r.refs)
     _check_ef(fc.bit_off, r.count)
+
+
+# ---------------------------------------------------------------------------
+# Byte-profile front compression ([BP] "Pipeline")
+# ---------------------------------------------------------------------------
+def test_leb128_standard_values():
+    # unsigned LEB128 as the DWARF standard defines and tabulates it
+    table = {0: [0x00], 1: [0x01], 2: [0x02], 127: [0x7F], 128: [0x80, 0x01],
+             129: [0x81, 0x01], 130: [0x82, 0x01], 12857: [0xB9, 0x64],
+             624485: [0xE5, 0x8E, 0x26], (1 << 32) - 1: [0xFF, 0xFF, 0xFF, 0xFF, 0x0F]}
+    for x, want in table.items():
+        assert oracle.leb128(x) == want
+    # every x decodes back (seven bits per byte, low group first) and only
+    # the last byte lacks the continuation bit
+    for x in list(range(1 << 15)) + [(1 << k) + d for k in range(15, 63) for d in (-1, 0, 1)]:
+        b = oracle.leb128(x)
+        assert sum((v & 0x7F) << (7 * t) for t, v in enumerate(b)) == x
+        assert all(v & 0x80 for v in b[:-1]) and not b[-1] & 0x80
+        assert len(b) == max(1, (x.bit_length() + 6) // 7)
+
+
+def test_bytefc_hand_derived(golden):
+    g = golden("bytefc_hand_derived.txt")
+    s = synth.strings_from_lists([b"ab", b"ac"], [], [None, b"\xff"], [])
+    refs = np.array([0, 1], np.uint32)
+    fc = oracle.bytefc_encode((s.A.key_arena, s.A.key_off), (s.A.val_arena, s.A.val_off),
+                              s.A.tomb, (s.B.key_arena, s.B.key_off),
+                              (s.B.val_arena, s.B.val_off), s.B.tomb, refs)
+    assert fc.lcp.tolist() == g["two_keys_lcp"] and fc.ctrl.tolist() == g["two_keys_ctrl"]
+    assert fc.rec_bits.tolist() == g["two_keys_rec"]
+    assert fc.payload.tolist() == g["two_keys_payload"]
+    s = synth.strings_from_lists([b"A"], [], [bytes(range(16))], [])
+    fc = oracle.bytefc_encode((s.A.key_arena, s.A.key_off), (s.A.val_arena, s.A.val_off),
+                              s.A.tomb, (s.B.key_arena, s.B.key_off),
+                              (s.B.val_arena, s.B.val_off), s.B.tomb,
+                              np.array([0], np.uint32), W=17)
+    assert fc.payload.tolist() == g["w17_payload"]
+
+
+def _byte_lcp(x: bytes, y: bytes) -> int:
+    n = 0
+    while n < min(len(x), len(y)) and x[n] == y[n]:
+        n += 1
+    return n
+
+
+def _check_bytefc_roundtrip(s, W=0):
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    N = r.count
+    fc = oracle.bytefc_encode((s.A.key_arena, s.A.key_off), (s.A.val_arena, s.A.val_off),
+                              s.A.tomb if len(s.A.tomb) else None,
+                              (s.B.key_arena, s.B.key_off), (s.B.val_arena, s.B.val_off),
+                              s.B.tomb if len(s.B.tomb) else None, r.refs, W=W)
+    keys = [s.B.key(x & 0x7FFFFFFF) if x >> 31 else s.A.key(x) for x in r.refs]
+    vals = [s.B.value(x & 0x7FFFFFFF) if x >> 31 else s.A.value(x) for x in r.refs]
+    assert int(fc.bit_off[N]) == fc.total_bits == int(fc.rec_bits.astype(np.int64).sum())
+    for i in range(N):
+        p = 0 if i == 0 else _byte_lcp(keys[i - 1], keys[i])
+        assert fc.lcp[i] == p
+        assert fc.ctrl[i] == (1 + p if i % 15 == 0 else len(keys[i - 1]) - p)
+        v = 1 if vals[i] is None else (W if W else 1 + len(oracle.leb128(len(vals[i]))) + len(vals[i]))
+        assert fc.rec_bits[i] == (len(oracle.leb128(int(fc.ctrl[i]))) +
+                                  len(oracle.leb128(len(keys[i]) - p)) + len(keys[i]) - p + v)
+    key_cap = sum(len(k) for k in keys)
+    val_cap = sum(len(v) for v in vals if v is not None)
+    (ka, ko), (va, vo), tomb = oracle.bytefc_decode(fc.payload, N, W, key_cap, val_cap)
+    for i in range(N):
+        assert bytes(ka[int(ko[i]):int(ko[i + 1])]) == keys[i]
+        assert bool((int(tomb[i // 32]) >> (i % 32)) & 1) == (vals[i] is None)
+        if vals[i] is not None:
+            assert bytes(va[int(vo[i]):int(vo[i + 1])]) == vals[i]
+    return fc
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_bytefc_roundtrip_prefix_tree(seed):
+    _check_bytefc_roundtrip(synth.strings(seed=seed, count=2000))
+
+
+def test_bytefc_roundtrip_edges_and_common_width():
+    _check_bytefc_roundtrip(synth.strings_from_lists(
+        [b"", b"a", b"ab", b"abc" * 60, b"b"], [b"a", b"abd", b"c" * 300],
+        [None, b"", b"x" * 200, b"y", None], [b"1", None, b""]))
+    rng = np.random.default_rng(4)
+    keysA = sorted({bytes(rng.integers(0, 256, size=int(rng.integers(1, 20)), dtype=np.uint8))
+                    for _ in range(300)})
+    keysB = sorted(set(keysA[::3]) | {bytes([200 + t % 50]) * (t % 7 + 1) for t in range(40)})
+    valsA = [bytes(rng.integers(0, 256, size=16, dtype=np.uint8)) for _ in keysA]
+    valsB = [bytes(rng.integers(0, 256, size=16, dtype=np.uint8)) for _ in keysB]
+    s = synth.strings_from_lists(keysA, keysB, valsA, valsB)
+    _check_bytefc_roundtrip(s, W=17)
