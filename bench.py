@@ -779,6 +779,29 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
                                "frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": per,
                                "gpu_launches_per_step": 7,
                                "l2": "flushed (256 MiB write) before every step"}
+    # The byte profile in place of the bit profile: the same step with the
+    # byte-FC lengths scan and emit.
+    lcpb = torch.empty(N, dtype=torch.uint32, device=dev)
+    ctrlb = torch.empty(N, dtype=torch.uint32, device=dev)
+    recb = torch.empty(N, dtype=torch.uint32, device=dev)
+    offb = torch.empty(N + 1, dtype=torch.uint64, device=dev)
+    lsm.bytefc_lengths_scan(fc, refs, N, 0, lcpb, ctrlb, recb, offb, w4)
+    total_bytes = int(offb[N:].cpu().numpy()[0])
+    payb = torch.empty(max(total_bytes, 16), dtype=torch.uint8, device=dev)
+    stages_b = stages[:3] + [
+        ("bytefc_lengths_scan", lambda: lsm.bytefc_lengths_scan(fc, refs, N, 0, lcpb, ctrlb, recb,
+                                                                offb, w4)),
+        ("bytefc_emit", lambda: lsm.bytefc_emit(fc, refs, N, lcpb, ctrlb, offb, total_bytes, 0,
+                                                payb))]
+    ms_b, per_b = time_pipeline(torch, stages_b, steps, flush)
+    alg_b = alg - 4 * nwords + total_bytes
+    out["strings_fc_4M_4M"]["byte_profile"] = {
+        "ms_per_step": ms_b, "payload_bytes": total_bytes,
+        "gelem_s": (m + n) / (ms_b * 1e-3) / 1e9, "algorithmic_bytes": alg_b,
+        "gbs": alg_b / (ms_b * 1e-3) / 1e9, "frac": alg_b / (ms_b * 1e-3) / 1e9 / peak,
+        "kernel_ms": {k: per_b[k] for k in ("bytefc_lengths_scan", "bytefc_emit")},
+        "gpu_launches_per_step": 8}
+    del lcpb, ctrlb, recb, offb, payb
     # The same step followed by the Elias-Fano navigation over bit_off.
     n_ef, L, nl, nh, G = lsm.ef_sizes(N, total_bits)
     lows = torch.empty(max(nl, 1), dtype=torch.uint64, device=dev)

@@ -395,6 +395,41 @@ LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
                         const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                         uint32_t *payload, int64_t nwords, void *stream);
 
+/* ---- f4: byte-profile front compression ---------------------------------- */
+/* [BP] "Pipeline": the byte profile's records carry byte LEB128 counts, FC
+ * literals and optional-value tags, with 15-record blocks, and a common
+ * encoded value width leaves the value length out ("width seventeen means a
+ * one-byte presence tag and sixteen payload bytes"). The pages do not print
+ * the record grammar; this library reads it as the bit profile's record
+ * ([GC] control-argument equation) in bytes, with LEB128 in place of EG0:
+ *   p_i = byte LCP with record i-1's key (p_0 = 0), K_i = key length;
+ *   b_i = 1 + p_i when i mod 15 = 0, else K_{i-1} - p_i;
+ *   record = LEB128(b_i) LEB128(K_i - p_i) key bytes [p_i, K_i), then tag
+ *   byte 0 for a tombstone, or tag 1, LEB128(value length) and the value
+ *   bytes; under a common width W > 0 every record must be present with a
+ *   (W - 1)-byte value and the length is left out.
+ * LEB128 is unsigned: seven bits per byte, low group first, the top bit set
+ * on every byte but the last. Records follow each other with no padding.
+ * Inputs as lsm_fc_lengths_scan's (the prefix tables are not used).
+ * lsm_bytefc_lengths_scan writes lcp[i] = p_i, ctrl[i] = b_i, rec_bytes[i]
+ * (the record's bytes) and byte_off[0..N] (exclusive scan, byte_off[N] =
+ * the payload's bytes); rec_bytes and byte_off 16-byte aligned; ws sized by
+ * LSM_OP_FC_LENGTHS_SCAN for N. A tombstone or a value of another length
+ * under W > 0 records LSM_ERR_ARG, a record past 2^32 bytes
+ * LSM_ERR_OVERFLOW, in the device status word. */
+LSM_API int lsm_bytefc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
+                                    uint64_t W, uint32_t *lcp, uint32_t *ctrl,
+                                    uint32_t *rec_bytes, uint64_t *byte_off, void *ws,
+                                    size_t ws_bytes, void *stream);
+
+/* Writes the payload: record i's bytes at [byte_off[i], byte_off[i+1]) of
+ * payload (device, nbytes >= byte_off[N]); bytes past byte_off[N] are not
+ * written. lcp, ctrl, byte_off: lsm_bytefc_lengths_scan's outputs for the
+ * same inputs and W. One thread per record. */
+LSM_API int lsm_bytefc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N, uint64_t W,
+                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
+                            uint8_t *payload, int64_t nbytes, void *stream);
+
 /* ---- f2: Elias-Fano navigation over the record offsets ------------------- */
 /* [GC] "GPU construction experiment": physical offsets sampled at ordinals
  * 0, 15, 30, ... plus EOF; with a common encoded value width w every entry

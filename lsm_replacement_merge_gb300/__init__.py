@@ -101,6 +101,9 @@ def lib():
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
                 "lsm_fc_emit": ([P, P, I, P, P, P, P, I, P], ctypes.c_int),
                 "lsm_ef_sizes": ([I, ctypes.c_uint64, P], ctypes.c_int),
+                "lsm_bytefc_lengths_scan": ([P, P, I, ctypes.c_uint64, P, P, P, P, P, S, P],
+                                            ctypes.c_int),
+                "lsm_bytefc_emit": ([P, P, I, ctypes.c_uint64, P, P, P, P, I, P], ctypes.c_int),
                 "lsm_fc_ef_build": ([P, I, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, P, P],
                                     ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
@@ -573,6 +576,41 @@ def fc_emit(fc: FcInput, refs, N: int, lcp, ctrl, bit_off, nwords: int, payload=
            lib().lsm_fc_emit(ctypes.byref(c), _ptr(refs) if N else None, N,
                              _ptr(lcp) if N else None, _ptr(ctrl) if N else None, _ptr(bit_off),
                              _ptr(payload) if nwords else None, nwords, _stream(stream)))
+    return payload
+
+
+# ---------------------------------------------------------------------------
+# f4: byte-profile front compression
+# ---------------------------------------------------------------------------
+def bytefc_lengths_scan(fc: FcInput, refs, N: int, W: int = 0, lcp=None, ctrl=None,
+                        rec_bytes=None, byte_off=None, ws=None, stream=None):
+    dev = refs.device
+    if lcp is None:
+        lcp = _empty(max(N, 1), torch.uint32, dev)
+    if ctrl is None:
+        ctrl = _empty(max(N, 1), torch.uint32, dev)
+    if rec_bytes is None:
+        rec_bytes = _empty(max(N, 1), torch.uint32, dev)
+    if byte_off is None:
+        byte_off = _empty(N + 1, torch.uint64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_FC_LENGTHS_SCAN, N, 0, dev)
+    c = fc._c()
+    _check("lsm_bytefc_lengths_scan",
+           lib().lsm_bytefc_lengths_scan(ctypes.byref(c), _ptr(refs), N, W, _ptr(lcp), _ptr(ctrl),
+                                         _ptr(rec_bytes), _ptr(byte_off), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return lcp, ctrl, rec_bytes, byte_off
+
+
+def bytefc_emit(fc: FcInput, refs, N: int, lcp, ctrl, byte_off, nbytes: int, W: int = 0,
+                payload=None, stream=None):
+    if payload is None:
+        payload = _empty(max(nbytes, 1), torch.uint8, refs.device)
+    c = fc._c()
+    _check("lsm_bytefc_emit",
+           lib().lsm_bytefc_emit(ctypes.byref(c), _ptr(refs), N, W, _ptr(lcp), _ptr(ctrl),
+                                 _ptr(byte_off), _ptr(payload), nbytes, _stream(stream)))
     return payload
 
 

@@ -491,6 +491,31 @@ static int check_fc_input(const lsm_fc_input *in) {
   return LSM_OK;
 }
 
+LSM_API int lsm_bytefc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
+                                    uint64_t W, uint32_t *lcp, uint32_t *ctrl,
+                                    uint32_t *rec_bytes, uint64_t *byte_off, void *ws,
+                                    size_t ws_bytes, void *stream) {
+  if (int r = check_fc_input(in)) return r;
+  if (N < 0 || !byte_off || (N && (!refs || !lcp || !ctrl || !rec_bytes))) return LSM_ERR_ARG;
+  if (N > kMax31 || N > in->m + in->n) return LSM_ERR_OVERFLOW;
+  if (!aligned16(rec_bytes) || !aligned16(byte_off)) return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_FC_LENGTHS_SCAN, N, 0, ws, ws_bytes)) return r;
+  return cuda_status(launch_bytefc_lengths_scan(*in, refs, N, W, lcp, ctrl, rec_bytes, byte_off,
+                                                ws, status_ptr(),
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_bytefc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N, uint64_t W,
+                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
+                            uint8_t *payload, int64_t nbytes, void *stream) {
+  if (int r = check_fc_input(in)) return r;
+  if (N < 0 || nbytes < 0 || (N && (!refs || !lcp || !ctrl || !byte_off || !payload)))
+    return LSM_ERR_ARG;
+  if (N > kMax31 || N > in->m + in->n) return LSM_ERR_OVERFLOW;
+  return cuda_status(launch_bytefc_emit(*in, refs, N, W, lcp, ctrl, byte_off, payload, nbytes,
+                                        status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
 LSM_API int lsm_fc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
                                 uint32_t *lcp, uint32_t *ctrl, uint32_t *rec_bits,
                                 uint64_t *bit_off, void *ws, size_t ws_bytes, void *stream) {

@@ -1,0 +1,227 @@
+// bytefc.cu -- byte-profile front compression of the merged string records.
+//
+// "Everett: byte-profile GPU merge", "Pipeline": the byte profile's records
+// carry byte LEB128 counts, FC literals and optional-value tags, with
+// 15-record blocks; a common encoded value width drops the value length
+// ("width seventeen means a one-byte presence tag and sixteen payload
+// bytes"); records are sized, scanned and emitted in order. Record i (the
+// bit profile's grammar of "Everett: GPU construction experiment" with
+// bytes for bits and LEB128 for Exp-Golomb):
+//   p_i = byte LCP with record i-1's key (p_0 = 0), K_i = key bytes,
+//   b_i = 1 + p_i when i mod 15 = 0, else K_{i-1} - p_i;
+//   LEB128(b_i) LEB128(K_i - p_i) key bytes [p_i, K_i) then tag 0 for a
+//   tombstone, else tag 1, LEB128(value length) (left out under a common
+//   width W) and the value bytes.
+//
+//   bytefc_lengths_kernel  one tile of 1024 records per CTA, four records
+//                          per thread: key extents, byte LCP with the
+//                          predecessor from aligned 8-byte loads, control,
+//                          record length; the tile's total for the scan
+//   (scan)                 the FC pipeline's one-CTA tile scan and offsets
+//                          pass turn the lengths into byte offsets
+//   bytefc_emit_kernel     one thread per record writes its bytes at its
+//                          offset; records never share a byte, so no two
+//                          threads write the same address
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lsm {
+
+namespace {
+
+constexpr int kBfThreads = 256;
+constexpr int kBfItems = 4;
+constexpr int kBfTile = kBfThreads * kBfItems;
+
+struct BSource {
+  lsm_bytes key, val;
+  const uint32_t *tomb;
+};
+
+__device__ __forceinline__ const BSource &bpick(const BSource &a, const BSource &b, uint32_t ref) {
+  return (ref & LSM_REF_FROM_B) ? b : a;
+}
+
+// `need` (1..8) bytes of an 8-byte aligned arena from byte offset o, byte t
+// of the window in bits [8t, 8t+8) of the result (little-endian words); the
+// second aligned word is read only when the window reaches into it.
+__device__ __forceinline__ uint64_t bytes8_at(const uint8_t *arena, uint64_t o, int need) {
+  const uint64_t *w = reinterpret_cast<const uint64_t *>(arena);
+  const uint64_t t = o >> 3;
+  const int sh = static_cast<int>(o & 7);
+  uint64_t v = __ldg(w + t) >> (8 * sh);
+  if (sh + need > 8) v |= __ldg(w + t + 1) << (64 - 8 * sh);
+  return v;
+}
+
+// Byte LCP of two byte strings, clamped to the shorter one.
+__device__ __forceinline__ uint64_t byte_lcp(const uint8_t *aa, uint64_t ao, uint64_t alen,
+                                             const uint8_t *ba, uint64_t bo, uint64_t blen) {
+  const uint64_t L = alen < blen ? alen : blen;
+  for (uint64_t t = 0; t < L; t += 8) {
+    const int need = L - t < 8 ? static_cast<int>(L - t) : 8;
+    uint64_t x = bytes8_at(aa, ao + t, need) ^ bytes8_at(ba, bo + t, need);
+    if (need < 8) x &= (1ull << (8 * need)) - 1;
+    if (x) return t + (__ffsll(static_cast<long long>(x)) - 1) / 8;
+  }
+  return L;
+}
+
+__device__ __forceinline__ uint32_t leb_len(uint64_t x) {
+  uint32_t n = 1;
+  while (x >= 128) {
+    x >>= 7;
+    ++n;
+  }
+  return n;
+}
+
+__device__ __forceinline__ uint64_t put_leb(uint8_t *out, uint64_t pos, uint64_t x) {
+  do {
+    uint8_t b = static_cast<uint8_t>(x & 0x7F);
+    x >>= 7;
+    if (x) b |= 0x80;
+    out[pos++] = b;
+  } while (x);
+  return pos;
+}
+
+__device__ __forceinline__ bool is_tomb(const BSource &src, uint32_t idx) {
+  return src.tomb && ((__ldg(src.tomb + (idx >> 5)) >> (idx & 31)) & 1u);
+}
+
+__global__ void __launch_bounds__(kBfThreads) bytefc_lengths_kernel(
+    BSource sa, BSource sb, const uint32_t *__restrict__ refs, int64_t N, uint64_t W,
+    uint32_t *__restrict__ lcp, uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec,
+    uint64_t *__restrict__ tile_sum, int32_t *status) {
+  pdl_begin();
+  __shared__ uint64_t scratch[kBfThreads / 32 + 1];
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kBfTile + int64_t(threadIdx.x) * kBfItems;
+  uint64_t local = 0;
+#pragma unroll
+  for (int q = 0; q < kBfItems; ++q) {
+    const int64_t i = first + q;
+    if (i >= N) break;
+    const uint32_t r = __ldg(refs + i), idx = r & 0x7FFFFFFFu;
+    const BSource &src = bpick(sa, sb, r);
+    const uint64_t ks = __ldg(src.key.off + idx), K = __ldg(src.key.off + idx + 1) - ks;
+    uint64_t p = 0, Kp = 0;
+    if (i > 0) {
+      const uint32_t pr = __ldg(refs + i - 1), pidx = pr & 0x7FFFFFFFu;
+      const BSource &ps = bpick(sa, sb, pr);
+      const uint64_t pks = __ldg(ps.key.off + pidx);
+      Kp = __ldg(ps.key.off + pidx + 1) - pks;
+      p = byte_lcp(ps.key.arena, pks, Kp, src.key.arena, ks, K);
+    }
+    const uint64_t b = (i % 15 == 0) ? 1 + p : Kp - p;
+    uint64_t v;
+    if (is_tomb(src, idx)) {
+      v = 1;
+      if (W) report(status, LSM_ERR_ARG);  // a tombstone breaks the common width
+    } else {
+      const uint64_t vb = __ldg(src.val.off + idx + 1) - __ldg(src.val.off + idx);
+      if (W && vb + 1 != W) report(status, LSM_ERR_ARG);
+      v = W ? W : 1 + leb_len(vb) + vb;
+    }
+    const uint64_t L = leb_len(b) + leb_len(K - p) + (K - p) + v;
+    if (L > 0xFFFFFFFFull || b > 0xFFFFFFFFull) report(status, LSM_ERR_OVERFLOW);
+    lcp[i] = static_cast<uint32_t>(p);
+    ctrl[i] = static_cast<uint32_t>(b);
+    rec[i] = static_cast<uint32_t>(L);
+    local += static_cast<uint32_t>(L);
+  }
+  const uint64_t total = block_sum<kBfThreads, uint64_t>(local, scratch);
+  if (threadIdx.x == 0) tile_sum[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(256) bytefc_emit_kernel(
+    BSource sa, BSource sb, const uint32_t *__restrict__ refs, int64_t N, uint64_t W,
+    const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
+    const uint64_t *__restrict__ off, uint8_t *__restrict__ payload, int64_t nbytes,
+    int32_t *status) {
+  pdl_begin();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
+    const uint32_t r = __ldg(refs + i), idx = r & 0x7FFFFFFFu;
+    const BSource &src = bpick(sa, sb, r);
+    const uint64_t ks = __ldg(src.key.off + idx), K = __ldg(src.key.off + idx + 1) - ks;
+    const uint64_t p = __ldg(lcp + i), b = __ldg(ctrl + i);
+    uint64_t pos = __ldg(off + i);
+    const uint64_t end = __ldg(off + i + 1);
+    // lengths that do not match this record (not the lengths pass's output)
+    // are reported, and nothing is written past the record's own end
+    if (end > static_cast<uint64_t>(nbytes) || p > K || pos + leb_len(b) + leb_len(K - p) > end) {
+      report(status, LSM_ERR_ARG);
+      continue;
+    }
+    pos = put_leb(payload, pos, b);
+    pos = put_leb(payload, pos, K - p);
+    for (uint64_t t = p; t < K && pos < end; ++t) payload[pos++] = __ldg(src.key.arena + ks + t);
+    if (pos >= end) {  // no room left for the tag byte
+      report(status, LSM_ERR_ARG);
+      continue;
+    }
+    if (is_tomb(src, idx)) {
+      payload[pos++] = 0;
+    } else {
+      const uint64_t vs = __ldg(src.val.off + idx), vb = __ldg(src.val.off + idx + 1) - vs;
+      payload[pos++] = 1;
+      if (!W) {
+        if (pos + leb_len(vb) > end) {
+          report(status, LSM_ERR_ARG);
+          continue;
+        }
+        pos = put_leb(payload, pos, vb);
+      }
+      for (uint64_t t = 0; t < vb && pos < end; ++t) payload[pos++] = __ldg(src.val.arena + vs + t);
+    }
+    if (pos != end) report(status, LSM_ERR_ARG);
+  }
+}
+
+BSource bsource(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb) {
+  return BSource{key, val, tomb};
+}
+
+}  // namespace
+
+cudaError_t launch_bytefc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
+                                       uint64_t W, uint32_t *lcp, uint32_t *ctrl,
+                                       uint32_t *rec_bytes, uint64_t *byte_off, void *ws,
+                                       int32_t *status, cudaStream_t s) {
+  static_assert(kBfTile == 1024, "the offsets pass scans tiles of 1024 records");
+  if (fc_tile_records() != kBfTile) return cudaErrorInvalidValue;
+  uint64_t *tile_sum = static_cast<uint64_t *>(ws);
+  const int64_t tiles = (N + kBfTile - 1) / kBfTile;
+  profile_before(s);
+  cudaError_t err = launch_kernel(false, bytefc_lengths_kernel,
+                                  static_cast<unsigned>(tiles > 0 ? tiles : 1), kBfThreads, 0, s,
+                                  bsource(in.keyA, in.valA, in.tombA),
+                                  bsource(in.keyB, in.valB, in.tombB), refs, N, W, lcp, ctrl,
+                                  rec_bytes, tile_sum, status);
+  if (err == cudaSuccess) err = launch_fc_offsets(rec_bytes, N, tile_sum, byte_off, s);
+  profile_after(s);
+  return err;
+}
+
+cudaError_t launch_bytefc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N, uint64_t W,
+                               const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
+                               uint8_t *payload, int64_t nbytes, int32_t *status, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  int64_t blocks = (N + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  if (blocks > cap && cap > 0) blocks = cap;
+  profile_before(s);
+  const cudaError_t err = launch_kernel(false, bytefc_emit_kernel, static_cast<unsigned>(blocks),
+                                        256, 0, s, bsource(in.keyA, in.valA, in.tombA),
+                                        bsource(in.keyB, in.valB, in.tombB), refs, N, W, lcp, ctrl,
+                                        byte_off, payload, nbytes, status);
+  profile_after(s);
+  return err;
+}
+
+}  // namespace lsm

@@ -791,6 +791,19 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
   return err;
 }
 
+int64_t fc_tile_records() { return kFcTile; }
+
+cudaError_t launch_fc_offsets(const uint32_t *rec, int64_t N, uint64_t *tile_sum, uint64_t *off,
+                              cudaStream_t s) {
+  if (N <= 0) return cudaSuccess;
+  const int64_t tiles = fc_scan_tiles(N);
+  cudaError_t err = launch_kernel(true, fc_tile_scan_kernel, 1u, kScanThreads, 0, s, tile_sum, tiles);
+  if (err == cudaSuccess)
+    err = launch_kernel(true, fc_offsets_kernel, static_cast<unsigned>(tiles), kFcThreads, 0, s,
+                        rec, N, static_cast<const uint64_t *>(tile_sum), tiles, off);
+  return err;
+}
+
 cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                            uint32_t *payload, int64_t nwords, int32_t * /*status*/, cudaStream_t s) {

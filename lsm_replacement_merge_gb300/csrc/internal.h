@@ -109,6 +109,22 @@ cudaError_t launch_fc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t
                            const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *bit_off,
                            uint32_t *payload, int64_t nwords, int32_t *status, cudaStream_t s);
 
+// Offsets from per-record lengths: tile_sum[t] holds the total of records
+// [t T, (t+1) T) (T = fc_tile_records()) on entry; the one-CTA tile scan and
+// the offsets pass write off[0..N] (off[N] = the total).
+int64_t fc_tile_records();
+cudaError_t launch_fc_offsets(const uint32_t *rec, int64_t N, uint64_t *tile_sum, uint64_t *off,
+                              cudaStream_t s);
+
+// --- bytefc.cu ---
+cudaError_t launch_bytefc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
+                                       uint64_t W, uint32_t *lcp, uint32_t *ctrl,
+                                       uint32_t *rec_bytes, uint64_t *byte_off, void *ws,
+                                       int32_t *status, cudaStream_t s);
+cudaError_t launch_bytefc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N, uint64_t W,
+                               const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
+                               uint8_t *payload, int64_t nbytes, int32_t *status, cudaStream_t s);
+
 // --- scatter.cu ---
 cudaError_t launch_direct_scatter(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                   const uint32_t *C, const uint32_t *dir, const uint32_t *lb_B,

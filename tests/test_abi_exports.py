@@ -130,6 +130,20 @@ def test_fused_host_checks_without_gpu(lib):
     assert lib.lsm_replacement_merge_fused(*bad) == 6
 
 
+def test_bytefc_host_checks_without_gpu(lib):
+    I, P, S, U = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint64
+    fc = _FcInput(_Bytes(P(64), P(128)), _Bytes(P(64), P(128)), None, I(10),
+                  _Bytes(P(64), P(128)), _Bytes(P(64), P(128)), None, I(10), None, None)
+    assert lib.lsm_bytefc_lengths_scan(ctypes.byref(fc), P(16), I(-1), U(0), P(16), P(16),
+                                       P(16), P(16), P(16), S(1 << 20), None) == 1
+    assert lib.lsm_bytefc_lengths_scan(ctypes.byref(fc), P(16), I(21), U(0), P(16), P(16),
+                                       P(16), P(16), P(16), S(1 << 20), None) == 3
+    assert lib.lsm_bytefc_lengths_scan(ctypes.byref(fc), P(16), I(5), U(0), P(16), P(16),
+                                       P(20), P(16), P(16), S(1 << 20), None) == 7
+    assert lib.lsm_bytefc_emit(ctypes.byref(fc), P(16), I(5), U(0), P(16), P(16), P(16), None,
+                               I(100), None) == 1
+
+
 def test_merge_sort_host_checks_without_gpu(lib):
     I, P, S = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
     sizes = {}
