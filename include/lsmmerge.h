@@ -228,7 +228,10 @@ LSM_API int lsm_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t 
  *     LSM_ERR_OVERFLOW before anything is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept for the life of the
+ *     process: after cudaDeviceReset (or anything else that destroys the
+ *     device's primary context) it is stale, so do not call this entry point
+ *     on that device again after a reset.
  *   - Every call on a device shares the one array: calls that may overlap on
  *     the GPU (different streams, or different host threads) race and must be
  *     ordered by the caller. Each call rewrites every entry it reads, so the

@@ -24,7 +24,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "liblsmmerge.so")
 
 LSM_OK = 0
+LSM_ERR_ARG = 1
+LSM_ERR_DTYPE = 2
+LSM_ERR_OVERFLOW = 3
+LSM_ERR_CUDA = 4
 LSM_ERR_TIMEOUT = 5
+LSM_ERR_WORKSPACE = 6
+LSM_ERR_ALIGN = 7
 LSM_KEY_I32 = 1
 LSM_KEY_U64 = 2
 LSM_OP_MERGE_STABLE = 1

@@ -285,6 +285,47 @@ def test_replacement_str_vs_chronological_map(case):
     assert r.count == len(r.refs)
 
 
+def _side_keys(side):
+    off = side.key_off.astype(np.int64)
+    return [side.key_arena[off[t]:off[t + 1]].tobytes() for t in range(len(off) - 1)]
+
+
+def _str_bitmap_cases():
+    for ka, kb in _str_cases():
+        yield synth.strings_from_lists(ka, kb)
+    # stems: B keys that extend, shorten or equal A keys by one byte
+    yield synth.strings_from_lists(
+        [b"ab", b"abc", b"abd", b"b", b"b\x00\x00", b"ba"],
+        [b"a", b"ab", b"abb", b"abc\x00", b"abd", b"b\x00", b"ba", b"bb"])
+    # prefix-tree keys as in the string workload, small: shared 8-byte stems,
+    # keys longer than the 16-byte prefix cache, 20 % of B drawn from A
+    yield synth.strings(seed=17, count=3000, fanout=4, depth=4)
+    yield synth.strings(seed=18, count=2000, fanout=2, depth=4, max_suffix=40, min_suffix=12)
+
+
+@pytest.mark.parametrize("s", list(_str_bitmap_cases()))
+def test_replacement_str_bitmap_and_lower_bounds(s):
+    # C and lb_B of the string walk against Python's own byte order: bisect_left
+    # over the sorted bytes list of A gives each B key's lower bound, and a set
+    # membership test gives the collision bit of each A key ("Everett:
+    # collision bitmap and rank experiment", "Corrected record ordinals").
+    import bisect
+    ka, kb = _side_keys(s.A), _side_keys(s.B)
+    assert ka == sorted(ka) and kb == sorted(kb)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    lb = [bisect.bisect_left(ka, k) for k in kb]
+    assert r.lb_B.tolist() == lb
+    in_b = set(kb)
+    hit = np.array([t for t, k in enumerate(ka) if k in in_b], dtype=np.int64)
+    assert (r.C == synth._bitmap(hit, len(ka))).all()
+    # the ordinals by the closed forms, with R(i) counted from the membership test
+    R = np.concatenate([[0], np.cumsum([k in in_b for k in ka])]).astype(np.int64)
+    ordA = [oracle.ORD_DROPPED if ka[t] in in_b else t + bisect.bisect_left(kb, ka[t]) - R[t]
+            for t in range(len(ka))]
+    ordB = [j + lb[j] - R[lb[j]] for j in range(len(kb))]
+    assert r.ord_A.tolist() == ordA and r.ord_B.tolist() == ordB
+
+
 # ---------------------------------------------------------------------------
 # Rank and the rank512 directory
 # ---------------------------------------------------------------------------
