@@ -63,7 +63,9 @@ enum {
   LSM_ERR_CUDA = 4,      /* a CUDA launch or runtime call failed */
   LSM_ERR_TIMEOUT = 5,   /* a bounded device wait ran out (device status) */
   LSM_ERR_WORKSPACE = 6, /* workspace missing or smaller than required */
-  LSM_ERR_ALIGN = 7      /* a pointer misses its required alignment */
+  LSM_ERR_ALIGN = 7,     /* a pointer misses its required alignment */
+  LSM_ERR_UNSORTED = 8   /* only from the validators: an input breaks its order
+                            (device status) */
 };
 
 /* Key types. */
@@ -468,6 +470,31 @@ LSM_API int lsm_ef_sizes(int64_t N, uint64_t U, int64_t *sizes);
 LSM_API int lsm_fc_ef_build(const uint64_t *bit_off, int64_t N, uint64_t w, uint64_t U,
                             uint64_t *lows, uint64_t *highs, uint64_t *samples, uint64_t *sparse,
                             int64_t *d_nsparse, void *stream);
+
+/* ---- input validation ----------------------------------------------------- */
+/* The merge and replacement calls trust their inputs' order, as the pages'
+ * parser trusts its accepted inputs ([BP] "Pipeline": it checks framing,
+ * tags, offset bounds and retained lengths, not order). A caller that cannot
+ * vouch for an input runs one of these first. Each sets *d_first to -1 and
+ * then, on the device, to the smallest t whose pair (t, t+1) breaks the
+ * order, and records LSM_ERR_UNSORTED in the sticky device status word
+ * (lsm_get_device_status) when one does; nothing traps or faults.
+ *   strict = 1: strictly increasing (the unique-key inputs of the
+ *               replacement calls); strict = 0: nondecreasing (the inputs of
+ *               lsm_merge_stable).
+ * keys: device, count elements of key_type (int32 compares signed), aligned
+ * to the element size. d_first: device int64[1]. count < 2 leaves -1. */
+LSM_API int lsm_validate_sorted(int key_type, const void *keys, int64_t count, int strict,
+                                int64_t *d_first, void *stream);
+
+/* The same for a byte-string column (unsigned lexicographic order, a proper
+ * prefix first). arena_bytes is the arena's length: a pair whose offsets are
+ * out of order or past arena_bytes counts as a violation and its bytes are
+ * not read, so malformed offsets cannot cause an out-of-bounds access. With
+ * count = 1 the key's two offsets are checked. keys: as in lsm_bytes (arena
+ * 8-byte aligned and readable up to the next multiple of 8 bytes). */
+LSM_API int lsm_validate_sorted_str(const lsm_bytes *keys, int64_t count, uint64_t arena_bytes,
+                                    int strict, int64_t *d_first, void *stream);
 
 /* ---- tuning ----------------------------------------------------------------- */
 /* Selects the tile configuration of lsm_merge_stable for a key type:

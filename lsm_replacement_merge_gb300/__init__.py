@@ -31,6 +31,7 @@ LSM_ERR_CUDA = 4
 LSM_ERR_TIMEOUT = 5
 LSM_ERR_WORKSPACE = 6
 LSM_ERR_ALIGN = 7
+LSM_ERR_UNSORTED = 8
 LSM_KEY_I32 = 1
 LSM_KEY_U64 = 2
 LSM_OP_MERGE_STABLE = 1
@@ -117,6 +118,9 @@ def lib():
                 "lsm_tune_replace": ([ctypes.c_int] * 3, ctypes.c_int),
                 "lsm_set_profile_events": ([P, P], ctypes.c_int),
                 "lsm_rank_build_noalloc": ([P, I, P, P, P], ctypes.c_int),
+                "lsm_validate_sorted": ([ctypes.c_int, P, I, ctypes.c_int, P, P], ctypes.c_int),
+                "lsm_validate_sorted_str": ([P, I, ctypes.c_uint64, ctypes.c_int, P, P],
+                                            ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -308,6 +312,33 @@ class Bytes:
 
     def _c(self):
         return _Bytes(_ptr(self.arena), _ptr(self.off))
+
+
+def validate_sorted(keys, strict: bool, d_first=None, stream=None):
+    """lsm_validate_sorted: d_first (device int64[1]) = the first t whose pair
+    (t, t+1) breaks the order, or -1; a violation also records
+    LSM_ERR_UNSORTED in the device status word."""
+    if d_first is None:
+        d_first = _empty(1, torch.int64, keys.device)
+    _check("lsm_validate_sorted",
+           lib().lsm_validate_sorted(_key_type(keys), _ptr(keys) if keys.numel() else None,
+                                     keys.numel(), int(bool(strict)), _ptr(d_first),
+                                     _stream(stream)))
+    return d_first
+
+
+def validate_sorted_str(col: Bytes, strict: bool, arena_bytes=None, d_first=None, stream=None):
+    """lsm_validate_sorted_str over a CSR byte column (arena_bytes defaults to
+    the arena's readable length)."""
+    if d_first is None:
+        d_first = _empty(1, torch.int64, col.off.device)
+    if arena_bytes is None:
+        arena_bytes = col.arena.numel()
+    c = col._c()
+    _check("lsm_validate_sorted_str",
+           lib().lsm_validate_sorted_str(ctypes.byref(c), col.count, int(arena_bytes),
+                                         int(bool(strict)), _ptr(d_first), _stream(stream)))
+    return d_first
 
 
 def collision_mark_str(A: Bytes, B: Bytes, C=None, lb_B=None, ws=None, stream=None):

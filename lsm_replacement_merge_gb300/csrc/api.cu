@@ -167,6 +167,7 @@ LSM_API const char *lsm_status_string(int status) {
     case LSM_ERR_TIMEOUT: return "LSM_ERR_TIMEOUT: a bounded device wait ran out";
     case LSM_ERR_WORKSPACE: return "LSM_ERR_WORKSPACE: workspace missing or too small";
     case LSM_ERR_ALIGN: return "LSM_ERR_ALIGN: pointer alignment requirement not met";
+    case LSM_ERR_UNSORTED: return "LSM_ERR_UNSORTED: an input breaks its sorted order";
     default: return "unknown lsm status";
   }
 }
@@ -277,6 +278,30 @@ LSM_API int lsm_merge_sort(int key_type, const void *keys, const uint32_t *pay, 
   return cuda_status(launch_merge_sort(key_type, keys, pay, N, out_keys, out_pay, tmp,
                                        pay ? tmp_pay : nullptr, part, status_ptr(),
                                        static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_validate_sorted(int key_type, const void *keys, int64_t count, int strict,
+                                int64_t *d_first, void *stream) {
+  if (key_type != LSM_KEY_I32 && key_type != LSM_KEY_U64) return LSM_ERR_DTYPE;
+  if (count < 0 || !d_first || (count && !keys) || (strict != 0 && strict != 1)) return LSM_ERR_ARG;
+  if (count > (int64_t(1) << 40)) return LSM_ERR_OVERFLOW;
+  const uintptr_t esz = key_type == LSM_KEY_I32 ? 4 : 8;
+  if ((keys && (reinterpret_cast<uintptr_t>(keys) & (esz - 1))) || !aligned8(d_first))
+    return LSM_ERR_ALIGN;
+  return cuda_status(launch_validate_sorted(key_type, keys, count, strict, d_first, status_ptr(),
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_validate_sorted_str(const lsm_bytes *keys, int64_t count, uint64_t arena_bytes,
+                                    int strict, int64_t *d_first, void *stream) {
+  if (!keys || count < 0 || !d_first || (strict != 0 && strict != 1)) return LSM_ERR_ARG;
+  if (count && (!keys->off || (arena_bytes && !keys->arena))) return LSM_ERR_ARG;
+  if (count > kMax31) return LSM_ERR_OVERFLOW;
+  if ((keys->arena && !aligned8(keys->arena)) || (keys->off && !aligned8(keys->off)) ||
+      !aligned8(d_first))
+    return LSM_ERR_ALIGN;
+  return cuda_status(launch_validate_sorted_str(*keys, count, arena_bytes, strict, d_first,
+                                                status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,

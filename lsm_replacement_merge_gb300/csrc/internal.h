@@ -138,6 +138,16 @@ cudaError_t launch_ef_build(const uint64_t *bit_off, int64_t N, uint64_t w, uint
                             uint64_t *lows, uint64_t *highs, uint64_t *samples, uint64_t *sparse,
                             int64_t *d_nsparse, int32_t *status, cudaStream_t s);
 
+// --- validate.cu ---
+// Sets *d_first to -1, then to the smallest t whose pair (t, t+1) breaks the
+// order (strict: keys[t] < keys[t+1]; else keys[t] <= keys[t+1]); records
+// LSM_ERR_UNSORTED in `status` when one does.
+cudaError_t launch_validate_sorted(int key_type, const void *keys, int64_t count, int strict,
+                                   int64_t *d_first, int32_t *status, cudaStream_t s);
+cudaError_t launch_validate_sorted_str(const lsm_bytes &col, int64_t count, uint64_t arena_bytes,
+                                       int strict, int64_t *d_first, int32_t *status,
+                                       cudaStream_t s);
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
