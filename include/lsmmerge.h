@@ -427,6 +427,19 @@ LSM_API int lsm_bytefc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs
                                     uint32_t *rec_bytes, uint64_t *byte_off, void *ws,
                                     size_t ws_bytes, void *stream);
 
+/* The common encoded value width of the merged records, detected before they
+ * are sized ([BP] "Pipeline"; "seventeen" there is a one-byte presence tag
+ * and sixteen payload bytes): d_width[0] = 1 + L when every record that refs
+ * names (N of them) is present, not a tombstone, and every one of their
+ * values has L bytes; otherwise 0, and 0 for N = 0. Inputs that vary (other
+ * lengths, tombstones) can merge into an output of one width when the newer
+ * records replace the odd ones. d_width: device uint64[4], 8-byte aligned;
+ * elements 1..3 are scratch. The caller reads d_width[0] (one host read, as
+ * for the payload size) and passes it as W to lsm_bytefc_lengths_scan and
+ * lsm_bytefc_emit. */
+LSM_API int lsm_bytefc_value_width(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
+                                   uint64_t *d_width, void *stream);
+
 /* Writes the payload: record i's bytes at [byte_off[i], byte_off[i+1]) of
  * payload (device, nbytes >= byte_off[N]); bytes past byte_off[N] are not
  * written. lcp, ctrl, byte_off: lsm_bytefc_lengths_scan's outputs for the

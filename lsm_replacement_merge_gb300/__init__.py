@@ -111,6 +111,7 @@ def lib():
                 "lsm_bytefc_lengths_scan": ([P, P, I, ctypes.c_uint64, P, P, P, P, P, S, P],
                                             ctypes.c_int),
                 "lsm_bytefc_emit": ([P, P, I, ctypes.c_uint64, P, P, P, P, I, P], ctypes.c_int),
+                "lsm_bytefc_value_width": ([P, P, I, P, P], ctypes.c_int),
                 "lsm_fc_ef_build": ([P, I, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, P, P],
                                     ctypes.c_int),
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
@@ -638,6 +639,19 @@ def bytefc_lengths_scan(fc: FcInput, refs, N: int, W: int = 0, lcp=None, ctrl=No
                                          _ptr(rec_bytes), _ptr(byte_off), _ptr(ws), ws.numel(),
                                          _stream(stream)))
     return lcp, ctrl, rec_bytes, byte_off
+
+
+def bytefc_value_width(fc: FcInput, refs, N: int, d_width=None, stream=None):
+    """lsm_bytefc_value_width: device uint64[4] whose element 0 is the common
+    encoded value width of the N merged records (1 + the value length when
+    every record is present with one length, else 0)."""
+    if d_width is None:
+        d_width = _empty(4, torch.uint64, refs.device)
+    c = fc._c()
+    _check("lsm_bytefc_value_width",
+           lib().lsm_bytefc_value_width(ctypes.byref(c), _ptr(refs) if N else None, N,
+                                        _ptr(d_width), _stream(stream)))
+    return d_width
 
 
 def bytefc_emit(fc: FcInput, refs, N: int, lcp, ctrl, byte_off, nbytes: int, W: int = 0,

@@ -530,6 +530,16 @@ LSM_API int lsm_bytefc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+LSM_API int lsm_bytefc_value_width(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
+                                   uint64_t *d_width, void *stream) {
+  if (int r = check_fc_input(in)) return r;
+  if (N < 0 || !d_width || (N && !refs)) return LSM_ERR_ARG;
+  if (N > kMax31 || N > in->m + in->n) return LSM_ERR_OVERFLOW;
+  if (!aligned8(d_width)) return LSM_ERR_ALIGN;
+  return cuda_status(launch_bytefc_value_width(*in, refs, N, d_width,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 LSM_API int lsm_bytefc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N, uint64_t W,
                             const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
                             uint8_t *payload, int64_t nbytes, void *stream) {

@@ -183,6 +183,62 @@ __global__ void __launch_bounds__(256) bytefc_emit_kernel(
   }
 }
 
+// Common encoded value width ("Pipeline": detected before the records are
+// sized). acc[1] = the smallest value length, acc[2] = the largest, acc[3]
+// = 1 when a record is a tombstone; the finish step writes acc[0] = 1 +
+// the length when every record is present with one length, else 0.
+__global__ void __launch_bounds__(256) bytefc_width_reduce_kernel(
+    BSource sa, BSource sb, const uint32_t *__restrict__ refs, int64_t N,
+    unsigned long long *acc) {
+  pdl_begin();
+  __shared__ unsigned long long s_min[8], s_max[8];
+  __shared__ int s_tomb[8];
+  unsigned long long mn = ~0ull, mx = 0;
+  int tomb = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
+    const uint32_t r = __ldg(refs + i), idx = r & 0x7FFFFFFFu;
+    const BSource &src = bpick(sa, sb, r);
+    if (is_tomb(src, idx)) {
+      tomb = 1;
+    } else {
+      const unsigned long long vb = __ldg(src.val.off + idx + 1) - __ldg(src.val.off + idx);
+      mn = vb < mn ? vb : mn;
+      mx = vb > mx ? vb : mx;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+    const unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+    mn = a < mn ? a : mn;
+    mx = b > mx ? b : mx;
+  }
+  tomb = __any_sync(0xffffffffu, tomb);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    s_min[w] = mn;
+    s_max[w] = mx;
+    s_tomb[w] = tomb;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int t = 1; t < static_cast<int>(blockDim.x >> 5); ++t) {
+      mn = s_min[t] < mn ? s_min[t] : mn;
+      mx = s_max[t] > mx ? s_max[t] : mx;
+      tomb |= s_tomb[t];
+    }
+    if (mn != ~0ull) atomicMin(acc + 1, mn);
+    if (mx) atomicMax(acc + 2, mx);
+    if (tomb) atomicOr(acc + 3, 1ull);
+  }
+}
+
+__global__ void bytefc_width_finish_kernel(int64_t N, unsigned long long *acc) {
+  pdl_begin();
+  acc[0] = (N > 0 && !acc[3] && acc[1] == acc[2]) ? 1 + acc[1] : 0;
+}
+
 BSource bsource(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb) {
   return BSource{key, val, tomb};
 }
@@ -206,6 +262,24 @@ cudaError_t launch_bytefc_lengths_scan(const lsm_fc_input &in, const uint32_t *r
   if (err == cudaSuccess) err = launch_fc_offsets(rec_bytes, N, tile_sum, byte_off, s);
   profile_after(s);
   return err;
+}
+
+cudaError_t launch_bytefc_value_width(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
+                                      uint64_t *d_width, cudaStream_t s) {
+  auto *acc = reinterpret_cast<unsigned long long *>(d_width);
+  cudaError_t err = cudaMemsetAsync(acc + 1, 0xFF, sizeof(uint64_t), s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(acc + 2, 0, 2 * sizeof(uint64_t), s);
+  if (err != cudaSuccess) return err;
+  if (N > 0) {
+    int64_t blocks = (N + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    if (blocks > cap && cap > 0) blocks = cap;
+    err = launch_kernel(false, bytefc_width_reduce_kernel, static_cast<unsigned>(blocks), 256, 0,
+                        s, bsource(in.keyA, in.valA, in.tombA), bsource(in.keyB, in.valB, in.tombB),
+                        refs, N, acc);
+    if (err != cudaSuccess) return err;
+  }
+  return launch_kernel(false, bytefc_width_finish_kernel, 1, 1, 0, s, N, acc);
 }
 
 cudaError_t launch_bytefc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N, uint64_t W,

@@ -121,6 +121,9 @@ cudaError_t launch_bytefc_lengths_scan(const lsm_fc_input &in, const uint32_t *r
                                        uint64_t W, uint32_t *lcp, uint32_t *ctrl,
                                        uint32_t *rec_bytes, uint64_t *byte_off, void *ws,
                                        int32_t *status, cudaStream_t s);
+// d_width: device uint64[4]; [0] receives the common width, [1..3] scratch.
+cudaError_t launch_bytefc_value_width(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
+                                      uint64_t *d_width, cudaStream_t s);
 cudaError_t launch_bytefc_emit(const lsm_fc_input &in, const uint32_t *refs, int64_t N, uint64_t W,
                                const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
                                uint8_t *payload, int64_t nbytes, int32_t *status, cudaStream_t s);

@@ -404,6 +404,30 @@ def bytefc_encode(keysA, valsA, tombA, keysB, valsB, tombB, refs, W=0, with_payl
     return FC(lcp, ctrl, rec, off, payload, int(total))
 
 
+def bytefc_value_width(valsA_off, tombA, valsB_off, tombB, refs):
+    """The common encoded value width of the merged records ([BP] "Pipeline":
+    the width is detected before sizing; 17 = a one-byte presence tag and 16
+    value bytes): 1 + L when every record refs names is present and every one
+    of their values has L bytes, else 0 (0 for no records). Plain loop over
+    the records."""
+    offs = (np.asarray(valsA_off, np.int64), np.asarray(valsB_off, np.int64))
+    tombs = (tombA, tombB)
+    length = None
+    if len(refs) == 0:
+        return 0
+    for r in np.asarray(refs, np.uint32).tolist():
+        src, idx = r >> 31, r & 0x7FFFFFFF
+        t = tombs[src]
+        if t is not None and len(t) and (int(t[idx // 32]) >> (idx % 32)) & 1:
+            return 0
+        L = int(offs[src][idx + 1] - offs[src][idx])
+        if length is None:
+            length = L
+        elif L != length:
+            return 0
+    return 1 + length
+
+
 def bytefc_decode(payload, N, W, key_cap, val_cap):
     """Independent byte-profile decoder. Returns (keys (arena, off), vals (arena, off), tombs)."""
     payload = _c(payload, np.uint8)

@@ -86,3 +86,65 @@ def test_common_width_17(lsm):
 
 def test_config_strings_4M(lsm):
     check_bytefc(lsm, synth.strings())
+
+
+def _width_inputs():
+    rng = np.random.default_rng(9)
+    keysA = sorted({bytes(rng.integers(0, 256, size=int(rng.integers(1, 12)), dtype=np.uint8))
+                    for _ in range(5000)})
+    v = lambda L: bytes(rng.integers(0, 256, size=L, dtype=np.uint8))  # noqa: E731
+    # A varies: 16-byte values, some 5-byte values and some tombstones
+    valsA = [None if t % 11 == 3 else v(5 if t % 7 == 2 else 16) for t in range(len(keysA))]
+    odd = [k for k, x in zip(keysA, valsA) if x is None or len(x) != 16]
+    # B replaces every odd A record (and adds fresh keys) with 16-byte values
+    keysB = sorted(set(odd) | set(keysA[::17]) | {b"\xff" * (t % 5 + 13) for t in range(9)})
+    valsB = [v(16) for _ in keysB]
+    yield synth.strings_from_lists(keysA, keysB, valsA, valsB), 17
+    # one B tombstone survives: no common width
+    valsB2 = list(valsB)
+    valsB2[len(valsB2) // 2] = None
+    yield synth.strings_from_lists(keysA, keysB, valsA, valsB2), 0
+    # one B value of 15 bytes: no common width
+    valsB3 = list(valsB)
+    valsB3[3] = v(15)
+    yield synth.strings_from_lists(keysA, keysB, valsA, valsB3), 0
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_value_width_detected(lsm, case):
+    s, want = list(_width_inputs())[case]
+    fc = device_input(lsm, s)
+    refs, N = gpu_refs(lsm, fc)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    exp = oracle.bytefc_value_width(s.A.val_off, s.A.tomb, s.B.val_off, s.B.tomb, r.refs)
+    assert exp == want
+    W = int(down(lsm.bytefc_value_width(fc, refs, N))[0])
+    assert W == exp
+    # sized and emitted with the detected width, bit-exact against the oracle
+    check_bytefc(lsm, s, W=W)
+
+
+def test_width_errors_are_reported(lsm):
+    # W = 17 over records that do not all have it: LSM_ERR_ARG in the device
+    # status, for a surviving tombstone and for a 15-byte value
+    for case in (1, 2):
+        s, _ = list(_width_inputs())[case]
+        fc = device_input(lsm, s)
+        refs, N = gpu_refs(lsm, fc)
+        lsm.get_device_status(reset=True)
+        lsm.bytefc_lengths_scan(fc, refs, N, 17)
+        assert lsm.get_device_status(reset=True) == lsm.LSM_ERR_ARG
+    # an emit whose offsets do not match its records: reported, and nothing is
+    # written past the buffer the caller gave
+    s, _ = list(_width_inputs())[0]
+    fc = device_input(lsm, s)
+    refs, N = gpu_refs(lsm, fc)
+    lcp, ctrl, rec, off = lsm.bytefc_lengths_scan(fc, refs, N, 17)
+    assert lsm.get_device_status(reset=True) == lsm.LSM_OK
+    bad_off = off.clone()
+    bad_off[1:] -= 1  # every record one byte too short
+    total = int(down(off)[N])
+    buf = torch.full((total + 64,), 0xEE, dtype=torch.uint8, device="cuda")
+    lsm.bytefc_emit(fc, refs, N, lcp, ctrl, bad_off, total, 17, payload=buf)
+    assert lsm.get_device_status(reset=True) == lsm.LSM_ERR_ARG
+    assert (down(buf)[total:] == 0xEE).all()

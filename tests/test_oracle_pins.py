@@ -697,3 +697,25 @@ def test_bytefc_roundtrip_edges_and_common_width():
     valsB = [bytes(rng.integers(0, 256, size=16, dtype=np.uint8)) for _ in keysB]
     s = synth.strings_from_lists(keysA, keysB, valsA, valsB)
     _check_bytefc_roundtrip(s, W=17)
+
+
+def _width_case(keysA, valsA, keysB, valsB):
+    s = synth.strings_from_lists(keysA, keysB, valsA, valsB)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    return oracle.bytefc_value_width(s.A.val_off, s.A.tomb, s.B.val_off, s.B.tomb, r.refs)
+
+
+def test_bytefc_value_width_special_cases():
+    v16, v15 = b"v" * 16, b"w" * 15
+    # every survivor present with sixteen value bytes: width 17 ([BP] "Pipeline")
+    assert _width_case([b"a", b"b"], [v16, v16], [b"c"], [v16]) == 17
+    # a tombstone or a value of another length anywhere: no common width
+    assert _width_case([b"a", b"b"], [v16, None], [b"c"], [v16]) == 0
+    assert _width_case([b"a", b"b"], [v16, v15], [b"c"], [v16]) == 0
+    # the odd records replaced by newer ones of the common length: width 17
+    assert _width_case([b"a", b"b", b"c"], [v16, v15, None], [b"b", b"c"], [v16, v16]) == 17
+    # a newer tombstone survives and breaks it
+    assert _width_case([b"a", b"b"], [v16, v16], [b"b"], [None]) == 0
+    # empty values make width 1 (the tag alone); no records, no width
+    assert _width_case([b"a"], [b""], [b"b"], [b""]) == 1
+    assert _width_case([], [], [], []) == 0
