@@ -630,12 +630,20 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
     w1 = lsm.workspace(lsm.LSM_OP_COLLISION_MARK, m, n, dev)
     w2 = lsm.workspace(lsm.LSM_OP_RANK_BUILD, m, 0, dev)
     w3 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_COMPACT, m, n, dev)
+    w6 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_MERGE, m, n, dev)
     stages = [("collision_mark", lambda: lsm.collision_mark(A, B, C, lb, w1)),
               ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
               ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
                   m, n, C, dir_, lb, refs, oa, ob, cnt, w3))]
-    ms, per = time_pipeline(torch, stages, steps, flush)
+    # The step: the whole path in one call (partition + mark, rank512 build,
+    # compaction on the mark's diagonals); every output of the three calls.
+    whole = [("replacement_merge", lambda: lsm.replacement_merge(
+        A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w6))]
+    ms, per_whole = time_pipeline(torch, whole, steps, flush)
     N = int(cnt.item())
+    # the same work as three separate calls: per-kernel times (each call's
+    # main pipeline bracketed by events) and the step with one more partition
+    ms_sep, per = time_pipeline(torch, stages, steps, flush)
     alg = (8 * (m + n)                      # read keys
            + 4 * ((m + 31) // 32)           # write C
            + 12 * (m // 512 + 1)            # write dir
@@ -645,7 +653,14 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
                  "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
                  "frac": alg / (ms * 1e-3) / 1e9 / peak,
                  "frac_of_8TBs_nominal": alg / (ms * 1e-3) / 1e9 / 8000.0,
-                 "kernel_ms": per, "gpu_launches_per_step": 5,
+                 "call": "lsm_replacement_merge", "gpu_launches_per_step": 4,
+                 "mark_pipeline_ms": per_whole["replacement_merge"],
+                 "workspace_bytes": {"replacement_merge": w6.numel()},
+                 "separate_calls": {"ms_per_step": ms_sep, "kernel_ms": per,
+                                    "gpu_launches_per_step": 5,
+                                    "workspace_bytes": {"collision_mark": w1.numel(),
+                                                        "rank_build": w2.numel(),
+                                                        "replacement_merge_compact": w3.numel()}},
                  "l2": "flushed (256 MiB write) before every step"}
     # The materialized row: the same step plus the survivors' keys, values
     # and tombstone bits gathered in merged order.

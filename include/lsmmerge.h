@@ -81,7 +81,8 @@ enum {
   LSM_OP_FC_LENGTHS_SCAN = 6,
   LSM_OP_MERGE_SORT = 7,
   LSM_OP_RANK2048_BUILD = 8,
-  LSM_OP_REPLACEMENT_FUSED = 9
+  LSM_OP_REPLACEMENT_FUSED = 9,
+  LSM_OP_REPLACEMENT_MERGE = 10
 };
 
 #define LSM_REF_FROM_B 0x80000000u
@@ -295,6 +296,22 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                           uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
                                           int64_t *d_count, void *ws, size_t ws_bytes,
                                           void *stream);
+
+/* The whole replacement merge, a3 + a4 + a5, in one call: the outputs of
+ * lsm_collision_mark, lsm_rank_build and lsm_replacement_merge_compact in
+ * turn (C, lb_B, dir, *d_total = R(m), out_refs, ord_A, ord_B, *d_count = m
+ * + n - R(m)), by the same steps: the collision mark over merge-path tiles of
+ * the keys ([CB] "Corrected record ordinals"), the rank512 build ([CB]
+ * "Temporary rank layouts") and the compaction by merge path over positions
+ * ([CB] "The three experimental paths", third path), with the compaction's
+ * tiles on the mark's diagonals, so that the mark hands the compaction its
+ * co-ranks and no second partition is needed. Arguments, alignment and
+ * limits as those three calls; C needs no clearing. ws: at least
+ * lsm_workspace_size(LSM_OP_REPLACEMENT_MERGE, 0, m, n) bytes. */
+LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                  uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,
+                                  uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
+                                  int64_t *d_count, void *ws, size_t ws_bytes, void *stream);
 
 /* a3 + a4 + a5 in one call: the same outputs as lsm_collision_mark,
  * lsm_rank_build and lsm_replacement_merge_compact in turn (C, lb_B, dir,

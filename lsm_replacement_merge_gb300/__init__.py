@@ -43,6 +43,7 @@ LSM_OP_FC_LENGTHS_SCAN = 6
 LSM_OP_MERGE_SORT = 7
 LSM_OP_RANK2048_BUILD = 8
 LSM_OP_REPLACEMENT_FUSED = 9
+LSM_OP_REPLACEMENT_MERGE = 10
 REF_FROM_B = 0x80000000
 ORD_DROPPED = 0xFFFFFFFF
 
@@ -103,6 +104,8 @@ def lib():
                                                    ctypes.c_int),
                 "lsm_replacement_merge_fused": ([P, I, P, I, P, P, P, P, P, P, P, P, P, S, P],
                                                 ctypes.c_int),
+                "lsm_replacement_merge": ([P, I, P, I, P, P, P, P, P, P, P, P, P, S, P],
+                                          ctypes.c_int),
                 "lsm_replacement_materialize": ([P, P, P, I, P, P, P, I, P, P, P, P, P, P],
                                                 ctypes.c_int),
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
@@ -211,7 +214,9 @@ DEFAULT_MERGE_CONFIG = (11, 2, 1)
 
 
 REPLACE_VARIANTS = ((256, 11), (128, 23), (256, 23), (512, 11))
-DEFAULT_REPLACE_VARIANT = {0: (512, 11), 1: (256, 11)}  # kernel -> (threads, items)
+# (0, 0) selects the warp pipelines (the default); the rest the earlier
+# block-synchronous tile pipelines, kept for comparison
+DEFAULT_REPLACE_VARIANT = {0: (0, 0), 1: (0, 0)}  # kernel -> (threads, items)
 
 
 def tune_replace(kernel: int, threads: int, items_per_thread: int) -> None:
@@ -467,6 +472,39 @@ def replacement_merge_compact(m: int, n: int, C, dir_, lb_B, refs=None, ord_A=No
                                                _ptr(ord_A) if m else None, _ptr(ord_B) if n else None,
                                                _ptr(d_count), _ptr(ws), ws.numel(), _stream(stream)))
     return refs, ord_A, ord_B, d_count
+
+
+def replacement_merge(A, B, C=None, lb_B=None, dir_=None, d_total=None, refs=None,
+                      ord_A=None, ord_B=None, d_count=None, ws=None, stream=None):
+    """The whole path in one call (lsm_replacement_merge). Returns (C, lb_B,
+    dir, d_total, refs, ord_A, ord_B, d_count)."""
+    m, n = A.numel(), B.numel()
+    dev = A.device
+    if C is None:
+        C = _empty(max((m + 31) // 32, 4), torch.uint32, dev)
+    if lb_B is None:
+        lb_B = _empty(n, torch.uint32, dev)
+    if dir_ is None:
+        dir_ = _empty(3 * (m // 512 + 1), torch.uint32, dev)
+    if d_total is None:
+        d_total = _empty(1, torch.int64, dev)
+    if refs is None:
+        refs = _empty(max(m + n, 1), torch.uint32, dev)
+    if ord_A is None:
+        ord_A = _empty(m, torch.uint32, dev)
+    if ord_B is None:
+        ord_B = _empty(n, torch.uint32, dev)
+    if d_count is None:
+        d_count = _empty(1, torch.int64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_REPLACEMENT_MERGE, m, n, dev)
+    _check("lsm_replacement_merge",
+           lib().lsm_replacement_merge(
+               _ptr(A) if m else None, m, _ptr(B) if n else None, n, _ptr(C) if m else None,
+               _ptr(lb_B) if n else None, _ptr(dir_), _ptr(d_total), _ptr(refs),
+               _ptr(ord_A) if m else None, _ptr(ord_B) if n else None, _ptr(d_count), _ptr(ws),
+               ws.numel(), _stream(stream)))
+    return C, lb_B, dir_, d_total, refs, ord_A, ord_B, d_count
 
 
 def replacement_merge_fused(A, B, C=None, lb_B=None, dir_=None, d_total=None, refs=None,

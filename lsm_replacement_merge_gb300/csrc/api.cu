@@ -126,9 +126,18 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n, int key_type = LSM_KEY_U64) {
       c.take<uint64_t>(rank_build_ctas(m));
       break;
     }
+    case LSM_OP_REPLACEMENT_MERGE: {
+      const int64_t G = (m + n + replacement_tile() - 1) / replacement_tile();
+      c.take<int64_t>(G + 1);
+      c.take<int64_t>(G + 1);
+      c.take<uint64_t>(rank_build_ctas(m));
+      c.take<uint32_t>(merge_bitmap_words(m + n));
+      break;
+    }
     case LSM_OP_REPLACEMENT_COMPACT: {
       const int64_t D = replace_min_tile();
       c.take<int64_t>((m + n + D - 1) / D + 1);
+      c.take<uint32_t>(merge_bitmap_words(m + n));
       break;
     }
     case LSM_OP_FC_LENGTHS_SCAN:
@@ -191,7 +200,7 @@ LSM_API int lsm_workspace_size(int op, int key_type, int64_t m, int64_t n, size_
   if ((op == LSM_OP_MERGE_STABLE || op == LSM_OP_MERGE_SORT) && key_type != LSM_KEY_I32 &&
       key_type != LSM_KEY_U64)
     return LSM_ERR_DTYPE;
-  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_REPLACEMENT_FUSED) return LSM_ERR_ARG;
+  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_REPLACEMENT_MERGE) return LSM_ERR_ARG;
   *bytes = ws_bytes_for(op, m, n, key_type);
   return LSM_OK;
 }
@@ -406,8 +415,35 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
   Carver c{static_cast<uint8_t *>(ws)};
   const int64_t D = replace_min_tile();
   int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
-  return cuda_status(launch_compact(m, n, C, dir, lb_B, out_refs, ord_A, ord_B, d_count, part,
+  uint32_t *mb = c.take<uint32_t>(merge_bitmap_words(m + n));
+  return cuda_status(launch_compact(m, n, C, dir, lb_B, out_refs, ord_A, ord_B, d_count, part, mb,
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                  uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,
+                                  uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
+                                  int64_t *d_count, void *ws, size_t ws_bytes, void *stream) {
+  if (m < 0 || n < 0 || !dir || !d_total || !d_count) return LSM_ERR_ARG;
+  if ((m && (!A || !C || !ord_A)) || (n && (!B || !lb_B || !ord_B)) || (m + n && !out_refs))
+    return LSM_ERR_ARG;
+  if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
+  for (const void *p : {static_cast<const void *>(A), static_cast<const void *>(B),
+                        static_cast<const void *>(C), static_cast<const void *>(lb_B),
+                        static_cast<const void *>(out_refs), static_cast<const void *>(ord_A),
+                        static_cast<const void *>(ord_B)})
+    if (p && !aligned16(p)) return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_REPLACEMENT_MERGE, m, n, ws, ws_bytes)) return r;
+  Carver c{static_cast<uint8_t *>(ws)};
+  const int64_t G = (m + n + replacement_tile() - 1) / replacement_tile();
+  int64_t *part_m = c.take<int64_t>(G + 1);
+  int64_t *part_c = c.take<int64_t>(G + 1);
+  uint64_t *rank_ws = c.take<uint64_t>(rank_build_ctas(m));
+  uint32_t *mb = c.take<uint32_t>(merge_bitmap_words(m + n));
+  return cuda_status(launch_replacement_merge(A ? A : B, m, B ? B : A, n, C, lb_B, dir, d_total,
+                                              out_refs, ord_A, ord_B, d_count, part_m, part_c, mb,
+                                              rank_ws, status_ptr(),
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_replacement_merge_fused(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,

@@ -152,9 +152,14 @@ __global__ void __launch_bounds__(256) bytefc_emit_kernel(
     const uint64_t p = __ldg(lcp + i), b = __ldg(ctrl + i);
     uint64_t pos = __ldg(off + i);
     const uint64_t end = __ldg(off + i + 1);
-    // lengths that do not match this record (not the lengths pass's output)
-    // are reported, and nothing is written past the record's own end
-    if (end > static_cast<uint64_t>(nbytes) || p > K || pos + leb_len(b) + leb_len(K - p) > end) {
+    // a record whose offsets, lcp or control do not give exactly its own
+    // length (not the lengths pass's output for these inputs) is reported and
+    // not written, so that nothing lands outside [byte_off[i], byte_off[i+1])
+    const bool tomb = is_tomb(src, idx);
+    const uint64_t vlen = tomb ? 0 : __ldg(src.val.off + idx + 1) - __ldg(src.val.off + idx);
+    const uint64_t v = tomb ? 1 : (W ? W : 1 + leb_len(vlen) + vlen);
+    if (end > static_cast<uint64_t>(nbytes) || p > K || end < pos ||
+        leb_len(b) + leb_len(K - p) + (K - p) + v != end - pos || (W && (tomb || vlen + 1 != W))) {
       report(status, LSM_ERR_ARG);
       continue;
     }

@@ -44,6 +44,33 @@ cudaError_t launch_merge_sort(int key_type, const void *in, const uint32_t *in_p
                               void *out, uint32_t *out_pay, void *tmp, uint32_t *tmp_pay,
                               int64_t *part, int32_t *status, cudaStream_t s);
 
+// --- replacement.cu ---
+// Tile of the warp pipelines (mark and compaction share their diagonals).
+int64_t replacement_tile();
+// Words of the merge bitmap for m + n positions (padded for whole-tile copies).
+int64_t merge_bitmap_words(int64_t total);
+// Partition (clears C and MB) + mark; part_m: G + 1 co-ranks (A first on
+// ties); part_c: G + 1 co-ranks of the compaction (B first on ties), or
+// null; MB: the merge bitmap (merge_bitmap_words(m + n)), or null.
+cudaError_t launch_mark_tiles(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                              uint32_t *C, uint32_t *lb_B, uint32_t *MB, int64_t *part_m,
+                              int64_t *part_c, int32_t *status, cudaStream_t s);
+// Compaction; part_c: the mark's co-ranks (then MB is the mark's merge
+// bitmap), or null to compute both from lb_B (co-ranks into part_scratch,
+// G + 1; MB rebuilt).
+cudaError_t launch_compact_tiles(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
+                                 const uint32_t *lb_B, uint32_t *MB, const int64_t *part_c,
+                                 int64_t *part_scratch, uint32_t *refs, uint32_t *ord_A,
+                                 uint32_t *ord_B, int64_t *d_count, int32_t *status,
+                                 cudaStream_t s);
+// The whole path (mark, rank512 build, compaction). part_m, part_c: G + 1
+// each; MB: merge_bitmap_words(m + n); rank_ws: rank_build_ctas(m) uint64.
+cudaError_t launch_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
+                                    uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,
+                                    uint32_t *refs, uint32_t *ord_A, uint32_t *ord_B,
+                                    int64_t *d_count, int64_t *part_m, int64_t *part_c,
+                                    uint32_t *MB, void *rank_ws, int32_t *status, cudaStream_t s);
+
 // --- replace.cu ---
 cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                   uint32_t *C, uint32_t *lb_B, int64_t *part_i, int32_t *status,
@@ -62,10 +89,11 @@ cudaError_t launch_materialize(const uint64_t *A, const uint32_t *Aval, const ui
                                const uint32_t *tombB, int64_t n, const uint32_t *refs,
                                const int64_t *d_count, uint64_t *out_keys, uint32_t *out_vals,
                                uint32_t *out_tomb, int32_t *status, cudaStream_t s);
+// mb_scratch: merge_bitmap_words(m + n) uint32 (used by the default path).
 cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
-                           uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,
-                           cudaStream_t s);
+                           uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
+                           uint32_t *mb_scratch, int32_t *status, cudaStream_t s);
 // The compaction reading R(i) from the rank2048 directory (default tile shape).
 cudaError_t launch_compact_rank2048(int64_t m, int64_t n, const uint32_t *C, const uint64_t *dir,
                                     const uint64_t *epochs, const uint32_t *lb_B, uint32_t *refs,

@@ -1110,9 +1110,9 @@ struct ReplaceVariant {
   int T, E, S;
 };
 constexpr ReplaceVariant kReplaceVariants[] = {{256, 11, 2}, {128, 23, 2}, {256, 23, 2}, {512, 11, 2}};
-// Defaults, measured on the 12M + 4M uint64 workload: (512,11) for the
-// collision mark, (256,11) for the compaction.
-int g_mark_variant = 3, g_compact_variant = 0;
+// -1 selects the warp pipelines of replacement.cu (the default); 0..3 the
+// tile variants above (the earlier block-synchronous pipelines).
+int g_mark_variant = -1, g_compact_variant = -1;
 
 template <int V>
 cudaError_t launch_mark_variant(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
@@ -1136,6 +1136,8 @@ cudaError_t launch_mark_variant(const uint64_t *A, int64_t m, const uint64_t *B,
 cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                   uint32_t *C, uint32_t *lb_B, int64_t *part_i, int32_t *status,
                                   cudaStream_t s) {
+  if (g_mark_variant < 0)
+    return launch_mark_tiles(A, m, B, n, C, lb_B, nullptr, part_i, nullptr, status, s);
   switch (g_mark_variant) {
     case 1: return launch_mark_variant<1>(A, m, B, n, C, lb_B, part_i, status, s);
     case 2: return launch_mark_variant<2>(A, m, B, n, C, lb_B, part_i, status, s);
@@ -1180,6 +1182,12 @@ int64_t replace_min_tile() {
 }
 
 int set_replace_variant(int kernel, int threads, int items) {
+  if (threads == 0 && items == 0) {
+    if (kernel == 0) g_mark_variant = -1;
+    else if (kernel == 1) g_compact_variant = -1;
+    else return LSM_ERR_ARG;
+    return LSM_OK;
+  }
   for (int i = 0; i < 4; ++i) {
     if (kReplaceVariants[i].T == threads && kReplaceVariants[i].E == items) {
       if (kernel == 0) g_mark_variant = i;
@@ -1317,8 +1325,11 @@ cudaError_t launch_materialize(const uint64_t *A, const uint32_t *Aval, const ui
 
 cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
-                           uint32_t *ord_B, int64_t *d_count, int64_t *part_i, int32_t *status,
-                           cudaStream_t s) {
+                           uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
+                           uint32_t *mb_scratch, int32_t *status, cudaStream_t s) {
+  if (g_compact_variant < 0)
+    return launch_compact_tiles(m, n, C, dir, lb_B, mb_scratch, nullptr, part_i, refs, ord_A,
+                                ord_B, d_count, status, s);
   const Rank512Dir rank{dir};
   switch (g_compact_variant) {
     case 1: return launch_compact_variant<1>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i, status, s);

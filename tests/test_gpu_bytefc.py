@@ -141,8 +141,9 @@ def test_width_errors_are_reported(lsm):
     refs, N = gpu_refs(lsm, fc)
     lcp, ctrl, rec, off = lsm.bytefc_lengths_scan(fc, refs, N, 17)
     assert lsm.get_device_status(reset=True) == lsm.LSM_OK
-    bad_off = off.clone()
-    bad_off[1:] -= 1  # every record one byte too short
+    bad = down(off).copy()
+    bad[1:] -= 1  # every record one byte too short
+    bad_off = up(bad)
     total = int(down(off)[N])
     buf = torch.full((total + 64,), 0xEE, dtype=torch.uint8, device="cuda")
     lsm.bytefc_emit(fc, refs, N, lcp, ctrl, bad_off, total, 17, payload=buf)
