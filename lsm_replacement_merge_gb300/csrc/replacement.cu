@@ -754,12 +754,15 @@ struct Rank512At {
 #define LSM_REPL_PART_LANES 8
 #endif
 constexpr int kPartLanes = LSM_REPL_PART_LANES;
-// Tile shapes, measured on the 12M + 4M workload: the mark with 8 consumer
-// warps of 11 keys per lane, the compaction with 4 warps of 22 positions per
-// lane (the same D = 2816 diagonals; fewer, longer lane walks amortize each
-// warp's popcounts and scans: step 112 -> 101 us).
-constexpr int kTileT = 256, kTileE = 11, kMarkS = 3, kMarkHG = 8;
-constexpr int kCompactT = 128, kCompactE = 22, kCompactS = 4;
+// Tile shapes, measured on the 12M + 4M step (CUDA events, L2 flushed by a
+// write before each step): D = 3840 diagonals, the mark with 8 consumer warps
+// (15 merge positions per thread) and two stages, the compaction with 4 warps
+// of 30 positions per lane and four stages: 89.7 us, against 96.9 us for D =
+// 2816 (8 x 11 / 4 x 22), 90.8 us for D = 5632 and 95.9 us for D = 7680;
+// longer lane walks amortize each warp's popcounts and scans (4 x 30: 89.7
+// us, 8 x 15: 98.0 us).
+constexpr int kTileT = 256, kTileE = 15, kMarkS = 2, kMarkHG = 8;
+constexpr int kCompactT = 128, kCompactE = 30, kCompactS = 4;
 using MarkDefault = MarkTile<kTileT, kTileE, kMarkS, kMarkHG>;
 using CompactDefault = CompactTile<kCompactT, kCompactE, kCompactS, Rank512At>;
 static_assert(MarkDefault::D == CompactDefault::D, "the compaction reuses the mark's diagonals");
