@@ -46,6 +46,12 @@
 #include "pipeline.cuh"
 #include "rank512.cuh"
 
+// Minimum resident CTAs per SM the mark kernel is compiled for (register
+// budget); 1 leaves the choice to the compiler.
+#ifndef MARK_MIN_BLOCKS
+#define MARK_MIN_BLOCKS 1
+#endif
+
 namespace lsm {
 
 namespace {
@@ -133,7 +139,7 @@ struct WLayout {
 };
 
 template <class Spec>
-__global__ void __launch_bounds__(Spec::T + 32) warp_pipeline_kernel(typename Spec::Params p,
+__global__ void __launch_bounds__(Spec::T + 32, Spec::kMinBlocks) warp_pipeline_kernel(typename Spec::Params p,
                                                                      int64_t G, int32_t *status) {
   pdl_begin();
   using L = WLayout<Spec>;
@@ -267,14 +273,35 @@ __device__ __forceinline__ void warp_store_run(uint32_t *gbase, int64_t g0, int 
 
 // Count of x in [lo, hi) with a[x] < key (a sorted), by steps of the powers
 // of two below `span` (the largest hi - lo over the warp, so that every lane
-// takes the same number of steps): lo plus that count.
+// takes the same number of steps): lo plus that count. Each step loads at a
+// clamped index (inside [lo, hi)) and keeps the candidate only when it lies
+// inside the range, so that the step needs no branch. Spans below 64 (the
+// common case of a group of keys between two heads) run fully unrolled.
+__device__ __forceinline__ int count_below_step(const uint64_t *a, int x, int hi, uint64_t key,
+                                                int step) {
+  const int c = x + step;
+  const int ci = c < hi ? c : hi;  // >= x + 1 > lo whenever a step is taken
+  const bool lt = a[ci - 1] < key;
+  return (c <= hi && lt) ? c : x;
+}
+
 __device__ __forceinline__ int count_below(const uint64_t *a, int lo, int hi, uint64_t key,
                                            int span) {
   int x = lo;
-  for (int step = span ? (1 << (31 - __clz(span))) : 0; step; step >>= 1) {
-    const int c = x + step;
-    if (c <= hi && a[c - 1] < key) x = c;
+  if (span < 64) {
+    const int k = span ? 32 - __clz(span) : 0;  // steps: the bit length of span
+    switch (k) {
+      case 6: x = count_below_step(a, x, hi, key, 32); [[fallthrough]];
+      case 5: x = count_below_step(a, x, hi, key, 16); [[fallthrough]];
+      case 4: x = count_below_step(a, x, hi, key, 8); [[fallthrough]];
+      case 3: x = count_below_step(a, x, hi, key, 4); [[fallthrough]];
+      case 2: x = count_below_step(a, x, hi, key, 2); [[fallthrough]];
+      case 1: x = count_below_step(a, x, hi, key, 1); [[fallthrough]];
+      default: break;
+    }
+    return x;
   }
+  for (int step = 1 << (31 - __clz(span)); step; step >>= 1) x = count_below_step(a, x, hi, key, step);
   return x;
 }
 
@@ -319,6 +346,7 @@ struct MarkTile {
   static constexpr int D = T * E, NW = T / 32;
   static constexpr int kMaxHeads = D / HG + 4;
   static constexpr int NMB = D / 32;  // merge bitmap words of one tile
+  static constexpr int kMinBlocks = MARK_MIN_BLOCKS;
   static constexpr int64_t kStageBytes = align_up(int64_t(D + 4) * 8 + 160, 16);
   static constexpr int64_t kHeadsBytes = align_up(int64_t(kMaxHeads) * 4, 16);
   static constexpr int64_t kBitsBytes = align_up(int64_t(NMB) * 4, 16);
@@ -491,6 +519,7 @@ struct CompactTile {
   static constexpr int D = T * E, NW = T / 32, W = 32 * E;
   static constexpr int NMB = D / 32;       // merge bitmap words of one tile
   static constexpr int NCW = D / 32 + 4;   // C words of one tile, at most, and slack
+  static constexpr int kMinBlocks = 1;
   static constexpr int64_t kMBBytes = align_up(int64_t(NMB) * 4 + 16, 16);
   static constexpr int64_t kStageBytes = kMBBytes + align_up(int64_t(NCW + 8) * 4, 16);
   // per warp: refs (W words + alignment lead), ordinals (ord_A then ord_B,
