@@ -161,6 +161,44 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
+def host_info():
+    """Core count and CPU model of the host running the bench."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            txt = f.read()
+        for key in ("model name", "Model Name", "CPU part"):
+            for line in txt.splitlines():
+                if line.split(":")[0].strip() == key:
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+    except OSError:
+        pass
+    import platform
+    return {"cpu_count": os.cpu_count(), "cpu_model": model or platform.processor() or None,
+            "machine": platform.machine()}
+
+
+def build_info():
+    """How the library was built: nvcc flags, a digest of every kernel source
+    and the git commit when the tree is a checkout."""
+    from lsm_replacement_merge_gb300 import _build
+    h = hashlib.sha256()
+    for src in sorted(_build._deps()):
+        with open(src, "rb") as f:
+            h.update(f.read())
+    sha = None
+    try:
+        sha = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                             text=True, timeout=10).stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    flags = " ".join(_build.ARCH + _build.NVCC_FLAGS).replace(ROOT + os.sep, "")
+    return {"nvcc_flags": flags, "source_digest": h.hexdigest()[:16], "git_sha": sha}
+
+
 def ncu_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source changed since the counters were taken."""
@@ -232,7 +270,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "u64+u32", "data": "synthetic",
         "config": headline_config(m, n, None),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host_cores": os.cpu_count(),
+                         "cpu_model": host_info()["cpu_model"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -437,8 +476,10 @@ def main():
             oracle.merge(mi.A, mi.B, mi.Apay, mi.Bpay)
             t_cpu += time.perf_counter() - t0
             reps += 1
+        hi = host_info()
         cpu = {"value": reps * (m + n) / t_cpu / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "the whole 2^26 + 2^26 merge with payload, %d run(s)" % reps}
+               "sample": "the whole 2^26 + 2^26 merge with payload, %d run(s)" % reps,
+               "host_cores": hi["cpu_count"], "cpu_model": hi["cpu_model"]}
 
     sweep = None
     if args.sweep and rank == 0:
@@ -459,6 +500,7 @@ def main():
             sweep["%d,%d,%d" % cfg_e] = {"kernel_ms": kms, "gbs": alg_bytes / (kms * 1e-3) / 1e9}
         lsm.tune_merge(lsm.LSM_KEY_U64, *mcfg)
 
+    ws_bytes = ws.numel()
     del A, B, Ap, Bp, out_k, out_p, ws
     torch.cuda.empty_cache()
 
@@ -467,6 +509,27 @@ def main():
         workloads = extra_workloads(lsm, torch, dev, peak, args)
 
     launches = 2 * K  # partition + tile kernel per step
+    rep_roof = None
+    summary = {}
+    for name, w in workloads.items():
+        if isinstance(w, dict) and "ms_per_step" in w:
+            summary[name] = {k: w[k] for k in ("ms_per_step", "gelem_s", "gbs", "frac",
+                                               "frac_of_8TBs_nominal") if k in w}
+    rw = workloads.get("replace_u64_12M_4M")
+    if rw:
+        rep_roof = {"workload": "replacement merge, |A| = 12,000,000 + |B| = 4,000,000 uint64 "
+                                "keys, 25 % of B in A (refs-only outputs)",
+                    "call": rw.get("call"), "bound": "hbm", "ms_per_step": rw["ms_per_step"],
+                    "algorithmic_bytes": rw["algorithmic_bytes"], "achieved": rw["gbs"],
+                    "peak": peak, "unit": "GB/s", "frac": rw["frac"], "peak_source": peak_kind,
+                    "frac_of_8TBs_nominal": rw["frac_of_8TBs_nominal"],
+                    "target_frac_of_8TBs_nominal": 0.60,
+                    "kernel_ms_in_separate_calls": rw["separate_calls"]["kernel_ms"],
+                    "workspace_bytes": rw.get("workspace_bytes"), "traffic": None,
+                    "l2": rw.get("l2")}
+    if rank == 0 and workloads:
+        # the full per-workload record on its own line, before the result line
+        print(json.dumps({"workloads": workloads}), flush=True)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -479,11 +542,15 @@ def main():
                      "kernel_launches_timed": len(profiled),
                      "partition_ms": partition_ms,
                      "frac_of_8TBs_nominal": achieved / 8000.0},
+        "roofline_replacement": rep_roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
-        "workloads": workloads,
+        "workloads_summary": summary,
+        "workspace_bytes": {"merge_stable": ws_bytes},
+        "host": host_info(),
+        "build": build_info(),
     }
     if sweep:
         line["items_sweep"] = sweep
@@ -597,6 +664,7 @@ def extra_merge_sort(lsm, torch, dev, peak, steps, flush, out):
         "last_pass_tile_kernel_gbs": pass_bytes / (last * 1e-3) / 1e9,
         "last_pass_tile_kernel_frac": pass_bytes / (last * 1e-3) / 1e9 / peak,
         "gpu_launches_per_step": 1 + 2 * passes,
+        "workspace_bytes": {"merge_sort": ws.numel()},
         "l2": "flushed (256 MiB write) before every step; inputs 1.5 GiB"}
     del keys, pay, ok, op, ws
     torch.cuda.empty_cache()
@@ -793,6 +861,11 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
                                "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
                                "frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": per,
                                "gpu_launches_per_step": 7,
+                               "workspace_bytes": {"collision_mark_str": w1.numel(),
+                                                   "rank_build": w2.numel(),
+                                                   "replacement_merge_compact": w3.numel(),
+                                                   "fc_lengths_scan": w4.numel(),
+                                                   "prefix_tables": 8 * (pA.numel() + pB.numel())},
                                "l2": "flushed (256 MiB write) before every step"}
     # The byte profile in place of the bit profile: the same step with the
     # byte-FC lengths scan and emit.
