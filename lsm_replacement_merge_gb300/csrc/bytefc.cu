@@ -19,9 +19,10 @@
 //                          record length; the tile's total for the scan
 //   (scan)                 the FC pipeline's one-CTA tile scan and offsets
 //                          pass turn the lengths into byte offsets
-//   bytefc_emit_kernel     one thread per record writes its bytes at its
-//                          offset; records never share a byte, so no two
-//                          threads write the same address
+//   bytefc_emit_kernel     one CTA per 256 consecutive records: each thread
+//                          writes its record into a shared copy of their
+//                          contiguous byte span (records never share a
+//                          byte), one bulk store moves the aligned interior
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -80,16 +81,6 @@ __device__ __forceinline__ uint32_t leb_len(uint64_t x) {
   return n;
 }
 
-__device__ __forceinline__ uint64_t put_leb(uint8_t *out, uint64_t pos, uint64_t x) {
-  do {
-    uint8_t b = static_cast<uint8_t>(x & 0x7F);
-    x >>= 7;
-    if (x) b |= 0x80;
-    out[pos++] = b;
-  } while (x);
-  return pos;
-}
-
 __device__ __forceinline__ bool is_tomb(const BSource &src, uint32_t idx) {
   return src.tomb && ((__ldg(src.tomb + (idx >> 5)) >> (idx & 31)) & 1u);
 }
@@ -136,56 +127,6 @@ __global__ void __launch_bounds__(kBfThreads) bytefc_lengths_kernel(
   }
   const uint64_t total = block_sum<kBfThreads, uint64_t>(local, scratch);
   if (threadIdx.x == 0) tile_sum[blockIdx.x] = total;
-}
-
-__global__ void __launch_bounds__(256) bytefc_emit_kernel(
-    BSource sa, BSource sb, const uint32_t *__restrict__ refs, int64_t N, uint64_t W,
-    const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
-    const uint64_t *__restrict__ off, uint8_t *__restrict__ payload, int64_t nbytes,
-    int32_t *status) {
-  pdl_begin();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
-    const uint32_t r = __ldg(refs + i), idx = r & 0x7FFFFFFFu;
-    const BSource &src = bpick(sa, sb, r);
-    const uint64_t ks = __ldg(src.key.off + idx), K = __ldg(src.key.off + idx + 1) - ks;
-    const uint64_t p = __ldg(lcp + i), b = __ldg(ctrl + i);
-    uint64_t pos = __ldg(off + i);
-    const uint64_t end = __ldg(off + i + 1);
-    // a record whose offsets, lcp or control do not give exactly its own
-    // length (not the lengths pass's output for these inputs) is reported and
-    // not written, so that nothing lands outside [byte_off[i], byte_off[i+1])
-    const bool tomb = is_tomb(src, idx);
-    const uint64_t vlen = tomb ? 0 : __ldg(src.val.off + idx + 1) - __ldg(src.val.off + idx);
-    const uint64_t v = tomb ? 1 : (W ? W : 1 + leb_len(vlen) + vlen);
-    if (end > static_cast<uint64_t>(nbytes) || p > K || end < pos ||
-        leb_len(b) + leb_len(K - p) + (K - p) + v != end - pos || (W && (tomb || vlen + 1 != W))) {
-      report(status, LSM_ERR_ARG);
-      continue;
-    }
-    pos = put_leb(payload, pos, b);
-    pos = put_leb(payload, pos, K - p);
-    for (uint64_t t = p; t < K && pos < end; ++t) payload[pos++] = __ldg(src.key.arena + ks + t);
-    if (pos >= end) {  // no room left for the tag byte
-      report(status, LSM_ERR_ARG);
-      continue;
-    }
-    if (is_tomb(src, idx)) {
-      payload[pos++] = 0;
-    } else {
-      const uint64_t vs = __ldg(src.val.off + idx), vb = __ldg(src.val.off + idx + 1) - vs;
-      payload[pos++] = 1;
-      if (!W) {
-        if (pos + leb_len(vb) > end) {
-          report(status, LSM_ERR_ARG);
-          continue;
-        }
-        pos = put_leb(payload, pos, vb);
-      }
-      for (uint64_t t = 0; t < vb && pos < end; ++t) payload[pos++] = __ldg(src.val.arena + vs + t);
-    }
-    if (pos != end) report(status, LSM_ERR_ARG);
-  }
 }
 
 // Common encoded value width ("Pipeline": detected before the records are
@@ -244,6 +185,148 @@ __global__ void bytefc_width_finish_kernel(int64_t N, unsigned long long *acc) {
   acc[0] = (N > 0 && !acc[3] && acc[1] == acc[2]) ? 1 + acc[1] : 0;
 }
 
+// Record i's checked extent: its bytes [pos, end) when the offsets, lcp and
+// control give exactly its own length (the lengths pass's output for these
+// inputs and W); otherwise false (the record is reported and not written).
+struct RecordPlan {
+  uint64_t ks, K, p, b, vs, vlen, pos, end;
+  bool tomb;
+};
+
+__device__ __forceinline__ bool plan_record(const BSource &sa, const BSource &sb,
+                                            const uint32_t *__restrict__ refs,
+                                            const uint32_t *__restrict__ lcp,
+                                            const uint32_t *__restrict__ ctrl,
+                                            const uint64_t *__restrict__ off, int64_t i,
+                                            uint64_t W, RecordPlan &r, const BSource *&srcp) {
+  const uint32_t ref = __ldg(refs + i), idx = ref & 0x7FFFFFFFu;
+  const BSource &src = bpick(sa, sb, ref);
+  srcp = &src;
+  r.ks = __ldg(src.key.off + idx);
+  r.K = __ldg(src.key.off + idx + 1) - r.ks;
+  r.p = __ldg(lcp + i);
+  r.b = __ldg(ctrl + i);
+  r.pos = __ldg(off + i);
+  r.end = __ldg(off + i + 1);
+  r.tomb = is_tomb(src, idx);
+  r.vs = r.tomb ? 0 : __ldg(src.val.off + idx);
+  r.vlen = r.tomb ? 0 : __ldg(src.val.off + idx + 1) - r.vs;
+  const uint64_t v = r.tomb ? 1 : (W ? W : 1 + leb_len(r.vlen) + r.vlen);
+  return r.p <= r.K && r.end >= r.pos &&
+         leb_len(r.b) + leb_len(r.K - r.p) + (r.K - r.p) + v == r.end - r.pos &&
+         !(W && (r.tomb || r.vlen + 1 != W));
+}
+
+// Writes a planned record through `put(position, byte)`: LEB128(b),
+// LEB128(K - p), the key bytes [p, K) (read as aligned 8-byte words), the tag
+// byte, LEB128(value length) unless a common width W is given, the value
+// bytes.
+template <class Put>
+__device__ __forceinline__ void write_record(const BSource &src, const RecordPlan &r, uint64_t W,
+                                             const Put &put) {
+  uint64_t pos = r.pos;
+  auto leb = [&](uint64_t x) {
+    do {
+      uint8_t byte = static_cast<uint8_t>(x & 0x7F);
+      x >>= 7;
+      if (x) byte |= 0x80;
+      put(pos++, byte);
+    } while (x);
+  };
+  auto copy = [&](const uint8_t *arena, uint64_t from, uint64_t len) {
+    for (uint64_t t = 0; t < len; t += 8) {
+      const int need = len - t < 8 ? static_cast<int>(len - t) : 8;
+      const uint64_t w = bytes8_at(arena, from + t, need);
+      for (int q = 0; q < need; ++q) put(pos++, static_cast<uint8_t>(w >> (8 * q)));
+    }
+  };
+  leb(r.b);
+  leb(r.K - r.p);
+  copy(src.key.arena, r.ks + r.p, r.K - r.p);
+  put(pos++, r.tomb ? 0 : 1);
+  if (!r.tomb) {
+    if (!W) leb(r.vlen);
+    copy(src.val.arena, r.vs, r.vlen);
+  }
+}
+
+// One CTA per kBeRecords consecutive records: their bytes are one
+// contiguous span [s0, s1) of the payload. Each thread writes its record into
+// a shared copy of the span (records never share a byte), then the
+// 16-byte-aligned interior leaves with one bulk store and the at most 15
+// bytes at either end with plain stores. A span larger than the shared
+// buffer (very long keys or values) is written record by record straight to
+// global memory instead. A record whose extent does not match its fields is
+// reported (LSM_ERR_ARG) and its bytes in the span are zero.
+constexpr int kBeRecords = 256;
+constexpr int kBeBuf = 24 * 1024;
+
+__global__ void __launch_bounds__(kBeRecords) bytefc_emit_kernel(
+    BSource sa, BSource sb, const uint32_t *__restrict__ refs, int64_t N, uint64_t W,
+    const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
+    const uint64_t *__restrict__ off, uint8_t *__restrict__ payload, int64_t nbytes,
+    int32_t *status) {
+  pdl_begin();
+  __shared__ __align__(16) uint8_t buf[kBeBuf];
+  const int64_t R0 = static_cast<int64_t>(blockIdx.x) * kBeRecords;
+  const int64_t R1 = R0 + kBeRecords < N ? R0 + kBeRecords : N;
+  const int64_t i = R0 + threadIdx.x;
+  const uint64_t s0 = __ldg(off + R0), s1 = __ldg(off + R1);
+  // buf[0] mirrors the 16-byte boundary of the payload at or below s0, so
+  // that shared and global addresses agree modulo 16
+  const uint64_t pa = reinterpret_cast<uintptr_t>(payload);
+  const uint64_t base = s0 - ((pa + s0) & 15);
+  const bool staged = s1 >= s0 && s1 <= static_cast<uint64_t>(nbytes) &&
+                      s1 - base + 16 <= static_cast<uint64_t>(kBeBuf);
+  if (!staged) {
+    // record by record, straight to global memory
+    if (i < R1) {
+      RecordPlan r;
+      const BSource *src;
+      if (!plan_record(sa, sb, refs, lcp, ctrl, off, i, W, r, src) ||
+          r.end > static_cast<uint64_t>(nbytes)) {
+        report(status, LSM_ERR_ARG);
+      } else {
+        write_record(*src, r, W, [&](uint64_t q, uint8_t v) { payload[q] = v; });
+      }
+    }
+    return;
+  }
+  if (i < R1) {
+    RecordPlan r;
+    const BSource *src;
+    const bool ok = plan_record(sa, sb, refs, lcp, ctrl, off, i, W, r, src) && r.pos >= s0 &&
+                    r.end <= s1;
+    if (ok) {
+      write_record(*src, r, W, [&](uint64_t q, uint8_t v) { buf[q - base] = v; });
+    } else {
+      report(status, LSM_ERR_ARG);
+      // the record's bytes inside the span read as zero
+      const uint64_t a = r.pos < s0 ? s0 : (r.pos > s1 ? s1 : r.pos);
+      const uint64_t e = r.end > s1 ? s1 : (r.end < a ? a : r.end);
+      for (uint64_t q = a; q < e; ++q) buf[q - base] = 0;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  const uint64_t a0 = s0 + ((16 - ((pa + s0) & 15)) & 15), a1 = s1 - ((pa + s1) & 15);
+  if (a1 > a0) {
+    if (threadIdx.x == 0) {
+      bulk_s2g(payload + a0, buf + (a0 - base), static_cast<uint32_t>(a1 - a0));
+      bulk_commit();
+    }
+    // the bytes before a0 and from a1 on
+    const int head = static_cast<int>(a0 - s0), tail = static_cast<int>(s1 - a1);
+    const int t = threadIdx.x - 1;
+    if (t >= 0 && t < head) payload[s0 + t] = buf[s0 + t - base];
+    if (t >= 16 && t < 16 + tail) payload[a1 + (t - 16)] = buf[a1 + (t - 16) - base];
+  } else {
+    const int t = threadIdx.x;
+    for (uint64_t q = s0 + t; q < s1; q += blockDim.x) payload[q] = buf[q - base];
+  }
+  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 BSource bsource(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb) {
   return BSource{key, val, tomb};
 }
@@ -291,12 +374,10 @@ cudaError_t launch_bytefc_emit(const lsm_fc_input &in, const uint32_t *refs, int
                                const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
                                uint8_t *payload, int64_t nbytes, int32_t *status, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  int64_t blocks = (N + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-  if (blocks > cap && cap > 0) blocks = cap;
+  const int64_t blocks = (N + kBeRecords - 1) / kBeRecords;
   profile_before(s);
   const cudaError_t err = launch_kernel(false, bytefc_emit_kernel, static_cast<unsigned>(blocks),
-                                        256, 0, s, bsource(in.keyA, in.valA, in.tombA),
+                                        kBeRecords, 0, s, bsource(in.keyA, in.valA, in.tombA),
                                         bsource(in.keyB, in.valB, in.tombB), refs, N, W, lcp, ctrl,
                                         byte_off, payload, nbytes, status);
   profile_after(s);
