@@ -117,7 +117,7 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n, int key_type = LSM_KEY_U64) {
       c.take<uint64_t>(rank_build_ctas(m));
       break;
     case LSM_OP_RANK2048_BUILD:
-      c.take<uint32_t>(rank2048_build_ctas(m));
+      c.take<uint64_t>(rank2048_build_ctas(m));
       break;
     case LSM_OP_REPLACEMENT_FUSED: {
       const int64_t G = (m + n + fused_tile() - 1) / fused_tile();
@@ -384,8 +384,8 @@ LSM_API int lsm_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint
   if ((C && !aligned16(C)) || !aligned8(dir) || !aligned8(epochs)) return LSM_ERR_ALIGN;
   if (int r = check_ws(LSM_OP_RANK2048_BUILD, m, 0, ws, ws_bytes)) return r;
   Carver c{static_cast<uint8_t *>(ws)};
-  uint32_t *totals = c.take<uint32_t>(rank2048_build_ctas(m));
-  return cuda_status(launch_rank2048_build(C, m, dir, epochs, d_total, totals,
+  uint64_t *scratch = c.take<uint64_t>(rank2048_build_ctas(m));
+  return cuda_status(launch_rank2048_build(C, m, dir, epochs, d_total, scratch, status_ptr(),
                                            static_cast<cudaStream_t>(stream)));
 }
 
@@ -508,9 +508,10 @@ LSM_API int lsm_replacement_merge_compact_rank2048(int64_t m, int64_t n, const u
   Carver c{static_cast<uint8_t *>(ws)};
   const int64_t D = replace_min_tile();
   int64_t *part = c.take<int64_t>((m + n + D - 1) / D + 1);
-  return cuda_status(launch_compact_rank2048(m, n, C, dir, epochs, lb_B, out_refs, ord_A, ord_B,
-                                             d_count, part, status_ptr(),
-                                             static_cast<cudaStream_t>(stream)));
+  uint32_t *mb = c.take<uint32_t>(merge_bitmap_words(m + n));
+  return cuda_status(launch_compact_tiles_rank2048(m, n, C, dir, epochs, lb_B, mb, part, out_refs,
+                                                   ord_A, ord_B, d_count, status_ptr(),
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_replacement_materialize(const uint64_t *A, const uint32_t *Aval,

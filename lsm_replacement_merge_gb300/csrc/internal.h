@@ -63,6 +63,13 @@ cudaError_t launch_compact_tiles(int64_t m, int64_t n, const uint32_t *C, const 
                                  int64_t *part_scratch, uint32_t *refs, uint32_t *ord_A,
                                  uint32_t *ord_B, int64_t *d_count, int32_t *status,
                                  cudaStream_t s);
+// The same compaction reading R(i) from the rank2048 directory (co-ranks
+// and merge bitmap from lb_B; part_scratch G + 1, MB merge_bitmap_words).
+cudaError_t launch_compact_tiles_rank2048(int64_t m, int64_t n, const uint32_t *C,
+                                          const uint64_t *dir, const uint64_t *epochs,
+                                          const uint32_t *lb_B, uint32_t *MB, int64_t *part_scratch,
+                                          uint32_t *refs, uint32_t *ord_A, uint32_t *ord_B,
+                                          int64_t *d_count, int32_t *status, cudaStream_t s);
 // The whole path (mark, rank512 build, compaction). part_m, part_c: G + 1
 // each; MB: merge_bitmap_words(m + n); rank_ws: rank_build_ctas(m) uint64.
 cudaError_t launch_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
@@ -94,11 +101,6 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
                            const uint32_t *lb_B, uint32_t *refs, uint32_t *ord_A,
                            uint32_t *ord_B, int64_t *d_count, int64_t *part_i,
                            uint32_t *mb_scratch, int32_t *status, cudaStream_t s);
-// The compaction reading R(i) from the rank2048 directory (default tile shape).
-cudaError_t launch_compact_rank2048(int64_t m, int64_t n, const uint32_t *C, const uint64_t *dir,
-                                    const uint64_t *epochs, const uint32_t *lb_B, uint32_t *refs,
-                                    uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
-                                    int64_t *part_i, int32_t *status, cudaStream_t s);
 int64_t rank_build_ctas(int64_t m);
 // The fused pass: collision bits, lb_B, ordinals, refs and the count in one
 // tile pipeline. part_i: ceil((m+n)/fused_tile()) + 1 int64; state: as many
@@ -111,9 +113,10 @@ cudaError_t launch_replacement_fused(const uint64_t *A, int64_t m, const uint64_
 
 // --- rank2048.cu ---
 int64_t rank2048_build_ctas(int64_t m);
-// cta_totals: rank2048_build_ctas(m) uint32 of scratch.
+// ws: rank2048_build_ctas(m) uint64 of scratch (lookback states, or the
+// per-CTA totals of the two-launch form).
 cudaError_t launch_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs,
-                                  int64_t *d_total, uint32_t *cta_totals, cudaStream_t s);
+                                  int64_t *d_total, uint64_t *ws, int32_t *status, cudaStream_t s);
 cudaError_t launch_rank2048_query(const uint32_t *C, const uint64_t *dir, const uint64_t *epochs,
                                   int64_t m, const uint64_t *pos, int64_t q, uint64_t *out,
                                   int32_t *status, cudaStream_t s);

@@ -1,0 +1,66 @@
+// lookback.cuh -- decoupled lookback over per-CTA aggregates (device side).
+//
+// CTA t publishes its aggregate in state[t], then walks back over its
+// predecessors' states, 32 at a time (one per lane of warp 0), summing
+// aggregates until it meets an inclusive prefix; it then publishes its own
+// inclusive prefix. A state word is epoch << 32 | inclusive << 31 | value
+// (31-bit values): a word from another call carries another epoch and reads
+// as "not yet published", so the states need no clearing pass. Every CTA a
+// wait depends on must be resident (callers launch only as many CTAs as fit
+// at once); each wait is bounded in time, after which the missing aggregate
+// counts as zero and LSM_ERR_TIMEOUT is recorded.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace lsm {
+
+// Called by the 32 lanes of warp 0 of CTA t; returns the sum of the
+// aggregates of CTAs 0 .. t-1 (in every lane).
+__device__ __forceinline__ uint32_t lookback_exclusive(uint64_t *state, uint32_t t, uint32_t agg,
+                                                       uint32_t epoch, int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t tag = static_cast<uint64_t>(epoch) << 32;
+  if (t == 0) {
+    if (lane == 0) st_relaxed_u64(state, tag | (1ull << 31) | agg);
+    return 0;
+  }
+  if (lane == 0) st_relaxed_u64(state + t, tag | agg);
+  uint32_t prefix = 0;
+  int64_t base = static_cast<int64_t>(t) - 1;
+  const uint64_t t0 = globaltimer_ns();
+  bool late = false;
+  for (;;) {
+    const int64_t idx = base - lane;
+    uint64_t v = idx >= 0 ? ld_relaxed_u64(state + idx) : (tag | (1ull << 31));
+    uint32_t polls = 0;
+    while (!__all_sync(0xffffffffu, (v >> 32) == epoch)) {
+      if ((v >> 32) != epoch) v = ld_relaxed_u64(state + idx);
+      if ((++polls & 31) == 0 &&
+          __any_sync(0xffffffffu, globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs))) {
+        late = true;
+        if ((v >> 32) != epoch) v = tag | (1ull << 31);  // give up: count it as zero
+      }
+    }
+    const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 31) & 1u);
+    uint32_t c = static_cast<uint32_t>(v & 0x7FFFFFFFu);
+    if (inc) {
+      const int first = __ffs(inc) - 1;
+      c = lane <= first ? c : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    prefix += c;
+    if (inc) break;
+    base -= 32;
+  }
+  if (lane == 0) {
+    if (late) report(status, LSM_ERR_TIMEOUT);
+    st_relaxed_u64(state + t, tag | (1ull << 31) | ((prefix + agg) & 0x7FFFFFFFu));
+  }
+  return prefix;
+}
+
+}  // namespace lsm

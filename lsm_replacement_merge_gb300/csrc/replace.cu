@@ -49,9 +49,9 @@
 #include <mutex>
 
 #include "common.cuh"
-#include "rank2048.cuh"
 #include "rank512.cuh"
 #include "internal.h"
+#include "lookback.cuh"
 #include "pipeline.cuh"
 
 namespace lsm {
@@ -193,19 +193,12 @@ __global__ void __launch_bounds__(kRankThreads) rank_finish_kernel(const uint32_
   if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) *d_total = static_cast<int64_t>(prefix) + cta_sum;
 }
 
-// The rank layouts the compaction reads R(i) from: the 512-bit directory
-// above, or the 2048-bit one ("Temporary rank layouts" names both; "Suggested
-// separate modes" compares them inside the whole pipeline).
+// The rank layout the earlier compaction reads R(i) from: the 512-bit
+// directory above.
 struct Rank512Dir {
   const uint32_t *dir;
   __device__ __forceinline__ uint64_t at(const uint32_t *__restrict__ C, int64_t p) const {
     return rank512_at(C, dir, p);
-  }
-};
-struct Rank2048Dir {
-  const uint64_t *dir, *epochs;
-  __device__ __forceinline__ uint64_t at(const uint32_t *__restrict__ C, int64_t p) const {
-    return rank2048_at(C, dir, epochs, p);
   }
 };
 
@@ -317,49 +310,8 @@ __global__ void __launch_bounds__(kRankThreads) rank_single_kernel(const uint32_
   uint32_t agg;
   const uint32_t excl = block_exclusive_sum<kRankThreads>(b < nblk ? tot : 0u, scratch, &agg);
   if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const uint64_t tag = static_cast<uint64_t>(epoch) << 32;
-    uint32_t prefix = 0;
-    if (t == 0) {
-      if (lane == 0) st_relaxed_u64(state, tag | (1ull << 31) | agg);
-    } else {
-      if (lane == 0) st_relaxed_u64(state + t, tag | agg);
-      int64_t base = static_cast<int64_t>(t) - 1;
-      const uint64_t t0 = globaltimer_ns();
-      bool late = false;
-      for (;;) {
-        const int64_t idx = base - lane;
-        uint64_t v = idx >= 0 ? ld_relaxed_u64(state + idx) : (tag | (1ull << 31));
-        uint32_t polls = 0;
-        while (!__all_sync(0xffffffffu, (v >> 32) == epoch)) {
-          if ((v >> 32) != epoch) v = ld_relaxed_u64(state + idx);
-          if ((++polls & 31) == 0 &&
-              __any_sync(0xffffffffu, globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs))) {
-            late = true;
-            if ((v >> 32) != epoch) v = tag | (1ull << 31);  // give up: count it as zero
-          }
-        }
-        const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 31) & 1u);
-        if (inc) {
-          const int first = __ffs(inc) - 1;
-          uint32_t c = lane <= first ? static_cast<uint32_t>(v & 0x7FFFFFFFu) : 0u;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-          prefix += c;
-          break;
-        }
-        uint32_t c = static_cast<uint32_t>(v & 0x7FFFFFFFu);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        prefix += c;
-        base -= 32;
-      }
-      if (lane == 0) {
-        if (late) report(status, LSM_ERR_TIMEOUT);
-        st_relaxed_u64(state + t, tag | (1ull << 31) | ((prefix + agg) & 0x7FFFFFFFu));
-      }
-    }
-    if (lane == 0) s_prefix = prefix;
+    const uint32_t prefix = lookback_exclusive(state, t, agg, epoch, status);
+    if (threadIdx.x == 0) s_prefix = prefix;
   }
   __syncthreads();
   const uint32_t prefix = s_prefix;
@@ -1339,16 +1291,6 @@ cudaError_t launch_compact(int64_t m, int64_t n, const uint32_t *C, const uint32
   }
 }
 
-// The same compaction reading R(i) from the rank2048 directory; the tile
-// shape is the default compaction variant's.
-cudaError_t launch_compact_rank2048(int64_t m, int64_t n, const uint32_t *C, const uint64_t *dir,
-                                    const uint64_t *epochs, const uint32_t *lb_B, uint32_t *refs,
-                                    uint32_t *ord_A, uint32_t *ord_B, int64_t *d_count,
-                                    int64_t *part_i, int32_t *status, cudaStream_t s) {
-  const Rank2048Dir rank{dir, epochs};
-  return launch_compact_variant<0>(m, n, C, rank, lb_B, refs, ord_A, ord_B, d_count, part_i,
-                                   status, s);
-}
 
 }  // namespace lsm
 

@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
+#include "rank2048.cuh"
 #include "rank512.cuh"
 
 // Minimum resident CTAs per SM the mark kernel is compiled for (register
@@ -775,6 +776,12 @@ struct Rank512At {
     return rank512_at(C, dir, p);
   }
 };
+struct Rank2048At {
+  const uint64_t *dir, *epochs;
+  __device__ __forceinline__ uint64_t at(const uint32_t *__restrict__ C, int64_t p) const {
+    return rank2048_at(C, dir, epochs, p);
+  }
+};
 
 // Lanes per diagonal of the co-rank partition. Measured on the 12M + 4M
 // step: 8 lanes 98.5 us, 16 lanes 100.5 us, 32 lanes 102.5 us (more lanes cut
@@ -794,6 +801,7 @@ constexpr int kTileT = 256, kTileE = 15, kMarkS = 2, kMarkHG = 8;
 constexpr int kCompactT = 128, kCompactE = 30, kCompactS = 4;
 using MarkDefault = MarkTile<kTileT, kTileE, kMarkS, kMarkHG>;
 using CompactDefault = CompactTile<kCompactT, kCompactE, kCompactS, Rank512At>;
+using Compact2048 = CompactTile<kCompactT, kCompactE, kCompactS, Rank2048At>;
 static_assert(MarkDefault::D == CompactDefault::D, "the compaction reuses the mark's diagonals");
 
 }  // namespace
@@ -823,12 +831,13 @@ cudaError_t launch_mark_tiles(const uint64_t *A, int64_t m, const uint64_t *B, i
   return err;
 }
 
-cudaError_t launch_compact_tiles(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
-                                 const uint32_t *lb_B, uint32_t *MB, const int64_t *part_c,
-                                 int64_t *part_scratch, uint32_t *refs, uint32_t *ord_A,
-                                 uint32_t *ord_B, int64_t *d_count, int32_t *status,
-                                 cudaStream_t s) {
-  constexpr int64_t D = CompactDefault::D;
+template <class Spec, class RD>
+cudaError_t launch_compact_with(int64_t m, int64_t n, const uint32_t *C, RD rank,
+                                const uint32_t *lb_B, uint32_t *MB, const int64_t *part_c,
+                                int64_t *part_scratch, uint32_t *refs, uint32_t *ord_A,
+                                uint32_t *ord_B, int64_t *d_count, int32_t *status,
+                                cudaStream_t s) {
+  constexpr int64_t D = Spec::D;
   const int64_t G = (m + n + D - 1) / D;
   if (G == 0) return launch_kernel(false, set_count_kernel2, 1, 1, 0, s, d_count, int64_t(0));
   if (!part_c) {
@@ -848,12 +857,29 @@ cudaError_t launch_compact_tiles(int64_t m, int64_t n, const uint32_t *C, const 
     if (err != cudaSuccess) return err;
     part_c = part_scratch;
   }
-  typename CompactDefault::Params p{m, n, G, C, Rank512At{dir}, MB, part_c, refs, ord_A, ord_B,
-                                    d_count};
+  typename Spec::Params p{m, n, G, C, rank, MB, part_c, refs, ord_A, ord_B, d_count};
   profile_before(s);
-  const cudaError_t err = launch_warp_pipeline<CompactDefault>(p, G, status, s);
+  const cudaError_t err = launch_warp_pipeline<Spec>(p, G, status, s);
   profile_after(s);
   return err;
+}
+
+cudaError_t launch_compact_tiles(int64_t m, int64_t n, const uint32_t *C, const uint32_t *dir,
+                                 const uint32_t *lb_B, uint32_t *MB, const int64_t *part_c,
+                                 int64_t *part_scratch, uint32_t *refs, uint32_t *ord_A,
+                                 uint32_t *ord_B, int64_t *d_count, int32_t *status,
+                                 cudaStream_t s) {
+  return launch_compact_with<CompactDefault>(m, n, C, Rank512At{dir}, lb_B, MB, part_c,
+                                             part_scratch, refs, ord_A, ord_B, d_count, status, s);
+}
+
+cudaError_t launch_compact_tiles_rank2048(int64_t m, int64_t n, const uint32_t *C,
+                                          const uint64_t *dir, const uint64_t *epochs,
+                                          const uint32_t *lb_B, uint32_t *MB, int64_t *part_scratch,
+                                          uint32_t *refs, uint32_t *ord_A, uint32_t *ord_B,
+                                          int64_t *d_count, int32_t *status, cudaStream_t s) {
+  return launch_compact_with<Compact2048>(m, n, C, Rank2048At{dir, epochs}, lb_B, MB, nullptr,
+                                          part_scratch, refs, ord_A, ord_B, d_count, status, s);
 }
 
 // The whole path: partition + mark (which also writes the merge bitmap and
