@@ -287,7 +287,11 @@ LSM_API int lsm_rank2048_query(const uint32_t *C, const uint64_t *dir, const uin
  *   ord_B[j]        j + lb_B[j] - R(lb_B[j])
  *   d_count[0]      N
  * The keys themselves are not read: B_j precedes A_i in the merge exactly
- * when lb_B[j] <= i, so the merge path runs over positions.
+ * when lb_B[j] <= i, so the merge path runs over positions: B_j sits at
+ * position j + lb_B[j] of the merge with B first on ties, and the call marks
+ * those positions in a bitmap in its workspace (a lb_B that is not
+ * nondecreasing with values <= m records LSM_ERR_ARG) before the tiles read
+ * it.
  * out_refs: device uint32[m + n] capacity; ord_A: uint32[m]; ord_B:
  * uint32[n]; d_count: int64[1]; C, lb_B, out_refs, ord_A and ord_B 16-byte
  * aligned. m, n < 2^31. */
@@ -403,9 +407,16 @@ LSM_API int lsm_fc_lengths_scan(const lsm_fc_input *in, const uint32_t *refs, in
                                 uint64_t *bit_off, void *ws, size_t ws_bytes, void *stream);
 
 /* ---- a7: word-owned payload emit ------------------------------------------ */
-/* [GC], the paragraphs on exact lengths and on the record layout: one thread
- * owns each 32-bit payload word, gathers its bits from the records that
- * overlap it and writes it once. Record i occupies bits [bit_off[i],
+/* [GC], the paragraphs on exact lengths and on the record layout, and the
+ * word-owned emit: each final 32-bit payload word is written to global
+ * memory exactly once, by its owner. The owner is a CTA rather than a
+ * thread: each CTA owns contiguous runs of 4096 payload words, composes a
+ * run in shared memory with one thread per record (fields written into the
+ * run's words, words that two fields or records share combined with a
+ * shared-memory OR) and moves the finished run to global memory with one
+ * bulk store. Measured on the 4M + 4M string workload: one thread per
+ * output word gathering its bits took 1130 us, this form 335 us. Record i
+ * occupies bits [bit_off[i],
  * bit_off[i+1]) as EG0(c_i) EG0(k_i - l_i) key bits [l_i, k_i) value, value
  * = 0 for a tombstone, else 1 EG0(byte length) bytes; EG0(x) is
  * floor(log2(x+1)) zero bits followed by x+1 in binary. Stream bit t is bit
@@ -458,9 +469,14 @@ LSM_API int lsm_bytefc_value_width(const lsm_fc_input *in, const uint32_t *refs,
                                    uint64_t *d_width, void *stream);
 
 /* Writes the payload: record i's bytes at [byte_off[i], byte_off[i+1]) of
- * payload (device, nbytes >= byte_off[N]); bytes past byte_off[N] are not
- * written. lcp, ctrl, byte_off: lsm_bytefc_lengths_scan's outputs for the
- * same inputs and W. One thread per record. */
+ * payload (device, nbytes >= byte_off[N], any alignment); bytes past
+ * byte_off[N] are not written. lcp, ctrl, byte_off: lsm_bytefc_lengths_scan's
+ * outputs for the same inputs and W. Each CTA takes 256 consecutive records,
+ * whose bytes form one contiguous span: one thread per record composes it in
+ * shared memory (records never share a byte) and the span leaves with one
+ * bulk store plus at most 15 plain bytes at either end. A record whose
+ * offsets, lcp or control do not give exactly its own length records
+ * LSM_ERR_ARG; its bytes read as zero. */
 LSM_API int lsm_bytefc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N, uint64_t W,
                             const uint32_t *lcp, const uint32_t *ctrl, const uint64_t *byte_off,
                             uint8_t *payload, int64_t nbytes, void *stream);
@@ -545,11 +561,12 @@ LSM_API int lsm_tune_merge(int key_type, int items_per_thread, int stages, int o
  * cudaEvent_t handles owned by the caller. */
 LSM_API int lsm_set_profile_events(void *start_event, void *stop_event);
 
-/* Selects the tile variant of lsm_collision_mark (kernel 0) or
- * lsm_replacement_merge_compact (kernel 1): threads per CTA and items per
- * thread, from the compiled set (256,11) (128,23) (256,23) (512,11).
- * Process-wide; the defaults are (512,11) for kernel 0 and (256,11) for
- * kernel 1. */
+/* Selects how lsm_collision_mark (kernel 0) or
+ * lsm_replacement_merge_compact (kernel 1) run: (0, 0) selects the warp
+ * pipelines that lsm_replacement_merge also uses (the default); threads per
+ * CTA and items per thread from the set (256,11) (128,23) (256,23) (512,11)
+ * select the earlier block-synchronous tile pipelines, kept for comparison.
+ * Process-wide. */
 LSM_API int lsm_tune_replace(int kernel, int threads, int items_per_thread);
 
 /* ---- test hook ------------------------------------------------------------ */

@@ -10,8 +10,11 @@
 //     (x+1)) + 1, so the record length is E(c_i) + E(k_i - l_i) + (k_i - l_i)
 //     + v_i; bits MSB first, no padding between records;
 //   - exact length scans into bit offsets (no independently encoded chunks,
-//     no FC reset at a cut), and one invocation per final 32-bit word that
-//     gathers its bits and writes the word once; unused final bits are zero.
+//     no FC reset at a cut), and a word-owned emit that writes every final
+//     32-bit word once; unused final bits are zero. Here the owner of a word
+//     is the CTA that owns its run (below), not one thread per word: the
+//     thread-per-word gather measured 1130 us on the 4M + 4M strings, the
+//     run composition 335 us.
 // EG0(x) is the order-0 Exp-Golomb code word: floor(log2(x+1)) zero bits,
 // then x+1 in binary; as a number of E(x) bits it is simply x + 1.
 //
