@@ -704,11 +704,16 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
               ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
                   m, n, C, dir_, lb, refs, oa, ob, cnt, w3))]
     # The step: the whole path in one call (partition + mark, rank512 build,
-    # compaction on the mark's diagonals); every output of the three calls.
+    # compaction on the mark's diagonals): C, dir, R(m), refs, ordinals and
+    # the count; the lower bounds are scratch on this path and not written.
     whole = [("replacement_merge", lambda: lsm.replacement_merge(
-        A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w6))]
+        A, B, C, None, dir_, tot, refs, oa, ob, cnt, w6, want_lb=False))]
     ms, per_whole = time_pipeline(torch, whole, steps, flush)
     N = int(cnt.item())
+    # the same call also writing lb_B (every output of the three calls)
+    whole_lb = [("replacement_merge", lambda: lsm.replacement_merge(
+        A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w6))]
+    ms_lb, _ = time_pipeline(torch, whole_lb, steps, flush)
     # the same work as three separate calls: per-kernel times (each call's
     # main pipeline bracketed by events) and the step with one more partition
     ms_sep, per = time_pipeline(torch, stages, steps, flush)
@@ -723,6 +728,8 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
                  "frac_of_8TBs_nominal": alg / (ms * 1e-3) / 1e9 / 8000.0,
                  "call": "lsm_replacement_merge", "gpu_launches_per_step": 4,
                  "mark_pipeline_ms": per_whole["replacement_merge"],
+                 "lb_B": "scratch, not written",
+                 "with_lb_B_written": {"ms_per_step": ms_lb},
                  "workspace_bytes": {"replacement_merge": w6.numel()},
                  "separate_calls": {"ms_per_step": ms_sep, "kernel_ms": per,
                                     "gpu_launches_per_step": 5,

@@ -310,7 +310,9 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
  * ([CB] "The three experimental paths", third path), with the compaction's
  * tiles on the mark's diagonals, so that the mark hands the compaction its
  * co-ranks and no second partition is needed. Arguments, alignment and
- * limits as those three calls; C needs no clearing. ws: at least
+ * limits as those three calls; C needs no clearing. lb_B may be null: the
+ * lower bounds are scratch on this path (the compaction reads the merge
+ * bitmap), and a null lb_B leaves them unwritten. ws: at least
  * lsm_workspace_size(LSM_OP_REPLACEMENT_MERGE, 0, m, n) bytes. */
 LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                   uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,

@@ -475,14 +475,15 @@ def replacement_merge_compact(m: int, n: int, C, dir_, lb_B, refs=None, ord_A=No
 
 
 def replacement_merge(A, B, C=None, lb_B=None, dir_=None, d_total=None, refs=None,
-                      ord_A=None, ord_B=None, d_count=None, ws=None, stream=None):
+                      ord_A=None, ord_B=None, d_count=None, ws=None, stream=None, want_lb=True):
     """The whole path in one call (lsm_replacement_merge). Returns (C, lb_B,
-    dir, d_total, refs, ord_A, ord_B, d_count)."""
+    dir, d_total, refs, ord_A, ord_B, d_count); with want_lb=False and no
+    lb_B given the lower bounds are not written and lb_B is None."""
     m, n = A.numel(), B.numel()
     dev = A.device
     if C is None:
         C = _empty(max((m + 31) // 32, 4), torch.uint32, dev)
-    if lb_B is None:
+    if lb_B is None and want_lb:
         lb_B = _empty(n, torch.uint32, dev)
     if dir_ is None:
         dir_ = _empty(3 * (m // 512 + 1), torch.uint32, dev)
@@ -501,9 +502,9 @@ def replacement_merge(A, B, C=None, lb_B=None, dir_=None, d_total=None, refs=Non
     _check("lsm_replacement_merge",
            lib().lsm_replacement_merge(
                _ptr(A) if m else None, m, _ptr(B) if n else None, n, _ptr(C) if m else None,
-               _ptr(lb_B) if n else None, _ptr(dir_), _ptr(d_total), _ptr(refs),
-               _ptr(ord_A) if m else None, _ptr(ord_B) if n else None, _ptr(d_count), _ptr(ws),
-               ws.numel(), _stream(stream)))
+               _ptr(lb_B) if (n and lb_B is not None) else None, _ptr(dir_), _ptr(d_total),
+               _ptr(refs), _ptr(ord_A) if m else None, _ptr(ord_B) if n else None, _ptr(d_count),
+               _ptr(ws), ws.numel(), _stream(stream)))
     return C, lb_B, dir_, d_total, refs, ord_A, ord_B, d_count
 
 

@@ -425,7 +425,8 @@ LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *
                                   uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
                                   int64_t *d_count, void *ws, size_t ws_bytes, void *stream) {
   if (m < 0 || n < 0 || !dir || !d_total || !d_count) return LSM_ERR_ARG;
-  if ((m && (!A || !C || !ord_A)) || (n && (!B || !lb_B || !ord_B)) || (m + n && !out_refs))
+  // lb_B may be null here: the compaction reads the merge bitmap, not lb_B
+  if ((m && (!A || !C || !ord_A)) || (n && (!B || !ord_B)) || (m + n && !out_refs))
     return LSM_ERR_ARG;
   if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
   for (const void *p : {static_cast<const void *>(A), static_cast<const void *>(B),

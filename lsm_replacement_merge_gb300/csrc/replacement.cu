@@ -48,9 +48,11 @@
 #include "rank512.cuh"
 
 // Minimum resident CTAs per SM the mark kernel is compiled for (register
-// budget); 1 leaves the choice to the compiler.
+// budget). Measured on the 12M + 4M step (whole path, L2 flushed by a write
+// before each step, medians of 50): 3 CTAs (72 registers, no spills) 89.8
+// us against 91.8 us for 2 (94 registers) and for the compiler's choice (96).
 #ifndef MARK_MIN_BLOCKS
-#define MARK_MIN_BLOCKS 1
+#define MARK_MIN_BLOCKS 3
 #endif
 
 namespace lsm {
@@ -306,6 +308,34 @@ __device__ __forceinline__ int count_below(const uint64_t *a, int lo, int hi, ui
   return x;
 }
 
+// Two independent count_below searches stepped together (the same number of
+// steps, from the larger span), so that each step's two shared loads and
+// compares overlap instead of forming one chain per key.
+__device__ __forceinline__ void count_below2(const uint64_t *a, int &x0, int hi0, uint64_t key0,
+                                             int &x1, int hi1, uint64_t key1, int span) {
+  if (span < 64) {
+    const int k = span ? 32 - __clz(span) : 0;
+    switch (k) {
+#define LSM_CB2_STEP(s)                                  \
+  x0 = count_below_step(a, x0, hi0, key0, s);            \
+  x1 = count_below_step(a, x1, hi1, key1, s);
+      case 6: LSM_CB2_STEP(32) [[fallthrough]];
+      case 5: LSM_CB2_STEP(16) [[fallthrough]];
+      case 4: LSM_CB2_STEP(8) [[fallthrough]];
+      case 3: LSM_CB2_STEP(4) [[fallthrough]];
+      case 2: LSM_CB2_STEP(2) [[fallthrough]];
+      case 1: LSM_CB2_STEP(1) [[fallthrough]];
+      default: break;
+#undef LSM_CB2_STEP
+    }
+    return;
+  }
+  for (int step = 1 << (31 - __clz(span)); step; step >>= 1) {
+    x0 = count_below_step(a, x0, hi0, key0, step);
+    x1 = count_below_step(a, x1, hi1, key1, step);
+  }
+}
+
 // The first x in [lo, hi] at which a monotone predicate (true, then false)
 // turns false, found by 16 lanes together: each round the half-warp tests
 // the 16 pivots lo + (l span) / 16 (l = 0..15) and keeps the gap between the
@@ -465,33 +495,47 @@ struct MarkTile {
       return false;
     }
     if (r > 0) flush_bits(p, g - static_cast<int64_t>(gridDim.x), work, r - 1);
-    // 2. every B key between its group's heads; lb_B straight to global
-    //    memory (32 consecutive words per warp), collisions by atomic OR
+    // 2. every B key between its group's heads, two keys per lane (b and
+    //    b + 32) searched together; lb_B straight to global memory (32
+    //    consecutive words per warp and key slot) unless the caller wants
+    //    none, collisions by atomic OR
     const uint32_t base = static_cast<uint32_t>(d.i0 - d.hp);
     const uint32_t jbase = static_cast<uint32_t>(d.j0);
-    uint32_t *lbo = p.lb_B + d.j0;
-    for (int b0 = warp * 32; b0 < nb; b0 += NW * 32) {
-      const int bi = b0 + lane;
-      const bool act = bi < nb;
-      const uint64_t key = sB[act ? bi : nb - 1];
-      const int h = bi / HG;
-      const int lo = act ? heads[h] : 0, hi = act ? heads[h + 1] : 0;
-      const int span = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(hi - lo)));
-      const int x = count_below(sAx, lo, hi, key, span);
-      if (act) {
-        lbo[bi] = base + static_cast<uint32_t>(x);
-        if (x < lenx && sAx[x] == key) {
-          const uint32_t ia = base + static_cast<uint32_t>(x);
-          atomicOr(p.C + (ia >> 5), 1u << (ia & 31));
-        }
+    uint32_t *lbo = p.lb_B ? p.lb_B + d.j0 : nullptr;
+    // the tile-relative position of B key bi with lower bound base + x in the
+    // merge with B first on ties is jbase + bi + base + x - k0; this tile
+    // owns positions [k0, k0 + D) (B[j0] falls at k0 - 1, in the previous
+    // tile, when it equals A[i0-1])
+    const uint32_t rbase = jbase + base - static_cast<uint32_t>(k0);
+    for (int b0 = warp * 64; b0 < nb; b0 += NW * 64) {
+      const int bi0 = b0 + lane, bi1 = bi0 + 32;
+      const bool act0 = bi0 < nb, act1 = bi1 < nb;
+      const uint64_t key0 = sB[act0 ? bi0 : nb - 1], key1 = sB[act1 ? bi1 : nb - 1];
+      const int h0 = bi0 / HG, h1 = bi1 / HG;
+      int x0 = act0 ? heads[h0] : 0, x1 = act1 ? heads[h1] : 0;
+      const int hi0 = act0 ? heads[h0 + 1] : 0, hi1 = act1 ? heads[h1 + 1] : 0;
+      const int sp = (hi0 - x0) > (hi1 - x1) ? (hi0 - x0) : (hi1 - x1);
+      const int span = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(sp)));
+      count_below2(sAx, x0, hi0, key0, x1, hi1, key1, span);
+      const bool hit0 = act0 && x0 < lenx && sAx[x0] == key0;
+      const bool hit1 = act1 && x1 < lenx && sAx[x1] == key1;
+      if (lbo) {
+        if (act0) lbo[bi0] = base + static_cast<uint32_t>(x0);
+        if (act1) lbo[bi1] = base + static_cast<uint32_t>(x1);
       }
-      // merge bitmap: B_j sits at position j + lb_B[j] of the merge with B
-      // first on ties; this tile owns positions [k0, k0 + D) (B[j0] falls at
-      // k0 - 1, in the previous tile, when it equals A[i0-1])
+      if (hit0) {
+        const uint32_t ia = base + static_cast<uint32_t>(x0);
+        atomicOr(p.C + (ia >> 5), 1u << (ia & 31));
+      }
+      if (hit1) {
+        const uint32_t ia = base + static_cast<uint32_t>(x1);
+        atomicOr(p.C + (ia >> 5), 1u << (ia & 31));
+      }
       if (p.MB) {
-        const int rp = static_cast<int>(jbase + static_cast<uint32_t>(bi) + base +
-                                        static_cast<uint32_t>(x) - static_cast<uint32_t>(k0));
-        if (act && rp >= 0) atomicOr(bits + (rp >> 5), 1u << (rp & 31));
+        const int rp0 = static_cast<int>(rbase + static_cast<uint32_t>(bi0 + x0));
+        const int rp1 = static_cast<int>(rbase + static_cast<uint32_t>(bi1 + x1));
+        if (act0 && rp0 >= 0) atomicOr(bits + (rp0 >> 5), 1u << (rp0 & 31));
+        if (act1 && rp1 >= 0) atomicOr(bits + (rp1 >> 5), 1u << (rp1 & 31));
       }
     }
     release_stage(empty);

@@ -28,12 +28,14 @@ def lsm():
     assert lsm.get_device_status() == lsm.LSM_OK
 
 
-def run_whole(lsm, A, B, ws=None):
+def run_whole(lsm, A, B, ws=None, want_lb=True):
     m, n = len(A), len(B)
-    C, lb, dir_, tot, refs, ordA, ordB, cnt = lsm.replacement_merge(up(A), up(B), ws=ws)
+    C, lb, dir_, tot, refs, ordA, ordB, cnt = lsm.replacement_merge(up(A), up(B), ws=ws,
+                                                                    want_lb=want_lb)
     N = int(cnt.item())
-    return dict(C=down(C)[:(m + 31) // 32], lb=down(lb), dir=down(dir_), total=int(tot.item()),
-                refs=down(refs)[:N], ordA=down(ordA), ordB=down(ordB), count=N)
+    return dict(C=down(C)[:(m + 31) // 32], lb=None if lb is None else down(lb), dir=down(dir_),
+                total=int(tot.item()), refs=down(refs)[:N], ordA=down(ordA), ordB=down(ordB),
+                count=N)
 
 
 @pytest.mark.parametrize("m,n,shared,universe", [c for c in REPLACE_CASES if c[0] + c[1] > 0] + [
@@ -106,3 +108,19 @@ def test_whole_path_equals_separate_calls(lsm):
     assert np.array_equal(down(ordA), whole["ordA"]) and np.array_equal(down(ordB), whole["ordB"])
     r = oracle.replacement_u64(inp.A, inp.B)
     assert N == r.count
+
+
+@pytest.mark.parametrize("m,n,shared", [(20000, 7000, 7000), (300000, 300000, 100000),
+                                        (2816, 2816, 1000), (0, 5000, 0), (5000, 0, 0)])
+def test_whole_path_without_lower_bounds(lsm, m, n, shared):
+    # lb_B is scratch on the whole path: a null lb_B leaves it unwritten and
+    # every other output unchanged
+    inp = synth.replace_random_small(seed=m + 3 * n + shared, m=m, n=n, shared=shared)
+    got = run_whole(lsm, inp.A, inp.B, want_lb=False)
+    assert got["lb"] is None
+    check_against_oracle(got, inp.A, inp.B)
+
+
+def test_whole_path_without_lower_bounds_12M_4M(lsm):
+    inp = synth.replace_u64()
+    check_against_oracle(run_whole(lsm, inp.A, inp.B, want_lb=False), inp.A, inp.B)
