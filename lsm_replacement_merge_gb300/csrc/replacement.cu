@@ -12,31 +12,33 @@
 // The path: a co-rank partition of the keys (A first on ties; also clears C),
 // the collision mark, the rank512 build and the compaction.
 //
-//   mark      per merge-path tile of D = T E keys the producer warp stages
+//   mark      per merge-path tile of D = T E keys the loader warp stages
 //             A[i0-1, i1) and B[j0, j1 + 1) with bulk copies; once they land
-//             it finds the lower bound of every HG-th B key of the tile in the
-//             staged A span (the group heads) and writes the compaction's
-//             co-rank at the tile start. The consumer warps then take 32 B
-//             keys each: every key's lower bound lies between its group's
-//             heads, found by a uniform-step search; lb_B goes to global
-//             memory straight from the lanes (32 consecutive words per warp)
-//             and a key equal to its lower-bound A key sets that collision bit
-//             with an atomic OR (C was cleared by the partition). No consumer
-//             barrier: each warp releases the stage on its own.
-//   compact   merge path over positions (B first on ties): B_j precedes A_i
-//             exactly when lb_B[j] <= i, so the merge of A's survivors and B
-//             needs lb_B and C only. Its tiles have the mark's diagonals: the
-//             co-rank at k0 in this order is the mark's i0, less one when
-//             A[i0-1] = B[j0] (the one equal pair that can straddle the cut).
-//             The producer stages lb_B[j0, j1) and the tile's C words, then
-//             prepares each consumer warp's start (B records before its first
-//             slot, by bisection) and prefix popcounts of the C words. Each
-//             warp owns 32 E consecutive slots: its B records set bits of a
-//             warp-private slot bitmap, two warp scans give every lane its
-//             first A and B record and its dropped records before, and each
-//             lane walks its E slots, writing refs and ordinals into shared
-//             buffers that one bulk store per output moves out (double
-//             buffered: one consumer barrier per tile).
+//             every consumer thread finds the lower bound of one HG-th B key
+//             (a group head) in the staged A span, and the last one writes
+//             the compaction's co-rank at the tile start. After one consumer
+//             barrier every lane searches two B keys between their groups'
+//             heads (the two searches stepped together); lb_B goes to global
+//             memory straight from the lanes when the caller wants it, a key
+//             equal to its lower-bound A key sets that collision bit with an
+//             atomic OR (C was cleared by the partition), and the key's
+//             position in the merge with B first on ties, j + lb_B[j], sets a
+//             bit of the tile's words of the merge bitmap MB in shared memory,
+//             which the last warp writes out at the next tile's barrier.
+//   compact   merge path over positions (B first on ties): position p of the
+//             merge holds a B record exactly when MB bit p is set, so the
+//             merge of A's survivors and B needs MB and C only. Its tiles have
+//             the mark's diagonals: the co-rank at k0 in this order is the
+//             mark's i0, less one when A[i0-1] = B[j0] (the one equal pair
+//             that can straddle the cut). The loader stages the tile's MB
+//             words and C words and fetches R(i0) from the rank directory.
+//             Each consumer warp owns 32 E consecutive positions: popcounts
+//             of the MB words and C words before them give its first B record
+//             and its dropped A records before, two warp scans place every
+//             lane, and each lane walks its E positions, writing refs and
+//             ordinals into the warp's shared buffers, which the warp moves
+//             out as three contiguous runs (bulk stores), with no barrier
+//             between consumer warps.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -53,6 +55,12 @@
 // us against 91.8 us for 2 (94 registers) and for the compiler's choice (96).
 #ifndef MARK_MIN_BLOCKS
 #define MARK_MIN_BLOCKS 3
+#endif
+// The same for the compaction kernel: 5 CTAs (72 registers, no spills)
+// 87.7 us against 88.8 us before its walk lost its branches, 90.8 us for 4
+// CTAs (94 registers) and 93.8 us for the compiler's choice (119, 3 CTAs).
+#ifndef COMPACT_MIN_BLOCKS
+#define COMPACT_MIN_BLOCKS 5
 #endif
 
 namespace lsm {
@@ -564,7 +572,7 @@ struct CompactTile {
   static constexpr int D = T * E, NW = T / 32, W = 32 * E;
   static constexpr int NMB = D / 32;       // merge bitmap words of one tile
   static constexpr int NCW = D / 32 + 4;   // C words of one tile, at most, and slack
-  static constexpr int kMinBlocks = 1;
+  static constexpr int kMinBlocks = COMPACT_MIN_BLOCKS;
   static constexpr int64_t kMBBytes = align_up(int64_t(NMB) * 4 + 16, 16);
   static constexpr int64_t kStageBytes = kMBBytes + align_up(int64_t(NCW + 8) * 4, 16);
   // per warp: refs (W words + alignment lead), ordinals (ord_A then ord_B,
@@ -716,7 +724,34 @@ struct CompactTile {
       const uint32_t ia0 = i0u + static_cast<uint32_t>(a_first), jb0 = j0u + static_cast<uint32_t>(bw0);
       if (lane == 0) bulk_wait_read_all();  // the previous tile's stores from these buffers
       __syncwarp();
-      if (!bad) {
+      if (!bad && __all_sync(0xffffffffu, nvalid == E)) {
+        // every lane holds E positions: a walk without branches. Running
+        // shared addresses of the next ord_A, ord_B and refs slots and the
+        // next ref values; a dropped A record's ref goes to a scratch word
+        // past the refs run (kRefsWords - 1 > 3 + W), so every position
+        // makes exactly two stores.
+        uint32_t pA = smem_u32(sOA + a_rel), pB = smem_u32(sOB + b_rel);
+        uint32_t pR = smem_u32(sR + out_rel);
+        const uint32_t dummy = smem_u32(wRefs + kRefsWords - 1);
+        uint32_t vA = ia0 + static_cast<uint32_t>(a_rel);
+        uint32_t vB = LSM_REF_FROM_B | (jb0 + static_cast<uint32_t>(b_rel));
+        uint32_t o = wout0 + static_cast<uint32_t>(out_rel);
+        uint32_t cw2 = cwin;
+#pragma unroll
+        for (int q = 0; q < E; ++q) {
+          const bool isB = (win >> q) & 1u;
+          const bool dr = !isB && (cw2 & 1u);
+          cw2 = isB ? cw2 : (cw2 >> 1);
+          st_shared_u32(isB ? pB : pA, dr ? LSM_ORD_DROPPED : o);
+          st_shared_u32(dr ? dummy : pR, isB ? vB : vA);
+          pB += isB ? 4u : 0u;
+          vB += isB ? 1u : 0u;
+          pA += isB ? 0u : 4u;
+          vA += isB ? 0u : 1u;
+          pR += dr ? 0u : 4u;
+          o += dr ? 0u : 1u;
+        }
+      } else if (!bad) {
 #pragma unroll
         for (int q = 0; q < E; ++q) {
           const bool valid = q < nvalid;
@@ -735,8 +770,6 @@ struct CompactTile {
           a_rel += isA ? 1 : 0;
         }
       }
-      (void)sOA;
-      (void)sOB;
       release_stage(empty);  // the stage is not read again
       fence_proxy_async_smem();
       __syncwarp();
