@@ -176,6 +176,16 @@ def host_info():
                 break
     except OSError:
         pass
+    # Arm hosts report an implementer and part number instead of a name
+    arm_parts = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+                 ("0x41", "0xd0c"): "Arm Neoverse-N1", ("0x41", "0xd49"): "Arm Neoverse-N2"}
+    try:
+        impl = next((ln.split(":", 1)[1].strip() for ln in txt.splitlines()
+                     if ln.split(":")[0].strip() == "CPU implementer"), None)
+        if model and impl and (impl, model) in arm_parts:
+            model = "%s (implementer %s, part %s)" % (arm_parts[(impl, model)], impl, model)
+    except NameError:
+        pass
     import platform
     return {"cpu_count": os.cpu_count(), "cpu_model": model or platform.processor() or None,
             "machine": platform.machine()}
