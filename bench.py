@@ -724,6 +724,13 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
     whole_lb = [("replacement_merge", lambda: lsm.replacement_merge(
         A, B, C, lb, dir_, tot, refs, oa, ob, cnt, w6))]
     ms_lb, _ = time_pipeline(torch, whole_lb, steps, flush)
+    # the same call in its other form: the mark and the compaction of each
+    # tile in one persistent kernel (R from the mark warps' published counts)
+    lsm.tune_replacement_merge(1)
+    try:
+        ms_one, _ = time_pipeline(torch, whole, steps, flush)
+    finally:
+        lsm.tune_replacement_merge(lsm.DEFAULT_REPLACEMENT_MERGE_MODE)
     # the same work as three separate calls: per-kernel times (each call's
     # main pipeline bracketed by events) and the step with one more partition
     ms_sep, per = time_pipeline(torch, stages, steps, flush)
@@ -740,6 +747,8 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
                  "mark_pipeline_ms": per_whole["replacement_merge"],
                  "lb_B": "scratch, not written",
                  "with_lb_B_written": {"ms_per_step": ms_lb},
+                 "form": "two tile pipelines (mark, rank512 build, compaction)",
+                 "one_kernel": {"ms_per_step": ms_one, "gpu_launches_per_step": 3},
                  "workspace_bytes": {"replacement_merge": w6.numel()},
                  "separate_calls": {"ms_per_step": ms_sep, "kernel_ms": per,
                                     "gpu_launches_per_step": 5,

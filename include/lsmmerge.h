@@ -571,6 +571,18 @@ LSM_API int lsm_set_profile_events(void *start_event, void *stop_event);
  * Process-wide. */
 LSM_API int lsm_tune_replace(int kernel, int threads, int items_per_thread);
 
+/* Selects the form of lsm_replacement_merge: mode 0 (the default) runs the
+ * mark and the compaction as two tile pipelines with the rank512 build
+ * between them; mode 1 runs the mark and the compaction of each tile in one
+ * persistent kernel (warp roles: a loader, mark warps, a lookback warp that
+ * finds R at the tile's first A record from the collision counts the mark
+ * warps publish, compaction warps), the tile's merge bitmap and collision
+ * bits handed over in shared memory, then the rank512 build. Both give the
+ * same outputs; mode 1 measured slower on the 12M + 4M workload (95.9 us
+ * against 87.7 us per step). Process-wide; other modes return
+ * LSM_ERR_ARG. */
+LSM_API int lsm_tune_replacement_merge(int mode);
+
 /* ---- test hook ------------------------------------------------------------ */
 /* Launches one block that waits, with the same bounded wait the kernels
  * use, on a device flag that nothing ever sets, and gives up after

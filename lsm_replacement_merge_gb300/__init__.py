@@ -120,6 +120,7 @@ def lib():
                 "lsm_debug_timeout_probe": ([I, P], ctypes.c_int),
                 "lsm_tune_merge": ([ctypes.c_int] * 4, ctypes.c_int),
                 "lsm_tune_replace": ([ctypes.c_int] * 3, ctypes.c_int),
+                "lsm_tune_replacement_merge": ([ctypes.c_int], ctypes.c_int),
                 "lsm_set_profile_events": ([P, P], ctypes.c_int),
                 "lsm_rank_build_noalloc": ([P, I, P, P, P], ctypes.c_int),
                 "lsm_validate_sorted": ([ctypes.c_int, P, I, ctypes.c_int, P, P], ctypes.c_int),
@@ -222,6 +223,15 @@ DEFAULT_REPLACE_VARIANT = {0: (0, 0), 1: (0, 0)}  # kernel -> (threads, items)
 def tune_replace(kernel: int, threads: int, items_per_thread: int) -> None:
     """Tile variant of collision_mark (kernel 0) or replacement_merge_compact (1)."""
     _check("lsm_tune_replace", lib().lsm_tune_replace(kernel, threads, items_per_thread))
+
+
+DEFAULT_REPLACEMENT_MERGE_MODE = 0
+
+
+def tune_replacement_merge(mode: int) -> None:
+    """Form of replacement_merge: 0 = two tile pipelines (the default), 1 =
+    the mark and the compaction in one kernel."""
+    _check("lsm_tune_replacement_merge", lib().lsm_tune_replacement_merge(mode))
 
 
 def tune_merge(key_type: int, items_per_thread: int, stages: int, out_tiles: int) -> None:

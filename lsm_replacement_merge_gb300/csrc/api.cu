@@ -420,6 +420,11 @@ LSM_API int lsm_replacement_merge_compact(int64_t m, int64_t n, const uint32_t *
                                     status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
+// lsm_replacement_merge's form: 0 = two pipelines (the default, measured
+// faster), 1 = the mark and the compaction in one kernel
+// (lsm_tune_replacement_merge).
+static int g_replacement_merge_mode = 0;
+
 LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                   uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,
                                   uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
@@ -441,10 +446,24 @@ LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *
   int64_t *part_c = c.take<int64_t>(G + 1);
   uint64_t *rank_ws = c.take<uint64_t>(rank_build_ctas(m));
   uint32_t *mb = c.take<uint32_t>(merge_bitmap_words(m + n));
+  if (g_replacement_merge_mode == 1)
+    // one kernel for the mark and the compaction: part_c's words hold the
+    // tiles' lookback states instead (G <= G + 1 words), the merge bitmap
+    // stays in shared memory
+    return cuda_status(launch_replacement_merge_one(
+        A ? A : B, m, B ? B : A, n, C, lb_B, dir, d_total, out_refs, ord_A, ord_B, d_count, part_m,
+        reinterpret_cast<uint64_t *>(part_c), rank_ws, status_ptr(),
+        static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_replacement_merge(A ? A : B, m, B ? B : A, n, C, lb_B, dir, d_total,
                                               out_refs, ord_A, ord_B, d_count, part_m, part_c, mb,
                                               rank_ws, status_ptr(),
                                               static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_tune_replacement_merge(int mode) {
+  if (mode != 0 && mode != 1) return LSM_ERR_ARG;
+  g_replacement_merge_mode = mode;
+  return LSM_OK;
 }
 
 LSM_API int lsm_replacement_merge_fused(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,

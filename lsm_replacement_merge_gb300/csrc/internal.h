@@ -72,6 +72,13 @@ cudaError_t launch_compact_tiles_rank2048(int64_t m, int64_t n, const uint32_t *
                                           int64_t *d_count, int32_t *status, cudaStream_t s);
 // The whole path (mark, rank512 build, compaction). part_m, part_c: G + 1
 // each; MB: merge_bitmap_words(m + n); rank_ws: rank_build_ctas(m) uint64.
+cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uint64_t *B,
+                                        int64_t n, uint32_t *C, uint32_t *lb_B, uint32_t *dir,
+                                        int64_t *d_total, uint32_t *refs, uint32_t *ord_A,
+                                        uint32_t *ord_B, int64_t *d_count, int64_t *part_m,
+                                        uint64_t *state, void *rank_ws, int32_t *status,
+                                        cudaStream_t s);
+int64_t replacement_fused_tile();
 cudaError_t launch_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                     uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,
                                     uint32_t *refs, uint32_t *ord_A, uint32_t *ord_B,

@@ -63,4 +63,51 @@ __device__ __forceinline__ uint32_t lookback_exclusive(uint64_t *state, uint32_t
   return prefix;
 }
 
+// The sum of the aggregates in state[lo, hi), called by a whole warp: 32 K
+// states per round of loads (K per lane, issued together), each polled
+// until its word carries this call's epoch (bounded: past the limit a
+// missing one counts as zero and LSM_ERR_TIMEOUT is recorded). For callers
+// that know the prefix at an earlier tile and need only the aggregates
+// since, so that no tile waits for another tile's prefix.
+template <int K>
+__device__ __forceinline__ uint32_t window_sum(const uint64_t *state, int64_t lo, int64_t hi,
+                                               uint32_t epoch, int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t tag = static_cast<uint64_t>(epoch) << 32;
+  const uint64_t t0 = globaltimer_ns();
+  bool late = false;
+  uint32_t sum = 0;
+  for (int64_t b = lo; b < hi; b += 32 * K) {
+    uint64_t v[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t idx = b + 32 * k + lane;
+      v[k] = idx < hi ? ld_relaxed_u64(state + idx) : tag;
+    }
+    uint32_t polls = 0;
+    for (;;) {
+      bool pub = true;
+#pragma unroll
+      for (int k = 0; k < K; ++k) pub = pub && (v[k] >> 32) == epoch;
+      if (__all_sync(0xffffffffu, pub)) break;
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if ((v[k] >> 32) != epoch) v[k] = ld_relaxed_u64(state + b + 32 * k + lane);
+      if ((++polls & 31) == 0 &&
+          __any_sync(0xffffffffu, globaltimer_ns() - t0 > static_cast<uint64_t>(kWaitLimitNs))) {
+        late = true;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+          if ((v[k] >> 32) != epoch) v[k] = tag;  // give up: counts as zero
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) sum += static_cast<uint32_t>(v[k] & 0x7FFFFFFFu);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (late && lane == 0) report(status, LSM_ERR_TIMEOUT);
+  return sum;
+}
+
 }  // namespace lsm

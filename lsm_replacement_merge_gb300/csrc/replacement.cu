@@ -41,10 +41,12 @@
 //             between consumer warps.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "common.cuh"
 #include "internal.h"
+#include "lookback.cuh"
 #include "pipeline.cuh"
 #include "rank2048.cuh"
 #include "rank512.cuh"
@@ -879,6 +881,411 @@ constexpr int kCompactT = 128, kCompactE = 30, kCompactS = 4;
 using MarkDefault = MarkTile<kTileT, kTileE, kMarkS, kMarkHG>;
 using CompactDefault = CompactTile<kCompactT, kCompactE, kCompactS, Rank512At>;
 using Compact2048 = CompactTile<kCompactT, kCompactE, kCompactS, Rank2048At>;
+
+// ---- the whole path in one persistent kernel ------------------------------------
+// The mark and the compaction of each tile in one CTA, by warp roles: the
+// loader warp stages tile g's keys as the mark pipeline does; eight mark
+// warps find the tile's lower bounds and put its merge-bitmap words and its
+// collision bits (indexed by staged A position) into a ring slot in shared
+// memory, as well as the bits of C, and the last of them publishes the
+// tile's collision count; the lookback warp adds the counts published since
+// this CTA's previous tile to R there, which gives R at the tile's first A
+// record ("Everett: collision bitmap and rank experiment", "Corrected
+// record ordinals": R(i) counts the collisions before i); four compaction
+// warps then place the tile's refs and ordinals
+// from the ring slot as the compaction pipeline does. With two ring slots
+// the mark warps run a tile ahead of the compaction warps, so that the
+// lookback's wait is off their path. The grid is sized so that every CTA is
+// resident, so every tile a lookback waits for is being worked on; every
+// wait is bounded in time.
+#ifndef FUSED_MARK_T
+#define FUSED_MARK_T 256
+#define FUSED_MARK_E 15
+#endif
+struct FusedMC {
+  static constexpr int TM = FUSED_MARK_T, EM = FUSED_MARK_E, D = TM * EM, HG = 8, NWM = TM / 32;
+  static constexpr int TC = 128, EC = 30, NWC = TC / 32, WC = 32 * EC;
+#ifndef FUSED_RING
+#define FUSED_RING 6
+#endif
+  static constexpr int S = 2, NB = FUSED_RING;
+  static constexpr int kLookWarp = (TM + TC) / 32, kLoadWarp = kLookWarp + 1;
+  static constexpr int kThreads = TM + TC + 64;
+  // states per lane in one round of the lookback's loads: 32 x 10 covers
+  // the P - 1 tiles between a CTA's consecutive tiles at two CTAs per SM
+  static constexpr int kLookK = 10;
+  static constexpr int NMB = D / 32 + 4;             // a tile's merge-bitmap words, window slack
+  static constexpr int NCT = (D + 2 + 31) / 32 + 4;  // collision words by staged A position
+  static constexpr int kRing = NMB + NCT;
+  static constexpr int kRefsWords = (WC + 8 + 3) & ~3;
+  static constexpr int kOrdWords = (WC + 12 + 3) & ~3;
+  static constexpr int kWarpWords = kRefsWords + kOrdWords;
+  static_assert(TC * EC == D, "the compaction covers the mark's tile");
+  static_assert(EC < 32, "a lane's positions fit one 32-bit window");
+  using Mark = MarkTile<TM, EM, S, HG>;
+  using MDesc = Mark::Desc;
+  struct TDesc {  // the compaction's view of a tile, written by the mark and the lookback
+    int64_t i0, j0, r0;
+    int32_t na, nb, wbit0, cnt, te, pad;
+    uint32_t hits, warps_done;  // the tile's collisions, mark warps finished (shared atomics)
+  };
+  static constexpr int64_t kHeadsBytes = align_up(int64_t(Mark::kMaxHeads) * 4, 16);
+  static constexpr int64_t kBars = 0;  // full[S], empty[S], markdone[NB], rdone[NB], cdone[NB]
+  static constexpr int64_t kMDesc = align_up(8 * (2 * S + 3 * NB), 64);
+  static constexpr int64_t kTDesc = kMDesc + 64 * S;
+  static constexpr int64_t kStage0 = align_up(kTDesc + 64 * NB, 128);
+  static constexpr int64_t kStageStride = align_up(Mark::kStageBytes, 128);
+  static constexpr int64_t kHeads = kStage0 + S * kStageStride;
+  static constexpr int64_t kRingOff = kHeads + 2 * kHeadsBytes;
+  static constexpr int64_t kCBuf = align_up(kRingOff + int64_t(NB) * kRing * 4, 128);
+  static constexpr int64_t kBytes = kCBuf + int64_t(NWC) * kWarpWords * 4;
+  static_assert(kBytes <= 113 * 1024, "two CTAs per SM");
+  static_assert(sizeof(TDesc) <= 64 && sizeof(MDesc) <= 64, "descriptor slots");
+  struct Params {
+    typename Mark::Params mp;  // keys, sizes, co-ranks, C, lb_B (MB and part_c unused)
+    uint32_t *refs, *ord_A, *ord_B;
+    int64_t *d_count;
+    uint64_t *state;  // G lookback words
+    uint32_t epoch;
+  };
+};
+
+__global__ void __launch_bounds__(FusedMC::kThreads, 2) fused_mc_kernel(FusedMC::Params p,
+                                                                      int64_t G,
+                                                                      int32_t *status) {
+  pdl_begin();
+  using F = FusedMC;
+  constexpr int S = F::S, NB = F::NB, TM = F::TM, HG = F::HG, D = F::D;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + F::kBars);
+  uint64_t *empty = full + S;
+  uint64_t *markdone = empty + S;
+  uint64_t *rdone = markdone + NB;
+  uint64_t *cdone = rdone + NB;
+  F::MDesc *mdesc = reinterpret_cast<F::MDesc *>(smem + F::kMDesc);
+  F::TDesc *tdesc = reinterpret_cast<F::TDesc *>(smem + F::kTDesc);
+  uint32_t *ring = reinterpret_cast<uint32_t *>(smem + F::kRingOff);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t P = gridDim.x;
+  const int64_t R = (G - blockIdx.x + P - 1) / P;  // tiles of this CTA (grid <= G)
+  const int64_t total = p.mp.m + p.mp.n;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], F::NWM);
+    }
+    for (int q = 0; q < NB; ++q) {
+      mbar_init(&markdone[q], F::NWM);
+      mbar_init(&rdone[q], 1);
+      mbar_init(&cdone[q], F::NWC);
+    }
+  }
+  __syncthreads();
+
+  if (warp == F::kLoadWarp) {
+    // the loader: co-ranks of 32 tiles at a time, then each tile's keys
+    int64_t v[4] = {0, 0, 0, 0};
+    for (int64_t r = 0; r < R; ++r) {
+      if ((r & 31) == 0) {
+        const int64_t gl = blockIdx.x + (r + lane) * P;
+        v[0] = v[1] = v[2] = v[3] = 0;
+        if (gl < G) F::Mark::fetch(p.mp, gl, v);
+      }
+      int64_t w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) w[t] = __shfl_sync(0xffffffffu, v[t], static_cast<int>(r & 31));
+      int failed = 0;
+      if (lane == 0) {
+        const int s = static_cast<int>(r % S);
+        if (r >= S && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>(((r / S) + 1) & 1),
+                                       kWaitLimitNs)) {
+          report(status, LSM_ERR_TIMEOUT);
+          failed = 1;
+        } else {
+          F::Mark::produce(p.mp, blockIdx.x + r * P, w,
+                           smem + F::kStage0 + s * F::kStageStride, mdesc[s], &full[s]);
+        }
+      }
+      if (__shfl_sync(0xffffffffu, failed, 0)) return;
+    }
+    return;
+  }
+
+  if (warp < F::NWM) {
+    // the mark warps
+    for (int64_t r = 0; r < R; ++r) {
+      const int s = static_cast<int>(r % S), q = static_cast<int>(r % NB);
+      const int64_t g = blockIdx.x + r * P;
+      bool ok = mbar_wait_sleep(&full[s], static_cast<uint32_t>((r / S) & 1), kWaitLimitNs);
+      // the ring slot's previous tile has left the compaction warps
+      if (ok && r >= NB)
+        ok = mbar_wait_sleep(&cdone[q], static_cast<uint32_t>(((r / NB) - 1) & 1), kWaitLimitNs);
+      const F::MDesc d = mdesc[s];
+      const uint8_t *stage = smem + F::kStage0 + s * F::kStageStride;
+      const uint64_t *sA = reinterpret_cast<const uint64_t *>(stage) + d.offA;
+      const uint64_t *sAx = sA - d.hp;
+      const uint64_t *sB = reinterpret_cast<const uint64_t *>(stage) + d.offB;
+      const int nb = d.nb, lenx = d.na + d.hp;
+      int *heads = reinterpret_cast<int *>(smem + F::kHeads + (r & 1) * F::kHeadsBytes);
+      const int nh = (nb + HG - 1) / HG;
+      uint32_t *mbt = ring + q * F::kRing;
+      uint32_t *ct = mbt + F::NMB;
+      const int64_t k0 = g * D;
+      const int cnt = d.na + d.nb;
+      if (ok) {
+        for (int x = tid; x < F::kRing; x += TM) mbt[x] = 0u;
+        if (tid == 0) {
+          tdesc[q].hits = 0u;
+          tdesc[q].warps_done = 0u;
+        }
+        for (int h = tid; h < nh; h += TM) heads[h] = count_below(sAx, 0, lenx, sB[h * HG], lenx);
+        if (tid == TM - 1) {
+          heads[nh] = lenx;
+          // the equal pair A[i0-1] = B[j0] at the tile's start (B first on
+          // ties: A[i0-1] is this tile's first A record) and A[i1-1] = B[j1]
+          // at its end (A[i1-1] belongs to the next tile)
+          const bool ts = d.hp && nb + d.hn > 0 && sA[-1] == sB[0];
+          const bool te = d.hn && lenx > 0 && sAx[lenx - 1] == sB[nb];
+          F::TDesc &t = tdesc[q];
+          t.i0 = d.i0 - (ts ? 1 : 0);
+          t.j0 = k0 - t.i0;
+          t.na = d.na + (ts ? 1 : 0) - (te ? 1 : 0);
+          t.nb = cnt - t.na;
+          t.wbit0 = d.hp - (ts ? 1 : 0);
+          t.cnt = cnt;
+          t.te = te ? 1 : 0;
+        }
+      }
+      if (named_sync_or(1, TM, !ok)) {
+        if (tid == 0) report(status, LSM_ERR_TIMEOUT);
+        break;
+      }
+      // B[j1] sits at the tile's last position when it equals A[i1-1]
+      if (tid == TM - 1 && tdesc[q].te) atomicOr(mbt + ((cnt - 1) >> 5), 1u << ((cnt - 1) & 31));
+      const uint32_t base = static_cast<uint32_t>(d.i0 - d.hp);
+      uint32_t *lbo = p.mp.lb_B ? p.mp.lb_B + d.j0 : nullptr;
+      uint32_t hits = 0;  // this warp's collisions (warp-uniform)
+      for (int b0 = warp * 64; b0 < nb; b0 += F::NWM * 64) {
+        const int bi0 = b0 + lane, bi1 = bi0 + 32;
+        const bool act0 = bi0 < nb, act1 = bi1 < nb;
+        const uint64_t key0 = sB[act0 ? bi0 : nb - 1], key1 = sB[act1 ? bi1 : nb - 1];
+        const int h0 = bi0 / HG, h1 = bi1 / HG;
+        int x0 = act0 ? heads[h0] : 0, x1 = act1 ? heads[h1] : 0;
+        const int hi0 = act0 ? heads[h0 + 1] : 0, hi1 = act1 ? heads[h1 + 1] : 0;
+        const int sp = (hi0 - x0) > (hi1 - x1) ? (hi0 - x0) : (hi1 - x1);
+        const int span =
+            static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(sp)));
+        count_below2(sAx, x0, hi0, key0, x1, hi1, key1, span);
+        const bool hit0 = act0 && x0 < lenx && sAx[x0] == key0;
+        const bool hit1 = act1 && x1 < lenx && sAx[x1] == key1;
+        hits += __popc(__ballot_sync(0xffffffffu, hit0)) + __popc(__ballot_sync(0xffffffffu, hit1));
+        if (lbo) {
+          if (act0) lbo[bi0] = base + static_cast<uint32_t>(x0);
+          if (act1) lbo[bi1] = base + static_cast<uint32_t>(x1);
+        }
+        if (hit0) {
+          const uint32_t ia = base + static_cast<uint32_t>(x0);
+          atomicOr(p.mp.C + (ia >> 5), 1u << (ia & 31));
+          atomicOr(ct + (x0 >> 5), 1u << (x0 & 31));
+        }
+        if (hit1) {
+          const uint32_t ia = base + static_cast<uint32_t>(x1);
+          atomicOr(p.mp.C + (ia >> 5), 1u << (ia & 31));
+          atomicOr(ct + (x1 >> 5), 1u << (x1 & 31));
+        }
+        // B key bi sits at tile position bi + x - hp of the merge with B
+        // first on ties (B[j0] falls before the tile when it equals A[i0-1])
+        const int rp0 = bi0 + x0 - d.hp, rp1 = bi1 + x1 - d.hp;
+        if (act0 && rp0 >= 0) atomicOr(mbt + (rp0 >> 5), 1u << (rp0 & 31));
+        if (act1 && rp1 >= 0) atomicOr(mbt + (rp1 >> 5), 1u << (rp1 & 31));
+      }
+      release_stage(&empty[s]);  // also orders the warp's shared writes before its arrival
+      if (lane == 0) {
+        // the tile's collision count goes to the lookback as soon as the last
+        // mark warp is done, so that no tile waits for another CTA's lookback
+        // warp to publish it
+        atomicAdd(&tdesc[q].hits, hits);
+        __threadfence_block();
+        if (atomicAdd(&tdesc[q].warps_done, 1u) == F::NWM - 1) {
+          __threadfence_block();
+          const uint32_t agg = atomicAdd(&tdesc[q].hits, 0u);
+          const uint64_t tag = static_cast<uint64_t>(p.epoch) << 32;
+          st_relaxed_u64(p.state + g, tag | agg);
+        }
+        mbar_arrive(&markdone[q]);
+      }
+    }
+    return;
+  }
+
+  if (warp == F::kLookWarp) {
+    // the lookback warp: R at each tile's first A record. This CTA's
+    // previous tile is g - P, so R(g) = R(g - P) plus the collision counts
+    // of tiles g - P .. g - 1, which their mark warps publish as soon as they
+    // are done: no tile waits for another tile's prefix.
+    uint32_t rprev = 0;  // R at this CTA's previous tile
+    for (int64_t r = 0; r < R; ++r) {
+      const int q = static_cast<int>(r % NB);
+      const int64_t g = blockIdx.x + r * P;
+      // R(g) needs only earlier tiles' counts: it is summed while this
+      // tile's own mark is still running
+      const uint32_t prefix = (r == 0 ? 0u : rprev) +
+                              window_sum<F::kLookK>(p.state, r == 0 ? 0 : g - P, g, p.epoch, status);
+      rprev = prefix;
+      // the ring slot holds this tile once its mark is done
+      if (!mbar_wait_sleep(&markdone[q], static_cast<uint32_t>((r / NB) & 1), kWaitLimitNs)) {
+        if (lane == 0) report(status, LSM_ERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        tdesc[q].r0 = prefix;
+        if (g == G - 1 && p.d_count)
+          *p.d_count = total - static_cast<int64_t>(prefix + tdesc[q].hits);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rdone[q]);
+    }
+    return;
+  }
+
+  // the compaction warps
+  const int cwarp = warp - F::NWM;
+  uint32_t *wRefs = reinterpret_cast<uint32_t *>(smem + F::kCBuf) + cwarp * F::kWarpWords;
+  uint32_t *wOrd = wRefs + F::kRefsWords;
+  constexpr int E = F::EC, W = F::WC;
+  for (int64_t r = 0; r < R; ++r) {
+    const int q = static_cast<int>(r % NB);
+    const int64_t g = blockIdx.x + r * P;
+    if (!mbar_wait_sleep(&rdone[q], static_cast<uint32_t>((r / NB) & 1), kWaitLimitNs)) {
+      if (lane == 0) report(status, LSM_ERR_TIMEOUT);
+      break;
+    }
+    const F::TDesc td = tdesc[q];
+    const uint32_t *mb = ring + q * F::kRing;
+    const uint32_t *cw = mb + F::NMB;
+    const int na = td.na, nb = td.nb, cnt = td.cnt;
+    const int s0 = cwarp * W;
+    bool bad = false;
+    if (s0 < cnt) {
+      const uint32_t i0u = static_cast<uint32_t>(td.i0), j0u = static_cast<uint32_t>(td.j0);
+      const int wbit0 = td.wbit0;
+      const int s1 = cnt - s0 < W ? cnt : s0 + W;
+      // B records before the warp's first position, dropped A records before
+      // its first A record
+      int pb = 0;
+      for (int x = lane; x < (s0 >> 5); x += 32) pb += __popc(mb[x]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
+      const int bw0 = pb;
+      int a_first = s0 - bw0;
+      // R(i0) <= i0 whatever the lookback returned, so that no run starts
+      // before the output
+      bad = a_first < 0 || a_first > na || td.r0 < 0 || td.r0 > td.i0;
+      if (bad) a_first = 0;
+      const int yend = wbit0 + a_first;
+      int pcnt = 0;
+      for (int x = lane; x < (yend >> 5); x += 32) pcnt += __popc(cw[x]);
+      if (lane == 0) {
+        if (yend & 31) pcnt += __popc(cw[yend >> 5] & ((1u << (yend & 31)) - 1u));
+        pcnt -= __popc(cw[0] & ((1u << wbit0) - 1u));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pcnt += __shfl_xor_sync(0xffffffffu, pcnt, o);
+      const int drop0 = pcnt;
+      const int y = lane * E;
+      const int nvalid = (s1 - s0) - y < 0 ? 0 : ((s1 - s0) - y < E ? (s1 - s0) - y : E);
+      const int sp = s0 + y;
+      const uint32_t w_lo = mb[sp >> 5];
+      const uint32_t w_hi = mb[(sp >> 5) + 1];
+      uint32_t win = static_cast<uint32_t>(((static_cast<uint64_t>(w_hi) << 32) | w_lo) >> (sp & 31));
+      win &= (1u << nvalid) - 1u;
+      const int numB = __popc(win);
+      const int numA = nvalid - numB;
+      const int incB = warp_inclusive_sum(numB);
+      const int nB_w = __shfl_sync(0xffffffffu, incB, 31);
+      const int nA_w = (s1 - s0) - nB_w;
+      bad = bad || a_first + nA_w > na || bw0 + nB_w > nb;
+      int a_rel = y - (incB - numB);
+      int b_rel = incB - numB;
+      const int xa = wbit0 + a_first + a_rel;
+      uint32_t cwin = static_cast<uint32_t>(
+          ((static_cast<uint64_t>(cw[(xa >> 5) + 1]) << 32) | cw[xa >> 5]) >> (xa & 31));
+      cwin &= numA ? (0xFFFFFFFFu >> (32 - numA)) : 0u;
+      const int drops = __popc(cwin);
+      const int incD = warp_inclusive_sum(drops);
+      const int kept_w = (s1 - s0) - __shfl_sync(0xffffffffu, incD, 31);
+      int out_rel = y - (incD - drops);
+      const int64_t gr0 = g * D - td.r0 + s0 - drop0;  // refs run
+      const int64_t ga0 = td.i0 + a_first;             // ord_A run
+      const int64_t gb0 = td.j0 + bw0;                 // ord_B run
+      const int offB = (nA_w + 7) & ~3;
+      uint32_t *sR = wRefs + (gr0 & 3);
+      uint32_t *sOA = wOrd + (ga0 & 3);
+      uint32_t *sOB = wOrd + offB + (gb0 & 3);
+      const uint32_t wout0 = static_cast<uint32_t>(gr0);
+      const uint32_t ia0 = i0u + static_cast<uint32_t>(a_first);
+      const uint32_t jb0 = j0u + static_cast<uint32_t>(bw0);
+      if (lane == 0) bulk_wait_read_all();  // the previous tile's stores from these buffers
+      __syncwarp();
+      if (!bad && __all_sync(0xffffffffu, nvalid == E)) {
+        uint32_t pA = smem_u32(sOA + a_rel), pB = smem_u32(sOB + b_rel);
+        uint32_t pR = smem_u32(sR + out_rel);
+        const uint32_t dummy = smem_u32(wRefs + F::kRefsWords - 1);
+        uint32_t vA = ia0 + static_cast<uint32_t>(a_rel);
+        uint32_t vB = LSM_REF_FROM_B | (jb0 + static_cast<uint32_t>(b_rel));
+        uint32_t o = wout0 + static_cast<uint32_t>(out_rel);
+        uint32_t cw2 = cwin;
+#pragma unroll
+        for (int qq = 0; qq < E; ++qq) {
+          const bool isB = (win >> qq) & 1u;
+          const bool dr = !isB && (cw2 & 1u);
+          cw2 = isB ? cw2 : (cw2 >> 1);
+          st_shared_u32(isB ? pB : pA, dr ? LSM_ORD_DROPPED : o);
+          st_shared_u32(dr ? dummy : pR, isB ? vB : vA);
+          pB += isB ? 4u : 0u;
+          vB += isB ? 1u : 0u;
+          pA += isB ? 0u : 4u;
+          vA += isB ? 0u : 1u;
+          pR += dr ? 0u : 4u;
+          o += dr ? 0u : 1u;
+        }
+      } else if (!bad) {
+#pragma unroll
+        for (int qq = 0; qq < E; ++qq) {
+          const bool valid = qq < nvalid;
+          const bool isB = (win >> qq) & 1u;
+          const bool isA = valid && !isB;
+          const bool dropped = isA && (cwin & 1u);
+          cwin >>= isA ? 1 : 0;
+          const uint32_t ref = isB ? (LSM_REF_FROM_B | (jb0 + static_cast<uint32_t>(b_rel)))
+                                   : (ia0 + static_cast<uint32_t>(a_rel));
+          const int oi = isB ? offB + static_cast<int>(gb0 & 3) + b_rel
+                             : static_cast<int>(ga0 & 3) + a_rel;
+          if (valid) wOrd[oi] = dropped ? LSM_ORD_DROPPED : wout0 + static_cast<uint32_t>(out_rel);
+          if (valid && !dropped) sR[out_rel] = ref;
+          out_rel += (valid && !dropped) ? 1 : 0;
+          b_rel += isB ? 1 : 0;
+          a_rel += isA ? 1 : 0;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cdone[q]);  // the ring slot is not read again
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (!bad) {
+        warp_store_run(p.refs, gr0, kept_w, wRefs);
+        warp_store_run(p.ord_A, ga0, nA_w, wOrd);
+        warp_store_run(p.ord_B, gb0, nB_w, wOrd + offB);
+        if (lane == 0) bulk_commit();
+      }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cdone[q]);
+    }
+    if (lane == 0 && bad) report(status, LSM_ERR_ARG);
+  }
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 static_assert(MarkDefault::D == CompactDefault::D, "the compaction reuses the mark's diagonals");
 
 }  // namespace
@@ -961,6 +1368,66 @@ cudaError_t launch_compact_tiles_rank2048(int64_t m, int64_t n, const uint32_t *
 
 // The whole path: partition + mark (which also writes the merge bitmap and
 // the compaction's co-ranks), rank512 build, compaction.
+int64_t replacement_fused_tile() { return FusedMC::D; }
+
+// The whole path with the mark and the compaction in one kernel: the co-rank
+// partition (which clears C), the fused kernel (refs, ordinals, C, the count;
+// lb_B when asked for), then the rank512 directory from the finished C.
+cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uint64_t *B,
+                                        int64_t n, uint32_t *C, uint32_t *lb_B, uint32_t *dir,
+                                        int64_t *d_total, uint32_t *refs, uint32_t *ord_A,
+                                        uint32_t *ord_B, int64_t *d_count, int64_t *part_m,
+                                        uint64_t *state, void *rank_ws, int32_t *status,
+                                        cudaStream_t s) {
+  static std::atomic<uint32_t> epoch_counter{0};
+  constexpr int64_t D = FusedMC::D;
+  const int64_t G = (m + n + D - 1) / D;
+  cudaError_t err = cudaSuccess;
+  if (G > 0) {
+    const int64_t nwords = (m + 31) / 32;
+    int64_t threads = (G + 1) * kPartLanes;
+    if (threads < nwords / 4) threads = nwords / 4;
+    const int64_t blocks = (threads + 255) / 256;
+    err = launch_kernel(true, corank_partition_kernel<kPartLanes>,
+                        static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s, KeysAFirst{A, B},
+                        m, n, D, G, part_m, C, nwords, static_cast<uint32_t *>(nullptr),
+                        int64_t(0));
+    if (err != cudaSuccess) return err;
+    static int per_sm = 0;
+    if (!per_sm) {
+      err = cudaFuncSetAttribute(fused_mc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(FusedMC::kBytes));
+      if (err != cudaSuccess) return err;
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_mc_kernel,
+                                                          FusedMC::kThreads, FusedMC::kBytes);
+      if (err != cudaSuccess) return err;
+      if (per_sm < 1) return cudaErrorLaunchOutOfResources;
+    }
+    // every CTA resident at once: a tile's lookback waits only for tiles
+    // that are being worked on
+    int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
+    if (grid > G) grid = G;
+    uint32_t epoch = ++epoch_counter;
+    if (epoch == 0) epoch = ++epoch_counter;
+    FusedMC::Params p{};
+    p.mp = FusedMC::Mark::Params{A, B, m, n, G, part_m, C, lb_B, nullptr, nullptr};
+    p.refs = refs;
+    p.ord_A = ord_A;
+    p.ord_B = ord_B;
+    p.d_count = d_count;
+    p.state = state;
+    p.epoch = epoch;
+    profile_before(s);
+    err = launch_kernel(true, fused_mc_kernel, static_cast<unsigned>(grid), FusedMC::kThreads,
+                        FusedMC::kBytes, s, p, G, status);
+    profile_after(s);
+    if (err != cudaSuccess) return err;
+  }
+  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s);
+  if (err != cudaSuccess || G > 0) return err;
+  return launch_kernel(false, set_count_kernel2, 1, 1, 0, s, d_count, int64_t(0));
+}
+
 cudaError_t launch_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                                     uint32_t *C, uint32_t *lb_B, uint32_t *dir, int64_t *d_total,
                                     uint32_t *refs, uint32_t *ord_A, uint32_t *ord_B,

@@ -1,7 +1,8 @@
 """GPU parity for the whole replacement merge in one call
-(lsm_replacement_merge: the collision mark, the rank512 build and the
-compaction, with the compaction's tiles on the mark's diagonals) against the
-oracle, bit-exact: C, lb_B, the directory, R(m), refs, ordinals and the
+(lsm_replacement_merge, in both its forms: the collision mark and the
+compaction in one kernel with a lookback for R, and as two pipelines with
+the rank512 build between them, the compaction's tiles on the mark's
+diagonals) against the oracle, bit-exact: C, lb_B, the directory, R(m), refs, ordinals and the
 count. Cases span several tiles with ragged tails, dense and sparse
 collisions, A-only and B-only stretches, ties at every tile boundary (B equal
 to A), single records, empty inputs and the two full-size workloads."""
@@ -20,12 +21,24 @@ from tests.test_oracle_pins import REPLACE_CASES  # noqa: E402
 
 
 @pytest.fixture(scope="module")
-def lsm():
+def lsm_mod():
     import lsm_replacement_merge_gb300 as lsm
     lsm.lib()
     lsm.get_device_status(reset=True)
     yield lsm
     assert lsm.get_device_status() == lsm.LSM_OK
+
+
+@pytest.fixture(params=[1, 0], ids=["one_kernel", "two_pipelines"])
+def lsm(lsm_mod, request):
+    # every test runs both forms of the call: the mark and the compaction in
+    # one kernel, and as two pipelines
+    lsm_mod.tune_replacement_merge(request.param)
+    try:
+        yield lsm_mod
+        assert lsm_mod.get_device_status() == lsm_mod.LSM_OK
+    finally:
+        lsm_mod.tune_replacement_merge(lsm_mod.DEFAULT_REPLACEMENT_MERGE_MODE)
 
 
 def run_whole(lsm, A, B, ws=None, want_lb=True):
