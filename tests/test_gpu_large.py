@@ -123,6 +123,39 @@ def test_replacement_beyond_2pow31_elements(lsm):
     assert bool((_u32(refs[:N]) == refs_exp).all())
 
 
+@pytest.mark.parametrize("mode", [0, 1], ids=["two_pipelines", "one_kernel"])
+def test_whole_path_beyond_2pow31_elements(lsm, mode):
+    # The whole-path call (lsm_replacement_merge) on the same 2.4 G records,
+    # both forms, equal to the separate calls, which the test above checks
+    # against closed forms: positions past 2^31 in the merge bitmap, the
+    # co-ranks, the lookback and the outputs.
+    _need(100)
+    m, n = (5 << 28) + 7, (1 << 30) - 3
+    A = torch.arange(m, device=dev(), dtype=torch.int64) * 3
+    B = torch.arange(n, device=dev(), dtype=torch.int64) * 2 + 1
+    C, lb = lsm.collision_mark(A, B)
+    dir_, tot = lsm.rank_build(C, m)
+    refs, ordA, ordB, cnt = lsm.replacement_merge_compact(m, n, C, dir_, lb)
+    del lb
+    lsm.tune_replacement_merge(mode)
+    try:
+        Cw, lbw, dirw, totw, refsw, ordAw, ordBw, cntw = lsm.replacement_merge(A, B, want_lb=False)
+    finally:
+        lsm.tune_replacement_merge(lsm.DEFAULT_REPLACEMENT_MERGE_MODE)
+    torch.cuda.synchronize()
+    assert lbw is None
+    N = int(cnt.item())
+    assert int(cntw.item()) == N and int(totw.item()) == int(tot.item())
+    words = (m + 31) // 32
+
+    def same(x, y):  # bitwise equality of two uint32 tensors
+        return bool((x.view(torch.int32) == y.view(torch.int32)).all())
+
+    assert same(Cw[:words], C[:words]) and same(dirw, dir_)
+    assert same(ordAw, ordA) and same(ordBw, ordB)
+    assert same(refsw[:N], refs[:N])
+
+
 def _eg0_len(x):
     import numpy as np
     return 2 * (np.floor(np.log2(x.astype(np.float64) + 1)).astype(np.int64)) + 1
