@@ -8,15 +8,15 @@ inputs already resident in HBM. The metric is merged elements per second
 (input elements / time); the line also reports the tile kernel's achieved HBM
 bandwidth against the measured copy peak.
 
-The same line carries, under "workloads", the other hot-path pipelines, each
-timed as a whole path:
+A line before the result carries, under "workloads", the other hot-path
+pipelines, each timed as a whole path:
   int32 4096+4096 merge          (latency-bound)
-  replacement 12,000,000 + 4,000,000 uint64 keys: collision_mark, rank_build,
-                                 replacement_merge_compact
+  replacement 12,000,000 + 4,000,000 uint64 keys: replacement_merge (mark,
+                                 rank512 build, compaction in one call)
   skewed replacement 2^24-1 + 65,536 keys (clustered)
-  string replacement + FC encode, 4,000,000 + 4,000,000 keys: collision_mark_str,
-                                 rank_build, replacement_merge_compact,
-                                 fc_lengths_scan, fc_emit
+  merge sort of 2^27 uint64 keys with payloads
+  string replacement + FC encode, 4,000,000 + 4,000,000 keys:
+                                 replacement_merge_str, fc_lengths_scan, fc_emit
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank merges its own independent problem of the
@@ -870,14 +870,25 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
     total_bits = int(off[N:].cpu().numpy()[0])
     nwords = (total_bits + 31) // 32
     payload = torch.empty(max(nwords, 4), dtype=torch.uint32, device=dev)
-    stages = [("collision_mark_str", lambda: lsm.collision_mark_str_prefix(Ak, Bk, C, lb, pA, pB,
-                                                                            w1)),
-              ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
-              ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
-                  m, n, C, dir_, lb, refs, oa, ob, cnt, w3)),
+    # The step: the string replacement merge in one call (partition, mark,
+    # which also writes the merge bitmap, the compaction's co-ranks and the
+    # key prefix tables, rank512 build, compaction), then the FC lengths
+    # scan and emit. lb_B is scratch on this path and not written.
+    w5 = lsm.workspace(lsm.LSM_OP_REPLACEMENT_MERGE_STR, m, n, dev)
+    stages = [("replacement_merge_str", lambda: lsm.replacement_merge_str(
+                  Ak, Bk, C, None, pA, pB, dir_, tot, refs, oa, ob, cnt, w5, want_lb=False)),
               ("fc_lengths_scan", lambda: lsm.fc_lengths_scan(fc, refs, N, lcp, ctrl, rec, off, w4)),
               ("fc_emit", lambda: lsm.fc_emit(fc, refs, N, lcp, ctrl, off, nwords, payload))]
     ms, per = time_pipeline(torch, stages, steps, flush)
+    # the same step with the mark, the rank build and the compaction as
+    # separate calls (the compaction then rebuilds the merge bitmap and its
+    # co-ranks from lb_B)
+    stages_sep = [("collision_mark_str", lambda: lsm.collision_mark_str_prefix(
+                      Ak, Bk, C, lb, pA, pB, w1)),
+                  ("rank_build", lambda: lsm.rank_build(C, m, dir_, tot, w2)),
+                  ("replacement_merge_compact", lambda: lsm.replacement_merge_compact(
+                      m, n, C, dir_, lb, refs, oa, ob, cnt, w3))] + stages[1:]
+    ms_sep, per_sep = time_pipeline(torch, stages_sep, steps, flush)
     key_bytes = len(s.A.key_arena) + len(s.B.key_arena) + 8 * (m + n + 2)
     val_bytes = len(s.A.val_arena) + len(s.B.val_arena) + 8 * (m + n + 2) + 4 * (len(s.A.tomb) + len(s.B.tomb))
     alg = (key_bytes + val_bytes                      # keys and values read once
@@ -887,12 +898,17 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
                                "ms_per_step": ms, "gelem_s": (m + n) / (ms * 1e-3) / 1e9,
                                "algorithmic_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
                                "frac": alg / (ms * 1e-3) / 1e9 / peak, "kernel_ms": per,
-                               "gpu_launches_per_step": 7,
-                               "workspace_bytes": {"collision_mark_str": w1.numel(),
-                                                   "rank_build": w2.numel(),
-                                                   "replacement_merge_compact": w3.numel(),
+                               "kernel_ms_note": "replacement_merge_str: its string mark kernel",
+                               "gpu_launches_per_step": 8,
+                               "workspace_bytes": {"replacement_merge_str": w5.numel(),
                                                    "fc_lengths_scan": w4.numel(),
                                                    "prefix_tables": 8 * (pA.numel() + pB.numel())},
+                               "separate_calls": {
+                                   "ms_per_step": ms_sep, "kernel_ms": per_sep,
+                                   "gpu_launches_per_step": 10,
+                                   "workspace_bytes": {"collision_mark_str": w1.numel(),
+                                                       "rank_build": w2.numel(),
+                                                       "replacement_merge_compact": w3.numel()}},
                                "l2": "flushed (256 MiB write) before every step"}
     # The byte profile in place of the bit profile: the same step with the
     # byte-FC lengths scan and emit.
@@ -903,7 +919,7 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
     lsm.bytefc_lengths_scan(fc, refs, N, 0, lcpb, ctrlb, recb, offb, w4)
     total_bytes = int(offb[N:].cpu().numpy()[0])
     payb = torch.empty(max(total_bytes, 16), dtype=torch.uint8, device=dev)
-    stages_b = stages[:3] + [
+    stages_b = stages[:1] + [
         ("bytefc_lengths_scan", lambda: lsm.bytefc_lengths_scan(fc, refs, N, 0, lcpb, ctrlb, recb,
                                                                 offb, w4)),
         ("bytefc_emit", lambda: lsm.bytefc_emit(fc, refs, N, lcpb, ctrlb, offb, total_bytes, 0,
@@ -915,7 +931,7 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
         "gelem_s": (m + n) / (ms_b * 1e-3) / 1e9, "algorithmic_bytes": alg_b,
         "gbs": alg_b / (ms_b * 1e-3) / 1e9, "frac": alg_b / (ms_b * 1e-3) / 1e9 / peak,
         "kernel_ms": {k: per_b[k] for k in ("bytefc_lengths_scan", "bytefc_emit")},
-        "gpu_launches_per_step": 8}
+        "gpu_launches_per_step": 9}
     del lcpb, ctrlb, recb, offb, payb
     # The same step followed by the Elias-Fano navigation over bit_off.
     n_ef, L, nl, nh, G = lsm.ef_sizes(N, total_bits)
@@ -932,7 +948,7 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
         "ms_per_step": ms_ef, "ef_entries": n_ef, "ef_L": L,
         "ef_sparse_entries": int(nsp.item()), "ef_algorithmic_bytes": ef_bytes,
         "kernel_ms": {"fc_ef_build": per_ef["fc_ef_build"]},
-        "gpu_launches_per_step": 9}
+        "gpu_launches_per_step": 10}
 
 
 if __name__ == "__main__":

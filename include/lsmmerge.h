@@ -82,7 +82,8 @@ enum {
   LSM_OP_MERGE_SORT = 7,
   LSM_OP_RANK2048_BUILD = 8,
   LSM_OP_REPLACEMENT_FUSED = 9,
-  LSM_OP_REPLACEMENT_MERGE = 10
+  LSM_OP_REPLACEMENT_MERGE = 10,
+  LSM_OP_REPLACEMENT_MERGE_STR = 11
 };
 
 #define LSM_REF_FROM_B 0x80000000u
@@ -582,6 +583,23 @@ LSM_API int lsm_tune_replace(int kernel, int threads, int items_per_thread);
  * against 87.7 us per step). Process-wide; other modes return
  * LSM_ERR_ARG. */
 LSM_API int lsm_tune_replacement_merge(int mode);
+
+/* The whole replacement merge for byte-string keys in one call: the outputs
+ * of lsm_collision_mark_str_prefix, lsm_rank_build and
+ * lsm_replacement_merge_compact in turn (C, lb_B and the prefix tables when
+ * given, dir, *d_total = R(m), out_refs, ord_A, ord_B, *d_count = m + n -
+ * R(m)), by the same steps; the string mark also records the merge with B
+ * first on ties as a bitmap and the compaction's co-ranks at every fourth of
+ * its tile boundaries, so that the compaction needs no partition and no
+ * lower bounds ([CB] "The three experimental paths", third path). Arguments,
+ * alignment and limits as those calls; C needs no clearing; lb_B, prefixA
+ * and prefixB may be NULL (then not written). ws: at least
+ * lsm_workspace_size(LSM_OP_REPLACEMENT_MERGE_STR, 0, m, n) bytes. */
+LSM_API int lsm_replacement_merge_str(const lsm_bytes *A, int64_t m, const lsm_bytes *B, int64_t n,
+                                      uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
+                                      uint64_t *prefixB, uint32_t *dir, int64_t *d_total,
+                                      uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
+                                      int64_t *d_count, void *ws, size_t ws_bytes, void *stream);
 
 /* ---- test hook ------------------------------------------------------------ */
 /* Launches one block that waits, with the same bounded wait the kernels

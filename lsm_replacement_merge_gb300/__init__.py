@@ -44,6 +44,7 @@ LSM_OP_MERGE_SORT = 7
 LSM_OP_RANK2048_BUILD = 8
 LSM_OP_REPLACEMENT_FUSED = 9
 LSM_OP_REPLACEMENT_MERGE = 10
+LSM_OP_REPLACEMENT_MERGE_STR = 11
 REF_FROM_B = 0x80000000
 ORD_DROPPED = 0xFFFFFFFF
 
@@ -106,6 +107,8 @@ def lib():
                                                 ctypes.c_int),
                 "lsm_replacement_merge": ([P, I, P, I, P, P, P, P, P, P, P, P, P, S, P],
                                           ctypes.c_int),
+                "lsm_replacement_merge_str": ([P, I, P, I, P, P, P, P, P, P, P, P, P, P, P, S, P],
+                                              ctypes.c_int),
                 "lsm_replacement_materialize": ([P, P, P, I, P, P, P, I, P, P, P, P, P, P],
                                                 ctypes.c_int),
                 "lsm_fc_lengths_scan": ([P, P, I, P, P, P, P, P, S, P], ctypes.c_int),
@@ -396,6 +399,49 @@ def collision_mark_str_prefix(A: Bytes, B: Bytes, C=None, lb_B=None, prefixA=Non
                                                _ptr(lb_B), _ptr(prefixA), _ptr(prefixB), _ptr(ws),
                                                ws.numel(), _stream(stream)))
     return C, lb_B, prefixA, prefixB
+
+
+def replacement_merge_str(A: Bytes, B: Bytes, C=None, lb_B=None, prefixA=None, prefixB=None,
+                          dir_=None, d_total=None, refs=None, ord_A=None, ord_B=None, d_count=None,
+                          ws=None, stream=None, want_lb=True, want_prefix=True):
+    """The whole replacement merge for string keys in one call
+    (lsm_replacement_merge_str). Returns (C, lb_B, prefixA, prefixB, dir,
+    d_total, refs, ord_A, ord_B, d_count); lb_B (want_lb=False) and the
+    prefix tables (want_prefix=False) are None when not asked for."""
+    m, n = A.count, B.count
+    dev = A.off.device
+    if C is None:
+        C = _empty(max((m + 31) // 32, 4), torch.uint32, dev)
+    if lb_B is None and want_lb:
+        lb_B = _empty(max(n, 1), torch.uint32, dev)
+    if prefixA is None and want_prefix:
+        prefixA = _empty(max(2 * m, 2), torch.uint64, dev)
+    if prefixB is None and want_prefix:
+        prefixB = _empty(max(2 * n, 2), torch.uint64, dev)
+    if dir_ is None:
+        dir_ = _empty(3 * (m // 512 + 1), torch.uint32, dev)
+    if d_total is None:
+        d_total = _empty(1, torch.int64, dev)
+    if refs is None:
+        refs = _empty(max(m + n, 1), torch.uint32, dev)
+    if ord_A is None:
+        ord_A = _empty(max(m, 1), torch.uint32, dev)
+    if ord_B is None:
+        ord_B = _empty(max(n, 1), torch.uint32, dev)
+    if d_count is None:
+        d_count = _empty(1, torch.int64, dev)
+    if ws is None:
+        ws = workspace(LSM_OP_REPLACEMENT_MERGE_STR, m, n, dev)
+    a, b = A._c(), B._c()
+    _check("lsm_replacement_merge_str",
+           lib().lsm_replacement_merge_str(
+               ctypes.byref(a), m, ctypes.byref(b), n, _ptr(C) if m else None,
+               _ptr(lb_B) if (n and lb_B is not None) else None,
+               _ptr(prefixA) if prefixA is not None else None,
+               _ptr(prefixB) if prefixB is not None else None, _ptr(dir_), _ptr(d_total),
+               _ptr(refs), _ptr(ord_A) if m else None, _ptr(ord_B) if n else None, _ptr(d_count),
+               _ptr(ws), ws.numel(), _stream(stream)))
+    return C, lb_B, prefixA, prefixB, dir_, d_total, refs, ord_A, ord_B, d_count
 
 
 def rank_build(C, m: int, dir_=None, d_total=None, ws=None, stream=None):

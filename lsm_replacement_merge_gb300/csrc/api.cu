@@ -134,6 +134,15 @@ size_t ws_bytes_for(int op, int64_t m, int64_t n, int key_type = LSM_KEY_U64) {
       c.take<uint32_t>(merge_bitmap_words(m + n));
       break;
     }
+    case LSM_OP_REPLACEMENT_MERGE_STR: {
+      const int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
+      const int64_t Dc = replacement_str_tile();
+      c.take<int64_t>((m + n + D - 1) / D + 1);
+      c.take<int64_t>((m + n + Dc - 1) / Dc + 1);
+      c.take<uint64_t>(rank_build_ctas(m));
+      c.take<uint32_t>(merge_bitmap_words(m + n));
+      break;
+    }
     case LSM_OP_REPLACEMENT_COMPACT: {
       const int64_t D = replace_min_tile();
       c.take<int64_t>((m + n + D - 1) / D + 1);
@@ -200,7 +209,7 @@ LSM_API int lsm_workspace_size(int op, int key_type, int64_t m, int64_t n, size_
   if ((op == LSM_OP_MERGE_STABLE || op == LSM_OP_MERGE_SORT) && key_type != LSM_KEY_I32 &&
       key_type != LSM_KEY_U64)
     return LSM_ERR_DTYPE;
-  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_REPLACEMENT_MERGE) return LSM_ERR_ARG;
+  if (op < LSM_OP_MERGE_STABLE || op > LSM_OP_REPLACEMENT_MERGE_STR) return LSM_ERR_ARG;
   *bytes = ws_bytes_for(op, m, n, key_type);
   return LSM_OK;
 }
@@ -458,6 +467,36 @@ LSM_API int lsm_replacement_merge(const uint64_t *A, int64_t m, const uint64_t *
                                               out_refs, ord_A, ord_B, d_count, part_m, part_c, mb,
                                               rank_ws, status_ptr(),
                                               static_cast<cudaStream_t>(stream)));
+}
+
+LSM_API int lsm_replacement_merge_str(const lsm_bytes *A, int64_t m, const lsm_bytes *B, int64_t n,
+                                      uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
+                                      uint64_t *prefixB, uint32_t *dir, int64_t *d_total,
+                                      uint32_t *out_refs, uint32_t *ord_A, uint32_t *ord_B,
+                                      int64_t *d_count, void *ws, size_t ws_bytes, void *stream) {
+  if (m < 0 || n < 0 || !A || !B || !dir || !d_total || !d_count) return LSM_ERR_ARG;
+  if ((m && (!A->arena || !A->off || !C || !ord_A)) || (n && (!B->arena || !B->off || !ord_B)) ||
+      (m + n && !out_refs))
+    return LSM_ERR_ARG;
+  if (m > kMax31 || n > kMax31) return LSM_ERR_OVERFLOW;
+  if ((m && !aligned8(A->arena)) || (n && !aligned8(B->arena))) return LSM_ERR_ALIGN;
+  for (const void *p : {static_cast<const void *>(C), static_cast<const void *>(lb_B),
+                        static_cast<const void *>(prefixA), static_cast<const void *>(prefixB),
+                        static_cast<const void *>(out_refs), static_cast<const void *>(ord_A),
+                        static_cast<const void *>(ord_B)})
+    if (p && !aligned16(p)) return LSM_ERR_ALIGN;
+  if (int r = check_ws(LSM_OP_REPLACEMENT_MERGE_STR, m, n, ws, ws_bytes)) return r;
+  Carver c{static_cast<uint8_t *>(ws)};
+  const int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
+  const int64_t Dc = replacement_str_tile();
+  int64_t *part_m = c.take<int64_t>((m + n + D - 1) / D + 1);
+  int64_t *part_c = c.take<int64_t>((m + n + Dc - 1) / Dc + 1);
+  uint64_t *rank_ws = c.take<uint64_t>(rank_build_ctas(m));
+  uint32_t *mb = c.take<uint32_t>(merge_bitmap_words(m + n));
+  return cuda_status(launch_replacement_merge_str(
+      *A, m, *B, n, C, n ? lb_B : nullptr, m ? prefixA : nullptr, n ? prefixB : nullptr, dir,
+      d_total, out_refs, ord_A, ord_B, d_count, part_m, part_c, mb, rank_ws, status_ptr(),
+      static_cast<cudaStream_t>(stream)));
 }
 
 LSM_API int lsm_tune_replacement_merge(int mode) {

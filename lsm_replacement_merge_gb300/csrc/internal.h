@@ -72,6 +72,14 @@ cudaError_t launch_compact_tiles_rank2048(int64_t m, int64_t n, const uint32_t *
                                           int64_t *d_count, int32_t *status, cudaStream_t s);
 // The whole path (mark, rank512 build, compaction). part_m, part_c: G + 1
 // each; MB: merge_bitmap_words(m + n); rank_ws: rank_build_ctas(m) uint64.
+cudaError_t launch_replacement_merge_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B,
+                                         int64_t n, uint32_t *C, uint32_t *lb_B,
+                                         uint64_t *prefixA, uint64_t *prefixB, uint32_t *dir,
+                                         int64_t *d_total, uint32_t *refs, uint32_t *ord_A,
+                                         uint32_t *ord_B, int64_t *d_count, int64_t *part_m,
+                                         int64_t *part_c, uint32_t *MB, void *rank_ws,
+                                         int32_t *status, cudaStream_t s);
+int64_t replacement_str_tile();
 cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uint64_t *B,
                                         int64_t n, uint32_t *C, uint32_t *lb_B, uint32_t *dir,
                                         int64_t *d_total, uint32_t *refs, uint32_t *ord_A,
@@ -130,6 +138,15 @@ cudaError_t launch_rank2048_query(const uint32_t *C, const uint64_t *dir, const 
 
 // --- strings.cu ---
 // prefixA / prefixB: optional key prefix tables (2 words per key), or NULL.
+// The string mark that also writes the merge bitmap MB (bit p set when
+// position p of the merge with B first on ties holds a B record) and the
+// compaction's co-ranks at every cstep-th tile start (part_c, one more at the
+// end); lb_B may be null.
+cudaError_t launch_collision_mark_str_mb(const lsm_bytes &A, int64_t m, const lsm_bytes &B,
+                                         int64_t n, uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
+                                         uint64_t *prefixB, int64_t *part_i, uint32_t *MB,
+                                         int64_t *part_c, int cstep, int32_t *status,
+                                         cudaStream_t s);
 cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,
                                       uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
                                       uint64_t *prefixB, int64_t *part_i, int32_t *status,

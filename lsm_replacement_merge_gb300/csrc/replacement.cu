@@ -881,6 +881,13 @@ constexpr int kCompactT = 128, kCompactE = 30, kCompactS = 4;
 using MarkDefault = MarkTile<kTileT, kTileE, kMarkS, kMarkHG>;
 using CompactDefault = CompactTile<kCompactT, kCompactE, kCompactS, Rank512At>;
 using Compact2048 = CompactTile<kCompactT, kCompactE, kCompactS, Rank2048At>;
+// The string keys' compaction: tiles of 4 x 896 positions, on every fourth
+// tile boundary of the string mark (which writes those co-ranks and the
+// merge bitmap)
+constexpr int kStrCompactE = 28;
+using CompactStr = CompactTile<kCompactT, kStrCompactE, kCompactS, Rank512At>;
+static_assert(CompactStr::D % (kMarkStrThreads * kMarkStrItems) == 0,
+              "string compaction tiles are whole string mark tiles");
 
 // ---- the whole path in one persistent kernel ------------------------------------
 // The mark and the compaction of each tile in one CTA, by warp roles: the
@@ -1364,6 +1371,30 @@ cudaError_t launch_compact_tiles_rank2048(int64_t m, int64_t n, const uint32_t *
                                           int64_t *d_count, int32_t *status, cudaStream_t s) {
   return launch_compact_with<Compact2048>(m, n, C, Rank2048At{dir, epochs}, lb_B, MB, nullptr,
                                           part_scratch, refs, ord_A, ord_B, d_count, status, s);
+}
+
+int64_t replacement_str_tile() { return CompactStr::D; }
+
+// The whole path for string keys: the string partition and mark (which also
+// writes the merge bitmap and the compaction's co-ranks at every fourth tile
+// start), the rank512 build, the compaction over positions.
+cudaError_t launch_replacement_merge_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B,
+                                         int64_t n, uint32_t *C, uint32_t *lb_B,
+                                         uint64_t *prefixA, uint64_t *prefixB, uint32_t *dir,
+                                         int64_t *d_total, uint32_t *refs, uint32_t *ord_A,
+                                         uint32_t *ord_B, int64_t *d_count, int64_t *part_m,
+                                         int64_t *part_c, uint32_t *MB, void *rank_ws,
+                                         int32_t *status, cudaStream_t s) {
+  constexpr int cstep = CompactStr::D / (kMarkStrThreads * kMarkStrItems);
+  cudaError_t err = cudaSuccess;
+  if (m + n > 0)
+    err = launch_collision_mark_str_mb(A, m, B, n, C, lb_B, prefixA, prefixB, part_m, MB, part_c,
+                                       cstep, status, s);
+  if (err != cudaSuccess) return err;
+  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s);
+  if (err != cudaSuccess) return err;
+  return launch_compact_with<CompactStr>(m, n, C, Rank512At{dir}, nullptr, MB, part_c, nullptr,
+                                         refs, ord_A, ord_B, d_count, status, s);
 }
 
 // The whole path: partition + mark (which also writes the merge bitmap and

@@ -202,7 +202,10 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
                                                                uint32_t *__restrict__ C,
                                                                uint32_t *__restrict__ lb_B,
                                                                uint64_t *__restrict__ prefixA,
-                                                               uint64_t *__restrict__ prefixB) {
+                                                               uint64_t *__restrict__ prefixB,
+                                                               uint32_t *__restrict__ MB,
+                                                               int64_t *__restrict__ part_c,
+                                                               int64_t G, int cstep) {
   static_assert(T % 32 == 0, "whole warps");
   pdl_begin();
   constexpr int D = T * E;
@@ -212,6 +215,8 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
   constexpr int kVCap = D / 2;           // pairs taken as equal, checked after
   __shared__ uint32_t sLB[D];
   __shared__ uint32_t sCw[D / 32 + 4];
+  static_assert(D % 32 == 0, "a tile's merge bitmap is whole words");
+  __shared__ uint32_t sMB[D / 32];  // the tile's merge bitmap words (when MB is given)
   __shared__ uint32_t sV[kVCap];
   __shared__ int sVn;
   const int tid = threadIdx.x;
@@ -226,6 +231,7 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
   const int64_t w0 = i0 >> 5;
   const int nw = na > 0 ? static_cast<int>(((i1 - 1) >> 5) - w0 + 1) : 0;
   for (int x = tid; x < nw; x += T) sCw[x] = 0u;
+  for (int x = tid; x < D / 32; x += T) sMB[x] = 0u;
 
   // A slots [A[i0-1]] A[i0..i1), then B slots B[j0..j1) [B[j1]]; start
   // offsets in sBeg with one end offset after each side's run
@@ -278,6 +284,7 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
   const int nbh = static_cast<int>(n - j0 < D + 1 ? n - j0 : D + 1);
   const int wb0 = static_cast<int>(i0 - (w0 << 5));
   const uint32_t i0u = static_cast<uint32_t>(i0);
+  bool tie0 = false;  // thread 0: A[i0-1] = B[j0], the pair that straddles the tile's start
   for (int pass = 0;; ++pass) {
     const bool exact = pass > 0;
     int lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
@@ -295,6 +302,7 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
     // equal to it (then that B's lower bound is one less than the A count).
     const bool pq = d < cnt && ai + hp > 0 && bi < nbh;
     bool prev_eq = keys.cmp(pq, hp + ai - 1, bi, exact) == 0 && pq;
+    if (tid == 0) tie0 = prev_eq;
     for (int s = 0; s < E; ++s) {
       // c = cmp(A head, B head); B head may be B[j1] (one past the tile)
       // only for the collision test of A's last element.
@@ -308,11 +316,18 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
         if (has_b && c == 0) {
           const int x = wb0 + ai;
           atomicOr(&sCw[x >> 5], 1u << (x & 31));
+          // B[j1] equal to the tile's last A key sits at the tile's last
+          // position of the merge with B first on ties
+          if (MB && bi == nb) atomicOr(&sMB[(cnt - 1) >> 5], 1u << ((cnt - 1) & 31));
         }
         prev_eq = has_b && c == 0;
         ++ai;
       } else {
         sLB[bi] = i0u + static_cast<uint32_t>(ai) - (prev_eq ? 1u : 0u);
+        // its position in the merge with B first on ties; one before the
+        // tile (in the previous tile) for B[j0] equal to A[i0-1]
+        const int rp = ai + bi - (prev_eq ? 1 : 0);
+        if (MB && rp >= 0) atomicOr(&sMB[rp >> 5], 1u << (rp & 31));
         prev_eq = false;
         ++bi;
       }
@@ -328,9 +343,19 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
     }
     if (!__syncthreads_or(wrong)) break;
     for (int x = tid; x < nw; x += T) sCw[x] = 0u;
+    for (int x = tid; x < D / 32; x += T) sMB[x] = 0u;
     __syncthreads();
   }
-  for (int x = tid; x < nb; x += T) lb_B[j0 + x] = sLB[x];
+  if (lb_B)
+    for (int x = tid; x < nb; x += T) lb_B[j0 + x] = sLB[x];
+  if (MB) {
+    // the tile's merge bitmap words (tile-owned: D is whole words), and the
+    // compaction's co-rank at every cstep-th tile start (B first on ties)
+    const int nmw = (cnt + 31) / 32;
+    for (int x = tid; x < nmw; x += T) MB[g * (D / 32) + x] = sMB[x];
+    if (tid == 0 && g % cstep == 0) part_c[g / cstep] = i0 - (tie0 ? 1 : 0);
+    if (tid == 0 && g == G - 1) part_c[(G + cstep - 1) / cstep] = m;
+  }
   for (int x = tid; x < nw; x += T) {
     const int64_t w = w0 + x;
     const uint32_t bits = sCw[x];
@@ -344,8 +369,17 @@ __global__ void __launch_bounds__(T) collision_mark_str_kernel(lsm_bytes A, int6
 
 cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,
                                       uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
-                                      uint64_t *prefixB, int64_t *part_i, int32_t * /*status*/,
+                                      uint64_t *prefixB, int64_t *part_i, int32_t *status,
                                       cudaStream_t s) {
+  return launch_collision_mark_str_mb(A, m, B, n, C, lb_B, prefixA, prefixB, part_i, nullptr,
+                                      nullptr, 1, status, s);
+}
+
+cudaError_t launch_collision_mark_str_mb(const lsm_bytes &A, int64_t m, const lsm_bytes &B,
+                                         int64_t n, uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
+                                         uint64_t *prefixB, int64_t *part_i, uint32_t *MB,
+                                         int64_t *part_c, int cstep, int32_t * /*status*/,
+                                         cudaStream_t s) {
   constexpr int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t nwords = (m + 31) / 32;
@@ -360,7 +394,7 @@ cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_b
   // SM leave the room free (measured: partition + mark 206 us against 209.5)
   err = launch_kernel(true, collision_mark_str_kernel<kMarkStrThreads, kMarkStrItems>,
                       static_cast<unsigned>(G), kMarkStrThreads, 0, s, A, m, B, n, part_i, C, lb_B,
-                      prefixA, prefixB);
+                      prefixA, prefixB, MB, part_c, G, cstep);
   profile_after(s);
   return err;
 }

@@ -1,5 +1,7 @@
 """GPU parity for the string-key collision mark (and the key-free compaction
-that follows it) against the oracle's string replacement walk."""
+that follows it) against the oracle's string replacement walk, as separate
+calls and as the whole path in one call (lsm_replacement_merge_str, whose
+string mark also writes the merge bitmap and the compaction's co-ranks)."""
 import numpy as np
 import pytest
 
@@ -38,16 +40,44 @@ def run_str(lsm, s):
     return down(C)[: (m + 31) // 32], down(lb), down(refs)[:N], down(ordA), down(ordB)
 
 
+def run_whole_str(lsm, s):
+    """lsm_replacement_merge_str: the same outputs in one call, plus the
+    directory, R(m), the count and the prefix tables."""
+    dev = torch.device("cuda:0")
+    A = lsm.Bytes.from_numpy(s.A.key_arena, s.A.key_off, dev)
+    B = lsm.Bytes.from_numpy(s.B.key_arena, s.B.key_off, dev)
+    m, n = A.count, B.count
+    C, lb, pA, pB, dir_, tot, refs, ordA, ordB, cnt = lsm.replacement_merge_str(A, B)
+    N = int(cnt.item())
+    out = dict(C=down(C)[: (m + 31) // 32], lb=down(lb)[:n], refs=down(refs)[:N],
+               ordA=down(ordA)[:m], ordB=down(ordB)[:n], dir=down(dir_), total=int(tot.item()),
+               count=N, pA=down(pA)[: 2 * m], pB=down(pB)[: 2 * n])
+    if m + n:
+        # the prefix tables equal those of the separate mark call
+        _, _, qA, qB = lsm.collision_mark_str_prefix(A, B)
+        assert np.array_equal(out["pA"], down(qA)[: 2 * m])
+        assert np.array_equal(out["pB"], down(qB)[: 2 * n])
+    return out
+
+
 def check(lsm, s):
-    got = run_str(lsm, s)
     r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    got = run_str(lsm, s)
     if got is None:
         assert r.count == 0
-        return
-    C, lb, refs, ordA, ordB = got
-    assert np.array_equal(C, r.C) and np.array_equal(lb, r.lb_B)
-    assert np.array_equal(refs, r.refs)
-    assert np.array_equal(ordA, r.ord_A) and np.array_equal(ordB, r.ord_B)
+    else:
+        C, lb, refs, ordA, ordB = got
+        assert np.array_equal(C, r.C) and np.array_equal(lb, r.lb_B)
+        assert np.array_equal(refs, r.refs)
+        assert np.array_equal(ordA, r.ord_A) and np.array_equal(ordB, r.ord_B)
+    # the whole path in one call, on the same input
+    m = len(s.A.key_off) - 1
+    w = run_whole_str(lsm, s)
+    assert w["count"] == r.count and w["total"] == m + (len(s.B.key_off) - 1) - r.count
+    assert np.array_equal(w["C"], r.C) and np.array_equal(w["lb"], r.lb_B)
+    assert np.array_equal(w["refs"], r.refs)
+    assert np.array_equal(w["ordA"], r.ord_A) and np.array_equal(w["ordB"], r.ord_B)
+    assert np.array_equal(w["dir"], oracle.rank512_dir(r.C, m))
 
 
 @pytest.mark.parametrize("case", list(_str_cases()))
@@ -97,3 +127,19 @@ def test_keys_with_one_16_byte_prefix(lsm):
 
 def test_config_strings_4M(lsm):
     check(lsm, synth.strings())
+
+
+def test_whole_path_str_without_lower_bounds_or_tables(lsm):
+    # lb_B and the prefix tables are optional on the whole path
+    st = synth.strings(seed=9, count=5000, fanout=8, depth=2, max_suffix=20)
+    dev = torch.device("cuda:0")
+    A = lsm.Bytes.from_numpy(st.A.key_arena, st.A.key_off, dev)
+    B = lsm.Bytes.from_numpy(st.B.key_arena, st.B.key_off, dev)
+    r = oracle.replacement_str(st.A.key_arena, st.A.key_off, st.B.key_arena, st.B.key_off)
+    C, lb, pA, pB, dir_, tot, refs, ordA, ordB, cnt = lsm.replacement_merge_str(
+        A, B, want_lb=False, want_prefix=False)
+    assert lb is None and pA is None and pB is None
+    N = int(cnt.item())
+    assert N == r.count
+    assert np.array_equal(down(refs)[:N], r.refs)
+    assert np.array_equal(down(ordA), r.ord_A) and np.array_equal(down(ordB), r.ord_B)
