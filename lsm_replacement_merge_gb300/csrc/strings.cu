@@ -30,7 +30,7 @@ namespace {
 struct StrAFirst {
   lsm_bytes A, B;
   __device__ __forceinline__ bool too_small(int64_t i, int64_t k) const {
-    return key_cmp(key_at(A, i), key_at(B, k - i - 1)) <= 0;
+    return key_cmp_prefix16(key_at(A, i), key_at(B, k - i - 1)) <= 0;
   }
 };
 
