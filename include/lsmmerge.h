@@ -446,7 +446,10 @@ LSM_API int lsm_fc_emit(const lsm_fc_input *in, const uint32_t *refs, int64_t N,
  *   (W - 1)-byte value and the length is left out.
  * LEB128 is unsigned: seven bits per byte, low group first, the top bit set
  * on every byte but the last. Records follow each other with no padding.
- * Inputs as lsm_fc_lengths_scan's (the prefix tables are not used).
+ * Inputs as lsm_fc_lengths_scan's; with the prefix tables, p_i comes from
+ * the keys' first 16 bytes there (their first differing byte, clamped to the
+ * shorter key), the arenas being read only when both keys are longer than
+ * 16 bytes and those agree.
  * lsm_bytefc_lengths_scan writes lcp[i] = p_i, ctrl[i] = b_i, rec_bytes[i]
  * (the record's bytes) and byte_off[0..N] (exclusive scan, byte_off[N] =
  * the payload's bytes); rec_bytes and byte_off 16-byte aligned; ws sized by

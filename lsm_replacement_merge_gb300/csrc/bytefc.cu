@@ -41,6 +41,7 @@ constexpr int kBfTile = kBfThreads * kBfItems;
 struct BSource {
   lsm_bytes key, val;
   const uint32_t *tomb;
+  const uint64_t *prefix;  // the key prefix table (bytes 0..15 big-endian), or NULL
 };
 
 __device__ __forceinline__ const BSource &bpick(const BSource &a, const BSource &b, uint32_t ref) {
@@ -106,7 +107,23 @@ __global__ void __launch_bounds__(kBfThreads) bytefc_lengths_kernel(
       const BSource &ps = bpick(sa, sb, pr);
       const uint64_t pks = __ldg(ps.key.off + pidx);
       Kp = __ldg(ps.key.off + pidx + 1) - pks;
-      p = byte_lcp(ps.key.arena, pks, Kp, src.key.arena, ks, K);
+      if (src.prefix && ps.prefix) {
+        // the first 16 bytes from the prefix tables: the first differing
+        // byte of the big-endian words, clamped to the shorter key; bytes
+        // past 16 only when both keys are longer and the 16 agree
+        const ulonglong2 u = __ldg(reinterpret_cast<const ulonglong2 *>(ps.prefix) + pidx);
+        const ulonglong2 v = __ldg(reinterpret_cast<const ulonglong2 *>(src.prefix) + idx);
+        const uint64_t L = Kp < K ? Kp : K;
+        const uint64_t d0 = u.x ^ v.x, d1 = u.y ^ v.y;
+        if (d0) p = static_cast<uint64_t>(__clzll(static_cast<long long>(d0))) / 8;
+        else if (d1) p = 8 + static_cast<uint64_t>(__clzll(static_cast<long long>(d1))) / 8;
+        else p = L > 16 ? 16 + byte_lcp(ps.key.arena, pks + 16, Kp - 16, src.key.arena, ks + 16,
+                                        K - 16)
+                        : 16;
+        p = p < L ? p : L;
+      } else {
+        p = byte_lcp(ps.key.arena, pks, Kp, src.key.arena, ks, K);
+      }
     }
     const uint64_t b = (i % 15 == 0) ? 1 + p : Kp - p;
     uint64_t v;
@@ -327,8 +344,9 @@ __global__ void __launch_bounds__(kBeRecords) bytefc_emit_kernel(
   if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-BSource bsource(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb) {
-  return BSource{key, val, tomb};
+BSource bsource(const lsm_bytes &key, const lsm_bytes &val, const uint32_t *tomb,
+                const uint64_t *prefix = nullptr) {
+  return BSource{key, val, tomb, prefix};
 }
 
 }  // namespace
@@ -344,9 +362,9 @@ cudaError_t launch_bytefc_lengths_scan(const lsm_fc_input &in, const uint32_t *r
   profile_before(s);
   cudaError_t err = launch_kernel(false, bytefc_lengths_kernel,
                                   static_cast<unsigned>(tiles > 0 ? tiles : 1), kBfThreads, 0, s,
-                                  bsource(in.keyA, in.valA, in.tombA),
-                                  bsource(in.keyB, in.valB, in.tombB), refs, N, W, lcp, ctrl,
-                                  rec_bytes, tile_sum, status);
+                                  bsource(in.keyA, in.valA, in.tombA, in.prefixA),
+                                  bsource(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, W, lcp,
+                                  ctrl, rec_bytes, tile_sum, status);
   if (err == cudaSuccess) err = launch_fc_offsets(rec_bytes, N, tile_sum, byte_off, s);
   profile_after(s);
   return err;

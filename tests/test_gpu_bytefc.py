@@ -15,7 +15,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 from tests.gpu_util import down, up  # noqa: E402
-from tests.test_gpu_fc import device_input, gpu_refs  # noqa: E402
+from tests.test_gpu_fc import _prefix_table, device_input, gpu_refs  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -43,6 +43,16 @@ def check_bytefc(lsm, s, W=0):
     assert np.array_equal(down(ctrl)[:N], exp.ctrl)
     assert np.array_equal(down(rec)[:N], exp.rec_bits)
     assert np.array_equal(down(off), exp.bit_off)
+    # the same lengths with the key prefix tables (the LCP from their first
+    # 16 bytes), built on the host from their definition
+    if fc.keyA.count and fc.keyB.count:
+        fc2 = device_input(lsm, s)
+        fc2.prefixA = up(_prefix_table(s.A.key_arena, s.A.key_off))
+        fc2.prefixB = up(_prefix_table(s.B.key_arena, s.B.key_off))
+        lcp2, ctrl2, rec2, off2 = lsm.bytefc_lengths_scan(fc2, refs, N, W)
+        assert np.array_equal(down(lcp2)[:N], exp.lcp)
+        assert np.array_equal(down(rec2)[:N], exp.rec_bits)
+        assert np.array_equal(down(off2), exp.bit_off)
     total = exp.total_bits
     payload = lsm.bytefc_emit(fc, refs, N, lcp, ctrl, off, total + 5, W,
                               payload=torch.full((total + 5,), 0xEE, dtype=torch.uint8,
