@@ -276,6 +276,102 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
   }
 }
 
+// The same lengths when both sources carry key prefix tables, without the
+// shared-memory phases: each thread takes four consecutive records and the
+// record before them, issues every load of the five (refs, key extents,
+// prefix words; value extents and tombstone words of its own four) before
+// using any, and computes the bit LCP, control and length of each; the
+// tile's total goes to tile_sum as above. A record's predecessor is loaded
+// again by the thread before it (measured faster than staging the tile).
+#ifndef FC_FLAT_MIN_BLOCKS
+#define FC_FLAT_MIN_BLOCKS 1
+#endif
+__global__ void __launch_bounds__(kFcThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_flat_kernel(
+    Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N, uint32_t *__restrict__ lcp,
+    uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec_bits, uint64_t *__restrict__ bit_off,
+    uint64_t *tile_sum, int32_t *status) {
+  pdl_begin();
+  __shared__ uint64_t scratch[kFcThreads / 32 + 1];
+  const int tid = threadIdx.x;
+  if (N == 0) {
+    if (tid == 0 && blockIdx.x == 0) bit_off[0] = 0;
+    return;
+  }
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kFcTile + int64_t(tid) * kFcItems;
+  constexpr int Q = kFcItems + 1;  // slot 0: the record before the thread's first
+  uint32_t rr[Q];
+  uint64_t kb[Q], ke[Q], p0[Q], p1[Q];
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int64_t i = first - 1 + q;
+    rr[q] = (i >= 0 && i < N) ? __ldg(refs + i) : 0u;
+  }
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int64_t i = first - 1 + q;
+    const bool live = i >= 0 && i < N;
+    const uint32_t idx = rr[q] & ~LSM_REF_FROM_B;
+    const Source &src = pick(sa, sb, rr[q]);
+    kb[q] = live ? __ldg(src.key.off + idx) : 0;
+    ke[q] = live ? __ldg(src.key.off + idx + 1) : 0;
+    ulonglong2 v = make_ulonglong2(0, 0);
+    if (live) v = __ldg(reinterpret_cast<const ulonglong2 *>(src.prefix) + idx);
+    p0[q] = v.x;
+    p1[q] = v.y;
+  }
+  uint64_t vb[kFcItems], ve[kFcItems];
+  uint32_t tw[kFcItems];
+#pragma unroll
+  for (int q = 0; q < kFcItems; ++q) {
+    const int64_t i = first + q;
+    const bool live = i < N;
+    const uint32_t idx = rr[q + 1] & ~LSM_REF_FROM_B;
+    const Source &src = pick(sa, sb, rr[q + 1]);
+    vb[q] = live ? __ldg(src.val.off + idx) : 0;
+    ve[q] = live ? __ldg(src.val.off + idx + 1) : 0;
+    tw[q] = (live && src.tomb) ? __ldg(src.tomb + (idx >> 5)) : 0u;
+  }
+  uint64_t sum = 0;
+  bool overflow = false;
+#pragma unroll
+  for (int q = 0; q < kFcItems; ++q) {
+    const int64_t i = first + q;
+    if (i >= N) break;
+    const uint32_t idx = rr[q + 1] & ~LSM_REF_FROM_B;
+    const uint64_t k = 8 * (ke[q + 1] - kb[q + 1]);
+    uint64_t l = 0, k_prev = 0;
+    if (i > 0) {
+      k_prev = 8 * (ke[q] - kb[q]);
+      const uint64_t L = k_prev < k ? k_prev : k;
+      const uint64_t d0 = p0[q] ^ p0[q + 1], d1 = p1[q] ^ p1[q + 1];
+      l = d0 ? static_cast<uint64_t>(__clzll(static_cast<long long>(d0)))
+             : (d1 ? 64 + static_cast<uint64_t>(__clzll(static_cast<long long>(d1))) : 128);
+      if (l > L) l = L;
+      if (l == 128 && L > 128) {
+        const uint8_t *pa = pick(sa, sb, rr[q]).key.arena;
+        const uint8_t *ca = pick(sa, sb, rr[q + 1]).key.arena;
+        l = 128 + bit_lcp(pa, kb[q] + 16, ke[q] - kb[q] - 16, ca, kb[q + 1] + 16,
+                          ke[q + 1] - kb[q + 1] - 16);
+      }
+    }
+    uint64_t v = 1;  // a tombstone is one bit
+    if (!((tw[q] >> (idx & 31)) & 1u)) {
+      const uint64_t vbytes = ve[q] - vb[q];
+      v = 1 + eg0_len(vbytes) + 8 * vbytes;
+    }
+    const uint64_t c = (i % 15 == 0) ? 1 + l : k_prev - l;
+    const uint64_t Lrec = eg0_len(c) + eg0_len(k - l) + (k - l) + v;
+    overflow |= (Lrec > 0xFFFFFFFFull) || (c > 0xFFFFFFFFull) || (v > 0xFFFFFFFFull);
+    lcp[i] = static_cast<uint32_t>(l);
+    ctrl[i] = static_cast<uint32_t>(c);
+    rec_bits[i] = static_cast<uint32_t>(Lrec);
+    sum += Lrec;
+  }
+  if (overflow) report(status, LSM_ERR_OVERFLOW);
+  const uint64_t agg = block_sum<kFcThreads, uint64_t>(sum, scratch);
+  if (tid == 0) tile_sum[blockIdx.x] = agg;
+}
+
 // The exclusive prefix sums of the tile totals, in place, by one CTA in
 // chunks of kScanThreads * 8; tile_sum[tiles] receives the grand total.
 constexpr int kScanThreads = 1024;
@@ -767,21 +863,34 @@ size_t fc_scan_workspace_bytes(int64_t N) {
   return static_cast<size_t>(256 + align_up(fc_scan_tiles(N) * 8, 256));
 }
 
+extern int g_fc_lengths_flat;
+
 cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs, int64_t N,
                                    uint32_t *lcp, uint32_t *ctrl, uint32_t *rec_bits,
                                    uint64_t *bit_off, void *ws, int32_t *status, cudaStream_t s) {
   const int64_t tiles = fc_scan_tiles(N);
   uint64_t *tile_sum = static_cast<uint64_t *>(ws);  // tiles + 1 entries
-  cudaError_t err = cudaFuncSetAttribute(fc_lengths_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(FcLayout::kBytes));
-  if (err != cudaSuccess) return err;
+  // prefix tables on both sides (an empty side needs none): the flat form
+  const bool flat = (in.prefixA || in.m == 0) && (in.prefixB || in.n == 0) &&
+                    (in.prefixA || in.prefixB) && g_fc_lengths_flat;
+  cudaError_t err = cudaSuccess;
+  if (!flat) {
+    err = cudaFuncSetAttribute(fc_lengths_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(FcLayout::kBytes));
+    if (err != cudaSuccess) return err;
+  }
   profile_before(s);
-  err = launch_kernel(false, fc_lengths_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
-                      kFcThreads, FcLayout::kBytes, s,
-                      make_source(in.keyA, in.valA, in.tombA, in.prefixA),
-                      make_source(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, lcp, ctrl,
-                      rec_bits, bit_off, tile_sum, status);
+  if (flat)
+    err = launch_kernel(false, fc_lengths_flat_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
+                        kFcThreads, 0, s, make_source(in.keyA, in.valA, in.tombA, in.prefixA),
+                        make_source(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, lcp, ctrl,
+                        rec_bits, bit_off, tile_sum, status);
+  else
+    err = launch_kernel(false, fc_lengths_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
+                        kFcThreads, FcLayout::kBytes, s,
+                        make_source(in.keyA, in.valA, in.tombA, in.prefixA),
+                        make_source(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, lcp, ctrl,
+                        rec_bits, bit_off, tile_sum, status);
   if (err == cudaSuccess && N > 0)
     // the one-CTA scan and the offsets pass after it launch early (PDL): an
     // early-launched CTA here holds no room that a wave before it needs
@@ -795,6 +904,13 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
 }
 
 int64_t fc_tile_records() { return kFcTile; }
+
+// 1: the flat lengths kernel when prefix tables are given (the default);
+// 0: always the staged one (for comparison).
+#ifndef FC_LENGTHS_FLAT
+#define FC_LENGTHS_FLAT 1
+#endif
+int g_fc_lengths_flat = FC_LENGTHS_FLAT;
 
 cudaError_t launch_fc_offsets(const uint32_t *rec, int64_t N, uint64_t *tile_sum, uint64_t *off,
                               cudaStream_t s) {
