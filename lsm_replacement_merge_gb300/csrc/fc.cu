@@ -31,12 +31,11 @@
 // fc_emit_kernel: persistent; each CTA writes a contiguous range of runs of
 // 4096 payload words (the word-owned emit at CTA granularity: every global
 // word is written once, by the CTA that owns it). The CTA's first run finds
-// its first record by 32-way probes over bit_off; every run stages the
-// metadata of the records from there in shared memory, one thread per
-// record writes the record's fields into the run's word buffer in shared
-// memory (words shared by two fields or records are ORed, words inside a
-// key or value field are stored whole), and the run leaves with one bulk
-// store.
+// its first record by 32-way probes over bit_off; in every run one thread
+// per record loads that record's metadata and writes its fields into the
+// run's word buffer in shared memory (words shared by two fields or records
+// are ORed, words inside a key or value field are stored whole), and the run
+// leaves with one bulk store.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -55,7 +54,7 @@ constexpr int kFcTile = kFcThreads * kFcItems;
 constexpr int kEmitThreads = 256;
 constexpr int kEmitWords = 16;  // words per thread
 constexpr int kEmitRun = kEmitThreads * kEmitWords;
-constexpr int kEmitMaxRec = 512;  // records whose metadata one run stages at a time
+constexpr int kEmitMaxRec = 512;  // records one chunk of a run loads at a time
 
 __device__ __forceinline__ uint64_t eg0_len(uint64_t x) {
   return 2 * static_cast<uint64_t>(63 - __clzll(static_cast<long long>(x + 1))) + 1;
@@ -484,21 +483,11 @@ __device__ __forceinline__ int64_t warp_record_at(const uint64_t *bit_off, int64
   return lo;
 }
 
-// Shared-memory layout of one emit run: the output words and the metadata
-// of up to kEmitMaxRec records overlapping the run.
+// Shared-memory layout of one emit run: its output words.
 struct EmitLayout {
-  static constexpr int64_t kOut = 0;                                   // u32[run]
-  static constexpr int64_t kS = kOut + int64_t(kEmitRun) * 4;          // u64[R + 1] start bits
-  static constexpr int64_t kKb = kS + int64_t(kEmitMaxRec + 1) * 8;    // u64 key byte begin
-  static constexpr int64_t kVb = kKb + int64_t(kEmitMaxRec) * 8;       // u64 value byte begin
-  static constexpr int64_t kC = kVb + int64_t(kEmitMaxRec) * 8;        // u32 control
-  static constexpr int64_t kL = kC + int64_t(kEmitMaxRec) * 4;         // u32 LCP bits
-  static constexpr int64_t kKl = kL + int64_t(kEmitMaxRec) * 4;        // u32 key bytes
-  static constexpr int64_t kVl = kKl + int64_t(kEmitMaxRec) * 4;       // u32 value bytes
-  static constexpr int64_t kF = kVl + int64_t(kEmitMaxRec) * 4;        // u32 flags
-  static constexpr int64_t kBytes = kF + int64_t(kEmitMaxRec) * 4 + 64;
+  static constexpr int64_t kOut = 0;                           // u32[run]
+  static constexpr int64_t kBytes = kOut + int64_t(kEmitRun) * 4 + 64;
 };
-constexpr uint32_t kFlagFromB = 1u, kFlagTomb = 2u;
 
 // ---- record-centric composition into a run's word buffer ------------------------
 // buf holds the run's words [w0, w0 + wn); only bits in the window [lo, hi)
@@ -714,12 +703,14 @@ __device__ __forceinline__ void emit_record32(uint32_t *buf, int H, int P, const
 
 // Persistent: CTA c writes the contiguous runs [c R / P, (c + 1) R / P) of
 // kEmitRun payload words each (R runs, P CTAs). Only its first run searches
-// bit_off for the record holding the run's first bit; every run then stages
-// the metadata of kEmitMaxRec records from that record on (more chunks when
-// the run needs more), composes the records that meet the run into a shared
-// word buffer (one thread per record), and takes the record holding the
-// next run's first bit from the staged offsets. Each run leaves by one bulk
-// store.
+// bit_off for the record holding the run's first bit; in every run each
+// thread then loads the metadata of its records among the kEmitMaxRec from
+// that record on (more chunks when the run needs more) and composes those
+// that meet the run into a shared word buffer at once, with no staging
+// arrays and no barrier between loads and composition (measured: 322 us
+// against 334.5 us with the metadata staged in shared memory first); the
+// record holding the next run's first bit is named by its own thread. Each
+// run leaves by one bulk store.
 __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N,
     const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
@@ -728,15 +719,7 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
   using L = EmitLayout;
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t *sOut = reinterpret_cast<uint32_t *>(smem + L::kOut);
-  uint64_t *sS = reinterpret_cast<uint64_t *>(smem + L::kS);
-  uint64_t *sKb = reinterpret_cast<uint64_t *>(smem + L::kKb);
-  uint64_t *sVb = reinterpret_cast<uint64_t *>(smem + L::kVb);
-  uint32_t *sC = reinterpret_cast<uint32_t *>(smem + L::kC);
-  uint32_t *sL = reinterpret_cast<uint32_t *>(smem + L::kL);
-  uint32_t *sKl = reinterpret_cast<uint32_t *>(smem + L::kKl);
-  uint32_t *sVl = reinterpret_cast<uint32_t *>(smem + L::kVl);
-  uint32_t *sF = reinterpret_cast<uint32_t *>(smem + L::kF);
-  __shared__ int64_t sNext;  // record holding the next run's first bit
+  __shared__ int64_t sNext2[2];  // record holding run r's first bit, in slot r & 1
   const int tid = threadIdx.x;
   const int64_t runs = (nwords + kEmitRun - 1) / kEmitRun;
   const int64_t P = gridDim.x;
@@ -746,7 +729,7 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     const int64_t lo0 = ra * kEmitRun * 32;
     int64_t r = 0;
     if (lo0 < total) r = warp_record_at(bit_off, 0, N - 1, static_cast<uint64_t>(lo0));
-    if (tid == 0) sNext = r;
+    if (tid == 0) sNext2[0] = sNext2[1] = r;
   }
   for (int64_t run = ra; run < rb; ++run) {
     const int64_t w0 = run * kEmitRun;
@@ -754,24 +737,25 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     const int64_t lo = w0 * 32;
     const int64_t hi = (w0 + wn) * 32 < total ? (w0 + wn) * 32 : total;
     for (int x = tid; x < kEmitRun; x += kEmitThreads) sOut[x] = 0u;
-    __syncthreads();  // sNext is set and sOut is clear
-    int64_t c0 = sNext;
+    __syncthreads();  // this run's first record is set and sOut is clear
+    int64_t c0 = sNext2[run & 1];
+    // each thread loads its records' metadata and composes them at once (no
+    // staging arrays, no barrier between loads and composition); the record
+    // holding bit hi names the next run's first record (in the other slot of
+    // sNext2, which no thread still reads)
     while (lo < hi) {
-      // records c0 .. c0 + R - 1, the first holding bit max(lo, ...) of this run
       const int R = static_cast<int>(N - c0 < kEmitMaxRec ? N - c0 : kEmitMaxRec);
-      // two records per thread per round; every load of a round is issued
-      // before any is used (the value offsets are read for tombstones too,
-      // which keeps them off the tombstone bit's dependency chain)
+      bool more = false;
       for (int x0 = tid; x0 < R; x0 += 2 * kEmitThreads) {
-        uint32_t ref[2];
-        uint64_t bo[2];
-        uint32_t cc[2], ll[2];
+        uint32_t ref[2], cc[2], ll[2];
+        uint64_t bo[2], be[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int x = x0 + u * kEmitThreads;
           const int64_t r = c0 + (x < R ? x : x0);
           ref[u] = __ldg(refs + r);
           bo[u] = __ldg(bit_off + r);
+          be[u] = __ldg(bit_off + r + 1);
           cc[u] = __ldg(ctrl + r);
           ll[u] = __ldg(lcp + r);
         }
@@ -791,50 +775,35 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
         for (int u = 0; u < 2; ++u) {
           const int x = x0 + u * kEmitThreads;
           if (x >= R) continue;
+          const int64_t r = c0 + x;
+          const int64_t rs = static_cast<int64_t>(bo[u]), re = static_cast<int64_t>(be[u]);
+          if (rs <= hi && hi < re) sNext2[(run + 1) & 1] = r;
+          if (x == R - 1 && re <= hi && r + 1 < N) {
+            // the chunk ends at or before hi: the record after it starts
+            // the next run, or the next chunk goes on with this run
+            if (re == hi) sNext2[(run + 1) & 1] = r + 1;
+            else more = true;
+          }
+          if (rs >= hi) continue;
           const uint32_t idx = ref[u] & ~LSM_REF_FROM_B;
           const bool tomb = (tw[u] >> (idx & 31)) & 1u;
-          sS[x] = bo[u];
-          if (x == R - 1) sS[R] = __ldg(bit_off + c0 + x + 1);
-          sC[x] = cc[u];
-          sL[x] = ll[u];
-          sKb[x] = kb[u];
-          sKl[x] = static_cast<uint32_t>(ke[u] - kb[u]);
-          sVb[x] = tomb ? 0 : vb[u];
-          sVl[x] = tomb ? 0u : static_cast<uint32_t>(ve[u] - vb[u]);
-          sF[x] = ((ref[u] & LSM_REF_FROM_B) ? kFlagFromB : 0u) | (tomb ? kFlagTomb : 0u);
+          const Source &src = pick(sa, sb, ref[u]);
+          RecordMeta M;
+          M.s = rs;
+          M.e = re;
+          M.c = cc[u];
+          M.l = ll[u];
+          M.key = KeyRef{src.key.arena, kb[u], ke[u]};
+          M.k = 8 * (ke[u] - kb[u]);
+          M.tomb = tomb;
+          M.val = KeyRef{src.val.arena, tomb ? 0 : vb[u], tomb ? 0 : ve[u]};
+          if (M.e - M.s < (int64_t(1) << 30))
+            emit_record32(sOut, static_cast<int>(hi - lo), static_cast<int>(M.s - lo), M);
+          else
+            emit_record(sOut, w0, lo, hi, M);
         }
       }
-      __syncthreads();
-      for (int x = tid; x < R && static_cast<int64_t>(sS[x]) < hi; x += kEmitThreads) {
-        RecordMeta M;
-        M.s = static_cast<int64_t>(sS[x]);
-        M.e = static_cast<int64_t>(sS[x + 1]);
-        M.c = sC[x];
-        M.l = sL[x];
-        const uint32_t f = sF[x];
-        const Source &src = (f & kFlagFromB) ? sb : sa;
-        M.key = KeyRef{src.key.arena, sKb[x], sKb[x] + sKl[x]};
-        M.k = 8 * static_cast<uint64_t>(sKl[x]);
-        M.tomb = (f & kFlagTomb) != 0;
-        M.val = KeyRef{src.val.arena, sVb[x], sVb[x] + sVl[x]};
-        if (M.e - M.s < (int64_t(1) << 30))
-          emit_record32(sOut, static_cast<int>(hi - lo), static_cast<int>(M.s - lo), M);
-        else
-          emit_record(sOut, w0, lo, hi, M);
-      }
-      const bool more = static_cast<int64_t>(sS[R]) < hi && c0 + R < N;
-      if (!more && tid == 0) {
-        // the record holding bit hi: the first staged record ending past it
-        int a = 0, b = R;
-        while (a < b) {
-          const int mid = (a + b) >> 1;
-          if (static_cast<int64_t>(sS[mid + 1]) <= hi) a = mid + 1;
-          else b = mid;
-        }
-        sNext = c0 + (a < R ? a : R - 1);
-      }
-      __syncthreads();  // the chunk's metadata is free for the next chunk
-      if (!more) break;
+      if (!__syncthreads_or(more)) break;
       c0 += R;
     }
     fence_proxy_async_smem();
