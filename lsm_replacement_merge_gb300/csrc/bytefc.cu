@@ -267,6 +267,53 @@ __device__ __forceinline__ void write_record(const BSource &src, const RecordPla
   }
 }
 
+// write_record into a shared copy of the span (dst = the copy at the
+// record's first byte): the counts and the tag as single bytes; the key and
+// value bytes by 4-byte stores once the destination is 4-byte aligned (each
+// 8-byte read of the arena gives two), single bytes at either end.
+__device__ __forceinline__ void write_record_smem(const BSource &src, const RecordPlan &r,
+                                                  uint64_t W, uint8_t *dst) {
+  uint32_t at = 0;
+  auto leb = [&](uint64_t x) {
+    do {
+      uint8_t byte = static_cast<uint8_t>(x & 0x7F);
+      x >>= 7;
+      if (x) byte |= 0x80;
+      dst[at++] = byte;
+    } while (x);
+  };
+  auto copy = [&](const uint8_t *arena, uint64_t from, uint64_t len) {
+    uint64_t t = 0;
+    // bytes until the destination is 4-byte aligned
+    const uint32_t lead = static_cast<uint32_t>((4 - (smem_u32(dst + at) & 3)) & 3);
+    const uint64_t h = lead < len ? lead : len;
+    if (h) {
+      const uint64_t w = bytes8_at(arena, from, static_cast<int>(h));
+      for (uint64_t q = 0; q < h; ++q) dst[at++] = static_cast<uint8_t>(w >> (8 * q));
+      t = h;
+    }
+    for (; t + 8 <= len; t += 8) {
+      const uint64_t w = bytes8_at(arena, from + t, 8);
+      *reinterpret_cast<uint32_t *>(dst + at) = static_cast<uint32_t>(w);
+      *reinterpret_cast<uint32_t *>(dst + at + 4) = static_cast<uint32_t>(w >> 32);
+      at += 8;
+    }
+    if (t < len) {
+      const int need = static_cast<int>(len - t);
+      const uint64_t w = bytes8_at(arena, from + t, need);
+      for (int q = 0; q < need; ++q) dst[at++] = static_cast<uint8_t>(w >> (8 * q));
+    }
+  };
+  leb(r.b);
+  leb(r.K - r.p);
+  copy(src.key.arena, r.ks + r.p, r.K - r.p);
+  dst[at++] = r.tomb ? 0 : 1;
+  if (!r.tomb) {
+    if (!W) leb(r.vlen);
+    copy(src.val.arena, r.vs, r.vlen);
+  }
+}
+
 // One CTA per kBeRecords consecutive records: their bytes are one
 // contiguous span [s0, s1) of the payload. Each thread writes its record into
 // a shared copy of the span (records never share a byte), then the
@@ -315,7 +362,7 @@ __global__ void __launch_bounds__(kBeRecords) bytefc_emit_kernel(
     const bool ok = plan_record(sa, sb, refs, lcp, ctrl, off, i, W, r, src) && r.pos >= s0 &&
                     r.end <= s1;
     if (ok) {
-      write_record(*src, r, W, [&](uint64_t q, uint8_t v) { buf[q - base] = v; });
+      write_record_smem(*src, r, W, buf + (r.pos - base));
     } else {
       report(status, LSM_ERR_ARG);
       // the record's bytes inside the span read as zero
