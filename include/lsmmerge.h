@@ -34,6 +34,15 @@
  *     predecessor tile) gives up after about one second, records
  *     LSM_ERR_TIMEOUT in a sticky device status word and returns;
  *     lsm_get_device_status() reads it.
+ *   - Stream capture: every call except lsm_get_device_status (which
+ *     synchronizes) issues only kernel launches and memsets on `stream` and
+ *     keeps no per-call host state, so a call captured into a CUDA graph can
+ *     be replayed on new contents of the same buffers. Make one uncaptured
+ *     call of each entry point first (it sets kernel attributes and looks up
+ *     the device status word's address). Calls that find a
+ *     prefix by a decoupled lookback over per-CTA state words in the
+ *     workspace zero those words at every call, before the kernel that reads
+ *     them, so the workspace rule below holds for them too.
  *   - Bitmaps hold bit t in 32-bit word t/32 at bit position t%32.
  *   - A reference is src<<31 | index with src 0 = A and src 1 = B.
  */

@@ -49,12 +49,15 @@ cudaError_t launch_merge_sort(int key_type, const void *in, const uint32_t *in_p
 int64_t replacement_tile();
 // Words of the merge bitmap for m + n positions (padded for whole-tile copies).
 int64_t merge_bitmap_words(int64_t total);
-// Partition (clears C and MB) + mark; part_m: G + 1 co-ranks (A first on
+// Partition (clears C) + mark; part_m: G + 1 co-ranks (A first on
 // ties); part_c: G + 1 co-ranks of the compaction (B first on ties), or
 // null; MB: the merge bitmap (merge_bitmap_words(m + n)), or null.
+// clear[0, nclear): words (lookback states of a later kernel) the partition
+// zeroes too.
 cudaError_t launch_mark_tiles(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                               uint32_t *C, uint32_t *lb_B, uint32_t *MB, int64_t *part_m,
-                              int64_t *part_c, int32_t *status, cudaStream_t s);
+                              int64_t *part_c, int32_t *status, cudaStream_t s,
+                              uint64_t *clear = nullptr, int64_t nclear = 0);
 // Compaction; part_c: the mark's co-ranks (then MB is the mark's merge
 // bitmap), or null to compute both from lb_B (co-ranks into part_scratch,
 // G + 1; MB rebuilt).
@@ -99,10 +102,12 @@ cudaError_t launch_collision_mark(const uint64_t *A, int64_t m, const uint64_t *
                                   cudaStream_t s);
 cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
                               uint32_t *cta_totals, cudaStream_t s);
-// Workspace version: one launch (epoch-tagged lookback) when the CTAs fit on
-// the device at once, else count + finish. ws: rank_build_ctas(m) uint64.
+// Workspace version: one launch (decoupled lookback) when the CTAs fit on
+// the device at once, else count + finish. ws: rank_build_ctas(m) uint64;
+// ws_clear: an earlier kernel on s has zeroed them for this call (else a
+// memset node does).
 cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
-                                 void *ws, int32_t *status, cudaStream_t s);
+                                 void *ws, int32_t *status, cudaStream_t s, bool ws_clear = false);
 cudaError_t launch_rank_query(const uint32_t *C, const uint32_t *dir, int64_t m,
                               const uint32_t *pos, int64_t q, uint32_t *out, int32_t *status,
                               cudaStream_t s);
@@ -141,12 +146,14 @@ cudaError_t launch_rank2048_query(const uint32_t *C, const uint64_t *dir, const 
 // The string mark that also writes the merge bitmap MB (bit p set when
 // position p of the merge with B first on ties holds a B record) and the
 // compaction's co-ranks at every cstep-th tile start (part_c, one more at the
-// end); lb_B may be null.
+// end); lb_B may be null. The partition also zeroes clear[0, nclear) (a
+// later kernel's lookback states).
 cudaError_t launch_collision_mark_str_mb(const lsm_bytes &A, int64_t m, const lsm_bytes &B,
                                          int64_t n, uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
                                          uint64_t *prefixB, int64_t *part_i, uint32_t *MB,
                                          int64_t *part_c, int cstep, int32_t *status,
-                                         cudaStream_t s);
+                                         cudaStream_t s, uint64_t *clear = nullptr,
+                                         int64_t nclear = 0);
 cudaError_t launch_collision_mark_str(const lsm_bytes &A, int64_t m, const lsm_bytes &B, int64_t n,
                                       uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
                                       uint64_t *prefixB, int64_t *part_i, int32_t *status,

@@ -24,7 +24,6 @@
 // and writes its entries, reading C once.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 
 #include "common.cuh"
@@ -113,7 +112,7 @@ __global__ void __launch_bounds__(kRank2048Threads) rank2048_finish_kernel(
 
 __global__ void __launch_bounds__(kRank2048Threads) rank2048_single_kernel(
     const uint32_t *__restrict__ C, int64_t m, uint64_t *__restrict__ dir,
-    uint64_t *__restrict__ epochs, int64_t *__restrict__ d_total, uint64_t *state, uint32_t epoch,
+    uint64_t *__restrict__ epochs, int64_t *__restrict__ d_total, uint64_t *state,
     int32_t *status) {
   pdl_begin();
   __shared__ uint32_t scratch[kRank2048Threads / 32 + 1];
@@ -128,7 +127,7 @@ __global__ void __launch_bounds__(kRank2048Threads) rank2048_single_kernel(
   uint32_t agg;
   const uint32_t excl = block_exclusive_sum<kRank2048Threads>(b < nblk ? tot : 0u, scratch, &agg);
   if (threadIdx.x < 32) {
-    const uint32_t prefix = lookback_exclusive(state, t, agg, epoch, status);
+    const uint32_t prefix = lookback_exclusive(state, t, agg, status);
     if (threadIdx.x == 0) s_prefix = prefix;
   }
   __syncthreads();
@@ -164,7 +163,6 @@ int64_t rank2048_build_ctas(int64_t m) {
 
 cudaError_t launch_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, uint64_t *epochs,
                                   int64_t *d_total, uint64_t *ws, int32_t *status, cudaStream_t s) {
-  static std::atomic<uint32_t> epoch_counter{0};
   static int per_sm = -1;  // CTAs of rank2048_single_kernel resident per SM
   if (per_sm < 0) {
     int v = 0;
@@ -175,13 +173,13 @@ cudaError_t launch_rank2048_build(const uint32_t *C, int64_t m, uint64_t *dir, u
   }
   const int64_t ctas = rank2048_build_ctas(m);
   if (m < (int64_t(1) << 31) && ctas <= static_cast<int64_t>(device_sm_count()) * per_sm) {
-    // every CTA resident at once, so each CTA a lookback waits for is running
-    uint32_t epoch = ++epoch_counter;
-    if (epoch == 0) epoch = ++epoch_counter;
+    // every CTA resident at once, so each CTA a lookback waits for is
+    // running; the lookback states start from zero at every call
+    cudaError_t err = cudaMemsetAsync(ws, 0, static_cast<size_t>(ctas) * 8, s);
+    if (err != cudaSuccess) return err;
     profile_before(s);
-    const cudaError_t err = launch_kernel(true, rank2048_single_kernel, static_cast<unsigned>(ctas),
-                                          kRank2048Threads, 0, s, C, m, dir, epochs, d_total, ws,
-                                          epoch, status);
+    err = launch_kernel(true, rank2048_single_kernel, static_cast<unsigned>(ctas),
+                        kRank2048Threads, 0, s, C, m, dir, epochs, d_total, ws, status);
     profile_after(s);
     return err;
   }

@@ -43,7 +43,6 @@
 //                    rank query. Refs and ordinals leave by bulk stores.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -278,16 +277,15 @@ __global__ void __launch_bounds__(kPosThreads) partition_positions_kernel(
 
 // Single-launch rank512 build: every CTA counts its 256 blocks, publishes
 // its total, looks back over its predecessors for the prefix (decoupled
-// lookback) and writes its entries. A state word is epoch << 32 | inclusive
-// flag << 31 | value; a word from another call carries another epoch and
-// reads as "not yet published", so the state needs no clearing pass. Used
-// only when all CTAs are resident at once, so every CTA a lookback waits for
-// is running; each wait is bounded in time.
+// lookback) and writes its entries. The state words are zero at launch (the
+// launcher clears them, or a kernel earlier on the stream did). Used only
+// when all CTAs are resident at once, so every CTA a lookback waits for is
+// running; each wait is bounded in time.
 __global__ void __launch_bounds__(kRankThreads) rank_single_kernel(const uint32_t *__restrict__ C,
                                                                    int64_t m,
                                                                    uint32_t *__restrict__ dir,
                                                                    int64_t *__restrict__ d_total,
-                                                                   uint64_t *state, uint32_t epoch,
+                                                                   uint64_t *state,
                                                                    int32_t *status) {
   pdl_begin();
   __shared__ uint32_t scratch[kRankThreads / 32 + 1];
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(kRankThreads) rank_single_kernel(const uint32_
   uint32_t agg;
   const uint32_t excl = block_exclusive_sum<kRankThreads>(b < nblk ? tot : 0u, scratch, &agg);
   if (threadIdx.x < 32) {
-    const uint32_t prefix = lookback_exclusive(state, t, agg, epoch, status);
+    const uint32_t prefix = lookback_exclusive(state, t, agg, status);
     if (threadIdx.x == 0) s_prefix = prefix;
   }
   __syncthreads();
@@ -1167,8 +1165,7 @@ cudaError_t launch_rank_build(const uint32_t *C, int64_t m, uint32_t *dir, int64
 }
 
 cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, int64_t *d_total,
-                                 void *ws, int32_t *status, cudaStream_t s) {
-  static std::atomic<uint32_t> epoch_counter{0};
+                                 void *ws, int32_t *status, cudaStream_t s, bool ws_clear) {
   static int per_sm = -1;  // CTAs of rank_single_kernel resident per SM
   if (per_sm < 0) {
     int v = 0;
@@ -1181,12 +1178,14 @@ cudaError_t launch_rank_build_ws(const uint32_t *C, int64_t m, uint32_t *dir, in
   // one launch only while every CTA is resident at once, so each CTA a
   // lookback waits for is already running
   if (ctas <= static_cast<int64_t>(device_sm_count()) * per_sm) {
-    uint32_t epoch = ++epoch_counter;
-    if (epoch == 0) epoch = ++epoch_counter;
+    if (!ws_clear) {
+      const cudaError_t e = cudaMemsetAsync(ws, 0, static_cast<size_t>(ctas) * 8, s);
+      if (e != cudaSuccess) return e;
+    }
     profile_before(s);
     const cudaError_t err = launch_kernel(true, rank_single_kernel, static_cast<unsigned>(ctas),
                                           kRankThreads, 0, s, C, m, dir, d_total,
-                                          static_cast<uint64_t *>(ws), epoch, status);
+                                          static_cast<uint64_t *>(ws), status);
     profile_after(s);
     return err;
   }

@@ -41,7 +41,6 @@
 //             between consumer warps.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 
 #include "common.cuh"
@@ -80,21 +79,24 @@ struct KeysAFirst {
 
 // The co-rank of every diagonal k_g = min(g D, m + n), g = 0..G, by a group
 // of L lanes per diagonal (L + 1-way splits per round: about log_{L+1}(n)
-// dependent rounds of loads); the same launch clears C and the merge bitmap.
+// dependent rounds of loads); the same launch clears C and the lookback
+// states of the kernels after it (Z0[0, n0), Z1[0, n1)).
 template <int L>
 __global__ void __launch_bounds__(256) corank_partition_kernel(KeysAFirst pred, int64_t m, int64_t n,
                                                                int64_t D, int64_t G,
                                                                int64_t *__restrict__ out_i,
                                                                uint32_t *__restrict__ C,
                                                                int64_t nwords,
-                                                               uint32_t *__restrict__ MB,
-                                                               int64_t nmb) {
+                                                               uint64_t *__restrict__ Z0,
+                                                               int64_t n0,
+                                                               uint64_t *__restrict__ Z1,
+                                                               int64_t n1) {
   pdl_begin();
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t w = gtid; w < nwords; w += stride) C[w] = 0u;
-  if (MB)
-    for (int64_t w = gtid; w < nmb; w += stride) MB[w] = 0u;
+  for (int64_t w = gtid; w < n0; w += stride) Z0[w] = 0u;
+  for (int64_t w = gtid; w < n1; w += stride) Z1[w] = 0u;
   const int64_t g = gtid / L;
   const bool active = g <= G;
   const int64_t total = m + n;
@@ -953,7 +955,6 @@ struct FusedMC {
     uint32_t *refs, *ord_A, *ord_B;
     int64_t *d_count;
     uint64_t *state;  // G lookback words
-    uint32_t epoch;
   };
 };
 
@@ -1116,8 +1117,7 @@ __global__ void __launch_bounds__(FusedMC::kThreads, 2) fused_mc_kernel(FusedMC:
         if (atomicAdd(&tdesc[q].warps_done, 1u) == F::NWM - 1) {
           __threadfence_block();
           const uint32_t agg = atomicAdd(&tdesc[q].hits, 0u);
-          const uint64_t tag = static_cast<uint64_t>(p.epoch) << 32;
-          st_relaxed_u64(p.state + g, tag | agg);
+          st_relaxed_u64(p.state + g, kPublished | agg);
         }
         mbar_arrive(&markdone[q]);
       }
@@ -1137,7 +1137,7 @@ __global__ void __launch_bounds__(FusedMC::kThreads, 2) fused_mc_kernel(FusedMC:
       // R(g) needs only earlier tiles' counts: it is summed while this
       // tile's own mark is still running
       const uint32_t prefix = (r == 0 ? 0u : rprev) +
-                              window_sum<F::kLookK>(p.state, r == 0 ? 0 : g - P, g, p.epoch, status);
+                              window_sum<F::kLookK>(p.state, r == 0 ? 0 : g - P, g, status);
       rprev = prefix;
       // the ring slot holds this tile once its mark is done
       if (!mbar_wait_sleep(&markdone[q], static_cast<uint32_t>((r / NB) & 1), kWaitLimitNs)) {
@@ -1303,17 +1303,18 @@ int64_t merge_bitmap_words(int64_t total) { return align_up((total + 31) / 32, 4
 
 cudaError_t launch_mark_tiles(const uint64_t *A, int64_t m, const uint64_t *B, int64_t n,
                               uint32_t *C, uint32_t *lb_B, uint32_t *MB, int64_t *part_m,
-                              int64_t *part_c, int32_t *status, cudaStream_t s) {
+                              int64_t *part_c, int32_t *status, cudaStream_t s,
+                              uint64_t *clear, int64_t nclear) {
   constexpr int64_t D = MarkDefault::D;
   const int64_t G = (m + n + D - 1) / D;
-  const int64_t nwords = (m + 31) / 32;
-  const int64_t nmb = 0;  // the mark writes every word of the merge bitmap
+  const int64_t nwords = (m + 31) / 32;  // the mark writes every word of MB itself
   int64_t threads = (G + 1) * kPartLanes;
-  if (threads < (nwords + nmb) / 4) threads = (nwords + nmb) / 4;
+  if (threads < nwords / 4) threads = nwords / 4;
   const int64_t blocks = (threads + 255) / 256;
   cudaError_t err = launch_kernel(true, corank_partition_kernel<kPartLanes>,
                                   static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s,
-                                  KeysAFirst{A, B}, m, n, D, G, part_m, C, nwords, MB, nmb);
+                                  KeysAFirst{A, B}, m, n, D, G, part_m, C, nwords, clear, nclear,
+                                  static_cast<uint64_t *>(nullptr), int64_t(0));
   if (err != cudaSuccess || G == 0) return err;
   typename MarkDefault::Params p{A, B, m, n, G, part_m, C, lb_B, part_c, MB};
   profile_before(s);
@@ -1389,9 +1390,10 @@ cudaError_t launch_replacement_merge_str(const lsm_bytes &A, int64_t m, const ls
   cudaError_t err = cudaSuccess;
   if (m + n > 0)
     err = launch_collision_mark_str_mb(A, m, B, n, C, lb_B, prefixA, prefixB, part_m, MB, part_c,
-                                       cstep, status, s);
+                                       cstep, status, s, static_cast<uint64_t *>(rank_ws),
+                                       rank_build_ctas(m));
   if (err != cudaSuccess) return err;
-  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s);
+  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s, m + n > 0);
   if (err != cudaSuccess) return err;
   return launch_compact_with<CompactStr>(m, n, C, Rank512At{dir}, nullptr, MB, part_c, nullptr,
                                          refs, ord_A, ord_B, d_count, status, s);
@@ -1410,7 +1412,6 @@ cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uin
                                         uint32_t *ord_B, int64_t *d_count, int64_t *part_m,
                                         uint64_t *state, void *rank_ws, int32_t *status,
                                         cudaStream_t s) {
-  static std::atomic<uint32_t> epoch_counter{0};
   constexpr int64_t D = FusedMC::D;
   const int64_t G = (m + n + D - 1) / D;
   cudaError_t err = cudaSuccess;
@@ -1419,10 +1420,12 @@ cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uin
     int64_t threads = (G + 1) * kPartLanes;
     if (threads < nwords / 4) threads = nwords / 4;
     const int64_t blocks = (threads + 255) / 256;
+    // the partition also zeroes both lookback states: the tiles' and the
+    // rank512 build's
     err = launch_kernel(true, corank_partition_kernel<kPartLanes>,
                         static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s, KeysAFirst{A, B},
-                        m, n, D, G, part_m, C, nwords, static_cast<uint32_t *>(nullptr),
-                        int64_t(0));
+                        m, n, D, G, part_m, C, nwords, state, G,
+                        static_cast<uint64_t *>(rank_ws), rank_build_ctas(m));
     if (err != cudaSuccess) return err;
     static int per_sm = 0;
     if (!per_sm) {
@@ -1438,8 +1441,6 @@ cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uin
     // that are being worked on
     int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
     if (grid > G) grid = G;
-    uint32_t epoch = ++epoch_counter;
-    if (epoch == 0) epoch = ++epoch_counter;
     FusedMC::Params p{};
     p.mp = FusedMC::Mark::Params{A, B, m, n, G, part_m, C, lb_B, nullptr, nullptr};
     p.refs = refs;
@@ -1447,14 +1448,13 @@ cudaError_t launch_replacement_merge_one(const uint64_t *A, int64_t m, const uin
     p.ord_B = ord_B;
     p.d_count = d_count;
     p.state = state;
-    p.epoch = epoch;
     profile_before(s);
     err = launch_kernel(true, fused_mc_kernel, static_cast<unsigned>(grid), FusedMC::kThreads,
                         FusedMC::kBytes, s, p, G, status);
     profile_after(s);
     if (err != cudaSuccess) return err;
   }
-  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s);
+  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s, G > 0);
   if (err != cudaSuccess || G > 0) return err;
   return launch_kernel(false, set_count_kernel2, 1, 1, 0, s, d_count, int64_t(0));
 }
@@ -1465,9 +1465,11 @@ cudaError_t launch_replacement_merge(const uint64_t *A, int64_t m, const uint64_
                                     int64_t *d_count, int64_t *part_m, int64_t *part_c,
                                     uint32_t *MB, void *rank_ws, int32_t *status, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
-  if (m + n > 0) err = launch_mark_tiles(A, m, B, n, C, lb_B, MB, part_m, part_c, status, s);
+  if (m + n > 0)
+    err = launch_mark_tiles(A, m, B, n, C, lb_B, MB, part_m, part_c, status, s,
+                            static_cast<uint64_t *>(rank_ws), rank_build_ctas(m));
   if (err != cudaSuccess) return err;
-  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s);
+  err = launch_rank_build_ws(C, m, dir, d_total, rank_ws, status, s, m + n > 0);
   if (err != cudaSuccess) return err;
   return launch_compact_tiles(m, n, C, dir, lb_B, MB, part_c, nullptr, refs, ord_A, ord_B, d_count,
                               status, s);

@@ -45,11 +45,14 @@ __global__ void __launch_bounds__(256) partition_str_kernel(StrAFirst pred, int6
                                                             int64_t D, int64_t G,
                                                             int64_t *__restrict__ out_i,
                                                             uint32_t *__restrict__ clear_words,
-                                                            int64_t nclear) {
+                                                            int64_t nclear,
+                                                            uint64_t *__restrict__ clear_states,
+                                                            int64_t nstates) {
   pdl_begin();
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t w = gtid; w < nclear; w += stride) clear_words[w] = 0u;
+  for (int64_t w = gtid; w < nstates; w += stride) clear_states[w] = 0u;
   const int64_t g = gtid / kStrPartitionLanes;
   const bool active = g <= G;
   const int64_t total = m + n;
@@ -379,7 +382,7 @@ cudaError_t launch_collision_mark_str_mb(const lsm_bytes &A, int64_t m, const ls
                                          int64_t n, uint32_t *C, uint32_t *lb_B, uint64_t *prefixA,
                                          uint64_t *prefixB, int64_t *part_i, uint32_t *MB,
                                          int64_t *part_c, int cstep, int32_t * /*status*/,
-                                         cudaStream_t s) {
+                                         cudaStream_t s, uint64_t *clear, int64_t nclear) {
   constexpr int64_t D = int64_t(kMarkStrThreads) * kMarkStrItems;
   const int64_t G = (m + n + D - 1) / D;
   const int64_t nwords = (m + 31) / 32;
@@ -387,7 +390,7 @@ cudaError_t launch_collision_mark_str_mb(const lsm_bytes &A, int64_t m, const ls
   if (threads < nwords / 4) threads = nwords / 4;
   cudaError_t err = launch_kernel(false, partition_str_kernel,
                                   static_cast<unsigned>((threads + 255) / 256), 256, 0, s,
-                                  StrAFirst{A, B}, m, n, D, G, part_i, C, nwords);
+                                  StrAFirst{A, B}, m, n, D, G, part_i, C, nwords, clear, nclear);
   if (err != cudaSuccess || G == 0) return err;
   profile_before(s);
   // launched early behind the partition (PDL), whose fewer than one CTA per
