@@ -276,28 +276,41 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
 }
 
 // The same lengths when both sources carry key prefix tables, without the
-// shared-memory phases: each thread takes four consecutive records and the
-// record before them, issues every load of the five (refs, key extents,
-// prefix words; value extents and tombstone words of its own four) before
-// using any, and computes the bit LCP, control and length of each; the
-// tile's total goes to tile_sum as above. A record's predecessor is loaded
-// again by the thread before it (measured faster than staging the tile).
+// shared-memory phases: each thread takes kFlatItems consecutive records and
+// the record before them, issues every load of them (refs, key extents,
+// prefix words; value extents and tombstone words of its own records)
+// before using any, and computes the bit LCP, control and length of each;
+// the tile's total goes to tile_sum as above. A record's predecessor is
+// loaded again by the thread before it (measured faster than staging the
+// tile). The pass waits on those loads, so warps per SM decide its time:
+// measured on the 4M + 4M strings (lengths + scan + offsets, L2 flushed),
+// 512 threads of two records at two CTAs per SM (64 registers, 32 warps)
+// 116-119 us, against 137-144 us for 256 threads of four (107 registers,
+// 16 warps), 131-137 us for those at three CTAs per SM (80 registers, with
+// spills), 179-182 us for 512 threads at one CTA per SM (72 registers) and
+// 175-178 us for 1024 threads of one record (48 registers, one CTA).
 #ifndef FC_FLAT_MIN_BLOCKS
-#define FC_FLAT_MIN_BLOCKS 1
+#define FC_FLAT_MIN_BLOCKS 2
 #endif
-__global__ void __launch_bounds__(kFcThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_flat_kernel(
+#ifndef FC_FLAT_THREADS
+#define FC_FLAT_THREADS 512
+#endif
+constexpr int kFlatThreads = FC_FLAT_THREADS;  // threads of one tile of kFcTile records
+constexpr int kFlatItems = kFcTile / kFlatThreads;
+static_assert(kFlatItems * kFlatThreads == kFcTile, "a flat tile is one scan tile");
+__global__ void __launch_bounds__(kFlatThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_flat_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N, uint32_t *__restrict__ lcp,
     uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec_bits, uint64_t *__restrict__ bit_off,
     uint64_t *tile_sum, int32_t *status) {
   pdl_begin();
-  __shared__ uint64_t scratch[kFcThreads / 32 + 1];
+  __shared__ uint64_t scratch[kFlatThreads / 32 + 1];
   const int tid = threadIdx.x;
   if (N == 0) {
     if (tid == 0 && blockIdx.x == 0) bit_off[0] = 0;
     return;
   }
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kFcTile + int64_t(tid) * kFcItems;
-  constexpr int Q = kFcItems + 1;  // slot 0: the record before the thread's first
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kFcTile + int64_t(tid) * kFlatItems;
+  constexpr int Q = kFlatItems + 1;  // slot 0: the record before the thread's first
   uint32_t rr[Q];
   uint64_t kb[Q], ke[Q], p0[Q], p1[Q];
 #pragma unroll
@@ -318,10 +331,10 @@ __global__ void __launch_bounds__(kFcThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_fla
     p0[q] = v.x;
     p1[q] = v.y;
   }
-  uint64_t vb[kFcItems], ve[kFcItems];
-  uint32_t tw[kFcItems];
+  uint64_t vb[kFlatItems], ve[kFlatItems];
+  uint32_t tw[kFlatItems];
 #pragma unroll
-  for (int q = 0; q < kFcItems; ++q) {
+  for (int q = 0; q < kFlatItems; ++q) {
     const int64_t i = first + q;
     const bool live = i < N;
     const uint32_t idx = rr[q + 1] & ~LSM_REF_FROM_B;
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(kFcThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_fla
   uint64_t sum = 0;
   bool overflow = false;
 #pragma unroll
-  for (int q = 0; q < kFcItems; ++q) {
+  for (int q = 0; q < kFlatItems; ++q) {
     const int64_t i = first + q;
     if (i >= N) break;
     const uint32_t idx = rr[q + 1] & ~LSM_REF_FROM_B;
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(kFcThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_fla
     sum += Lrec;
   }
   if (overflow) report(status, LSM_ERR_OVERFLOW);
-  const uint64_t agg = block_sum<kFcThreads, uint64_t>(sum, scratch);
+  const uint64_t agg = block_sum<kFlatThreads, uint64_t>(sum, scratch);
   if (tid == 0) tile_sum[blockIdx.x] = agg;
 }
 
@@ -851,7 +864,7 @@ cudaError_t launch_fc_lengths_scan(const lsm_fc_input &in, const uint32_t *refs,
   profile_before(s);
   if (flat)
     err = launch_kernel(false, fc_lengths_flat_kernel, static_cast<unsigned>(tiles > 0 ? tiles : 1),
-                        kFcThreads, 0, s, make_source(in.keyA, in.valA, in.tombA, in.prefixA),
+                        kFlatThreads, 0, s, make_source(in.keyA, in.valA, in.tombA, in.prefixA),
                         make_source(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, lcp, ctrl,
                         rec_bits, bit_off, tile_sum, status);
   else
