@@ -723,8 +723,14 @@ __device__ __forceinline__ void emit_record32(uint32_t *buf, int H, int P, const
 // arrays and no barrier between loads and composition (measured: 322 us
 // against 334.5 us with the metadata staged in shared memory first); the
 // record holding the next run's first bit is named by its own thread. Each
-// run leaves by one bulk store.
-__global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
+// run leaves by one bulk store. One record in flight per thread at five
+// CTAs per SM (48 registers): 309-310 us, against 318-319 us for two records
+// in flight at four (64 registers), 345 us for one record at six (40
+// registers) and 367 us for two at five.
+#ifndef EMIT_MIN_BLOCKS
+#define EMIT_MIN_BLOCKS 5
+#endif
+__global__ void __launch_bounds__(kEmitThreads, EMIT_MIN_BLOCKS) fc_emit_kernel(
     Source sa, Source sb, const uint32_t *__restrict__ refs, int64_t N,
     const uint32_t *__restrict__ lcp, const uint32_t *__restrict__ ctrl,
     const uint64_t *__restrict__ bit_off, uint32_t *__restrict__ payload, int64_t nwords) {
@@ -759,62 +765,39 @@ __global__ void __launch_bounds__(kEmitThreads) fc_emit_kernel(
     while (lo < hi) {
       const int R = static_cast<int>(N - c0 < kEmitMaxRec ? N - c0 : kEmitMaxRec);
       bool more = false;
-      for (int x0 = tid; x0 < R; x0 += 2 * kEmitThreads) {
-        uint32_t ref[2], cc[2], ll[2];
-        uint64_t bo[2], be[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int x = x0 + u * kEmitThreads;
-          const int64_t r = c0 + (x < R ? x : x0);
-          ref[u] = __ldg(refs + r);
-          bo[u] = __ldg(bit_off + r);
-          be[u] = __ldg(bit_off + r + 1);
-          cc[u] = __ldg(ctrl + r);
-          ll[u] = __ldg(lcp + r);
+      for (int x = tid; x < R; x += kEmitThreads) {
+        const int64_t r = c0 + x;
+        const uint32_t ref = __ldg(refs + r);
+        const int64_t rs = static_cast<int64_t>(__ldg(bit_off + r));
+        const int64_t re = static_cast<int64_t>(__ldg(bit_off + r + 1));
+        const uint32_t cc = __ldg(ctrl + r), ll = __ldg(lcp + r);
+        const uint32_t idx = ref & ~LSM_REF_FROM_B;
+        const Source &src = pick(sa, sb, ref);
+        const uint64_t kb = __ldg(src.key.off + idx), ke = __ldg(src.key.off + idx + 1);
+        const uint64_t vb = __ldg(src.val.off + idx), ve = __ldg(src.val.off + idx + 1);
+        const uint32_t tw = src.tomb ? __ldg(src.tomb + (idx >> 5)) : 0u;
+        if (rs <= hi && hi < re) sNext2[(run + 1) & 1] = r;
+        if (x == R - 1 && re <= hi && r + 1 < N) {
+          // the chunk ends at or before hi: the record after it starts the
+          // next run, or the next chunk goes on with this run
+          if (re == hi) sNext2[(run + 1) & 1] = r + 1;
+          else more = true;
         }
-        uint64_t kb[2], ke[2], vb[2], ve[2];
-        uint32_t tw[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint32_t idx = ref[u] & ~LSM_REF_FROM_B;
-          const Source &src = pick(sa, sb, ref[u]);
-          kb[u] = __ldg(src.key.off + idx);
-          ke[u] = __ldg(src.key.off + idx + 1);
-          vb[u] = __ldg(src.val.off + idx);
-          ve[u] = __ldg(src.val.off + idx + 1);
-          tw[u] = src.tomb ? __ldg(src.tomb + (idx >> 5)) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int x = x0 + u * kEmitThreads;
-          if (x >= R) continue;
-          const int64_t r = c0 + x;
-          const int64_t rs = static_cast<int64_t>(bo[u]), re = static_cast<int64_t>(be[u]);
-          if (rs <= hi && hi < re) sNext2[(run + 1) & 1] = r;
-          if (x == R - 1 && re <= hi && r + 1 < N) {
-            // the chunk ends at or before hi: the record after it starts
-            // the next run, or the next chunk goes on with this run
-            if (re == hi) sNext2[(run + 1) & 1] = r + 1;
-            else more = true;
-          }
-          if (rs >= hi) continue;
-          const uint32_t idx = ref[u] & ~LSM_REF_FROM_B;
-          const bool tomb = (tw[u] >> (idx & 31)) & 1u;
-          const Source &src = pick(sa, sb, ref[u]);
-          RecordMeta M;
-          M.s = rs;
-          M.e = re;
-          M.c = cc[u];
-          M.l = ll[u];
-          M.key = KeyRef{src.key.arena, kb[u], ke[u]};
-          M.k = 8 * (ke[u] - kb[u]);
-          M.tomb = tomb;
-          M.val = KeyRef{src.val.arena, tomb ? 0 : vb[u], tomb ? 0 : ve[u]};
-          if (M.e - M.s < (int64_t(1) << 30))
-            emit_record32(sOut, static_cast<int>(hi - lo), static_cast<int>(M.s - lo), M);
-          else
-            emit_record(sOut, w0, lo, hi, M);
-        }
+        if (rs >= hi) continue;
+        const bool tomb = (tw >> (idx & 31)) & 1u;
+        RecordMeta M;
+        M.s = rs;
+        M.e = re;
+        M.c = cc;
+        M.l = ll;
+        M.key = KeyRef{src.key.arena, kb, ke};
+        M.k = 8 * (ke - kb);
+        M.tomb = tomb;
+        M.val = KeyRef{src.val.arena, tomb ? 0 : vb, tomb ? 0 : ve};
+        if (M.e - M.s < (int64_t(1) << 30))
+          emit_record32(sOut, static_cast<int>(hi - lo), static_cast<int>(M.s - lo), M);
+        else
+          emit_record(sOut, w0, lo, hi, M);
       }
       if (!__syncthreads_or(more)) break;
       c0 += R;
