@@ -17,6 +17,9 @@
 //                          per thread: key extents, byte LCP with the
 //                          predecessor from aligned 8-byte loads, control,
 //                          record length; the tile's total for the scan
+//                          (bytefc_lengths_flat_kernel when the inputs
+//                          carry key prefix tables: 512 threads of two
+//                          records, every load issued before any is used)
 //   (scan)                 the FC pipeline's one-CTA tile scan and offsets
 //                          pass turn the lengths into byte offsets
 //   bytefc_emit_kernel     one CTA per 256 consecutive records: each thread
@@ -28,6 +31,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "fcrecords.cuh"
 #include "internal.h"
 
 namespace lsm {
@@ -143,6 +147,69 @@ __global__ void __launch_bounds__(kBfThreads) bytefc_lengths_kernel(
     local += static_cast<uint32_t>(L);
   }
   const uint64_t total = block_sum<kBfThreads, uint64_t>(local, scratch);
+  if (threadIdx.x == 0) tile_sum[blockIdx.x] = total;
+}
+
+// The same lengths when both sources carry key prefix tables: each of 512
+// threads takes two consecutive records and the record before them
+// (FlatRecords: every load issued before any is used), two CTAs per SM.
+// The byte LCP is the first byte at which the 16-byte prefixes differ,
+// clamped to the shorter key; bytes past 16 come from the arenas only when
+// both keys are longer and all 16 agree. Measured on the 4M + 4M strings
+// (lengths + scan + offsets, L2 flushed): 115 us against 141 us for
+// bytefc_lengths_kernel on the same tables (four records per thread, each
+// record's loads after the previous record's).
+constexpr int kBfFlatThreads = 512;
+constexpr int kBfFlatItems = kBfTile / kBfFlatThreads;
+static_assert(kBfFlatItems * kBfFlatThreads == kBfTile, "a flat tile is one scan tile");
+
+__global__ void __launch_bounds__(kBfFlatThreads, 2) bytefc_lengths_flat_kernel(
+    BSource sa, BSource sb, const uint32_t *__restrict__ refs, int64_t N, uint64_t W,
+    uint32_t *__restrict__ lcp, uint32_t *__restrict__ ctrl, uint32_t *__restrict__ rec,
+    uint64_t *__restrict__ tile_sum, int32_t *status) {
+  pdl_begin();
+  __shared__ uint64_t scratch[kBfFlatThreads / 32 + 1];
+  const int64_t first =
+      static_cast<int64_t>(blockIdx.x) * kBfTile + int64_t(threadIdx.x) * kBfFlatItems;
+  FlatRecords<BSource, kBfFlatItems> R;
+  R.load(sa, sb, refs, N, first);
+  uint64_t local = 0;
+  bool bad_width = false, overflow = false;
+#pragma unroll
+  for (int q = 0; q < kBfFlatItems; ++q) {
+    const int64_t i = first + q;
+    if (i >= N) break;
+    const uint64_t K = R.ke[q + 1] - R.kb[q + 1];
+    uint64_t p = 0, Kp = 0;
+    if (i > 0) {
+      Kp = R.ke[q] - R.kb[q];
+      const uint64_t L = Kp < K ? Kp : K;
+      p = R.prefix_agree_bits(q) / 8;
+      if (p == 16 && L > 16)
+        p = 16 + byte_lcp(bpick(sa, sb, R.rr[q]).key.arena, R.kb[q] + 16, Kp - 16,
+                          bpick(sa, sb, R.rr[q + 1]).key.arena, R.kb[q + 1] + 16, K - 16);
+      p = p < L ? p : L;
+    }
+    const uint64_t b = (i % 15 == 0) ? 1 + p : Kp - p;
+    uint64_t v;
+    if (R.tomb(q)) {
+      v = 1;
+      bad_width |= W != 0;  // a tombstone breaks the common width
+    } else {
+      const uint64_t vb = R.ve[q] - R.vb[q];
+      bad_width |= W && vb + 1 != W;
+      v = W ? W : 1 + leb_len(vb) + vb;
+    }
+    const uint64_t L = leb_len(b) + leb_len(K - p) + (K - p) + v;
+    overflow |= L > 0xFFFFFFFFull || b > 0xFFFFFFFFull;
+    lcp[i] = static_cast<uint32_t>(p);
+    ctrl[i] = static_cast<uint32_t>(b);
+    rec[i] = static_cast<uint32_t>(L);
+    local += static_cast<uint32_t>(L);
+  }
+  if (bad_width) report(status, LSM_ERR_ARG);
+  if (overflow) report(status, LSM_ERR_OVERFLOW);
+  const uint64_t total = block_sum<kBfFlatThreads, uint64_t>(local, scratch);
   if (threadIdx.x == 0) tile_sum[blockIdx.x] = total;
 }
 
@@ -406,12 +473,21 @@ cudaError_t launch_bytefc_lengths_scan(const lsm_fc_input &in, const uint32_t *r
   if (fc_tile_records() != kBfTile) return cudaErrorInvalidValue;
   uint64_t *tile_sum = static_cast<uint64_t *>(ws);
   const int64_t tiles = (N + kBfTile - 1) / kBfTile;
+  // prefix tables on both sources (an empty one needs none): the flat form
+  const bool flat = (in.prefixA || in.m == 0) && (in.prefixB || in.n == 0) &&
+                    (in.prefixA || in.prefixB);
   profile_before(s);
-  cudaError_t err = launch_kernel(false, bytefc_lengths_kernel,
-                                  static_cast<unsigned>(tiles > 0 ? tiles : 1), kBfThreads, 0, s,
-                                  bsource(in.keyA, in.valA, in.tombA, in.prefixA),
-                                  bsource(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, W, lcp,
-                                  ctrl, rec_bytes, tile_sum, status);
+  cudaError_t err =
+      flat ? launch_kernel(false, bytefc_lengths_flat_kernel,
+                           static_cast<unsigned>(tiles > 0 ? tiles : 1), kBfFlatThreads, 0, s,
+                           bsource(in.keyA, in.valA, in.tombA, in.prefixA),
+                           bsource(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, W, lcp, ctrl,
+                           rec_bytes, tile_sum, status)
+           : launch_kernel(false, bytefc_lengths_kernel,
+                           static_cast<unsigned>(tiles > 0 ? tiles : 1), kBfThreads, 0, s,
+                           bsource(in.keyA, in.valA, in.tombA, in.prefixA),
+                           bsource(in.keyB, in.valB, in.tombB, in.prefixB), refs, N, W, lcp, ctrl,
+                           rec_bytes, tile_sum, status);
   if (err == cudaSuccess) err = launch_fc_offsets(rec_bytes, N, tile_sum, byte_off, s);
   profile_after(s);
   return err;

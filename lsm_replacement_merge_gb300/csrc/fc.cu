@@ -41,6 +41,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "fcrecords.cuh"
 #include "internal.h"
 #include "strings.cuh"
 
@@ -277,9 +278,8 @@ __global__ void __launch_bounds__(kFcThreads) fc_lengths_kernel(
 
 // The same lengths when both sources carry key prefix tables, without the
 // shared-memory phases: each thread takes kFlatItems consecutive records and
-// the record before them, issues every load of them (refs, key extents,
-// prefix words; value extents and tombstone words of its own records)
-// before using any, and computes the bit LCP, control and length of each;
+// the record before them (FlatRecords: every load issued before any is
+// used) and computes the bit LCP, control and length of each;
 // the tile's total goes to tile_sum as above. A record's predecessor is
 // loaded again by the thread before it (measured faster than staging the
 // tile). The pass waits on those loads, so warps per SM decide its time:
@@ -310,65 +310,31 @@ __global__ void __launch_bounds__(kFlatThreads, FC_FLAT_MIN_BLOCKS) fc_lengths_f
     return;
   }
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kFcTile + int64_t(tid) * kFlatItems;
-  constexpr int Q = kFlatItems + 1;  // slot 0: the record before the thread's first
-  uint32_t rr[Q];
-  uint64_t kb[Q], ke[Q], p0[Q], p1[Q];
-#pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    const int64_t i = first - 1 + q;
-    rr[q] = (i >= 0 && i < N) ? __ldg(refs + i) : 0u;
-  }
-#pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    const int64_t i = first - 1 + q;
-    const bool live = i >= 0 && i < N;
-    const uint32_t idx = rr[q] & ~LSM_REF_FROM_B;
-    const Source &src = pick(sa, sb, rr[q]);
-    kb[q] = live ? __ldg(src.key.off + idx) : 0;
-    ke[q] = live ? __ldg(src.key.off + idx + 1) : 0;
-    ulonglong2 v = make_ulonglong2(0, 0);
-    if (live) v = __ldg(reinterpret_cast<const ulonglong2 *>(src.prefix) + idx);
-    p0[q] = v.x;
-    p1[q] = v.y;
-  }
-  uint64_t vb[kFlatItems], ve[kFlatItems];
-  uint32_t tw[kFlatItems];
-#pragma unroll
-  for (int q = 0; q < kFlatItems; ++q) {
-    const int64_t i = first + q;
-    const bool live = i < N;
-    const uint32_t idx = rr[q + 1] & ~LSM_REF_FROM_B;
-    const Source &src = pick(sa, sb, rr[q + 1]);
-    vb[q] = live ? __ldg(src.val.off + idx) : 0;
-    ve[q] = live ? __ldg(src.val.off + idx + 1) : 0;
-    tw[q] = (live && src.tomb) ? __ldg(src.tomb + (idx >> 5)) : 0u;
-  }
+  FlatRecords<Source, kFlatItems> R;
+  R.load(sa, sb, refs, N, first);
   uint64_t sum = 0;
   bool overflow = false;
 #pragma unroll
   for (int q = 0; q < kFlatItems; ++q) {
     const int64_t i = first + q;
     if (i >= N) break;
-    const uint32_t idx = rr[q + 1] & ~LSM_REF_FROM_B;
-    const uint64_t k = 8 * (ke[q + 1] - kb[q + 1]);
+    const uint64_t k = 8 * (R.ke[q + 1] - R.kb[q + 1]);
     uint64_t l = 0, k_prev = 0;
     if (i > 0) {
-      k_prev = 8 * (ke[q] - kb[q]);
+      k_prev = 8 * (R.ke[q] - R.kb[q]);
       const uint64_t L = k_prev < k ? k_prev : k;
-      const uint64_t d0 = p0[q] ^ p0[q + 1], d1 = p1[q] ^ p1[q + 1];
-      l = d0 ? static_cast<uint64_t>(__clzll(static_cast<long long>(d0)))
-             : (d1 ? 64 + static_cast<uint64_t>(__clzll(static_cast<long long>(d1))) : 128);
+      l = R.prefix_agree_bits(q);
       if (l > L) l = L;
       if (l == 128 && L > 128) {
-        const uint8_t *pa = pick(sa, sb, rr[q]).key.arena;
-        const uint8_t *ca = pick(sa, sb, rr[q + 1]).key.arena;
-        l = 128 + bit_lcp(pa, kb[q] + 16, ke[q] - kb[q] - 16, ca, kb[q + 1] + 16,
-                          ke[q + 1] - kb[q + 1] - 16);
+        const uint8_t *pa = pick(sa, sb, R.rr[q]).key.arena;
+        const uint8_t *ca = pick(sa, sb, R.rr[q + 1]).key.arena;
+        l = 128 + bit_lcp(pa, R.kb[q] + 16, R.ke[q] - R.kb[q] - 16, ca, R.kb[q + 1] + 16,
+                          R.ke[q + 1] - R.kb[q + 1] - 16);
       }
     }
     uint64_t v = 1;  // a tombstone is one bit
-    if (!((tw[q] >> (idx & 31)) & 1u)) {
-      const uint64_t vbytes = ve[q] - vb[q];
+    if (!R.tomb(q)) {
+      const uint64_t vbytes = R.ve[q] - R.vb[q];
       v = 1 + eg0_len(vbytes) + 8 * vbytes;
     }
     const uint64_t c = (i % 15 == 0) ? 1 + l : k_prev - l;

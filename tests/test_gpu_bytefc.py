@@ -45,12 +45,16 @@ def check_bytefc(lsm, s, W=0):
     assert np.array_equal(down(off), exp.bit_off)
     # the same lengths with the key prefix tables (the LCP from their first
     # 16 bytes), built on the host from their definition
-    if fc.keyA.count and fc.keyB.count:
+    # (an empty source needs no table)
+    if fc.keyA.count or fc.keyB.count:
         fc2 = device_input(lsm, s)
-        fc2.prefixA = up(_prefix_table(s.A.key_arena, s.A.key_off))
-        fc2.prefixB = up(_prefix_table(s.B.key_arena, s.B.key_off))
+        if fc.keyA.count:
+            fc2.prefixA = up(_prefix_table(s.A.key_arena, s.A.key_off))
+        if fc.keyB.count:
+            fc2.prefixB = up(_prefix_table(s.B.key_arena, s.B.key_off))
         lcp2, ctrl2, rec2, off2 = lsm.bytefc_lengths_scan(fc2, refs, N, W)
         assert np.array_equal(down(lcp2)[:N], exp.lcp)
+        assert np.array_equal(down(ctrl2)[:N], exp.ctrl)
         assert np.array_equal(down(rec2)[:N], exp.rec_bits)
         assert np.array_equal(down(off2), exp.bit_off)
     total = exp.total_bits
@@ -142,6 +146,11 @@ def test_width_errors_are_reported(lsm):
         fc = device_input(lsm, s)
         refs, N = gpu_refs(lsm, fc)
         lsm.get_device_status(reset=True)
+        lsm.bytefc_lengths_scan(fc, refs, N, 17)
+        assert lsm.get_device_status(reset=True) == lsm.LSM_ERR_ARG
+        # the same through the key prefix tables (the flat lengths kernel)
+        fc.prefixA = up(_prefix_table(s.A.key_arena, s.A.key_off)) if fc.keyA.count else None
+        fc.prefixB = up(_prefix_table(s.B.key_arena, s.B.key_off)) if fc.keyB.count else None
         lsm.bytefc_lengths_scan(fc, refs, N, 17)
         assert lsm.get_device_status(reset=True) == lsm.LSM_ERR_ARG
     # an emit whose offsets do not match its records: reported, and nothing is
