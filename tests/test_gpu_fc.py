@@ -164,7 +164,7 @@ def test_config_strings_4M(lsm):
 
 def test_many_tiny_records_per_run(lsm):
     # 3-byte keys sharing long prefixes, mostly tombstones: a dozen bits per
-    # record, so one run of 4096 payload words holds ~10,000 records and its
+    # record, so one run of 8192 payload words holds ~20,000 records and its
     # metadata is staged in many chunks; words straddle chunk boundaries.
     ka = [int(x).to_bytes(3, "big") for x in range(0, 120000, 2)]
     kb = [int(x).to_bytes(3, "big") for x in range(1, 120000, 6)]
@@ -174,7 +174,7 @@ def test_many_tiny_records_per_run(lsm):
 
 
 def test_records_spanning_many_runs(lsm):
-    # values of 40-100 KB: a record covers several runs of 4096 words, so
+    # values of 40-100 KB: a record covers one or more runs of 8192 words, so
     # whole runs are composed from one record's value bytes
     rng = np.random.default_rng(21)
     ka = [b"k%04d" % t for t in range(0, 40, 2)]
