@@ -1,5 +1,7 @@
 """Calls captured in a CUDA graph and replayed on new inputs, and calls whose
-workspace holds stale words, against the oracle, bit-exact.
+workspace holds stale words, against the oracle, bit-exact: the whole
+replacement step (u64, both forms, and strings), the standalone rank
+builds, the stable merge, the merge sort and the FC lengths scan + emit.
 
 The single-launch rank builds (rank512 and rank2048) and the one-kernel
 replacement merge find their prefixes by a decoupled lookback over per-CTA
@@ -216,4 +218,96 @@ def test_whole_path_str_graph_replay(lsm):
         assert np.array_equal(down(ordA)[:SM], r.ord_A)
         assert np.array_equal(down(ordB)[:SN], r.ord_B)
         assert np.array_equal(down(dir_), oracle.rank512_dir(r.C, SM))
+    assert lsm.get_device_status() == lsm.LSM_OK
+
+
+# ---- the other calls: stable merge, merge sort, FC lengths + emit --------------------
+
+def test_merge_stable_graph_replay(lsm):
+    m, n = 200_003, 150_001
+    dev = torch.device("cuda:0")
+    A = torch.empty(m, dtype=torch.uint64, device=dev)
+    B = torch.empty(n, dtype=torch.uint64, device=dev)
+    Ap = up(np.arange(m, dtype=np.uint32))
+    Bp = up((m + np.arange(n)).astype(np.uint32))
+
+    def load(seed, hi):
+        rng = np.random.default_rng(seed)
+        a = np.sort(rng.integers(0, hi, size=m, dtype=np.uint64))
+        b = np.sort(rng.integers(0, hi, size=n, dtype=np.uint64))
+        A.copy_(up(a))
+        B.copy_(up(b))
+        return a, b
+
+    load(550, 1 << 40)
+    ws = _stale(lsm.workspace_size(lsm.LSM_OP_MERGE_STABLE, m, n))
+    keys, pay = lsm.merge_stable(A, B, Ap, Bp, ws=ws)
+    g = _capture(lambda: lsm.merge_stable(A, B, Ap, Bp, keys, pay, ws))
+    for seed, hi in ((551, 1 << 63), (552, 64), (553, 1 << 20)):  # ties in the second
+        a, b = load(seed, hi)
+        g.replay()
+        torch.cuda.synchronize()
+        ok, okp, _ = oracle.merge(a, b, np.arange(m, dtype=np.uint32),
+                                  (m + np.arange(n)).astype(np.uint32))
+        assert np.array_equal(down(keys), ok) and np.array_equal(down(pay), okp)
+    assert lsm.get_device_status() == lsm.LSM_OK
+
+
+def test_merge_sort_graph_replay(lsm):
+    N = 300_007
+    dev = torch.device("cuda:0")
+    keys_in = torch.empty(N, dtype=torch.uint64, device=dev)
+    pay_in = up(np.arange(N, dtype=np.uint32))
+
+    def load(seed):
+        s = synth.sort_u64(seed=seed, N=N)
+        k = s.keys >> np.uint64(seed % 7 * 8)  # more ties from seed to seed
+        keys_in.copy_(up(k))
+        return k
+
+    load(560)
+    ws = _stale(lsm.workspace_size(lsm.LSM_OP_MERGE_SORT, N, 0))
+    out_k, out_p = lsm.merge_sort(keys_in, pay_in, ws=ws)
+    g = _capture(lambda: lsm.merge_sort(keys_in, pay_in, out_k, out_p, ws))
+    for seed in (561, 562, 563):
+        k = load(seed)
+        g.replay()
+        torch.cuda.synchronize()
+        want_k, want_p, _ = oracle.merge_sort(k, np.arange(N, dtype=np.uint32))
+        assert np.array_equal(down(out_k), want_k) and np.array_equal(down(out_p), want_p)
+    assert lsm.get_device_status() == lsm.LSM_OK
+
+
+def test_fc_lengths_and_emit_graph_replay(lsm):
+    """The FC lengths scan and emit captured once and replayed after the
+    value bytes change in place (same extents, so the same lengths and a
+    different payload)."""
+    from tests.test_gpu_fc import device_input, gpu_refs
+    s = synth.strings(seed=570, count=30000, fanout=8, depth=3, max_suffix=30)
+    fc = device_input(lsm, s)
+    refs, N = gpu_refs(lsm, fc)
+    r = oracle.replacement_str(s.A.key_arena, s.A.key_off, s.B.key_arena, s.B.key_off)
+    ws = _stale(lsm.workspace_size(lsm.LSM_OP_FC_LENGTHS_SCAN, N, 0))
+    lcp, ctrl, rec, off = lsm.fc_lengths_scan(fc, refs, N, ws=ws)
+    nwords = (int(down(off[N:N + 1])[0]) + 31) // 32
+    payload = lsm.fc_emit(fc, refs, N, lcp, ctrl, off, nwords)
+
+    def call():
+        lsm.fc_lengths_scan(fc, refs, N, lcp, ctrl, rec, off, ws)
+        lsm.fc_emit(fc, refs, N, lcp, ctrl, off, nwords, payload)
+
+    g = _capture(call)
+    rng = np.random.default_rng(571)
+    for _ in range(3):
+        for side, dev_arena in ((s.A, fc.valA.arena), (s.B, fc.valB.arena)):
+            side.val_arena[:] = rng.integers(0, 256, len(side.val_arena)).astype(np.uint8)
+            dev_arena[:len(side.val_arena)].copy_(up(side.val_arena))
+        g.replay()
+        torch.cuda.synchronize()
+        exp = oracle.fc_encode((s.A.key_arena, s.A.key_off), (s.A.val_arena, s.A.val_off),
+                               s.A.tomb if len(s.A.tomb) else None,
+                               (s.B.key_arena, s.B.key_off), (s.B.val_arena, s.B.val_off),
+                               s.B.tomb if len(s.B.tomb) else None, r.refs)
+        assert np.array_equal(down(off), exp.bit_off)
+        assert np.array_equal(down(payload)[:len(exp.payload)], exp.payload)
     assert lsm.get_device_status() == lsm.LSM_OK
