@@ -752,7 +752,10 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
                  "one_kernel": {"ms_per_step": ms_one, "gpu_launches_per_step": 3},
                  "workspace_bytes": {"replacement_merge": w6.numel()},
                  "separate_calls": {"ms_per_step": ms_sep, "kernel_ms": per,
-                                    "gpu_launches_per_step": 5,
+                                    # mark: partition + pipeline; rank build;
+                                    # compaction from lb_B: its partition, the
+                                    # merge bitmap and the pipeline
+                                    "gpu_launches_per_step": 6,
                                     "workspace_bytes": {"collision_mark": w1.numel(),
                                                         "rank_build": w2.numel(),
                                                         "replacement_merge_compact": w3.numel()}},
@@ -774,7 +777,7 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
         "algorithmic_bytes": alg_mat, "gbs": alg_mat / (ms_mat * 1e-3) / 1e9,
         "frac": alg_mat / (ms_mat * 1e-3) / 1e9 / peak,
         "kernel_ms": {"replacement_materialize": per_mat["replacement_materialize"]},
-        "gpu_launches_per_step": 6}
+        "gpu_launches_per_step": 7}
     del vA, vB, tB, ok, ov, otb
     # The same step with the rank2048 directory in place of rank512 ("Suggested
     # separate modes": collision512 against collision2048 in the whole pipeline).
@@ -791,7 +794,7 @@ def extra_replace(lsm, torch, dev, peak, steps, flush, name, gen, out, sweep=Fal
         "ms_per_step": ms_2048, "gelem_s": (m + n) / (ms_2048 * 1e-3) / 1e9,
         "algorithmic_bytes": alg_2048, "gbs": alg_2048 / (ms_2048 * 1e-3) / 1e9,
         "frac": alg_2048 / (ms_2048 * 1e-3) / 1e9 / peak,
-        "kernel_ms": per_2048, "gpu_launches_per_step": 5,
+        "kernel_ms": per_2048, "gpu_launches_per_step": 6,
         "directory_bytes": {"rank512": 12 * (m // 512 + 1) + w2.numel(),
                             "rank2048": 8 * (m // 2048 + 1) + 8 * len(e2) + w4.numel()}}
     del d2, e2, w4
@@ -931,7 +934,8 @@ def extra_strings(lsm, torch, dev, peak, steps, flush, out):
         "gelem_s": (m + n) / (ms_b * 1e-3) / 1e9, "algorithmic_bytes": alg_b,
         "gbs": alg_b / (ms_b * 1e-3) / 1e9, "frac": alg_b / (ms_b * 1e-3) / 1e9 / peak,
         "kernel_ms": {k: per_b[k] for k in ("bytefc_lengths_scan", "bytefc_emit")},
-        "gpu_launches_per_step": 9}
+        # the string call's four, the byte lengths with the offset scan (three), the emit
+        "gpu_launches_per_step": 8}
     del lcpb, ctrlb, recb, offb, payb
     # The same step followed by the Elias-Fano navigation over bit_off.
     n_ef, L, nl, nh, G = lsm.ef_sizes(N, total_bits)
